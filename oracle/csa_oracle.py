@@ -1,0 +1,300 @@
+"""Plain CPU oracle for compressed sparse attention (CSA).
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import or call
+this module: only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` use it.  It shares no code with the CUDA library; both
+sides only share the seeded input generator in ``workloads``.
+
+Everything is computed in float64 with numpy, one definition at a time,
+straight from the pages:
+
+* "DeepSeek V4.1 Flash" (pypto-lib), sections "Serving-owned full RoPE
+  tables" (FP32 half-width tables, adjacent-pair rotation, negative position =
+  identity), "Compressor state ownership" (pooling softmax, BF16 rounding
+  before RMSNorm, Top-K acceptance rules, per-row tolerances).
+* "Hyper-Parallel ... DeepSeek V4 CP" (gitcode issue #2), sections
+  "二阶段 CP 总体算法" (shared-KV sparse attention with sinks, softmax_scale,
+  ori_win_left = 127), "7. Window KV Halo" (window includes self),
+  "8.2 ratio=128" and "10.3 Causal mask" (slot c visible to position p iff
+  c < (p + 1) // ratio).
+* "DeepSeek V4-Flash, MTP point", sections "What is quantized" (INT8 per-row
+  amax floored at 1e-4, scaled to 127, FP32 per-row scale) and "Attention
+  paths" (main compressor rotate=False, index-key compressor rotate=True).
+
+Readings taken where the pages are silent (each also listed in the design doc):
+ReLU per index head; the index-key scale applied after the head sum; the
+gate input x of the compressor is a separate [rows, Dx] operand (the
+workloads pass the raw KV rows); the sink is already a logit; lse includes
+the sink; RMSNorm optional; RoPE uses the last ``rope_dim`` dims.
+
+Parity pins live in ``tests/test_oracle_pins.py``.  Functions without an
+independent pin: none (every function below has at least one).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+BLOCK = 128  # rows per page
+
+# --------------------------------------------------------------------------
+# number formats
+# --------------------------------------------------------------------------
+
+
+def bf16_round(x):
+    """Round float64 values to the nearest BF16 value, ties to even.
+
+    BF16 keeps 8 significant bits.  Written from the definition: x = m * 2**e
+    with m in [0.5, 1); keep round-half-even(m * 2**8) / 2**8.  Normal range
+    only (the workloads never approach BF16's overflow or subnormal range).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def quantize_int8(y):
+    """Per-row INT8 quantisation on write ("DeepSeek V4-Flash, MTP point",
+    "What is quantized"): the row's amax, floored at 1e-4, is scaled to 127.
+
+    Returns (codes int8, scale float64) with scale = max(amax, 1e-4) / 127 and
+    code = clamp(round-half-even(y / scale), -127, 127).
+    """
+    y = np.asarray(y, dtype=np.float64)
+    amax = np.max(np.abs(y)) if y.size else 0.0
+    scale = max(amax, 1e-4) / 127.0
+    codes = np.clip(np.rint(y / scale), -127, 127).astype(np.int8)
+    return codes, scale
+
+
+# --------------------------------------------------------------------------
+# RoPE (DeepSeek V4.1 Flash, "Serving-owned full RoPE tables")
+# --------------------------------------------------------------------------
+
+
+def rope_rotate(vec, pos, cos_tab, sin_tab, rope_dim=64, inverse=False):
+    """Rotate the last ``rope_dim`` entries of ``vec`` (shape [..., D]) at
+    position ``pos`` by adjacent pairs (x[2i], x[2i+1]) using table row
+    ``pos``: (a, b) -> (a*c - b*s, a*s + b*c).  A negative position, or one
+    at or beyond the table capacity, leaves the vector unrotated (capacity
+    overflow is an error the device reports; the oracle mirrors its identity
+    fallback).  ``inverse`` rotates by the opposite angle.
+    """
+    v = as_f64(vec).copy()
+    if pos < 0 or pos >= cos_tab.shape[0]:
+        return v
+    c = as_f64(cos_tab[pos])
+    s = as_f64(sin_tab[pos])
+    if inverse:
+        s = -s
+    D = v.shape[-1]
+    a = v[..., D - rope_dim::2].copy()
+    b = v[..., D - rope_dim + 1::2].copy()
+    v[..., D - rope_dim::2] = a * c - b * s
+    v[..., D - rope_dim + 1::2] = a * s + b * c
+    return v
+
+
+# --------------------------------------------------------------------------
+# visibility and paging
+# --------------------------------------------------------------------------
+
+
+def visible_count(p, ratio, n_cmp):
+    """Compressed slot c is visible to query position p iff c < (p + 1) // ratio
+    ("Hyper-Parallel ... DeepSeek V4 CP", "10.3 Causal mask"), and only
+    published slots exist (c < n_cmp)."""
+    if p < 0:
+        return 0
+    return max(0, min(int(n_cmp), (int(p) + 1) // int(ratio)))
+
+
+def window_positions(p, window=128):
+    """Raw window of a query at position p: [max(0, p - window + 1), p],
+    self included (ori_win_left = window - 1, ori_win_right = 0;
+    "Hyper-Parallel ... DeepSeek V4 CP", "7. Window KV Halo")."""
+    if p < 0:
+        return []
+    return list(range(max(0, p - window + 1), p + 1))
+
+
+def as_f64(a):
+    """float64 numpy copy of a numpy array or a (CPU) torch tensor of any dtype."""
+    if hasattr(a, "detach"):
+        import torch
+        return a.detach().to(torch.float64).cpu().numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+def page_rows(pool, table_row, logical):
+    """Rows ``logical`` (iterable of request-local positions) of a paged pool
+    [pages, 128, ...] through one request's block table row, as float64."""
+    logical = np.asarray(list(logical), dtype=np.int64)
+    phys = np.asarray(table_row, dtype=np.int64)[logical // BLOCK]
+    assert np.all(phys >= 0), "read through an unmapped page"
+    if hasattr(pool, "detach"):
+        import torch
+        return as_f64(pool[torch.from_numpy(phys), torch.from_numpy(logical % BLOCK)])
+    return np.asarray(pool[phys, logical % BLOCK], dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# a1: gated compressor
+# --------------------------------------------------------------------------
+
+
+def compress(x, kv, w_gate, ape, ratio, positions, row_req, gamma=None, rms_eps=1e-6,
+             rotate=False, rope_cos=None, rope_sin=None, rope_dim=64, out="bf16"):
+    """Gated compression of every complete group of ``ratio`` rows.
+
+    A group g of request b is the positions g*r .. g*r + r - 1; it is complete
+    in this chunk when rows t-r+1 .. t all belong to b at those consecutive
+    positions, with p_t % r == r - 1.  Per channel d (512-channel KV plus a
+    512-channel gate score per token: "DeepSeek V4.1 Flash", "Compressor state
+    ownership", the recurrent-state row layout):
+
+        logit[j, d] = (x_j @ w_gate)[d] + ape[j, d]
+        w[:, d]     = softmax over j of logit[:, d]
+        y[d]        = sum_j w[j, d] * kv_j[d]
+
+    then y is rounded to BF16 ("BF16 rounding before RMSNorm"), optionally
+    RMS-normalised with ``gamma`` (rounded to BF16 again), optionally rotated
+    at the group start position g*r ("compression-group start positions";
+    rotate=True for the index-key compressor, "DeepSeek V4-Flash, MTP point",
+    "Attention paths"), and published as BF16 (``out="bf16"``) or as INT8
+    codes with an FP32 per-row scale (``out="int8"``).
+
+    Returns a list of (request, g, values) for bf16 or (request, g, codes,
+    scale) for int8, in row order.
+    """
+    x, kv, w_gate, ape = as_f64(x), as_f64(kv), as_f64(w_gate), as_f64(ape)
+    positions = as_f64(positions).astype(np.int64)
+    row_req = as_f64(row_req).astype(np.int64)
+    r = int(ratio)
+    results = []
+    for t in range(len(positions)):
+        b, p = int(row_req[t]), int(positions[t])
+        if b < 0 or p < 0 or p % r != r - 1 or t < r - 1:
+            continue
+        rows = [t - r + 1 + j for j in range(r)]
+        if any(int(row_req[s]) != b or int(positions[s]) != p - r + 1 + j
+               for j, s in enumerate(rows)):
+            continue
+        logits = x[rows] @ w_gate + ape[:r]  # [r, D]
+        mx = logits.max(axis=0, keepdims=True)
+        e = np.exp(logits - mx)
+        w = e / e.sum(axis=0, keepdims=True)
+        y = (w * kv[rows]).sum(axis=0)
+        y = bf16_round(y)
+        if gamma is not None:
+            g_ = as_f64(gamma)
+            y = bf16_round(y / np.sqrt(np.mean(y * y) + rms_eps) * g_)
+        g = p // r
+        if rotate:
+            y = rope_rotate(y, g * r, rope_cos, rope_sin, rope_dim)
+        if out == "bf16":
+            results.append((b, g, bf16_round(y)))
+        else:
+            codes, scale = quantize_int8(y)
+            results.append((b, g, codes, scale))
+    return results
+
+
+# --------------------------------------------------------------------------
+# a3: lightning-indexer scores
+# --------------------------------------------------------------------------
+
+
+def index_scores(q_idx_row, w_row, p, n_cmp_b, ratio, idx_pool, idx_scale_pool, table_row,
+                 relu=True, rope_cos=None, rope_sin=None, rope_dim=64):
+    """Scores of one query row against every visible compressed entry:
+
+        score[c] = scale_c * sum_h w[h] * ReLU(q_h . k_c),   c < visible_count
+
+    with q_h the row's index query of head h rotated at the row position p
+    (when tables are given) and k_c the INT8 index key of entry c
+    ("Hyper-Parallel ... DeepSeek V4 CP", "10. ratio=4 Global Top-k"; INT8
+    keys with an FP32 per-row scale: "DeepSeek V4-Flash, MTP point", "What is
+    quantized").  Since scale_c > 0, ReLU(scale * x) = scale * ReLU(x), so the
+    scale is applied after the head sum.  Returns float64 [visible].
+    """
+    nv = visible_count(p, ratio, n_cmp_b)
+    q = as_f64(q_idx_row)  # [H, Di]
+    if rope_cos is not None:
+        q = rope_rotate(q, p, rope_cos, rope_sin, rope_dim)
+    keys = page_rows(idx_pool, table_row, range(nv))  # [nv, Di]
+    scales = page_rows(idx_scale_pool, table_row, range(nv))
+    dots = keys @ q.T  # [nv, H]
+    if relu:
+        dots = np.maximum(dots, 0.0)
+    return scales * (dots @ as_f64(w_row))
+
+
+# --------------------------------------------------------------------------
+# a4: top-k
+# --------------------------------------------------------------------------
+
+
+def topk_select(scores, k):
+    """The k best entries by (score descending, index ascending), emitted as
+    logical positions in ascending order with trailing -1 padding
+    ("DeepSeek V4.1 Flash": logical-position ordering and trailing -1
+    padding in the Top-K acceptance rule; indexer workspaces padded with -1).
+    """
+    scores = np.asarray(scores, dtype=np.float64)
+    order = np.argsort(-scores, kind="stable")  # stable: equal scores keep ascending index
+    chosen = np.sort(order[:k])
+    out = np.full(k, -1, dtype=np.int64)
+    out[:len(chosen)] = chosen
+    return out
+
+
+# --------------------------------------------------------------------------
+# a5 / a6: shared-KV sparse attention with sink
+# --------------------------------------------------------------------------
+
+
+def sparse_attention(q_row, p, topk_row, kv_pool, kv_table_row, cmp_pool, cmp_table_row,
+                     sink, scale, window=128, rope_cos=None, rope_sin=None, rope_dim=64,
+                     inv_rope_out=False):
+    """One query row of shared-KV sparse attention
+    ("Hyper-Parallel ... DeepSeek V4 CP", "二阶段 CP 总体算法", Stage-2 with
+    cmp_sparse_indices, sinks, softmax_scale and ori_win_left = 127; the
+    candidate list is the selected compressed entries plus the raw window,
+    "9.1 Small-op fallback 路径": kv_full = [window kv, compressed kv]).
+
+    Each candidate row is both key and value.  Per head h:
+        l_i  = scale * q_h . k_i      (q rotated at p when tables are given)
+        o_h  = sum_i e^{l_i} k_i / (sum_i e^{l_i} + e^{sink_h})
+        lse_h = log(sum_i e^{l_i} + e^{sink_h})
+    A sink of None means -inf (plain softmax).  Two passes: max, then sums.
+    Returns (out [H, D] float64, lse [H] float64).
+    """
+    q = as_f64(q_row)
+    H, D = q.shape
+    if rope_cos is not None:
+        q = rope_rotate(q, p, rope_cos, rope_sin, rope_dim)
+    sel = [int(c) for c in np.asarray(topk_row).ravel() if int(c) >= 0]
+    parts = []
+    if sel:
+        parts.append(page_rows(cmp_pool, cmp_table_row, sel))
+    win = window_positions(p, window)
+    if win:
+        parts.append(page_rows(kv_pool, kv_table_row, win))
+    K = np.concatenate(parts, axis=0) if parts else np.zeros((0, D))
+    logits = scale * (q @ K.T)  # [H, n]
+    snk = np.full(H, -np.inf) if sink is None else as_f64(sink)
+    m = np.maximum(logits.max(axis=1) if K.shape[0] else np.full(H, -np.inf), snk)
+    out = np.zeros((H, D))
+    lse = np.full(H, -np.inf)
+    for h in range(H):
+        if not np.isfinite(m[h]):
+            continue
+        e = np.exp(logits[h] - m[h])
+        s = e.sum() + np.exp(snk[h] - m[h])
+        out[h] = (e @ K) / s
+        lse[h] = m[h] + np.log(s)
+    if inv_rope_out and rope_cos is not None:
+        out = rope_rotate(out, p, rope_cos, rope_sin, rope_dim, inverse=True)
+    return out, lse

@@ -1,0 +1,74 @@
+"""Whole-step drivers over a ``workloads.Workload`` — test infrastructure only.
+
+They chain the oracle's definitions in the order the V4 decode layer calls
+them ("DeepSeek V4-Flash, MTP point", "Attention paths": main compressor,
+index-key compressor, indexer, sparse attention) and never touch the CUDA
+library.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import csa_oracle as O
+
+
+def clone_pools(t):
+    return {k: t[k].clone() for k in ("cmp_pool", "idx_pool", "idx_scale")}
+
+
+def compress_step(t, spec, pools=None):
+    """Run both compressors over the chunk and publish into (cloned) pools.
+
+    Returns (pools, main_results, idx_results)."""
+    pools = clone_pools(t) if pools is None else pools
+    main = O.compress(t["kv_raw"], t["kv_raw"], t["w_gate"], t["ape"], spec.ratio,
+                      t["row_pos"], t["row_req"], out="bf16")
+    idx = O.compress(t["idx_raw"], t["idx_raw"], t["w_gate_i"], t["ape_i"], spec.ratio,
+                     t["row_pos"], t["row_req"], rotate=True, rope_cos=t["rope_cos"],
+                     rope_sin=t["rope_sin"], rope_dim=spec.rope_dim, out="int8")
+    table = t["cmp_table"].numpy()
+    for b, g, vals in main:
+        pg = int(table[b, g // O.BLOCK])
+        pools["cmp_pool"][pg, g % O.BLOCK] = torch.from_numpy(vals).to(torch.bfloat16)
+    for b, g, codes, scale in idx:
+        pg = int(table[b, g // O.BLOCK])
+        pools["idx_pool"][pg, g % O.BLOCK] = torch.from_numpy(codes)
+        pools["idx_scale"][pg, g % O.BLOCK] = float(np.float32(scale))
+    return pools, main, idx
+
+
+def index_row(t, spec, pools, row, relu=True):
+    b = int(t["row_req"][row])
+    p = int(t["row_pos"][row])
+    return O.index_scores(t["q_idx"][row], t["idx_w"][row], p, int(t["n_cmp"][b]), spec.ratio,
+                          pools["idx_pool"], pools["idx_scale"], t["cmp_table"][b].numpy(),
+                          relu=relu, rope_cos=t["rope_cos"], rope_sin=t["rope_sin"],
+                          rope_dim=spec.rope_dim)
+
+
+def attention_row(t, spec, pools, row, topk_row, inv_rope_out=False, use_sink=True):
+    b = int(t["row_req"][row])
+    p = int(t["row_pos"][row])
+    return O.sparse_attention(t["q"][row], p, topk_row, t["kv_pool"], t["kv_table"][b].numpy(),
+                              pools["cmp_pool"], t["cmp_table"][b].numpy(),
+                              t["sink"] if use_sink else None, 1.0 / np.sqrt(spec.head_dim),
+                              window=spec.window, rope_cos=t["rope_cos"],
+                              rope_sin=t["rope_sin"], rope_dim=spec.rope_dim,
+                              inv_rope_out=inv_rope_out)
+
+
+def full_step(t, spec, rows=None):
+    """Oracle's own chain: compress -> scores -> top-k -> attention for ``rows``."""
+    pools, _, _ = compress_step(t, spec)
+    rows = range(spec.n_rows) if rows is None else rows
+    res = {}
+    for row in rows:
+        if int(t["row_req"][row]) < 0:
+            continue
+        s = index_row(t, spec, pools, row)
+        sel = O.topk_select(s, spec.topk)
+        out, lse = attention_row(t, spec, pools, row, sel)
+        res[row] = dict(scores=s, topk=sel, out=out, lse=lse)
+    return pools, res

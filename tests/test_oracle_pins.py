@@ -1,0 +1,461 @@
+"""Pins of the CPU oracle to facts outside itself (no GPU needed).
+
+Each test checks the oracle against something it does not compute itself:
+a worked example printed on the pages (``tests/golden``), a hand-computed
+value, a closed form, a library routine (torch's BF16 cast, numpy complex
+multiplication, scipy's softmax/logsumexp, numpy's lexsort), or an
+invariant that a dropped term, a wrong sign or index, or a transposed
+operand would break.
+"""
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit, logsumexp, softmax
+
+import oracle as O
+from golden.load import constants, rows
+from workloads import BLOCK, rope_tables
+
+COS, SIN = rope_tables(4096, 64, 10000.0)
+
+
+def _cplx_rotate(v, pos, rope_dim=64):
+    """Rotation of adjacent pairs written as complex multiplication by e^{i*angle}."""
+    v = np.asarray(v, dtype=np.float64).copy()
+    D = v.shape[-1]
+    z = v[..., D - rope_dim::2] + 1j * v[..., D - rope_dim + 1::2]
+    rot = np.asarray(COS[pos], np.float64) + 1j * np.asarray(SIN[pos], np.float64)
+    z = z * rot
+    v[..., D - rope_dim::2] = z.real
+    v[..., D - rope_dim + 1::2] = z.imag
+    return v
+
+
+# ---------------------------------------------------------------- formats
+
+
+def test_bf16_round_matches_torch_cast():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal(20000).astype(np.float32) * np.float32(3.0)
+    # add exact ties (low 16 bits == 0x8000, normal range): must round half to even
+    expo = rng.integers(100, 150, 2000, dtype=np.uint32) << np.uint32(23)
+    mant = rng.integers(0, 128, 2000, dtype=np.uint32) << np.uint32(16)
+    ties = (expo | mant | np.uint32(0x8000)).view(np.float32)
+    x = np.concatenate([x, ties, -ties])
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.bf16_round(x.astype(np.float64)), ref)
+
+
+def test_int8_quant_constants_and_worked_example():
+    c = constants("int8_quant_constants.txt")
+    codes, s = O.quantize_int8(np.zeros(128))
+    assert s == pytest.approx(c["amax_eps"] / c["scale_max"], rel=1e-15)
+    assert np.all(codes == 0)
+    # hand-computed: amax 1 -> scale 1/127; 0.5*127 = 63.5 -> 64 (half to even),
+    # 0.25*127 = 31.75 -> 32, -1 -> -127
+    codes, s = O.quantize_int8(np.array([0.5, -1.0, 0.25, 0.0]))
+    assert s == pytest.approx(1.0 / 127.0, rel=1e-15)
+    assert codes.tolist() == [64, -127, 32, 0]
+    # 1.5/127 -> rounds to 2 (even), 2.5/127 -> 2 (even)
+    codes, s = O.quantize_int8(np.array([1.0, 1.5 / 127, 2.5 / 127]))
+    assert codes.tolist() == [127, 2, 2]
+
+
+def test_int8_quant_error_bound_and_amax_code():
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        y = rng.standard_normal(128) * rng.uniform(0.01, 10)
+        codes, s = O.quantize_int8(y)
+        assert np.max(np.abs(codes.astype(np.float64) * s - y)) <= s / 2 * (1 + 1e-12)
+        i = np.argmax(np.abs(y))
+        assert abs(int(codes[i])) == 127 and np.sign(codes[i]) == np.sign(y[i])
+
+
+# ---------------------------------------------------------------- RoPE
+
+
+def test_rope_identity_at_zero_and_negative_positions():
+    rng = np.random.default_rng(0)
+    v = rng.standard_normal((3, 512))
+    assert np.array_equal(O.rope_rotate(v, 0, COS, SIN), v)
+    assert np.array_equal(O.rope_rotate(v, -1, COS, SIN), v)
+    assert np.array_equal(O.rope_rotate(v, -77, COS, SIN), v)
+    # beyond capacity: identity (the device flags it)
+    assert np.array_equal(O.rope_rotate(v, 4096, COS, SIN), v)
+
+
+def test_rope_is_complex_multiplication_of_adjacent_pairs():
+    rng = np.random.default_rng(1)
+    for D in (512, 128):
+        v = rng.standard_normal((5, D))
+        for pos in (1, 7, 300, 4095):
+            got = O.rope_rotate(v, pos, COS, SIN)
+            assert np.allclose(got, _cplx_rotate(v, pos), rtol=0, atol=1e-12)
+            assert np.array_equal(got[:, :D - 64], v[:, :D - 64])
+
+
+def test_rope_relative_position_norm_and_inverse():
+    rng = np.random.default_rng(2)
+    q, k = rng.standard_normal(128), rng.standard_normal(128)
+    base = O.rope_rotate(q, 40, COS, SIN) @ O.rope_rotate(k, 10, COS, SIN)
+    for shift in (1, 100, 2000):
+        other = O.rope_rotate(q, 40 + shift, COS, SIN) @ O.rope_rotate(k, 10 + shift, COS, SIN)
+        assert other == pytest.approx(base, rel=1e-5, abs=1e-5)
+    r = O.rope_rotate(q, 1234, COS, SIN)
+    pair = lambda x: x[64::2] ** 2 + x[65::2] ** 2  # noqa: E731
+    assert np.allclose(pair(r), pair(q), rtol=1e-6)
+    back = O.rope_rotate(r, 1234, COS, SIN, inverse=True)
+    assert np.allclose(back, q, atol=1e-6)
+
+
+# ---------------------------------------------------------------- visibility / window
+
+
+def test_causal_visibility_worked_example_and_brute_force():
+    for p, r, vis in rows("causal_visibility.txt"):
+        p, r = int(p), int(r)
+        want = [int(c) for c in vis.split(",")]
+        assert list(range(O.visible_count(p, r, 10**9))) == want
+    # brute force: slot c pools positions c*r .. c*r+r-1; it is visible iff all
+    # of them are at or before p
+    for r in (1, 2, 4, 128):
+        for p in range(0, 600, 7):
+            brute = sum(1 for c in range(1000) if c * r + r - 1 <= p)
+            assert O.visible_count(p, r, 10**9) == brute
+            assert O.visible_count(p, r, 3) == min(3, brute)
+    assert O.visible_count(-1, 2, 100) == 0
+
+
+def test_window_worked_example():
+    for p, w, vis in rows("window_example.txt"):
+        assert O.window_positions(int(p), int(w)) == [int(x) for x in vis.split(",")]
+    assert O.window_positions(0, 128) == [0]
+    assert O.window_positions(300, 128) == list(range(173, 301))
+
+
+# ---------------------------------------------------------------- compressor
+
+
+def _bf16(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16)
+
+
+def _chunk(rng, n, D=64, Dx=64):
+    kv = _bf16(rng.standard_normal((n, D)))
+    x = _bf16(rng.standard_normal((n, Dx)))
+    return x, kv
+
+
+def test_compress_ratio1_is_identity():
+    rng = np.random.default_rng(4)
+    x, kv = _chunk(rng, 6)
+    w = _bf16(rng.standard_normal((64, 64)))
+    ape = rng.standard_normal((1, 64))
+    res = O.compress(x, kv, w, ape, 1, np.arange(10, 16), np.zeros(6, int))
+    assert [g for _, g, _ in res] == list(range(10, 16))
+    for i, (_, _, y) in enumerate(res):
+        assert np.array_equal(y, kv[i].double().numpy())
+
+
+def test_compress_equal_logits_give_the_mean():
+    rng = np.random.default_rng(5)
+    x, kv = _chunk(rng, 8)
+    w = torch.zeros((64, 64), dtype=torch.bfloat16)
+    res = O.compress(x, kv, w, np.zeros((4, 64)), 4, np.arange(8), np.zeros(8, int))
+    assert len(res) == 2
+    for b, g, y in res:
+        mean = kv[4 * g:4 * g + 4].double().numpy().mean(axis=0)
+        # the only difference from the plain mean is the final BF16 rounding
+        assert np.all(np.abs(y - mean) <= 2.0 ** -9 * np.abs(mean) * (1 + 1e-12))
+
+
+def test_compress_one_hot_ape_selects_a_row():
+    rng = np.random.default_rng(6)
+    x, kv = _chunk(rng, 4)
+    w = _bf16(rng.standard_normal((64, 64)) * 0.01)
+    ape = np.zeros((4, 64))
+    ape[2] = 1e4
+    (_, _, y), = O.compress(x, kv, w, ape, 4, np.arange(4), np.zeros(4, int))
+    assert np.array_equal(y, kv[2].double().numpy())
+
+
+def test_compress_gate_orientation_is_x_times_w():
+    # x_j0 has a single 1 at input channel k0; w_gate[k0, d0] is huge.
+    # Output channel d0 must select row j0; every other channel is the mean.
+    kv = _bf16(np.random.default_rng(8).standard_normal((4, 64)))
+    x = torch.zeros((4, 64), dtype=torch.bfloat16)
+    j0, k0, d0 = 1, 5, 40
+    x[j0, k0] = 1.0
+    w = torch.zeros((64, 64), dtype=torch.bfloat16)
+    w[k0, d0] = 1e4
+    (_, _, y), = O.compress(x, kv, w, np.zeros((4, 64)), 4, np.arange(4), np.zeros(4, int))
+    kvd = kv.double().numpy()
+    assert y[d0] == kvd[j0, d0]
+    others = [d for d in range(64) if d != d0]
+    assert np.allclose(y[others], kvd[:, others].mean(axis=0), rtol=2 ** -7, atol=1e-6)
+    assert not np.isclose(y[k0], kvd[j0, k0]) or np.isclose(kvd[:, k0].mean(), kvd[j0, k0])
+
+
+def test_compress_weights_sum_to_one_and_order_of_ape_rows():
+    rng = np.random.default_rng(9)
+    v = rng.standard_normal(64)
+    kv = _bf16(np.tile(v, (4, 1)))
+    x = _bf16(rng.standard_normal((4, 64)))
+    w = _bf16(rng.standard_normal((64, 64)))
+    ape = rng.standard_normal((4, 64)) * 3
+    (_, _, y), = O.compress(x, kv, w, ape, 4, np.arange(4), np.zeros(4, int))
+    assert np.array_equal(y, kv[0].double().numpy())  # any convex combination of equal rows
+    # APE row j applies to the j-th token of the group (position % ratio == j)
+    kv2 = _bf16(rng.standard_normal((4, 64)))
+    for j in range(4):
+        ape_hot = np.zeros((4, 64))
+        ape_hot[j] = 1e4
+        (_, _, yb), = O.compress(x, kv2, w, ape_hot, 4, np.arange(8, 12), np.zeros(4, int))
+        assert np.array_equal(yb, kv2[j].double().numpy())
+
+
+def test_compress_softmax_matches_scipy():
+    rng = np.random.default_rng(10)
+    x, kv = _chunk(rng, 4)
+    w = _bf16(rng.standard_normal((64, 64)) / 8)
+    ape = rng.standard_normal((4, 64))
+    (_, _, y), = O.compress(x, kv, w, ape, 4, np.arange(4), np.zeros(4, int))
+    logits = x.double().numpy() @ w.double().numpy() + ape
+    ref = (softmax(logits, axis=0) * kv.double().numpy()).sum(axis=0)
+    assert np.allclose(y, ref, rtol=2 ** -8, atol=1e-12)
+
+
+def test_compress_only_complete_groups_and_requests():
+    rng = np.random.default_rng(11)
+    x, kv = _chunk(rng, 9)
+    w = _bf16(rng.standard_normal((64, 64)))
+    ape = rng.standard_normal((2, 64))
+    # request 0: positions 5..8 (groups (6,7) complete; 5 and 8 are halves)
+    # request 1: positions 0..2 (group (0,1)); one padding row
+    pos = np.array([5, 6, 7, 8, 0, 1, 2, -1, 3])
+    req = np.array([0, 0, 0, 0, 1, 1, 1, -1, 1])
+    got = [(b, g) for b, g, _ in O.compress(x, kv, w, ape, 2, pos, req)]
+    assert got == [(0, 3), (1, 0)]  # row 8 (pos 3) follows a padding row: incomplete
+
+
+def test_compress_rotate_uses_group_start_and_int8_path():
+    rng = np.random.default_rng(12)
+    x, kv = _chunk(rng, 8, D=128, Dx=128)
+    w = _bf16(rng.standard_normal((128, 128)) / 11)
+    ape = rng.standard_normal((4, 128))
+    pos = np.arange(100, 108)
+    plain = O.compress(x, kv, w, ape, 4, pos, np.zeros(8, int))
+    rot = O.compress(x, kv, w, ape, 4, pos, np.zeros(8, int), rotate=True, rope_cos=COS,
+                     rope_sin=SIN)
+    q8 = O.compress(x, kv, w, ape, 4, pos, np.zeros(8, int), rotate=True, rope_cos=COS,
+                    rope_sin=SIN, out="int8")
+    for (_, g, yp), (_, g2, yr), (_, g3, codes, s) in zip(plain, rot, q8):
+        assert g == g2 == g3
+        want = _cplx_rotate(yp, g * 4)
+        assert np.allclose(yr, want, rtol=2 ** -8, atol=1e-6)
+        assert np.max(np.abs(codes * s - want)) <= s / 2 + 1e-9
+
+
+def test_compress_rmsnorm_unit_gamma():
+    rng = np.random.default_rng(13)
+    x, kv = _chunk(rng, 4)
+    w = _bf16(rng.standard_normal((64, 64)) / 8)
+    (_, _, y), = O.compress(x, kv, w, np.zeros((4, 64)), 4, np.arange(4), np.zeros(4, int),
+                            gamma=torch.ones(64, dtype=torch.bfloat16))
+    assert np.sqrt(np.mean(y * y)) == pytest.approx(1.0, rel=1e-2)
+
+
+# ---------------------------------------------------------------- indexer
+
+
+def _one_page_pool(keys, scales):
+    n, Di = keys.shape
+    pool = np.zeros((2, BLOCK, Di), np.int8)
+    sp = np.zeros((2, BLOCK), np.float32)
+    pool[1, :n] = keys
+    sp[1, :n] = scales
+    return pool, sp, np.array([1, 0])
+
+
+def test_index_scores_hand_example():
+    # one head, dim 4 (no rotation): q = [1, 2, 0, -1]
+    # key a = [3, -1, 5, 2]: dot = 3 - 2 + 0 - 2 = -1 -> ReLU 0
+    # key b = [1, 1, 1, 1]:  dot = 2 -> 0.5 * 2.0 * 2 = 2
+    pool, sp, table = _one_page_pool(np.array([[3, -1, 5, 2], [1, 1, 1, 1]], np.int8),
+                                     np.array([0.5, 0.5], np.float32))
+    q = np.array([[1.0, 2.0, 0.0, -1.0]])
+    s = O.index_scores(q, [2.0], p=1, n_cmp_b=2, ratio=1, idx_pool=pool, idx_scale_pool=sp,
+                       table_row=table)
+    assert s.tolist() == [0.0, 2.0]
+    s = O.index_scores(q, [2.0], p=1, n_cmp_b=2, ratio=1, idx_pool=pool, idx_scale_pool=sp,
+                       table_row=table, relu=False)
+    assert s.tolist() == [-1.0, 2.0]
+    # visibility: at p = 0 with ratio 1 only entry 0 is visible
+    s = O.index_scores(q, [2.0], p=0, n_cmp_b=2, ratio=1, idx_pool=pool, idx_scale_pool=sp,
+                       table_row=table)
+    assert s.tolist() == [0.0]
+
+
+def test_index_scores_heads_weights_and_scale():
+    rng = np.random.default_rng(14)
+    keys = rng.integers(-127, 128, (20, 8), dtype=np.int8)
+    scales = rng.uniform(1e-3, 1e-2, 20).astype(np.float32)
+    pool, sp, table = _one_page_pool(keys, scales)
+    q = rng.standard_normal((3, 8))
+    w = rng.standard_normal(3)
+    kw = dict(p=100, n_cmp_b=20, ratio=1, idx_pool=pool, idx_scale_pool=sp, table_row=table)
+    s = O.index_scores(q, w, **kw)
+    # one head at a time: contributions add, and a head with a negative dot adds nothing
+    per = [O.index_scores(q[h:h + 1], w[h:h + 1], **kw) for h in range(3)]
+    assert np.allclose(s, sum(per), rtol=1e-12, atol=1e-12)
+    for h in range(3):
+        dots = keys.astype(np.float64) @ q[h]
+        assert np.all(per[h][dots < 0] == 0)
+        assert np.allclose(per[h][dots > 0], scales.astype(np.float64)[dots > 0] * w[h] * dots[dots > 0])
+    # doubling every scale doubles every score
+    pool2, sp2, _ = _one_page_pool(keys, scales * 2)
+    s2 = O.index_scores(q, w, **{**kw, "idx_pool": pool2, "idx_scale_pool": sp2})
+    assert np.allclose(s2, 2 * s, rtol=1e-6)
+
+
+def test_index_scores_rotate_query_at_row_position_and_paging():
+    rng = np.random.default_rng(15)
+    nkeys = 300
+    keys = rng.integers(-127, 128, (nkeys, 128), dtype=np.int8)
+    scales = rng.uniform(1e-3, 1e-2, nkeys).astype(np.float32)
+    pool = np.zeros((5, BLOCK, 128), np.int8)
+    sp = np.zeros((5, BLOCK), np.float32)
+    table = np.array([3, 0, 4])
+    for c in range(nkeys):
+        pool[table[c // BLOCK], c % BLOCK] = keys[c]
+        sp[table[c // BLOCK], c % BLOCK] = scales[c]
+    q = rng.standard_normal((4, 128))
+    w = rng.standard_normal(4)
+    p = 700
+    s = O.index_scores(q, w, p, nkeys, 2, pool, sp, table, rope_cos=COS, rope_sin=SIN)
+    assert len(s) == min(nkeys, (p + 1) // 2)
+    qr = _cplx_rotate(q, p)
+    dots = np.maximum(keys[:len(s)].astype(np.float64) @ qr.T, 0)
+    assert np.allclose(s, scales[:len(s)] * (dots @ w), rtol=1e-9, atol=1e-9)
+    # a different physical placement of the same logical pages changes nothing
+    pool_b = np.zeros_like(pool)
+    sp_b = np.zeros_like(sp)
+    table_b = np.array([1, 2, 0])
+    for j in range(3):
+        pool_b[table_b[j]] = pool[table[j]]
+        sp_b[table_b[j]] = sp[table[j]]
+    s_b = O.index_scores(q, w, p, nkeys, 2, pool_b, sp_b, table_b, rope_cos=COS, rope_sin=SIN)
+    assert np.array_equal(s, s_b)
+
+
+# ---------------------------------------------------------------- top-k
+
+
+def test_topk_matches_lexsort_with_ties():
+    rng = np.random.default_rng(16)
+    for n, k in [(50, 10), (300, 128), (1000, 999), (64, 64), (20, 64)]:
+        s = rng.integers(-5, 6, n).astype(np.float64)  # many ties
+        got = O.topk_select(s, k)
+        order = np.lexsort((np.arange(n), -s))  # primary -score, then index
+        want = np.sort(order[:k])
+        assert np.array_equal(got[:len(want)], want)
+        assert np.all(got[len(want):] == -1)
+        assert np.all(np.diff(got[:len(want)]) > 0)
+
+
+# ---------------------------------------------------------------- attention
+
+
+def _attn_fixture(rng, n_cmp=40, kv_len=50, D=512, H=4):
+    P = 4
+    kv_pool = _bf16(rng.standard_normal((P, BLOCK, D)))
+    cmp_pool = _bf16(rng.standard_normal((P, BLOCK, D)))
+    kv_table = np.array([2, -1, -1, -1])
+    cmp_table = np.array([3, -1, -1, -1])
+    q = _bf16(rng.standard_normal((H, D)))
+    sink = rng.standard_normal(H)
+    return kv_pool, cmp_pool, kv_table, cmp_table, q, sink
+
+
+def _dense_candidates(kv_pool, cmp_pool, kv_table, cmp_table, sel, win):
+    rows_ = [cmp_pool[cmp_table[c // BLOCK], c % BLOCK].double().numpy() for c in sel]
+    rows_ += [kv_pool[kv_table[p // BLOCK], p % BLOCK].double().numpy() for p in win]
+    return np.stack(rows_)
+
+
+def test_attention_without_sink_is_textbook_softmax_attention():
+    rng = np.random.default_rng(17)
+    kv_pool, cmp_pool, kv_table, cmp_table, q, _ = _attn_fixture(rng)
+    sel = [3, 7, 11, -1, -1]
+    p, scale = 45, 1 / np.sqrt(512)
+    out, lse = O.sparse_attention(q, p, sel, kv_pool, kv_table, cmp_pool, cmp_table, None, scale,
+                                  window=8)
+    K = _dense_candidates(kv_pool, cmp_pool, kv_table, cmp_table, [3, 7, 11], range(38, 46))
+    logits = scale * q.double().numpy() @ K.T
+    assert np.allclose(out, softmax(logits, axis=1) @ K, rtol=1e-10, atol=1e-12)
+    assert np.allclose(lse, logsumexp(logits, axis=1), rtol=1e-12)
+
+
+def test_attention_sink_sits_in_the_denominator():
+    rng = np.random.default_rng(18)
+    kv_pool, cmp_pool, kv_table, cmp_table, q, sink = _attn_fixture(rng)
+    sel = [0, 5, 9]
+    p, scale = 20, 1 / np.sqrt(512)
+    out, lse = O.sparse_attention(q, p, sel, kv_pool, kv_table, cmp_pool, cmp_table, sink, scale,
+                                  window=16)
+    K = _dense_candidates(kv_pool, cmp_pool, kv_table, cmp_table, sel, range(5, 21))
+    logits = scale * q.double().numpy() @ K.T
+    ext = np.concatenate([logits, sink[:, None]], axis=1)
+    wts = softmax(ext, axis=1)[:, :-1]
+    assert np.allclose(out, wts @ K, rtol=1e-10, atol=1e-12)
+    assert np.allclose(lse, logsumexp(ext, axis=1), rtol=1e-12)
+
+
+def test_attention_single_candidate_closed_form():
+    rng = np.random.default_rng(19)
+    kv_pool, cmp_pool, kv_table, cmp_table, q, sink = _attn_fixture(rng)
+    scale = 0.05
+    out, lse = O.sparse_attention(q, 0, [-1, -1], kv_pool, kv_table, cmp_pool, cmp_table, sink,
+                                  scale)
+    v = kv_pool[kv_table[0], 0].double().numpy()
+    ell = scale * q.double().numpy() @ v
+    assert np.allclose(out, expit(ell - sink)[:, None] * v[None, :], rtol=1e-12, atol=1e-14)
+    assert np.allclose(lse, np.logaddexp(ell, sink), rtol=1e-12)
+
+
+def test_attention_full_selection_equals_dense_and_paging_invariance():
+    rng = np.random.default_rng(20)
+    kv_pool, cmp_pool, kv_table, cmp_table, q, sink = _attn_fixture(rng)
+    p, r, n_cmp = 37, 2, 19
+    nv = O.visible_count(p, r, n_cmp)
+    sel = O.topk_select(rng.standard_normal(nv), 64)  # k >= visible: everything, then -1
+    assert np.array_equal(sel[:nv], np.arange(nv)) and np.all(sel[nv:] == -1)
+    scale = 1 / np.sqrt(512)
+    out, lse = O.sparse_attention(q, p, sel, kv_pool, kv_table, cmp_pool, cmp_table, sink, scale)
+    K = _dense_candidates(kv_pool, cmp_pool, kv_table, cmp_table, range(nv), range(0, p + 1))
+    ext = np.concatenate([scale * q.double().numpy() @ K.T, sink[:, None]], axis=1)
+    assert np.allclose(out, softmax(ext, axis=1)[:, :-1] @ K, rtol=1e-10, atol=1e-12)
+    # move the pages elsewhere
+    kv2, cmp2 = kv_pool.clone(), cmp_pool.clone()
+    kv2[0], cmp2[1] = kv_pool[kv_table[0]], cmp_pool[cmp_table[0]]
+    out2, lse2 = O.sparse_attention(q, p, sel, kv2, np.array([0, -1, -1, -1]), cmp2,
+                                    np.array([1, -1, -1, -1]), sink, scale)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def test_attention_rotates_query_at_row_position_and_inverse_output():
+    rng = np.random.default_rng(21)
+    kv_pool, cmp_pool, kv_table, cmp_table, q, sink = _attn_fixture(rng)
+    p, scale = 60, 1 / np.sqrt(512)
+    sel = [1, 2]
+    out, _ = O.sparse_attention(q, p, sel, kv_pool, kv_table, cmp_pool, cmp_table, sink, scale,
+                                rope_cos=COS, rope_sin=SIN)
+    K = _dense_candidates(kv_pool, cmp_pool, kv_table, cmp_table, sel, range(0, p + 1))
+    qr = _cplx_rotate(q.double().numpy(), p)
+    ext = np.concatenate([scale * qr @ K.T, sink[:, None]], axis=1)
+    want = softmax(ext, axis=1)[:, :-1] @ K
+    assert np.allclose(out, want, rtol=1e-9, atol=1e-12)
+    out_inv, _ = O.sparse_attention(q, p, sel, kv_pool, kv_table, cmp_pool, cmp_table, sink,
+                                    scale, rope_cos=COS, rope_sin=SIN, inv_rope_out=True)
+    assert np.allclose(_cplx_rotate(out_inv, p), want, atol=1e-9)

@@ -1,0 +1,226 @@
+"""Seeded workload generator (inputs only; see the package docstring)."""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+BLOCK = 128  # rows per KV page (V4-Flash MTP page, "Deployment configuration")
+
+
+@dataclass
+class WorkloadSpec:
+    """Shape of one synthetic CSA step.
+
+    Request b holds ``ctx[b]`` tokens after this step; the step's query rows
+    are its last ``chunk[b]`` positions.  ``n_cmp[b] = ctx[b] // ratio``
+    compressed entries are published.
+    """
+
+    name: str
+    ctx: list
+    chunk: list
+    ratio: int
+    topk: int
+    seed: int
+    mode: str = "decode"  # "decode" or "prefill"
+    heads: int = 64
+    head_dim: int = 512
+    idx_heads: int = 64
+    idx_dim: int = 128
+    window: int = 128
+    rope_dim: int = 64
+    theta: float = 10000.0
+    rope_cap: int | None = None  # default: next power of two above the largest position
+    kv_pool_pages: int | None = None  # default: exactly the pages used
+    cmp_pool_pages: int | None = None
+    kv_pages: str = "all"  # "all" or "window" (only pages the window reads; others -1)
+    cmp_init: str = "random"  # "random" or "zeros" (filled by the compressor)
+    pad_rows: int = 0  # trailing padding rows (row_req = -1)
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def n_req(self) -> int:
+        return len(self.ctx)
+
+    @property
+    def n_rows(self) -> int:
+        return int(sum(self.chunk)) + self.pad_rows
+
+
+CONFIGS = {
+    # 1 request, rows at positions 1022 and 1023, ratio 2, top-k 128, table capacity 4096.
+    "tiny_decode": WorkloadSpec("tiny_decode", [1024], [2], ratio=2, topk=128, seed=0,
+                                rope_cap=4096),
+    # 4 requests x 2 rows, contexts 8192/6000/4097/2048, ratio 2, top-k 512,
+    # one shared pool of 256 pages each for kv and cmp.
+    "serving_decode": WorkloadSpec("serving_decode", [8192, 6000, 4097, 2048], [2, 2, 2, 2],
+                                   ratio=2, topk=512, seed=1, kv_pool_pages=256,
+                                   cmp_pool_pages=256),
+    # 4 requests x 2 rows at 131,072 context, ratio 1, top-k 1024.
+    "ratio1_decode": WorkloadSpec("ratio1_decode", [131072] * 4, [2] * 4, ratio=1, topk=1024,
+                                  seed=2, kv_pages="window"),
+    # 1 request, 8192 tokens at positions 0..8191, ratio 4, top-k 512; the
+    # compressor fills cmp_kv and idx_kv in the same step.
+    "chunked_prefill": WorkloadSpec("chunked_prefill", [8192], [8192], ratio=4, topk=512, seed=3,
+                                    mode="prefill", cmp_init="zeros"),
+    # 4 requests x 2 rows at 1,048,576 positions, ratio 4, top-k 2048.
+    "million_decode": WorkloadSpec("million_decode", [1048576] * 4, [2] * 4, ratio=4, topk=2048,
+                                   seed=4, kv_pages="window"),
+}
+
+
+def spec_for(name: str, **overrides) -> WorkloadSpec:
+    spec = dataclasses.replace(CONFIGS[name])
+    return dataclasses.replace(spec, **overrides) if overrides else spec
+
+
+def _next_pow2_above(x: int) -> int:
+    return 1 << int(x).bit_length()
+
+
+def rope_tables(capacity: int, rope_dim: int = 64, theta: float = 10000.0):
+    """FP32 half-width cos/sin tables [capacity, rope_dim // 2] (fixture initialisation)."""
+    half = rope_dim // 2
+    inv_freq = theta ** (-2.0 * np.arange(half, dtype=np.float64) / rope_dim)
+    cos = np.empty((capacity, half), dtype=np.float32)
+    sin = np.empty((capacity, half), dtype=np.float32)
+    step = 1 << 16
+    for p0 in range(0, capacity, step):
+        p = np.arange(p0, min(capacity, p0 + step), dtype=np.float64)
+        ang = p[:, None] * inv_freq[None, :]
+        cos[p0:p0 + len(p)] = np.cos(ang)
+        sin[p0:p0 + len(p)] = np.sin(ang)
+    return torch.from_numpy(cos), torch.from_numpy(sin)
+
+
+def _normal_bf16(rng, shape, std=1.0):
+    a = rng.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        a *= np.float32(std)
+    return torch.from_numpy(a).to(torch.bfloat16)
+
+
+@dataclass
+class Workload:
+    spec: WorkloadSpec
+    t: dict  # name -> CPU tensor
+
+    def __getattr__(self, k):
+        t = self.__dict__.get("t")
+        if t is not None and k in t:
+            return t[k]
+        raise AttributeError(k)
+
+    def to(self, device) -> dict:
+        return {k: v.to(device) for k, v in self.t.items()}
+
+
+def make_workload(spec: WorkloadSpec) -> Workload:
+    rng = np.random.default_rng(spec.seed)
+    B, r, Dm, Di = spec.n_req, spec.ratio, spec.head_dim, spec.idx_dim
+    ctx = [int(c) for c in spec.ctx]
+    chunk = [int(c) for c in spec.chunk]
+    assert len(chunk) == B and all(0 <= chunk[b] <= ctx[b] for b in range(B))
+    n_cmp = [c // r for c in ctx]
+
+    # query rows: the last chunk[b] positions of each request, then padding
+    row_req, row_pos = [], []
+    for b in range(B):
+        for p in range(ctx[b] - chunk[b], ctx[b]):
+            row_req.append(b)
+            row_pos.append(p)
+    row_req += [-1] * spec.pad_rows
+    row_pos += [-1] * spec.pad_rows
+    T = len(row_req)
+    max_pos = max(ctx) - 1
+    cap = spec.rope_cap or _next_pow2_above(max_pos)
+
+    # ---- paging: which logical pages exist, then a random physical assignment
+    kv_max_blocks = max(1, max(math.ceil(c / BLOCK) for c in ctx))
+    cmp_max_blocks = max(1, max(math.ceil(n / BLOCK) for n in n_cmp))
+    kv_need = []  # (b, logical page)
+    for b in range(B):
+        npg = math.ceil(ctx[b] / BLOCK)
+        if spec.kv_pages == "window":
+            lo = max(0, ctx[b] - chunk[b] - (spec.window - 1))
+            pages = range(lo // BLOCK, npg)
+        else:
+            pages = range(npg)
+        kv_need += [(b, j) for j in pages]
+    cmp_need = [(b, j) for b in range(B) for j in range(math.ceil(n_cmp[b] / BLOCK))]
+    P_kv = spec.kv_pool_pages or max(1, len(kv_need))
+    P_c = spec.cmp_pool_pages or max(1, len(cmp_need))
+    assert P_kv >= len(kv_need) and P_c >= len(cmp_need)
+    kv_perm = rng.permutation(P_kv)
+    cmp_perm = rng.permutation(P_c)
+    kv_table = np.full((B, kv_max_blocks), -1, dtype=np.int32)
+    cmp_table = np.full((B, cmp_max_blocks), -1, dtype=np.int32)
+    for i, (b, j) in enumerate(kv_need):
+        kv_table[b, j] = kv_perm[i]
+    for i, (b, j) in enumerate(cmp_need):
+        cmp_table[b, j] = cmp_perm[i]
+
+    # ---- pools
+    kv_pool = _normal_bf16(rng, (P_kv, BLOCK, Dm))
+    if spec.cmp_init == "random":
+        cmp_pool = _normal_bf16(rng, (P_c, BLOCK, Dm))
+        idx_pool = torch.from_numpy(rng.integers(-127, 128, size=(P_c, BLOCK, Di), dtype=np.int8))
+        idx_scale = torch.from_numpy(
+            rng.uniform(1e-3, 1e-2, size=(P_c, BLOCK)).astype(np.float32))
+    else:
+        cmp_pool = torch.zeros((P_c, BLOCK, Dm), dtype=torch.bfloat16)
+        idx_pool = torch.zeros((P_c, BLOCK, Di), dtype=torch.int8)
+        idx_scale = torch.zeros((P_c, BLOCK), dtype=torch.float32)
+
+    # ---- per-row activations
+    q = _normal_bf16(rng, (T, spec.heads, Dm))
+    q_idx = _normal_bf16(rng, (T, spec.idx_heads, Di))
+    idx_w = torch.from_numpy(
+        (rng.standard_normal((T, spec.idx_heads)) / 8.0).astype(np.float32))
+    sink = torch.from_numpy(rng.standard_normal(spec.heads).astype(np.float32))
+    # raw KV rows of this chunk are the pool rows at the rows' positions (the
+    # window cache holds the same rows); the index compressor gets its own rows
+    kv_raw = torch.empty((T, Dm), dtype=torch.bfloat16)
+    for t in range(T):
+        b, p = row_req[t], row_pos[t]
+        if b >= 0:
+            kv_raw[t] = kv_pool[int(kv_table[b, p // BLOCK]), p % BLOCK]
+        else:
+            kv_raw[t] = _normal_bf16(rng, (Dm,))
+    idx_raw = _normal_bf16(rng, (T, Di))
+    w_gate = _normal_bf16(rng, (Dm, Dm), std=1.0 / math.sqrt(Dm))
+    ape = torch.from_numpy(rng.standard_normal((r, Dm)).astype(np.float32))
+    w_gate_i = _normal_bf16(rng, (Di, Di), std=1.0 / math.sqrt(Di))
+    ape_i = torch.from_numpy(rng.standard_normal((r, Di)).astype(np.float32))
+    rope_cos, rope_sin = rope_tables(cap, spec.rope_dim, spec.theta)
+
+    t = dict(
+        row_req=torch.tensor(row_req, dtype=torch.int32),
+        row_pos=torch.tensor(row_pos, dtype=torch.int32),
+        kv_len=torch.tensor(ctx, dtype=torch.int32),
+        n_cmp=torch.tensor(n_cmp, dtype=torch.int32),
+        kv_pool=kv_pool,
+        kv_table=torch.from_numpy(kv_table),
+        cmp_pool=cmp_pool,
+        idx_pool=idx_pool,
+        idx_scale=idx_scale,
+        cmp_table=torch.from_numpy(cmp_table),
+        q=q,
+        q_idx=q_idx,
+        idx_w=idx_w,
+        sink=sink,
+        kv_raw=kv_raw,
+        idx_raw=idx_raw,
+        w_gate=w_gate,
+        ape=ape,
+        w_gate_i=w_gate_i,
+        ape_i=ape_i,
+        rope_cos=rope_cos,
+        rope_sin=rope_sin,
+    )
+    return Workload(spec=spec, t=t)
