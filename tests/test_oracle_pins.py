@@ -167,7 +167,7 @@ def test_compress_equal_logits_give_the_mean():
     for b, g, y in res:
         mean = kv[4 * g:4 * g + 4].double().numpy().mean(axis=0)
         # the only difference from the plain mean is the final BF16 rounding
-        assert np.all(np.abs(y - mean) <= 2.0 ** -9 * np.abs(mean) * (1 + 1e-12))
+        assert np.all(np.abs(y - mean) <= 2.0 ** -8 * np.abs(mean) * (1 + 1e-12))
 
 
 def test_compress_one_hot_ape_selects_a_row():
