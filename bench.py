@@ -1,0 +1,437 @@
+"""Benchmark of the CSA hot path on GB300.
+
+One step = one pass of the whole path over one batch: the main compressor,
+the index-key compressor, the indexer top-k and the sparse attention (decode
+or prefill).  Default workload: serving decode (4 requests x 2 rows, contexts
+8192/6000/4097/2048, ratio 2, top-k 512).  Other workloads: --workload
+tiny_decode | ratio1_decode | chunked_prefill | million_decode.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores instead (a bounded sample of the same workload).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "CSA decode token-rows/s + % HBM roofline; prefill tokens/s + % tensor roofline"
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+
+# DRAM traffic per launch from an ncu capture, keyed by kernel; each entry
+# names the source it was taken on (sha1 of the kernel's .cu) so a changed
+# kernel reports null.  Values come from the profiles/ summaries.
+NCU_TRAFFIC = {}
+
+
+def _env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ---------------------------------------------------------------- algorithmic work
+
+
+def algorithmic_work(wl):
+    """Per-kernel algorithmic bytes and FLOPs of one step (see the design doc,
+    "Measurement"), from the workload's shapes only."""
+    s = wl.spec
+    T = s.n_rows
+    rows = [(int(wl.row_req[i]), int(wl.row_pos[i])) for i in range(T)]
+    rows = [(b, p) for b, p in rows if b >= 0]
+    n_cmp = [int(x) for x in wl.n_cmp]
+    vis = [max(0, min(n_cmp[b], (p + 1) // s.ratio)) for b, p in rows]
+    req_vis = {}
+    for (b, _), v in zip(rows, vis):
+        req_vis[b] = max(req_vis.get(b, 0), v)
+    H, D, Hi, Di, W = s.heads, s.head_dim, s.idx_heads, s.idx_dim, s.window
+    sel = [min(s.topk, v) for v in vis]
+    win = [min(W, p + 1) for _, p in rows]
+    idx_bytes = sum(v * (Di + 4) for v in req_vis.values()) + len(rows) * Hi * (Di * 2 + 4)
+    idx_flops = sum(2 * Hi * Di * v for v in vis)
+    if s.mode == "prefill":
+        # window rows are shared by neighbouring query rows: count each once
+        attn_bytes = (len(rows) * H * D * 2 * 2 + sum(n_cmp) * D * 2 +
+                      sum(int(x) for x in wl.kv_len) * D * 2)
+    else:
+        attn_bytes = (sum(sel) * D * 2 + len(req_vis) * (W + 1) * D * 2 +
+                      len(rows) * H * D * 2 * 2 + sum(sel) * 4)
+    attn_flops = sum(4 * H * D * (k + w) for k, w in zip(sel, win))
+    gate_flops = 2 * T * (D * D + Di * Di)
+    topk_bytes = sum(vis) * 4 + len(rows) * s.topk * 8
+    return {
+        "index_score": {"bytes": idx_bytes, "flops": idx_flops},
+        "index_topk": {"bytes": topk_bytes, "flops": 0},
+        "attn_partial": {"bytes": attn_bytes, "flops": attn_flops},
+        "attn_prefill": {"bytes": attn_bytes, "flops": attn_flops},
+        "attn_combine": {"bytes": len(rows) * H * D * 2, "flops": 0},
+        "compress_gate": {"bytes": T * (D + Di) * 2 * 2, "flops": gate_flops},
+        "compress_pool": {"bytes": T * (D + Di) * 2, "flops": 0},
+        "_rows": len(rows),
+    }
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- reference arm (CPU oracle)
+
+
+def _oracle_cores():
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:  # threadpoolctl is optional
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_sample(wl, budget_s=10.0, max_rows=None):
+    """Time the oracle's chain (compress, scores, top-k, attention) on a bounded
+    sample of the workload's rows; returns (rows/s, description)."""
+    import numpy as np  # noqa: F401
+
+    from oracle import step as OS
+
+    s = wl.spec
+    rows = [i for i in range(s.n_rows) if int(wl.row_req[i]) >= 0]
+    if max_rows is not None:
+        rows = rows[:max_rows]
+    t0 = time.perf_counter()
+    pools, _, _ = OS.compress_step(wl.t, s)
+    t_comp = time.perf_counter() - t0
+    done = 0
+    t1 = time.perf_counter()
+    for row in rows:
+        sc = OS.index_row(wl.t, s, pools, row)
+        from oracle import topk_select
+
+        sel = topk_select(sc, s.topk)
+        OS.attention_row(wl.t, s, pools, row, sel)
+        done += 1
+        if time.perf_counter() - t1 > budget_s:
+            break
+    t_rows = time.perf_counter() - t1
+    # compression is per step; charge it per row in proportion
+    per_row = t_rows / done + t_comp / max(1, len(rows))
+    desc = (f"oracle chain on {done} of {len(rows)} rows of {s.name} "
+            f"(compress of the whole chunk {t_comp:.2f}s, rows {t_rows:.2f}s)")
+    return 1.0 / per_row, desc, done
+
+
+def run_reference(args, wl):
+    rate, desc, done = oracle_sample(wl, budget_s=args.ref_budget)
+    cores = _oracle_cores()
+    unit = "tokens/s" if wl.spec.mode == "prefill" else "token_rows/s"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": unit, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(wl, args),
+        "cpu_baseline": {"value": rate, "unit": unit, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": rate, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(wl, args):
+    s = wl.spec
+    return {"workload": s.name, "requests": s.n_req, "rows": s.n_rows, "contexts": s.ctx,
+            "ratio": s.ratio, "topk": s.topk, "heads": s.heads, "head_dim": s.head_dim,
+            "idx_heads": s.idx_heads, "idx_dim": s.idx_dim, "window": s.window,
+            "l2": "flushed before every timed step (256 MiB write)",
+            "parallelism": f"replicas x{args.gpus}"}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+
+def _src_sha(name):
+    path = os.path.join(ROOT, "prefill_csa_compress_gb300", "csrc", name)
+    try:
+        return hashlib.sha1(open(path, "rb").read()).hexdigest()[:12]
+    except OSError:
+        return None
+
+
+KERNEL_SRC = {"index_score": "k_index.cu", "index_topk": "k_index.cu",
+              "attn_partial": "k_attn.cu", "attn_combine": "k_attn.cu",
+              "attn_prefill": "k_attn.cu", "compress_gate": "k_compress.cu",
+              "compress_pool": "k_compress.cu"}
+
+
+def run_gpu(args, wl, rank, world, local_rank):
+    import torch
+
+    import prefill_csa_compress_gb300 as csa
+    from prefill_csa_compress_gb300.pipeline import CsaStep
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    s = wl.spec
+    t = wl.to(dev)
+    prefill = s.mode == "prefill"
+    step = CsaStep(t, s.ratio, s.topk, prefill=prefill).prepare()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    work = algorithmic_work(wl)
+    units = work["_rows"]
+
+    def flush_l2():
+        flush.fill_(1)
+
+    # ---- warm-up (also finds the dominant kernel)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    kernels = ["index_score", "index_topk", "attn_prefill" if prefill else "attn_partial",
+               "attn_combine", "compress_gate", "compress_pool"]
+    per_kernel = {}
+    for k in kernels:
+        csa.prof_enable(k, 64)
+        for _ in range(3):
+            flush_l2()
+            step.run()
+        ms, n = csa.prof_read(k)
+        csa.prof_disable()
+        if n:
+            per_kernel[k] = {"ms_per_launch": ms / n, "launches_per_step": n / 3}
+    dominant = max(per_kernel, key=lambda k: per_kernel[k]["ms_per_launch"] *
+                   per_kernel[k]["launches_per_step"])
+    launches_per_step = None
+
+    # ---- timed region: device time of exactly K steps, L2 flushed before each
+    csa.prof_enable(dominant, args.steps * 4 + 8)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    lc0 = csa.launch_count()
+    wall0 = time.perf_counter()
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush_l2()
+            ev[i][0].record(stream)
+            step.run()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    launches = csa.launch_count() - lc0
+    if dist:
+        dist.barrier()
+    dom_ms, dom_n = csa.prof_read(dominant)
+    csa.prof_disable()
+    total_ms = sum(a.elapsed_time(b) for a, b in ev)
+    if dist:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    value = units * world * args.steps / (total_ms / 1e3)
+    launches_per_step = launches / args.steps
+    status = int(step.status.item())
+
+    # ---- end to end through the public API with host buffers
+    per_step_inputs = ["q", "q_idx", "idx_w", "kv_raw", "idx_raw", "row_req", "row_pos",
+                       "kv_len", "n_cmp"]
+    host_in = {k: wl.t[k].pin_memory() for k in per_step_inputs}
+    host_out = step.out.cpu().pin_memory()
+    host_lse = step.lse.cpu().pin_memory()
+    bi = sum(v.numel() * v.element_size() for v in host_in.values())
+    bo = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+    ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush_l2()
+        ee[i][0].record(stream)
+        for k, v in host_in.items():
+            t[k].copy_(v, non_blocking=True)
+        step.run()
+        host_out.copy_(step.out, non_blocking=True)
+        host_lse.copy_(step.lse, non_blocking=True)
+        ee[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in ee)
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = units * world * args.steps / (e2e_ms / 1e3)
+
+    # ---- roofline of the dominant kernel
+    peaks = _peaks()
+    dom_avg_ms = dom_ms / max(1, dom_n)
+    w = work[dominant]
+    if prefill and w["flops"] > 0 and dominant in ("attn_prefill", "index_score"):
+        achieved = w["flops"] / (dom_avg_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"]}
+    else:
+        per_launch = w["bytes"] / max(1.0, per_kernel[dominant]["launches_per_step"])
+        achieved = per_launch / (dom_avg_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    tr = NCU_TRAFFIC.get((s.name, dominant))
+    roof["traffic"] = tr["bytes"] if tr and tr["src"] == _src_sha(KERNEL_SRC[dominant]) else None
+    roof["kernel"] = dominant
+    roof["kernel_ms"] = dom_avg_ms
+    roof["peak_source"] = peaks["source"]
+
+    result = None
+    if rank == 0:
+        unit = "tokens/s" if prefill else "token_rows/s"
+        result = {
+            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": _config(wl, args), "roofline": roof,
+            "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": bi,
+                    "d2h_bytes_per_step": bo},
+            "gpu_launches": launches, "launches_per_step": launches_per_step,
+            "clocks": clk.summary(), "wall_s": wall, "device_status": status,
+            "per_kernel_ms": {k: v["ms_per_launch"] * v["launches_per_step"]
+                              for k, v in per_kernel.items()},
+        }
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="serving_decode")
+    ap.add_argument("--ref-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local_rank = _env_rank()
+
+    from workloads import make_workload, spec_for
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        run_reference(args, make_workload(spec_for(args.workload)))
+        return 0
+
+    spec = spec_for(args.workload)
+    if world > 1:
+        # weak scaling: every rank runs its own batch of the same shape
+        spec.seed = spec.seed + 1000 * rank
+    wl = make_workload(spec)
+    # the oracle's CPU timing runs before any CUDA work (no fork after CUDA init)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, desc, _ = oracle_sample(wl, budget_s=args.ref_budget)
+        cpu = {"value": rate, "unit": "tokens/s" if spec.mode == "prefill" else "token_rows/s",
+               "cores": _oracle_cores(), "kind": "oracle", "sample": desc}
+    res = run_gpu(args, wl, rank, world, local_rank)
+    if rank == 0:
+        res["cpu_baseline"] = cpu
+        print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

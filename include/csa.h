@@ -1,0 +1,309 @@
+/*
+ * csa.h - C ABI of the GB300 (sm_103a) compressed sparse attention library.
+ *
+ * Compressed sparse attention (CSA) as in DeepSeek-V4 / V4.1: a gated
+ * compressor pools every `ratio` raw KV rows into one compressed entry, an
+ * INT8 "lightning" indexer scores the compressed entries of every query row
+ * and keeps the top-k, and shared-KV sparse attention runs over the selected
+ * entries plus a 128-token causal raw window with a per-head sink logit.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All tensors are caller-owned DEVICE pointers, dense and row-major in the
+ *   shapes given below (no strides beyond those shapes).  The library keeps no
+ *   pointer after a call returns and allocates no device memory: scratch is
+ *   the caller's `workspace`.  Calling with workspace == NULL only stores the
+ *   number of bytes the call needs in `workspace_bytes` and returns CSA_OK.
+ * - Paged pools hold 128-row pages ([pages, 128, width]).  A block table row
+ *   b maps request b's logical page j to a physical page; entries of pages a
+ *   call never reads may be -1 ("DeepSeek V4-Flash, MTP point", "Deployment
+ *   configuration": 128-token pages; "DeepSeek V4.1 Flash", compressed KV and
+ *   index keys share one block table).
+ * - BF16 tensors are passed as `const void*` (IEEE bfloat16 bit patterns).
+ * - RoPE tables are FP32 half-width [rope_cap, 32] cos/sin tables; the last 64
+ *   channels of a vector are rotated by adjacent pairs (x[2i], x[2i+1]) ->
+ *   (x[2i]c - x[2i+1]s, x[2i]s + x[2i+1]c) at a position's table row; a
+ *   negative position means the identity ("DeepSeek V4.1 Flash",
+ *   "Serving-owned full RoPE tables").  A position >= rope_cap also gives the
+ *   identity and raises CSA_DEV_POS_GE_CAP.
+ * - Every call is asynchronous on `stream` (a cudaStream_t) and never
+ *   synchronises.  The return value reports host-side argument checks and
+ *   launch errors only.  Data errors found on the device (bad page, bad
+ *   position, bad index) are OR-ed into the optional caller word
+ *   `*status_dev` (CSA_DEV_* bits) and the offending element is skipped; the
+ *   device never traps.
+ * - A row with row_req[t] < 0 is padding: it is neither read nor written
+ *   ("DeepSeek-V4.1 native paged runtime": a padding token's batch id is -1).
+ * - Every args struct starts with `struct_size`; set it to sizeof(struct).
+ */
+#ifndef CSA_H_
+#define CSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CSA_API __attribute__((visibility("default")))
+
+typedef void *csa_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  CSA_OK = 0,
+  CSA_ERR_INVALID_ARG = 1, /* a null pointer, a bad size or a misaligned pointer */
+  CSA_ERR_UNSUPPORTED = 2, /* a shape this build does not implement */
+  CSA_ERR_CUDA = 3,        /* a CUDA launch or runtime error */
+  CSA_ERR_TIMEOUT = 4      /* reserved: a bounded device wait gave up */
+} csa_status_t;
+
+/* bits OR-ed into *status_dev by the kernels */
+#define CSA_DEV_BAD_BLOCK 0x1u  /* block-table entry < 0 or >= pool pages on a page that is read */
+#define CSA_DEV_BAD_POS 0x2u    /* a window position >= kv_len, or a bad request id */
+#define CSA_DEV_BAD_INDEX 0x4u  /* a top-k entry outside [0, visible count) */
+#define CSA_DEV_POS_GE_CAP 0x8u /* a position >= rope_cap (rotation skipped) */
+#define CSA_DEV_TIMEOUT 0x10u   /* reserved */
+
+#define CSA_BLOCK 128    /* rows per page */
+#define CSA_ROPE_DIM 64  /* rotated channels (the last 64) */
+#define CSA_WINDOW 128   /* raw window, self included */
+#define CSA_MAX_TOPK 2048
+
+typedef enum { CSA_OUT_BF16 = 0, CSA_OUT_INT8 = 1 } csa_out_mode_t;
+typedef enum { CSA_MODE_AUTO = 0, CSA_MODE_DECODE = 1, CSA_MODE_PREFILL = 2 } csa_mode_t;
+
+/* ------------------------------------------------------------------------
+ * csa_compress - gated compression of every complete group of `ratio` rows.
+ *
+ * Source: "DeepSeek V4.1 Flash", "Compressor state ownership" (each token
+ * carries a KV projection and a gate score of the same width; the pooling
+ * softmax; BF16 rounding before RMSNorm) and "Serving-owned full RoPE tables"
+ * (compressed rows rotate at their compression-group start position);
+ * "DeepSeek V4-Flash, MTP point", "Attention paths" (main compressor
+ * rotate=False, index-key compressor rotate=True) and "What is quantized"
+ * (INT8 idx_kv quantised on write: amax floored at 1e-4 scaled to 127, FP32
+ * per-row scale).
+ *
+ * Group g of request b is positions g*r .. g*r+r-1.  It is written iff rows
+ * t-r+1 .. t of this chunk are request b at exactly those positions.  Per
+ * channel d:  logit[j,d] = (x_j . w_gate[:,d]) + ape[j,d];  w = softmax_j;
+ * y[d] = sum_j w[j,d] kv_j[d];  y = bf16(y);  optionally
+ * y = bf16(gamma * y / sqrt(mean(y^2) + rms_eps));  optionally rotate at g*r;
+ * then store BF16 into cmp_pool, or INT8 codes + FP32 scale into
+ * idx_pool/idx_scale_pool, at logical entry g of request b.
+ *
+ * Shapes: x bf16 [n_rows, dx]; kv bf16 [n_rows, d]; w_gate bf16 [dx, d];
+ * ape f32 [ratio, d]; gamma bf16 [d] or NULL; positions, row_req i32 [n_rows];
+ * block_table i32 [n_req, max_blocks]; cmp_pool bf16 [n_blocks, 128, d];
+ * idx_pool i8 [n_blocks, 128, d]; idx_scale_pool f32 [n_blocks, 128].
+ * Supported: ratio in {1, 2, 4}; d in {128, 512}; dx a multiple of 64 <= 1024.
+ * Workspace: n_rows * d * 4 bytes (gate logits), rounded up.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  uint32_t struct_size;
+  int32_t n_rows;
+  int32_t ratio;
+  int32_t dx;
+  int32_t d;
+  int32_t out_mode; /* csa_out_mode_t */
+  int32_t rotate;   /* 1: rotate at the group start (needs rope tables) */
+  int32_t rope_cap;
+  const void *x;
+  const void *kv;
+  const void *w_gate;
+  const float *ape;
+  const void *gamma;
+  float rms_eps;
+  const int32_t *positions;
+  const int32_t *row_req;
+  const float *rope_cos;
+  const float *rope_sin;
+  const int32_t *block_table;
+  int32_t n_req;
+  int32_t max_blocks;
+  int32_t n_blocks;
+  void *cmp_pool;
+  int8_t *idx_pool;
+  float *idx_scale_pool;
+  uint32_t *status_dev;
+  void *workspace;
+  size_t workspace_bytes;
+} csa_compress_args;
+
+CSA_API csa_status_t csa_compress(csa_compress_args *args, csa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * csa_index_topk - lightning-indexer scores and deterministic top-k.
+ *
+ * Source: "Hyper-Parallel ... DeepSeek V4 CP" (gitcode issue #2), sections
+ * "10. ratio=4 Global Top-k" (per-row index queries and head weights against
+ * the compressed index keys; outputs are compressed slot ids), "10.3 Causal
+ * mask" (slot c is visible to position p iff c < (p+1)//ratio); "DeepSeek
+ * V4.1 Flash", "Compressor state ownership" (selections in logical-position
+ * order with trailing -1 padding); "DeepSeek V4-Flash, MTP point" (INT8
+ * idx_kv with FP32 per-row idx_kv_scale).
+ *
+ * For row t of request b = row_req[t] at p = row_pos[t], visible entries are
+ * c < V = min(n_cmp[b], (p+1)/ratio) and
+ *   score[c] = scale_c * sum_h w[t,h] * act(q_h . k_c),   act = ReLU if relu
+ * where q_h is q_idx[t,h,:] rotated at p when rope tables are given (NULL:
+ * q_idx is already rotated) and k_c the INT8 key.  The k best entries by
+ * (score descending, index ascending) are written to topk_idx[t] as logical
+ * positions in ascending order, padded with -1 when V < k; topk_score (if
+ * non-NULL) gets their scores in the same order (padding: -inf).  `scores`
+ * (if non-NULL, f32 [n_rows, score_cols], score_cols >= max_blocks*128)
+ * receives every visible score; entries c >= V are left untouched.
+ *
+ * Shapes: q_idx bf16 [n_rows, n_heads, 128]; weights f32 [n_rows, n_heads];
+ * row_req, row_pos i32 [n_rows]; n_cmp i32 [n_req]; idx_pool i8
+ * [n_blocks, 128, 128]; idx_scale_pool f32 [n_blocks, 128]; cmp_block_table
+ * i32 [n_req, max_blocks]; topk_idx i32 [n_rows, topk]; topk_score f32
+ * [n_rows, topk] or NULL.  Supported: n_heads == 64, head_dim == 128,
+ * 1 <= topk <= 2048, ratio >= 1.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  uint32_t struct_size;
+  int32_t n_rows;
+  int32_t n_heads;
+  int32_t head_dim;
+  int32_t ratio;
+  int32_t topk;
+  int32_t relu;
+  int32_t mode; /* csa_mode_t: a tiling hint only; results do not depend on it */
+  const void *q_idx;
+  const float *weights;
+  const int32_t *row_req;
+  const int32_t *row_pos;
+  const int32_t *n_cmp;
+  const int8_t *idx_pool;
+  const float *idx_scale_pool;
+  const int32_t *cmp_block_table;
+  int32_t n_req;
+  int32_t max_blocks;
+  int32_t n_blocks;
+  const float *rope_cos;
+  const float *rope_sin;
+  int32_t rope_cap;
+  int32_t *topk_idx;
+  float *topk_score;
+  float *scores;
+  int32_t score_cols;
+  uint32_t *status_dev;
+  void *workspace;
+  size_t workspace_bytes;
+} csa_index_args;
+
+CSA_API csa_status_t csa_index_topk(csa_index_args *args, csa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * csa_sparse_attn_decode / csa_sparse_attn_prefill - shared-KV sparse
+ * attention with an attention sink.
+ *
+ * Source: "Hyper-Parallel ... DeepSeek V4 CP", "二阶段 CP 总体算法" (Stage-2:
+ * sparse attention over the window KV and the selected compressed KV with
+ * sinks, softmax_scale and ori_win_left = 127; outputs out and lse), "9.1"
+ * (the candidate list is the window rows followed by the compressed rows),
+ * "7. Window KV Halo" (the window includes the query's own position);
+ * "DeepSeek V4-Flash, MTP point", "Deployment configuration" (decode: 2 rows
+ * per request; prefill: up to 8192 tokens walked in 128-token tiles).
+ *
+ * For row t (request b, position p), candidates are cmp entry c for every
+ * c = topk_idx[t, i] >= 0 and raw row p' for p' in [max(0, p-window+1), p].
+ * Each candidate row k_i is both key and value.  Per head h, with q_h =
+ * q[t,h,:] rotated at p:
+ *   l_i = softmax_scale * q_h . k_i
+ *   out[t,h,:] = sum_i e^{l_i} k_i / (sum_i e^{l_i} + e^{sink_h})
+ *   lse[t,h]   = log(sum_i e^{l_i} + e^{sink_h})
+ * sink == NULL means -inf (plain softmax).  inv_rope_out rotates the output
+ * back by -p.  Top-k entries must be unique (the indexer guarantees it); an
+ * entry outside [0, min(n_cmp[b], (p+1)/ratio)) raises CSA_DEV_BAD_INDEX and
+ * is skipped; a window position >= kv_len[b] raises CSA_DEV_BAD_POS and is
+ * skipped.
+ *
+ * Shapes: q bf16 [n_rows, n_heads, 512]; kv_pool, cmp_pool bf16
+ * [*, 128, 512]; kv_block_table i32 [n_req, kv_max_blocks]; cmp_block_table
+ * i32 [n_req, cmp_max_blocks]; kv_len, n_cmp i32 [n_req]; topk_idx i32
+ * [n_rows, topk]; sink f32 [n_heads] or NULL; out bf16 [n_rows, n_heads,
+ * 512]; lse f32 [n_rows, n_heads] or NULL.  Supported: n_heads == 64,
+ * head_dim == 512, window == 128, topk <= 2048.
+ * The decode call splits each row's candidates over CTAs and merges the
+ * partial softmaxes; the prefill call is tiled for many rows.  Both compute
+ * the same function.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  uint32_t struct_size;
+  int32_t n_rows;
+  int32_t n_heads;
+  int32_t head_dim;
+  int32_t ratio;
+  int32_t topk;
+  int32_t window;
+  int32_t inv_rope_out;
+  float softmax_scale;
+  const void *q;
+  const int32_t *row_req;
+  const int32_t *row_pos;
+  const int32_t *topk_idx;
+  const void *kv_pool;
+  const int32_t *kv_block_table;
+  int32_t kv_max_blocks;
+  int32_t kv_n_blocks;
+  const int32_t *kv_len;
+  const void *cmp_pool;
+  const int32_t *cmp_block_table;
+  int32_t cmp_max_blocks;
+  int32_t cmp_n_blocks;
+  const int32_t *n_cmp;
+  int32_t n_req;
+  const float *sink;
+  const float *rope_cos;
+  const float *rope_sin;
+  int32_t rope_cap;
+  void *out;
+  float *lse;
+  uint32_t *status_dev;
+  void *workspace;
+  size_t workspace_bytes;
+} csa_attn_args;
+
+CSA_API csa_status_t csa_sparse_attn_decode(csa_attn_args *args, csa_stream_t stream);
+CSA_API csa_status_t csa_sparse_attn_prefill(csa_attn_args *args, csa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Library information and measurement hooks (no counterpart on the pages).
+ * ---------------------------------------------------------------------- */
+
+/* "csa <version> sm_103a" */
+CSA_API const char *csa_version(void);
+/* human-readable name of a status code */
+CSA_API const char *csa_status_string(csa_status_t s);
+/* number of kernels this process has launched through the library */
+CSA_API uint64_t csa_launch_count(void);
+
+/* Kernel identifiers for the timing hooks. */
+typedef enum {
+  CSA_K_COMPRESS_GATE = 0,
+  CSA_K_COMPRESS_POOL = 1,
+  CSA_K_INDEX_SCORE = 2,
+  CSA_K_INDEX_TOPK = 3,
+  CSA_K_ATTN_PARTIAL = 4,
+  CSA_K_ATTN_COMBINE = 5,
+  CSA_K_ATTN_PREFILL = 6,
+  CSA_K_COUNT = 7
+} csa_kernel_id_t;
+
+/* Record a CUDA event pair around every launch of kernel `kernel_id` (up to
+ * `max_launches` launches) on the launching stream.  Events are created by
+ * the library; this allocates no device memory. */
+CSA_API csa_status_t csa_prof_enable(int32_t kernel_id, int32_t max_launches);
+/* Synchronise the recorded events and return the summed device time (ms) and
+ * the number of launches recorded since csa_prof_enable. */
+CSA_API csa_status_t csa_prof_read(int32_t kernel_id, float *total_ms, int32_t *n_launches);
+CSA_API csa_status_t csa_prof_disable(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_H_ */

@@ -1,0 +1,261 @@
+// extern "C" entry points: host-side argument checks, workspace layout and
+// kernel dispatch.  No entry point synchronises or allocates device memory.
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "csa_internal.cuh"
+
+namespace csa {
+
+// ---------------------------------------------------------------- launch accounting
+
+static std::atomic<uint64_t> g_launches{0};
+
+struct ProfState {
+  std::mutex mu;
+  int kernel_id = -1;
+  int max_launches = 0;
+  int recorded = 0;
+  std::vector<cudaEvent_t> ev;  // 2 per launch
+};
+static ProfState g_prof;
+
+void launch_begin(int kernel_id, cudaStream_t s) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (g_prof.kernel_id != kernel_id) return;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (g_prof.recorded < g_prof.max_launches)
+    cudaEventRecord(g_prof.ev[2 * g_prof.recorded], s);
+}
+
+void launch_end(int kernel_id, cudaStream_t s) {
+  if (g_prof.kernel_id != kernel_id) return;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (g_prof.recorded < g_prof.max_launches) {
+    cudaEventRecord(g_prof.ev[2 * g_prof.recorded + 1], s);
+    ++g_prof.recorded;
+  }
+}
+
+}  // namespace csa
+
+using namespace csa;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+csa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
+
+// ---- decode split-K geometry: fill about two waves of the 152 SMs
+constexpr int kAttnTile = 32;
+constexpr int kTargetCtas = 2 * 152;
+
+void attn_geometry(const csa_attn_args &a, bool decode, int *n_splits, int *tiles_per_split) {
+  const int n_cand = a.topk + a.window;
+  const int tiles = (n_cand + kAttnTile - 1) / kAttnTile;
+  if (!decode || a.n_rows <= 0) {
+    *n_splits = 1;
+    *tiles_per_split = tiles;
+    return;
+  }
+  int want = (kTargetCtas + a.n_rows - 1) / a.n_rows;
+  if (want < 1) want = 1;
+  if (want > tiles) want = tiles;
+  const int tps = (tiles + want - 1) / want;
+  *tiles_per_split = tps;
+  *n_splits = (tiles + tps - 1) / tps;
+}
+
+size_t attn_partial_bytes(const csa_attn_args &a, int n_splits) {
+  if (n_splits <= 1) return 0;
+  return align_up((size_t)a.n_rows * n_splits * kHeads * (kHeadDim + 2) * sizeof(float), kAlign);
+}
+
+// shape checks (enough to size the workspace)
+csa_status_t check_attn_shape(const csa_attn_args *a) {
+  if (!a || a->struct_size < sizeof(csa_attn_args)) return CSA_ERR_INVALID_ARG;
+  if (a->n_rows < 0 || a->n_req < 0 || a->topk < 0 || a->topk > CSA_MAX_TOPK)
+    return CSA_ERR_INVALID_ARG;
+  if (a->n_heads != kHeads || a->head_dim != kHeadDim || a->window != kWindow)
+    return CSA_ERR_UNSUPPORTED;
+  if (a->ratio < 1) return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
+// pointer and size checks before a launch
+csa_status_t check_attn_args(const csa_attn_args *a) {
+  if (!a->q || !a->row_req || !a->row_pos || !a->kv_pool || !a->kv_block_table || !a->kv_len ||
+      !a->cmp_pool || !a->cmp_block_table || !a->n_cmp || !a->out)
+    return CSA_ERR_INVALID_ARG;
+  if (a->topk > 0 && !a->topk_idx) return CSA_ERR_INVALID_ARG;
+  if ((a->rope_cos == nullptr) != (a->rope_sin == nullptr)) return CSA_ERR_INVALID_ARG;
+  if (a->rope_cos && a->rope_cap <= 0) return CSA_ERR_INVALID_ARG;
+  if (a->kv_max_blocks <= 0 || a->cmp_max_blocks <= 0 || a->kv_n_blocks <= 0 ||
+      a->cmp_n_blocks <= 0 || a->n_req <= 0)
+    return CSA_ERR_INVALID_ARG;
+  if (!aligned16(a->q) || !aligned16(a->kv_pool) || !aligned16(a->cmp_pool) || !aligned16(a->out))
+    return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
+csa_status_t run_attn(csa_attn_args *a, cudaStream_t s, bool decode) {
+  csa_status_t st = check_attn_shape(a);
+  if (st != CSA_OK) return st;
+  int n_splits = 1, tps = 1;
+  attn_geometry(*a, decode, &n_splits, &tps);
+  const size_t need = attn_partial_bytes(*a, n_splits);
+  if (!a->workspace) {
+    a->workspace_bytes = need;
+    return CSA_OK;
+  }
+  if (a->workspace_bytes < need) return CSA_ERR_INVALID_ARG;
+  if (a->n_rows == 0) return CSA_OK;
+  st = check_attn_args(a);
+  if (st != CSA_OK) return st;
+  return from_cuda(launch_attn(*a, n_splits, tps, static_cast<float *>(a->workspace), s));
+}
+
+}  // namespace
+
+extern "C" {
+
+CSA_API const char *csa_version(void) { return "csa 0.1.0 sm_103a"; }
+
+CSA_API const char *csa_status_string(csa_status_t s) {
+  switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_INVALID_ARG: return "invalid argument";
+    case CSA_ERR_UNSUPPORTED: return "unsupported shape";
+    case CSA_ERR_CUDA: return "CUDA error";
+    case CSA_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+CSA_API uint64_t csa_launch_count(void) { return g_launches.load(); }
+
+// ---------------------------------------------------------------- compress
+
+CSA_API csa_status_t csa_compress(csa_compress_args *a, csa_stream_t stream) {
+  if (!a || a->struct_size < sizeof(csa_compress_args)) return CSA_ERR_INVALID_ARG;
+  if (a->n_rows < 0 || a->n_req < 0) return CSA_ERR_INVALID_ARG;
+  if (a->ratio != 1 && a->ratio != 2 && a->ratio != 4) return CSA_ERR_UNSUPPORTED;
+  if (a->d != 128 && a->d != 512) return CSA_ERR_UNSUPPORTED;
+  if (a->dx <= 0 || a->dx % 64 != 0 || a->dx > 1024) return CSA_ERR_UNSUPPORTED;
+  if (a->out_mode != CSA_OUT_BF16 && a->out_mode != CSA_OUT_INT8) return CSA_ERR_INVALID_ARG;
+  const size_t need = align_up((size_t)a->n_rows * a->d * sizeof(float), kAlign);
+  if (!a->workspace) {
+    a->workspace_bytes = need;
+    return CSA_OK;
+  }
+  if (a->workspace_bytes < need) return CSA_ERR_INVALID_ARG;
+  if (a->n_rows == 0) return CSA_OK;
+  if (!a->x || !a->kv || !a->w_gate || !a->ape || !a->positions || !a->row_req ||
+      !a->block_table)
+    return CSA_ERR_INVALID_ARG;
+  if (a->n_req <= 0 || a->max_blocks <= 0 || a->n_blocks <= 0) return CSA_ERR_INVALID_ARG;
+  if (a->out_mode == CSA_OUT_BF16 && !a->cmp_pool) return CSA_ERR_INVALID_ARG;
+  if (a->out_mode == CSA_OUT_INT8 && (!a->idx_pool || !a->idx_scale_pool))
+    return CSA_ERR_INVALID_ARG;
+  if (a->rotate && (!a->rope_cos || !a->rope_sin || a->rope_cap <= 0)) return CSA_ERR_INVALID_ARG;
+  return from_cuda(
+      launch_compress(*a, static_cast<float *>(a->workspace), static_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------- index + top-k
+
+CSA_API csa_status_t csa_index_topk(csa_index_args *a, csa_stream_t stream) {
+  if (!a || a->struct_size < sizeof(csa_index_args)) return CSA_ERR_INVALID_ARG;
+  if (a->n_rows < 0 || a->n_req < 0) return CSA_ERR_INVALID_ARG;
+  if (a->n_heads != kHeads || a->head_dim != kIdxDim) return CSA_ERR_UNSUPPORTED;
+  if (a->topk < 1 || a->topk > CSA_MAX_TOPK || a->ratio < 1) return CSA_ERR_INVALID_ARG;
+  if (a->max_blocks <= 0) return CSA_ERR_INVALID_ARG;
+  const int n_cap = a->max_blocks * kBlock;
+  const bool own_scores = a->scores != nullptr;
+  if (own_scores && a->score_cols < n_cap) return CSA_ERR_INVALID_ARG;
+  const size_t need =
+      own_scores ? 0 : align_up((size_t)a->n_rows * n_cap * sizeof(float), kAlign);
+  if (!a->workspace) {
+    a->workspace_bytes = need;
+    return CSA_OK;
+  }
+  if (a->workspace_bytes < need) return CSA_ERR_INVALID_ARG;
+  if (a->n_rows == 0) return CSA_OK;
+  if (!a->q_idx || !a->weights || !a->row_req || !a->row_pos || !a->n_cmp || !a->idx_pool ||
+      !a->idx_scale_pool || !a->cmp_block_table || !a->topk_idx)
+    return CSA_ERR_INVALID_ARG;
+  if (a->n_req <= 0 || a->n_blocks <= 0) return CSA_ERR_INVALID_ARG;
+  if ((a->rope_cos == nullptr) != (a->rope_sin == nullptr)) return CSA_ERR_INVALID_ARG;
+  if (a->rope_cos && a->rope_cap <= 0) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(a->idx_pool) || !aligned16(a->q_idx)) return CSA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float *scores = own_scores ? a->scores : static_cast<float *>(a->workspace);
+  const int cols = own_scores ? a->score_cols : n_cap;
+  cudaError_t e = launch_index_scores(*a, scores, cols, s);
+  if (e != cudaSuccess) return CSA_ERR_CUDA;
+  return from_cuda(launch_index_topk(*a, scores, cols, s));
+}
+
+// ---------------------------------------------------------------- attention
+
+CSA_API csa_status_t csa_sparse_attn_decode(csa_attn_args *a, csa_stream_t stream) {
+  return run_attn(a, static_cast<cudaStream_t>(stream), true);
+}
+
+CSA_API csa_status_t csa_sparse_attn_prefill(csa_attn_args *a, csa_stream_t stream) {
+  return run_attn(a, static_cast<cudaStream_t>(stream), false);
+}
+
+// ---------------------------------------------------------------- timing hooks
+
+CSA_API csa_status_t csa_prof_enable(int32_t kernel_id, int32_t max_launches) {
+  if (kernel_id < 0 || kernel_id >= CSA_K_COUNT || max_launches <= 0) return CSA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
+  g_prof.ev.assign(2 * (size_t)max_launches, nullptr);
+  for (auto &e : g_prof.ev)
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      g_prof.ev.clear();
+      g_prof.kernel_id = -1;
+      return CSA_ERR_CUDA;
+    }
+  g_prof.max_launches = max_launches;
+  g_prof.recorded = 0;
+  g_prof.kernel_id = kernel_id;
+  return CSA_OK;
+}
+
+CSA_API csa_status_t csa_prof_read(int32_t kernel_id, float *total_ms, int32_t *n_launches) {
+  if (!total_ms || !n_launches) return CSA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  *total_ms = 0.f;
+  *n_launches = 0;
+  if (g_prof.kernel_id != kernel_id) return CSA_OK;
+  float sum = 0.f;
+  for (int i = 0; i < g_prof.recorded; ++i) {
+    if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess) return CSA_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess)
+      return CSA_ERR_CUDA;
+    sum += ms;
+  }
+  *total_ms = sum;
+  *n_launches = g_prof.recorded;
+  return CSA_OK;
+}
+
+CSA_API csa_status_t csa_prof_disable(void) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
+  g_prof.ev.clear();
+  g_prof.kernel_id = -1;
+  g_prof.recorded = 0;
+  g_prof.max_launches = 0;
+  return CSA_OK;
+}
+
+}  // extern "C"

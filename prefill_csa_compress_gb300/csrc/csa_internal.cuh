@@ -1,0 +1,77 @@
+// Internal declarations shared by the CSA kernels and the C-ABI layer.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "csa.h"
+
+namespace csa {
+
+constexpr int kBlock = CSA_BLOCK;       // rows per page
+constexpr int kRopeDim = CSA_ROPE_DIM;  // rotated channels
+constexpr int kRopeHalf = kRopeDim / 2;
+constexpr int kHeadDim = 512;           // attention head / KV width
+constexpr int kIdxDim = 128;            // index-key width
+constexpr int kHeads = 64;              // query heads and index heads
+constexpr int kWindow = CSA_WINDOW;
+
+// ---------------------------------------------------------------- host side
+
+// Bracket one kernel launch: counts launches and, when enabled, records a
+// CUDA event pair on the launching stream for that kernel id.
+void launch_begin(int kernel_id, cudaStream_t s);
+void launch_end(int kernel_id, cudaStream_t s);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Launchers (one per kernel family); each returns cudaGetLastError().
+cudaError_t launch_compress(const csa_compress_args &a, float *logits, cudaStream_t s);
+cudaError_t launch_index_scores(const csa_index_args &a, float *scores, int score_cols,
+                                cudaStream_t s);
+cudaError_t launch_index_topk(const csa_index_args &a, const float *scores, int score_cols,
+                              cudaStream_t s);
+cudaError_t launch_attn(const csa_attn_args &a, int n_splits, int tiles_per_split,
+                        float *partials, cudaStream_t s);
+
+// ---------------------------------------------------------------- device side
+
+__device__ __forceinline__ void flag(uint32_t *status, uint32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ float round_bf16(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// Physical row of logical position `pos` of request b in a paged pool, or -1
+// (and a flag) when the page is unmapped or outside the pool.
+__device__ __forceinline__ long long page_row(const int32_t *table, int max_blocks, int n_blocks,
+                                              int b, int pos, uint32_t *status) {
+  int page = pos / kBlock;
+  if (page >= max_blocks) {
+    flag(status, CSA_DEV_BAD_BLOCK);
+    return -1;
+  }
+  int phys = table[(long long)b * max_blocks + page];
+  if (phys < 0 || phys >= n_blocks) {
+    flag(status, CSA_DEV_BAD_BLOCK);
+    return -1;
+  }
+  return (long long)phys * kBlock + (pos % kBlock);
+}
+
+// Number of compressed entries visible to a query at position p:
+// min(n_cmp, (p + 1) / ratio), 0 for negative positions.
+__device__ __forceinline__ int visible_count(int p, int ratio, int n_cmp) {
+  if (p < 0) return 0;
+  int v = (p + 1) / ratio;
+  return v < n_cmp ? v : n_cmp;
+}
+
+}  // namespace csa

@@ -1,0 +1,123 @@
+"""One CSA step over resident device buffers: main compressor, index-key
+compressor, indexer top-k, then sparse attention -- the order the V4 decode
+layer calls them ("DeepSeek V4-Flash, MTP point", "Attention paths").
+
+``CsaStep`` owns the outputs and workspaces so that repeated steps allocate
+nothing; it is plumbing around the four library calls and computes nothing
+itself.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import _binding as B
+
+
+class CsaStep:
+    """Buffers and call sequence for one step.
+
+    ``t`` maps names to device tensors: row_req, row_pos, kv_len, n_cmp,
+    kv_pool, kv_table, cmp_pool, idx_pool, idx_scale, cmp_table, q, q_idx,
+    idx_w, sink, kv_raw, idx_raw, w_gate, ape, w_gate_i, ape_i, rope_cos,
+    rope_sin.  ``ratio``, ``topk`` and ``prefill`` describe the step.
+    """
+
+    def __init__(self, t: dict, ratio: int, topk: int, prefill: bool = False,
+                 compress: bool = True, status: bool = True):
+        self.t = t
+        self.ratio = int(ratio)
+        self.topk = int(topk)
+        self.prefill = bool(prefill)
+        self.do_compress = bool(compress)
+        dev = t["q"].device
+        T = t["q"].shape[0]
+        self.topk_idx = torch.full((T, self.topk), -1, dtype=torch.int32, device=dev)
+        self.topk_score = torch.empty((T, self.topk), dtype=torch.float32, device=dev)
+        self.out = torch.zeros_like(t["q"])
+        self.lse = torch.zeros(t["q"].shape[:2], dtype=torch.float32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev) if status else None
+        self.ws = {}
+        self._prepared = None
+
+    def _ws(self, name):
+        return self.ws.get(name)
+
+    def compress(self, stream=None):
+        t = self.t
+        self.ws["cm"] = B.csa_compress(
+            x=t["kv_raw"], kv=t["kv_raw"], w_gate=t["w_gate"], ape=t["ape"], ratio=self.ratio,
+            positions=t["row_pos"], row_req=t["row_req"], block_table=t["cmp_table"], out="bf16",
+            cmp_pool=t["cmp_pool"], status=self.status, workspace=self._ws("cm"), stream=stream)
+        self.ws["ci"] = B.csa_compress(
+            x=t["idx_raw"], kv=t["idx_raw"], w_gate=t["w_gate_i"], ape=t["ape_i"],
+            ratio=self.ratio, positions=t["row_pos"], row_req=t["row_req"],
+            block_table=t["cmp_table"], out="int8", idx_pool=t["idx_pool"],
+            idx_scale_pool=t["idx_scale"], rotate=True, rope_cos=t["rope_cos"],
+            rope_sin=t["rope_sin"], status=self.status, workspace=self._ws("ci"), stream=stream)
+
+    def index(self, stream=None, scores=None):
+        t = self.t
+        self.ws["ix"] = B.csa_index_topk(
+            q_idx=t["q_idx"], weights=t["idx_w"], row_req=t["row_req"], row_pos=t["row_pos"],
+            n_cmp=t["n_cmp"], ratio=self.ratio, idx_pool=t["idx_pool"],
+            idx_scale_pool=t["idx_scale"], cmp_block_table=t["cmp_table"], topk=self.topk,
+            topk_idx=self.topk_idx, topk_score=self.topk_score, scores=scores,
+            rope_cos=t["rope_cos"], rope_sin=t["rope_sin"],
+            mode=B.CSA_MODE_PREFILL if self.prefill else B.CSA_MODE_DECODE, status=self.status,
+            workspace=self._ws("ix"), stream=stream)
+
+    def attention(self, stream=None, topk_idx=None):
+        t = self.t
+        fn = B.csa_sparse_attn_prefill if self.prefill else B.csa_sparse_attn_decode
+        self.ws["at"] = fn(
+            q=t["q"], row_req=t["row_req"], row_pos=t["row_pos"],
+            topk_idx=self.topk_idx if topk_idx is None else topk_idx, kv_pool=t["kv_pool"],
+            kv_block_table=t["kv_table"], kv_len=t["kv_len"], cmp_pool=t["cmp_pool"],
+            cmp_block_table=t["cmp_table"], n_cmp=t["n_cmp"], ratio=self.ratio, out=self.out,
+            lse=self.lse, sink=t["sink"], rope_cos=t["rope_cos"], rope_sin=t["rope_sin"],
+            status=self.status, workspace=self._ws("at"), stream=stream)
+
+    def prepare(self):
+        """Marshal the step's calls once (buffers must stay in place)."""
+        t = self.t
+        calls = []
+        if self.do_compress:
+            calls.append(B.csa_compress(
+                x=t["kv_raw"], kv=t["kv_raw"], w_gate=t["w_gate"], ape=t["ape"],
+                ratio=self.ratio, positions=t["row_pos"], row_req=t["row_req"],
+                block_table=t["cmp_table"], out="bf16", cmp_pool=t["cmp_pool"],
+                status=self.status, prepare=True))
+            calls.append(B.csa_compress(
+                x=t["idx_raw"], kv=t["idx_raw"], w_gate=t["w_gate_i"], ape=t["ape_i"],
+                ratio=self.ratio, positions=t["row_pos"], row_req=t["row_req"],
+                block_table=t["cmp_table"], out="int8", idx_pool=t["idx_pool"],
+                idx_scale_pool=t["idx_scale"], rotate=True, rope_cos=t["rope_cos"],
+                rope_sin=t["rope_sin"], status=self.status, prepare=True))
+        calls.append(B.csa_index_topk(
+            q_idx=t["q_idx"], weights=t["idx_w"], row_req=t["row_req"], row_pos=t["row_pos"],
+            n_cmp=t["n_cmp"], ratio=self.ratio, idx_pool=t["idx_pool"],
+            idx_scale_pool=t["idx_scale"], cmp_block_table=t["cmp_table"], topk=self.topk,
+            topk_idx=self.topk_idx, topk_score=self.topk_score, rope_cos=t["rope_cos"],
+            rope_sin=t["rope_sin"],
+            mode=B.CSA_MODE_PREFILL if self.prefill else B.CSA_MODE_DECODE, status=self.status,
+            prepare=True))
+        fn = B.csa_sparse_attn_prefill if self.prefill else B.csa_sparse_attn_decode
+        calls.append(fn(
+            q=t["q"], row_req=t["row_req"], row_pos=t["row_pos"], topk_idx=self.topk_idx,
+            kv_pool=t["kv_pool"], kv_block_table=t["kv_table"], kv_len=t["kv_len"],
+            cmp_pool=t["cmp_pool"], cmp_block_table=t["cmp_table"], n_cmp=t["n_cmp"],
+            ratio=self.ratio, out=self.out, lse=self.lse, sink=t["sink"],
+            rope_cos=t["rope_cos"], rope_sin=t["rope_sin"], status=self.status, prepare=True))
+        self._prepared = calls
+        return self
+
+    def run(self, stream=None):
+        if self._prepared is not None:
+            for c in self._prepared:
+                c(stream)
+            return
+        if self.do_compress:
+            self.compress(stream)
+        self.index(stream)
+        self.attention(stream)

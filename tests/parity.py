@@ -1,0 +1,106 @@
+"""Comparison rules between the CUDA path and the oracle.
+
+Tolerances (stated once, used by every parity test):
+* BF16 outputs (attention out, compressed cmp_kv): max |err| <= 2e-2 and
+  mean |err| <= 2e-3 against the float64 oracle, plus the per-row bounds of
+  "DeepSeek V4.1 Flash" (tests/golden/row_tolerances.txt).
+* Indexer scores: |err| <= 1e-4 * |s|, or, where heads cancel,
+  |err| <= 1e-5 * scale_c * sum_h |w_h| * sum_d |q_hd * k_cd|.
+* Top-k: the selected set equals the oracle's wherever the oracle's k-th and
+  (k+1)-th scores are separated by more than their tolerances; otherwise
+  every selected entry must score within tolerance of every unselected one
+  (the Top-K acceptance rule of "DeepSeek V4.1 Flash": eligibility,
+  uniqueness, ascending positions, trailing -1, cutoff score quality).
+* INT8 codes: exact, except +-1 where y/scale lies within 1e-3 of a .5
+  boundary; scales within 1e-6 relative.
+* lse: within 2e-4 absolute.
+"""
+
+import numpy as np
+
+from golden.load import constants
+
+ROW = constants("row_tolerances.txt")
+BF16_MAX_ABS = 2e-2
+BF16_MEAN_ABS = 2e-3
+SCORE_REL = 1e-4
+SCORE_FLOOR = 1e-5
+LSE_ABS = 2e-4
+
+
+def check_bf16(got, ref, what="output"):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    err = np.abs(got - ref)
+    assert err.max() <= BF16_MAX_ABS, f"{what}: max abs err {err.max():.3e}"
+    assert err.mean() <= BF16_MEAN_ABS, f"{what}: mean abs err {err.mean():.3e}"
+    # per-row bounds (rows = all but the last axis)
+    g2 = got.reshape(-1, got.shape[-1])
+    r2 = ref.reshape(-1, ref.shape[-1])
+    rms_ref = np.sqrt(np.mean(r2 ** 2, axis=1))
+    rms_err = np.sqrt(np.mean((g2 - r2) ** 2, axis=1))
+    max_err = np.max(np.abs(g2 - r2), axis=1)
+    bad = rms_err > ROW["rms_abs"] + ROW["rms_rel"] * rms_ref
+    assert not bad.any(), f"{what}: {bad.sum()} rows over the RMS bound"
+    bad = max_err > ROW["max_abs"] + ROW["max_rel"] * rms_ref
+    assert not bad.any(), f"{what}: {bad.sum()} rows over the peak bound"
+    return float(err.max()), float(err.mean())
+
+
+def score_tolerance(q_rot, w, keys, scales):
+    """Per-entry score tolerance (see module docstring).  q_rot [H, Di] float64
+    (already rotated), w [H], keys [n, Di] float64, scales [n]."""
+    mag = np.abs(keys) @ np.abs(q_rot).T  # [n, H]: sum_d |q_hd k_cd|
+    floor = SCORE_FLOOR * scales * (mag @ np.abs(w))
+    return floor
+
+
+def check_scores(got, ref, floor):
+    got = np.asarray(got, np.float64)
+    tol = np.maximum(SCORE_REL * np.abs(ref), floor)
+    err = np.abs(got - ref)
+    bad = err > tol
+    assert not bad.any(), (f"{bad.sum()} scores out of tolerance; worst "
+                           f"{(err / np.maximum(tol, 1e-300)).max():.2f}x tol")
+    return tol
+
+
+def check_topk(sel, ref_scores, tol, k):
+    """GPU selection `sel` (length k, ascending, -1 padded) against the oracle's
+    float64 scores of the visible entries."""
+    sel = np.asarray(sel, np.int64)
+    V = len(ref_scores)
+    n = min(k, V)
+    chosen = sel[:n]
+    assert np.all(sel[n:] == -1), "padding must be -1"
+    assert np.all(chosen >= 0) and np.all(chosen < V), "eligibility"
+    assert np.all(np.diff(chosen) > 0), "ascending and unique"
+    if V <= k:
+        assert np.array_equal(chosen, np.arange(V))
+        return True
+    mask = np.zeros(V, bool)
+    mask[chosen] = True
+    lo_in = np.min(ref_scores[mask] + tol[mask])
+    hi_out = np.max(ref_scores[~mask] - tol[~mask])
+    assert lo_in >= hi_out, "cutoff score quality: an unselected entry clearly beats a selected one"
+    # exact set where the oracle's boundary is clear
+    order = np.argsort(-ref_scores, kind="stable")
+    kth, k1 = order[k - 1], order[k]
+    clear = (ref_scores[kth] - tol[kth]) > (ref_scores[k1] + tol[k1])
+    if clear:
+        assert np.array_equal(np.sort(order[:k]), chosen), "set differs at a clear boundary"
+    return clear
+
+
+def check_int8(codes, scale, ref_codes, ref_scale, y_over_s=None):
+    codes = np.asarray(codes, np.int64)
+    ref_codes = np.asarray(ref_codes, np.int64)
+    assert abs(float(scale) - float(ref_scale)) <= 1e-6 * abs(float(ref_scale)), "scale"
+    diff = np.abs(codes - ref_codes)
+    assert diff.max() <= 1, "code off by more than one"
+    if y_over_s is not None and diff.max() == 1:
+        frac = np.abs(np.abs(np.asarray(y_over_s)) % 1.0 - 0.5)
+        assert np.all(frac[diff == 1] <= 1e-3), "code differs away from a .5 boundary"
+    return int((diff > 0).sum())

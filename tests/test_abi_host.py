@@ -1,0 +1,119 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+symbol ``include/csa.h`` declares, the ctypes structs match the C layout, and
+argument validation / workspace queries answer without touching the device."""
+
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "csa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from prefill_csa_compress_gb300 import build as B
+
+    B.build()
+    from prefill_csa_compress_gb300 import _binding
+
+    return _binding.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return re.findall(r"CSA_API\s+[\w\s\*]+?\b(csa_\w+)\s*\(", src)
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert {"csa_compress", "csa_index_topk", "csa_sparse_attn_decode",
+            "csa_sparse_attn_prefill"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in csa.h but not exported"
+
+
+def test_version_and_status_strings(L):
+    from prefill_csa_compress_gb300 import _binding as b
+
+    assert "sm_103a" in b.version()
+    assert b.status_string(0) == "ok"
+    assert b.status_string(2) == "unsupported shape"
+
+
+def _c_layout(struct, fields):
+    prog = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(){",
+            f'printf("%zu\\n", sizeof({struct}));']
+    prog += [f'printf("%zu\\n", offsetof({struct}, {f}));' for f in fields]
+    prog.append("return 0;}")
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "l.c")
+        exe = os.path.join(d, "l")
+        open(c, "w").write("\n".join(prog))
+        subprocess.check_call(["gcc", c, "-o", exe])
+        return [int(x) for x in subprocess.check_output([exe]).split()]
+
+
+@pytest.mark.parametrize("cname,pyname", [("csa_compress_args", "CompressArgs"),
+                                          ("csa_index_args", "IndexArgs"),
+                                          ("csa_attn_args", "AttnArgs")])
+def test_ctypes_layout_matches_c(cname, pyname):
+    from prefill_csa_compress_gb300 import _binding as b
+
+    S = getattr(b, pyname)
+    fields = [f for f, _ in S._fields_]
+    got = _c_layout(cname, fields)
+    assert got[0] == ctypes.sizeof(S)
+    for f, off in zip(fields, got[1:]):
+        assert getattr(S, f).offset == off, f
+
+
+def _compress_args(b, **kw):
+    a = b.CompressArgs()
+    a.struct_size = ctypes.sizeof(a)
+    a.n_rows, a.ratio, a.dx, a.d = 8192, 4, 512, 512
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_workspace_queries_and_validation(L):
+    from prefill_csa_compress_gb300 import _binding as b
+
+    a = _compress_args(b)
+    assert L.csa_compress(ctypes.byref(a), None) == b.CSA_OK
+    assert a.workspace_bytes == 8192 * 512 * 4
+    assert L.csa_compress(ctypes.byref(_compress_args(b, ratio=3)), None) == b.CSA_ERR_UNSUPPORTED
+    assert L.csa_compress(ctypes.byref(_compress_args(b, d=256)), None) == b.CSA_ERR_UNSUPPORTED
+    bad = _compress_args(b)
+    bad.struct_size = 8
+    assert L.csa_compress(ctypes.byref(bad), None) == b.CSA_ERR_INVALID_ARG
+    # a real workspace but no tensors: rejected on the host before any launch
+    dummy = ctypes.create_string_buffer(256)
+    a = _compress_args(b, n_rows=1, workspace=ctypes.addressof(dummy), workspace_bytes=256)
+    assert L.csa_compress(ctypes.byref(a), None) == b.CSA_ERR_INVALID_ARG
+    assert L.csa_compress(None, None) == b.CSA_ERR_INVALID_ARG
+
+    ia = b.IndexArgs()
+    ia.struct_size = ctypes.sizeof(ia)
+    ia.n_rows, ia.n_heads, ia.head_dim, ia.ratio, ia.topk, ia.max_blocks = 8, 64, 128, 4, 2048, 2048
+    assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_OK
+    assert ia.workspace_bytes == 8 * 2048 * 128 * 4
+    ia.topk = 4096
+    assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_ERR_INVALID_ARG
+    ia.topk, ia.n_heads = 512, 32
+    assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_ERR_UNSUPPORTED
+
+    aa = b.AttnArgs()
+    aa.struct_size = ctypes.sizeof(aa)
+    aa.n_rows, aa.n_heads, aa.head_dim, aa.ratio, aa.topk, aa.window = 8, 64, 512, 4, 2048, 128
+    assert L.csa_sparse_attn_decode(ctypes.byref(aa), None) == b.CSA_OK
+    assert aa.workspace_bytes > 0
+    assert L.csa_sparse_attn_prefill(ctypes.byref(aa), None) == b.CSA_OK
+    assert aa.workspace_bytes == 0
+    aa.window = 64
+    assert L.csa_sparse_attn_decode(ctypes.byref(aa), None) == b.CSA_ERR_UNSUPPORTED

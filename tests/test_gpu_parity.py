@@ -1,0 +1,267 @@
+"""CUDA path vs the float64 oracle, element by element, through the C ABI.
+
+Small cases span several tiles and ragged tails; the full-size workloads are
+checked on sampled rows the oracle computes one by one.  Tolerances are in
+``tests/parity.py``.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from oracle import step as OS
+from parity import (LSE_ABS, check_bf16, check_int8, check_scores, check_topk,
+                    score_tolerance)
+from workloads import BLOCK, make_workload, random_selection, spec_for
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import prefill_csa_compress_gb300 as csa  # noqa: E402
+from prefill_csa_compress_gb300.pipeline import CsaStep  # noqa: E402
+
+DEV = torch.device("cuda:0")
+
+
+_CACHE = {}
+
+
+def _load(spec):
+    key = repr(spec)
+    if key not in _CACHE:
+        if len(_CACHE) > 2:
+            _CACHE.clear()
+        _CACHE[key] = make_workload(spec)
+    wl = _CACHE[key]
+    return wl, wl.to(DEV)
+
+
+def _status(step):
+    return int(step.status.item()) if step.status is not None else 0
+
+
+def _rope_q(t, row, key="q_idx"):
+    p = int(t["row_pos"][row])
+    return O.rope_rotate(t[key][row], p, t["rope_cos"], t["rope_sin"])
+
+
+# ------------------------------------------------------------------ compressor
+
+
+@pytest.mark.parametrize("name,over", [
+    ("chunked_prefill", dict(ctx=[1000], chunk=[1000], seed=31)),       # ragged: 250 groups
+    ("chunked_prefill", dict(ctx=[1030, 70], chunk=[1030, 70], ratio=2, seed=32, pad_rows=3)),
+    ("chunked_prefill", dict(ctx=[300], chunk=[300], ratio=1, seed=33)),
+    ("serving_decode", {}),
+    ("chunked_prefill", {}),                                            # full 8192-token chunk
+])
+def test_compress_parity(name, over):
+    spec = spec_for(name, **over)
+    wl, t = _load(spec)
+    step = CsaStep(t, spec.ratio, spec.topk, prefill=spec.mode == "prefill")
+    step.compress()
+    torch.cuda.synchronize()
+    assert _status(step) == 0
+    pools, main, idx = OS.compress_step(wl.t, spec)
+    table = wl.cmp_table.numpy()
+    got_cmp = t["cmp_pool"].cpu()
+    got_idx = t["idx_pool"].cpu()
+    got_sc = t["idx_scale"].cpu()
+    assert len(main) == len(idx) > 0 or spec.name == "serving_decode"
+    g_rows, r_rows = [], []
+    n_diff = 0
+    for (b, g, vals), (_, _, codes, scale) in zip(main, idx):
+        pg, row = int(table[b, g // BLOCK]), g % BLOCK
+        g_rows.append(got_cmp[pg, row].double().numpy())
+        r_rows.append(vals)
+        n_diff += check_int8(got_idx[pg, row].numpy(), got_sc[pg, row].item(), codes,
+                             np.float32(scale))
+    check_bf16(np.stack(g_rows), np.stack(r_rows), "cmp_kv")
+    # INT8 codes may differ only at exact rounding boundaries: rare
+    assert n_diff <= max(2, len(idx) // 20)
+    # entries not written by this step are untouched
+    written = {(b, g) for b, g, _ in main}
+    ref_pool = wl.cmp_pool
+    for b in range(spec.n_req):
+        for g in range(0, int(wl.n_cmp[b]), 97):
+            if (b, g) not in written:
+                pg = int(table[b, g // BLOCK])
+                assert torch.equal(got_cmp[pg, g % BLOCK], ref_pool[pg, g % BLOCK])
+
+
+# ------------------------------------------------------------------ indexer
+
+
+def _check_index_rows(wl, t, spec, step, rows, scores_dev):
+    torch.cuda.synchronize()
+    assert _status(step) == 0
+    pools = {"cmp_pool": wl.cmp_pool, "idx_pool": wl.idx_pool, "idx_scale": wl.idx_scale}
+    sel = step.topk_idx.cpu().numpy()
+    sc_all = scores_dev.cpu().numpy() if scores_dev is not None else None
+    n_clear = 0
+    for row in rows:
+        b = int(wl.row_req[row])
+        if b < 0:
+            assert np.all(sel[row] == -1)  # untouched padding row (initialised to -1)
+            continue
+        ref = OS.index_row(wl.t, spec, pools, row)
+        V = len(ref)
+        keys = O.page_rows(wl.idx_pool, wl.cmp_table[b].numpy(), range(V))
+        scl = O.page_rows(wl.idx_scale, wl.cmp_table[b].numpy(), range(V))
+        floor = score_tolerance(_rope_q(wl.t, row), O.as_f64(wl.idx_w[row]), keys, scl)
+        if sc_all is not None:
+            tol = check_scores(sc_all[row, :V], ref, floor)
+        else:
+            tol = np.maximum(1e-4 * np.abs(ref), floor)
+        n_clear += check_topk(sel[row], ref, tol, spec.topk)
+        # scores reported for the selection match the oracle's
+        chosen = sel[row][sel[row] >= 0]
+        ts = step.topk_score.cpu().numpy()[row][:len(chosen)]
+        assert np.all(np.abs(ts - ref[chosen]) <= np.maximum(1e-4 * np.abs(ref[chosen]),
+                                                             floor[chosen]))
+    return n_clear
+
+
+@pytest.mark.parametrize("name,over", [
+    ("tiny_decode", {}),
+    ("serving_decode", {}),
+    ("serving_decode", dict(ctx=[300, 5, 129, 2000], chunk=[3, 1, 2, 40], topk=64, seed=41,
+                            pad_rows=2)),
+    ("chunked_prefill", dict(ctx=[700], chunk=[700], cmp_init="random", topk=40, seed=42)),
+    ("ratio1_decode", dict(ctx=[3000, 2500], chunk=[2, 2], topk=1024, seed=43)),
+])
+def test_index_topk_parity(name, over):
+    spec = spec_for(name, **over)
+    wl, t = _load(spec)
+    step = CsaStep(t, spec.ratio, spec.topk, prefill=spec.mode == "prefill", compress=False)
+    n_cap = t["cmp_table"].shape[1] * BLOCK
+    scores = torch.full((spec.n_rows, n_cap), float("nan"), device=DEV)
+    step.index(scores=scores)
+    _check_index_rows(wl, t, spec, step, range(spec.n_rows), scores)
+
+
+@pytest.mark.parametrize("name", ["ratio1_decode", "million_decode"])
+def test_index_topk_full_size_sampled(name):
+    spec = spec_for(name)
+    wl, t = _load(spec)
+    step = CsaStep(t, spec.ratio, spec.topk, compress=False)
+    n_cap = t["cmp_table"].shape[1] * BLOCK
+    scores = torch.empty((spec.n_rows, n_cap), device=DEV)
+    step.index(scores=scores)
+    _check_index_rows(wl, t, spec, step, [0, 5], scores)
+    # the workspace path (no caller score buffer) selects the same entries
+    sel_a = step.topk_idx.clone()
+    step.index()
+    torch.cuda.synchronize()
+    assert torch.equal(sel_a, step.topk_idx)
+
+
+def test_index_topk_prefill_full_size_sampled():
+    spec = spec_for("chunked_prefill", cmp_init="random")
+    wl, t = _load(spec)
+    step = CsaStep(t, spec.ratio, spec.topk, prefill=True, compress=False)
+    n_cap = t["cmp_table"].shape[1] * BLOCK
+    scores = torch.empty((spec.n_rows, n_cap), device=DEV)
+    step.index(scores=scores)
+    _check_index_rows(wl, t, spec, step, [0, 3, 2046, 2047, 2048, 4095, 8191], scores)
+
+
+# ------------------------------------------------------------------ attention
+
+
+def _attn_case(spec, sel_seed, prefill, rows=None, use_sink=True):
+    wl, t = _load(spec)
+    limits = [O.visible_count(int(wl.row_pos[i]), spec.ratio, int(wl.n_cmp[int(wl.row_req[i])]))
+              if int(wl.row_req[i]) >= 0 else 0 for i in range(spec.n_rows)]
+    sel = random_selection(limits, spec.topk, sel_seed)
+    step = CsaStep(t, spec.ratio, spec.topk, prefill=prefill, compress=False)
+    if not use_sink:
+        t["sink"] = None
+    step.attention(topk_idx=sel.to(DEV))
+    torch.cuda.synchronize()
+    assert _status(step) == 0
+    out = step.out.cpu().double().numpy()
+    lse = step.lse.cpu().numpy()
+    pools = {"cmp_pool": wl.cmp_pool}
+    rows = range(spec.n_rows) if rows is None else rows
+    g, r, gl, rl = [], [], [], []
+    for row in rows:
+        if int(wl.row_req[row]) < 0:
+            assert np.all(out[row] == 0)  # padding rows untouched (zero-initialised)
+            continue
+        o_ref, l_ref = OS.attention_row(wl.t, spec, pools, row, sel[row].numpy(),
+                                        use_sink=use_sink)
+        g.append(out[row])
+        r.append(o_ref)
+        gl.append(lse[row])
+        rl.append(l_ref)
+    check_bf16(np.stack(g), np.stack(r), "attention out")
+    assert np.max(np.abs(np.stack(gl) - np.stack(rl))) <= LSE_ABS
+
+
+@pytest.mark.parametrize("prefill", [False, True])
+@pytest.mark.parametrize("name,over", [
+    ("tiny_decode", {}),
+    ("serving_decode", {}),
+    ("serving_decode", dict(ctx=[130, 5, 129, 3000], chunk=[3, 5, 2, 7], topk=100, seed=51,
+                            pad_rows=2)),
+    ("chunked_prefill", dict(ctx=[300], chunk=[300], cmp_init="random", topk=48, seed=52)),
+])
+def test_attention_parity(name, over, prefill):
+    spec = spec_for(name, **over)
+    _attn_case(spec, 7, prefill)
+
+
+def test_attention_without_sink():
+    _attn_case(spec_for("serving_decode", topk=64, seed=53), 8, False, use_sink=False)
+
+
+@pytest.mark.parametrize("name", ["ratio1_decode", "million_decode"])
+def test_attention_decode_full_size(name):
+    _attn_case(spec_for(name), 9, False)
+
+
+def test_attention_prefill_full_size_sampled():
+    spec = spec_for("chunked_prefill", cmp_init="random")
+    _attn_case(spec, 10, True, rows=[0, 1, 127, 128, 2047, 4000, 8191])
+
+
+# ------------------------------------------------------------------ whole step
+
+
+@pytest.mark.parametrize("name", ["tiny_decode", "serving_decode"])
+def test_decode_step_chain(name):
+    """compress -> index -> attention on the GPU, against the oracle's own chain."""
+    spec = spec_for(name)
+    wl, t = _load(spec)
+    step = CsaStep(t, spec.ratio, spec.topk)
+    step.run()
+    torch.cuda.synchronize()
+    assert _status(step) == 0
+    pools, res = OS.full_step(wl.t, spec)
+    sel = step.topk_idx.cpu().numpy()
+    out = step.out.cpu().double().numpy()
+    gpu_idx = t["idx_pool"].cpu()
+    same = 0
+    for row, rr in res.items():
+        b = int(wl.row_req[row])
+        V = len(rr["scores"])
+        table = wl.cmp_table[b].numpy()
+        keys = O.page_rows(pools["idx_pool"], table, range(V))
+        scl = O.page_rows(pools["idx_scale"], table, range(V))
+        q_rot = _rope_q(wl.t, row)
+        w = O.as_f64(wl.idx_w[row])
+        floor = score_tolerance(q_rot, w, keys, scl)
+        # where the GPU's quantiser rounded a code the other way at a .5 boundary,
+        # the score may move by at most scale * sum_h |w_h| * sum_d |q_hd| |dcode_d|
+        dcode = np.abs(O.page_rows(gpu_idx, table, range(V)) - keys)
+        extra = scl * ((dcode @ np.abs(q_rot).T) @ np.abs(w)) * 1.001
+        tol = np.maximum(1e-4 * np.abs(rr["scores"]), floor) + extra
+        check_topk(sel[row], rr["scores"], tol, spec.topk)
+        if np.array_equal(sel[row], rr["topk"]):
+            same += 1
+            check_bf16(out[row], rr["out"], f"row {row} out")
+    assert same >= len(res) // 2

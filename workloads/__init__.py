@@ -26,6 +26,7 @@ from .gen import (  # noqa: F401
     Workload,
     WorkloadSpec,
     make_workload,
+    random_selection,
     rope_tables,
     spec_for,
 )

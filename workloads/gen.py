@@ -224,3 +224,18 @@ def make_workload(spec: WorkloadSpec) -> Workload:
         rope_sin=rope_sin,
     )
     return Workload(spec=spec, t=t)
+
+
+def random_selection(limits, k, seed):
+    """Seeded selections for feeding the attention call directly: for row t,
+    min(k, limits[t]) distinct integers drawn uniformly from [0, limits[t]),
+    in ascending order, padded with -1 (an input, not a computed top-k)."""
+    rng = np.random.default_rng(seed)
+    out = np.full((len(limits), k), -1, dtype=np.int32)
+    for t, lim in enumerate(limits):
+        lim = int(lim)
+        if lim <= 0:
+            continue
+        m = min(k, lim)
+        out[t, :m] = np.sort(rng.choice(lim, size=m, replace=False))
+    return torch.from_numpy(out)
