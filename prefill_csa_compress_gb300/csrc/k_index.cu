@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(1024) index_topk_kernel(csa_index_args a,
     const int sel = gt | (eq && eq_rank < remaining);
     int sel_total;
     const int pos = sel_base + block_exclusive_scan(sel, warp_sums, &sel_total);
-    if (sel) {
+    if (sel && pos < k) {
       out[pos] = c;
       if (out_s) out_s[pos] = sc[c];
     }
