@@ -191,7 +191,8 @@ CSA_API csa_status_t csa_index_topk(csa_index_args *a, csa_stream_t stream) {
   if (a->n_req <= 0 || a->n_blocks <= 0) return CSA_ERR_INVALID_ARG;
   if ((a->rope_cos == nullptr) != (a->rope_sin == nullptr)) return CSA_ERR_INVALID_ARG;
   if (a->rope_cos && a->rope_cap <= 0) return CSA_ERR_INVALID_ARG;
-  if (!aligned16(a->idx_pool) || !aligned16(a->q_idx)) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(a->idx_pool) || !aligned16(a->q_idx) || !aligned16(a->idx_scale_pool))
+    return CSA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float *scores = own_scores ? a->scores : static_cast<float *>(a->workspace);
   const int cols = own_scores ? a->score_cols : n_cap;

@@ -1,4 +1,4 @@
-// Lightning-indexer scores over INT8 index keys and the deterministic top-k.
+// Deterministic top-k over the lightning-indexer scores.
 //
 // Source: "Hyper-Parallel ... DeepSeek V4 CP" (gitcode issue #2), "10. ratio=4
 // Global Top-k" and "10.3 Causal mask"; "DeepSeek V4.1 Flash", "Compressor
@@ -8,83 +8,6 @@
 
 namespace csa {
 namespace {
-
-constexpr int SC_KEYS = 128;  // keys per CTA, one per thread
-
-// score[t, c] = scale_c * sum_h w[t,h] * act(q_h . k_c) for the CTA's 128 keys.
-__global__ void __launch_bounds__(SC_KEYS) index_score_kernel(csa_index_args a,
-                                                              float *__restrict__ scores,
-                                                              int score_cols) {
-  __shared__ float qs[kHeads][kIdxDim];
-  __shared__ float ws[kHeads];
-  const int t = blockIdx.y;
-  const int b = a.row_req[t];
-  if (b < 0) return;
-  if (b >= a.n_req) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
-    return;
-  }
-  const int p = a.row_pos[t];
-  int V = visible_count(p, a.ratio, a.n_cmp[b]);
-  if (V > a.max_blocks * kBlock) {  // more entries than the block table can address
-    V = a.max_blocks * kBlock;
-    if (threadIdx.x == 0 && blockIdx.x == 0) flag(a.status_dev, CSA_DEV_BAD_BLOCK);
-  }
-  const int c0 = blockIdx.x * SC_KEYS;
-  if (c0 >= V) return;
-
-  // query rows, rotated at p in FP32
-  const uint16_t *q = static_cast<const uint16_t *>(a.q_idx) + (long long)t * kHeads * kIdxDim;
-  bool rot = a.rope_cos != nullptr && p >= 0;
-  if (rot && p >= a.rope_cap) {
-    rot = false;
-    if (threadIdx.x == 0 && blockIdx.x == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
-  }
-  for (int e = threadIdx.x; e < kHeads * kIdxDim / 2; e += blockDim.x) {
-    const int h = e / (kIdxDim / 2), i2 = e % (kIdxDim / 2);
-    float x0 = bf16_bits_to_float(q[h * kIdxDim + 2 * i2]);
-    float x1 = bf16_bits_to_float(q[h * kIdxDim + 2 * i2 + 1]);
-    if (rot && 2 * i2 >= kIdxDim - kRopeDim) {
-      const int i = i2 - (kIdxDim - kRopeDim) / 2;
-      const float c = a.rope_cos[(long long)p * kRopeHalf + i];
-      const float s = a.rope_sin[(long long)p * kRopeHalf + i];
-      const float y0 = x0 * c - x1 * s, y1 = x0 * s + x1 * c;
-      x0 = y0;
-      x1 = y1;
-    }
-    qs[h][2 * i2] = x0;
-    qs[h][2 * i2 + 1] = x1;
-  }
-  if (threadIdx.x < kHeads) ws[threadIdx.x] = a.weights[(long long)t * kHeads + threadIdx.x];
-  __syncthreads();
-
-  const int c = c0 + threadIdx.x;
-  if (c >= V) return;
-  const long long row =
-      page_row(a.cmp_block_table, a.max_blocks, a.n_blocks, b, c, a.status_dev);
-  float score = -INFINITY;
-  if (row >= 0) {
-    float k[kIdxDim];
-    const int4 *src = reinterpret_cast<const int4 *>(a.idx_pool + row * kIdxDim);
-#pragma unroll
-    for (int v = 0; v < kIdxDim / 16; ++v) {
-      int4 w4 = src[v];
-      const int8_t *bytes = reinterpret_cast<const int8_t *>(&w4);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) k[v * 16 + j] = (float)bytes[j];
-    }
-    float acc = 0.f;
-    for (int h = 0; h < kHeads; ++h) {
-      float dot = 0.f;
-#pragma unroll
-      for (int d = 0; d < kIdxDim; ++d) dot = fmaf(qs[h][d], k[d], dot);
-      if (a.relu) dot = fmaxf(dot, 0.f);
-      acc = fmaf(ws[h], dot, acc);
-    }
-    score = a.idx_scale_pool[row] * acc;
-  }
-  scores[(long long)t * score_cols + c] = score;
-}
 
 // Order-preserving 32-bit key of a float score: larger score -> larger key.
 // +0 and -0 share a key; NaN maps to the smallest key.
@@ -199,17 +122,6 @@ __global__ void __launch_bounds__(1024) index_topk_kernel(csa_index_args a,
 }
 
 }  // namespace
-
-cudaError_t launch_index_scores(const csa_index_args &a, float *scores, int score_cols,
-                                cudaStream_t s) {
-  if (a.n_rows <= 0) return cudaSuccess;
-  const int n_cap = a.max_blocks * kBlock;
-  dim3 grid((n_cap + SC_KEYS - 1) / SC_KEYS, a.n_rows);
-  launch_begin(CSA_K_INDEX_SCORE, s);
-  index_score_kernel<<<grid, SC_KEYS, 0, s>>>(a, scores, score_cols);
-  launch_end(CSA_K_INDEX_SCORE, s);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_index_topk(const csa_index_args &a, const float *scores, int score_cols,
                               cudaStream_t s) {
