@@ -50,9 +50,10 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 csa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
 
-// ---- decode split-K geometry: fill about two waves of the 152 SMs
-constexpr int kAttnTile = 32;
-constexpr int kTargetCtas = 2 * 152;
+// ---- decode split-K geometry: one 128-candidate tile per CTA while the grid
+// fits in about two waves of the GPU; beyond that, tiles are grouped per CTA.
+constexpr int kAttnTile = 128;
+constexpr long long kTargetCtas = 2 * 148;
 
 void attn_geometry(const csa_attn_args &a, bool decode, int *n_splits, int *tiles_per_split) {
   const int n_cand = a.topk + a.window;
@@ -62,17 +63,18 @@ void attn_geometry(const csa_attn_args &a, bool decode, int *n_splits, int *tile
     *tiles_per_split = tiles;
     return;
   }
-  int want = (kTargetCtas + a.n_rows - 1) / a.n_rows;
-  if (want < 1) want = 1;
-  if (want > tiles) want = tiles;
-  const int tps = (tiles + want - 1) / want;
+  const long long work = (long long)a.n_rows * tiles;
+  int tps = (int)((work + kTargetCtas - 1) / kTargetCtas);
+  if (tps < 1) tps = 1;
+  if (tps > tiles) tps = tiles;
   *tiles_per_split = tps;
   *n_splits = (tiles + tps - 1) / tps;
 }
 
 size_t attn_partial_bytes(const csa_attn_args &a, int n_splits) {
   if (n_splits <= 1) return 0;
-  return align_up((size_t)a.n_rows * n_splits * kHeads * (kHeadDim + 2) * sizeof(float), kAlign);
+  return align_up((size_t)a.n_rows * n_splits * (kHeads * kHeadDim + 2 * kHeads) * sizeof(float),
+                  kAlign);
 }
 
 // shape checks (enough to size the workspace)

@@ -13,7 +13,11 @@ Tolerances (stated once, used by every parity test):
   uniqueness, ascending positions, trailing -1, cutoff score quality).
 * INT8 codes: exact, except +-1 where y/scale lies within 1e-3 of a .5
   boundary; scales within 1e-6 relative.
-* lse: within 2e-4 absolute.
+* lse: within 2e-3 absolute.  The tensor-core path feeds the query to the
+  MMA in BF16; its 448 unrotated channels are BF16 inputs already, the 64
+  rotated channels are rounded (relative error <= 2^-9).  A logit then moves
+  by about softmax_scale * 2^-9 * sqrt(64) * E|q| * E|k| ~ 4e-4 for N(0,1)
+  data; 2e-3 is five times that.  Denominators are summed in FP32.
 """
 
 import numpy as np
@@ -25,17 +29,19 @@ BF16_MAX_ABS = 2e-2
 BF16_MEAN_ABS = 2e-3
 SCORE_REL = 1e-4
 SCORE_FLOOR = 1e-5
-LSE_ABS = 2e-4
+LSE_ABS = 2e-3
 
 
-def check_bf16(got, ref, what="output"):
+def check_bf16(got, ref, what="output", magnitude=1.0):
+    """``magnitude`` scales the absolute bounds for outputs whose values are
+    larger than the O(1) outputs of the workloads (BF16 error is relative)."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     err = np.abs(got - ref)
-    assert err.max() <= BF16_MAX_ABS, f"{what}: max abs err {err.max():.3e}"
-    assert err.mean() <= BF16_MEAN_ABS, f"{what}: mean abs err {err.mean():.3e}"
+    assert err.max() <= BF16_MAX_ABS * magnitude, f"{what}: max abs err {err.max():.3e}"
+    assert err.mean() <= BF16_MEAN_ABS * magnitude, f"{what}: mean abs err {err.mean():.3e}"
     # per-row bounds (rows = all but the last axis)
     g2 = got.reshape(-1, got.shape[-1])
     r2 = ref.reshape(-1, ref.shape[-1])

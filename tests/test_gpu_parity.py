@@ -172,15 +172,36 @@ def test_index_topk_prefill_full_size_sampled():
 # ------------------------------------------------------------------ attention
 
 
-def _attn_case(spec, sel_seed, prefill, rows=None, use_sink=True):
-    wl, t = _load(spec)
+def _attn_case(spec, sel_seed, prefill, rows=None, use_sink=True, inv_rope_out=False,
+               softmax_scale=None, shrink_first=0):
+    if shrink_first:
+        # a fresh workload whose first `shrink_first` compressed entries are
+        # scaled down 16x: the first candidate tile then has far smaller logits
+        # than the later ones and the running maximum must move
+        wl = make_workload(spec)
+        for b in range(spec.n_req):
+            for c in range(shrink_first):
+                pg = int(wl.cmp_table[b, c // BLOCK])
+                wl.cmp_pool[pg, c % BLOCK] = (wl.cmp_pool[pg, c % BLOCK].float() / 16).bfloat16()
+        t = wl.to(DEV)
+    else:
+        wl, t = _load(spec)
     limits = [O.visible_count(int(wl.row_pos[i]), spec.ratio, int(wl.n_cmp[int(wl.row_req[i])]))
               if int(wl.row_req[i]) >= 0 else 0 for i in range(spec.n_rows)]
     sel = random_selection(limits, spec.topk, sel_seed)
     step = CsaStep(t, spec.ratio, spec.topk, prefill=prefill, compress=False)
     if not use_sink:
         t["sink"] = None
-    step.attention(topk_idx=sel.to(DEV))
+    if inv_rope_out or softmax_scale is not None:
+        fn = csa.csa_sparse_attn_prefill if prefill else csa.csa_sparse_attn_decode
+        fn(q=t["q"], row_req=t["row_req"], row_pos=t["row_pos"], topk_idx=sel.to(DEV),
+           kv_pool=t["kv_pool"], kv_block_table=t["kv_table"], kv_len=t["kv_len"],
+           cmp_pool=t["cmp_pool"], cmp_block_table=t["cmp_table"], n_cmp=t["n_cmp"],
+           ratio=spec.ratio, out=step.out, lse=step.lse, sink=t["sink"],
+           softmax_scale=softmax_scale, rope_cos=t["rope_cos"], rope_sin=t["rope_sin"],
+           inv_rope_out=inv_rope_out, status=step.status)
+    else:
+        step.attention(topk_idx=sel.to(DEV))
     torch.cuda.synchronize()
     assert _status(step) == 0
     out = step.out.cpu().double().numpy()
@@ -192,14 +213,23 @@ def _attn_case(spec, sel_seed, prefill, rows=None, use_sink=True):
         if int(wl.row_req[row]) < 0:
             assert np.all(out[row] == 0)  # padding rows untouched (zero-initialised)
             continue
-        o_ref, l_ref = OS.attention_row(wl.t, spec, pools, row, sel[row].numpy(),
-                                        use_sink=use_sink)
+        if softmax_scale is None:
+            o_ref, l_ref = OS.attention_row(wl.t, spec, pools, row, sel[row].numpy(),
+                                            use_sink=use_sink, inv_rope_out=inv_rope_out)
+        else:
+            b = int(wl.row_req[row])
+            o_ref, l_ref = O.sparse_attention(
+                wl.q[row], int(wl.row_pos[row]), sel[row].numpy(), wl.kv_pool,
+                wl.kv_table[b].numpy(), wl.cmp_pool, wl.cmp_table[b].numpy(),
+                wl.sink if use_sink else None, softmax_scale, window=spec.window,
+                rope_cos=wl.rope_cos, rope_sin=wl.rope_sin, inv_rope_out=inv_rope_out)
         g.append(out[row])
         r.append(o_ref)
         gl.append(lse[row])
         rl.append(l_ref)
-    check_bf16(np.stack(g), np.stack(r), "attention out")
-    assert np.max(np.abs(np.stack(gl) - np.stack(rl))) <= LSE_ABS
+    mag = max(1.0, float(np.max(np.abs(np.stack(r)))) / 2)
+    check_bf16(np.stack(g), np.stack(r), "attention out", magnitude=mag)
+    assert np.max(np.abs(np.stack(gl) - np.stack(rl))) <= LSE_ABS * max(1.0, np.max(np.abs(rl)))
 
 
 @pytest.mark.parametrize("prefill", [False, True])
@@ -213,6 +243,18 @@ def _attn_case(spec, sel_seed, prefill, rows=None, use_sink=True):
 def test_attention_parity(name, over, prefill):
     spec = spec_for(name, **over)
     _attn_case(spec, 7, prefill)
+
+
+@pytest.mark.parametrize("prefill", [False, True])
+def test_attention_inverse_rope_output(prefill):
+    _attn_case(spec_for("serving_decode", topk=200, seed=54), 11, prefill, inv_rope_out=True)
+
+
+@pytest.mark.parametrize("prefill", [False, True])
+def test_attention_large_logits_move_the_running_max(prefill):
+    # logits with a spread of hundreds: the running maximum must move between tiles
+    _attn_case(spec_for("chunked_prefill", ctx=[2400], chunk=[5], cmp_init="random", topk=512,
+                        seed=55), 12, prefill, softmax_scale=0.15, shrink_first=200)
 
 
 def test_attention_without_sink():
