@@ -179,8 +179,9 @@ CSA_API csa_status_t csa_index_topk(csa_index_args *a, csa_stream_t stream) {
   const int n_cap = a->max_blocks * kBlock;
   const bool own_scores = a->scores != nullptr;
   if (own_scores && a->score_cols < n_cap) return CSA_ERR_INVALID_ARG;
-  const size_t need =
+  const size_t score_bytes =
       own_scores ? 0 : align_up((size_t)a->n_rows * n_cap * sizeof(float), kAlign);
+  const size_t need = score_bytes + topk_ws_bytes(a->n_rows, n_cap);
   if (!a->workspace) {
     a->workspace_bytes = need;
     return CSA_OK;
@@ -198,9 +199,11 @@ CSA_API csa_status_t csa_index_topk(csa_index_args *a, csa_stream_t stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float *scores = own_scores ? a->scores : static_cast<float *>(a->workspace);
   const int cols = own_scores ? a->score_cols : n_cap;
-  cudaError_t e = launch_index_scores(*a, scores, cols, s);
+  void *topk_ws = static_cast<uint8_t *>(a->workspace) + score_bytes;
+  cudaError_t e =
+      launch_index_scores(*a, scores, cols, topk_counters(topk_ws, a->n_rows, n_cap), s);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
-  return from_cuda(launch_index_topk(*a, scores, cols, s));
+  return from_cuda(launch_index_topk(*a, scores, cols, topk_ws, s));
 }
 
 // ---------------------------------------------------------------- attention

@@ -28,10 +28,15 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Launchers (one per kernel family); each returns cudaGetLastError().
 cudaError_t launch_compress(const csa_compress_args &a, float *logits, cudaStream_t s);
+// `zero_ctr` (n_rows words, may be null) is cleared by the scoring kernel for
+// the top-k kernel that follows it on the stream.
 cudaError_t launch_index_scores(const csa_index_args &a, float *scores, int score_cols,
-                                cudaStream_t s);
+                                uint32_t *zero_ctr, cudaStream_t s);
 cudaError_t launch_index_topk(const csa_index_args &a, const float *scores, int score_cols,
-                              cudaStream_t s);
+                              void *topk_ws, cudaStream_t s);
+bool topk_is_long(int n_cap);
+size_t topk_ws_bytes(int n_rows, int n_cap);
+uint32_t *topk_counters(void *ws, int n_rows, int n_cap);
 cudaError_t launch_attn(const csa_attn_args &a, int n_splits, int tiles_per_split,
                         float *partials, cudaStream_t s);
 

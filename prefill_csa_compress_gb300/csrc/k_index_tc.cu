@@ -92,7 +92,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 template <int G>
 __global__ void __launch_bounds__(IT_THREADS, 1)
     index_score_tc_kernel(csa_index_args a, float *__restrict__ scores, int cols, int n_groups,
-                          int chunk_tiles, int units_per_group) {
+                          int chunk_tiles, int units_per_group, uint32_t *zero_ctr) {
   using C = IdxTc<G>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   IdxMisc *M = reinterpret_cast<IdxMisc *>(sm + C::OFF_MISC);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  if (zero_ctr && blockIdx.x == 0)
+    for (int i = tid; i < a.n_rows; i += IT_THREADS) zero_ctr[i] = 0u;
   const bool rope = a.rope_cos != nullptr;
   const int n_kchunks = rope ? 3 : 2;
   const int n_cap = a.max_blocks * kBlock;
@@ -381,7 +383,8 @@ int sm_count() {
 }
 
 template <int G>
-cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, cudaStream_t s) {
+cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, uint32_t *zero_ctr,
+                      cudaStream_t s) {
   using C = IdxTc<G>;
   static bool attr[64] = {};
   int dev = 0;
@@ -403,7 +406,7 @@ cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, cudaStre
   const int grid = (int)(n_units < sms ? n_units : sms);
   launch_begin(CSA_K_INDEX_SCORE, s);
   index_score_tc_kernel<G><<<grid, IT_THREADS, C::SMEM, s>>>(a, scores, cols, n_groups, chunk,
-                                                             upg);
+                                                             upg, zero_ctr);
   launch_end(CSA_K_INDEX_SCORE, s);
   return cudaGetLastError();
 }
@@ -411,10 +414,11 @@ cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, cudaStre
 }  // namespace
 
 cudaError_t launch_index_scores(const csa_index_args &a, float *scores, int score_cols,
-                                cudaStream_t s) {
+                                uint32_t *zero_ctr, cudaStream_t s) {
   if (a.n_rows <= 0) return cudaSuccess;
   const bool wide = a.mode == CSA_MODE_PREFILL || (a.mode == CSA_MODE_AUTO && a.n_rows > 64);
-  return wide ? launch_tc<4>(a, scores, score_cols, s) : launch_tc<2>(a, scores, score_cols, s);
+  return wide ? launch_tc<4>(a, scores, score_cols, zero_ctr, s)
+              : launch_tc<2>(a, scores, score_cols, zero_ctr, s);
 }
 
 }  // namespace csa

@@ -102,7 +102,12 @@ def test_workspace_queries_and_validation(L):
     ia.struct_size = ctypes.sizeof(ia)
     ia.n_rows, ia.n_heads, ia.head_dim, ia.ratio, ia.topk, ia.max_blocks = 8, 64, 128, 4, 2048, 2048
     assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_OK
-    assert ia.workspace_bytes == 8 * 2048 * 128 * 4
+    # scores (8 rows x 262144 FP32) plus the multi-CTA top-k scratch
+    assert ia.workspace_bytes > 8 * 2048 * 128 * 4
+    ia.max_blocks = 16  # short rows: scores only
+    assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_OK
+    assert ia.workspace_bytes == 8 * 16 * 128 * 4
+    ia.max_blocks = 2048
     ia.topk = 4096
     assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_ERR_INVALID_ARG
     ia.topk, ia.n_heads = 512, 32
