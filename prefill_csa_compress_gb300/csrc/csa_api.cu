@@ -164,6 +164,7 @@ CSA_API csa_status_t csa_compress(csa_compress_args *a, csa_stream_t stream) {
   if (a->out_mode == CSA_OUT_INT8 && (!a->idx_pool || !a->idx_scale_pool))
     return CSA_ERR_INVALID_ARG;
   if (a->rotate && (!a->rope_cos || !a->rope_sin || a->rope_cap <= 0)) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(a->x) || !aligned16(a->kv) || !aligned16(a->w_gate)) return CSA_ERR_INVALID_ARG;
   return from_cuda(
       launch_compress(*a, static_cast<float *>(a->workspace), static_cast<cudaStream_t>(stream)));
 }

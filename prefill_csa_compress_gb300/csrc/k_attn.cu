@@ -189,10 +189,18 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     if (tid == 0 && split == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
   }
   const uint16_t *qg = static_cast<const uint16_t *>(a.q) + (long long)t * kHeads * kHeadDim;
+  // all 4096 16-byte pieces in flight at once, straight into the swizzled layout
   for (int e = tid; e < kHeads * (kHeadDim / 8); e += AT_THREADS) {
     const int h = e >> 6, u = e & 63, kc = u >> 3, jj = u & 7;
-    uint4 x = *reinterpret_cast<const uint4 *>(qg + h * kHeadDim + u * 8);
-    if (rot && u * 8 >= kHeadDim - kRopeDim) {
+    tc::cp_async16(Qs + kc * 8192 + h * 128 + ((jj ^ (h & 7)) << 4), qg + h * kHeadDim + u * 8);
+  }
+  tc::cp_async_wait_all();
+  if (rot) {  // rotate the last 64 channels in place (each thread its own pieces)
+    for (int e = tid; e < kHeads * (kHeadDim / 8); e += AT_THREADS) {
+      const int h = e >> 6, u = e & 63, kc = u >> 3, jj = u & 7;
+      if (u * 8 < kHeadDim - kRopeDim) continue;
+      uint4 *slot = reinterpret_cast<uint4 *>(Qs + kc * 8192 + h * 128 + ((jj ^ (h & 7)) << 4));
+      const uint4 x = *slot;
       uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -202,9 +210,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const float x0 = bf16_lo(w[q]), x1 = bf16_hi(w[q]);
         w[q] = pack2(x0 * c - x1 * s, x0 * s + x1 * c);
       }
-      x = make_uint4(w[0], w[1], w[2], w[3]);
+      *slot = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    *reinterpret_cast<uint4 *>(Qs + kc * 8192 + h * 128 + ((jj ^ (h & 7)) << 4)) = x;
   }
   tc::tc_fence_before();
   __syncthreads();

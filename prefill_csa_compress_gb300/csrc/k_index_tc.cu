@@ -174,49 +174,54 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
       const int tb = chunk * chunk_tiles;
       const int te = min(tiles_total, tb + chunk_tiles);
       if (tb >= te) continue;  // uniform across the CTA
-      // queries (B operand) and head weights
+      // queries (B operand): every 16-byte piece in flight at once (cp.async),
+      // then the rotated half is split in place into BF16 hi (chunk 1) and lo
+      // (chunk 2) by the thread that copied it
       for (int e = tid; e < 16 * C::N; e += IT_THREADS) {
         const int n = e / 16, part = (e / 8) % 2, jj = e % 8;
         const int i = n / kHeads, h = n % kHeads;
         const int t = g * G + i;
-        const uint32_t sw = (uint32_t)((jj ^ (n & 7)) << 4);
-        uint8_t *d0 = Bs + n * 128 + sw;
-        uint4 x = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
-        if (rb[i] == b) {
-          const uint16_t *src = static_cast<const uint16_t *>(a.q_idx) +
-                                ((long long)t * kHeads + h) * kIdxDim + part * 64 + jj * 8;
-          x = *reinterpret_cast<const uint4 *>(src);
+        uint8_t *d = Bs + part * C::B_CHUNK + n * 128 + ((jj ^ (n & 7)) << 4);
+        if (rb[i] == b)
+          tc::cp_async16(d, static_cast<const uint16_t *>(a.q_idx) +
+                                ((long long)t * kHeads + h) * kIdxDim + part * 64 + jj * 8);
+        else
+          *reinterpret_cast<uint4 *>(d) = make_uint4(0, 0, 0, 0);
+        if (part == 1)
+          *reinterpret_cast<uint4 *>(d + C::B_CHUNK) = make_uint4(0, 0, 0, 0);
+      }
+      tc::cp_async_wait_all();
+      if (rope) {
+        for (int e = tid; e < 16 * C::N; e += IT_THREADS) {
+          const int n = e / 16, part = (e / 8) % 2, jj = e % 8;
+          const int i = n / kHeads, h = n % kHeads;
+          const int t = g * G + i;
+          if (part != 1 || rb[i] != b) continue;
           const int p = a.row_pos[t];
-          if (part == 1 && rope && p >= 0) {
-            if (p >= a.rope_cap) {
-              if (h == 0 && jj == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
-            } else {
-              const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-              uint32_t hw[4], lw[4];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float x0 = __uint_as_float(xw[q] << 16);
-                const float x1 = __uint_as_float(xw[q] & 0xFFFF0000u);
-                const int pair = jj * 4 + q;
-                const float c = a.rope_cos[(long long)p * kRopeHalf + pair];
-                const float s = a.rope_sin[(long long)p * kRopeHalf + pair];
-                const float y0 = x0 * c - x1 * s;
-                const float y1 = x0 * s + x1 * c;
-                const __nv_bfloat162 hb = __floats2bfloat162_rn(y0, y1);
-                const float h0 = __low2float(hb), h1 = __high2float(hb);
-                hw[q] = *reinterpret_cast<const uint32_t *>(&hb);
-                lw[q] = pack_bf16(y0 - h0, y1 - h1);
-              }
-              x = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-              lo = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            }
+          if (p < 0) continue;
+          if (p >= a.rope_cap) {
+            if (h == 0 && jj == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
+            continue;
           }
-        }
-        if (part == 0) {
-          *reinterpret_cast<uint4 *>(d0) = x;
-        } else {
-          *reinterpret_cast<uint4 *>(d0 + C::B_CHUNK) = x;
-          *reinterpret_cast<uint4 *>(d0 + 2 * C::B_CHUNK) = lo;
+          uint8_t *d = Bs + C::B_CHUNK + n * 128 + ((jj ^ (n & 7)) << 4);
+          const uint4 x = *reinterpret_cast<const uint4 *>(d);
+          const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float x0 = __uint_as_float(xw[q] << 16);
+            const float x1 = __uint_as_float(xw[q] & 0xFFFF0000u);
+            const int pair = jj * 4 + q;
+            const float c = a.rope_cos[(long long)p * kRopeHalf + pair];
+            const float s = a.rope_sin[(long long)p * kRopeHalf + pair];
+            const float y0 = x0 * c - x1 * s;
+            const float y1 = x0 * s + x1 * c;
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(y0, y1);
+            hw[q] = *reinterpret_cast<const uint32_t *>(&hb);
+            lw[q] = pack_bf16(y0 - __low2float(hb), y1 - __high2float(hb));
+          }
+          *reinterpret_cast<uint4 *>(d) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4 *>(d + C::B_CHUNK) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
       }
       for (int e = tid; e < G * kHeads; e += IT_THREADS) {
