@@ -10,54 +10,80 @@
 // columns hold the dot products with the G rows x 64 heads of a row group
 // (N = 64G).  The head reduction then happens inside one thread with no
 // cross-lane traffic.  A CTA streams the pages of one request:
-//   warp 8      bulk-copies each INT8 page (16 KB) and its scales into a ring,
-//   warps 4..7  convert INT8 -> BF16 (exact: |v| <= 127 fits BF16's 8-bit
-//               significand) into the 128-byte-swizzled K-major layout,
-//   warp 9      issues tcgen05.mma (A = keys, B = queries) into a double-
-//               buffered TMEM accumulator,
-//   warps 0..3  read TMEM and apply ReLU, the head weights and the key scale.
-// Queries rotated by RoPE in FP32 are split into BF16 hi + lo parts so that the
-// BF16 tensor-core product keeps FP32-level accuracy (K = 64 + 64 + 64).
+//   warp 12     bulk-copies each INT8 page (16 KB) and its scales into a ring,
+//   warps 4..11 convert INT8 -> FP16 (exact, 10 instructions per 8 keys) into
+//               the 128-byte-swizzled K-major layout (a ring of A tiles),
+//   warp 13     issues tcgen05.mma (A = keys, B = queries) into a ring of
+//               TMEM accumulators (all 512 columns),
+//   warps 0..3  read TMEM and apply ReLU, the head weights and the key scale;
+//               with warp 13 they also build the query operand at the start
+//               of each pass while the first pages are already in flight.
+// The queries enter the MMA as FP16: each (row, head) is scaled by a power of
+// two that puts its largest |q| in [2^13, 2^14) (exact; the inverse factor is
+// folded into that head's weight, since ReLU(2^e x) = 2^e ReLU(x)).  The RoPE
+// half, rotated in FP32, is split into FP16 hi + lo parts so that the product
+// keeps FP32-level accuracy (K = 64 + 64 + 64).
+#include <cuda.h>
+#include <cstring>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
 #include "csa_internal.cuh"
 #include "tc.cuh"
 
 namespace csa {
 namespace {
 
-constexpr int IT_THREADS = 320;  // 10 warps
+// warps 0..3: epilogue (and the query operand at each pass start)
+// warps 4..11: converters; warp 12: producer; warp 13: MMA issuer
+constexpr int IT_THREADS = 448;
+constexpr int IT_CONV = 256;      // converter threads
+constexpr int IT_BUILD = 160;     // query builders: warps 0..3 and warp 13
+constexpr int W_PROD = 12, W_MMA = 13;
 
 template <int G>
 struct IdxTc {
+  // G == 2 (decode row pairs): the converted keys go to TMEM as the MMA's A
+  // operand, which keeps shared memory for the page ring and the queries.
+  // G == 4 (prefill): N = 256 fills TMEM with accumulators; A stays in smem.
+  static constexpr bool ATMEM = G == 2;
   static constexpr int N = G * kHeads;            // MMA N
-  static constexpr int NS = G == 2 ? 4 : 3;       // staging ring depth
+  static constexpr int NS = ATMEM ? 8 : 3;        // staging ring depth
+  static constexpr int NA = 2;                    // converted A tiles
+  static constexpr int NT = ATMEM ? 3 : 2;        // TMEM accumulator slots
+  static constexpr int A_COL = 0;                 // TMEM A tiles (64 columns each)
+  static constexpr int ACC_COL = ATMEM ? NA * 64 : 0;
   static constexpr int B_CHUNK = N * 128;         // bytes of one 64-wide K chunk of B
   static constexpr int A_CHUNK = kBlock * 128;    // 16 KB
-  static constexpr int A_BUF = 2 * A_CHUNK;       // 128 keys x 128 dims bf16
+  static constexpr int A_BUF = 2 * A_CHUNK;       // 128 keys x 128 dims fp16
   static constexpr int PAGE = kBlock * kIdxDim;   // 16 KB of int8 keys
   static constexpr int OFF_B = 0;
   static constexpr int OFF_A = OFF_B + 3 * B_CHUNK;
-  static constexpr int OFF_ST = OFF_A + 2 * A_BUF;
+  static constexpr int OFF_ST = OFF_A + (ATMEM ? 0 : NA * A_BUF);
   static constexpr int OFF_STSC = OFF_ST + NS * PAGE;
   static constexpr int OFF_SC = OFF_STSC + NS * kBlock * 4;
-  static constexpr int OFF_W = OFF_SC + 2 * kBlock * 4;
-  static constexpr int OFF_MISC = OFF_W + G * kHeads * 4;
-  static constexpr int SMEM = OFF_MISC + 512 + 1024;  // + alignment slack
-  static constexpr uint32_t TMEM_COLS = 2 * N;
+  static constexpr int OFF_W = OFF_SC + 4 * kBlock * 4;
+  static constexpr int OFF_ROPE = OFF_W + G * kHeads * 4;   // per row: 32 cos, 32 sin
+  static constexpr int OFF_MISC = OFF_ROPE + G * 64 * 4;
+  static constexpr int SMEM = OFF_MISC + 512 + 1024;        // + alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;
 };
 
 struct IdxMisc {
-  uint64_t st_full[4];
-  uint64_t st_empty[4];
-  uint64_t a_full[2];
-  uint64_t mma_done[2];
-  uint64_t tmem_empty[2];
+  uint64_t st_full[8];
+  uint64_t st_empty[8];
+  uint64_t a_full[3];    // converters -> MMA
+  uint64_t a_free[3];    // MMA commit -> converters (A tile may be overwritten)
+  uint64_t acc_full[4];  // MMA commit -> epilogue
+  uint64_t acc_empty[4]; // epilogue -> converters (slot and its scales free)
   uint32_t tmem_base;
-  int st_ok[4];
-  int a_ok[2];
+  int st_ok[8];
+  int a_ok[4];
   volatile int abort;
   int row_t[4];
   int row_V[4];
   int row_on[4];
+  int row_p[4];
 };
 
 __device__ __forceinline__ void set_abort(IdxMisc *m, uint32_t *status) {
@@ -65,34 +91,36 @@ __device__ __forceinline__ void set_abort(IdxMisc *m, uint32_t *status) {
   flag(status, CSA_DEV_TIMEOUT);
 }
 
-// 8 int8 -> 8 bf16, exactly: (v ^ 0x80) placed in the mantissa of 2^23 gives
-// 2^23 + 128 + v as an FP32 value.
-__device__ __forceinline__ uint4 i8x8_to_bf16x8(uint2 raw) {
-  const uint32_t w[2] = {raw.x ^ 0x80808080u, raw.y ^ 0x80808080u};
+// 8 int8 -> 8 fp16, exactly: the offset-binary byte (v ^ 0x80) placed in the
+// low mantissa bits of 1024.0 gives 1024 + 128 + v; subtracting 1152 leaves v.
+__device__ __forceinline__ uint4 i8x8_to_f16x8(uint2 raw) {
+  const uint32_t a = raw.x ^ 0x80808080u, b = raw.y ^ 0x80808080u;
+  const uint32_t p[4] = {__byte_perm(a, 0x64646464u, 0x5140u), __byte_perm(a, 0x64646464u, 0x5342u),
+                         __byte_perm(b, 0x64646464u, 0x5140u), __byte_perm(b, 0x64646464u, 0x5342u)};
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
   uint32_t out[4];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    float f[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      f[k] = __uint_as_float(__byte_perm(w[h], 0x4B000000u, 0x7440u | k)) - 8388736.0f;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(f[0], f[1]);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(f[2], f[3]);
-    out[2 * h] = *reinterpret_cast<uint32_t *>(&lo);
-    out[2 * h + 1] = *reinterpret_cast<uint32_t *>(&hi);
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h = __hsub2(*reinterpret_cast<const __half2 *>(&p[i]), bias);
+    out[i] = *reinterpret_cast<const uint32_t *>(&h);
   }
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t *>(&v);
+__device__ __forceinline__ uint32_t pack_f16(float a, float b) {
+  const __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void named_barrier(int id, int n_threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n_threads) : "memory");
 }
 
 template <int G>
 __global__ void __launch_bounds__(IT_THREADS, 1)
     index_score_tc_kernel(csa_index_args a, float *__restrict__ scores, int cols, int n_groups,
-                          int chunk_tiles, int units_per_group, uint32_t *zero_ctr) {
+                          int chunk_tiles, int units_per_group, uint32_t *zero_ctr,
+                          const __grid_constant__ CUtensorMap keys_map) {
   using C = IdxTc<G>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -103,6 +131,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   float *StSc = reinterpret_cast<float *>(sm + C::OFF_STSC);
   float *Sc = reinterpret_cast<float *>(sm + C::OFF_SC);
   float *Ws = reinterpret_cast<float *>(sm + C::OFF_W);
+  float *Rope = reinterpret_cast<float *>(sm + C::OFF_ROPE);
   IdxMisc *M = reinterpret_cast<IdxMisc *>(sm + C::OFF_MISC);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -115,17 +144,20 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   if (tid == 0) {
     for (int s = 0; s < C::NS; ++s) {
       tc::mbar_init(&M->st_full[s], 1);
-      tc::mbar_init(&M->st_empty[s], 128);
+      tc::mbar_init(&M->st_empty[s], IT_CONV);
     }
-    for (int j = 0; j < 2; ++j) {
-      tc::mbar_init(&M->a_full[j], 128);
-      tc::mbar_init(&M->mma_done[j], 1);
-      tc::mbar_init(&M->tmem_empty[j], 128);
+    for (int j = 0; j < C::NA; ++j) {
+      tc::mbar_init(&M->a_full[j], IT_CONV);
+      tc::mbar_init(&M->a_free[j], 1);
+    }
+    for (int j = 0; j < C::NT; ++j) {
+      tc::mbar_init(&M->acc_full[j], 1);
+      tc::mbar_init(&M->acc_empty[j], 128);
     }
     M->abort = 0;
     tc::mbar_fence_init();
   }
-  if (warp == 9) tc::tmem_alloc(&M->tmem_base, C::TMEM_COLS);
+  if (warp == W_MMA) tc::tmem_alloc(&M->tmem_base, C::TMEM_COLS);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -153,7 +185,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
       for (int j = 0; j < pi; ++j) first = first && rb[j] != b;
       if (!first) continue;
 
-      // ---------------- pass setup (all threads)
+      // ---------------- pass start (all roles have finished the previous pass)
       __syncthreads();
       if (M->abort) break;
       int vmax = 0;
@@ -174,65 +206,112 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
       const int tb = chunk * chunk_tiles;
       const int te = min(tiles_total, tb + chunk_tiles);
       if (tb >= te) continue;  // uniform across the CTA
-      // queries (B operand): every 16-byte piece in flight at once (cp.async),
-      // then the rotated half is split in place into BF16 hi (chunk 1) and lo
-      // (chunk 2) by the thread that copied it
-      for (int e = tid; e < 16 * C::N; e += IT_THREADS) {
-        const int n = e / 16, part = (e / 8) % 2, jj = e % 8;
-        const int i = n / kHeads, h = n % kHeads;
-        const int t = g * G + i;
-        uint8_t *d = Bs + part * C::B_CHUNK + n * 128 + ((jj ^ (n & 7)) << 4);
-        if (rb[i] == b)
-          tc::cp_async16(d, static_cast<const uint16_t *>(a.q_idx) +
-                                ((long long)t * kHeads + h) * kIdxDim + part * 64 + jj * 8);
-        else
-          *reinterpret_cast<uint4 *>(d) = make_uint4(0, 0, 0, 0);
-        if (part == 1)
-          *reinterpret_cast<uint4 *>(d + C::B_CHUNK) = make_uint4(0, 0, 0, 0);
-      }
-      tc::cp_async_wait_all();
-      if (rope) {
-        for (int e = tid; e < 16 * C::N; e += IT_THREADS) {
+      const int nt = te - tb;
+
+      if (warp < 4 || warp == W_MMA) {
+        // ---------------- query operand (overlaps the first page copies)
+        const int bt = warp < 4 ? tid : 128 + lane;
+        for (int e = bt; e < 16 * C::N; e += IT_BUILD) {
           const int n = e / 16, part = (e / 8) % 2, jj = e % 8;
           const int i = n / kHeads, h = n % kHeads;
+          if (rb[i] == b)
+            tc::cp_async16(Bs + part * C::B_CHUNK + n * 128 + ((jj ^ (n & 7)) << 4),
+                           static_cast<const uint16_t *>(a.q_idx) +
+                               ((long long)(g * G + i) * kHeads + h) * kIdxDim + part * 64 +
+                               jj * 8);
+        }
+        // head weights, row positions and the rows' RoPE table entries
+        for (int e = bt; e < G * (kHeads + 64); e += IT_BUILD) {
+          const int i = e / (kHeads + 64), f = e % (kHeads + 64);
           const int t = g * G + i;
-          if (part != 1 || rb[i] != b) continue;
+          if (rb[i] != b) continue;
           const int p = a.row_pos[t];
-          if (p < 0) continue;
-          if (p >= a.rope_cap) {
-            if (h == 0 && jj == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
+          if (f < kHeads) {
+            Ws[i * kHeads + f] = a.weights[(long long)t * kHeads + f];
+          } else if (rope && p >= 0 && p < a.rope_cap) {
+            const int q = f - kHeads;  // 0..31 cos, 32..63 sin
+            Rope[i * 64 + q] = q < 32 ? a.rope_cos[(long long)p * kRopeHalf + q]
+                                      : a.rope_sin[(long long)p * kRopeHalf + q - 32];
+          }
+          if (f == 0) M->row_p[i] = p;
+        }
+        tc::cp_async_wait_all();
+        named_barrier(1, IT_BUILD);
+        // in place: scale the (row, head) by 2^e (its 16 pieces sit in 16
+        // consecutive lanes), convert to FP16, and split the rotated half into
+        // hi (chunk 1) + lo (chunk 2)
+        for (int e0 = 0; e0 < 16 * C::N; e0 += IT_BUILD) {
+          const int e = e0 + bt;
+          const bool live = e < 16 * C::N;
+          const int n = live ? e / 16 : 0, part = (e / 8) % 2, jj = e % 8;
+          const int i = n / kHeads;
+          const bool on = live && rb[i] == b;
+          uint8_t *d = Bs + part * C::B_CHUNK + n * 128 + ((jj ^ (n & 7)) << 4);
+          float x[8];
+          float mx = 0.f;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) x[q] = 0.f;
+          if (on) {
+            const uint4 raw = *reinterpret_cast<const uint4 *>(d);
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              x[2 * q] = __uint_as_float(w[q] << 16);
+              x[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(x[q]));
+          }
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          if (!live) continue;
+          if (!on) {
+            *reinterpret_cast<uint4 *>(d) = make_uint4(0, 0, 0, 0);
+            if (part == 1) *reinterpret_cast<uint4 *>(d + C::B_CHUNK) = make_uint4(0, 0, 0, 0);
+            if (part == 0 && jj == 0) Ws[n] = 0.f;
             continue;
           }
-          uint8_t *d = Bs + C::B_CHUNK + n * 128 + ((jj ^ (n & 7)) << 4);
-          const uint4 x = *reinterpret_cast<const uint4 *>(d);
-          const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+          int ex = 0;
+          if (mx > 0.f) {
+            int E;
+            frexpf(mx, &E);
+            ex = min(100, max(-100, 14 - E));
+          }
+          if (part == 0 && jj == 0) Ws[n] = ldexpf(Ws[n], -ex);
+          const int p = M->row_p[i];
+          bool rot = part == 1 && rope && p >= 0;
+          if (rot && p >= a.rope_cap) {
+            rot = false;
+            if ((n & 63) == 0 && jj == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
+          }
+          if (rot) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int pair = jj * 4 + q;
+              const float c = Rope[i * 64 + pair], sn = Rope[i * 64 + 32 + pair];
+              const float x0 = x[2 * q], x1 = x[2 * q + 1];
+              x[2 * q] = x0 * c - x1 * sn;
+              x[2 * q + 1] = x0 * sn + x1 * c;
+            }
+          }
           uint32_t hw[4], lw[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float x0 = __uint_as_float(xw[q] << 16);
-            const float x1 = __uint_as_float(xw[q] & 0xFFFF0000u);
-            const int pair = jj * 4 + q;
-            const float c = a.rope_cos[(long long)p * kRopeHalf + pair];
-            const float s = a.rope_sin[(long long)p * kRopeHalf + pair];
-            const float y0 = x0 * c - x1 * s;
-            const float y1 = x0 * s + x1 * c;
-            const __nv_bfloat162 hb = __floats2bfloat162_rn(y0, y1);
-            hw[q] = *reinterpret_cast<const uint32_t *>(&hb);
-            lw[q] = pack_bf16(y0 - __low2float(hb), y1 - __high2float(hb));
+            const float y0 = ldexpf(x[2 * q], ex), y1 = ldexpf(x[2 * q + 1], ex);
+            const __half2 hv = __floats2half2_rn(y0, y1);
+            hw[q] = *reinterpret_cast<const uint32_t *>(&hv);
+            lw[q] = pack_f16(y0 - __low2float(hv), y1 - __high2float(hv));
           }
           *reinterpret_cast<uint4 *>(d) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4 *>(d + C::B_CHUNK) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          if (part == 1)
+            *reinterpret_cast<uint4 *>(d + C::B_CHUNK) =
+                rot ? make_uint4(lw[0], lw[1], lw[2], lw[3]) : make_uint4(0, 0, 0, 0);
         }
+        tc::fence_async_shared();
+        named_barrier(1, IT_BUILD);
       }
-      for (int e = tid; e < G * kHeads; e += IT_THREADS) {
-        const int i = e / kHeads, t = g * G + i;
-        Ws[e] = rb[i] == b ? a.weights[(long long)t * kHeads + (e % kHeads)] : 0.f;
-      }
-      tc::fence_async_shared();
-      __syncthreads();
 
-      const int nt = te - tb;
-      if (warp == 8) {
+      if (warp == W_PROD) {
         // ---------------- producer: one page (and its scales) per tile
         if (lane == 0) {
           for (int k = 0; k < nt && !M->abort; ++k) {
@@ -250,8 +329,11 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
             M->st_ok[s] = ok;
             if (ok) {
               tc::mbar_arrive_expect_tx(&M->st_full[s], C::PAGE + kBlock * 4);
-              tc::bulk_g2s(St + s * C::PAGE, a.idx_pool + (long long)phys * C::PAGE, C::PAGE,
-                           &M->st_full[s]);
+              if constexpr (C::ATMEM)  // 128-byte swizzled rows: conflict-free row reads
+                tc::tma_load_2d(St + s * C::PAGE, &keys_map, 0, phys * kBlock, &M->st_full[s]);
+              else
+                tc::bulk_g2s(St + s * C::PAGE, a.idx_pool + (long long)phys * C::PAGE, C::PAGE,
+                             &M->st_full[s]);
               tc::bulk_g2s(StSc + s * kBlock, a.idx_scale_pool + (long long)phys * kBlock,
                            kBlock * 4, &M->st_full[s]);
             } else {
@@ -260,100 +342,159 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
             }
           }
         }
-      } else if (warp >= 4 && warp < 8) {
-        // ---------------- converters: int8 page -> bf16 swizzled A tile
+      } else if (warp >= 4 && warp < 12) {
+        // ---------------- converters: int8 page -> fp16 swizzled A tile
         const int ct = tid - 128;
         for (int k = 0; k < nt; ++k) {
           const uint32_t itk = it + k;
-          const int s = itk % C::NS, j = itk % 2;
+          const int s = itk % C::NS, j = itk % C::NA, q4 = itk % C::NT;
           if (!tc::mbar_wait(&M->st_full[s], (itk / C::NS) & 1) ||
-              !tc::mbar_wait(&M->tmem_empty[j], ((itk / 2) & 1) ^ 1)) {
+              !tc::mbar_wait(&M->a_free[j], ((itk / C::NA) & 1) ^ 1) ||
+              !tc::mbar_wait(&M->acc_empty[q4], ((itk / C::NT) & 1) ^ 1)) {
             set_abort(M, a.status_dev);
             break;
           }
           const int ok = M->st_ok[s];
+          if constexpr (C::ATMEM) {
+            // thread = one key row (TMEM lane) x one half of its 128 dims
+            const int wq = (warp - 4) & 3, half = (warp - 4) >> 2;
+            const int r = wq * 32 + lane;
+            if (ok) {
+              const uint8_t *src = St + s * C::PAGE + r * 128;
+              uint32_t packed[32];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const int cc = half * 4 + c;
+                const uint4 raw = *reinterpret_cast<const uint4 *>(src + ((cc ^ (r & 7)) << 4));
+                const uint4 lo = i8x8_to_f16x8(make_uint2(raw.x, raw.y));
+                const uint4 hi = i8x8_to_f16x8(make_uint2(raw.z, raw.w));
+                packed[8 * c + 0] = lo.x;
+                packed[8 * c + 1] = lo.y;
+                packed[8 * c + 2] = lo.z;
+                packed[8 * c + 3] = lo.w;
+                packed[8 * c + 4] = hi.x;
+                packed[8 * c + 5] = hi.y;
+                packed[8 * c + 6] = hi.z;
+                packed[8 * c + 7] = hi.w;
+              }
+              tc::tmem_st32u(tmem + ((uint32_t)(wq * 32) << 16) + C::A_COL + j * 64 + half * 32,
+                             packed);
+              tc::tmem_wait_st();
+              if (half == 0) Sc[q4 * kBlock + r] = StSc[s * kBlock + r];
+            }
+            if (ct == 0) M->a_ok[q4] = ok;
+            tc::tc_fence_before();
+          } else {
           if (ok) {
             const uint8_t *src = St + s * C::PAGE;
             uint8_t *dst = As + j * C::A_BUF;
-#pragma unroll 4
-            for (int q = 0; q < 16; ++q) {
-              const int unit = q * 128 + ct;
-              const int r = unit / 16, jc = unit % 16;
-              const int kc = jc / 8, jj = jc % 8;
-              const uint2 raw = *reinterpret_cast<const uint2 *>(src + r * 128 + jc * 8);
-              *reinterpret_cast<uint4 *>(dst + kc * C::A_CHUNK + r * 128 +
-                                         ((jj ^ (r & 7)) << 4)) = i8x8_to_bf16x8(raw);
+            uint2 raw[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int unit = q * IT_CONV + ct;
+              raw[q] = *reinterpret_cast<const uint2 *>(src + (unit >> 4) * 128 + (unit & 15) * 8);
             }
-            Sc[j * kBlock + ct] = StSc[s * kBlock + ct];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int unit = q * IT_CONV + ct;
+              const int r = unit >> 4, jc = unit & 15;
+              const int kc = jc >> 3, jj = jc & 7;
+              *reinterpret_cast<uint4 *>(dst + kc * C::A_CHUNK + r * 128 + ((jj ^ (r & 7)) << 4)) =
+                  i8x8_to_f16x8(raw[q]);
+            }
+            if (ct < kBlock) Sc[q4 * kBlock + ct] = StSc[s * kBlock + ct];
           }
-          if (ct == 0) M->a_ok[j] = ok;
+          if (ct == 0) M->a_ok[q4] = ok;
           tc::fence_async_shared();
+          }
           tc::mbar_arrive(&M->a_full[j]);
           tc::mbar_arrive(&M->st_empty[s]);
         }
-      } else if (warp == 9) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
-          constexpr uint32_t idesc = tc::idesc_bf16_f32(128, C::N);
-          const uint32_t a_base = tc::smem_u32(As), b_base = tc::smem_u32(Bs);
-          for (int k = 0; k < nt; ++k) {
-            const uint32_t itk = it + k;
-            const int j = itk % 2;
-            if (!tc::mbar_wait(&M->a_full[j], (itk / 2) & 1)) {
-              set_abort(M, a.status_dev);
-              break;
-            }
-            tc::tc_fence_after();
-            const uint32_t d = tmem + j * C::N;
-            for (int kc = 0; kc < n_kchunks; ++kc) {
-              const uint32_t a_off = a_base + j * C::A_BUF + (kc == 0 ? 0 : C::A_CHUNK);
-              const uint32_t b_off = b_base + kc * C::B_CHUNK;
+      } else if (warp == W_MMA) {
+        // ---------------- MMA issuer: the whole warp runs the loop with
+        // warp-uniform operands; one elected lane issues
+        constexpr uint32_t idesc = tc::idesc_f16_f32(128, C::N);
+        const uint32_t a_base = tc::smem_u32(As), b_base = tc::smem_u32(Bs);
+        uint64_t bd[12];
 #pragma unroll
-              for (int s16 = 0; s16 < 4; ++s16)
-                tc::mma_bf16(d, tc::desc_sw128(a_off + s16 * 32), tc::desc_sw128(b_off + s16 * 32),
-                             idesc, (kc | s16) != 0);
-            }
-            tc::mma_commit(&M->mma_done[j]);
-          }
-        }
-      } else {
-        // ---------------- epilogue: warps 0..3 own TMEM lanes 32*warp .. +31
-        const int r = tid;  // key within the tile
+        for (int kc = 0; kc < 3; ++kc)
+#pragma unroll
+          for (int s16 = 0; s16 < 4; ++s16)
+            bd[kc * 4 + s16] = tc::desc_sw128(b_base + kc * C::B_CHUNK + s16 * 32);
         for (int k = 0; k < nt; ++k) {
           const uint32_t itk = it + k;
-          const int j = itk % 2;
-          if (!tc::mbar_wait(&M->mma_done[j], (itk / 2) & 1)) {
+          const int j = itk % C::NA;
+          if (!tc::mbar_wait(&M->a_full[j], (itk / C::NA) & 1)) {
             set_abort(M, a.status_dev);
             break;
           }
           tc::tc_fence_after();
-          const int ok = M->a_ok[j];
-          const float scale = Sc[j * kBlock + r];
+          const uint32_t d = tmem + C::ACC_COL + (itk % C::NT) * C::N;
+          if constexpr (C::ATMEM) {
+            const uint32_t a_t = tmem + C::A_COL + j * 64;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              tc::mma_f16_ta_elect(d, a_t + (i < 4 ? 0 : 32) + (i & 3) * 8, bd[i], idesc, i != 0);
+            if (n_kchunks == 3) {
+#pragma unroll
+              for (int i = 8; i < 12; ++i)
+                tc::mma_f16_ta_elect(d, a_t + 32 + (i & 3) * 8, bd[i], idesc, 1u);
+            }
+          } else {
+            const uint32_t a_off = a_base + j * C::A_BUF;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              tc::mma_ss_elect(d, tc::desc_sw128(a_off + (i < 4 ? 0 : C::A_CHUNK) + (i & 3) * 32),
+                               bd[i], idesc, i != 0);
+            if (n_kchunks == 3) {
+#pragma unroll
+              for (int i = 8; i < 12; ++i)
+                tc::mma_ss_elect(d, tc::desc_sw128(a_off + C::A_CHUNK + (i & 3) * 32), bd[i],
+                                 idesc, 1u);
+            }
+          }
+          tc::mma_commit_elect(&M->a_free[j]);
+          tc::mma_commit_elect(&M->acc_full[itk % C::NT]);
+          __syncwarp();
+        }
+      } else if (warp < 4) {
+        // ---------------- epilogue: warps 0..3 own TMEM lanes 32*warp .. +31
+        const int r = tid;  // key within the tile
+        for (int k = 0; k < nt; ++k) {
+          const uint32_t itk = it + k;
+          const int q4 = itk % C::NT;
+          if (!tc::mbar_wait(&M->acc_full[q4], (itk / C::NT) & 1)) {
+            set_abort(M, a.status_dev);
+            break;
+          }
+          tc::tc_fence_after();
+          const int ok = M->a_ok[q4];
+          const float scale = Sc[q4 * kBlock + r];
           const int c = (tb + k) * kBlock + r;
 #pragma unroll
           for (int i = 0; i < G; ++i) {
             if (!M->row_on[i]) continue;
-            float acc = 0.f;
+            float v[64];
+            tc::tmem_ld64(tmem + ((uint32_t)(warp * 32) << 16) + C::ACC_COL + q4 * C::N +
+                              i * kHeads,
+                          v);
+            const float4 *w4 = reinterpret_cast<const float4 *>(Ws + i * kHeads);
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              float v[32];
-              tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + j * C::N + i * kHeads +
-                                half * 32,
-                            v);
-              const float *w = Ws + i * kHeads + half * 32;
-              if (a.relu) {
+            for (int h4 = 0; h4 < 16; ++h4) {
+              const float4 w = w4[h4];
+              float x[4];
 #pragma unroll
-                for (int h = 0; h < 32; ++h) acc = fmaf(w[h], fmaxf(v[h], 0.f), acc);
-              } else {
-#pragma unroll
-                for (int h = 0; h < 32; ++h) acc = fmaf(w[h], v[h], acc);
-              }
+              for (int q = 0; q < 4; ++q) x[q] = a.relu ? fmaxf(v[4 * h4 + q], 0.f) : v[4 * h4 + q];
+              acc0 = tc::ffma2(make_float2(w.x, w.y), make_float2(x[0], x[1]), acc0);
+              acc1 = tc::ffma2(make_float2(w.z, w.w), make_float2(x[2], x[3]), acc1);
             }
+            const float sum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
             if (c < M->row_V[i])
-              scores[(long long)M->row_t[i] * cols + c] = ok ? scale * acc : -INFINITY;
+              scores[(long long)M->row_t[i] * cols + c] = ok ? scale * sum : -INFINITY;
           }
           tc::tc_fence_before();
-          tc::mbar_arrive(&M->tmem_empty[j]);
+          tc::mbar_arrive(&M->acc_empty[q4]);
         }
       }
       it += nt;
@@ -361,7 +502,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   }
 
   // drain: wait (bounded) for copies still in flight, then free TMEM
-  if (warp == 8 && lane == 0 && M->abort) {
+  if (warp == W_PROD && lane == 0 && M->abort) {
     for (int k = 0; k < C::NS && k < (int)it; ++k) {
       const uint32_t itk = it - 1 - k;
       tc::mbar_wait(&M->st_full[itk % C::NS], (itk / C::NS) & 1, 100000000ull);
@@ -370,7 +511,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == 9) tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == W_MMA) tc::tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 int sm_count() {
@@ -387,10 +528,36 @@ int sm_count() {
   return cached[dev];
 }
 
+// Tensor map of the INT8 key pool as a 2D [pages * 128 rows, 128 bytes] array,
+// one page per box, 128-byte swizzle.
+bool encode_keys_map(const csa_index_args &a, CUtensorMap *map) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)kIdxDim, (cuuint64_t)a.n_blocks * kBlock};
+  const cuuint64_t strides[1] = {(cuuint64_t)kIdxDim};
+  const cuuint32_t box[2] = {(cuuint32_t)kIdxDim, (cuuint32_t)kBlock};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(a.idx_pool), dims,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int G>
 cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, uint32_t *zero_ctr,
                       cudaStream_t s) {
   using C = IdxTc<G>;
+  CUtensorMap keys_map;
+  memset(&keys_map, 0, sizeof(keys_map));
+  if (C::ATMEM && !encode_keys_map(a, &keys_map)) return cudaErrorInvalidValue;
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -411,7 +578,7 @@ cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, uint32_t
   const int grid = (int)(n_units < sms ? n_units : sms);
   launch_begin(CSA_K_INDEX_SCORE, s);
   index_score_tc_kernel<G><<<grid, IT_THREADS, C::SMEM, s>>>(a, scores, cols, n_groups, chunk,
-                                                             upg, zero_ctr);
+                                                             upg, zero_ctr, keys_map);
   launch_end(CSA_K_INDEX_SCORE, s);
   return cudaGetLastError();
 }
