@@ -34,12 +34,14 @@
 namespace csa {
 namespace {
 
-// warps 0..3: epilogue (and the query operand at each pass start)
-// warps 4..11: converters; warp 12: producer; warp 13: MMA issuer
-constexpr int IT_THREADS = 448;
+// warps 0..7: epilogue (two warps per TMEM sub-partition, split by row);
+// warps 8..15: converters; warp 16: producer; warp 17: MMA issuer.  All
+// warps but the producer build the query operand at the start of a pass.
+constexpr int IT_THREADS = 576;
+constexpr int IT_EPI = 256;       // epilogue threads
 constexpr int IT_CONV = 256;      // converter threads
-constexpr int IT_BUILD = 160;     // query builders: warps 0..3 and warp 13
-constexpr int W_PROD = 12, W_MMA = 13;
+constexpr int IT_BUILD = 544;     // query builders: every warp but the producer
+constexpr int W_CONV0 = 8, W_PROD = 16, W_MMA = 17;
 
 template <int G>
 struct IdxTc {
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
     }
     for (int j = 0; j < C::NT; ++j) {
       tc::mbar_init(&M->acc_full[j], 1);
-      tc::mbar_init(&M->acc_empty[j], 128);
+      tc::mbar_init(&M->acc_empty[j], IT_EPI);
     }
     M->abort = 0;
     tc::mbar_fence_init();
@@ -208,9 +210,9 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
       if (tb >= te) continue;  // uniform across the CTA
       const int nt = te - tb;
 
-      if (warp < 4 || warp == W_MMA) {
+      if (warp != W_PROD) {
         // ---------------- query operand (overlaps the first page copies)
-        const int bt = warp < 4 ? tid : 128 + lane;
+        const int bt = warp < W_PROD ? tid : tid - 32;
         for (int e = bt; e < 16 * C::N; e += IT_BUILD) {
           const int n = e / 16, part = (e / 8) % 2, jj = e % 8;
           const int i = n / kHeads, h = n % kHeads;
@@ -271,13 +273,14 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
             if (part == 0 && jj == 0) Ws[n] = 0.f;
             continue;
           }
+          // 2^ex puts the head's largest |q| in [2^13, 2^14); exact scaling
           int ex = 0;
           if (mx > 0.f) {
-            int E;
-            frexpf(mx, &E);
+            const int E = (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 126;  // mx in [2^(E-1), 2^E)
             ex = min(100, max(-100, 14 - E));
           }
-          if (part == 0 && jj == 0) Ws[n] = ldexpf(Ws[n], -ex);
+          const float up = __uint_as_float((uint32_t)(127 + ex) << 23);
+          if (part == 0 && jj == 0) Ws[n] *= __uint_as_float((uint32_t)(127 - ex) << 23);
           const int p = M->row_p[i];
           bool rot = part == 1 && rope && p >= 0;
           if (rot && p >= a.rope_cap) {
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
           uint32_t hw[4], lw[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float y0 = ldexpf(x[2 * q], ex), y1 = ldexpf(x[2 * q + 1], ex);
+            const float y0 = x[2 * q] * up, y1 = x[2 * q + 1] * up;
             const __half2 hv = __floats2half2_rn(y0, y1);
             hw[q] = *reinterpret_cast<const uint32_t *>(&hv);
             lw[q] = pack_f16(y0 - __low2float(hv), y1 - __high2float(hv));
@@ -342,9 +345,9 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
             }
           }
         }
-      } else if (warp >= 4 && warp < 12) {
-        // ---------------- converters: int8 page -> fp16 swizzled A tile
-        const int ct = tid - 128;
+      } else if (warp >= W_CONV0 && warp < W_PROD) {
+        // ---------------- converters: int8 page -> fp16 A tile
+        const int ct = tid - W_CONV0 * 32;
         for (int k = 0; k < nt; ++k) {
           const uint32_t itk = it + k;
           const int s = itk % C::NS, j = itk % C::NA, q4 = itk % C::NT;
@@ -357,7 +360,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
           const int ok = M->st_ok[s];
           if constexpr (C::ATMEM) {
             // thread = one key row (TMEM lane) x one half of its 128 dims
-            const int wq = (warp - 4) & 3, half = (warp - 4) >> 2;
+            const int wq = (warp - W_CONV0) & 3, half = (warp - W_CONV0) >> 2;
             const int r = wq * 32 + lane;
             if (ok) {
               const uint8_t *src = St + s * C::PAGE + r * 128;
@@ -457,9 +460,11 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
           tc::mma_commit_elect(&M->acc_full[itk % C::NT]);
           __syncwarp();
         }
-      } else if (warp < 4) {
-        // ---------------- epilogue: warps 0..3 own TMEM lanes 32*warp .. +31
-        const int r = tid;  // key within the tile
+      } else if (warp < W_CONV0) {
+        // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 and
+        // the rows i with i % 2 == w / 4
+        const int r = (warp & 3) * 32 + lane;  // key within the tile
+        const int i0 = warp >> 2;
         for (int k = 0; k < nt; ++k) {
           const uint32_t itk = it + k;
           const int q4 = itk % C::NT;
@@ -472,10 +477,10 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
           const float scale = Sc[q4 * kBlock + r];
           const int c = (tb + k) * kBlock + r;
 #pragma unroll
-          for (int i = 0; i < G; ++i) {
+          for (int i = i0; i < G; i += 2) {
             if (!M->row_on[i]) continue;
             float v[64];
-            tc::tmem_ld64(tmem + ((uint32_t)(warp * 32) << 16) + C::ACC_COL + q4 * C::N +
+            tc::tmem_ld64(tmem + ((uint32_t)((warp & 3) * 32) << 16) + C::ACC_COL + q4 * C::N +
                               i * kHeads,
                           v);
             const float4 *w4 = reinterpret_cast<const float4 *>(Ws + i * kHeads);
