@@ -197,6 +197,33 @@ typedef struct {
 CSA_API csa_status_t csa_index_topk(csa_index_args *args, csa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * csa_index_topk_noalloc - csa_index_topk that needs no caller workspace.
+ *
+ * No counterpart on the pages.  Some callers cannot hand this library device
+ * memory: an engine plugin whose device memory is planned once when the
+ * engine is built and may not call the CUDA allocator while it serves, or a
+ * latency-critical decode loop that must not call cudaMalloc/cudaFree because
+ * those can synchronise the whole device and stall every other stream.  This
+ * variant computes exactly what csa_index_topk computes, with the same
+ * arguments; `workspace`/`workspace_bytes` are ignored and it allocates
+ * nothing.  Its score scratch is one array of CSA_NOALLOC_MAX_SCORES FP32
+ * entries (4 MiB) inside the library, held on every GPU that loads the
+ * library until the process exits.  Limits: a row may hold at most 8192
+ * entries (max_blocks * 128 <= 8192) and, unless the caller passes its own
+ * `scores` buffer, n_rows * max_blocks * 128 <= CSA_NOALLOC_MAX_SCORES; larger
+ * calls return CSA_ERR_UNSUPPORTED and launch nothing.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every
+ * call on a device shares the array, so calls that overlap on the GPU (two
+ * streams, or two threads) race and must be serialised by the caller.  The
+ * array keeps the previous call's scores; nothing in it has to start at zero,
+ * because only entries a call writes are read back.
+ * ---------------------------------------------------------------------- */
+#define CSA_NOALLOC_MAX_SCORES (1u << 20)
+
+CSA_API csa_status_t csa_index_topk_noalloc(csa_index_args *args, csa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * csa_sparse_attn_decode / csa_sparse_attn_prefill - shared-KV sparse
  * attention with an attention sink.
  *

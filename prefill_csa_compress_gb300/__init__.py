@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     CsaError,
     csa_compress,
     csa_index_topk,
+    csa_index_topk_noalloc,
     csa_sparse_attn_decode,
     csa_sparse_attn_prefill,
     launch_count,

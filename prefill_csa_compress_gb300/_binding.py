@@ -90,6 +90,7 @@ def lib():
                 "g.build()\"` (the CSA path has no CPU fallback)")
         L = ctypes.CDLL(LIB_PATH)
         for name, argt in (("csa_compress", CompressArgs), ("csa_index_topk", IndexArgs),
+                           ("csa_index_topk_noalloc", IndexArgs),
                            ("csa_sparse_attn_decode", AttnArgs),
                            ("csa_sparse_attn_prefill", AttnArgs)):
             f = getattr(L, name)
@@ -273,6 +274,37 @@ def csa_index_topk(*, q_idx, weights, row_req, row_pos, n_cmp, ratio, idx_pool, 
     a.score_cols = int(scores.shape[1]) if scores is not None else 0
     a.status_dev = _p(status, torch.int32, "status")
     return _run("csa_index_topk", a, workspace, stream, q_idx.device, prepare)
+
+
+def csa_index_topk_noalloc(*, q_idx, weights, row_req, row_pos, n_cmp, ratio, idx_pool,
+                           idx_scale_pool, cmp_block_table, topk, topk_idx, topk_score=None,
+                           scores=None, relu=True, rope_cos=None, rope_sin=None,
+                           mode=CSA_MODE_AUTO, status=None, stream=None):
+    """csa_index_topk without a caller workspace: the library's own score
+    scratch is used (``include/csa.h``: csa_index_topk_noalloc)."""
+    a = IndexArgs()
+    a.struct_size = ctypes.sizeof(IndexArgs)
+    a.n_rows, a.n_heads, a.head_dim = (int(x) for x in q_idx.shape)
+    a.ratio, a.topk, a.relu, a.mode = int(ratio), int(topk), 1 if relu else 0, int(mode)
+    a.q_idx = _p(q_idx, torch.bfloat16, "q_idx")
+    a.weights = _p(weights, torch.float32, "weights")
+    a.row_req = _p(row_req, torch.int32, "row_req")
+    a.row_pos = _p(row_pos, torch.int32, "row_pos")
+    a.n_cmp = _p(n_cmp, torch.int32, "n_cmp")
+    a.idx_pool = _p(idx_pool, torch.int8, "idx_pool")
+    a.idx_scale_pool = _p(idx_scale_pool, torch.float32, "idx_scale_pool")
+    a.cmp_block_table = _p(cmp_block_table, torch.int32, "cmp_block_table")
+    a.n_req, a.max_blocks = int(cmp_block_table.shape[0]), int(cmp_block_table.shape[1])
+    a.n_blocks = int(idx_pool.shape[0])
+    _fill_common_rope(a, rope_cos, rope_sin)
+    a.topk_idx = _p(topk_idx, torch.int32, "topk_idx")
+    a.topk_score = _p(topk_score, torch.float32, "topk_score")
+    a.scores = _p(scores, torch.float32, "scores")
+    a.score_cols = int(scores.shape[1]) if scores is not None else 0
+    a.status_dev = _p(status, torch.int32, "status")
+    st = lib().csa_index_topk_noalloc(ctypes.byref(a), _stream(stream))
+    if st != CSA_OK:
+        raise CsaError("csa_index_topk_noalloc", st)
 
 
 def _attn(fn_name, *, q, row_req, row_pos, topk_idx, kv_pool, kv_block_table, kv_len, cmp_pool,

@@ -1,0 +1,76 @@
+// csa_index_topk_noalloc: the indexer top-k for callers that cannot allocate
+// device memory (see include/csa.h).  Its score scratch is a file-scope device
+// array shared by every call on a device.
+#include <mutex>
+
+#include "csa_internal.cuh"
+
+namespace {
+
+constexpr size_t kMaxScores = CSA_NOALLOC_MAX_SCORES;
+
+// Score scratch for calls that bring no workspace: kMaxScores FP32 entries
+// (4 MiB), resident on every GPU that loads the library until the process
+// exits.  Host code must not pass this symbol to a kernel: its device address
+// comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) float g_noalloc_scores[kMaxScores];
+
+std::mutex g_mu;
+float *g_ptr[64] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current).  Returns nullptr on failure.
+float *scratch_for_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scores) != cudaSuccess || !p) return nullptr;
+    g_ptr[dev] = static_cast<float *>(p);
+  }
+  return g_ptr[dev];
+}
+
+}  // namespace
+
+using namespace csa;
+
+extern "C" CSA_API csa_status_t csa_index_topk_noalloc(csa_index_args *a, csa_stream_t stream) {
+  if (!a || a->struct_size < sizeof(csa_index_args)) return CSA_ERR_INVALID_ARG;
+  if (a->n_rows < 0 || a->n_req < 0) return CSA_ERR_INVALID_ARG;
+  if (a->n_heads != kHeads || a->head_dim != kIdxDim) return CSA_ERR_UNSUPPORTED;
+  if (a->topk < 1 || a->topk > CSA_MAX_TOPK || a->ratio < 1 || a->max_blocks <= 0)
+    return CSA_ERR_INVALID_ARG;
+  const long long n_cap = (long long)a->max_blocks * kBlock;
+  // only the single-CTA top-k (rows of at most 8192 entries) runs without
+  // further scratch; the scores must fit the static array
+  if (topk_is_long((int)n_cap)) return CSA_ERR_UNSUPPORTED;
+  const bool own_scores = a->scores != nullptr;
+  if (own_scores && a->score_cols < n_cap) return CSA_ERR_INVALID_ARG;
+  if (!own_scores && (long long)a->n_rows * n_cap > (long long)kMaxScores)
+    return CSA_ERR_UNSUPPORTED;
+  if (a->n_rows == 0) return CSA_OK;
+  if (!a->q_idx || !a->weights || !a->row_req || !a->row_pos || !a->n_cmp || !a->idx_pool ||
+      !a->idx_scale_pool || !a->cmp_block_table || !a->topk_idx)
+    return CSA_ERR_INVALID_ARG;
+  if (a->n_req <= 0 || a->n_blocks <= 0) return CSA_ERR_INVALID_ARG;
+  if ((a->rope_cos == nullptr) != (a->rope_sin == nullptr)) return CSA_ERR_INVALID_ARG;
+  if (a->rope_cos && a->rope_cap <= 0) return CSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(a->idx_pool) & 15u) ||
+      (reinterpret_cast<uintptr_t>(a->q_idx) & 15u) ||
+      (reinterpret_cast<uintptr_t>(a->idx_scale_pool) & 15u))
+    return CSA_ERR_INVALID_ARG;
+  float *scores = a->scores;
+  int cols = a->score_cols;
+  if (!own_scores) {
+    scores = scratch_for_current_device();
+    if (!scores) return CSA_ERR_CUDA;
+    cols = (int)n_cap;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // entries past a row's visible count are never read, so the scratch needs no
+  // clearing between calls
+  if (launch_index_scores(*a, scores, cols, nullptr, s) != cudaSuccess) return CSA_ERR_CUDA;
+  return launch_index_topk(*a, scores, cols, nullptr, s) == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+}
