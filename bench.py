@@ -240,7 +240,7 @@ def _src_sha(name):
         return None
 
 
-KERNEL_SRC = {"index_score": "k_index.cu", "index_topk": "k_index.cu",
+KERNEL_SRC = {"index_score": "k_index_tc.cu", "index_topk": "k_index.cu",
               "attn_partial": "k_attn.cu", "attn_combine": "k_attn.cu",
               "attn_prefill": "k_attn.cu", "compress_gate": "k_compress.cu",
               "compress_pool": "k_compress.cu"}

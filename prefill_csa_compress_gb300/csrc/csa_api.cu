@@ -118,6 +118,7 @@ csa_status_t run_attn(csa_attn_args *a, cudaStream_t s, bool decode) {
   if (a->n_rows == 0) return CSA_OK;
   st = check_attn_args(a);
   if (st != CSA_OK) return st;
+  if (!decode && attn_prefill_supported(*a)) return from_cuda(launch_attn_prefill(*a, s));
   return from_cuda(launch_attn(*a, n_splits, tps, static_cast<float *>(a->workspace), s));
 }
 

@@ -28,8 +28,11 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Launchers (one per kernel family); each returns cudaGetLastError().
 cudaError_t launch_compress(const csa_compress_args &a, float *logits, cudaStream_t s);
-// `zero_ctr` (n_rows words, may be null) is cleared by the scoring kernel for
-// the top-k kernel that follows it on the stream.
+// Words per row of the long-row top-k control block (barrier counter and
+// three digit histograms).
+constexpr int kTopkCtlWords = 32 + 2048 + 2048 + 1024;
+// `zero_ctr` (n_rows x kTopkCtlWords words, may be null) is cleared by the
+// scoring kernel for the top-k kernel that follows it on the stream.
 cudaError_t launch_index_scores(const csa_index_args &a, float *scores, int score_cols,
                                 uint32_t *zero_ctr, cudaStream_t s);
 cudaError_t launch_index_topk(const csa_index_args &a, const float *scores, int score_cols,
@@ -37,6 +40,10 @@ cudaError_t launch_index_topk(const csa_index_args &a, const float *scores, int 
 bool topk_is_long(int n_cap);
 size_t topk_ws_bytes(int n_rows, int n_cap);
 uint32_t *topk_counters(void *ws, int n_rows, int n_cap);
+// The persistent prefill kernel (k_attn_prefill.cu) covers top-k sizes that
+// are multiples of 4; other shapes take the split kernel with one split.
+bool attn_prefill_supported(const csa_attn_args &a);
+cudaError_t launch_attn_prefill(const csa_attn_args &a, cudaStream_t s);
 cudaError_t launch_attn(const csa_attn_args &a, int n_splits, int tiles_per_split,
                         float *partials, cudaStream_t s);
 

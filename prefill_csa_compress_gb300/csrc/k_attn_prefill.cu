@@ -1,0 +1,666 @@
+// Prefill shared-KV sparse attention with an attention sink: a persistent,
+// warp-specialised tcgen05 pipeline.  Same function as the split kernel in
+// k_attn.cu ("Hyper-Parallel ... DeepSeek V4 CP" (gitcode issue #2),
+// "二阶段 CP 总体算法": Stage-2 sparse attention with sinks, softmax_scale and
+// ori_win_left = 127, outputs out and lse; "9.1": the candidates are the
+// selected compressed entries followed by the raw causal window; "7. Window KV
+// Halo": the window includes the query's own position).
+//
+// One CTA per SM walks query rows; per row the candidates are processed in
+// tiles of 128 with the candidates on the MMA's M side and the 64 heads on N:
+//   S^T[c, h]  = K[c, :] . q_h              (A = gathered tile, K-major)
+//   O^T[d, h] += sum_c K[c, d] P[c, h]      (A = same tile read MN-major)
+// Roles:
+//   warps 0..2  producers: warp 0 loads the row's q with TMA; all three
+//               gather the candidate rows with 16-byte cp.async straight into
+//               the 128-byte-swizzled layout (eight lanes per 128-byte row
+//               slice, so each warp request covers whole sectors), up to four
+//               64-channel chunks in flight per thread; a chunk of the tile is
+//               refilled as soon as the previous tile's P.V has finished
+//               reading it;
+//   warp 3      MMA issuer (one elected lane);
+//   warps 4..11 softmax and epilogue: thread = (candidate, half of the heads).
+//               The running maximum per head only moves (and O^T is rescaled
+//               in TMEM) when a tile's logits exceed it by more than 2^8;
+//               checking that costs one barrier reduction per tile.  FP32
+//               denominators come from a warp reduce-scatter.  At the end of a
+//               row they normalise O^T out of TMEM and store the output.
+// TMEM: S^T in columns [0, 64), O^T (four 128-channel tiles) in [64, 320).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+#include "csa_internal.cuh"
+#include "tc.cuh"
+
+namespace csa {
+namespace {
+
+constexpr int AP_THREADS = 384;
+constexpr int AP_PROD = 96;   // producer threads (warps 0..2)
+constexpr int AP_MMA_WARP = 3;
+constexpr int AP_SOFT = 256;  // softmax / epilogue threads (warps 4..11)
+constexpr int AP_BAR = 1;     // their named barrier
+constexpr int AP_PBAR = 2;    // the producers' named barrier
+constexpr int AP_LOOKAHEAD = 3;  // chunks a producer thread keeps in flight beyond the newest
+constexpr int CT = 128;       // candidates per tile
+constexpr int S_COL = 0, O_COL = 64;
+constexpr uint32_t AP_TMEM_COLS = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;
+
+constexpr int OFF_Q = 0;                   // 8 chunks x (64 heads x 128 B)
+constexpr int OFF_KV = OFF_Q + 8 * 8192;   // 8 chunks x (128 cands x 128 B)
+constexpr int OFF_P = OFF_KV + 8 * 16384;  // P^T, MN-major: 128 cands x 64 heads
+constexpr int OFF_MISC = OFF_P + 16384;
+
+struct ApRow {
+  int t, p, b;
+  uint32_t tiles;  // bit g: tile g of the row's candidate list is processed
+};
+
+struct ApMisc {
+  uint64_t q_full, q_rot, q_empty, s_full, p_full, o_full, o_empty, mma_done;
+  uint64_t kv_full[8];
+  uint64_t kv_empty[4];  // one per pair of chunks (one 128-channel tile of P.V)
+  uint64_t mask_full[2];
+  uint32_t tmem_base;
+  int abort;
+  ApRow row[2];
+  uint32_t valid[2][CT / 4];  // one byte per candidate of the tile
+  int32_t tbl[64];            // the row's compressed-page table (up to 64 pages)
+  alignas(16) float m_s[kHeads];  // running reference per head (log2 domain)
+  alignas(16) float l_s[kHeads];  // running denominator per head
+  alignas(16) float corr_s[kHeads];
+  alignas(16) float inv_s[kHeads];
+  alignas(16) float red[4][kHeads];
+  alignas(16) float red_l[4][kHeads];
+};
+constexpr int AP_SMEM = OFF_MISC + (int)sizeof(ApMisc) + 1024;
+static_assert(AP_SMEM <= 227 * 1024, "shared memory");
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool ap_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                        uint32_t *status) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = tc::global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (*abort) return false;
+      if (tc::global_ns() - t0 > 2000000000ull) {
+        *abort = 1;
+        flag(status, CSA_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2(float x, float y) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(x, y);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// P^T row c (one candidate): 64 heads as 8 swizzled 16-byte chunks.
+__device__ __forceinline__ uint8_t *prow_chunk(uint8_t *P, int c, int j) {
+  return P + (c >> 3) * 1024 + (c & 7) * 128 + ((j ^ (c & 7)) << 4);
+}
+
+// Column-wise reduction of x[0..31] over the 32 lanes (reduce-scatter):
+// afterwards lane l holds the reduction of column l.
+template <bool MAX>
+__device__ __forceinline__ float warp_col_reduce32(const float (&x)[32]) {
+  const int lane = threadIdx.x & 31;
+  float a[16];
+  {
+    const bool up = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float keep = up ? x[16 + i] : x[i], send = up ? x[i] : x[16 + i];
+      const float o = __shfl_xor_sync(0xffffffffu, send, 16);
+      a[i] = MAX ? fmaxf(keep, o) : keep + o;
+    }
+  }
+  float b[8];
+  {
+    const bool up = lane & 8;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float keep = up ? a[8 + i] : a[i], send = up ? a[i] : a[8 + i];
+      const float o = __shfl_xor_sync(0xffffffffu, send, 8);
+      b[i] = MAX ? fmaxf(keep, o) : keep + o;
+    }
+  }
+  float c[4];
+  {
+    const bool up = lane & 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float keep = up ? b[4 + i] : b[i], send = up ? b[i] : b[4 + i];
+      const float o = __shfl_xor_sync(0xffffffffu, send, 4);
+      c[i] = MAX ? fmaxf(keep, o) : keep + o;
+    }
+  }
+  float d[2];
+  {
+    const bool up = lane & 2;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float keep = up ? c[2 + i] : c[i], send = up ? c[i] : c[2 + i];
+      const float o = __shfl_xor_sync(0xffffffffu, send, 2);
+      d[i] = MAX ? fmaxf(keep, o) : keep + o;
+    }
+  }
+  const bool up = lane & 1;
+  const float keep = up ? d[1] : d[0], send = up ? d[0] : d[1];
+  const float o = __shfl_xor_sync(0xffffffffu, send, 1);
+  return MAX ? fmaxf(keep, o) : keep + o;
+}
+
+__device__ __forceinline__ void load32(const float *src, float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 f = reinterpret_cast<const float4 *>(src)[i];
+    v[4 * i] = f.x;
+    v[4 * i + 1] = f.y;
+    v[4 * i + 2] = f.z;
+    v[4 * i + 3] = f.w;
+  }
+}
+
+__global__ void __launch_bounds__(AP_THREADS, 1)
+    attn_prefill_kernel(csa_attn_args a, const __grid_constant__ CUtensorMap qmap,
+                        const __grid_constant__ CUtensorMap cmap,
+                        const __grid_constant__ CUtensorMap kmap) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~uintptr_t(1023));
+  uint8_t *Qs = sm + OFF_Q;
+  uint8_t *KVs = sm + OFF_KV;
+  uint8_t *Ps = sm + OFF_P;
+  ApMisc *M = reinterpret_cast<ApMisc *>(sm + OFF_MISC);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_cand = a.topk + a.window;
+  volatile int *abort = &M->abort;
+
+  if (tid == 0) {
+    tc::mbar_init(&M->q_full, 1);
+    tc::mbar_init(&M->q_rot, 1);
+    tc::mbar_init(&M->q_empty, 1);
+    tc::mbar_init(&M->s_full, 1);
+    tc::mbar_init(&M->p_full, 1);
+    tc::mbar_init(&M->o_full, 1);
+    tc::mbar_init(&M->o_empty, 1);
+    tc::mbar_init(&M->mma_done, 1);
+    for (int i = 0; i < 8; ++i) tc::mbar_init(&M->kv_full[i], AP_PROD);
+    for (int i = 0; i < 4; ++i) tc::mbar_init(&M->kv_empty[i], 1);
+    for (int i = 0; i < 2; ++i) tc::mbar_init(&M->mask_full[i], AP_PROD);
+    M->abort = 0;
+    tc::mbar_fence_init();
+  }
+  if (tid < kHeads) {
+    M->m_s[tid] = -INFINITY;
+    M->l_s[tid] = 0.f;
+  }
+  if (warp == AP_MMA_WARP) tc::tmem_alloc(&M->tmem_base, AP_TMEM_COLS);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = M->tmem_base;
+
+  if (warp < 3) {
+    // ================================================================ producers
+    const int pw = warp;                  // 0..2
+    const int ptid = tid;                 // 0..95
+    const int sub = lane >> 3, piece = lane & 7;
+    // The three producer warps run the same loops to the end even after an
+    // abort (work is skipped, not the loops), so their named barriers match.
+    uint32_t row_it = 0, tile_it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < a.n_rows; t += gridDim.x) {
+      const int b = a.row_req[t];
+      if (b < 0) continue;
+      if (b >= a.n_req) {
+        if (ptid == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
+        continue;
+      }
+      const int p = a.row_pos[t];
+      const int V = min(visible_count(p, a.ratio, a.n_cmp[b]), a.cmp_max_blocks * kBlock);
+      const int kvl = a.kv_len[b];
+      const int32_t *sel = a.topk_idx + (long long)t * a.topk;
+      // the row's compressed-page table, read once (tables of up to 64 pages)
+      const bool cache_tbl = a.cmp_max_blocks <= 64;
+      tc::bar_sync(AP_PBAR, AP_PROD);  // every producer is done with the previous row
+      if (cache_tbl)
+        for (int i = ptid; i < a.cmp_max_blocks; i += AP_PROD)
+          M->tbl[i] = a.cmp_block_table[(long long)b * a.cmp_max_blocks + i];
+      // tiles holding at least one candidate; out-of-range entries are flagged once
+      uint32_t tiles = 0;
+      for (int j0 = 0; j0 < n_cand; j0 += 32) {
+        const int j = j0 + lane;
+        bool v = false;
+        if (j < a.topk) {
+          const int c = sel[j];
+          v = c >= 0 && c < V;
+          if (c >= V && pw == 0) flag(a.status_dev, CSA_DEV_BAD_INDEX);
+        } else if (j < n_cand) {
+          const int pp = p - a.window + 1 + (j - a.topk);
+          v = pp >= 0 && pp < kvl;
+          if (pp >= kvl && pw == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
+        }
+        if (__ballot_sync(0xffffffffu, v)) tiles |= 1u << (j0 / CT);
+      }
+      if (!tiles) tiles = 1u << ((n_cand - 1) / CT);  // an all-empty tile still yields out = 0
+      tc::bar_sync(AP_PBAR, AP_PROD);  // the page table is in place
+      if (pw == 0 && ok) {
+        ok = __all_sync(0xffffffffu, ap_wait(&M->q_empty, (row_it & 1) ^ 1, abort, a.status_dev));
+        if (ok && lane == 0) {
+          ApRow &R = M->row[row_it & 1];
+          R.t = t;
+          R.p = p;
+          R.b = b;
+          R.tiles = tiles;
+          tc::mbar_arrive_expect_tx(&M->q_full, 8 * 8192);
+          for (int kc = 0; kc < 8; ++kc)
+            tc::tma_load_2d(Qs + kc * 8192, &qmap, kc * 64, t * kHeads, &M->q_full);
+        }
+        __syncwarp();
+      }
+      for (uint32_t mm = tiles; mm; mm &= mm - 1) {
+        ok = ok && !*abort;
+        const int g0 = (__ffs(mm) - 1) * CT;
+        const int slot = tile_it & 1;
+        // rows of this thread: r = 4 * rg + sub for rg = pw, pw + 3, ... (< 32);
+        // eight lanes (one 16-byte piece each) share a row
+        const uint16_t *src[11];
+        uint32_t vmask = 0;
+#pragma unroll
+        for (int i = 0; i < 11; ++i) {
+          const int rg = pw + 3 * i;
+          src[i] = static_cast<const uint16_t *>(a.kv_pool);
+          if (rg >= 32) continue;
+          const int r = 4 * rg + sub, j = g0 + r;
+          long long row = -1;
+          const void *pool = a.kv_pool;
+          if (j < a.topk) {
+            pool = a.cmp_pool;
+            const int c = sel[j];
+            if (c >= 0 && c < V) {
+              if (cache_tbl) {
+                const int phys = M->tbl[c / kBlock];
+                if (phys >= 0 && phys < a.cmp_n_blocks)
+                  row = (long long)phys * kBlock + (c % kBlock);
+                else if (piece == 0)
+                  flag(a.status_dev, CSA_DEV_BAD_BLOCK);
+              } else {
+                row = page_row(a.cmp_block_table, a.cmp_max_blocks, a.cmp_n_blocks, b, c,
+                               piece == 0 ? a.status_dev : nullptr);
+              }
+            }
+          } else if (j < n_cand) {
+            const int pp = p - a.window + 1 + (j - a.topk);
+            if (pp >= 0 && pp < kvl)
+              row = page_row(a.kv_block_table, a.kv_max_blocks, a.kv_n_blocks, b, pp,
+                             piece == 0 ? a.status_dev : nullptr);
+          }
+          if (row >= 0) {
+            src[i] = static_cast<const uint16_t *>(pool) + row * kHeadDim + piece * 8;
+            vmask |= 1u << i;
+          }
+          if (piece == 0) reinterpret_cast<uint8_t *>(M->valid[slot])[r] = row >= 0 ? 1 : 0;
+        }
+        if (ok) tc::mbar_arrive(&M->mask_full[slot]);
+        for (int kc = 0; kc < 8 && ok; ++kc) {
+          if ((kc & 1) == 0) {
+            ok = __all_sync(0xffffffffu, ap_wait(&M->kv_empty[kc >> 1], (tile_it & 1) ^ 1, abort,
+                                                 a.status_dev));
+            if (!ok) break;
+          }
+          uint8_t *dst = KVs + kc * 16384;
+#pragma unroll
+          for (int i = 0; i < 11; ++i) {
+            const int rg = pw + 3 * i;
+            if (rg >= 32) continue;
+            const int r = 4 * rg + sub;
+            tc::cp_async16_zfill(dst + r * 128 + ((piece ^ (r & 7)) << 4), src[i] + kc * 64,
+                                 (vmask >> i) & 1u);
+          }
+          tc::cp_async_commit();
+          if (kc >= AP_LOOKAHEAD) {
+            tc::cp_async_wait<AP_LOOKAHEAD>();
+            tc::fence_async_shared();
+            tc::mbar_arrive(&M->kv_full[kc - AP_LOOKAHEAD]);
+          }
+        }
+        tc::cp_async_wait<0>();
+        if (ok) {
+          tc::fence_async_shared();
+          for (int kc = 8 - AP_LOOKAHEAD; kc < 8; ++kc) tc::mbar_arrive(&M->kv_full[kc]);
+        }
+        ++tile_it;
+      }
+      ++row_it;
+    }
+    // copies in flight land before the CTA retires
+    tc::cp_async_wait<0>();
+    if (!ok && pw == 0) tc::mbar_wait(&M->q_full, (row_it - 1) & 1, 50000000ull);
+  } else if (warp == AP_MMA_WARP) {
+    // ================================================================ MMA issuer
+    constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, kHeads);
+    constexpr uint32_t idesc_pv = tc::idesc_bf16_f32_mn(128, kHeads);
+    const uint32_t kv = tc::smem_u32(KVs), qq = tc::smem_u32(Qs), pp = tc::smem_u32(Ps);
+    uint32_t row_it = 0, tile_it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < a.n_rows && ok; t += gridDim.x) {
+      const int b = a.row_req[t];
+      if (b < 0 || b >= a.n_req) continue;
+      ok = __all_sync(0xffffffffu, ap_wait(&M->q_full, row_it & 1, abort, a.status_dev));
+      if (!ok) break;
+      const uint32_t tiles = M->row[row_it & 1].tiles;
+      bool first = true;
+      for (uint32_t mm = tiles; mm && ok; mm &= mm - 1) {
+        const bool last = (mm & (mm - 1)) == 0;
+        for (int kc = 0; kc < 8; ++kc) {
+          ok = __all_sync(0xffffffffu, ap_wait(&M->kv_full[kc], tile_it & 1, abort, a.status_dev));
+          if (ok && first && kc == 7)
+            ok = __all_sync(0xffffffffu, ap_wait(&M->q_rot, row_it & 1, abort, a.status_dev));
+          if (!ok) break;
+          tc::tc_fence_after();
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            tc::mma_ss_elect(tmem + S_COL, tc::desc_sw128(kv + kc * 16384 + s * 32),
+                             tc::desc_sw128(qq + kc * 8192 + s * 32), idesc_qk,
+                             (kc | s) != 0 ? 1u : 0u);
+        }
+        if (!ok) break;
+        tc::mma_commit_elect(&M->s_full);
+        if (last) tc::mma_commit_elect(&M->q_empty);
+        if (first) {
+          ok = __all_sync(0xffffffffu,
+                          ap_wait(&M->o_empty, (row_it & 1) ^ 1, abort, a.status_dev));
+          if (!ok) break;
+        }
+        ok = __all_sync(0xffffffffu, ap_wait(&M->p_full, tile_it & 1, abort, a.status_dev));
+        if (!ok) break;
+        tc::tc_fence_after();
+        for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            tc::mma_ss_elect(tmem + O_COL + mt * 64,
+                             tc::desc_sw128_mn(kv + 2 * mt * 16384 + ks * 2048, 16384, 1024),
+                             tc::desc_sw128_mn(pp + ks * 2048, 16384, 1024), idesc_pv,
+                             (!first || ks > 0) ? 1u : 0u);
+          tc::mma_commit_elect(&M->kv_empty[mt]);
+        }
+        if (last) tc::mma_commit_elect(&M->o_full);
+        first = false;
+        ++tile_it;
+      }
+      ++row_it;
+    }
+    // every issued MMA has completed before TMEM is released
+    tc::mma_commit_elect(&M->mma_done);
+    tc::mbar_wait(&M->mma_done, 0, 100000000ull);
+  } else {
+    // ================================================================ softmax / epilogue
+    const int sw = warp - 4;                // 0..7
+    const int qd = warp & 3;                // TMEM lane quarter of this warp
+    const int h0 = (sw >> 2) * 32;          // first head of this thread's half
+    const int c = qd * 32 + lane;           // candidate = TMEM lane
+    const int stid = sw * 32 + lane;        // 0..255
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    const float sl2 = a.softmax_scale * kLog2e;
+    uint32_t row_it = 0, tile_it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < a.n_rows && ok; t += gridDim.x) {
+      const int b = a.row_req[t];
+      if (b < 0 || b >= a.n_req) continue;
+      ok = tc::bar_and(AP_BAR, AP_SOFT, ap_wait(&M->q_full, row_it & 1, abort, a.status_dev));
+      if (!ok) break;
+      const ApRow R = M->row[row_it & 1];
+      // ---- rotate q's last 64 channels at p (FP32, rounded to BF16) in place
+      bool rot = a.rope_cos != nullptr && R.p >= 0;
+      if (rot && R.p >= a.rope_cap) {
+        rot = false;
+        if (stid == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
+      }
+      if (rot) {
+        for (int e = stid; e < kHeads * 8; e += AP_SOFT) {
+          const int h = e >> 3, jj = e & 7;
+          uint4 *slot = reinterpret_cast<uint4 *>(Qs + 7 * 8192 + h * 128 + ((jj ^ (h & 7)) << 4));
+          const uint4 x4 = *slot;
+          uint32_t w[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int pair = jj * 4 + q;
+            const float cs = a.rope_cos[(long long)R.p * kRopeHalf + pair];
+            const float sn = a.rope_sin[(long long)R.p * kRopeHalf + pair];
+            const float x0 = __uint_as_float(w[q] << 16), x1 = __uint_as_float(w[q] & 0xFFFF0000u);
+            w[q] = pack2(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+          }
+          *slot = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        tc::fence_async_shared();
+      }
+      tc::bar_sync(AP_BAR, AP_SOFT);
+      if (stid == 0) tc::mbar_arrive(&M->q_rot);
+
+      bool first = true;
+      for (uint32_t mm = R.tiles; mm && ok; mm &= mm - 1) {
+        const int slot = tile_it & 1;
+        ok = tc::bar_and(AP_BAR, AP_SOFT,
+                         ap_wait(&M->mask_full[slot], (tile_it >> 1) & 1, abort, a.status_dev) &&
+                             ap_wait(&M->s_full, tile_it & 1, abort, a.status_dev));
+        if (!ok) break;
+        const bool valid = reinterpret_cast<const uint8_t *>(M->valid[slot])[c] != 0;
+        tc::tc_fence_after();
+        float x[32];
+        tc::tmem_ld32(tmem + lane_off + S_COL + h0, x);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = valid ? x[j] * sl2 : -INFINITY;
+        float mref[32];
+        load32(M->m_s + h0, mref);
+        bool exceed = false;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) exceed |= x[j] > mref[j] + kRescaleLog2;
+        if (tc::bar_or(AP_BAR, AP_SOFT, exceed)) {
+          // move the reference of the heads whose maximum grew past 2^8
+          const float mx = warp_col_reduce32<true>(x);
+          const int h = h0 + lane;
+          M->red[qd][h] = mx;
+          tc::bar_sync(AP_BAR, AP_SOFT);
+          const float mt = fmaxf(fmaxf(M->red[0][h], M->red[1][h]), fmaxf(M->red[2][h], M->red[3][h]));
+          const float mo = M->m_s[h];
+          float mn = mo, corr = 1.f;
+          if (mo == -INFINITY) {
+            mn = mt;
+          } else if (mt > mo + kRescaleLog2) {
+            mn = mt;
+            corr = exp2f(mo - mt);
+          }
+          tc::bar_sync(AP_BAR, AP_SOFT);
+          if (qd == 0) {
+            M->m_s[h] = mn;
+            M->corr_s[h] = corr;
+            M->l_s[h] *= corr;
+          }
+          tc::bar_sync(AP_BAR, AP_SOFT);
+          load32(M->m_s + h0, mref);
+          if (!first) {
+            float cr[32];
+            load32(M->corr_s + h0, cr);
+            bool any = false;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) any |= cr[j] != 1.f;
+            if (__any_sync(0xffffffffu, any)) {
+#pragma unroll 1
+              for (int m4 = 0; m4 < 4; ++m4) {
+                float v[32];
+                const uint32_t addr = tmem + lane_off + O_COL + m4 * 64 + h0;
+                tc::tmem_ld32(addr, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] *= cr[j];
+                tc::tmem_st32(addr, v);
+              }
+            }
+          }
+        }
+        // ---- P = 2^(x - m) as BF16 into the MN-major P^T rows
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = mref[j] == -INFINITY ? 0.f : exp2f(x[j] - mref[j]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4 *>(prow_chunk(Ps, c, (h0 >> 3) + q)) =
+              make_uint4(pack2(x[8 * q], x[8 * q + 1]), pack2(x[8 * q + 2], x[8 * q + 3]),
+                         pack2(x[8 * q + 4], x[8 * q + 5]), pack2(x[8 * q + 6], x[8 * q + 7]));
+        tc::fence_async_shared();
+        // FP32 denominators: per-head sums of the unrounded probabilities
+        const float sum = warp_col_reduce32<false>(x);
+        M->red_l[qd][h0 + lane] = sum;
+        tc::tc_fence_before();
+        tc::bar_sync(AP_BAR, AP_SOFT);
+        if (stid == 0) tc::mbar_arrive(&M->p_full);
+        if (qd == 0) {
+          const int h = h0 + lane;
+          M->l_s[h] += (M->red_l[0][h] + M->red_l[1][h]) + (M->red_l[2][h] + M->red_l[3][h]);
+        }
+        first = false;
+        ++tile_it;
+      }
+      if (!ok) break;
+
+      // ---- epilogue: out = O^T / L, lse = log L, with the sink in L
+      ok = tc::bar_and(AP_BAR, AP_SOFT, ap_wait(&M->o_full, row_it & 1, abort, a.status_dev));
+      if (!ok) break;
+      if (qd == 0) {
+        const int h = h0 + lane;
+        const float s2 = a.sink ? a.sink[h] * kLog2e : -INFINITY;
+        float m = M->m_s[h], l = M->l_s[h];
+        if (m == -INFINITY) {
+          m = s2;
+          l = 0.f;
+        }
+        const float L = (m == -INFINITY) ? 0.f : l + exp2f(s2 - m);
+        M->inv_s[h] = L > 0.f ? 1.f / L : 0.f;
+        if (a.lse) a.lse[(long long)R.t * kHeads + h] = L > 0.f ? (m + log2f(L)) * kLn2 : -INFINITY;
+      }
+      tc::bar_sync(AP_BAR, AP_SOFT);
+      float inv[32];
+      load32(M->inv_s + h0, inv);
+      const bool inv_rope = a.inv_rope_out && a.rope_cos != nullptr && R.p >= 0 && R.p < a.rope_cap;
+      __nv_bfloat16 *out =
+          static_cast<__nv_bfloat16 *>(a.out) + (long long)R.t * kHeads * kHeadDim;
+      tc::tc_fence_after();
+#pragma unroll 1
+      for (int m4 = 0; m4 < 4; ++m4) {
+        float v[32];
+        tc::tmem_ld32(tmem + lane_off + O_COL + m4 * 64 + h0, v);
+        const int d = m4 * 128 + qd * 32 + lane;
+        float cs = 1.f, sn = 0.f;
+        if (inv_rope && d >= kHeadDim - kRopeDim) {
+          const int pair = (d - (kHeadDim - kRopeDim)) >> 1;
+          cs = a.rope_cos[(long long)R.p * kRopeHalf + pair];
+          sn = a.rope_sin[(long long)R.p * kRopeHalf + pair];
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float o = v[j] * inv[j];
+          if (inv_rope && m4 == 3 && qd >= 2) {  // channels 448.. of the last tile
+            const float other = __shfl_xor_sync(0xffffffffu, o, 1);
+            o = (d & 1) ? (-other * sn + o * cs) : (o * cs + other * sn);
+          }
+          out[(h0 + j) * kHeadDim + d] = __float2bfloat16_rn(o);
+        }
+      }
+      tc::tc_fence_before();
+      tc::bar_sync(AP_BAR, AP_SOFT);
+      if (stid == 0) tc::mbar_arrive(&M->o_empty);
+      if (qd == 0) {
+        M->m_s[h0 + lane] = -INFINITY;
+        M->l_s[h0 + lane] = 0.f;
+      }
+      ++row_it;
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == AP_MMA_WARP) tc::tmem_dealloc(tmem, AP_TMEM_COLS);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return nullptr;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return encode;
+}
+
+// 2D BF16 tensor map [rows, 512] with a row stride of 1024 bytes, box
+// {64 channels, box_rows}, 128-byte swizzle.
+bool encode_rows_map(CUtensorMap *map, const void *base, long long rows, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode || rows <= 0 || rows > 0x7FFFFFFFll) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool attn_prefill_supported(const csa_attn_args &a) {
+  return a.topk % 4 == 0 && a.window % 4 == 0 && a.topk + a.window <= 32 * CT &&
+         (a.topk == 0 || a.cmp_n_blocks > 0) && a.kv_n_blocks > 0;
+}
+
+cudaError_t launch_attn_prefill(const csa_attn_args &a, cudaStream_t s) {
+  if (a.n_rows <= 0) return cudaSuccess;
+  CUtensorMap qmap, cmap, kmap;
+  memset(&qmap, 0, sizeof(qmap));
+  memset(&cmap, 0, sizeof(cmap));
+  memset(&kmap, 0, sizeof(kmap));
+  if (!encode_rows_map(&qmap, a.q, (long long)a.n_rows * kHeads, kHeads) ||
+      !encode_rows_map(&kmap, a.kv_pool, (long long)a.kv_n_blocks * kBlock, 1))
+    return cudaErrorInvalidValue;
+  if (a.topk > 0) {
+    if (!encode_rows_map(&cmap, a.cmp_pool, (long long)a.cmp_n_blocks * kBlock, 1))
+      return cudaErrorInvalidValue;
+  } else {
+    cmap = kmap;
+  }
+  static bool attr[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr[dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AP_SMEM);
+    if (e != cudaSuccess) return e;
+    attr[dev] = true;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 148;
+  const int grid = a.n_rows < sms ? a.n_rows : sms;
+  launch_begin(CSA_K_ATTN_PREFILL, s);
+  attn_prefill_kernel<<<grid, AP_THREADS, AP_SMEM, s>>>(a, qmap, cmap, kmap);
+  launch_end(CSA_K_ATTN_PREFILL, s);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

@@ -5,13 +5,19 @@
 // logical-position ordering and trailing -1; "Hyper-Parallel ... DeepSeek V4
 // CP", "10.3 Causal mask" for the visible range).
 //
-// Scores become order-preserving 32-bit keys.  Rows up to 8192 entries are
-// selected by one CTA in shared memory (4-digit radix select, then an
-// ordered compaction).  Longer rows are split over S CTAs of a cooperative
-// launch: each slice histograms the top 11 key bits, the CTAs of a row meet
-// at a bounded barrier, every slice marks its certain winners in a bitmap
-// and spills the entries of the threshold bin, and the row's first CTA
-// resolves those exactly and compacts the bitmap into ascending positions.
+// Scores become order-preserving 32-bit keys, held in registers (each thread
+// owns a contiguous run of positions).  A three-digit radix select (11, 11
+// and 10 key bits) finds the k-th largest key T and how many keys equal to T
+// are taken; equal keys are taken in ascending position.  Rows up to 8192
+// entries are selected by one CTA.  Longer rows are split into S slices, the
+// CTAs of a cooperative launch: each slice adds its digit histogram into the
+// row's histogram in global memory and the slices meet at a bounded barrier
+// per digit.  At the last digit every slice also publishes the suffix sums of
+// its own histogram, so that each slice can work out, without a further
+// barrier, how many entries the slices before it emit; it then writes its
+// winners in ascending position order at that offset.
+#include <algorithm>
+
 #include "csa_internal.cuh"
 #include "tc.cuh"
 
@@ -54,127 +60,28 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *
   return base + x - v;
 }
 
-// Warp 0 finds, scanning digits from the top, the digit d whose cumulative
-// count first reaches `remaining`; returns d and the count above it.
-__device__ __forceinline__ void warp_find_digit(const uint32_t *hist, int n_digits, int remaining,
-                                                int *digit, int *above) {
-  const int lane = threadIdx.x & 31;
-  int cum = 0, sel = -1, before = 0;
-  for (int base = n_digits - 1; base >= 0 && sel < 0; base -= 32) {
-    const int cnt = (int)hist[base - lane];
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, cum + incl >= remaining);
-    if (hit) {
-      const int l = __ffs(hit) - 1;
-      sel = base - l;
-      before = cum + __shfl_sync(0xffffffffu, incl - cnt, l);
-    } else {
-      cum += __shfl_sync(0xffffffffu, incl, 31);
-    }
-  }
-  *digit = sel < 0 ? 0 : sel;
-  *above = before;
+// ---------------------------------------------------------------- radix select
+
+constexpr int TK_SHORT_KPT = 16;  // one CTA per row: rows up to 512 x 16 entries
+constexpr int TK_LONG_THREADS = 512;
+constexpr int TK_LONG_KPT = 32;   // entries per thread of a long-row slice
+constexpr int TK_B1 = 2048, TK_B2 = 2048, TK_B3 = 1024;  // 11 + 11 + 10 key bits
+constexpr int TK_CTL_HDR = 32;  // barrier counter, alone in its 128-byte line
+static_assert(TK_CTL_HDR + TK_B1 + TK_B2 + TK_B3 == kTopkCtlWords, "row control block");
+constexpr int TK_REC_WORDS = 1056;  // per slice: suffix counts [0, 1024] and the count above
+constexpr int TK_REC_GT = 1025;     // the 22-bit prefix, at word 1025
+
+// Dynamic shared memory of a CTA of NT threads: one first-digit histogram per
+// warp (the first digit is the most crowded: keep warps off each other's
+// counters) and the CTA's histogram.
+template <int NT>
+constexpr int topk_smem_bytes() {
+  return (NT / 32 + 1) * TK_B1 * 4;
 }
 
-// ---------------------------------------------------------------- short rows
-
-constexpr int SR_THREADS = 256;
-constexpr int SR_MAX = 8192;
-
-__global__ void __launch_bounds__(SR_THREADS) topk_short_kernel(csa_index_args a,
-                                                                const float *__restrict__ scores,
-                                                                int cols) {
-  __shared__ uint32_t keys[SR_MAX];
-  __shared__ uint32_t hist[256];
-  __shared__ int warp_sums[32];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_rem;
-  const int t = blockIdx.x;
-  const int b = a.row_req[t];
-  if (b < 0 || b >= a.n_req) return;
-  const int V = min(min(visible_count(a.row_pos[t], a.ratio, a.n_cmp[b]), a.max_blocks * kBlock),
-                    SR_MAX);
-  const int k = a.topk;
-  int32_t *out = a.topk_idx + (long long)t * k;
-  float *out_s = a.topk_score ? a.topk_score + (long long)t * k : nullptr;
-  const float *sc = scores + (long long)t * cols;
-  if (V <= k) {
-    for (int i = threadIdx.x; i < k; i += SR_THREADS) {
-      out[i] = i < V ? i : -1;
-      if (out_s) out_s[i] = i < V ? sc[i] : -INFINITY;
-    }
-    return;
-  }
-  for (int c = threadIdx.x; c < V; c += SR_THREADS) keys[c] = order_key(sc[c]);
-  // radix select of the k-th largest key, 4 digits of 8 bits
-  uint32_t prefix = 0, mask = 0;
-  int remaining = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += SR_THREADS) hist[i] = 0;
-    __syncthreads();
-    for (int c = threadIdx.x; c < V; c += SR_THREADS) {
-      const uint32_t key = keys[c];
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      int d, above;
-      warp_find_digit(hist, 256, remaining, &d, &above);
-      if (threadIdx.x == 0) {
-        s_prefix = prefix | ((uint32_t)d << shift);
-        s_rem = remaining - above;
-      }
-    }
-    __syncthreads();
-    prefix = s_prefix;
-    remaining = s_rem;
-    mask |= 255u << shift;
-  }
-  const uint32_t T = prefix;  // the k-th largest key; `remaining` equal keys are taken
-  int eq_base = 0, sel_base = 0;
-  for (int c0 = 0; c0 < V; c0 += SR_THREADS) {
-    const int c = c0 + threadIdx.x;
-    const uint32_t key = c < V ? keys[c] : 0u;
-    const int gt = (c < V && key > T) ? 1 : 0;
-    const int eq = (c < V && key == T) ? 1 : 0;
-    int eq_total, sel_total;
-    const int eq_rank = eq_base + block_exclusive_scan(eq, warp_sums, &eq_total);
-    const int sel = gt | (eq && eq_rank < remaining);
-    const int pos = sel_base + block_exclusive_scan(sel, warp_sums, &sel_total);
-    if (sel && pos < k) {
-      out[pos] = c;
-      if (out_s) out_s[pos] = sc[c];
-    }
-    eq_base += eq_total;
-    sel_base += sel_total;
-  }
-  for (int i = sel_base + threadIdx.x; i < k; i += SR_THREADS) {
-    out[i] = -1;
-    if (out_s) out_s[i] = -INFINITY;
-  }
-}
-
-// ---------------------------------------------------------------- long rows
-
-constexpr int LR_THREADS = 512;
-constexpr int LR_BINS = 2048;  // top 11 key bits
-constexpr int LR_TIE_SMEM = 4096;
-
-struct LongWs {
-  uint32_t *hist_part;  // [rows][S][2048]
-  uint32_t *tie_count;  // [rows][S]
-  uint64_t *ties;       // [rows][S][slice]  (key << 32 | ~position)
-  uint32_t *bitmap;     // [rows][n_cap / 32]
-  uint32_t *counters;   // [rows], zeroed by the scoring kernel
-};
-
-// Barrier of the S CTAs that share a row.  Waits at most ~1 s; returns false
-// (and flags CSA_DEV_TIMEOUT) when it gives up.
+// Barrier of the S CTAs that share a row: the counter only grows, barrier j
+// waits for j*S arrivals.  Waits at most ~1 s; returns false (and flags
+// CSA_DEV_TIMEOUT) when it gives up.
 __device__ bool row_barrier(uint32_t *ctr, uint32_t target, uint32_t *status, int *s_ok) {
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -188,7 +95,7 @@ __device__ bool row_barrier(uint32_t *ctr, uint32_t target, uint32_t *status, in
         flag(status, CSA_DEV_TIMEOUT);
         break;
       }
-      __nanosleep(64);
+      __nanosleep(32);
     }
     __threadfence();
     *s_ok = ok;
@@ -197,45 +104,57 @@ __device__ bool row_barrier(uint32_t *ctr, uint32_t target, uint32_t *status, in
   return *s_ok != 0;
 }
 
-// Radix select of the `need` largest 64-bit composites among the ties (the
-// composites are unique since positions differ); returns the smallest taken.
-template <typename Visit>
-__device__ uint64_t select_ties(int need, uint32_t *hist, int *s_digit, int *s_rem, Visit visit) {
-  uint64_t prefix = 0, mask = 0;
-  int remaining = need;
-  for (int shift = 56; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += LR_THREADS) hist[i] = 0;
-    __syncthreads();
-    visit([&](uint64_t v) {
-      if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & 255u], 1u);
-    });
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      int d, above;
-      warp_find_digit(hist, 256, remaining, &d, &above);
-      if (threadIdx.x == 0) {
-        *s_digit = d;
-        *s_rem = remaining - above;
-      }
-    }
-    __syncthreads();
-    prefix |= (uint64_t)(*s_digit) << shift;
-    remaining = *s_rem;
-    mask |= (uint64_t)255 << shift;
-    __syncthreads();
+// The digit d at which the count of keys with digit >= d (scanning from the
+// top) first reaches `remaining`, and the count strictly above d.  Every
+// thread takes nb / blockDim.x consecutive bins.
+__device__ __forceinline__ void block_find_digit(const uint32_t *hist, int nb, int remaining,
+                                                 int *warp_sums, int *s_digit, int *s_above) {
+  const int per = nb / (int)blockDim.x;
+  const int hi = nb - 1 - (int)threadIdx.x * per;
+  int local = 0;
+  for (int j = 0; j < per; ++j) local += (int)hist[hi - j];
+  if (threadIdx.x == 0) {
+    *s_digit = 0;
+    *s_above = 0;
   }
-  return prefix;
+  int total;
+  const int before = block_exclusive_scan(local, warp_sums, &total);
+  if (before < remaining && before + local >= remaining) {
+    int cum = before;
+    for (int j = 0; j < per; ++j) {
+      const int h = (int)hist[hi - j];
+      if (cum + h >= remaining) {
+        *s_digit = hi - j;
+        *s_above = cum;
+        break;
+      }
+      cum += h;
+    }
+  }
+  __syncthreads();
 }
 
-__global__ void __launch_bounds__(LR_THREADS) topk_long_kernel(csa_index_args a,
-                                                              const float *__restrict__ scores,
-                                                              int cols, LongWs ws, int S,
-                                                              int slice) {
-  __shared__ uint32_t hist[LR_BINS];
+// Score back from its order key (-0 comes back as +0).
+__device__ __forceinline__ float key_score(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// One CTA of NT threads per (slice, row).  MULTI: S > 1 slices per row meeting
+// at barriers through the row's control block `ctl` (zeroed by the scoring
+// kernel) and the per-slice records `rec`.
+template <int NT, int KPT, bool MULTI>
+__global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
+                                                        const float *__restrict__ scores, int cols,
+                                                        int row0, int S, int slice, uint32_t *ctl,
+                                                        uint32_t *rec) {
+  constexpr int NW = NT / 32;
+  extern __shared__ __align__(16) uint32_t tk_smem[];
+  uint32_t *priv = tk_smem;               // [NW][TK_B1]
+  uint32_t *hist = tk_smem + NW * TK_B1;  // [TK_B1]
   __shared__ int warp_sums[32];
-  __shared__ int s_ok, s_ntie, s_digit, s_rem;
-  __shared__ uint64_t tie_s[LR_TIE_SMEM];
-  const int t = blockIdx.y, s = blockIdx.x, tid = threadIdx.x;
+  __shared__ int s_digit, s_above, s_ok;
+  __shared__ int s_gt_before, s_eq_before;
+  const int t = row0 + blockIdx.y, s = blockIdx.x, tid = threadIdx.x, warp = tid >> 5;
   const int b = a.row_req[t];
   if (b < 0 || b >= a.n_req) return;  // uniform over the row's CTAs
   const int n_cap = a.max_blocks * kBlock;
@@ -246,145 +165,154 @@ __global__ void __launch_bounds__(LR_THREADS) topk_long_kernel(csa_index_args a,
   const float *sc = scores + (long long)t * cols;
   if (V <= k) {
     if (s == 0)
-      for (int i = tid; i < k; i += LR_THREADS) {
+      for (int i = tid; i < k; i += NT) {
         out[i] = i < V ? i : -1;
         if (out_s) out_s[i] = i < V ? sc[i] : -INFINITY;
       }
     return;
   }
   const int c_lo = s * slice, c_hi = min(V, c_lo + slice);
-  uint32_t *ctr = ws.counters + t;
+  const int c0 = c_lo + tid * KPT;
+  const int nv = max(0, min(KPT, c_hi - c0));
 
-  // ---- phase 1: histogram of this slice's top 11 key bits
-  for (int i = tid; i < LR_BINS; i += LR_THREADS) hist[i] = 0;
-  __syncthreads();
-  for (int c = c_lo + tid; c < c_hi; c += LR_THREADS)
-    atomicAdd(&hist[order_key(sc[c]) >> 21], 1u);
-  __syncthreads();
-  uint32_t *hp = ws.hist_part + ((long long)t * S + s) * LR_BINS;
-  for (int i = tid; i < LR_BINS; i += LR_THREADS) hp[i] = hist[i];
-  if (!row_barrier(ctr, (uint32_t)S, a.status_dev, &s_ok)) return;
+  // ---- keys of this thread's run of positions
+  uint32_t key[KPT];
+  if (nv == KPT && (reinterpret_cast<uintptr_t>(sc + c0) & 15u) == 0) {
+#pragma unroll
+    for (int i = 0; i < KPT; i += 4) {
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(sc + c0 + i));
+      key[i] = order_key(v.x);
+      key[i + 1] = order_key(v.y);
+      key[i + 2] = order_key(v.z);
+      key[i + 3] = order_key(v.w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) key[i] = i < nv ? order_key(__ldcg(sc + c0 + i)) : 0u;
+  }
 
-  // ---- phase 2: threshold bin b* of the row (same result in every CTA)
-  for (int i = tid; i < LR_BINS; i += LR_THREADS) {
-    uint32_t sum = 0;
-    for (int j = 0; j < S; ++j) sum += ws.hist_part[((long long)t * S + j) * LR_BINS + i];
-    hist[i] = sum;
-  }
-  __syncthreads();
-  if (tid < 32) {
-    int d, above;
-    warp_find_digit(hist, LR_BINS, k, &d, &above);
-    if (tid == 0) {
-      s_digit = d;
-      s_rem = k - above;  // entries of bin b* to take
-      s_ntie = 0;
+  uint32_t *row_ctl = MULTI ? ctl + (long long)t * kTopkCtlWords : nullptr;
+  int remaining = k;
+  uint32_t prefix = 0, pmask = 0;
+  int gt22 = 0;
+#pragma unroll 1
+  for (int j = 0; j < 3; ++j) {  // digit j: nb bins at `shift`
+    const int nb = j == 2 ? TK_B3 : TK_B1;
+    const int shift = j == 0 ? 21 : (j == 1 ? 10 : 0);
+    if (j == 0) {
+      uint4 *p4 = reinterpret_cast<uint4 *>(priv);
+      for (int i = tid; i < NW * TK_B1 / 4; i += NT) p4[i] = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      for (int i = tid; i < nb; i += NT) hist[i] = 0u;
     }
-  }
-  __syncthreads();
-  const uint32_t bstar = (uint32_t)s_digit;
-  const int need = s_rem;
-  // mark certain winners (bin > b*), spill the threshold bin
-  uint64_t *tie_g = ws.ties + ((long long)t * S + s) * slice;
-  uint32_t *bm = ws.bitmap + (long long)t * (n_cap / 32);
-  for (int w0 = c_lo; w0 < c_hi; w0 += 32 * LR_THREADS) {
-    const int c0 = w0 + tid * 32;
-    if (c0 < c_hi) {
-      uint32_t word = 0;
-#pragma unroll 4
-      for (int i = 0; i < 32; ++i) {
-        const int c = c0 + i;
-        if (c < c_hi) {
-          const uint32_t key = order_key(sc[c]);
-          const uint32_t bin = key >> 21;
-          if (bin > bstar) {
-            word |= 1u << i;
-          } else if (bin == bstar) {
-            const int slot = atomicAdd(&s_ntie, 1);
-            tie_g[slot] = ((uint64_t)key << 32) | (uint64_t)(~(uint32_t)c);
-          }
-        }
-      }
-      bm[c0 >> 5] = word;
-    }
-  }
-  __syncthreads();
-  if (tid == 0) ws.tie_count[(long long)t * S + s] = (uint32_t)s_ntie;
-  if (!row_barrier(ctr, (uint32_t)(2 * S), a.status_dev, &s_ok)) return;
-  if (s != 0) return;
-
-  // ---- phase 3 (first CTA of the row): exact choice inside the threshold bin
-  int n_tie = 0;
-  for (int j = 0; j < S; ++j) n_tie += (int)ws.tie_count[(long long)t * S + j];
-  auto each_tie_global = [&](auto &&f) {
-    for (int j = 0; j < S; ++j) {
-      const int nj = (int)ws.tie_count[(long long)t * S + j];
-      const uint64_t *src = ws.ties + ((long long)t * S + j) * slice;
-      for (int i = tid; i < nj; i += LR_THREADS) f(src[i]);
-    }
-  };
-  uint64_t cut;
-  if (n_tie <= LR_TIE_SMEM) {
-    int off = 0;
-    for (int j = 0; j < S; ++j) {
-      const int nj = (int)ws.tie_count[(long long)t * S + j];
-      const uint64_t *src = ws.ties + ((long long)t * S + j) * slice;
-      for (int i = tid; i < nj; i += LR_THREADS) tie_s[off + i] = src[i];
-      off += nj;
+    if (MULTI && j == 2) {
+      // keys above the 22-bit prefix, for the offsets of later slices
+      int c = 0;
+#pragma unroll
+      for (int i = 0; i < KPT; ++i) c += (i < nv && (key[i] >> 10) > (prefix >> 10)) ? 1 : 0;
+      int tot;
+      block_exclusive_scan(c, warp_sums, &tot);
+      gt22 = tot;
     }
     __syncthreads();
-    auto each_tie_smem = [&](auto &&f) {
-      for (int i = tid; i < n_tie; i += LR_THREADS) f(tie_s[i]);
-    };
-    cut = select_ties(need, hist, &s_digit, &s_rem, each_tie_smem);
-    each_tie_smem([&](uint64_t v) {
-      if (v >= cut) {
-        const uint32_t c = ~(uint32_t)(v & 0xFFFFFFFFu);
-        atomicOr(&bm[c >> 5], 1u << (c & 31));
+    if (j == 0) {
+      uint32_t *mine = priv + warp * TK_B1;
+#pragma unroll
+      for (int i = 0; i < KPT; ++i)
+        if (i < nv) atomicAdd(&mine[key[i] >> 21], 1u);
+      __syncthreads();
+      for (int i = tid; i < TK_B1; i += NT) {
+        uint32_t sum = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) sum += priv[w * TK_B1 + i];
+        hist[i] = sum;
       }
-    });
-  } else {
-    cut = select_ties(need, hist, &s_digit, &s_rem, each_tie_global);
-    each_tie_global([&](uint64_t v) {
-      if (v >= cut) {
-        const uint32_t c = ~(uint32_t)(v & 0xFFFFFFFFu);
-        atomicOr(&bm[c >> 5], 1u << (c & 31));
-      }
-    });
-  }
-  __threadfence_block();
-  __syncthreads();
-
-  // ---- ordered compaction of the bitmap: positions ascending
-  const int n_words = (V + 31) / 32;
-  const int per = (n_words + LR_THREADS - 1) / LR_THREADS;
-  const int w_lo = min(n_words, tid * per), w_hi = min(n_words, w_lo + per);
-  const uint32_t tail_mask = (V & 31) ? ((1u << (V & 31)) - 1u) : 0xFFFFFFFFu;
-  int cnt = 0;
-  for (int w = w_lo; w < w_hi; ++w) {
-    uint32_t word = bm[w];
-    if (w == n_words - 1) word &= tail_mask;
-    cnt += __popc(word);
-  }
-  int total;
-  int pos = block_exclusive_scan(cnt, warp_sums, &total);
-  for (int w = w_lo; w < w_hi; ++w) {
-    uint32_t word = bm[w];
-    if (w == n_words - 1) word &= tail_mask;
-    while (word) {
-      const int i = __ffs(word) - 1;
-      word &= word - 1;
-      const int c = w * 32 + i;
-      if (pos < k) {
-        out[pos] = c;
-        if (out_s) out_s[pos] = sc[c];
-      }
-      ++pos;
+    } else {
+#pragma unroll
+      for (int i = 0; i < KPT; ++i)
+        if (i < nv && (key[i] & pmask) == prefix) atomicAdd(&hist[(key[i] >> shift) & (nb - 1)], 1u);
     }
+    __syncthreads();
+    if (MULTI) {
+      uint32_t *g = row_ctl + TK_CTL_HDR + (j == 0 ? 0 : (j == 1 ? TK_B1 : TK_B1 + TK_B2));
+      for (int i = tid; i < nb; i += NT) {
+        const uint32_t v = hist[i];
+        if (v) atomicAdd(&g[i], v);
+      }
+      if (j == 2) {
+        // suffix sums of this slice's own last-digit histogram
+        static_assert(TK_B3 == 2 * NT || !MULTI, "two last-digit bins per thread");
+        uint32_t *r = rec + ((long long)t * S + s) * TK_REC_WORDS;
+        const int hi = TK_B3 - 1 - 2 * tid;
+        const int h0 = (int)hist[hi], h1 = (int)hist[hi - 1];
+        int tot;
+        const int before = block_exclusive_scan(h0 + h1, warp_sums, &tot);
+        r[hi] = (uint32_t)(before + h0);
+        r[hi - 1] = (uint32_t)(before + h0 + h1);
+        if (tid == 0) {
+          r[TK_B3] = 0u;
+          r[TK_REC_GT] = (uint32_t)gt22;
+        }
+      }
+      if (!row_barrier(row_ctl, (uint32_t)((j + 1) * S), a.status_dev, &s_ok)) return;
+      for (int i = tid; i < nb; i += NT) hist[i] = __ldcg(&g[i]);
+      __syncthreads();
+    }
+    block_find_digit(hist, nb, remaining, warp_sums, &s_digit, &s_above);
+    prefix |= (uint32_t)s_digit << shift;
+    pmask |= (uint32_t)(nb - 1) << shift;
+    remaining -= s_above;
   }
-  for (int i = total + tid; i < k; i += LR_THREADS) {
-    out[i] = -1;
-    if (out_s) out_s[i] = -INFINITY;
+  const uint32_t T = prefix;  // the k-th largest key; `remaining` keys equal to T are taken
+  const int d3 = (int)(T & (TK_B3 - 1));
+
+  // ---- entries of the slices before this one
+  int gt_before = 0, eq_before = 0;
+  if (MULTI) {
+    if (tid == 0) {
+      s_gt_before = 0;
+      s_eq_before = 0;
+    }
+    __syncthreads();
+    for (int j = tid; j < s; j += NT) {
+      const uint32_t *r = rec + ((long long)t * S + j) * TK_REC_WORDS;
+      const int above = (int)__ldcg(r + d3 + 1);
+      const int ge = (int)__ldcg(r + d3);
+      atomicAdd(&s_gt_before, (int)__ldcg(r + TK_REC_GT) + above);
+      atomicAdd(&s_eq_before, ge - above);
+    }
+    __syncthreads();
+    gt_before = s_gt_before;
+    eq_before = s_eq_before;
+  }
+  const int quota = max(0, remaining - eq_before);  // equal keys this slice may still take
+  const int offset = gt_before + min(remaining, eq_before);
+
+  // ---- ordered compaction: greater keys, then equal keys by ascending position
+  int n_gt = 0, n_eq = 0;
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    n_gt += (i < nv && key[i] > T) ? 1 : 0;
+    n_eq += (i < nv && key[i] == T) ? 1 : 0;
+  }
+  int tot;
+  const int eq_rank = block_exclusive_scan(n_eq, warp_sums, &tot);
+  const int take_eq = max(0, min(n_eq, quota - eq_rank));
+  int pos = offset + block_exclusive_scan(n_gt + take_eq, warp_sums, &tot);
+  int eq_seen = 0;
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    if (i < nv) {
+      bool take = key[i] > T;
+      if (key[i] == T) take = eq_seen++ < take_eq;
+      if (take) {
+        if (pos < k) {
+          out[pos] = c0 + i;
+          if (out_s) out_s[pos] = key_score(key[i]);
+        }
+        ++pos;
+      }
+    }
   }
 }
 
@@ -402,39 +330,60 @@ int device_sms() {
   return cached[dev];
 }
 
+constexpr int TK_SHORT_MAX = 512 * TK_SHORT_KPT;
+constexpr int TK_SLICE_MAX = TK_LONG_THREADS * TK_LONG_KPT;
+
+// Opt a kernel into more than 48 KB of dynamic shared memory, once per device.
+template <typename K>
+cudaError_t allow_smem(K kern, int bytes, bool *done) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (done[dev]) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
+}
+
+template <int NT>
+cudaError_t launch_short(const csa_index_args &a, const float *scores, int cols, cudaStream_t s) {
+  static bool done[64] = {};
+  const auto kern = topk_radix_kernel<NT, TK_SHORT_KPT, false>;
+  constexpr int smem = topk_smem_bytes<NT>();
+  cudaError_t e = allow_smem(kern, smem, done);
+  if (e != cudaSuccess) return e;
+  constexpr int kMaxGridY = 65535;
+  for (int row0 = 0; row0 < a.n_rows; row0 += kMaxGridY)
+    kern<<<dim3(1, std::min(kMaxGridY, a.n_rows - row0)), NT, smem, s>>>(
+        a, scores, cols, row0, 1, NT * TK_SHORT_KPT, nullptr, nullptr);
+  return cudaGetLastError();
+}
+
 struct LongLayout {
-  size_t hist, tie_count, ties, bitmap, counters, total;
+  size_t ctl, rec, total;
 };
 
-LongLayout long_layout(int n_rows, int n_cap, int S, int slice) {
+LongLayout long_layout(int n_rows, int S) {
   LongLayout L;
-  size_t off = 0;
-  L.hist = off;
-  off += align_up((size_t)n_rows * S * LR_BINS * 4, 256);
-  L.tie_count = off;
-  off += align_up((size_t)n_rows * S * 4, 256);
-  L.ties = off;
-  off += align_up((size_t)n_rows * S * slice * 8, 256);
-  L.bitmap = off;
-  off += align_up((size_t)n_rows * (n_cap / 32) * 4, 256);
-  L.counters = off;
-  off += align_up((size_t)n_rows * 4, 256);
-  L.total = off;
+  L.ctl = 0;
+  L.rec = align_up((size_t)n_rows * kTopkCtlWords * 4, 256);
+  L.total = L.rec + align_up((size_t)n_rows * S * TK_REC_WORDS * 4, 256);
   return L;
 }
 
 }  // namespace
 
-bool topk_is_long(int n_cap) { return n_cap > SR_MAX; }
+bool topk_is_long(int n_cap) { return n_cap > TK_SHORT_MAX; }
 
-// Slices per row for the long-row path: about one CTA per SM in total, each
-// slice a multiple of 32 entries (one bitmap word per thread step).
+// Slices per row for the long-row path: about one CTA per SM over the rows,
+// each slice a multiple of 32 entries and at most 512 x 32 entries.
 void topk_long_geometry(int n_rows, int n_cap, int *S, int *slice) {
-  int s = n_rows > 0 ? (148 + n_rows - 1) / n_rows : 1;
-  if (s < 1) s = 1;
-  if (s > 64) s = 64;
+  const int s_min = (n_cap + TK_SLICE_MAX - 1) / TK_SLICE_MAX;
+  int s = n_rows > 0 ? device_sms() / n_rows : 1;
+  if (s < s_min) s = s_min;
   int sl = (n_cap + s - 1) / s;
   sl = (sl + 31) / 32 * 32;
+  if (sl > TK_SLICE_MAX) sl = TK_SLICE_MAX;
   *S = (n_cap + sl - 1) / sl;
   *slice = sl;
 }
@@ -443,15 +392,12 @@ size_t topk_ws_bytes(int n_rows, int n_cap) {
   if (!topk_is_long(n_cap)) return 0;
   int S, slice;
   topk_long_geometry(n_rows, n_cap, &S, &slice);
-  return long_layout(n_rows, n_cap, S, slice).total;
+  return long_layout(n_rows, S).total;
 }
 
 uint32_t *topk_counters(void *ws, int n_rows, int n_cap) {
   if (!topk_is_long(n_cap)) return nullptr;
-  int S, slice;
-  topk_long_geometry(n_rows, n_cap, &S, &slice);
-  return reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) +
-                                      long_layout(n_rows, n_cap, S, slice).counters);
+  return reinterpret_cast<uint32_t *>(ws);
 }
 
 cudaError_t launch_index_topk(const csa_index_args &a, const float *scores, int score_cols,
@@ -459,39 +405,44 @@ cudaError_t launch_index_topk(const csa_index_args &a, const float *scores, int 
   if (a.n_rows <= 0) return cudaSuccess;
   const int n_cap = a.max_blocks * kBlock;
   if (!topk_is_long(n_cap)) {
+    // the smallest CTA whose threads hold a whole row, 16 entries each
     launch_begin(CSA_K_INDEX_TOPK, s);
-    topk_short_kernel<<<a.n_rows, SR_THREADS, 0, s>>>(a, scores, score_cols);
+    const cudaError_t e = n_cap <= 128 * TK_SHORT_KPT   ? launch_short<128>(a, scores, score_cols, s)
+                          : n_cap <= 256 * TK_SHORT_KPT ? launch_short<256>(a, scores, score_cols, s)
+                                                        : launch_short<512>(a, scores, score_cols, s);
     launch_end(CSA_K_INDEX_TOPK, s);
-    return cudaGetLastError();
+    return e;
   }
   int S, slice;
   topk_long_geometry(a.n_rows, n_cap, &S, &slice);
-  const LongLayout L = long_layout(a.n_rows, n_cap, S, slice);
+  const LongLayout L = long_layout(a.n_rows, S);
   uint8_t *base = static_cast<uint8_t *>(topk_ws);
-  LongWs ws;
-  ws.hist_part = reinterpret_cast<uint32_t *>(base + L.hist);
-  ws.tie_count = reinterpret_cast<uint32_t *>(base + L.tie_count);
-  ws.ties = reinterpret_cast<uint64_t *>(base + L.ties);
-  ws.bitmap = reinterpret_cast<uint32_t *>(base + L.bitmap);
-  ws.counters = reinterpret_cast<uint32_t *>(base + L.counters);
-  const dim3 grid(S, a.n_rows);
-  if (S > 1) {
-    // the CTAs of a row wait on one another: they must all be resident at once
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_long_kernel, LR_THREADS, 0) !=
-            cudaSuccess ||
-        (long long)S * a.n_rows > (long long)per_sm * device_sms())
-      return cudaErrorCooperativeLaunchTooLarge;
-  }
+  uint32_t *ctl = reinterpret_cast<uint32_t *>(base + L.ctl);
+  uint32_t *rec = reinterpret_cast<uint32_t *>(base + L.rec);
+  // the CTAs of a row wait on one another: a launch holds only as many rows
+  // as can be resident at once
+  const auto kern = topk_radix_kernel<TK_LONG_THREADS, TK_LONG_KPT, true>;
+  constexpr int smem = topk_smem_bytes<TK_LONG_THREADS>();
+  static bool done[64] = {};
+  cudaError_t e = allow_smem(kern, smem, done);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, TK_LONG_THREADS, smem);
+  if (e != cudaSuccess) return e;
+  const long long resident = (long long)per_sm * device_sms();
+  if (resident < S) return cudaErrorCooperativeLaunchTooLarge;
+  const int rows_per_launch = (int)std::min<long long>(a.n_rows, resident / S);
   csa_index_args aa = a;
   const float *sp = scores;
   int cols = score_cols;
-  void *args[] = {&aa, &sp, &cols, &ws, &S, &slice};
   launch_begin(CSA_K_INDEX_TOPK, s);
-  cudaError_t e = S > 1 ? cudaLaunchCooperativeKernel((const void *)topk_long_kernel, grid,
-                                                      dim3(LR_THREADS), args, 0, s)
-                        : cudaLaunchKernel((const void *)topk_long_kernel, grid,
-                                           dim3(LR_THREADS), args, 0, s);
+  for (int row0 = 0; row0 < a.n_rows && e == cudaSuccess; row0 += rows_per_launch) {
+    const int nr = std::min(rows_per_launch, a.n_rows - row0);
+    int r0 = row0, SS = S, sl = slice;
+    void *args[] = {&aa, &sp, &cols, &r0, &SS, &sl, &ctl, &rec};
+    e = cudaLaunchCooperativeKernel((const void *)kern, dim3(S, nr), dim3(TK_LONG_THREADS), args,
+                                    smem, s);
+  }
   launch_end(CSA_K_INDEX_TOPK, s);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

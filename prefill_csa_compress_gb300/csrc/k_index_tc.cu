@@ -137,8 +137,12 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   IdxMisc *M = reinterpret_cast<IdxMisc *>(sm + C::OFF_MISC);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  if (zero_ctr && blockIdx.x == 0)
-    for (int i = tid; i < a.n_rows; i += IT_THREADS) zero_ctr[i] = 0u;
+  if (zero_ctr) {
+    const long long n_words = (long long)a.n_rows * kTopkCtlWords;
+    for (long long i = (long long)blockIdx.x * IT_THREADS + tid; i < n_words;
+         i += (long long)gridDim.x * IT_THREADS)
+      zero_ctr[i] = 0u;
+  }
   const bool rope = a.rope_cos != nullptr;
   const int n_kchunks = rope ? 3 : 2;
   const int n_cap = a.max_blocks * kBlock;

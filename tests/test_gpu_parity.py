@@ -150,6 +150,11 @@ def test_compress_direct(n_rows, ratio, dx, d, out, with_gamma):
 # ------------------------------------------------------------------ indexer
 
 
+def _stable_topk(scores, k):
+    order = np.lexsort((np.arange(len(scores)), -scores.astype(np.float64)))
+    return np.sort(order[:k]).astype(np.int32)
+
+
 def _check_index_rows(wl, t, spec, step, rows, scores_dev):
     torch.cuda.synchronize()
     assert _status(step) == 0
@@ -169,6 +174,11 @@ def _check_index_rows(wl, t, spec, step, rows, scores_dev):
         floor = score_tolerance(_rope_q(wl.t, row), O.as_f64(wl.idx_w[row]), keys, scl)
         if sc_all is not None:
             tol = check_scores(sc_all[row, :V], ref, floor)
+            # the selection is exactly the (score desc, index asc) top-k of the
+            # scores the kernel computed
+            mine = _stable_topk(sc_all[row, :V], spec.topk)
+            assert np.array_equal(sel[row][:len(mine)], mine)
+            assert np.all(sel[row][len(mine):] == -1)
         else:
             tol = np.maximum(1e-4 * np.abs(ref), floor)
         n_clear += check_topk(sel[row], ref, tol, spec.topk)
@@ -212,6 +222,27 @@ def test_index_topk_full_size_sampled(name):
     step.index()
     torch.cuda.synchronize()
     assert torch.equal(sel_a, step.topk_idx)
+
+
+@pytest.mark.parametrize("ctx,topk", [([3000, 2500], 512), ([40000, 30000], 2048),
+                                      ([9000, 8500], 2048)])
+def test_index_topk_exact_ties(ctx, topk):
+    # three distinct key rows under one scale: each query row's scores take
+    # three values, so the cut falls inside a large group of equal scores and
+    # the smallest positions of that group must be taken (one CTA per row for
+    # the first case, rows split over many CTAs for the others)
+    spec = spec_for("ratio1_decode", ctx=ctx, chunk=[2, 2], topk=topk, seed=44)
+    wl = make_workload(spec)
+    pick = torch.from_numpy(np.random.default_rng(7).integers(0, 3, size=wl.idx_pool.shape[:2]))
+    base = wl.idx_pool[0, :3].clone()
+    wl.t["idx_pool"] = base[pick].contiguous()
+    wl.t["idx_scale"] = torch.full_like(wl.idx_scale, float(wl.idx_scale[0, 0]))
+    t = wl.to(DEV)
+    step = CsaStep(t, spec.ratio, spec.topk, compress=False)
+    n_cap = t["cmp_table"].shape[1] * BLOCK
+    scores = torch.empty((spec.n_rows, n_cap), device=DEV)
+    step.index(scores=scores)
+    _check_index_rows(wl, t, spec, step, range(spec.n_rows), scores)
 
 
 def test_index_topk_prefill_full_size_sampled():
