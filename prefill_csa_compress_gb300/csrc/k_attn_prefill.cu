@@ -11,18 +11,20 @@
 //   S^T[c, h]  = K[c, :] . q_h              (A = gathered tile, K-major)
 //   O^T[d, h] += sum_c K[c, d] P[c, h]      (A = same tile read MN-major)
 // Roles:
-//   warps 0..2  producers: warp 0 loads the row's q with TMA; all three
-//               gather the candidate rows with 16-byte cp.async straight into
-//               the 128-byte-swizzled layout (eight lanes per 128-byte row
-//               slice, so each warp request covers whole sectors), up to four
-//               64-channel chunks in flight per thread; a chunk of the tile is
-//               refilled as soon as the previous tile's P.V has finished
-//               reading it;
-//   warp 3      MMA issuer (one elected lane);
-//   warps 4..11 softmax and epilogue: thread = (candidate, half of the heads).
-//               The running maximum per head only moves (and O^T is rescaled
-//               in TMEM) when a tile's logits exceed it by more than 2^8;
-//               checking that costs one barrier reduction per tile.  FP32
+//   warp 0      producer: resolves each tile's candidates to pool-row
+//               addresses (a two-slot table in shared memory) and loads each
+//               row's q with TMA;
+//   warp 1      MMA issuer (one elected lane);
+//   warps 2..9  softmax, gather and epilogue; thread = (candidate, half of the
+//               heads).  Right after handing tile i's P to the MMA they gather
+//               tile i+1 with 16-byte cp.async straight into the
+//               128-byte-swizzled layout (eight lanes per 128-byte row slice,
+//               so each warp request covers whole sectors), all 128 KB in
+//               flight; a 64-channel chunk is refilled as soon as tile i's P.V
+//               has finished reading it, and the MMA starts on each chunk as
+//               it lands.  The running maximum per head only moves (and O^T is
+//               rescaled in TMEM) when a tile's logits exceed it by more than
+//               2^8; checking that costs one barrier reduction per tile.  FP32
 //               denominators come from a warp reduce-scatter.  At the end of a
 //               row they normalise O^T out of TMEM and store the output.
 // TMEM: S^T in columns [0, 64), O^T (four 128-channel tiles) in [64, 320).
@@ -37,13 +39,12 @@
 namespace csa {
 namespace {
 
-constexpr int AP_THREADS = 384;
-constexpr int AP_PROD = 96;   // producer threads (warps 0..2)
-constexpr int AP_MMA_WARP = 3;
-constexpr int AP_SOFT = 256;  // softmax / epilogue threads (warps 4..11)
+constexpr int AP_THREADS = 320;
+constexpr int AP_PROD_WARP = 0;
+constexpr int AP_MMA_WARP = 1;
+constexpr int AP_SOFT0 = 2;   // first softmax warp
+constexpr int AP_SOFT = 256;  // softmax / gather / epilogue threads (warps 2..9)
 constexpr int AP_BAR = 1;     // their named barrier
-constexpr int AP_PBAR = 2;    // the producers' named barrier
-constexpr int AP_LOOKAHEAD = 3;  // chunks a producer thread keeps in flight beyond the newest
 constexpr int CT = 128;       // candidates per tile
 constexpr int S_COL = 0, O_COL = 64;
 constexpr uint32_t AP_TMEM_COLS = 512;
@@ -65,14 +66,14 @@ struct ApMisc {
   uint64_t q_full, q_rot, q_empty, s_full, p_full, o_full, o_empty, mma_done;
   uint64_t kv_full[8];
   uint64_t kv_empty[4];  // one per pair of chunks (one 128-channel tile of P.V)
-  uint64_t mask_full[2];
+  uint64_t tab_full[2];   // the producer filled the tile's address table
+  uint64_t tab_empty[2];  // the gatherers have read it
   uint32_t tmem_base;
   int abort;
   ApRow row[2];
-  uint32_t valid[2][CT / 4];  // one byte per candidate of the tile
   int32_t tbl[64];            // the row's compressed-page table (up to 64 pages)
+  const uint16_t *src[2][CT];  // pool row of each candidate of the tile, or null
   alignas(16) float m_s[kHeads];  // running reference per head (log2 domain)
-  alignas(16) float l_s[kHeads];  // running denominator per head
   alignas(16) float corr_s[kHeads];
   alignas(16) float inv_s[kHeads];
   alignas(16) float red[4][kHeads];
@@ -172,9 +173,7 @@ __device__ __forceinline__ void load32(const float *src, float (&v)[32]) {
 }
 
 __global__ void __launch_bounds__(AP_THREADS, 1)
-    attn_prefill_kernel(csa_attn_args a, const __grid_constant__ CUtensorMap qmap,
-                        const __grid_constant__ CUtensorMap cmap,
-                        const __grid_constant__ CUtensorMap kmap) {
+    attn_prefill_kernel(csa_attn_args a, const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~uintptr_t(1023));
@@ -195,158 +194,141 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
     tc::mbar_init(&M->o_full, 1);
     tc::mbar_init(&M->o_empty, 1);
     tc::mbar_init(&M->mma_done, 1);
-    for (int i = 0; i < 8; ++i) tc::mbar_init(&M->kv_full[i], AP_PROD);
+    for (int i = 0; i < 8; ++i) tc::mbar_init(&M->kv_full[i], AP_SOFT);
     for (int i = 0; i < 4; ++i) tc::mbar_init(&M->kv_empty[i], 1);
-    for (int i = 0; i < 2; ++i) tc::mbar_init(&M->mask_full[i], AP_PROD);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&M->tab_full[i], 32);
+      tc::mbar_init(&M->tab_empty[i], AP_SOFT / 32);
+    }
     M->abort = 0;
     tc::mbar_fence_init();
   }
-  if (tid < kHeads) {
-    M->m_s[tid] = -INFINITY;
-    M->l_s[tid] = 0.f;
-  }
+  if (tid < kHeads) M->m_s[tid] = -INFINITY;
   if (warp == AP_MMA_WARP) tc::tmem_alloc(&M->tmem_base, AP_TMEM_COLS);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = M->tmem_base;
 
-  if (warp < 3) {
-    // ================================================================ producers
-    const int pw = warp;                  // 0..2
-    const int ptid = tid;                 // 0..95
-    const int sub = lane >> 3, piece = lane & 7;
-    // The three producer warps run the same loops to the end even after an
-    // abort (work is skipped, not the loops), so their named barriers match.
-    uint32_t row_it = 0, tile_it = 0;
+  // the rows this CTA serves: t = blockIdx.x + i * gridDim.x with a valid request
+  auto next_row = [&](int t) {
+    for (t += gridDim.x; t < a.n_rows; t += gridDim.x) {
+      const int b = a.row_req[t];
+      if (b >= 0 && b < a.n_req) return t;
+    }
+    return a.n_rows;
+  };
+  const int first_row = next_row((int)blockIdx.x - (int)gridDim.x);
+
+  if (warp == AP_PROD_WARP) {
+    // ================================================================ producer
+    uint32_t row_it = 0, tile_it = 0, q_loads = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < a.n_rows; t += gridDim.x) {
       const int b = a.row_req[t];
       if (b < 0) continue;
       if (b >= a.n_req) {
-        if (ptid == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
+        if (lane == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
         continue;
       }
+      if (!ok) break;
       const int p = a.row_pos[t];
       const int V = min(visible_count(p, a.ratio, a.n_cmp[b]), a.cmp_max_blocks * kBlock);
       const int kvl = a.kv_len[b];
       const int32_t *sel = a.topk_idx + (long long)t * a.topk;
       // the row's compressed-page table, read once (tables of up to 64 pages)
       const bool cache_tbl = a.cmp_max_blocks <= 64;
-      tc::bar_sync(AP_PBAR, AP_PROD);  // every producer is done with the previous row
+      __syncwarp();
       if (cache_tbl)
-        for (int i = ptid; i < a.cmp_max_blocks; i += AP_PROD)
+        for (int i = lane; i < a.cmp_max_blocks; i += 32)
           M->tbl[i] = a.cmp_block_table[(long long)b * a.cmp_max_blocks + i];
       // tiles holding at least one candidate; out-of-range entries are flagged once
-      uint32_t tiles = 0;
-      for (int j0 = 0; j0 < n_cand; j0 += 32) {
-        const int j = j0 + lane;
-        bool v = false;
-        if (j < a.topk) {
-          const int c = sel[j];
-          v = c >= 0 && c < V;
-          if (c >= V && pw == 0) flag(a.status_dev, CSA_DEV_BAD_INDEX);
-        } else if (j < n_cand) {
-          const int pp = p - a.window + 1 + (j - a.topk);
-          v = pp >= 0 && pp < kvl;
-          if (pp >= kvl && pw == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
+      uint32_t mine = 0;
+      for (int j0 = 0; j0 < a.topk; j0 += 16 * 32) {
+        int c[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int j = j0 + 32 * u + lane;
+          c[u] = j < a.topk ? sel[j] : -1;
         }
-        if (__ballot_sync(0xffffffffu, v)) tiles |= 1u << (j0 / CT);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int j = j0 + 32 * u + lane;
+          if (c[u] >= 0 && c[u] < V) mine |= 1u << (j / CT);
+          if (c[u] >= V) flag(a.status_dev, CSA_DEV_BAD_INDEX);
+        }
       }
+      for (int j = a.topk + lane; j < n_cand; j += 32) {
+        const int pp = p - a.window + 1 + (j - a.topk);
+        if (pp >= 0 && pp < kvl) mine |= 1u << (j / CT);
+        if (pp >= kvl) flag(a.status_dev, CSA_DEV_BAD_POS);
+      }
+      uint32_t tiles = __reduce_or_sync(0xffffffffu, mine);
       if (!tiles) tiles = 1u << ((n_cand - 1) / CT);  // an all-empty tile still yields out = 0
-      tc::bar_sync(AP_PBAR, AP_PROD);  // the page table is in place
-      if (pw == 0 && ok) {
-        ok = __all_sync(0xffffffffu, ap_wait(&M->q_empty, (row_it & 1) ^ 1, abort, a.status_dev));
-        if (ok && lane == 0) {
-          ApRow &R = M->row[row_it & 1];
-          R.t = t;
-          R.p = p;
-          R.b = b;
-          R.tiles = tiles;
-          tc::mbar_arrive_expect_tx(&M->q_full, 8 * 8192);
-          for (int kc = 0; kc < 8; ++kc)
-            tc::tma_load_2d(Qs + kc * 8192, &qmap, kc * 64, t * kHeads, &M->q_full);
-        }
-        __syncwarp();
-      }
-      for (uint32_t mm = tiles; mm; mm &= mm - 1) {
-        ok = ok && !*abort;
+      __syncwarp();
+      for (uint32_t mm = tiles; mm && ok; mm &= mm - 1) {
         const int g0 = (__ffs(mm) - 1) * CT;
         const int slot = tile_it & 1;
-        // rows of this thread: r = 4 * rg + sub for rg = pw, pw + 3, ... (< 32);
-        // eight lanes (one 16-byte piece each) share a row
-        const uint16_t *src[11];
-        uint32_t vmask = 0;
+        ok = __all_sync(0xffffffffu, ap_wait(&M->tab_empty[slot], ((tile_it >> 1) & 1) ^ 1, abort,
+                                             a.status_dev));
+        if (!ok) break;
+        int c[4];
 #pragma unroll
-        for (int i = 0; i < 11; ++i) {
-          const int rg = pw + 3 * i;
-          src[i] = static_cast<const uint16_t *>(a.kv_pool);
-          if (rg >= 32) continue;
-          const int r = 4 * rg + sub, j = g0 + r;
+        for (int u = 0; u < 4; ++u) {
+          const int j = g0 + 32 * u + lane;
+          c[u] = j < a.topk ? sel[j] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = g0 + 32 * u + lane;
           long long row = -1;
           const void *pool = a.kv_pool;
           if (j < a.topk) {
             pool = a.cmp_pool;
-            const int c = sel[j];
-            if (c >= 0 && c < V) {
+            if (c[u] >= 0 && c[u] < V) {
               if (cache_tbl) {
-                const int phys = M->tbl[c / kBlock];
+                const int phys = M->tbl[c[u] / kBlock];
                 if (phys >= 0 && phys < a.cmp_n_blocks)
-                  row = (long long)phys * kBlock + (c % kBlock);
-                else if (piece == 0)
+                  row = (long long)phys * kBlock + (c[u] % kBlock);
+                else
                   flag(a.status_dev, CSA_DEV_BAD_BLOCK);
               } else {
-                row = page_row(a.cmp_block_table, a.cmp_max_blocks, a.cmp_n_blocks, b, c,
-                               piece == 0 ? a.status_dev : nullptr);
+                row = page_row(a.cmp_block_table, a.cmp_max_blocks, a.cmp_n_blocks, b, c[u],
+                               a.status_dev);
               }
             }
           } else if (j < n_cand) {
             const int pp = p - a.window + 1 + (j - a.topk);
             if (pp >= 0 && pp < kvl)
               row = page_row(a.kv_block_table, a.kv_max_blocks, a.kv_n_blocks, b, pp,
-                             piece == 0 ? a.status_dev : nullptr);
+                             a.status_dev);
           }
-          if (row >= 0) {
-            src[i] = static_cast<const uint16_t *>(pool) + row * kHeadDim + piece * 8;
-            vmask |= 1u << i;
-          }
-          if (piece == 0) reinterpret_cast<uint8_t *>(M->valid[slot])[r] = row >= 0 ? 1 : 0;
+          M->src[slot][32 * u + lane] =
+              row < 0 ? nullptr : static_cast<const uint16_t *>(pool) + row * kHeadDim;
         }
-        if (ok) tc::mbar_arrive(&M->mask_full[slot]);
-        for (int kc = 0; kc < 8 && ok; ++kc) {
-          if ((kc & 1) == 0) {
-            ok = __all_sync(0xffffffffu, ap_wait(&M->kv_empty[kc >> 1], (tile_it & 1) ^ 1, abort,
-                                                 a.status_dev));
-            if (!ok) break;
+        tc::mbar_arrive(&M->tab_full[slot]);
+        if (mm == tiles) {
+          // the row's q, once the previous row's last QK^T has read its own
+          ok = __all_sync(0xffffffffu, ap_wait(&M->q_empty, (row_it & 1) ^ 1, abort, a.status_dev));
+          if (ok && lane == 0) {
+            ApRow &R = M->row[row_it & 1];
+            R.t = t;
+            R.p = p;
+            R.b = b;
+            R.tiles = tiles;
+            tc::mbar_arrive_expect_tx(&M->q_full, 8 * 8192);
+            for (int kc = 0; kc < 8; ++kc)
+              tc::tma_load_2d(Qs + kc * 8192, &qmap, kc * 64, t * kHeads, &M->q_full);
           }
-          uint8_t *dst = KVs + kc * 16384;
-#pragma unroll
-          for (int i = 0; i < 11; ++i) {
-            const int rg = pw + 3 * i;
-            if (rg >= 32) continue;
-            const int r = 4 * rg + sub;
-            tc::cp_async16_zfill(dst + r * 128 + ((piece ^ (r & 7)) << 4), src[i] + kc * 64,
-                                 (vmask >> i) & 1u);
-          }
-          tc::cp_async_commit();
-          if (kc >= AP_LOOKAHEAD) {
-            tc::cp_async_wait<AP_LOOKAHEAD>();
-            tc::fence_async_shared();
-            tc::mbar_arrive(&M->kv_full[kc - AP_LOOKAHEAD]);
-          }
-        }
-        tc::cp_async_wait<0>();
-        if (ok) {
-          tc::fence_async_shared();
-          for (int kc = 8 - AP_LOOKAHEAD; kc < 8; ++kc) tc::mbar_arrive(&M->kv_full[kc]);
+          if (ok) ++q_loads;
+          __syncwarp();
         }
         ++tile_it;
       }
       ++row_it;
     }
-    // copies in flight land before the CTA retires
-    tc::cp_async_wait<0>();
-    if (!ok && pw == 0) tc::mbar_wait(&M->q_full, (row_it - 1) & 1, 50000000ull);
+    // a q load still in flight lands before the CTA retires
+    if (!ok && q_loads) tc::mbar_wait(&M->q_full, (q_loads - 1) & 1, 50000000ull);
   } else if (warp == AP_MMA_WARP) {
     // ================================================================ MMA issuer
     constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, kHeads);
@@ -354,9 +336,7 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
     const uint32_t kv = tc::smem_u32(KVs), qq = tc::smem_u32(Qs), pp = tc::smem_u32(Ps);
     uint32_t row_it = 0, tile_it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < a.n_rows && ok; t += gridDim.x) {
-      const int b = a.row_req[t];
-      if (b < 0 || b >= a.n_req) continue;
+    for (int t = first_row; t < a.n_rows && ok; t = next_row(t)) {
       ok = __all_sync(0xffffffffu, ap_wait(&M->q_full, row_it & 1, abort, a.status_dev));
       if (!ok) break;
       const uint32_t tiles = M->row[row_it & 1].tiles;
@@ -405,23 +385,67 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
     tc::mma_commit_elect(&M->mma_done);
     tc::mbar_wait(&M->mma_done, 0, 100000000ull);
   } else {
-    // ================================================================ softmax / epilogue
-    const int sw = warp - 4;                // 0..7
+    // ================================================================ softmax / gather / epilogue
+    const int sw = warp - AP_SOFT0;         // 0..7
     const int qd = warp & 3;                // TMEM lane quarter of this warp
     const int h0 = (sw >> 2) * 32;          // first head of this thread's half
     const int c = qd * 32 + lane;           // candidate = TMEM lane
     const int stid = sw * 32 + lane;        // 0..255
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const float sl2 = a.softmax_scale * kLog2e;
+    // gather: this thread copies 16-byte piece `piece` of rows r = 32 * i +
+    // 4 * sw + sub (i < 4) of every chunk
+    const int sub = lane >> 3, piece = lane & 7;
     uint32_t row_it = 0, tile_it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < a.n_rows && ok; t += gridDim.x) {
-      const int b = a.row_req[t];
-      if (b < 0 || b >= a.n_req) continue;
-      ok = tc::bar_and(AP_BAR, AP_SOFT, ap_wait(&M->q_full, row_it & 1, abort, a.status_dev));
-      if (!ok) break;
-      const ApRow R = M->row[row_it & 1];
-      // ---- rotate q's last 64 channels at p (FP32, rounded to BF16) in place
+
+    // Gather tile `it` (its address table in slot it & 1) into the KV buffer;
+    // returns this thread's candidate validity for that tile.  While the
+    // copies fly, `mid()` runs.
+    auto gather = [&](uint32_t it, auto &&mid) -> bool {
+      const int slot = it & 1;
+      bool good = ap_wait(&M->tab_full[slot], (it >> 1) & 1, abort, a.status_dev);
+      const uint16_t *src[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) src[i] = M->src[slot][32 * i + 4 * sw + sub];
+      const bool my_valid = M->src[slot][c] != nullptr;
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&M->tab_empty[slot]);
+      for (int kc = 0; kc < 8; ++kc) {
+        if ((kc & 1) == 0 && good)
+          good = ap_wait(&M->kv_empty[kc >> 1], (it & 1) ^ 1, abort, a.status_dev);
+        if (good) {
+          uint8_t *dst = KVs + kc * 16384;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = 32 * i + 4 * sw + sub;
+            const uint16_t *g = src[i] ? src[i] + kc * 64 + piece * 8
+                                       : static_cast<const uint16_t *>(a.kv_pool);
+            tc::cp_async16_zfill(dst + r * 128 + ((piece ^ (r & 7)) << 4), g, src[i] != nullptr);
+          }
+        }
+        tc::cp_async_commit();
+      }
+      mid();
+      // chunk kc has landed once at most 7 - kc newer groups are pending
+#define AP_LAND(N)                                      \
+  tc::cp_async_wait<N>();                              \
+  if (good) {                                          \
+    tc::fence_async_shared();                          \
+    tc::mbar_arrive(&M->kv_full[7 - N]);               \
+  }
+      AP_LAND(7) AP_LAND(6) AP_LAND(5) AP_LAND(4) AP_LAND(3) AP_LAND(2) AP_LAND(1) AP_LAND(0)
+#undef AP_LAND
+      ok = ok && good;
+      return my_valid;
+    };
+
+    // Wait for the q of row iteration `it`, rotate its last 64 channels at p
+    // (FP32, rounded to BF16) in place and release it to the MMA.
+    auto rope_row = [&](uint32_t it, ApRow &R) {
+      ok = tc::bar_and(AP_BAR, AP_SOFT, ok && ap_wait(&M->q_full, it & 1, abort, a.status_dev));
+      if (!ok) return;
+      R = M->row[it & 1];
       bool rot = a.rope_cos != nullptr && R.p >= 0;
       if (rot && R.p >= a.rope_cap) {
         rot = false;
@@ -447,15 +471,21 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
       }
       tc::bar_sync(AP_BAR, AP_SOFT);
       if (stid == 0) tc::mbar_arrive(&M->q_rot);
+    };
 
+    bool valid = false;
+    ApRow R_next;
+    if (first_row < a.n_rows) {
+      valid = gather(0, [] {});
+      rope_row(0, R_next);
+    }
+    for (int t = first_row; t < a.n_rows && ok; t = next_row(t)) {
+      const ApRow R = R_next;
       bool first = true;
+      float lacc = 0.f;  // this warp's partial denominator of head h0 + lane
       for (uint32_t mm = R.tiles; mm && ok; mm &= mm - 1) {
-        const int slot = tile_it & 1;
-        ok = tc::bar_and(AP_BAR, AP_SOFT,
-                         ap_wait(&M->mask_full[slot], (tile_it >> 1) & 1, abort, a.status_dev) &&
-                             ap_wait(&M->s_full, tile_it & 1, abort, a.status_dev));
+        ok = tc::bar_and(AP_BAR, AP_SOFT, ok && ap_wait(&M->s_full, tile_it & 1, abort, a.status_dev));
         if (!ok) break;
-        const bool valid = reinterpret_cast<const uint8_t *>(M->valid[slot])[c] != 0;
         tc::tc_fence_after();
         float x[32];
         tc::tmem_ld32(tmem + lane_off + S_COL + h0, x);
@@ -485,8 +515,8 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
           if (qd == 0) {
             M->m_s[h] = mn;
             M->corr_s[h] = corr;
-            M->l_s[h] *= corr;
           }
+          lacc *= corr;  // every warp's partial denominator of head h moves with it
           tc::bar_sync(AP_BAR, AP_SOFT);
           load32(M->m_s + h0, mref);
           if (!first) {
@@ -517,28 +547,38 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
               make_uint4(pack2(x[8 * q], x[8 * q + 1]), pack2(x[8 * q + 2], x[8 * q + 3]),
                          pack2(x[8 * q + 4], x[8 * q + 5]), pack2(x[8 * q + 6], x[8 * q + 7]));
         tc::fence_async_shared();
-        // FP32 denominators: per-head sums of the unrounded probabilities
-        const float sum = warp_col_reduce32<false>(x);
-        M->red_l[qd][h0 + lane] = sum;
         tc::tc_fence_before();
         tc::bar_sync(AP_BAR, AP_SOFT);
         if (stid == 0) tc::mbar_arrive(&M->p_full);
-        if (qd == 0) {
-          const int h = h0 + lane;
-          M->l_s[h] += (M->red_l[0][h] + M->red_l[1][h]) + (M->red_l[2][h] + M->red_l[3][h]);
-        }
+        // FP32 denominators (this warp's per-head sums of the unrounded
+        // probabilities, lane l: head h0 + l) while the next tile is gathered
+        auto colsum = [&] { lacc += warp_col_reduce32<false>(x); };
+        const bool more = (mm & (mm - 1)) != 0 || next_row(t) < a.n_rows;
+        if (more)
+          valid = gather(tile_it + 1, colsum);
+        else
+          colsum();
         first = false;
         ++tile_it;
       }
       if (!ok) break;
+      // the next row's q is rotated before this row's epilogue, so that its
+      // first QK^T does not wait for the output stores
+      if (next_row(t) < a.n_rows) {
+        rope_row(row_it + 1, R_next);
+        if (!ok) break;
+      }
 
       // ---- epilogue: out = O^T / L, lse = log L, with the sink in L
       ok = tc::bar_and(AP_BAR, AP_SOFT, ap_wait(&M->o_full, row_it & 1, abort, a.status_dev));
       if (!ok) break;
+      M->red_l[qd][h0 + lane] = lacc;
+      tc::bar_sync(AP_BAR, AP_SOFT);
       if (qd == 0) {
         const int h = h0 + lane;
         const float s2 = a.sink ? a.sink[h] * kLog2e : -INFINITY;
-        float m = M->m_s[h], l = M->l_s[h];
+        float m = M->m_s[h];
+        float l = (M->red_l[0][h] + M->red_l[1][h]) + (M->red_l[2][h] + M->red_l[3][h]);
         if (m == -INFINITY) {
           m = s2;
           l = 0.f;
@@ -578,12 +618,10 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
       tc::tc_fence_before();
       tc::bar_sync(AP_BAR, AP_SOFT);
       if (stid == 0) tc::mbar_arrive(&M->o_empty);
-      if (qd == 0) {
-        M->m_s[h0 + lane] = -INFINITY;
-        M->l_s[h0 + lane] = 0.f;
-      }
+      if (qd == 0) M->m_s[h0 + lane] = -INFINITY;
       ++row_it;
     }
+    tc::cp_async_wait<0>();
   }
 
   tc::tc_fence_before();
@@ -607,7 +645,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 2D BF16 tensor map [rows, 512] with a row stride of 1024 bytes, box
-// {64 channels, box_rows}, 128-byte swizzle.
+// {64 channels, box_rows}, 128-byte swizzle (the q rows of a query row).
 bool encode_rows_map(CUtensorMap *map, const void *base, long long rows, int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode || rows <= 0 || rows > 0x7FFFFFFFll) return false;
@@ -623,26 +661,14 @@ bool encode_rows_map(CUtensorMap *map, const void *base, long long rows, int box
 
 }  // namespace
 
-bool attn_prefill_supported(const csa_attn_args &a) {
-  return a.topk % 4 == 0 && a.window % 4 == 0 && a.topk + a.window <= 32 * CT &&
-         (a.topk == 0 || a.cmp_n_blocks > 0) && a.kv_n_blocks > 0;
-}
+bool attn_prefill_supported(const csa_attn_args &a) { return a.topk + a.window <= 32 * CT; }
 
 cudaError_t launch_attn_prefill(const csa_attn_args &a, cudaStream_t s) {
   if (a.n_rows <= 0) return cudaSuccess;
-  CUtensorMap qmap, cmap, kmap;
+  CUtensorMap qmap;
   memset(&qmap, 0, sizeof(qmap));
-  memset(&cmap, 0, sizeof(cmap));
-  memset(&kmap, 0, sizeof(kmap));
-  if (!encode_rows_map(&qmap, a.q, (long long)a.n_rows * kHeads, kHeads) ||
-      !encode_rows_map(&kmap, a.kv_pool, (long long)a.kv_n_blocks * kBlock, 1))
+  if (!encode_rows_map(&qmap, a.q, (long long)a.n_rows * kHeads, kHeads))
     return cudaErrorInvalidValue;
-  if (a.topk > 0) {
-    if (!encode_rows_map(&cmap, a.cmp_pool, (long long)a.cmp_n_blocks * kBlock, 1))
-      return cudaErrorInvalidValue;
-  } else {
-    cmap = kmap;
-  }
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -658,7 +684,7 @@ cudaError_t launch_attn_prefill(const csa_attn_args &a, cudaStream_t s) {
     sms = 148;
   const int grid = a.n_rows < sms ? a.n_rows : sms;
   launch_begin(CSA_K_ATTN_PREFILL, s);
-  attn_prefill_kernel<<<grid, AP_THREADS, AP_SMEM, s>>>(a, qmap, cmap, kmap);
+  attn_prefill_kernel<<<grid, AP_THREADS, AP_SMEM, s>>>(a, qmap);
   launch_end(CSA_K_ATTN_PREFILL, s);
   return cudaGetLastError();
 }
