@@ -99,7 +99,9 @@ def algorithmic_work(wl):
 
 
 class ClockSampler:
-    """nvidia-smi samples during the timed region."""
+    """nvidia-smi samples (every 20 ms) taken during the timed region, which
+    ``mark_start``/``mark_end`` delimit; a region shorter than one sampling
+    period reports the sample nearest to it."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -108,23 +110,34 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host time, csv line)
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE,
+                 "-i", str(self.gpu), "-lms", "20"], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            deadline = time.time() + 3.0
+            while not self.lines and time.time() < deadline:  # sampling is running
+                time.sleep(0.01)
         except OSError:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+        time.sleep(0.05)  # the first sample after the region, for short regions
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -137,7 +150,18 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = list(self.lines)
+        window = "timed region"
+        if self.t0 is not None and self.t1 is not None:
+            inside = [ln for t, ln in lines if self.t0 <= t <= self.t1]
+            if not inside:
+                after = [ln for t, ln in lines if t > self.t1]
+                inside = after[:1]
+                window = "first sample after the timed region (region shorter than 20 ms)"
+            lines = inside
+        else:
+            lines = [ln for _, ln in lines]
+        for ln in lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -153,7 +177,7 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         sm.sort()
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": window}
 
 
 # ---------------------------------------------------------------- reference arm (CPU oracle)
@@ -277,42 +301,63 @@ def run_gpu(args, wl, rank, world, local_rank):
     torch.cuda.synchronize()
     kernels = ["index_score", "index_topk", "attn_prefill" if prefill else "attn_partial",
                "attn_combine", "compress_gate", "compress_pool"]
+    # per-kernel durations: the step captured with that kernel's event pairs,
+    # replayed three times with L2 flushed before each replay
     per_kernel = {}
     for k in kernels:
-        csa.prof_enable(k, 64)
+        csa.prof_enable(k, 16)
+        step.capture()
+        tot, cnt = 0.0, 0
         for _ in range(3):
             flush_l2()
-            step.run()
-        ms, n = csa.prof_read(k)
+            step.replay()
+            torch.cuda.synchronize()
+            ms, n = csa.prof_read(k)
+            tot += ms
+            cnt += n
+        step.drop_graph()
         csa.prof_disable()
-        if n:
-            per_kernel[k] = {"ms_per_launch": ms / n, "launches_per_step": n / 3}
+        if cnt:
+            per_kernel[k] = {"ms_per_launch": tot / cnt, "launches_per_step": cnt / 3}
     dominant = max(per_kernel, key=lambda k: per_kernel[k]["ms_per_launch"] *
                    per_kernel[k]["launches_per_step"])
     launches_per_step = None
 
+    # ---- the step as one CUDA graph (one host launch per step, so the device
+    # never waits for the host); the dominant kernel's event pair is recorded
+    # inside the graph, so its duration is read back after every replay
+    csa.prof_enable(dominant, 16)
+    lc0 = csa.launch_count()
+    step.capture()
+    launches_per_step = csa.launch_count() - lc0
+    step.replay()
+    torch.cuda.synchronize()
+
     # ---- timed region: device time of exactly K steps, L2 flushed before each
-    csa.prof_enable(dominant, args.steps * 4 + 8)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    lc0 = csa.launch_count()
+    dom_ms, dom_n = 0.0, 0
     wall0 = time.perf_counter()
     with ClockSampler(local_rank) as clk:
+        clk.mark_start()
         for i in range(args.steps):
             flush_l2()
             ev[i][0].record(stream)
-            step.run()
+            step.replay()
             ev[i][1].record(stream)
+            ev[i][1].synchronize()
+            ms, n = csa.prof_read(dominant)
+            dom_ms += ms
+            dom_n += n
         torch.cuda.synchronize()
+        clk.mark_end()
     wall = time.perf_counter() - wall0
-    launches = csa.launch_count() - lc0
+    launches = launches_per_step * args.steps
     if dist:
         dist.barrier()
-    dom_ms, dom_n = csa.prof_read(dominant)
-    csa.prof_disable()
     total_ms = sum(a.elapsed_time(b) for a, b in ev)
     if dist:
         tt = torch.tensor([total_ms], device=dev)
@@ -320,7 +365,6 @@ def run_gpu(args, wl, rank, world, local_rank):
         total_ms = float(tt.item())
     ms_per_step = total_ms / args.steps
     value = units * world * args.steps / (total_ms / 1e3)
-    launches_per_step = launches / args.steps
     status = int(step.status.item())
 
     # ---- end to end through the public API with host buffers
@@ -341,7 +385,7 @@ def run_gpu(args, wl, rank, world, local_rank):
         ee[i][0].record(stream)
         for k, v in host_in.items():
             t[k].copy_(v, non_blocking=True)
-        step.run()
+        step.replay()
         host_out.copy_(step.out, non_blocking=True)
         host_lse.copy_(step.lse, non_blocking=True)
         ee[i][1].record(stream)
@@ -352,6 +396,8 @@ def run_gpu(args, wl, rank, world, local_rank):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
     e2e_value = units * world * args.steps / (e2e_ms / 1e3)
+    step.drop_graph()
+    csa.prof_disable()  # the graph recorded these events: released after its last replay
 
     # ---- roofline of the dominant kernel
     peaks = _peaks()

@@ -21,19 +21,28 @@ struct ProfState {
 };
 static ProfState g_prof;
 
+// Inside stream capture an event record becomes a graph node only with the
+// external flag; such nodes re-record the event at every replay.
+void record_event(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
+
 void launch_begin(int kernel_id, cudaStream_t s) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (g_prof.kernel_id != kernel_id) return;
   std::lock_guard<std::mutex> lk(g_prof.mu);
-  if (g_prof.recorded < g_prof.max_launches)
-    cudaEventRecord(g_prof.ev[2 * g_prof.recorded], s);
+  if (g_prof.recorded < g_prof.max_launches) record_event(g_prof.ev[2 * g_prof.recorded], s);
 }
 
 void launch_end(int kernel_id, cudaStream_t s) {
   if (g_prof.kernel_id != kernel_id) return;
   std::lock_guard<std::mutex> lk(g_prof.mu);
   if (g_prof.recorded < g_prof.max_launches) {
-    cudaEventRecord(g_prof.ev[2 * g_prof.recorded + 1], s);
+    record_event(g_prof.ev[2 * g_prof.recorded + 1], s);
     ++g_prof.recorded;
   }
 }

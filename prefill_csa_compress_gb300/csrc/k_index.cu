@@ -175,12 +175,14 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
   const int c0 = c_lo + tid * KPT;
   const int nv = max(0, min(KPT, c_hi - c0));
 
-  // ---- keys of this thread's run of positions
+  // ---- keys of this thread's run of positions (through L1: the scores come
+  // from the scoring kernel that ran before this one; each thread's run covers
+  // whole 128-byte lines, fetched once for its consecutive vector loads)
   uint32_t key[KPT];
   if (nv == KPT && (reinterpret_cast<uintptr_t>(sc + c0) & 15u) == 0) {
 #pragma unroll
     for (int i = 0; i < KPT; i += 4) {
-      const float4 v = __ldcg(reinterpret_cast<const float4 *>(sc + c0 + i));
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(sc + c0 + i));
       key[i] = order_key(v.x);
       key[i + 1] = order_key(v.y);
       key[i + 2] = order_key(v.z);
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < KPT; ++i) key[i] = i < nv ? order_key(__ldcg(sc + c0 + i)) : 0u;
+    for (int i = 0; i < KPT; ++i) key[i] = i < nv ? order_key(__ldg(sc + c0 + i)) : 0u;
   }
 
   uint32_t *row_ctl = MULTI ? ctl + (long long)t * kTopkCtlWords : nullptr;
@@ -295,10 +297,12 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
     n_gt += (i < nv && key[i] > T) ? 1 : 0;
     n_eq += (i < nv && key[i] == T) ? 1 : 0;
   }
+  // one scan of both counts (each total stays below 2^16)
   int tot;
-  const int eq_rank = block_exclusive_scan(n_eq, warp_sums, &tot);
+  const int before = block_exclusive_scan((n_eq << 16) | n_gt, warp_sums, &tot);
+  const int eq_rank = before >> 16, gt_rank = before & 0xFFFF;
   const int take_eq = max(0, min(n_eq, quota - eq_rank));
-  int pos = offset + block_exclusive_scan(n_gt + take_eq, warp_sums, &tot);
+  int pos = offset + gt_rank + min(eq_rank, quota);
   int eq_seen = 0;
 #pragma unroll
   for (int i = 0; i < KPT; ++i) {

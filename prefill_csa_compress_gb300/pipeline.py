@@ -4,7 +4,10 @@ layer calls them ("DeepSeek V4-Flash, MTP point", "Attention paths").
 
 ``CsaStep`` owns the outputs and workspaces so that repeated steps allocate
 nothing; it is plumbing around the four library calls and computes nothing
-itself.
+itself.  The main compressor's output is read only by the attention call, so
+``run`` issues it on a side stream, where it overlaps the index-key
+compressor and the indexer; ``capture`` records a whole step as a CUDA graph
+so that a repeated step costs one launch on the host.
 """
 
 from __future__ import annotations
@@ -39,6 +42,8 @@ class CsaStep:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev) if status else None
         self.ws = {}
         self._prepared = None
+        self._side = None
+        self._graph = None
 
     def _ws(self, name):
         return self.ws.get(name)
@@ -113,11 +118,41 @@ class CsaStep:
         return self
 
     def run(self, stream=None):
-        if self._prepared is not None:
-            for c in self._prepared:
+        if self._prepared is None:
+            if self.do_compress:
+                self.compress(stream)
+            self.index(stream)
+            self.attention(stream)
+            return
+        calls = self._prepared
+        if not self.do_compress:
+            for c in calls:
                 c(stream)
             return
-        if self.do_compress:
-            self.compress(stream)
-        self.index(stream)
-        self.attention(stream)
+        main = torch.cuda.current_stream() if stream is None else stream
+        if self._side is None:
+            self._side = torch.cuda.Stream(device=self.t["q"].device)
+        side = self._side
+        side.wait_stream(main)             # inputs of this step are in place
+        calls[0](side)                     # main compressor -> cmp_pool
+        for c in calls[1:-1]:              # index-key compressor, indexer top-k
+            c(main)
+        main.wait_stream(side)             # attention reads the new cmp_pool rows
+        calls[-1](main)
+
+    def capture(self):
+        """Record one step (as ``run`` issues it) into a CUDA graph; ``replay``
+        then launches the whole step at once.  Call after a warm-up ``run``."""
+        if self._prepared is None:
+            self.prepare()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            self.run()
+        self._graph = g
+        return self
+
+    def replay(self):
+        self._graph.replay()
+
+    def drop_graph(self):
+        self._graph = None
