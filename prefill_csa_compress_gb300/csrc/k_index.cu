@@ -104,34 +104,61 @@ __device__ bool row_barrier(uint32_t *ctr, uint32_t target, uint32_t *status, in
   return *s_ok != 0;
 }
 
-// The digit d at which the count of keys with digit >= d (scanning from the
-// top) first reaches `remaining`, and the count strictly above d.  Every
-// thread takes nb / blockDim.x consecutive bins.
-__device__ __forceinline__ void block_find_digit(const uint32_t *hist, int nb, int remaining,
-                                                 int *warp_sums, int *s_digit, int *s_above) {
-  const int per = nb / (int)blockDim.x;
-  const int hi = nb - 1 - (int)threadIdx.x * per;
+// Warp 0: the digit d at which the count of keys with digit >= d (scanning
+// from the top) first reaches `remaining`, and the count strictly above d.
+// Lane l sums nb/32 consecutive bins from the top (read in a lane-rotated
+// order, so that eight lanes of a quarter-warp hit distinct bank groups),
+// a warp scan finds the crossing lane, and a second scan over that lane's
+// bins (two per lane) finds the digit.
+__device__ __forceinline__ void warp_find_digit(const uint32_t *hist, int nb, int remaining,
+                                                int *s_digit, int *s_above) {
+  const int lane = threadIdx.x & 31;
+  const int per = nb >> 5;  // 64 or 32 bins per lane
+  const int lo = nb - (lane + 1) * per;
+  const uint4 *v = reinterpret_cast<const uint4 *>(hist + lo);
+  const int nv4 = per >> 2;
   int local = 0;
-  for (int j = 0; j < per; ++j) local += (int)hist[hi - j];
-  if (threadIdx.x == 0) {
-    *s_digit = 0;
-    *s_above = 0;
+  for (int j = 0; j < nv4; ++j) {
+    const uint4 x = v[(j + lane) & (nv4 - 1)];
+    local += (int)(x.x + x.y + x.z + x.w);
   }
-  int total;
-  const int before = block_exclusive_scan(local, warp_sums, &total);
-  if (before < remaining && before + local >= remaining) {
-    int cum = before;
-    for (int j = 0; j < per; ++j) {
-      const int h = (int)hist[hi - j];
-      if (cum + h >= remaining) {
-        *s_digit = hi - j;
-        *s_above = cum;
-        break;
-      }
-      cum += h;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, incl - local < remaining && incl >= remaining);
+  if (!hit) {
+    if (lane == 0) {
+      *s_digit = 0;
+      *s_above = 0;
+    }
+    return;
+  }
+  const int L = __ffs(hit) - 1;
+  const int before = __shfl_sync(0xffffffffu, incl - local, L);
+  // lane m takes bins top - 2m and top - 2m - 1 of lane L's range
+  const int top = nb - 1 - L * per;
+  const int h0 = 2 * lane < per ? (int)hist[top - 2 * lane] : 0;
+  const int h1 = 2 * lane + 1 < per ? (int)hist[top - 2 * lane - 1] : 0;
+  int incl2 = h0 + h1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl2, o);
+    if (lane >= o) incl2 += y;
+  }
+  const int b4 = before + incl2 - (h0 + h1);  // count above this lane's pair
+  const unsigned hit2 = __ballot_sync(0xffffffffu, b4 < remaining && b4 + h0 + h1 >= remaining);
+  if (lane == __ffs(hit2) - 1) {
+    if (b4 + h0 >= remaining) {
+      *s_digit = top - 2 * lane;
+      *s_above = b4;
+    } else {
+      *s_digit = top - 2 * lane - 1;
+      *s_above = b4 + h0;
     }
   }
-  __syncthreads();
 }
 
 // Score back from its order key (-0 comes back as +0).
@@ -260,7 +287,8 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
       for (int i = tid; i < nb; i += NT) hist[i] = __ldcg(&g[i]);
       __syncthreads();
     }
-    block_find_digit(hist, nb, remaining, warp_sums, &s_digit, &s_above);
+    if (tid < 32) warp_find_digit(hist, nb, remaining, &s_digit, &s_above);
+    __syncthreads();
     prefix |= (uint32_t)s_digit << shift;
     pmask |= (uint32_t)(nb - 1) << shift;
     remaining -= s_above;
@@ -302,7 +330,13 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
   const int before = block_exclusive_scan((n_eq << 16) | n_gt, warp_sums, &tot);
   const int eq_rank = before >> 16, gt_rank = before & 0xFFFF;
   const int take_eq = max(0, min(n_eq, quota - eq_rank));
-  int pos = offset + gt_rank + min(eq_rank, quota);
+  // the slice's winners are staged in shared memory (the first-digit
+  // histograms are free by now) and leave in coalesced stores
+  const int n_sel = tot & 0xFFFF;
+  const int n_take = min(n_sel + min(quota, tot >> 16), k - offset);
+  int32_t *st_idx = reinterpret_cast<int32_t *>(priv);
+  uint32_t *st_key = priv + k;
+  int pos = gt_rank + min(eq_rank, quota);
   int eq_seen = 0;
 #pragma unroll
   for (int i = 0; i < KPT; ++i) {
@@ -310,13 +344,18 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
       bool take = key[i] > T;
       if (key[i] == T) take = eq_seen++ < take_eq;
       if (take) {
-        if (pos < k) {
-          out[pos] = c0 + i;
-          if (out_s) out_s[pos] = key_score(key[i]);
+        if (pos < n_take) {
+          st_idx[pos] = c0 + i;
+          st_key[pos] = key[i];
         }
         ++pos;
       }
     }
+  }
+  __syncthreads();
+  for (int i = tid; i < n_take; i += NT) {
+    out[offset + i] = st_idx[i];
+    if (out_s) out_s[offset + i] = key_score(st_key[i]);
   }
 }
 
