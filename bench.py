@@ -31,13 +31,54 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 
 # DRAM traffic per launch from an ncu capture, keyed by kernel; each entry
 # names the source it was taken on (sha1 of the kernel's .cu) so a changed
-# kernel reports null.  Values come from the profiles/ summaries.
-NCU_TRAFFIC = {}
+# kernel reports null.  Values are from `ncu --metrics dram__bytes_read.sum,
+# dram__bytes_write.sum` captures of these same bench workloads.
+NCU_TRAFFIC = {
+    ("chunked_prefill", "attn_prefill"): {"bytes": 1058798811, "src": "0104addba7fa"},
+    ("chunked_prefill", "compress_gate"): {"bytes": 5536873, "src": "c353edbc7e4f"},
+    ("chunked_prefill", "compress_pool"): {"bytes": 16081061, "src": "c353edbc7e4f"},
+    ("chunked_prefill", "index_score"): {"bytes": 149993527, "src": "99ffb8faede4"},
+    ("chunked_prefill", "index_topk"): {"bytes": 34512896, "src": "fce9c9dad6ae"},
+    ("million_decode", "attn_combine"): {"bytes": 17915520, "src": "4e0a12628023"},
+    ("million_decode", "attn_partial"): {"bytes": 17827596, "src": "4e0a12628023"},
+    ("million_decode", "compress_pool"): {"bytes": 22833, "src": "c353edbc7e4f"},
+    ("million_decode", "index_score"): {"bytes": 142226408, "src": "99ffb8faede4"},
+    ("million_decode", "index_topk"): {"bytes": 8639878, "src": "fce9c9dad6ae"},
+    ("serving_decode", "attn_combine"): {"bytes": 5283413, "src": "4e0a12628023"},
+    ("serving_decode", "attn_partial"): {"bytes": 4600728, "src": "4e0a12628023"},
+    ("serving_decode", "compress_pool"): {"bytes": 308983, "src": "c353edbc7e4f"},
+    ("serving_decode", "index_score"): {"bytes": 1536219, "src": "99ffb8faede4"},
+    ("serving_decode", "index_topk"): {"bytes": 121935, "src": "fce9c9dad6ae"},
+}
 
 
 def _env_rank():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# ---------------------------------------------------------------- multi-rank host logic
+
+
+def rank_seed(seed, rank, world):
+    """Weak scaling: every rank runs its own batch of the same shape."""
+    return seed + 1000 * rank if world > 1 else seed
+
+
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The slowest rank's time (identity on one rank)."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, steps, total_ms):
+    """Units every rank processed, per second of the slowest rank's time."""
+    return units_per_rank * world * steps / (total_ms / 1e3)
 
 
 def _peaks():
@@ -266,7 +307,7 @@ def _src_sha(name):
 
 KERNEL_SRC = {"index_score": "k_index_tc.cu", "index_topk": "k_index.cu",
               "attn_partial": "k_attn.cu", "attn_combine": "k_attn.cu",
-              "attn_prefill": "k_attn.cu", "compress_gate": "k_compress.cu",
+              "attn_prefill": "k_attn_prefill.cu", "compress_gate": "k_compress.cu",
               "compress_pool": "k_compress.cu"}
 
 
@@ -358,13 +399,9 @@ def run_gpu(args, wl, rank, world, local_rank):
     launches = launches_per_step * args.steps
     if dist:
         dist.barrier()
-    total_ms = sum(a.elapsed_time(b) for a, b in ev)
-    if dist:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), dist, dev)
     ms_per_step = total_ms / args.steps
-    value = units * world * args.steps / (total_ms / 1e3)
+    value = whole_job_rate(units, world, args.steps, total_ms)
     status = int(step.status.item())
 
     # ---- end to end through the public API with host buffers
@@ -390,12 +427,8 @@ def run_gpu(args, wl, rank, world, local_rank):
         host_lse.copy_(step.lse, non_blocking=True)
         ee[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in ee)
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = units * world * args.steps / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ee), dist, dev)
+    e2e_value = whole_job_rate(units, world, args.steps, e2e_ms)
     step.drop_graph()
     csa.prof_disable()  # the graph recorded these events: released after its last replay
 
@@ -439,7 +472,7 @@ def run_gpu(args, wl, rank, world, local_rank):
     return result
 
 
-def main():
+def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
@@ -448,7 +481,7 @@ def main():
     ap.add_argument("--workload", default="serving_decode")
     ap.add_argument("--ref-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     rank, world, local_rank = _env_rank()
@@ -462,9 +495,7 @@ def main():
         return 0
 
     spec = spec_for(args.workload)
-    if world > 1:
-        # weak scaling: every rank runs its own batch of the same shape
-        spec.seed = spec.seed + 1000 * rank
+    spec.seed = rank_seed(spec.seed, rank, world)
     wl = make_workload(spec)
     # the oracle's CPU timing runs before any CUDA work (no fork after CUDA init)
     cpu = None
