@@ -254,8 +254,11 @@ CSA_API csa_status_t csa_index_topk_noalloc(csa_index_args *args, csa_stream_t s
  * [n_rows, topk]; sink f32 [n_heads] or NULL; out bf16 [n_rows, n_heads,
  * 512]; lse f32 [n_rows, n_heads] or NULL.  Supported: n_heads == 64,
  * head_dim == 512, window == 128, topk <= 2048.
- * The decode call splits each row's candidates over CTAs and merges the
- * partial softmaxes; the prefill call is tiled for many rows.  Both compute
+ * The decode call splits each row's candidates over the CTAs of a thread-
+ * block cluster and merges the partial softmaxes in distributed shared
+ * memory; the prefill call is tiled for many rows.  Neither needs a
+ * workspace (the size query returns 0; a workspace passed in is unused, but
+ * a non-null pointer is what makes the call launch).  Both compute
  * the same function.
  * ---------------------------------------------------------------------- */
 typedef struct {

@@ -59,33 +59,6 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 csa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
 
-// ---- decode split-K geometry: one 128-candidate tile per CTA while the grid
-// fits in about two waves of the GPU; beyond that, tiles are grouped per CTA.
-constexpr int kAttnTile = 128;
-constexpr long long kTargetCtas = 2 * 148;
-
-void attn_geometry(const csa_attn_args &a, bool decode, int *n_splits, int *tiles_per_split) {
-  const int n_cand = a.topk + a.window;
-  const int tiles = (n_cand + kAttnTile - 1) / kAttnTile;
-  if (!decode || a.n_rows <= 0) {
-    *n_splits = 1;
-    *tiles_per_split = tiles;
-    return;
-  }
-  const long long work = (long long)a.n_rows * tiles;
-  int tps = (int)((work + kTargetCtas - 1) / kTargetCtas);
-  if (tps < 1) tps = 1;
-  if (tps > tiles) tps = tiles;
-  *tiles_per_split = tps;
-  *n_splits = (tiles + tps - 1) / tps;
-}
-
-size_t attn_partial_bytes(const csa_attn_args &a, int n_splits) {
-  if (n_splits <= 1) return 0;
-  return align_up((size_t)a.n_rows * n_splits * (kHeads * kHeadDim + 2 * kHeads) * sizeof(float),
-                  kAlign);
-}
-
 // shape checks (enough to size the workspace)
 csa_status_t check_attn_shape(const csa_attn_args *a) {
   if (!a || a->struct_size < sizeof(csa_attn_args)) return CSA_ERR_INVALID_ARG;
@@ -116,19 +89,16 @@ csa_status_t check_attn_args(const csa_attn_args *a) {
 csa_status_t run_attn(csa_attn_args *a, cudaStream_t s, bool decode) {
   csa_status_t st = check_attn_shape(a);
   if (st != CSA_OK) return st;
-  int n_splits = 1, tps = 1;
-  attn_geometry(*a, decode, &n_splits, &tps);
-  const size_t need = attn_partial_bytes(*a, n_splits);
-  if (!a->workspace) {
-    a->workspace_bytes = need;
+  if (!a->workspace) {  // neither path needs scratch memory
+    a->workspace_bytes = 0;
     return CSA_OK;
   }
-  if (a->workspace_bytes < need) return CSA_ERR_INVALID_ARG;
   if (a->n_rows == 0) return CSA_OK;
   st = check_attn_args(a);
   if (st != CSA_OK) return st;
-  if (!decode && attn_prefill_supported(*a)) return from_cuda(launch_attn_prefill(*a, s));
-  return from_cuda(launch_attn(*a, n_splits, tps, static_cast<float *>(a->workspace), s));
+  if (decode) return from_cuda(launch_attn_decode(*a, s));
+  if (!attn_prefill_supported(*a)) return CSA_ERR_UNSUPPORTED;
+  return from_cuda(launch_attn_prefill(*a, s));
 }
 
 }  // namespace

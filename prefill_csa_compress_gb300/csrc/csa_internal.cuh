@@ -40,12 +40,13 @@ cudaError_t launch_index_topk(const csa_index_args &a, const float *scores, int 
 bool topk_is_long(int n_cap);
 size_t topk_ws_bytes(int n_rows, int n_cap);
 uint32_t *topk_counters(void *ws, int n_rows, int n_cap);
-// The persistent prefill kernel (k_attn_prefill.cu) covers top-k sizes that
-// are multiples of 4; other shapes take the split kernel with one split.
+// The persistent prefill kernel (k_attn_prefill.cu).
 bool attn_prefill_supported(const csa_attn_args &a);
 cudaError_t launch_attn_prefill(const csa_attn_args &a, cudaStream_t s);
-cudaError_t launch_attn(const csa_attn_args &a, int n_splits, int tiles_per_split,
-                        float *partials, cudaStream_t s);
+// Decode attention (k_attn.cu): a row's candidate tiles split over the CTAs
+// of one cluster, merged in distributed shared memory.
+void attn_decode_geometry(const csa_attn_args &a, int *n_splits, int *tiles_per_split);
+cudaError_t launch_attn_decode(const csa_attn_args &a, cudaStream_t s);
 
 // ---------------------------------------------------------------- device side
 

@@ -1,62 +1,90 @@
-// Shared-KV sparse attention with an attention sink on the tcgen05 tensor
-// cores.  Candidates of a query row are its selected compressed entries
-// followed by its raw causal window; each candidate row is both key and value.
+// Decode shared-KV sparse attention with an attention sink, the candidates of
+// a row split over the CTAs of one thread-block cluster.  Candidates of a
+// query row are its selected compressed entries followed by its raw causal
+// window; each candidate row is both key and value.
 //
 // Source: "Hyper-Parallel ... DeepSeek V4 CP" (gitcode issue #2),
 // "二阶段 CP 总体算法" (Stage-2 sparse attention with sinks, softmax_scale,
 // ori_win_left = 127; outputs out and lse), "9.1" (candidate list = window KV
 // and selected compressed KV) and "7. Window KV Halo" (window includes self).
 //
-// GB300 mapping.  Every contraction is an M=128 tcgen05.mma with the 128
-// CANDIDATES of a tile on the M side and the 64 heads on the N side:
-//   S^T[c, h] = K[c, :] . q_h          (A = gathered tile, K-major; B = q, K-major)
-//   O^T[d, h] += sum_c K[c, d] P[c, h]  (A = the same tile read MN-major; B = P^T, MN-major)
-// so the gathered tile is staged once in shared memory and serves as key and
-// as value.  The tile is gathered row by row with cp.async straight into the
-// 128-byte-swizzled layout the MMA reads.  Softmax statistics per head reduce
-// across TMEM lanes through a small shared transpose; the running maximum is
-// only moved (and O^T rescaled in TMEM) when it grows by more than 2^8, so the
-// common case never touches the accumulator.  Decode splits a row's
-// candidates over CTAs (one 128-candidate tile each) and merges the partial
-// softmaxes in a second kernel; prefill keeps a row in one CTA and writes the
-// output directly.
-#include "csa_internal.cuh"
-#include "tc.cuh"
+// GB300 mapping.  A row's 128-candidate tiles are dealt to the S CTAs of a
+// cluster (S <= 16, one CTA per SM).  Each CTA loads the row's q with TMA while
+// it gathers its first tile with cp.async (q and the gather overlap), runs the
+// tile's two contractions on tcgen05 (see attn_common.cuh) and a softmax whose
+// running maximum only moves past a 2^8 growth.  The partial softmaxes merge
+// through distributed shared memory: every CTA parks its O^T (FP32) and its
+// per-head maximum and denominator in its own shared memory, and after a
+// cluster barrier CTA r normalises the r-th slice of the output by reading
+// the matching slices of all S partials -- no partial ever reaches HBM and no
+// second kernel runs.
+#include <cstring>
+
+#include "attn_common.cuh"
 
 namespace csa {
 namespace {
 
-constexpr int AT_THREADS = 128;
-constexpr int CT = 128;  // candidates per tile
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleLog2 = 8.0f;  // move the running max only past a 2^8 growth
+using namespace attn;
 
-constexpr int OFF_Q = 0;                      // 64 heads x 512 bf16, K-major: 8 chunks x 8 KB
-constexpr int OFF_KV = OFF_Q + 8 * 8192;      // 128 cands x 512 bf16: 8 chunks x 16 KB
-constexpr int OFF_P = OFF_KV + 8 * 16384;     // P^T, MN-major: 128 cands x 64 heads bf16
-constexpr int OFF_MISC = OFF_P + 16384;
-constexpr int ATTN_SMEM = OFF_MISC + 4096 + 1024;
-constexpr uint32_t ATTN_TMEM_COLS = 512;      // S^T: cols [0,64); O^T tile m: [64+64m, 128+64m)
-constexpr int REC_FLOATS = kHeads * kHeadDim + 2 * kHeads;  // partial record per (row, split)
+constexpr int AD_THREADS = 256;
+constexpr int AD_BAR = 1;  // named barrier over all 256 threads (the softmax's)
+constexpr int AD_MAX_CLUSTER = 16;
 
-struct AttnMisc {
-  uint64_t bar_qk;
-  uint64_t bar_pv;
+struct AdMisc {
+  uint64_t q_full, mma_bar, done_bar;
   uint32_t tmem_base;
-  int any_rescale;
-  const uint16_t *rowp[CT];
-  float m_ref[kHeads];  // running reference (log2 domain)
-  float l_acc[kHeads];
-  float corr[kHeads];
-  float red[2][kHeads];
-  float red4[4][kHeads];
+  int pad;
+  SoftState st;
+  const uint16_t *src[CT];  // pool row of each candidate of the tile, or null
+  alignas(16) float m_loc[kHeads];  // this CTA's reference per head (log2), -inf if none
+  alignas(16) float l_loc[kHeads];  // this CTA's denominator per head
+  alignas(16) float red_l[4][kHeads];
+  alignas(16) float w_all[AD_MAX_CLUSTER][kHeads];  // scale of each CTA's partial
+  alignas(16) float inv_L[kHeads];
 };
+constexpr int AD_SMEM = OFF_MISC + (int)sizeof(AdMisc) + 1024;
+static_assert(AD_SMEM <= 227 * 1024, "shared memory");
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+
+// Address of `p` (this CTA's shared memory) in the shared memory of CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(tc::smem_u32(p)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_peer_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Pool row of candidate j of row t (its list: top-k entries, then the
+// window), or null when absent; data errors raise their flag.
 __device__ __forceinline__ const uint16_t *candidate_row(const csa_attn_args &a, int t, int b,
-                                                        int p, int V, int gi) {
-  if (gi < a.topk) {
-    const int c = a.topk_idx[(long long)t * a.topk + gi];
+                                                         int p, int V, int kvl, int j) {
+  if (j < a.topk) {
+    const int c = a.topk_idx[(long long)t * a.topk + j];
     if (c < 0) return nullptr;
     if (c >= V) {
       flag(a.status_dev, CSA_DEV_BAD_INDEX);
@@ -66,9 +94,10 @@ __device__ __forceinline__ const uint16_t *candidate_row(const csa_attn_args &a,
         page_row(a.cmp_block_table, a.cmp_max_blocks, a.cmp_n_blocks, b, c, a.status_dev);
     return row < 0 ? nullptr : static_cast<const uint16_t *>(a.cmp_pool) + row * kHeadDim;
   }
-  const int pp = p - a.window + 1 + (gi - a.topk);
+  if (j >= a.topk + a.window) return nullptr;
+  const int pp = p - a.window + 1 + (j - a.topk);
   if (pp < 0) return nullptr;
-  if (pp >= a.kv_len[b]) {
+  if (pp >= kvl) {
     flag(a.status_dev, CSA_DEV_BAD_POS);
     return nullptr;
   }
@@ -77,455 +106,303 @@ __device__ __forceinline__ const uint16_t *candidate_row(const csa_attn_args &a,
   return row < 0 ? nullptr : static_cast<const uint16_t *>(a.kv_pool) + row * kHeadDim;
 }
 
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t *>(&v);
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// P^T buffer: row c (one candidate) holds 64 heads as 8 swizzled 16-byte chunks.
-__device__ __forceinline__ uint8_t *prow_chunk(uint8_t *P, int c, int j) {
-  return P + (c >> 3) * 1024 + (c & 7) * 128 + ((j ^ (c & 7)) << 4);
-}
-
-__device__ __forceinline__ float p_at(const uint8_t *P, int c, int h) {
-  const uint16_t v = *reinterpret_cast<const uint16_t *>(
-      P + (c >> 3) * 1024 + (c & 7) * 128 + (((h >> 3) ^ (c & 7)) << 4) + (h & 7) * 2);
-  return bf16_bits_to_float(v);
-}
-
-// Column sums of x[0..63] over the 32 lanes of a warp by a butterfly
-// reduce-scatter: afterwards lane l holds the warp sums of columns 2l, 2l+1.
-__device__ __forceinline__ float2 warp_colsum64(const float (&x)[64]) {
-  const int lane = threadIdx.x & 31;
-  float a[32];
-  {
-    const bool up = lane & 16;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float send = up ? x[i] : x[32 + i];
-      a[i] = (up ? x[32 + i] : x[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-  }
-  float b[16];
-  {
-    const bool up = lane & 8;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float send = up ? a[i] : a[16 + i];
-      b[i] = (up ? a[16 + i] : a[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-  }
-  float c[8];
-  {
-    const bool up = lane & 4;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float send = up ? b[i] : b[8 + i];
-      c[i] = (up ? b[8 + i] : b[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
-  }
-  float d[4];
-  {
-    const bool up = lane & 2;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float send = up ? c[i] : c[4 + i];
-      d[i] = (up ? c[4 + i] : c[i]) + __shfl_xor_sync(0xffffffffu, send, 2);
-    }
-  }
-  const bool up = lane & 1;
-  const float s0 = (up ? d[2] : d[0]) + __shfl_xor_sync(0xffffffffu, up ? d[0] : d[2], 1);
-  const float s1 = (up ? d[3] : d[1]) + __shfl_xor_sync(0xffffffffu, up ? d[1] : d[3], 1);
-  return make_float2(s0, s1);
-}
-
-__device__ __forceinline__ bool wait_or_flag(uint64_t *bar, uint32_t parity, uint32_t *status) {
-  if (tc::mbar_wait(bar, parity)) return true;
-  flag(status, CSA_DEV_TIMEOUT);
-  return false;
-}
-
-__global__ void __launch_bounds__(AT_THREADS, 1)
-    attn_tc_kernel(csa_attn_args a, int n_splits, int tiles_per_split, float *__restrict__ partials) {
+__global__ void __launch_bounds__(AD_THREADS, 1)
+    attn_decode_kernel(csa_attn_args a, int tiles_per_split,
+                       const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~uintptr_t(1023));
   uint8_t *Qs = sm + OFF_Q;
   uint8_t *KVs = sm + OFF_KV;
   uint8_t *Ps = sm + OFF_P;
-  AttnMisc *M = reinterpret_cast<AttnMisc *>(sm + OFF_MISC);
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int t = blockIdx.y, split = blockIdx.x;
+  float *Os = reinterpret_cast<float *>(KVs);  // O[h][d] (FP32) once the tiles are done
+  AdMisc *M = reinterpret_cast<AdMisc *>(sm + OFF_MISC);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t = blockIdx.y;
+  const uint32_t s = cluster_rank(), S = gridDim.x;
   const int b = a.row_req[t];
-  if (b < 0) return;
+  if (b < 0) return;  // every CTA of the cluster serves the same row
   if (b >= a.n_req) {
-    if (tid == 0 && split == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
+    if (tid == 0 && s == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
     return;
   }
   const int p = a.row_pos[t];
   const int V = min(visible_count(p, a.ratio, a.n_cmp[b]), a.cmp_max_blocks * kBlock);
-  const int n_cand = a.topk + a.window;
-  const int g_begin = split * tiles_per_split * CT;
-  const int g_end = min(n_cand, g_begin + tiles_per_split * CT);
+  const int kvl = a.kv_len[b];
+  const int n_tiles = (a.topk + a.window + CT - 1) / CT;
+  const int g_begin = (int)s * tiles_per_split;
+  const int g_end = min(n_tiles, g_begin + tiles_per_split);
 
   if (tid == 0) {
-    tc::mbar_init(&M->bar_qk, 1);
-    tc::mbar_init(&M->bar_pv, 1);
+    tc::mbar_init(&M->q_full, 1);
+    tc::mbar_init(&M->mma_bar, 1);
+    tc::mbar_init(&M->done_bar, 1);
     tc::mbar_fence_init();
   }
-  if (warp == 0) tc::tmem_alloc(&M->tmem_base, ATTN_TMEM_COLS);
-  if (tid < kHeads) {
-    M->m_ref[tid] = -INFINITY;
-    M->l_acc[tid] = 0.f;
-  }
-
-  // ---- q rotated at p (FP32), rounded to BF16, K-major swizzled
-  bool rot = a.rope_cos != nullptr && p >= 0;
-  if (rot && p >= a.rope_cap) {
-    rot = false;
-    if (tid == 0 && split == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
-  }
-  const uint16_t *qg = static_cast<const uint16_t *>(a.q) + (long long)t * kHeads * kHeadDim;
-  // all 4096 16-byte pieces in flight at once, straight into the swizzled layout
-  for (int e = tid; e < kHeads * (kHeadDim / 8); e += AT_THREADS) {
-    const int h = e >> 6, u = e & 63, kc = u >> 3, jj = u & 7;
-    tc::cp_async16(Qs + kc * 8192 + h * 128 + ((jj ^ (h & 7)) << 4), qg + h * kHeadDim + u * 8);
-  }
-  tc::cp_async_wait_all();
-  if (rot) {  // rotate the last 64 channels in place (each thread its own pieces)
-    for (int e = tid; e < kHeads * (kHeadDim / 8); e += AT_THREADS) {
-      const int h = e >> 6, u = e & 63, kc = u >> 3, jj = u & 7;
-      if (u * 8 < kHeadDim - kRopeDim) continue;
-      uint4 *slot = reinterpret_cast<uint4 *>(Qs + kc * 8192 + h * 128 + ((jj ^ (h & 7)) << 4));
-      const uint4 x = *slot;
-      uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int pair = (u * 8 - (kHeadDim - kRopeDim)) / 2 + q;
-        const float c = a.rope_cos[(long long)p * kRopeHalf + pair];
-        const float s = a.rope_sin[(long long)p * kRopeHalf + pair];
-        const float x0 = bf16_lo(w[q]), x1 = bf16_hi(w[q]);
-        w[q] = pack2(x0 * c - x1 * s, x0 * s + x1 * c);
-      }
-      *slot = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  }
+  if (tid < kHeads) M->st.m[tid] = -INFINITY;
+  if (warp == 0) tc::tmem_alloc(&M->tmem_base, TMEM_COLS);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = M->tmem_base;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const float sl2 = a.softmax_scale * kLog2e;
-  uint32_t ph_qk = 0, ph_pv = 0;
-  int n_done = 0;  // tiles accumulated into O^T
-  bool ok = true;
+  const uint32_t kv = tc::smem_u32(KVs), qq = tc::smem_u32(Qs), pp = tc::smem_u32(Ps);
 
-  for (int g0 = g_begin; g0 < g_end && ok; g0 += CT) {
+  // q of the row by TMA, in flight while the first tile is gathered
+  const bool has_tiles = g_begin < g_end;
+  if (has_tiles && tid == 0) {
+    tc::mbar_arrive_expect_tx(&M->q_full, 8 * 8192);
+    for (int kc = 0; kc < 8; ++kc)
+      tc::tma_load_2d(Qs + kc * 8192, &qmap, kc * 64, t * kHeads, &M->q_full);
+  }
+  bool rot = a.rope_cos != nullptr && p >= 0;
+  if (rot && p >= a.rope_cap) {
+    rot = false;
+    if (tid == 0 && s == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
+  }
+
+  const int qd = warp & 3, h0 = (warp >> 2) * 32, c = qd * 32 + lane;
+  const int sub = lane >> 3, piece = lane & 7;  // gather: rows 32 i + 4 warp + sub, 16-byte piece
+  const float sl2 = a.softmax_scale * kLog2e;
+  float lacc = 0.f;  // this warp's partial denominator of head h0 + lane
+  bool first = true, ok = true, q_ready = false;
+  uint32_t phase = 0;
+
+  for (int g = g_begin; g < g_end && ok; ++g) {
     // ---- candidate rows of this tile
+    if (tid < CT) M->src[tid] = candidate_row(a, t, b, p, V, kvl, g * CT + tid);
+    if (__syncthreads_count(tid < CT && M->src[tid] != nullptr) == 0) continue;
+    const bool valid = M->src[c] != nullptr;
+    // ---- gather the tile into the swizzled layout (the previous P.V is done)
     {
-      const int gi = g0 + tid;
-      M->rowp[tid] = gi < g_end ? candidate_row(a, t, b, p, V, gi) : nullptr;
+      const uint16_t *src[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) src[i] = M->src[32 * i + 4 * warp + sub];
+      for (int kc = 0; kc < 8; ++kc) {
+        uint8_t *dst = KVs + kc * 16384;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 32 * i + 4 * warp + sub;
+          const uint16_t *gsrc = src[i] ? src[i] + kc * 64 + piece * 8
+                                        : static_cast<const uint16_t *>(a.kv_pool);
+          tc::cp_async16_zfill(dst + r * 128 + ((piece ^ (r & 7)) << 4), gsrc, src[i] != nullptr);
+        }
+      }
     }
-    const int n_valid = __syncthreads_count(M->rowp[tid] != nullptr);
-    if (n_valid == 0) continue;
-    // ---- gather into the swizzled tile (the previous PV has completed)
-#pragma unroll 4
-    for (int q = 0; q < 64; ++q) {
-      const int unit = q * AT_THREADS + tid;
-      const int c = unit >> 6, u = unit & 63, kc = u >> 3, jj = u & 7;
-      uint8_t *dst = KVs + kc * 16384 + c * 128 + ((jj ^ (c & 7)) << 4);
-      const uint16_t *src = M->rowp[c];
-      if (src)
-        tc::cp_async16(dst, src + u * 8);
-      else
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    if (!q_ready) {
+      // q landed meanwhile: rotate its last 64 channels at p
+      if (!tc::mbar_wait(&M->q_full, 0)) {
+        ok = false;
+        flag(a.status_dev, CSA_DEV_TIMEOUT);
+      }
+      if (rot) rope_q_tile(Qs, a, p, tid, AD_THREADS);
+      q_ready = true;
     }
     tc::cp_async_wait_all();
     tc::fence_async_shared();
     __syncthreads();
 
     // ---- S^T = K q^T
-    if (tid == 0) {
+    if (warp == 0) {
       tc::tc_fence_after();
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(128, kHeads);
-      const uint32_t kv = tc::smem_u32(KVs), qq = tc::smem_u32(Qs);
-      for (int kc = 0; kc < 8; ++kc)
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-          tc::mma_bf16(tmem, tc::desc_sw128(kv + kc * 16384 + s * 32),
-                       tc::desc_sw128(qq + kc * 8192 + s * 32), idesc, (kc | s) != 0);
-      tc::mma_commit(&M->bar_qk);
+      for (int kc = 0; kc < 8; ++kc) issue_qk(tmem, kv, qq, kc);
+      tc::mma_commit_elect(&M->mma_bar);
     }
-    ok = wait_or_flag(&M->bar_qk, ph_qk, a.status_dev);
-    ph_qk ^= 1;
-    tc::tc_fence_after();
+    if (!tc::mbar_wait(&M->mma_bar, phase)) ok = false;
+    phase ^= 1;
 
-    // ---- logits of this thread's candidate (log2 domain)
-    const bool valid = M->rowp[tid] != nullptr;
-    float x[kHeads];
-    {
-      float v[32];
-      tc::tmem_ld32(tmem + lane_base, v);
-#pragma unroll
-      for (int h = 0; h < 32; ++h) x[h] = valid ? v[h] * sl2 : -INFINITY;
-      tc::tmem_ld32(tmem + lane_base + 32, v);
-#pragma unroll
-      for (int h = 0; h < 32; ++h) x[32 + h] = valid ? v[h] * sl2 : -INFINITY;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<uint4 *>(prow_chunk(Ps, tid, j)) =
-          make_uint4(pack2(x[8 * j], x[8 * j + 1]), pack2(x[8 * j + 2], x[8 * j + 3]),
-                     pack2(x[8 * j + 4], x[8 * j + 5]), pack2(x[8 * j + 6], x[8 * j + 7]));
-    __syncthreads();
-    {
-      const int h = tid & 63, half = tid >> 6;
-      float mx = -INFINITY;
-      for (int c = half * 64; c < half * 64 + 64; ++c) mx = fmaxf(mx, p_at(Ps, c, h));
-      M->red[half][h] = mx;
-      if (tid == 0) M->any_rescale = 0;
-    }
-    __syncthreads();
-    if (tid < kHeads) {
-      const int h = tid;
-      const float mt = fmaxf(M->red[0][h], M->red[1][h]);
-      const float mo = M->m_ref[h];
-      float corr = 1.f;
-      if (mo == -INFINITY) {
-        M->m_ref[h] = mt;  // first finite tile sets the reference
-      } else if (mt > mo + kRescaleLog2) {
-        M->m_ref[h] = mt;
-        corr = exp2f(mo - mt);
-      }
-      M->corr[h] = corr;
-      M->l_acc[h] *= corr;
-      if (corr != 1.f && n_done > 0) M->any_rescale = 1;
-    }
-    __syncthreads();
-    if (M->any_rescale) {  // rare: bring O^T to the new reference
-#pragma unroll 1
-      for (int mt = 0; mt < 4; ++mt)
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          float v[32];
-          const uint32_t addr = tmem + lane_base + 64 + mt * 64 + hh * 32;
-          tc::tmem_ld32(addr, v);
-#pragma unroll
-          for (int h = 0; h < 32; ++h) v[h] *= M->corr[hh * 32 + h];
-          tc::tmem_st32(addr, v);
-        }
-      tc::tc_fence_before();
-    }
-    // ---- P = 2^(x - m), BF16, MN-major rows
-#pragma unroll
-    for (int h = 0; h < kHeads; ++h) {
-      const float m = M->m_ref[h];
-      x[h] = (m == -INFINITY) ? 0.f : exp2f(x[h] - m);
-    }
-    __syncthreads();  // all column reads of the previous P contents are done
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<uint4 *>(prow_chunk(Ps, tid, j)) =
-          make_uint4(pack2(x[8 * j], x[8 * j + 1]), pack2(x[8 * j + 2], x[8 * j + 3]),
-                     pack2(x[8 * j + 4], x[8 * j + 5]), pack2(x[8 * j + 6], x[8 * j + 7]));
+    // ---- softmax; P^T to shared memory
+    float x[32];
+    softmax_tile(tmem, qd, h0, valid, sl2, first, &M->st, Ps, AD_BAR, lacc, x);
     tc::fence_async_shared();
-    {
-      // FP32 denominators: per-head sums of the unrounded probabilities
-      const float2 s2 = warp_colsum64(x);
-      const int lane = tid & 31;
-      M->red4[warp][2 * lane] = s2.x;
-      M->red4[warp][2 * lane + 1] = s2.y;
-    }
-    __syncthreads();
-    // ---- O^T += V^T P^T (4 dim tiles of 128)
-    if (tid == 0) {
-      tc::tc_fence_after();
-      constexpr uint32_t idesc = tc::idesc_bf16_f32_mn(128, kHeads);
-      const uint32_t kv = tc::smem_u32(KVs), pp = tc::smem_u32(Ps);
-      for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          tc::mma_bf16(tmem + 64 + mt * 64,
-                       tc::desc_sw128_mn(kv + 2 * mt * 16384 + ks * 2048, 16384, 1024),
-                       tc::desc_sw128_mn(pp + ks * 2048, 16384, 1024), idesc,
-                       (n_done > 0 || ks > 0) ? 1u : 0u);
-      tc::mma_commit(&M->bar_pv);
-    }
-    if (tid < kHeads)
-      M->l_acc[tid] += (M->red4[0][tid] + M->red4[1][tid]) + (M->red4[2][tid] + M->red4[3][tid]);
-    ok = wait_or_flag(&M->bar_pv, ph_pv, a.status_dev) && ok;
-    ph_pv ^= 1;
-    tc::tc_fence_after();
-    ++n_done;
-    ok = __syncthreads_and(ok);  // a timed-out wait ends the row for the whole CTA
-  }
-  __syncthreads();
+    tc::tc_fence_before();
+    tc::bar_sync(AD_BAR, AD_THREADS);
 
-  // ---- epilogue: thread = output channel lane of each 128-channel tile
-  if (n_splits == 1) {
-    if (tid < kHeads) {
-      const int h = tid;
-      const float s2 = a.sink ? a.sink[h] * kLog2e : -INFINITY;
-      float m = M->m_ref[h], l = n_done ? M->l_acc[h] : 0.f;
-      if (m == -INFINITY) {
-        m = s2;
-        l = 0.f;
-      }
-      const float L = (m == -INFINITY) ? 0.f : l + exp2f(s2 - m);
-      M->corr[h] = L > 0.f ? 1.f / L : 0.f;  // reuse as 1/L
-      if (a.lse) a.lse[(long long)t * kHeads + h] = L > 0.f ? (m + log2f(L)) * kLn2 : -INFINITY;
+    // ---- O^T += V^T P^T
+    if (warp == 0) {
+      tc::tc_fence_after();
+      for (int mt = 0; mt < 4; ++mt) issue_pv(tmem, kv, pp, mt, !first);
+      tc::mma_commit_elect(&M->mma_bar);
     }
-    __syncthreads();
-    const bool inv = a.inv_rope_out && a.rope_cos != nullptr && p >= 0 && p < a.rope_cap;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + (long long)t * kHeads * kHeadDim;
-    for (int mt = 0; mt < 4; ++mt) {
-      const int d = mt * 128 + tid;
-      for (int hh = 0; hh < 2; ++hh) {
-        float v[32];
-        if (n_done) {
-          tc::tmem_ld32(tmem + lane_base + 64 + mt * 64 + hh * 32, v);
-        } else {
+    lacc += warp_col_reduce32<false>(x);
+    if (!tc::mbar_wait(&M->mma_bar, phase)) ok = false;
+    phase ^= 1;
+    tc::tc_fence_after();
+    first = false;
+    ok = __syncthreads_and(ok);
+    if (!ok && tid == 0) flag(a.status_dev, CSA_DEV_TIMEOUT);
+  }
+  if (has_tiles && !q_ready) tc::mbar_wait(&M->q_full, 0, 50000000ull);  // no tile had candidates
+  if (!ok && warp == 0) {
+    // nothing of ours may still run on TMEM when it is released
+    tc::mma_commit_elect(&M->done_bar);
+    tc::mbar_wait(&M->done_bar, 0, 100000000ull);
+  }
+
+  // ---- this CTA's partial: per-head reference and denominator, O^T as O[h][d]
+  M->red_l[qd][h0 + lane] = lacc;
+  __syncthreads();
+  if (tid < kHeads) {
+    const int h = tid;
+    M->m_loc[h] = first ? -INFINITY : M->st.m[h];
+    M->l_loc[h] = first ? 0.f : (M->red_l[0][h] + M->red_l[1][h]) + (M->red_l[2][h] + M->red_l[3][h]);
+  }
+  if (!first) {
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+#pragma unroll 1
+    for (int m4 = 0; m4 < 4; ++m4) {
+      float v[32];
+      tc::tmem_ld32(tmem + lane_off + O_COL + m4 * 64 + h0, v);
+      const int d = m4 * 128 + qd * 32 + lane;
 #pragma unroll
-          for (int h = 0; h < 32; ++h) v[h] = 0.f;
-        }
-#pragma unroll
-        for (int h = 0; h < 32; ++h) {
-          float o = v[h] * M->corr[hh * 32 + h];
-          if (inv && d >= kHeadDim - kRopeDim) {
-            const float other = __shfl_xor_sync(0xffffffffu, o, 1);
-            const int pair = (d - (kHeadDim - kRopeDim)) >> 1;
-            const float c = a.rope_cos[(long long)p * kRopeHalf + pair];
-            const float s = a.rope_sin[(long long)p * kRopeHalf + pair];
-            o = (d & 1) ? (-other * s + o * c) : (o * c + other * s);
-          }
-          out[(hh * 32 + h) * kHeadDim + d] = __float2bfloat16_rn(o);
-        }
-      }
-    }
-  } else {
-    float *rec = partials + ((long long)t * n_splits + split) * REC_FLOATS;
-    for (int mt = 0; mt < 4; ++mt)
-      for (int hh = 0; hh < 2; ++hh) {
-        float v[32];
-        if (n_done) {
-          tc::tmem_ld32(tmem + lane_base + 64 + mt * 64 + hh * 32, v);
-        } else {
-#pragma unroll
-          for (int h = 0; h < 32; ++h) v[h] = 0.f;
-        }
-#pragma unroll
-        for (int h = 0; h < 32; ++h) rec[(hh * 32 + h) * kHeadDim + mt * 128 + tid] = v[h];
-      }
-    if (tid < kHeads) {
-      rec[kHeads * kHeadDim + tid] = n_done ? M->m_ref[tid] : -INFINITY;
-      rec[kHeads * kHeadDim + kHeads + tid] = n_done ? M->l_acc[tid] : 0.f;
+      for (int j = 0; j < 32; ++j) Os[(h0 + j) * kHeadDim + d] = v[j];
     }
   }
   tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  if (warp == 0) tc::tmem_dealloc(tmem, ATTN_TMEM_COLS);
-}
+  cluster_sync();
 
-// Merge a row's split partials with the sink.  One CTA per (head, row);
-// each thread owns four consecutive output channels.
-__global__ void __launch_bounds__(128) attn_combine_kernel(csa_attn_args a, int n_splits,
-                                                           const float *__restrict__ partials) {
-  __shared__ float wsplit[64];
-  __shared__ float sL, sM;
-  const int h = blockIdx.x, t = blockIdx.y;
-  const int b = a.row_req[t];
-  if (b < 0 || b >= a.n_req) return;
-  const int p = a.row_pos[t];
-  const float *rec0 = partials + (long long)t * n_splits * REC_FLOATS;
-  if (threadIdx.x == 0) {
+  // ---- merge weights: one thread per head reads every CTA's statistics
+  if (tid < kHeads) {
+    const int h = tid;
     const float s2 = a.sink ? a.sink[h] * kLog2e : -INFINITY;
     float mx = s2;
-    for (int s = 0; s < n_splits; ++s) mx = fmaxf(mx, rec0[s * REC_FLOATS + kHeads * kHeadDim + h]);
+    for (uint32_t q = 0; q < S; ++q) mx = fmaxf(mx, ld_peer_f32(peer_addr(&M->m_loc[h], q)));
     float L = 0.f;
     if (mx != -INFINITY) {
       L = exp2f(s2 - mx);
-      for (int s = 0; s < n_splits; ++s) {
-        const float ms = rec0[s * REC_FLOATS + kHeads * kHeadDim + h];
-        const float w = ms == -INFINITY ? 0.f : exp2f(ms - mx);
-        if (s < 64) wsplit[s] = w;
-        L += w * rec0[s * REC_FLOATS + kHeads * kHeadDim + kHeads + h];
+      for (uint32_t q = 0; q < S; ++q) {
+        const float mq = ld_peer_f32(peer_addr(&M->m_loc[h], q));
+        const float w = mq == -INFINITY ? 0.f : exp2f(mq - mx);
+        M->w_all[q][h] = w;
+        if (w != 0.f) L += w * ld_peer_f32(peer_addr(&M->l_loc[h], q));
       }
+    } else {
+      for (uint32_t q = 0; q < S; ++q) M->w_all[q][h] = 0.f;
     }
-    sL = L;
-    sM = mx;
-    if (a.lse) a.lse[(long long)t * kHeads + h] = L > 0.f ? (mx + log2f(L)) * kLn2 : -INFINITY;
+    M->inv_L[h] = L > 0.f ? 1.f / L : 0.f;
+    if (s == 0 && a.lse)
+      a.lse[(long long)t * kHeads + h] = L > 0.f ? (mx + log2f(L)) * kLn2 : -INFINITY;
   }
   __syncthreads();
-  const float invL = sL > 0.f ? 1.f / sL : 0.f;
-  const int d = threadIdx.x * 4;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (sL > 0.f) {
-    for (int s = 0; s < n_splits; ++s) {
-      float w;
-      if (s < 64) {
-        w = wsplit[s];
-      } else {
-        const float ms = rec0[s * REC_FLOATS + kHeads * kHeadDim + h];
-        w = ms == -INFINITY ? 0.f : exp2f(ms - sM);
-      }
+
+  // ---- this CTA's slice of the output: 4 channels per step, all partials
+  const bool inv = a.inv_rope_out && a.rope_cos != nullptr && p >= 0 && p < a.rope_cap;
+  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + (long long)t * kHeads * kHeadDim;
+  constexpr int kUnits = kHeads * kHeadDim / 4;
+  const int u0 = (int)((long long)kUnits * s / S), u1 = (int)((long long)kUnits * (s + 1) / S);
+  for (int u = u0 + tid; u < u1; u += AD_THREADS) {
+    const int h = u / (kHeadDim / 4), d = (u % (kHeadDim / 4)) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (uint32_t q = 0; q < S; ++q) {
+      const float w = M->w_all[q][h];
       if (w == 0.f) continue;
-      const float4 v = *reinterpret_cast<const float4 *>(rec0 + s * REC_FLOATS + h * kHeadDim + d);
+      const float4 v = ld_peer_f32x4(peer_addr(Os + h * kHeadDim + d, q));
       acc.x = fmaf(w, v.x, acc.x);
       acc.y = fmaf(w, v.y, acc.y);
       acc.z = fmaf(w, v.z, acc.z);
       acc.w = fmaf(w, v.w, acc.w);
     }
-  }
-  float o[4] = {acc.x * invL, acc.y * invL, acc.z * invL, acc.w * invL};
-  if (a.inv_rope_out && a.rope_cos != nullptr && p >= 0 && p < a.rope_cap &&
-      d >= kHeadDim - kRopeDim) {
+    const float il = M->inv_L[h];
+    float o[4] = {acc.x * il, acc.y * il, acc.z * il, acc.w * il};
+    if (inv && d >= kHeadDim - kRopeDim) {
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int pair = (d + 2 * q - (kHeadDim - kRopeDim)) >> 1;
-      const float c = a.rope_cos[(long long)p * kRopeHalf + pair];
-      const float s = a.rope_sin[(long long)p * kRopeHalf + pair];
-      const float x0 = o[2 * q], x1 = o[2 * q + 1];
-      o[2 * q] = x0 * c + x1 * s;
-      o[2 * q + 1] = -x0 * s + x1 * c;
+      for (int q2 = 0; q2 < 2; ++q2) {
+        const int pair = (d + 2 * q2 - (kHeadDim - kRopeDim)) >> 1;
+        const float cs = a.rope_cos[(long long)p * kRopeHalf + pair];
+        const float sn = a.rope_sin[(long long)p * kRopeHalf + pair];
+        const float x0 = o[2 * q2], x1 = o[2 * q2 + 1];
+        o[2 * q2] = x0 * cs + x1 * sn;
+        o[2 * q2 + 1] = -x0 * sn + x1 * cs;
+      }
     }
+    uint2 packed = make_uint2(pack2(o[0], o[1]), pack2(o[2], o[3]));
+    *reinterpret_cast<uint2 *>(out + h * kHeadDim + d) = packed;
   }
-  __nv_bfloat162 *out = reinterpret_cast<__nv_bfloat162 *>(
-      static_cast<__nv_bfloat16 *>(a.out) + ((long long)t * kHeads + h) * kHeadDim + d);
-  out[0] = __floats2bfloat162_rn(o[0], o[1]);
-  out[1] = __floats2bfloat162_rn(o[2], o[3]);
+  // peers may still read this CTA's shared memory until everyone is done
+  cluster_sync();
+  tc::tc_fence_after();
+  if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// Largest cluster the decode kernel may use on this device (16 where the
+// device schedules it, else the portable 8).
+int max_cluster() {
+  static int cached[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 8;
+  if (!cached[dev]) {
+    int best = 8;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16, 1, 1);
+    cfg.blockDim = dim3(AD_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = AD_SMEM;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 16;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                             1) == cudaSuccess &&
+        cudaOccupancyMaxActiveClusters(&n, attn_decode_kernel, &cfg) == cudaSuccess && n > 0)
+      best = 16;
+    cudaGetLastError();  // a refused query leaves no error behind
+    cached[dev] = best;
+  }
+  return cached[dev];
+}
+
+// Opt the kernel into its shared memory, once per device.
+cudaError_t prepare_kernel() {
+  static bool done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (done[dev]) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(
+      attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AD_SMEM);
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
 }
 
 }  // namespace
 
-int attn_record_floats() { return REC_FLOATS; }
+void attn_decode_geometry(const csa_attn_args &a, int *n_splits, int *tiles_per_split) {
+  const int tiles = (a.topk + a.window + CT - 1) / CT;
+  const int mc = prepare_kernel() == cudaSuccess ? max_cluster() : 8;
+  const int tps = (tiles + mc - 1) / mc;
+  *tiles_per_split = tps;
+  *n_splits = (tiles + tps - 1) / tps;
+}
 
-cudaError_t launch_attn(const csa_attn_args &a, int n_splits, int tiles_per_split,
-                        float *partials, cudaStream_t s) {
+cudaError_t launch_attn_decode(const csa_attn_args &a, cudaStream_t s) {
   if (a.n_rows <= 0) return cudaSuccess;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, ATTN_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
-  dim3 grid(n_splits, a.n_rows);
-  const int kid = n_splits == 1 ? CSA_K_ATTN_PREFILL : CSA_K_ATTN_PARTIAL;
-  launch_begin(kid, s);
-  attn_tc_kernel<<<grid, AT_THREADS, ATTN_SMEM, s>>>(a, n_splits, tiles_per_split, partials);
-  launch_end(kid, s);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || n_splits == 1) return e;
-  launch_begin(CSA_K_ATTN_COMBINE, s);
-  attn_combine_kernel<<<dim3(kHeads, a.n_rows), 128, 0, s>>>(a, n_splits, partials);
-  launch_end(CSA_K_ATTN_COMBINE, s);
-  return cudaGetLastError();
+  CUtensorMap qmap;
+  memset(&qmap, 0, sizeof(qmap));
+  if (!encode_rows_map(&qmap, a.q, (long long)a.n_rows * kHeads, kHeads))
+    return cudaErrorInvalidValue;
+  cudaError_t e = prepare_kernel();
+  if (e != cudaSuccess) return e;
+  int n_splits, tps;
+  attn_decode_geometry(a, &n_splits, &tps);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_splits, a.n_rows, 1);
+  cfg.blockDim = dim3(AD_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = AD_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = n_splits;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  launch_begin(CSA_K_ATTN_PARTIAL, s);
+  e = cudaLaunchKernelEx(&cfg, attn_decode_kernel, a, tps, qmap);
+  launch_end(CSA_K_ATTN_PARTIAL, s);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace csa

@@ -33,8 +33,7 @@
 
 #include <cstring>
 
-#include "csa_internal.cuh"
-#include "tc.cuh"
+#include "attn_common.cuh"
 
 namespace csa {
 namespace {
@@ -45,17 +44,7 @@ constexpr int AP_MMA_WARP = 1;
 constexpr int AP_SOFT0 = 2;   // first softmax warp
 constexpr int AP_SOFT = 256;  // softmax / gather / epilogue threads (warps 2..9)
 constexpr int AP_BAR = 1;     // their named barrier
-constexpr int CT = 128;       // candidates per tile
-constexpr int S_COL = 0, O_COL = 64;
-constexpr uint32_t AP_TMEM_COLS = 512;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleLog2 = 8.0f;
-
-constexpr int OFF_Q = 0;                   // 8 chunks x (64 heads x 128 B)
-constexpr int OFF_KV = OFF_Q + 8 * 8192;   // 8 chunks x (128 cands x 128 B)
-constexpr int OFF_P = OFF_KV + 8 * 16384;  // P^T, MN-major: 128 cands x 64 heads
-constexpr int OFF_MISC = OFF_P + 16384;
+using namespace attn;
 
 struct ApRow {
   int t, p, b;
@@ -73,10 +62,8 @@ struct ApMisc {
   ApRow row[2];
   int32_t tbl[64];            // the row's compressed-page table (up to 64 pages)
   const uint16_t *src[2][CT];  // pool row of each candidate of the tile, or null
-  alignas(16) float m_s[kHeads];  // running reference per head (log2 domain)
-  alignas(16) float corr_s[kHeads];
+  SoftState st;
   alignas(16) float inv_s[kHeads];
-  alignas(16) float red[4][kHeads];
   alignas(16) float red_l[4][kHeads];
 };
 constexpr int AP_SMEM = OFF_MISC + (int)sizeof(ApMisc) + 1024;
@@ -97,78 +84,6 @@ __device__ __forceinline__ bool ap_wait(uint64_t *bar, uint32_t parity, volatile
         return false;
       }
     }
-  }
-}
-
-__device__ __forceinline__ uint32_t pack2(float x, float y) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(x, y);
-  return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// P^T row c (one candidate): 64 heads as 8 swizzled 16-byte chunks.
-__device__ __forceinline__ uint8_t *prow_chunk(uint8_t *P, int c, int j) {
-  return P + (c >> 3) * 1024 + (c & 7) * 128 + ((j ^ (c & 7)) << 4);
-}
-
-// Column-wise reduction of x[0..31] over the 32 lanes (reduce-scatter):
-// afterwards lane l holds the reduction of column l.
-template <bool MAX>
-__device__ __forceinline__ float warp_col_reduce32(const float (&x)[32]) {
-  const int lane = threadIdx.x & 31;
-  float a[16];
-  {
-    const bool up = lane & 16;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float keep = up ? x[16 + i] : x[i], send = up ? x[i] : x[16 + i];
-      const float o = __shfl_xor_sync(0xffffffffu, send, 16);
-      a[i] = MAX ? fmaxf(keep, o) : keep + o;
-    }
-  }
-  float b[8];
-  {
-    const bool up = lane & 8;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float keep = up ? a[8 + i] : a[i], send = up ? a[i] : a[8 + i];
-      const float o = __shfl_xor_sync(0xffffffffu, send, 8);
-      b[i] = MAX ? fmaxf(keep, o) : keep + o;
-    }
-  }
-  float c[4];
-  {
-    const bool up = lane & 4;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float keep = up ? b[4 + i] : b[i], send = up ? b[i] : b[4 + i];
-      const float o = __shfl_xor_sync(0xffffffffu, send, 4);
-      c[i] = MAX ? fmaxf(keep, o) : keep + o;
-    }
-  }
-  float d[2];
-  {
-    const bool up = lane & 2;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float keep = up ? c[2 + i] : c[i], send = up ? c[i] : c[2 + i];
-      const float o = __shfl_xor_sync(0xffffffffu, send, 2);
-      d[i] = MAX ? fmaxf(keep, o) : keep + o;
-    }
-  }
-  const bool up = lane & 1;
-  const float keep = up ? d[1] : d[0], send = up ? d[0] : d[1];
-  const float o = __shfl_xor_sync(0xffffffffu, send, 1);
-  return MAX ? fmaxf(keep, o) : keep + o;
-}
-
-__device__ __forceinline__ void load32(const float *src, float (&v)[32]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float4 f = reinterpret_cast<const float4 *>(src)[i];
-    v[4 * i] = f.x;
-    v[4 * i + 1] = f.y;
-    v[4 * i + 2] = f.z;
-    v[4 * i + 3] = f.w;
   }
 }
 
@@ -203,8 +118,8 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
     M->abort = 0;
     tc::mbar_fence_init();
   }
-  if (tid < kHeads) M->m_s[tid] = -INFINITY;
-  if (warp == AP_MMA_WARP) tc::tmem_alloc(&M->tmem_base, AP_TMEM_COLS);
+  if (tid < kHeads) M->st.m[tid] = -INFINITY;
+  if (warp == AP_MMA_WARP) tc::tmem_alloc(&M->tmem_base, TMEM_COLS);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -331,8 +246,6 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
     if (!ok && q_loads) tc::mbar_wait(&M->q_full, (q_loads - 1) & 1, 50000000ull);
   } else if (warp == AP_MMA_WARP) {
     // ================================================================ MMA issuer
-    constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, kHeads);
-    constexpr uint32_t idesc_pv = tc::idesc_bf16_f32_mn(128, kHeads);
     const uint32_t kv = tc::smem_u32(KVs), qq = tc::smem_u32(Qs), pp = tc::smem_u32(Ps);
     uint32_t row_it = 0, tile_it = 0;
     bool ok = true;
@@ -349,11 +262,7 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
             ok = __all_sync(0xffffffffu, ap_wait(&M->q_rot, row_it & 1, abort, a.status_dev));
           if (!ok) break;
           tc::tc_fence_after();
-#pragma unroll
-          for (int s = 0; s < 4; ++s)
-            tc::mma_ss_elect(tmem + S_COL, tc::desc_sw128(kv + kc * 16384 + s * 32),
-                             tc::desc_sw128(qq + kc * 8192 + s * 32), idesc_qk,
-                             (kc | s) != 0 ? 1u : 0u);
+          issue_qk(tmem, kv, qq, kc);
         }
         if (!ok) break;
         tc::mma_commit_elect(&M->s_full);
@@ -367,12 +276,7 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
         if (!ok) break;
         tc::tc_fence_after();
         for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            tc::mma_ss_elect(tmem + O_COL + mt * 64,
-                             tc::desc_sw128_mn(kv + 2 * mt * 16384 + ks * 2048, 16384, 1024),
-                             tc::desc_sw128_mn(pp + ks * 2048, 16384, 1024), idesc_pv,
-                             (!first || ks > 0) ? 1u : 0u);
+          issue_pv(tmem, kv, pp, mt, !first);
           tc::mma_commit_elect(&M->kv_empty[mt]);
         }
         if (last) tc::mma_commit_elect(&M->o_full);
@@ -452,21 +356,7 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
         if (stid == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
       }
       if (rot) {
-        for (int e = stid; e < kHeads * 8; e += AP_SOFT) {
-          const int h = e >> 3, jj = e & 7;
-          uint4 *slot = reinterpret_cast<uint4 *>(Qs + 7 * 8192 + h * 128 + ((jj ^ (h & 7)) << 4));
-          const uint4 x4 = *slot;
-          uint32_t w[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int pair = jj * 4 + q;
-            const float cs = a.rope_cos[(long long)R.p * kRopeHalf + pair];
-            const float sn = a.rope_sin[(long long)R.p * kRopeHalf + pair];
-            const float x0 = __uint_as_float(w[q] << 16), x1 = __uint_as_float(w[q] & 0xFFFF0000u);
-            w[q] = pack2(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
-          }
-          *slot = make_uint4(w[0], w[1], w[2], w[3]);
-        }
+        rope_q_tile(Qs, a, R.p, stid, AP_SOFT);
         tc::fence_async_shared();
       }
       tc::bar_sync(AP_BAR, AP_SOFT);
@@ -486,66 +376,8 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
       for (uint32_t mm = R.tiles; mm && ok; mm &= mm - 1) {
         ok = tc::bar_and(AP_BAR, AP_SOFT, ok && ap_wait(&M->s_full, tile_it & 1, abort, a.status_dev));
         if (!ok) break;
-        tc::tc_fence_after();
         float x[32];
-        tc::tmem_ld32(tmem + lane_off + S_COL + h0, x);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = valid ? x[j] * sl2 : -INFINITY;
-        float mref[32];
-        load32(M->m_s + h0, mref);
-        bool exceed = false;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) exceed |= x[j] > mref[j] + kRescaleLog2;
-        if (tc::bar_or(AP_BAR, AP_SOFT, exceed)) {
-          // move the reference of the heads whose maximum grew past 2^8
-          const float mx = warp_col_reduce32<true>(x);
-          const int h = h0 + lane;
-          M->red[qd][h] = mx;
-          tc::bar_sync(AP_BAR, AP_SOFT);
-          const float mt = fmaxf(fmaxf(M->red[0][h], M->red[1][h]), fmaxf(M->red[2][h], M->red[3][h]));
-          const float mo = M->m_s[h];
-          float mn = mo, corr = 1.f;
-          if (mo == -INFINITY) {
-            mn = mt;
-          } else if (mt > mo + kRescaleLog2) {
-            mn = mt;
-            corr = exp2f(mo - mt);
-          }
-          tc::bar_sync(AP_BAR, AP_SOFT);
-          if (qd == 0) {
-            M->m_s[h] = mn;
-            M->corr_s[h] = corr;
-          }
-          lacc *= corr;  // every warp's partial denominator of head h moves with it
-          tc::bar_sync(AP_BAR, AP_SOFT);
-          load32(M->m_s + h0, mref);
-          if (!first) {
-            float cr[32];
-            load32(M->corr_s + h0, cr);
-            bool any = false;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) any |= cr[j] != 1.f;
-            if (__any_sync(0xffffffffu, any)) {
-#pragma unroll 1
-              for (int m4 = 0; m4 < 4; ++m4) {
-                float v[32];
-                const uint32_t addr = tmem + lane_off + O_COL + m4 * 64 + h0;
-                tc::tmem_ld32(addr, v);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] *= cr[j];
-                tc::tmem_st32(addr, v);
-              }
-            }
-          }
-        }
-        // ---- P = 2^(x - m) as BF16 into the MN-major P^T rows
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = mref[j] == -INFINITY ? 0.f : exp2f(x[j] - mref[j]);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4 *>(prow_chunk(Ps, c, (h0 >> 3) + q)) =
-              make_uint4(pack2(x[8 * q], x[8 * q + 1]), pack2(x[8 * q + 2], x[8 * q + 3]),
-                         pack2(x[8 * q + 4], x[8 * q + 5]), pack2(x[8 * q + 6], x[8 * q + 7]));
+        softmax_tile(tmem, qd, h0, valid, sl2, first, &M->st, Ps, AP_BAR, lacc, x);
         tc::fence_async_shared();
         tc::tc_fence_before();
         tc::bar_sync(AP_BAR, AP_SOFT);
@@ -577,7 +409,7 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
       if (qd == 0) {
         const int h = h0 + lane;
         const float s2 = a.sink ? a.sink[h] * kLog2e : -INFINITY;
-        float m = M->m_s[h];
+        float m = M->st.m[h];
         float l = (M->red_l[0][h] + M->red_l[1][h]) + (M->red_l[2][h] + M->red_l[3][h]);
         if (m == -INFINITY) {
           m = s2;
@@ -618,7 +450,7 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
       tc::tc_fence_before();
       tc::bar_sync(AP_BAR, AP_SOFT);
       if (stid == 0) tc::mbar_arrive(&M->o_empty);
-      if (qd == 0) M->m_s[h0 + lane] = -INFINITY;
+      if (qd == 0) M->st.m[h0 + lane] = -INFINITY;
       ++row_it;
     }
     tc::cp_async_wait<0>();
@@ -627,7 +459,7 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == AP_MMA_WARP) tc::tmem_dealloc(tmem, AP_TMEM_COLS);
+  if (warp == AP_MMA_WARP) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -644,8 +476,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return encode;
 }
 
-// 2D BF16 tensor map [rows, 512] with a row stride of 1024 bytes, box
-// {64 channels, box_rows}, 128-byte swizzle (the q rows of a query row).
+}  // namespace
+
+namespace attn {
 bool encode_rows_map(CUtensorMap *map, const void *base, long long rows, int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode || rows <= 0 || rows > 0x7FFFFFFFll) return false;
@@ -658,8 +491,7 @@ bool encode_rows_map(CUtensorMap *map, const void *base, long long rows, int box
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
 }
-
-}  // namespace
+}  // namespace attn
 
 bool attn_prefill_supported(const csa_attn_args &a) { return a.topk + a.window <= 32 * CT; }
 

@@ -116,8 +116,12 @@ def test_workspace_queries_and_validation(L):
     aa = b.AttnArgs()
     aa.struct_size = ctypes.sizeof(aa)
     aa.n_rows, aa.n_heads, aa.head_dim, aa.ratio, aa.topk, aa.window = 8, 64, 512, 4, 2048, 128
+    # both attention calls keep their scratch on chip (the decode split merges
+    # in distributed shared memory): no workspace
+    aa.workspace_bytes = 123
     assert L.csa_sparse_attn_decode(ctypes.byref(aa), None) == b.CSA_OK
-    assert aa.workspace_bytes > 0
+    assert aa.workspace_bytes == 0
+    aa.workspace_bytes = 123
     assert L.csa_sparse_attn_prefill(ctypes.byref(aa), None) == b.CSA_OK
     assert aa.workspace_bytes == 0
     aa.window = 64
