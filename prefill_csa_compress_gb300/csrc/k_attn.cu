@@ -32,16 +32,17 @@ constexpr int AD_BAR = 1;  // named barrier over all 256 threads (the softmax's)
 constexpr int AD_MAX_CLUSTER = 16;
 
 struct AdMisc {
-  uint64_t q_full, mma_bar, done_bar;
+  uint64_t q_full, mma_bar, done_bar, recv_bar;
   uint32_t tmem_base;
   int pad;
   SoftState st;
   const uint16_t *src[CT];  // pool row of each candidate of the tile, or null
-  alignas(16) float m_loc[kHeads];  // this CTA's reference per head (log2), -inf if none
-  alignas(16) float l_loc[kHeads];  // this CTA's denominator per head
+  alignas(16) float m_all[AD_MAX_CLUSTER][kHeads];  // every CTA's reference per head (log2)
+  alignas(16) float l_all[AD_MAX_CLUSTER][kHeads];  // every CTA's denominator per head
   alignas(16) float red_l[4][kHeads];
   alignas(16) float w_all[AD_MAX_CLUSTER][kHeads];  // scale of each CTA's partial
   alignas(16) float inv_L[kHeads];
+  alignas(16) float inv_l[kHeads];  // 1 / this CTA's denominator per head
 };
 constexpr int AD_SMEM = OFF_MISC + (int)sizeof(AdMisc) + 1024;
 static_assert(AD_SMEM <= 227 * 1024, "shared memory");
@@ -52,31 +53,45 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   return r;
 }
 
+// Split cluster barrier: arrive early, wait where it matters.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
                    "memory");
 }
 
-// Address of `p` (this CTA's shared memory) in the shared memory of CTA `rank`.
-__device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank) {
+// Address of shared-memory address `la` (this CTA) in the shared memory of CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr_u32(uint32_t la, uint32_t rank) {
   uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(tc::smem_u32(p)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(la), "r"(rank));
   return r;
 }
 
-__device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
+__device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank) {
+  return peer_addr_u32(tc::smem_u32(p), rank);
 }
 
-__device__ __forceinline__ float4 ld_peer_f32x4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
+__device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to the
+// shared memory of CTA `rank`, completing on that CTA's mbarrier.
+__device__ __forceinline__ void bulk_to_peer(const void *src, uint32_t dst_local, uint32_t bytes,
+                                             uint64_t *bar_local, uint32_t rank) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(peer_addr_u32(dst_local, rank)),
+      "r"(tc::smem_u32(src)), "r"(bytes), "r"(peer_addr(bar_local, rank))
+      : "memory");
 }
 
 // Pool row of candidate j of row t (its list: top-k entries, then the
@@ -115,7 +130,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   uint8_t *Qs = sm + OFF_Q;
   uint8_t *KVs = sm + OFF_KV;
   uint8_t *Ps = sm + OFF_P;
-  float *Os = reinterpret_cast<float *>(KVs);  // O[h][d] (FP32) once the tiles are done
+  // once the tiles are done: this CTA's normalised partial O[h][d] / l[h] (BF16)
+  uint16_t *Os = reinterpret_cast<uint16_t *>(KVs);
   AdMisc *M = reinterpret_cast<AdMisc *>(sm + OFF_MISC);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.y;
@@ -137,9 +153,13 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     tc::mbar_init(&M->q_full, 1);
     tc::mbar_init(&M->mma_bar, 1);
     tc::mbar_init(&M->done_bar, 1);
+    tc::mbar_init(&M->recv_bar, 1);
     tc::mbar_fence_init();
   }
   if (tid < kHeads) M->st.m[tid] = -INFINITY;
+  // every CTA of the cluster must have started before any of them touches a
+  // peer's shared memory: the matching wait comes before the first remote store
+  cluster_arrive_relaxed();
   if (warp == 0) tc::tmem_alloc(&M->tmem_base, TMEM_COLS);
   tc::tc_fence_before();
   __syncthreads();
@@ -160,6 +180,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     if (tid == 0 && s == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
   }
 
+  // the sink logit of head tid, read now rather than at the merge
+  const float sink2 = tid < kHeads && a.sink ? a.sink[tid] * kLog2e : -INFINITY;
   const int qd = warp & 3, h0 = (warp >> 2) * 32, c = qd * 32 + lane;
   const int sub = lane >> 3, piece = lane & 7;  // gather: rows 32 i + 4 warp + sub, 16-byte piece
   const float sl2 = a.softmax_scale * kLog2e;
@@ -238,42 +260,80 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     tc::mbar_wait(&M->done_bar, 0, 100000000ull);
   }
 
-  // ---- this CTA's partial: per-head reference and denominator, O^T as O[h][d]
+  // ---- this CTA's partial: its per-head reference and denominator go to
+  // every CTA of the cluster (remote stores, ordered by the cluster barrier);
+  // O^T / l stays here as BF16 O[h][d] (normalised, so BF16 keeps it to
+  // 2^-9 relative whatever the magnitudes)
   M->red_l[qd][h0 + lane] = lacc;
   __syncthreads();
   if (tid < kHeads) {
-    const int h = tid;
-    M->m_loc[h] = first ? -INFINITY : M->st.m[h];
-    M->l_loc[h] = first ? 0.f : (M->red_l[0][h] + M->red_l[1][h]) + (M->red_l[2][h] + M->red_l[3][h]);
+    const float l = (M->red_l[0][tid] + M->red_l[1][tid]) + (M->red_l[2][tid] + M->red_l[3][tid]);
+    M->inv_l[tid] = !first && l > 0.f ? 1.f / l : 0.f;
   }
-  if (!first) {
+  cluster_wait();
+  for (int e = tid; e < kHeads * (int)S; e += AD_THREADS) {
+    const int h = e % kHeads;
+    const uint32_t q = e / kHeads;
+    const float m = first ? -INFINITY : M->st.m[h];
+    const float l =
+        first ? 0.f : (M->red_l[0][h] + M->red_l[1][h]) + (M->red_l[2][h] + M->red_l[3][h]);
+    st_peer_f32(peer_addr(&M->m_all[s][h], q), m);
+    st_peer_f32(peer_addr(&M->l_all[s][h], q), l);
+  }
+  __syncthreads();
+  // output slices: CTA r normalises units [slice_lo(r), slice_lo(r + 1)) of
+  // 8 channels; peers send it their part of that slice into its (now free) q
+  // buffer, one region per sender (regions of senders above r move down one,
+  // so S - 1 regions of kUnits / S + 1 units fit in the 64 KB)
+  constexpr int kUnits = kHeads * kHeadDim / 8;
+  auto slice_lo = [&](uint32_t r) { return (int)((long long)kUnits * r / S); };
+  const int u0 = slice_lo(s), u1 = slice_lo(s + 1);
+  const uint32_t region = (uint32_t)(kUnits / S + 1) * 16;  // bytes per sender
+  if (tid == 0) tc::mbar_arrive_expect_tx(&M->recv_bar, (uint32_t)(u1 - u0) * 16 * (S - 1));
+  if (first) {
+    // no candidates here: a zero partial, so that peers may read it unmasked
+    for (int e = tid; e < kHeads * kHeadDim / 8; e += AD_THREADS)
+      reinterpret_cast<uint4 *>(Os)[e] = make_uint4(0u, 0u, 0u, 0u);
+  } else {
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    float il[32];
+    load32(M->inv_l + h0, il);
 #pragma unroll 1
     for (int m4 = 0; m4 < 4; ++m4) {
       float v[32];
       tc::tmem_ld32(tmem + lane_off + O_COL + m4 * 64 + h0, v);
       const int d = m4 * 128 + qd * 32 + lane;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) Os[(h0 + j) * kHeadDim + d] = v[j];
+      for (int j = 0; j < 32; ++j)
+        Os[(h0 + j) * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j] * il[j]));
     }
   }
+  tc::fence_async_shared();  // the parked partial is read by the bulk copies
   tc::tc_fence_before();
   cluster_sync();
+  if (tid == 0)
+    for (uint32_t r = 0; r < S; ++r) {
+      if (r == s) continue;
+      const int lo = slice_lo(r), hi = slice_lo(r + 1);
+      const uint32_t slot = s < r ? s : s - 1;
+      bulk_to_peer(Os + (size_t)lo * 8, tc::smem_u32(Qs) + slot * region, (uint32_t)(hi - lo) * 16,
+                   &M->recv_bar, r);
+    }
 
-  // ---- merge weights: one thread per head reads every CTA's statistics
+  // ---- merge weights: one thread per head, from the statistics every CTA sent
   if (tid < kHeads) {
     const int h = tid;
-    const float s2 = a.sink ? a.sink[h] * kLog2e : -INFINITY;
+    const float s2 = sink2;
     float mx = s2;
-    for (uint32_t q = 0; q < S; ++q) mx = fmaxf(mx, ld_peer_f32(peer_addr(&M->m_loc[h], q)));
+    for (uint32_t q = 0; q < S; ++q) mx = fmaxf(mx, M->m_all[q][h]);
     float L = 0.f;
     if (mx != -INFINITY) {
       L = exp2f(s2 - mx);
       for (uint32_t q = 0; q < S; ++q) {
-        const float mq = ld_peer_f32(peer_addr(&M->m_loc[h], q));
+        const float mq = M->m_all[q][h];
         const float w = mq == -INFINITY ? 0.f : exp2f(mq - mx);
-        M->w_all[q][h] = w;
-        if (w != 0.f) L += w * ld_peer_f32(peer_addr(&M->l_loc[h], q));
+        M->w_all[q][h] = w * M->l_all[q][h];  // the partial was parked divided by l
+        L += w * M->l_all[q][h];
       }
     } else {
       for (uint32_t q = 0; q < S; ++q) M->w_all[q][h] = 0.f;
@@ -284,40 +344,44 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   }
   __syncthreads();
 
-  // ---- this CTA's slice of the output: 4 channels per step, all partials
+  // ---- this CTA's slice of the output, 8 channels per step: its own part
+  // from the parked partial, the peers' parts from the receive regions
+  if (S > 1 && !tc::mbar_wait(&M->recv_bar, 0)) flag(a.status_dev, CSA_DEV_TIMEOUT);
   const bool inv = a.inv_rope_out && a.rope_cos != nullptr && p >= 0 && p < a.rope_cap;
   __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + (long long)t * kHeads * kHeadDim;
-  constexpr int kUnits = kHeads * kHeadDim / 4;
-  const int u0 = (int)((long long)kUnits * s / S), u1 = (int)((long long)kUnits * (s + 1) / S);
   for (int u = u0 + tid; u < u1; u += AD_THREADS) {
-    const int h = u / (kHeadDim / 4), d = (u % (kHeadDim / 4)) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int h = u / (kHeadDim / 8), d = (u % (kHeadDim / 8)) * 8;
+    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (uint32_t q = 0; q < S; ++q) {
+      const uint32_t slot = q < s ? q : q - 1;
+      const uint4 v = q == s ? reinterpret_cast<const uint4 *>(Os)[u]
+                             : *reinterpret_cast<const uint4 *>(Qs + slot * region + (u - u0) * 16);
       const float w = M->w_all[q][h];
-      if (w == 0.f) continue;
-      const float4 v = ld_peer_f32x4(peer_addr(Os + h * kHeadDim + d, q));
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
-    }
-    const float il = M->inv_L[h];
-    float o[4] = {acc.x * il, acc.y * il, acc.z * il, acc.w * il};
-    if (inv && d >= kHeadDim - kRopeDim) {
+      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int q2 = 0; q2 < 2; ++q2) {
-        const int pair = (d + 2 * q2 - (kHeadDim - kRopeDim)) >> 1;
-        const float cs = a.rope_cos[(long long)p * kRopeHalf + pair];
-        const float sn = a.rope_sin[(long long)p * kRopeHalf + pair];
-        const float x0 = o[2 * q2], x1 = o[2 * q2 + 1];
-        o[2 * q2] = x0 * cs + x1 * sn;
-        o[2 * q2 + 1] = -x0 * sn + x1 * cs;
+      for (int i = 0; i < 4; ++i) {
+        o[2 * i] = fmaf(w, __uint_as_float(wd[i] << 16), o[2 * i]);
+        o[2 * i + 1] = fmaf(w, __uint_as_float(wd[i] & 0xFFFF0000u), o[2 * i + 1]);
       }
     }
-    uint2 packed = make_uint2(pack2(o[0], o[1]), pack2(o[2], o[3]));
-    *reinterpret_cast<uint2 *>(out + h * kHeadDim + d) = packed;
+    const float il = M->inv_L[h];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] *= il;
+    if (inv && d >= kHeadDim - kRopeDim) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int pair = (d + 2 * i - (kHeadDim - kRopeDim)) >> 1;
+        const float cs = a.rope_cos[(long long)p * kRopeHalf + pair];
+        const float sn = a.rope_sin[(long long)p * kRopeHalf + pair];
+        const float x0 = o[2 * i], x1 = o[2 * i + 1];
+        o[2 * i] = x0 * cs + x1 * sn;
+        o[2 * i + 1] = -x0 * sn + x1 * cs;
+      }
+    }
+    *reinterpret_cast<uint4 *>(out + h * kHeadDim + d) =
+        make_uint4(pack2(o[0], o[1]), pack2(o[2], o[3]), pack2(o[4], o[5]), pack2(o[6], o[7]));
   }
-  // peers may still read this CTA's shared memory until everyone is done
+  // this CTA's outgoing copies have landed once every peer is through its wait
   cluster_sync();
   tc::tc_fence_after();
   if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
