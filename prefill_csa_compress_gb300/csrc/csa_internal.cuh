@@ -26,6 +26,44 @@ void launch_end(int kernel_id, cudaStream_t s);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Launch a kernel with programmatic dependent launch: it may be scheduled
+// while the previous kernel on the stream finishes, and waits for it in
+// griddep_wait() before touching global memory.  `cluster_x` > 0 launches
+// clusters of that many CTAs along x; `cooperative` makes the grid's CTAs
+// co-resident (the launch fails if they cannot all be) and is launched
+// without the early start.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, int cluster_x, bool cooperative, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[3];
+  unsigned n = 0;
+  if (!cooperative) {  // a cooperative grid is launched whole, after its predecessor
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 0) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = (unsigned)cluster_x;
+    attrs[n].val.clusterDim.y = 1;
+    attrs[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (cooperative) {
+    attrs[n].id = cudaLaunchAttributeCooperative;
+    attrs[n].val.cooperative = 1;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Launchers (one per kernel family); each returns cudaGetLastError().
 cudaError_t launch_compress(const csa_compress_args &a, float *logits, cudaStream_t s);
 // Words per row of the long-row top-k control block (barrier counter and

@@ -133,6 +133,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   // once the tiles are done: this CTA's normalised partial O[h][d] / l[h] (BF16)
   uint16_t *Os = reinterpret_cast<uint16_t *>(KVs);
   AdMisc *M = reinterpret_cast<AdMisc *>(sm + OFF_MISC);
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.y;
   const uint32_t s = cluster_rank(), S = gridDim.x;
@@ -451,20 +453,9 @@ cudaError_t launch_attn_decode(const csa_attn_args &a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   int n_splits, tps;
   attn_decode_geometry(a, &n_splits, &tps);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_splits, a.n_rows, 1);
-  cfg.blockDim = dim3(AD_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = AD_SMEM;
-  cfg.stream = s;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = n_splits;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
   launch_begin(CSA_K_ATTN_PARTIAL, s);
-  e = cudaLaunchKernelEx(&cfg, attn_decode_kernel, a, tps, qmap);
+  e = launch_kernel(attn_decode_kernel, dim3(n_splits, a.n_rows), dim3(AD_THREADS),
+                    (size_t)AD_SMEM, s, n_splits, false, a, tps, qmap);
   launch_end(CSA_K_ATTN_PARTIAL, s);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -96,6 +96,8 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
   uint8_t *KVs = sm + OFF_KV;
   uint8_t *Ps = sm + OFF_P;
   ApMisc *M = reinterpret_cast<ApMisc *>(sm + OFF_MISC);
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_cand = a.topk + a.window;
   volatile int *abort = &M->abort;
@@ -516,9 +518,10 @@ cudaError_t launch_attn_prefill(const csa_attn_args &a, cudaStream_t s) {
     sms = 148;
   const int grid = a.n_rows < sms ? a.n_rows : sms;
   launch_begin(CSA_K_ATTN_PREFILL, s);
-  attn_prefill_kernel<<<grid, AP_THREADS, AP_SMEM, s>>>(a, qmap);
+  const cudaError_t e = launch_kernel(attn_prefill_kernel, dim3(grid), dim3(AP_THREADS),
+                                      (size_t)AP_SMEM, s, 0, false, a, qmap);
   launch_end(CSA_K_ATTN_PREFILL, s);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace csa

@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const uint16_t *__rest
                                                           const uint16_t *__restrict__ w,
                                                           float *__restrict__ logits, int n_rows,
                                                           int dx, int d) {
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
   __shared__ float xs[GT_ROWS][GT_K + 1];
   __shared__ float ws[GT_K][GT_COLS];
   const int tx = threadIdx.x % GT_COLS;
@@ -87,6 +89,8 @@ __device__ __forceinline__ float block_max(float v, float *red) {
 }
 
 __global__ void compress_pool_kernel(csa_compress_args a, const float *__restrict__ logits) {
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
   __shared__ float ys[512];
   __shared__ float red[32];
   const int t = blockIdx.x;
@@ -174,6 +178,8 @@ constexpr int FC_MAX_W_BYTES = 128 * 1024;
 
 template <int COLS>
 __global__ void __launch_bounds__(FC_THREADS) compress_fused_kernel(csa_compress_args a) {
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
   extern __shared__ __align__(16) uint8_t fc_smem[];
   constexpr int PARTS = FC_THREADS / COLS;
   const int dx = a.dx, D = a.d, r = a.ratio;
@@ -311,9 +317,10 @@ cudaError_t launch_fused(const csa_compress_args &a, cudaStream_t s) {
     attr[dev] = true;
   }
   launch_begin(CSA_K_COMPRESS_POOL, s);
-  compress_fused_kernel<COLS><<<dim3(a.d / COLS, a.n_rows), FC_THREADS, smem, s>>>(a);
+  const cudaError_t e = launch_kernel(compress_fused_kernel<COLS>, dim3(a.d / COLS, a.n_rows),
+                                      dim3(FC_THREADS), smem, s, 0, false, a);
   launch_end(CSA_K_COMPRESS_POOL, s);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -329,16 +336,17 @@ cudaError_t launch_compress(const csa_compress_args &a, float *logits, cudaStrea
   }
   dim3 g1((a.d + GT_COLS - 1) / GT_COLS, (a.n_rows + GT_ROWS - 1) / GT_ROWS);
   launch_begin(CSA_K_COMPRESS_GATE, s);
-  gate_logits_kernel<<<g1, 256, 0, s>>>(static_cast<const uint16_t *>(a.x),
-                                        static_cast<const uint16_t *>(a.w_gate), logits, a.n_rows,
-                                        a.dx, a.d);
+  cudaError_t e = launch_kernel(gate_logits_kernel, g1, dim3(256), 0, s, 0, false,
+                                static_cast<const uint16_t *>(a.x),
+                                static_cast<const uint16_t *>(a.w_gate), logits, a.n_rows, a.dx,
+                                a.d);
   launch_end(CSA_K_COMPRESS_GATE, s);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   launch_begin(CSA_K_COMPRESS_POOL, s);
-  compress_pool_kernel<<<a.n_rows, a.d, 0, s>>>(a, logits);
+  e = launch_kernel(compress_pool_kernel, dim3(a.n_rows), dim3(a.d), 0, s, 0, false, a,
+                    static_cast<const float *>(logits));
   launch_end(CSA_K_COMPRESS_POOL, s);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace csa

@@ -181,6 +181,8 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
   __shared__ int warp_sums[32];
   __shared__ int s_digit, s_above, s_ok;
   __shared__ int s_gt_before, s_eq_before;
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
   const int t = row0 + blockIdx.y, s = blockIdx.x, tid = threadIdx.x, warp = tid >> 5;
   const int b = a.row_req[t];
   if (b < 0 || b >= a.n_req) return;  // uniform over the row's CTAs
@@ -396,10 +398,11 @@ cudaError_t launch_short(const csa_index_args &a, const float *scores, int cols,
   cudaError_t e = allow_smem(kern, smem, done);
   if (e != cudaSuccess) return e;
   constexpr int kMaxGridY = 65535;
-  for (int row0 = 0; row0 < a.n_rows; row0 += kMaxGridY)
-    kern<<<dim3(1, std::min(kMaxGridY, a.n_rows - row0)), NT, smem, s>>>(
-        a, scores, cols, row0, 1, NT * TK_SHORT_KPT, nullptr, nullptr);
-  return cudaGetLastError();
+  for (int row0 = 0; row0 < a.n_rows && e == cudaSuccess; row0 += kMaxGridY)
+    e = launch_kernel(kern, dim3(1, std::min(kMaxGridY, a.n_rows - row0)), dim3(NT),
+                      (size_t)smem, s, 0, false, a, scores, cols, row0, 1, NT * TK_SHORT_KPT,
+                      static_cast<uint32_t *>(nullptr), static_cast<uint32_t *>(nullptr));
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 struct LongLayout {
@@ -481,10 +484,8 @@ cudaError_t launch_index_topk(const csa_index_args &a, const float *scores, int 
   launch_begin(CSA_K_INDEX_TOPK, s);
   for (int row0 = 0; row0 < a.n_rows && e == cudaSuccess; row0 += rows_per_launch) {
     const int nr = std::min(rows_per_launch, a.n_rows - row0);
-    int r0 = row0, SS = S, sl = slice;
-    void *args[] = {&aa, &sp, &cols, &r0, &SS, &sl, &ctl, &rec};
-    e = cudaLaunchCooperativeKernel((const void *)kern, dim3(S, nr), dim3(TK_LONG_THREADS), args,
-                                    smem, s);
+    e = launch_kernel(kern, dim3(S, nr), dim3(TK_LONG_THREADS), (size_t)smem, s, 0, true, aa, sp,
+                      cols, row0, S, slice, ctl, rec);
   }
   launch_end(CSA_K_INDEX_TOPK, s);
   return e != cudaSuccess ? e : cudaGetLastError();

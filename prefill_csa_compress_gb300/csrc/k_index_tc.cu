@@ -135,6 +135,8 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   float *Ws = reinterpret_cast<float *>(sm + C::OFF_W);
   float *Rope = reinterpret_cast<float *>(sm + C::OFF_ROPE);
   IdxMisc *M = reinterpret_cast<IdxMisc *>(sm + C::OFF_MISC);
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   if (zero_ctr) {
@@ -586,10 +588,11 @@ cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, uint32_t
   const long long n_units = (long long)n_groups * upg;
   const int grid = (int)(n_units < sms ? n_units : sms);
   launch_begin(CSA_K_INDEX_SCORE, s);
-  index_score_tc_kernel<G><<<grid, IT_THREADS, C::SMEM, s>>>(a, scores, cols, n_groups, chunk,
-                                                             upg, zero_ctr, keys_map);
+  const cudaError_t e = launch_kernel(index_score_tc_kernel<G>, dim3(grid), dim3(IT_THREADS),
+                                      (size_t)C::SMEM, s, 0, false, a, scores, cols, n_groups,
+                                      chunk, upg, zero_ctr, keys_map);
   launch_end(CSA_K_INDEX_SCORE, s);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -105,6 +105,20 @@ __device__ __forceinline__ void tma_gather4(void *dst, const void *tmap, int x, 
       : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Wait until the grids this one depends on (the previous kernel on the
+// stream, when launched with programmatic serialization) have completed and
+// their memory is visible; a no-op otherwise.  Every kernel calls it before
+// its first global-memory access.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next kernel on the stream be scheduled now (it still waits for
+// this grid's completion in its own griddep_wait).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- named barriers
 
 __device__ __forceinline__ void bar_sync(int id, int n_threads) {
