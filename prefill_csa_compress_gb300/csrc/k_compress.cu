@@ -6,11 +6,176 @@
 // and "Serving-owned full RoPE tables" (group-start rotation); "DeepSeek
 // V4-Flash, MTP point", "What is quantized" (INT8 on write, amax floored at
 // 1e-4, scaled to 127).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
 #include "csa_internal.cuh"
 #include "tc.cuh"
 
 namespace csa {
 namespace {
+
+// ---------------------------------------------------------------------------
+// Long chunks on the tensor cores: logits[t, d] = sum_k x[t, k] w_gate[k, d].
+// One CTA per 128-row x 128-column tile of logits.  x tiles (K-major) and
+// w_gate tiles (read as they lie, N-major: 64 columns of one k per 128-byte
+// row) arrive by TMA into a 4-stage ring of 64-wide K chunks; one elected
+// thread issues M = 128, N = 128, K = 16 BF16 MMAs into TMEM; four warps read
+// the FP32 tile back (lane = row) and store it.
+// ---------------------------------------------------------------------------
+constexpr int GG_THREADS = 128;
+constexpr int GG_M = 128, GG_N = 128, GG_K = 64, GG_STAGES = 4;
+constexpr int GG_A_BYTES = GG_M * GG_K * 2;   // 16 KB
+constexpr int GG_B_BYTES = GG_N * GG_K * 2;   // 16 KB: two 64-column groups of 8 KB
+constexpr int GG_STAGE = GG_A_BYTES + GG_B_BYTES;
+constexpr int GG_SMEM = GG_STAGES * GG_STAGE + 1024 + 256;
+
+__global__ void __launch_bounds__(GG_THREADS, 1)
+    gate_gemm_tc_kernel(float *__restrict__ logits, int n_rows, int dx, int d,
+                        const __grid_constant__ CUtensorMap xmap,
+                        const __grid_constant__ CUtensorMap wmap, uint32_t *status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~uintptr_t(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(sm + GG_STAGES * GG_STAGE);
+  uint64_t *empty = full + GG_STAGES;
+  uint64_t *acc_full = empty + GG_STAGES;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row0 = blockIdx.y * GG_M, col0 = blockIdx.x * GG_N;
+  const int n_k = dx / GG_K;
+  if (tid == 0) {
+    for (int i = 0; i < GG_STAGES; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+    }
+    tc::mbar_init(acc_full, 1);
+    tc::mbar_fence_init();
+  }
+  if (warp == 0) tc::tmem_alloc(tmem_slot, GG_N);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+  if (warp == 0) {
+    if (lane == 0)
+      for (int kc = 0; kc < n_k && ok; ++kc) {
+        const int st = kc % GG_STAGES;
+        if (kc >= GG_STAGES && !tc::mbar_wait(&empty[st], ((kc / GG_STAGES) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        uint8_t *A = sm + st * GG_STAGE, *B = A + GG_A_BYTES;
+        tc::mbar_arrive_expect_tx(&full[st], GG_STAGE);
+        tc::tma_load_2d(A, &xmap, kc * GG_K, row0, &full[st]);
+        tc::tma_load_2d(B, &wmap, col0, kc * GG_K, &full[st]);
+        tc::tma_load_2d(B + GG_B_BYTES / 2, &wmap, col0 + 64, kc * GG_K, &full[st]);
+      }
+  } else if (warp == 1) {
+    // A K-major, B N-major (w_gate rows are k)
+    constexpr uint32_t idesc = tc::idesc_bf16_f32(GG_M, GG_N) | (1u << 16);
+    for (int kc = 0; kc < n_k && ok; ++kc) {
+      const int st = kc % GG_STAGES;
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&full[st], (kc / GG_STAGES) & 1));
+      if (!ok) break;
+      tc::tc_fence_after();
+      const uint32_t A = tc::smem_u32(sm + st * GG_STAGE), B = A + GG_A_BYTES;
+#pragma unroll
+      for (int k16 = 0; k16 < GG_K / 16; ++k16)
+        tc::mma_ss_elect(tmem, tc::desc_sw128(A + k16 * 32),
+                         tc::desc_sw128_mn(B + k16 * 2048, GG_B_BYTES / 2, 1024), idesc,
+                         (kc | k16) != 0 ? 1u : 0u);
+      tc::mma_commit_elect(&empty[st]);
+    }
+    tc::mma_commit_elect(acc_full);
+  }
+  __syncwarp();
+  // ---- epilogue: lane = row, 128 FP32 columns
+  if (!tc::mbar_wait(acc_full, 0)) {
+    ok = false;
+    if (tid == 0) flag(status, CSA_DEV_TIMEOUT);
+  }
+  tc::tc_fence_after();
+  const int row = row0 + warp * 32 + lane;
+#pragma unroll 1
+  for (int c32 = 0; c32 < GG_N / 32; ++c32) {
+    float v[32];
+    tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c32 * 32, v);
+    if (ok && row < n_rows) {
+      float4 *dst = reinterpret_cast<float4 *>(logits + (long long)row * d + col0 + c32 * 32);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 0) tc::tmem_dealloc(tmem, GG_N);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 gg_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return nullptr;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return encode;
+}
+
+// 2D BF16 map [outer, inner] (row stride inner * 2 bytes), box {64, box_outer},
+// 128-byte swizzle.
+bool gg_map(CUtensorMap *map, const void *base, long long inner, long long outer, int box_outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = gg_encoder();
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+// The tensor-core gate GEMM covers K in 64s, N in 128s and 16-byte-aligned
+// operands; other shapes take the CUDA-core kernel below.
+bool gate_gemm_tc_ok(const csa_compress_args &a, const float *logits) {
+  return a.dx % GG_K == 0 && a.d % GG_N == 0 && a.dx >= GG_K &&
+         (reinterpret_cast<uintptr_t>(a.x) & 15u) == 0 &&
+         (reinterpret_cast<uintptr_t>(a.w_gate) & 15u) == 0 &&
+         (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
+}
+
+cudaError_t launch_gate_gemm_tc(const csa_compress_args &a, float *logits, cudaStream_t s) {
+  CUtensorMap xmap, wmap;
+  memset(&xmap, 0, sizeof(xmap));
+  memset(&wmap, 0, sizeof(wmap));
+  if (!gg_map(&xmap, a.x, a.dx, a.n_rows, GG_M) || !gg_map(&wmap, a.w_gate, a.d, a.dx, GG_K))
+    return cudaErrorInvalidValue;
+  static bool attr[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(gate_gemm_tc_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, GG_SMEM);
+    if (e != cudaSuccess) return e;
+    attr[dev] = true;
+  }
+  const dim3 grid(a.d / GG_N, (a.n_rows + GG_M - 1) / GG_M);
+  return launch_kernel(gate_gemm_tc_kernel, grid, dim3(GG_THREADS), (size_t)GG_SMEM, s, 0, false,
+                       logits, a.n_rows, a.dx, a.d, xmap, wmap, a.status_dev);
+}
 
 // ---------------------------------------------------------------------------
 // logits[t, d] = sum_k x[t, k] * w_gate[k, d]   (FP32 accumulate)
@@ -336,10 +501,12 @@ cudaError_t launch_compress(const csa_compress_args &a, float *logits, cudaStrea
   }
   dim3 g1((a.d + GT_COLS - 1) / GT_COLS, (a.n_rows + GT_ROWS - 1) / GT_ROWS);
   launch_begin(CSA_K_COMPRESS_GATE, s);
-  cudaError_t e = launch_kernel(gate_logits_kernel, g1, dim3(256), 0, s, 0, false,
-                                static_cast<const uint16_t *>(a.x),
-                                static_cast<const uint16_t *>(a.w_gate), logits, a.n_rows, a.dx,
-                                a.d);
+  cudaError_t e =
+      gate_gemm_tc_ok(a, logits)
+          ? launch_gate_gemm_tc(a, logits, s)
+          : launch_kernel(gate_logits_kernel, g1, dim3(256), 0, s, 0, false,
+                          static_cast<const uint16_t *>(a.x),
+                          static_cast<const uint16_t *>(a.w_gate), logits, a.n_rows, a.dx, a.d);
   launch_end(CSA_K_COMPRESS_GATE, s);
   if (e != cudaSuccess) return e;
   launch_begin(CSA_K_COMPRESS_POOL, s);

@@ -5,9 +5,11 @@ layer calls them ("DeepSeek V4-Flash, MTP point", "Attention paths").
 ``CsaStep`` owns the outputs and workspaces so that repeated steps allocate
 nothing; it is plumbing around the four library calls and computes nothing
 itself.  The main compressor's output is read only by the attention call, so
-``run`` issues it on a side stream, where it overlaps the index-key
-compressor and the indexer; ``capture`` records a whole step as a CUDA graph
-so that a repeated step costs one launch on the host.
+``run`` issues it on a side stream of default priority, where it overlaps the
+index-key compressor and the indexer; those and the attention run on a
+high-priority stream, so that the main compressor's blocks take only the SMs
+the critical path leaves free.  ``capture`` records a whole step as a CUDA
+graph so that a repeated step costs one launch on the host.
 """
 
 from __future__ import annotations
@@ -43,6 +45,7 @@ class CsaStep:
         self.ws = {}
         self._prepared = None
         self._side = None
+        self._crit = None
         self._graph = None
 
     def _ws(self, name):
@@ -129,16 +132,21 @@ class CsaStep:
             for c in calls:
                 c(stream)
             return
-        main = torch.cuda.current_stream() if stream is None else stream
+        caller = torch.cuda.current_stream() if stream is None else stream
         if self._side is None:
-            self._side = torch.cuda.Stream(device=self.t["q"].device)
-        side = self._side
-        side.wait_stream(main)             # inputs of this step are in place
+            dev = self.t["q"].device
+            self._side = torch.cuda.Stream(device=dev)
+            self._crit = torch.cuda.Stream(device=dev,
+                                           priority=torch.cuda.Stream.priority_range()[1])
+        side, crit = self._side, self._crit
+        side.wait_stream(caller)           # inputs of this step are in place
+        crit.wait_stream(caller)
         calls[0](side)                     # main compressor -> cmp_pool
         for c in calls[1:-1]:              # index-key compressor, indexer top-k
-            c(main)
-        main.wait_stream(side)             # attention reads the new cmp_pool rows
-        calls[-1](main)
+            c(crit)
+        crit.wait_stream(side)             # attention reads the new cmp_pool rows
+        calls[-1](crit)
+        caller.wait_stream(crit)
 
     def capture(self):
         """Record one step (as ``run`` issues it) into a CUDA graph; ``replay``
