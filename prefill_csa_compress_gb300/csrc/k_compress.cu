@@ -148,15 +148,8 @@ bool gg_map(CUtensorMap *map, const void *base, long long inner, long long outer
          CUDA_SUCCESS;
 }
 
-// The tensor-core gate GEMM covers K in 64s, N in 128s and 16-byte-aligned
-// operands; other shapes take the CUDA-core kernel below.
-bool gate_gemm_tc_ok(const csa_compress_args &a, const float *logits) {
-  return a.dx % GG_K == 0 && a.d % GG_N == 0 && a.dx >= GG_K &&
-         (reinterpret_cast<uintptr_t>(a.x) & 15u) == 0 &&
-         (reinterpret_cast<uintptr_t>(a.w_gate) & 15u) == 0 &&
-         (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
-}
-
+// The gate GEMM wants K in 64s, N in 128s and 16-byte-aligned operands, which
+// the compressor's argument checks guarantee (d in {128, 512}, dx % 64 == 0).
 cudaError_t launch_gate_gemm_tc(const csa_compress_args &a, float *logits, cudaStream_t s) {
   CUtensorMap xmap, wmap;
   memset(&xmap, 0, sizeof(xmap));
@@ -178,58 +171,9 @@ cudaError_t launch_gate_gemm_tc(const csa_compress_args &a, float *logits, cudaS
 }
 
 // ---------------------------------------------------------------------------
-// logits[t, d] = sum_k x[t, k] * w_gate[k, d]   (FP32 accumulate)
-// Tile: 32 rows x 64 columns per CTA, K staged through shared memory in 64s.
-// ---------------------------------------------------------------------------
-constexpr int GT_ROWS = 32, GT_COLS = 64, GT_K = 64;
-
-__global__ void __launch_bounds__(256) gate_logits_kernel(const uint16_t *__restrict__ x,
-                                                          const uint16_t *__restrict__ w,
-                                                          float *__restrict__ logits, int n_rows,
-                                                          int dx, int d) {
-  tc::griddep_wait();
-  tc::griddep_launch_dependents();
-  __shared__ float xs[GT_ROWS][GT_K + 1];
-  __shared__ float ws[GT_K][GT_COLS];
-  const int tx = threadIdx.x % GT_COLS;
-  const int ty = threadIdx.x / GT_COLS;  // 0..3, 8 rows each
-  const int col = blockIdx.x * GT_COLS + tx;
-  const int row0 = blockIdx.y * GT_ROWS;
-  float acc[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-
-  for (int k0 = 0; k0 < dx; k0 += GT_K) {
-    for (int e = threadIdx.x; e < GT_ROWS * GT_K; e += blockDim.x) {
-      int r = e / GT_K, k = e % GT_K;
-      int gr = row0 + r;
-      xs[r][k] = gr < n_rows ? bf16_bits_to_float(x[(long long)gr * dx + k0 + k]) : 0.f;
-    }
-    for (int e = threadIdx.x; e < GT_K * GT_COLS; e += blockDim.x) {
-      int k = e / GT_COLS, c = e % GT_COLS;
-      int gc = blockIdx.x * GT_COLS + c;
-      ws[k][c] = gc < d ? bf16_bits_to_float(w[(long long)(k0 + k) * d + gc]) : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int k = 0; k < GT_K; ++k) {
-      float wv = ws[k][tx];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(xs[ty * 8 + i][k], wv, acc[i]);
-    }
-    __syncthreads();
-  }
-  if (col < d) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      int gr = row0 + ty * 8 + i;
-      if (gr < n_rows) logits[(long long)gr * d + col] = acc[i];
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// One CTA per candidate group-end row t; one thread per channel.
+// Long chunks, pooling: one CTA per row that closes a group (thread = channel)
+// takes the group's logits, softmax over its r rows per channel, the pooled
+// value and the BF16 / RMSNorm / RoPE / INT8 epilogue.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float block_sum(float v, float *red) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -335,8 +279,9 @@ __global__ void compress_pool_kernel(csa_compress_args a, const float *__restric
 
 // ---------------------------------------------------------------------------
 // Short chunks: one CTA per (group-end row, column tile) does the whole group.
-// COLS = 64 for a BF16 slice of a wide row (no row-wide statistic needed), or
-// COLS = d = 128 for the whole row (RMSNorm / INT8 amax inside the CTA).
+// COLS = 16 for a BF16 slice of a wide row (no row-wide statistic needed:
+// narrow slices spread the W_gate loads over many SMs), or COLS = d = 128 for
+// the whole row (RMSNorm / INT8 amax inside the CTA).
 // ---------------------------------------------------------------------------
 constexpr int FC_THREADS = 256;
 constexpr int FC_MAX_W_BYTES = 128 * 1024;
@@ -385,7 +330,7 @@ __global__ void __launch_bounds__(FC_THREADS) compress_fused_kernel(csa_compress
   // logits: thread (column c, part) sums its K range for the r rows
   {
     const int c = tid % COLS, pr = tid / COLS;
-    const int k_lo = pr * (dx / PARTS), k_hi = k_lo + dx / PARTS;
+    const int k_lo = pr * (dx / PARTS), k_hi = pr == PARTS - 1 ? dx : k_lo + dx / PARTS;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int k = k_lo; k < k_hi; ++k) {
       const float w = bf16_bits_to_float(Ws[k * COLS + c]);
@@ -496,17 +441,13 @@ cudaError_t launch_compress(const csa_compress_args &a, float *logits, cudaStrea
   if (a.n_rows <= 256) {
     if (a.d == 128 && (size_t)a.dx * 128 * 2 <= FC_MAX_W_BYTES) return launch_fused<128>(a, s);
     if (a.d == 512 && a.out_mode == CSA_OUT_BF16 && !a.gamma &&
-        (size_t)a.dx * 64 * 2 <= FC_MAX_W_BYTES)
-      return launch_fused<64>(a, s);
+        (size_t)a.dx * 16 * 2 <= FC_MAX_W_BYTES)
+      return launch_fused<16>(a, s);
   }
-  dim3 g1((a.d + GT_COLS - 1) / GT_COLS, (a.n_rows + GT_ROWS - 1) / GT_ROWS);
+  if (a.dx % GG_K != 0 || a.d % GG_N != 0 || (reinterpret_cast<uintptr_t>(logits) & 15u) != 0)
+    return cudaErrorInvalidValue;
   launch_begin(CSA_K_COMPRESS_GATE, s);
-  cudaError_t e =
-      gate_gemm_tc_ok(a, logits)
-          ? launch_gate_gemm_tc(a, logits, s)
-          : launch_kernel(gate_logits_kernel, g1, dim3(256), 0, s, 0, false,
-                          static_cast<const uint16_t *>(a.x),
-                          static_cast<const uint16_t *>(a.w_gate), logits, a.n_rows, a.dx, a.d);
+  cudaError_t e = launch_gate_gemm_tc(a, logits, s);
   launch_end(CSA_K_COMPRESS_GATE, s);
   if (e != cudaSuccess) return e;
   launch_begin(CSA_K_COMPRESS_POOL, s);

@@ -6,9 +6,9 @@ layer calls them ("DeepSeek V4-Flash, MTP point", "Attention paths").
 nothing; it is plumbing around the four library calls and computes nothing
 itself.  The main compressor's output is read only by the attention call, so
 ``run`` issues it on a side stream of default priority, where it overlaps the
-index-key compressor and the indexer; those and the attention run on a
-high-priority stream, so that the main compressor's blocks take only the SMs
-the critical path leaves free.  ``capture`` records a whole step as a CUDA
+index-key compressor; that and the rest of the step run on a high-priority
+stream, so that the main compressor's blocks take only the SMs the critical
+path leaves free.  ``capture`` records a whole step as a CUDA
 graph so that a repeated step costs one launch on the host.
 """
 
@@ -142,10 +142,12 @@ class CsaStep:
         side.wait_stream(caller)           # inputs of this step are in place
         crit.wait_stream(caller)
         calls[0](side)                     # main compressor -> cmp_pool
-        for c in calls[1:-1]:              # index-key compressor, indexer top-k
+        calls[1](crit)                     # index-key compressor -> idx_pool
+        # the attention reads the new cmp_pool rows; joining here, before the
+        # indexer, keeps the indexer -> top-k -> attention launches one chain
+        crit.wait_stream(side)
+        for c in calls[2:]:                # indexer top-k, attention
             c(crit)
-        crit.wait_stream(side)             # attention reads the new cmp_pool rows
-        calls[-1](crit)
         caller.wait_stream(crit)
 
     def capture(self):

@@ -93,11 +93,13 @@ def test_compress_parity(name, over):
 
 
 @pytest.mark.parametrize("n_rows,ratio,dx,d,out,with_gamma", [
-    (12, 4, 512, 512, "bf16", False),    # short chunk: fused kernel, 64-column slices
+    (12, 4, 512, 512, "bf16", False),    # short chunk: fused kernel, 16-column slices
+    (12, 2, 192, 512, "bf16", False),    # fused kernel, K = 192
+    (600, 2, 192, 512, "bf16", False),   # long chunk: tensor-core GEMM with a 3-chunk K loop
     (12, 4, 128, 128, "int8", True),     # short chunk: fused whole-row kernel with RMSNorm
     (7, 1, 256, 128, "bf16", True),
     (12, 2, 512, 512, "bf16", True),     # RMSNorm over 512 channels: GEMM + pooling kernels
-    (600, 4, 512, 512, "int8", True),    # long chunk: GEMM + pooling kernels
+    (600, 4, 512, 512, "int8", True),    # long chunk: tensor-core gate GEMM + pooling kernel
 ])
 def test_compress_direct(n_rows, ratio, dx, d, out, with_gamma):
     """csa_compress called directly: x separate from kv, optional RMSNorm,
