@@ -34,21 +34,6 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # kernel reports null.  Values are from `ncu --metrics dram__bytes_read.sum,
 # dram__bytes_write.sum` captures of these same bench workloads.
 NCU_TRAFFIC = {
-    ("chunked_prefill", "attn_prefill"): {"bytes": 1058798811, "src": "0104addba7fa"},
-    ("chunked_prefill", "compress_gate"): {"bytes": 5536873, "src": "c353edbc7e4f"},
-    ("chunked_prefill", "compress_pool"): {"bytes": 16081061, "src": "c353edbc7e4f"},
-    ("chunked_prefill", "index_score"): {"bytes": 149993527, "src": "99ffb8faede4"},
-    ("chunked_prefill", "index_topk"): {"bytes": 34512896, "src": "fce9c9dad6ae"},
-    ("million_decode", "attn_combine"): {"bytes": 17915520, "src": "4e0a12628023"},
-    ("million_decode", "attn_partial"): {"bytes": 17827596, "src": "4e0a12628023"},
-    ("million_decode", "compress_pool"): {"bytes": 22833, "src": "c353edbc7e4f"},
-    ("million_decode", "index_score"): {"bytes": 142226408, "src": "99ffb8faede4"},
-    ("million_decode", "index_topk"): {"bytes": 8639878, "src": "fce9c9dad6ae"},
-    ("serving_decode", "attn_combine"): {"bytes": 5283413, "src": "4e0a12628023"},
-    ("serving_decode", "attn_partial"): {"bytes": 4600728, "src": "4e0a12628023"},
-    ("serving_decode", "compress_pool"): {"bytes": 308983, "src": "c353edbc7e4f"},
-    ("serving_decode", "index_score"): {"bytes": 1536219, "src": "99ffb8faede4"},
-    ("serving_decode", "index_topk"): {"bytes": 121935, "src": "fce9c9dad6ae"},
 }
 
 
@@ -122,16 +107,32 @@ def algorithmic_work(wl):
         attn_bytes = (sum(sel) * D * 2 + len(req_vis) * (W + 1) * D * 2 +
                       len(rows) * H * D * 2 * 2 + sum(sel) * 4)
     attn_flops = sum(4 * H * D * (k + w) for k, w in zip(sel, win))
-    gate_flops = 2 * T * (D * D + Di * Di)
     topk_bytes = sum(vis) * 4 + len(rows) * s.topk * 8
+    # compressors (main: x, kv [T, D] BF16 -> BF16 rows; index keys: [T, Di] ->
+    # INT8 rows + FP32 scale); a group is r consecutive rows of one request
+    # ending at a position p with p % r == r - 1
+    r = s.ratio
+    rr, rp = [int(x) for x in wl.row_req], [int(x) for x in wl.row_pos]
+    groups = sum(1 for i in range(r - 1, T)
+                 if rr[i] >= 0 and rp[i] % r == r - 1 and
+                 all(rr[i - j] == rr[i] and rp[i - j] == rp[i] - j for j in range(1, r)))
+    dims = ((D, D * 2), (Di, Di + 4))          # (d, output bytes per group)
+    w_bytes = sum(d * d * 2 + r * d * 4 for d, _ in dims)    # W_gate and ape
+    out_bytes = sum(groups * ob for _, ob in dims)
+    gate_flops = 2 * T * (D * D + Di * Di)
     return {
         "index_score": {"bytes": idx_bytes, "flops": idx_flops},
         "index_topk": {"bytes": topk_bytes, "flops": 0},
-        "attn_partial": {"bytes": attn_bytes, "flops": attn_flops},
+        "attn_decode": {"bytes": attn_bytes, "flops": attn_flops},
         "attn_prefill": {"bytes": attn_bytes, "flops": attn_flops},
-        "attn_combine": {"bytes": len(rows) * H * D * 2, "flops": 0},
-        "compress_gate": {"bytes": T * (D + Di) * 2 * 2, "flops": gate_flops},
-        "compress_pool": {"bytes": T * (D + Di) * 2, "flops": 0},
+        # long chunks: x and W_gate in, FP32 logits out; then logits and kv in, rows out
+        "compress_gate": {"bytes": w_bytes + sum(T * d * (2 + 4) for d, _ in dims),
+                          "flops": gate_flops},
+        "compress_pool": {"bytes": sum(T * d * (4 + 2) for d, _ in dims) + out_bytes,
+                          "flops": 0},
+        # short chunks: W_gate, ape and the r rows of x and kv of every group in, rows out
+        "compress_fused": {"bytes": w_bytes + sum(groups * r * d * 2 * 2 for d, _ in dims) +
+                           out_bytes, "flops": 2 * groups * r * (D * D + Di * Di)},
         "_rows": len(rows),
     }
 
@@ -306,9 +307,9 @@ def _src_sha(name):
 
 
 KERNEL_SRC = {"index_score": "k_index_tc.cu", "index_topk": "k_index.cu",
-              "attn_partial": "k_attn.cu", "attn_combine": "k_attn.cu",
-              "attn_prefill": "k_attn_prefill.cu", "compress_gate": "k_compress.cu",
-              "compress_pool": "k_compress.cu"}
+              "attn_decode": "k_attn.cu", "attn_prefill": "k_attn_prefill.cu",
+              "compress_gate": "k_compress.cu", "compress_pool": "k_compress.cu",
+              "compress_fused": "k_compress.cu"}
 
 
 def run_gpu(args, wl, rank, world, local_rank):
@@ -340,10 +341,11 @@ def run_gpu(args, wl, rank, world, local_rank):
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
-    kernels = ["index_score", "index_topk", "attn_prefill" if prefill else "attn_partial",
-               "attn_combine", "compress_gate", "compress_pool"]
+    kernels = ["index_score", "index_topk", "attn_prefill" if prefill else "attn_decode",
+               "compress_gate", "compress_pool", "compress_fused"]
     # per-kernel durations: the step captured with that kernel's event pairs,
-    # replayed three times with L2 flushed before each replay
+    # its calls issued one after another on one stream (no kernel shares the
+    # GPU with the timed one), replayed three times with L2 flushed before each
     per_kernel = {}
     for k in kernels:
         csa.prof_enable(k, 16)
@@ -436,12 +438,13 @@ def run_gpu(args, wl, rank, world, local_rank):
     peaks = _peaks()
     dom_avg_ms = dom_ms / max(1, dom_n)
     w = work[dominant]
-    if prefill and w["flops"] > 0 and dominant in ("attn_prefill", "index_score"):
-        achieved = w["flops"] / (dom_avg_ms / 1e3) / 1e12
+    n_per_step = max(1.0, per_kernel[dominant]["launches_per_step"])
+    if prefill and w["flops"] > 0 and dominant in ("attn_prefill", "index_score", "compress_gate"):
+        achieved = w["flops"] / n_per_step / (dom_avg_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"]}
     else:
-        per_launch = w["bytes"] / max(1.0, per_kernel[dominant]["launches_per_step"])
+        per_launch = w["bytes"] / n_per_step
         achieved = per_launch / (dom_avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"]}

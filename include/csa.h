@@ -133,6 +133,22 @@ typedef struct {
 
 CSA_API csa_status_t csa_compress(csa_compress_args *args, csa_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * csa_compress_pair: the two compressors of one attention layer -- the main
+ * KV compressor and the index-key compressor, which pool the same rows --
+ * in one call.  The result is exactly that of csa_compress(first) followed by
+ * csa_compress(second) on the same stream; when both calls take the
+ * short-chunk path (at most 256 rows) they share one kernel launch, so the
+ * next call on the stream waits for one grid instead of two.
+ *
+ * Each struct is checked, size-queried (workspace == NULL stores its
+ * workspace_bytes; the call then returns CSA_OK without launching) and owns
+ * its workspace exactly as in csa_compress.  The two calls must not write the
+ * same pool rows.
+ * ---------------------------------------------------------------------- */
+CSA_API csa_status_t csa_compress_pair(csa_compress_args *first, csa_compress_args *second,
+                                       csa_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * csa_index_topk - lightning-indexer scores and deterministic top-k.
  *
@@ -313,20 +329,29 @@ CSA_API uint64_t csa_launch_count(void);
 
 /* Kernel identifiers for the timing hooks. */
 typedef enum {
-  CSA_K_COMPRESS_GATE = 0,
-  CSA_K_COMPRESS_POOL = 1,
-  CSA_K_INDEX_SCORE = 2,
-  CSA_K_INDEX_TOPK = 3,
-  CSA_K_ATTN_PARTIAL = 4,
-  CSA_K_ATTN_COMBINE = 5,
+  CSA_K_COMPRESS_GATE = 0,  /* long chunks: gate logits GEMM */
+  CSA_K_COMPRESS_POOL = 1,  /* long chunks: softmax pooling and publication */
+  CSA_K_COMPRESS_FUSED = 2, /* short chunks: the whole compressor in one kernel */
+  CSA_K_INDEX_SCORE = 3,
+  CSA_K_INDEX_TOPK = 4,
+  CSA_K_ATTN_DECODE = 5,
   CSA_K_ATTN_PREFILL = 6,
   CSA_K_COUNT = 7
 } csa_kernel_id_t;
 
-/* Record a CUDA event pair around every launch of kernel `kernel_id` (up to
- * `max_launches` launches) on the launching stream.  Events are created by
- * the library; this allocates no device memory. */
+/* Time every launch of kernel `kernel_id` (up to `max_launches` launches)
+ * with a CUDA event pair: the first event completes when the work issued on
+ * the launching stream before the kernel is done, the second when the kernel
+ * is done.  Both are recorded on a library-owned side stream forked from the
+ * launching stream, so the launching stream gains no node between the kernel
+ * and its neighbours (their programmatic launch overlap is kept).  Events and
+ * the side stream are created by the library; no device memory is allocated.
+ * Inside stream capture, csa_prof_join must bring the side stream back into
+ * the captured stream before the capture ends. */
 CSA_API csa_status_t csa_prof_enable(int32_t kernel_id, int32_t max_launches);
+/* Make `stream` wait for every timing event recorded so far (a no-op when
+ * timing is off). */
+CSA_API csa_status_t csa_prof_join(csa_stream_t stream);
 /* Synchronise the recorded events and return the summed device time (ms) and
  * the number of launches recorded since csa_prof_enable. */
 CSA_API csa_status_t csa_prof_read(int32_t kernel_id, float *total_ms, int32_t *n_launches);

@@ -23,8 +23,8 @@ CSA_DEV_BAD_BLOCK, CSA_DEV_BAD_POS, CSA_DEV_BAD_INDEX, CSA_DEV_POS_GE_CAP, CSA_D
 CSA_OUT_BF16, CSA_OUT_INT8 = 0, 1
 CSA_MODE_AUTO, CSA_MODE_DECODE, CSA_MODE_PREFILL = 0, 1, 2
 KERNEL_IDS = {
-    "compress_gate": 0, "compress_pool": 1, "index_score": 2, "index_topk": 3,
-    "attn_partial": 4, "attn_combine": 5, "attn_prefill": 6,
+    "compress_gate": 0, "compress_pool": 1, "compress_fused": 2, "index_score": 3,
+    "index_topk": 4, "attn_decode": 5, "attn_prefill": 6,
 }
 
 
@@ -96,6 +96,9 @@ def lib():
             f = getattr(L, name)
             f.argtypes = [ctypes.POINTER(argt), c_void_p]
             f.restype = c_int32
+        L.csa_compress_pair.argtypes = [ctypes.POINTER(CompressArgs), ctypes.POINTER(CompressArgs),
+                                        c_void_p]
+        L.csa_compress_pair.restype = c_int32
         L.csa_version.restype = ctypes.c_char_p
         L.csa_status_string.argtypes = [c_int32]
         L.csa_status_string.restype = ctypes.c_char_p
@@ -105,6 +108,8 @@ def lib():
         L.csa_prof_read.argtypes = [c_int32, ctypes.POINTER(c_float), ctypes.POINTER(c_int32)]
         L.csa_prof_read.restype = c_int32
         L.csa_prof_disable.restype = c_int32
+        L.csa_prof_join.argtypes = [c_void_p]
+        L.csa_prof_join.restype = c_int32
         _lib = L
     return _lib
 
@@ -121,10 +126,25 @@ def launch_count() -> int:
     return int(lib().csa_launch_count())
 
 
+_prof_on = False
+
+
 def prof_enable(kernel: str, max_launches: int) -> None:
+    global _prof_on
     st = lib().csa_prof_enable(KERNEL_IDS[kernel], int(max_launches))
     if st != CSA_OK:
         raise CsaError("csa_prof_enable", st)
+    _prof_on = True
+
+
+def prof_join(stream=None) -> None:
+    """Bring the timing events' side stream back into ``stream`` (needed
+    before a stream capture that recorded timed launches ends)."""
+    if not _prof_on:
+        return
+    st = lib().csa_prof_join(_stream(stream))
+    if st != CSA_OK:
+        raise CsaError("csa_prof_join", st)
 
 
 def prof_read(kernel: str):
@@ -136,7 +156,9 @@ def prof_read(kernel: str):
 
 
 def prof_disable() -> None:
+    global _prof_on
     lib().csa_prof_disable()
+    _prof_on = False
 
 
 # ---------------------------------------------------------------- marshalling helpers
@@ -168,12 +190,12 @@ class PreparedCall:
     def __init__(self, fn_name, args, workspace):
         self.fn_name = fn_name
         self.fn = getattr(lib(), fn_name)
-        self.args = args
+        self.args = args if isinstance(args, tuple) else (args,)
         self.workspace = workspace
-        self._ref = ctypes.byref(args)
+        self._refs = tuple(ctypes.byref(a) for a in self.args)
 
     def __call__(self, stream=None):
-        st = self.fn(self._ref, _stream(stream))
+        st = self.fn(*self._refs, _stream(stream))
         if st != CSA_OK:
             raise CsaError(self.fn_name, st)
         return self.workspace
@@ -207,12 +229,9 @@ def _fill_common_rope(args, rope_cos, rope_sin):
 # ---------------------------------------------------------------- the four calls
 
 
-def csa_compress(*, x, kv, w_gate, ape, ratio, positions, row_req, block_table, out="bf16",
-                 cmp_pool=None, idx_pool=None, idx_scale_pool=None, gamma=None, rms_eps=1e-6,
-                 rotate=False, rope_cos=None, rope_sin=None, status=None, workspace=None,
-                 stream=None, prepare=False):
-    """Gated compression of the chunk's complete groups into a paged pool
-    (``include/csa.h``: csa_compress)."""
+def _compress_struct(*, x, kv, w_gate, ape, ratio, positions, row_req, block_table, out="bf16",
+                     cmp_pool=None, idx_pool=None, idx_scale_pool=None, gamma=None, rms_eps=1e-6,
+                     rotate=False, rope_cos=None, rope_sin=None, status=None):
     a = CompressArgs()
     a.struct_size = ctypes.sizeof(CompressArgs)
     a.n_rows = int(x.shape[0])
@@ -240,7 +259,41 @@ def csa_compress(*, x, kv, w_gate, ape, ratio, positions, row_req, block_table, 
         a.idx_scale_pool = _p(idx_scale_pool, torch.float32, "idx_scale_pool")
         a.n_blocks = int(idx_pool.shape[0])
     a.status_dev = _p(status, torch.int32, "status")
-    return _run("csa_compress", a, workspace, stream, x.device, prepare)
+    return a
+
+
+def csa_compress(*, workspace=None, stream=None, prepare=False, **kw):
+    """Gated compression of the chunk's complete groups into a paged pool
+    (``include/csa.h``: csa_compress).  Keywords: x, kv, w_gate, ape, ratio,
+    positions, row_req, block_table, out ("bf16" or "int8"), cmp_pool or
+    idx_pool + idx_scale_pool, gamma, rms_eps, rotate, rope_cos, rope_sin,
+    status."""
+    a = _compress_struct(**kw)
+    return _run("csa_compress", a, workspace, stream, kw["x"].device, prepare)
+
+
+def csa_compress_pair(first: dict, second: dict, *, workspaces=(None, None), stream=None,
+                      prepare=False):
+    """Two compressors of one layer in one call (``include/csa.h``:
+    csa_compress_pair); ``first`` and ``second`` hold csa_compress's keywords.
+    Returns the two workspaces (or the prepared call)."""
+    structs, wss = [], []
+    for kw, ws in zip((first, second), workspaces):
+        a = _compress_struct(**kw)
+        a.workspace, a.workspace_bytes = None, 0
+        st = lib().csa_compress(ctypes.byref(a), None)  # size query
+        if st != CSA_OK:
+            raise CsaError("csa_compress_pair", st)
+        need = int(a.workspace_bytes)
+        if ws is None or ws.numel() < need:
+            ws = torch.empty(max(need, 256), dtype=torch.uint8, device=kw["x"].device)
+        a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+        structs.append(a)
+        wss.append(ws)
+    call = PreparedCall("csa_compress_pair", tuple(structs), tuple(wss))
+    if prepare:
+        return call
+    return call(stream)
 
 
 def csa_index_topk(*, q_idx, weights, row_req, row_pos, n_cmp, ratio, idx_pool, idx_scale_pool,

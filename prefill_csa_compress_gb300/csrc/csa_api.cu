@@ -17,7 +17,10 @@ struct ProfState {
   int kernel_id = -1;
   int max_launches = 0;
   int recorded = 0;
-  std::vector<cudaEvent_t> ev;  // 2 per launch
+  std::vector<cudaEvent_t> ev;     // 2 per launch
+  cudaStream_t side = nullptr;     // where the timing events are recorded
+  cudaEvent_t fork = nullptr;      // hands the launching stream's position to `side`
+  cudaEvent_t join = nullptr;
 };
 static ProfState g_prof;
 
@@ -31,18 +34,27 @@ void record_event(cudaEvent_t e, cudaStream_t s) {
     cudaEventRecord(e, s);
 }
 
+// Records `e` on the side stream once everything issued so far on `s` is
+// done.  Nothing is added to `s` itself, so the next kernel on `s` still
+// launches as a programmatic dependent of the one before it.
+static void record_beside(cudaEvent_t e, cudaStream_t s) {
+  cudaEventRecord(g_prof.fork, s);
+  cudaStreamWaitEvent(g_prof.side, g_prof.fork, 0);
+  record_event(e, g_prof.side);
+}
+
 void launch_begin(int kernel_id, cudaStream_t s) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (g_prof.kernel_id != kernel_id) return;
   std::lock_guard<std::mutex> lk(g_prof.mu);
-  if (g_prof.recorded < g_prof.max_launches) record_event(g_prof.ev[2 * g_prof.recorded], s);
+  if (g_prof.recorded < g_prof.max_launches) record_beside(g_prof.ev[2 * g_prof.recorded], s);
 }
 
 void launch_end(int kernel_id, cudaStream_t s) {
   if (g_prof.kernel_id != kernel_id) return;
   std::lock_guard<std::mutex> lk(g_prof.mu);
   if (g_prof.recorded < g_prof.max_launches) {
-    record_event(g_prof.ev[2 * g_prof.recorded + 1], s);
+    record_beside(g_prof.ev[2 * g_prof.recorded + 1], s);
     ++g_prof.recorded;
   }
 }
@@ -122,7 +134,10 @@ CSA_API uint64_t csa_launch_count(void) { return g_launches.load(); }
 
 // ---------------------------------------------------------------- compress
 
-CSA_API csa_status_t csa_compress(csa_compress_args *a, csa_stream_t stream) {
+// Host checks of one compressor call.  Sets *size_query when the call only
+// reports its workspace size (already stored in a->workspace_bytes).
+static csa_status_t check_compress(csa_compress_args *a, bool *size_query) {
+  *size_query = false;
   if (!a || a->struct_size < sizeof(csa_compress_args)) return CSA_ERR_INVALID_ARG;
   if (a->n_rows < 0 || a->n_req < 0) return CSA_ERR_INVALID_ARG;
   if (a->ratio != 1 && a->ratio != 2 && a->ratio != 4) return CSA_ERR_UNSUPPORTED;
@@ -132,6 +147,7 @@ CSA_API csa_status_t csa_compress(csa_compress_args *a, csa_stream_t stream) {
   const size_t need = align_up((size_t)a->n_rows * a->d * sizeof(float), kAlign);
   if (!a->workspace) {
     a->workspace_bytes = need;
+    *size_query = true;
     return CSA_OK;
   }
   if (a->workspace_bytes < need) return CSA_ERR_INVALID_ARG;
@@ -145,8 +161,27 @@ CSA_API csa_status_t csa_compress(csa_compress_args *a, csa_stream_t stream) {
     return CSA_ERR_INVALID_ARG;
   if (a->rotate && (!a->rope_cos || !a->rope_sin || a->rope_cap <= 0)) return CSA_ERR_INVALID_ARG;
   if (!aligned16(a->x) || !aligned16(a->kv) || !aligned16(a->w_gate)) return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
+CSA_API csa_status_t csa_compress(csa_compress_args *a, csa_stream_t stream) {
+  bool query = false;
+  const csa_status_t st = check_compress(a, &query);
+  if (st != CSA_OK || query || a->n_rows == 0) return st;
   return from_cuda(
       launch_compress(*a, static_cast<float *>(a->workspace), static_cast<cudaStream_t>(stream)));
+}
+
+CSA_API csa_status_t csa_compress_pair(csa_compress_args *first, csa_compress_args *second,
+                                       csa_stream_t stream) {
+  bool q1 = false, q2 = false;
+  csa_status_t st = check_compress(first, &q1);
+  if (st != CSA_OK) return st;
+  st = check_compress(second, &q2);
+  if (st != CSA_OK || q1 || q2) return st;
+  return from_cuda(launch_compress_pair(*first, static_cast<float *>(first->workspace), *second,
+                                        static_cast<float *>(second->workspace),
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 // ---------------------------------------------------------------- index + top-k
@@ -199,20 +234,51 @@ CSA_API csa_status_t csa_sparse_attn_prefill(csa_attn_args *a, csa_stream_t stre
 
 // ---------------------------------------------------------------- timing hooks
 
+static void prof_release() {
+  for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
+  g_prof.ev.clear();
+  if (g_prof.fork) cudaEventDestroy(g_prof.fork);
+  if (g_prof.join) cudaEventDestroy(g_prof.join);
+  if (g_prof.side) cudaStreamDestroy(g_prof.side);
+  g_prof.fork = g_prof.join = nullptr;
+  g_prof.side = nullptr;
+  g_prof.kernel_id = -1;
+  g_prof.recorded = 0;
+  g_prof.max_launches = 0;
+}
+
 CSA_API csa_status_t csa_prof_enable(int32_t kernel_id, int32_t max_launches) {
   if (kernel_id < 0 || kernel_id >= CSA_K_COUNT || max_launches <= 0) return CSA_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_prof.mu);
-  for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
+  prof_release();
+  bool ok = cudaStreamCreateWithFlags(&g_prof.side, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&g_prof.fork, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&g_prof.join, cudaEventDisableTiming) == cudaSuccess;
   g_prof.ev.assign(2 * (size_t)max_launches, nullptr);
-  for (auto &e : g_prof.ev)
-    if (cudaEventCreate(&e) != cudaSuccess) {
-      g_prof.ev.clear();
-      g_prof.kernel_id = -1;
-      return CSA_ERR_CUDA;
-    }
+  for (auto &e : g_prof.ev) ok = ok && cudaEventCreate(&e) == cudaSuccess;
+  if (!ok) {
+    prof_release();
+    return CSA_ERR_CUDA;
+  }
   g_prof.max_launches = max_launches;
   g_prof.recorded = 0;
   g_prof.kernel_id = kernel_id;
+  return CSA_OK;
+}
+
+CSA_API csa_status_t csa_prof_join(csa_stream_t stream) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (!g_prof.side) return CSA_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // inside a capture, join only a side stream that this capture forked
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone, ss = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess ||
+      cudaStreamIsCapturing(g_prof.side, &ss) != cudaSuccess)
+    return CSA_ERR_CUDA;
+  if ((cs == cudaStreamCaptureStatusActive) != (ss == cudaStreamCaptureStatusActive)) return CSA_OK;
+  if (cudaEventRecord(g_prof.join, g_prof.side) != cudaSuccess ||
+      cudaStreamWaitEvent(s, g_prof.join, 0) != cudaSuccess)
+    return CSA_ERR_CUDA;
   return CSA_OK;
 }
 
@@ -237,11 +303,7 @@ CSA_API csa_status_t csa_prof_read(int32_t kernel_id, float *total_ms, int32_t *
 
 CSA_API csa_status_t csa_prof_disable(void) {
   std::lock_guard<std::mutex> lk(g_prof.mu);
-  for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
-  g_prof.ev.clear();
-  g_prof.kernel_id = -1;
-  g_prof.recorded = 0;
-  g_prof.max_launches = 0;
+  prof_release();
   return CSA_OK;
 }
 

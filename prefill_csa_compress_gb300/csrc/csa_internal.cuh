@@ -66,6 +66,9 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 
 // Launchers (one per kernel family); each returns cudaGetLastError().
 cudaError_t launch_compress(const csa_compress_args &a, float *logits, cudaStream_t s);
+// two compressors of one layer; one launch when both take the short-chunk path
+cudaError_t launch_compress_pair(const csa_compress_args &a, float *logits_a,
+                                 const csa_compress_args &b, float *logits_b, cudaStream_t s);
 // Words per row of the long-row top-k control block (barrier counter and
 // three digit histograms).
 constexpr int kTopkCtlWords = 32 + 2048 + 2048 + 1024;

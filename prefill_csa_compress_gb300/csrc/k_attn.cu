@@ -453,10 +453,10 @@ cudaError_t launch_attn_decode(const csa_attn_args &a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   int n_splits, tps;
   attn_decode_geometry(a, &n_splits, &tps);
-  launch_begin(CSA_K_ATTN_PARTIAL, s);
+  launch_begin(CSA_K_ATTN_DECODE, s);
   e = launch_kernel(attn_decode_kernel, dim3(n_splits, a.n_rows), dim3(AD_THREADS),
                     (size_t)AD_SMEM, s, n_splits, false, a, tps, qmap);
-  launch_end(CSA_K_ATTN_PARTIAL, s);
+  launch_end(CSA_K_ATTN_DECODE, s);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -281,40 +281,45 @@ __global__ void compress_pool_kernel(csa_compress_args a, const float *__restric
 // Short chunks: one CTA per (group-end row, column tile) does the whole group.
 // COLS = 16 for a BF16 slice of a wide row (no row-wide statistic needed:
 // narrow slices spread the W_gate loads over many SMs), or COLS = d = 128 for
-// the whole row (RMSNorm / INT8 amax inside the CTA).
+// the whole row (RMSNorm / INT8 amax inside the CTA).  Once the CTA knows its
+// group, every input it needs is requested at once (W_gate slice and x rows
+// into shared memory; the block-table entry, kv, ape, RoPE and gamma entries
+// into registers), so the group costs one memory round trip after the row
+// check rather than one per dependent read.
 // ---------------------------------------------------------------------------
 constexpr int FC_THREADS = 256;
 constexpr int FC_MAX_W_BYTES = 128 * 1024;
 
 template <int COLS>
-__global__ void __launch_bounds__(FC_THREADS) compress_fused_kernel(csa_compress_args a) {
-  tc::griddep_wait();
-  tc::griddep_launch_dependents();
-  extern __shared__ __align__(16) uint8_t fc_smem[];
+__device__ __forceinline__ void fused_group(const csa_compress_args &a, const int cb, const int t,
+                                            uint8_t *fc_smem) {
   constexpr int PARTS = FC_THREADS / COLS;
-  const int dx = a.dx, D = a.d, r = a.ratio;
+  const int dx = a.dx, D = a.d, r = a.ratio, tid = threadIdx.x;
   uint16_t *Ws = reinterpret_cast<uint16_t *>(fc_smem);               // [dx][COLS]
   uint16_t *Xs = Ws + (size_t)dx * COLS;                               // [r][dx]
   float *part = reinterpret_cast<float *>(Xs + 4 * dx);               // [PARTS][4][COLS]
   float *ys = part + PARTS * 4 * COLS;                                 // [COLS]
   float *red = ys + COLS;                                              // [32]
-  const int t = blockIdx.y, c0 = blockIdx.x * COLS, tid = threadIdx.x;
-  const int b = a.row_req[t], p = a.positions[t];
+  const int c0 = cb * COLS;
+  // does row t close a group of r consecutive positions of one request?
+  int bj[4], pj[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int tj = max(t - j, 0);
+    bj[j] = j < r ? a.row_req[tj] : 0;
+    pj[j] = j < r ? a.positions[tj] : 0;
+  }
+  const int b = bj[0], p = pj[0];
   if (b < 0 || p < 0 || (p % r) != r - 1 || t < r - 1) return;
-  for (int j = 1; j < r; ++j)
-    if (a.row_req[t - j] != b || a.positions[t - j] != p - j) return;
+#pragma unroll
+  for (int j = 1; j < 4; ++j)
+    if (j < r && (bj[j] != b || pj[j] != p - j)) return;
   if (b >= a.n_req) {
-    if (tid == 0 && blockIdx.x == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
+    if (tid == 0 && cb == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
     return;
   }
-  const int g = p / r, page = g / kBlock;
-  const int phys = page < a.max_blocks ? a.block_table[(long long)b * a.max_blocks + page] : -1;
-  if (phys < 0 || phys >= a.n_blocks) {
-    if (tid == 0 && blockIdx.x == 0) flag(a.status_dev, CSA_DEV_BAD_BLOCK);
-    return;
-  }
-  const int t0 = t - r + 1;
-  // stage the weight slice and the group's x rows (all copies in flight at once)
+  const int g = p / r, page = g / kBlock, t0 = t - r + 1;
+  // ---- every input of the group in flight at once
   const uint16_t *wg = static_cast<const uint16_t *>(a.w_gate);
   const uint16_t *xg = static_cast<const uint16_t *>(a.x);
   for (int e = tid; e < dx * (COLS / 8); e += FC_THREADS) {
@@ -325,41 +330,71 @@ __global__ void __launch_bounds__(FC_THREADS) compress_fused_kernel(csa_compress
     const int j = e / (dx / 8), q = e % (dx / 8);
     tc::cp_async16(Xs + j * dx + q * 8, xg + (long long)(t0 + j) * dx + q * 8);
   }
+  const int phys = page < a.max_blocks ? a.block_table[(long long)b * a.max_blocks + page] : -1;
+  const int c = tid, d = c0 + c;
+  const int pos = g * r;  // RoPE position: the group start
+  const bool rope_ok = pos < a.rope_cap;
+  const bool rot_here = a.rotate && rope_ok && c < COLS && d >= D - kRopeDim;
+  const uint16_t *kvg = static_cast<const uint16_t *>(a.kv);
+  uint16_t kvj[4] = {0, 0, 0, 0};
+  float apej[4] = {0.f, 0.f, 0.f, 0.f};
+  float cs = 1.f, sn = 0.f, gam = 1.f;
+  if (c < COLS) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < r) {
+        kvj[j] = kvg[(long long)(t0 + j) * D + d];
+        apej[j] = a.ape[j * D + d];
+      }
+    if (rot_here) {
+      const int i = (d - (D - kRopeDim)) >> 1;
+      cs = a.rope_cos[(long long)pos * kRopeHalf + i];
+      sn = a.rope_sin[(long long)pos * kRopeHalf + i];
+    }
+    if (a.gamma && COLS == D) gam = bf16_bits_to_float(static_cast<const uint16_t *>(a.gamma)[d]);
+  }
   tc::cp_async_wait_all();
   __syncthreads();
-  // logits: thread (column c, part) sums its K range for the r rows
+  if (phys < 0 || phys >= a.n_blocks) {  // the same for every thread of the CTA
+    if (tid == 0 && cb == 0) flag(a.status_dev, CSA_DEV_BAD_BLOCK);
+    return;
+  }
+  // ---- logits: thread (column c, part) sums its K range for the r rows
   {
-    const int c = tid % COLS, pr = tid / COLS;
+    const int cc = tid % COLS, pr = tid / COLS;
     const int k_lo = pr * (dx / PARTS), k_hi = pr == PARTS - 1 ? dx : k_lo + dx / PARTS;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int k = k_lo; k < k_hi; ++k) {
-      const float w = bf16_bits_to_float(Ws[k * COLS + c]);
+      const float w = bf16_bits_to_float(Ws[k * COLS + cc]);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         if (j < r) acc[j] = fmaf(bf16_bits_to_float(Xs[j * dx + k]), w, acc[j]);
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) part[(pr * 4 + j) * COLS + c] = acc[j];
+    for (int j = 0; j < 4; ++j) part[(pr * 4 + j) * COLS + cc] = acc[j];
   }
   __syncthreads();
-  const uint16_t *kv = static_cast<const uint16_t *>(a.kv);
+  // ---- softmax over the r positions of each channel, pooled kv, BF16 round
   float y = 0.f;
-  const int c = tid, d = c0 + c;
   if (c < COLS) {
     float lg[4];
     float mx = -INFINITY;
-    for (int j = 0; j < r; ++j) {
-      float l = a.ape[j * D + d];
-      for (int pr = 0; pr < PARTS; ++pr) l += part[(pr * 4 + j) * COLS + c];
-      lg[j] = l;
-      mx = fmaxf(mx, l);
-    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < r) {
+        float l = apej[j];
+        for (int pr = 0; pr < PARTS; ++pr) l += part[(pr * 4 + j) * COLS + c];
+        lg[j] = l;
+        mx = fmaxf(mx, l);
+      }
     float s = 0.f;
-    for (int j = 0; j < r; ++j) {
-      const float e = expf(lg[j] - mx);
-      s += e;
-      y = fmaf(e, bf16_bits_to_float(kv[(long long)(t0 + j) * D + d]), y);
-    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < r) {
+        const float e = expf(lg[j] - mx);
+        s += e;
+        y = fmaf(e, bf16_bits_to_float(kvj[j]), y);
+      }
     y = round_bf16(y / s);
   }
   // row-wide statistics exist only in the whole-row variant (COLS == D)
@@ -371,20 +406,14 @@ __global__ void __launch_bounds__(FC_THREADS) compress_fused_kernel(csa_compress
     float ss = 0.f;
     for (int i = 0; i < FC_THREADS / 32; ++i) ss += red[i];
     __syncthreads();
-    if (c < COLS)
-      y = round_bf16(y * rsqrtf(ss / (float)D + a.rms_eps) *
-                     bf16_bits_to_float(static_cast<const uint16_t *>(a.gamma)[d]));
+    if (c < COLS) y = round_bf16(y * rsqrtf(ss / (float)D + a.rms_eps) * gam);
   }
   if (a.rotate) {
-    const int pos = g * r;
     if (c < COLS) ys[c] = y;
     __syncthreads();
-    if (pos >= a.rope_cap) {
+    if (!rope_ok) {
       if (tid == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
-    } else if (c < COLS && d >= D - kRopeDim) {
-      const int i = (d - (D - kRopeDim)) >> 1;
-      const float cs = a.rope_cos[(long long)pos * kRopeHalf + i];
-      const float sn = a.rope_sin[(long long)pos * kRopeHalf + i];
+    } else if (rot_here) {
       y = (d & 1) == 0 ? ys[c] * cs - ys[c + 1] * sn : ys[c - 1] * sn + ys[c] * cs;
     }
   }
@@ -408,28 +437,89 @@ __global__ void __launch_bounds__(FC_THREADS) compress_fused_kernel(csa_compress
 }
 
 template <int COLS>
+__global__ void __launch_bounds__(FC_THREADS)
+    compress_fused_kernel(const __grid_constant__ csa_compress_args a) {
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
+  extern __shared__ __align__(16) uint8_t fc_smem[];
+  fused_group<COLS>(a, blockIdx.x, blockIdx.y, fc_smem);
+}
+
+// Two compressors of one layer (the main KV compressor and the index-key
+// compressor read the same rows) in one grid: column tiles [0, n_a) serve the
+// first, the rest the second.
+template <int CA, int CB>
+__global__ void __launch_bounds__(FC_THREADS)
+    compress_fused_pair_kernel(const __grid_constant__ csa_compress_args a,
+                               const __grid_constant__ csa_compress_args b, int n_a) {
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
+  extern __shared__ __align__(16) uint8_t fc_smem[];
+  const int x = blockIdx.x, t = blockIdx.y;
+  if (x < n_a) {
+    if (t < a.n_rows) fused_group<CA>(a, x, t, fc_smem);
+  } else if (t < b.n_rows) {
+    fused_group<CB>(b, x - n_a, t, fc_smem);
+  }
+}
+
+template <int COLS>
 size_t fused_smem(const csa_compress_args &a) {
   return (size_t)a.dx * COLS * 2 + 4 * (size_t)a.dx * 2 +
          (FC_THREADS / COLS) * 4 * COLS * 4 + COLS * 4 + 32 * 4;
 }
 
-template <int COLS>
-cudaError_t launch_fused(const csa_compress_args &a, cudaStream_t s) {
-  const size_t smem = fused_smem<COLS>(a);
-  static bool attr[64] = {};
+// the short-chunk column tile for this call, or 0 when it takes the long path
+int fused_cols(const csa_compress_args &a) {
+  if (a.n_rows > 256) return 0;
+  if (a.d == 128 && (size_t)a.dx * 128 * 2 <= FC_MAX_W_BYTES) return 128;
+  if (a.d == 512 && a.out_mode == CSA_OUT_BF16 && !a.gamma && (size_t)a.dx * 16 * 2 <= FC_MAX_W_BYTES)
+    return 16;
+  return 0;
+}
+
+// The dynamic shared-memory limit is raised once per kernel and device
+// (CB == 0: the single-compressor kernel of column tile CA).
+template <int CA, int CB>
+cudaError_t allow_fused_smem() {
+  static bool done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(compress_fused_kernel<COLS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         FC_MAX_W_BYTES + 32 * 1024);
-    if (e != cudaSuccess) return e;
-    attr[dev] = true;
-  }
-  launch_begin(CSA_K_COMPRESS_POOL, s);
-  const cudaError_t e = launch_kernel(compress_fused_kernel<COLS>, dim3(a.d / COLS, a.n_rows),
-                                      dim3(FC_THREADS), smem, s, 0, false, a);
-  launch_end(CSA_K_COMPRESS_POOL, s);
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  cudaError_t e;
+  if constexpr (CB == 0)
+    e = cudaFuncSetAttribute(compress_fused_kernel<CA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             FC_MAX_W_BYTES + 32 * 1024);
+  else
+    e = cudaFuncSetAttribute(compress_fused_pair_kernel<CA, CB>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, FC_MAX_W_BYTES + 32 * 1024);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+
+template <int COLS>
+cudaError_t launch_fused(const csa_compress_args &a, cudaStream_t s) {
+  cudaError_t e = allow_fused_smem<COLS, 0>();
+  if (e != cudaSuccess) return e;
+  launch_begin(CSA_K_COMPRESS_FUSED, s);
+  e = launch_kernel(compress_fused_kernel<COLS>, dim3(a.d / COLS, a.n_rows), dim3(FC_THREADS),
+                    fused_smem<COLS>(a), s, 0, false, a);
+  launch_end(CSA_K_COMPRESS_FUSED, s);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int CA, int CB>
+cudaError_t launch_fused_pair(const csa_compress_args &a, const csa_compress_args &b,
+                              cudaStream_t s) {
+  cudaError_t e = allow_fused_smem<CA, CB>();
+  if (e != cudaSuccess) return e;
+  const int n_a = a.d / CA, n_b = b.d / CB;
+  const size_t smem = fused_smem<CA>(a) > fused_smem<CB>(b) ? fused_smem<CA>(a) : fused_smem<CB>(b);
+  launch_begin(CSA_K_COMPRESS_FUSED, s);
+  e = launch_kernel(compress_fused_pair_kernel<CA, CB>,
+                    dim3(n_a + n_b, a.n_rows > b.n_rows ? a.n_rows : b.n_rows), dim3(FC_THREADS),
+                    smem, s, 0, false, a, b, n_a);
+  launch_end(CSA_K_COMPRESS_FUSED, s);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -438,12 +528,9 @@ cudaError_t launch_fused(const csa_compress_args &a, cudaStream_t s) {
 cudaError_t launch_compress(const csa_compress_args &a, float *logits, cudaStream_t s) {
   if (a.n_rows <= 0) return cudaSuccess;
   // short chunks (decode): one fused kernel per call
-  if (a.n_rows <= 256) {
-    if (a.d == 128 && (size_t)a.dx * 128 * 2 <= FC_MAX_W_BYTES) return launch_fused<128>(a, s);
-    if (a.d == 512 && a.out_mode == CSA_OUT_BF16 && !a.gamma &&
-        (size_t)a.dx * 16 * 2 <= FC_MAX_W_BYTES)
-      return launch_fused<16>(a, s);
-  }
+  const int cols = fused_cols(a);
+  if (cols == 128) return launch_fused<128>(a, s);
+  if (cols == 16) return launch_fused<16>(a, s);
   if (a.dx % GG_K != 0 || a.d % GG_N != 0 || (reinterpret_cast<uintptr_t>(logits) & 15u) != 0)
     return cudaErrorInvalidValue;
   launch_begin(CSA_K_COMPRESS_GATE, s);
@@ -455,6 +542,17 @@ cudaError_t launch_compress(const csa_compress_args &a, float *logits, cudaStrea
                     static_cast<const float *>(logits));
   launch_end(CSA_K_COMPRESS_POOL, s);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_compress_pair(const csa_compress_args &a, float *logits_a,
+                                 const csa_compress_args &b, float *logits_b, cudaStream_t s) {
+  const int ca = a.n_rows > 0 ? fused_cols(a) : -1, cb = b.n_rows > 0 ? fused_cols(b) : -1;
+  if (ca == 16 && cb == 128) return launch_fused_pair<16, 128>(a, b, s);
+  if (ca == 128 && cb == 16) return launch_fused_pair<128, 16>(a, b, s);
+  if (ca == 128 && cb == 128) return launch_fused_pair<128, 128>(a, b, s);
+  if (ca == 16 && cb == 16) return launch_fused_pair<16, 16>(a, b, s);
+  const cudaError_t e = launch_compress(a, logits_a, s);
+  return e != cudaSuccess ? e : launch_compress(b, logits_b, s);
 }
 
 }  // namespace csa

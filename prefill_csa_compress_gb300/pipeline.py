@@ -3,13 +3,12 @@ compressor, indexer top-k, then sparse attention -- the order the V4 decode
 layer calls them ("DeepSeek V4-Flash, MTP point", "Attention paths").
 
 ``CsaStep`` owns the outputs and workspaces so that repeated steps allocate
-nothing; it is plumbing around the four library calls and computes nothing
-itself.  The main compressor's output is read only by the attention call, so
-``run`` issues it on a side stream of default priority, where it overlaps the
-index-key compressor; that and the rest of the step run on a high-priority
-stream, so that the main compressor's blocks take only the SMs the critical
-path leaves free.  ``capture`` records a whole step as a CUDA
-graph so that a repeated step costs one launch on the host.
+nothing; it is plumbing around the library calls and computes nothing itself.
+Both compressors go through one ``csa_compress_pair`` call (one launch for
+short chunks), and every call of the step is issued on one stream, where each
+kernel is launched as a programmatic dependent of the one before it.
+``capture`` records a whole step as a CUDA graph so that a repeated step
+costs one launch on the host.
 """
 
 from __future__ import annotations
@@ -44,25 +43,28 @@ class CsaStep:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev) if status else None
         self.ws = {}
         self._prepared = None
-        self._side = None
-        self._crit = None
         self._graph = None
 
     def _ws(self, name):
         return self.ws.get(name)
 
-    def compress(self, stream=None):
+    def _compress_kw(self):
         t = self.t
-        self.ws["cm"] = B.csa_compress(
-            x=t["kv_raw"], kv=t["kv_raw"], w_gate=t["w_gate"], ape=t["ape"], ratio=self.ratio,
-            positions=t["row_pos"], row_req=t["row_req"], block_table=t["cmp_table"], out="bf16",
-            cmp_pool=t["cmp_pool"], status=self.status, workspace=self._ws("cm"), stream=stream)
-        self.ws["ci"] = B.csa_compress(
-            x=t["idx_raw"], kv=t["idx_raw"], w_gate=t["w_gate_i"], ape=t["ape_i"],
-            ratio=self.ratio, positions=t["row_pos"], row_req=t["row_req"],
-            block_table=t["cmp_table"], out="int8", idx_pool=t["idx_pool"],
-            idx_scale_pool=t["idx_scale"], rotate=True, rope_cos=t["rope_cos"],
-            rope_sin=t["rope_sin"], status=self.status, workspace=self._ws("ci"), stream=stream)
+        main = dict(x=t["kv_raw"], kv=t["kv_raw"], w_gate=t["w_gate"], ape=t["ape"],
+                    ratio=self.ratio, positions=t["row_pos"], row_req=t["row_req"],
+                    block_table=t["cmp_table"], out="bf16", cmp_pool=t["cmp_pool"],
+                    status=self.status)
+        keys = dict(x=t["idx_raw"], kv=t["idx_raw"], w_gate=t["w_gate_i"], ape=t["ape_i"],
+                    ratio=self.ratio, positions=t["row_pos"], row_req=t["row_req"],
+                    block_table=t["cmp_table"], out="int8", idx_pool=t["idx_pool"],
+                    idx_scale_pool=t["idx_scale"], rotate=True, rope_cos=t["rope_cos"],
+                    rope_sin=t["rope_sin"], status=self.status)
+        return main, keys
+
+    def compress(self, stream=None):
+        main, keys = self._compress_kw()
+        self.ws["cp"] = B.csa_compress_pair(main, keys, workspaces=self.ws.get("cp", (None, None)),
+                                            stream=stream)
 
     def index(self, stream=None, scores=None):
         t = self.t
@@ -91,17 +93,8 @@ class CsaStep:
         t = self.t
         calls = []
         if self.do_compress:
-            calls.append(B.csa_compress(
-                x=t["kv_raw"], kv=t["kv_raw"], w_gate=t["w_gate"], ape=t["ape"],
-                ratio=self.ratio, positions=t["row_pos"], row_req=t["row_req"],
-                block_table=t["cmp_table"], out="bf16", cmp_pool=t["cmp_pool"],
-                status=self.status, prepare=True))
-            calls.append(B.csa_compress(
-                x=t["idx_raw"], kv=t["idx_raw"], w_gate=t["w_gate_i"], ape=t["ape_i"],
-                ratio=self.ratio, positions=t["row_pos"], row_req=t["row_req"],
-                block_table=t["cmp_table"], out="int8", idx_pool=t["idx_pool"],
-                idx_scale_pool=t["idx_scale"], rotate=True, rope_cos=t["rope_cos"],
-                rope_sin=t["rope_sin"], status=self.status, prepare=True))
+            main, keys = self._compress_kw()
+            calls.append(B.csa_compress_pair(main, keys, prepare=True))
         calls.append(B.csa_index_topk(
             q_idx=t["q_idx"], weights=t["idx_w"], row_req=t["row_req"], row_pos=t["row_pos"],
             n_cmp=t["n_cmp"], ratio=self.ratio, idx_pool=t["idx_pool"],
@@ -126,29 +119,10 @@ class CsaStep:
                 self.compress(stream)
             self.index(stream)
             self.attention(stream)
-            return
-        calls = self._prepared
-        if not self.do_compress:
-            for c in calls:
+        else:
+            for c in self._prepared:
                 c(stream)
-            return
-        caller = torch.cuda.current_stream() if stream is None else stream
-        if self._side is None:
-            dev = self.t["q"].device
-            self._side = torch.cuda.Stream(device=dev)
-            self._crit = torch.cuda.Stream(device=dev,
-                                           priority=torch.cuda.Stream.priority_range()[1])
-        side, crit = self._side, self._crit
-        side.wait_stream(caller)           # inputs of this step are in place
-        crit.wait_stream(caller)
-        calls[0](side)                     # main compressor -> cmp_pool
-        calls[1](crit)                     # index-key compressor -> idx_pool
-        # the attention reads the new cmp_pool rows; joining here, before the
-        # indexer, keeps the indexer -> top-k -> attention launches one chain
-        crit.wait_stream(side)
-        for c in calls[2:]:                # indexer top-k, attention
-            c(crit)
-        caller.wait_stream(crit)
+        B.prof_join(stream)
 
     def capture(self):
         """Record one step (as ``run`` issues it) into a CUDA graph; ``replay``

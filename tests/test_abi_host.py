@@ -97,6 +97,18 @@ def test_workspace_queries_and_validation(L):
     a = _compress_args(b, n_rows=1, workspace=ctypes.addressof(dummy), workspace_bytes=256)
     assert L.csa_compress(ctypes.byref(a), None) == b.CSA_ERR_INVALID_ARG
     assert L.csa_compress(None, None) == b.CSA_ERR_INVALID_ARG
+    # the pair: both structs size-queried, either one's error returned
+    a1, a2 = _compress_args(b), _compress_args(b, d=128)
+    assert L.csa_compress_pair(ctypes.byref(a1), ctypes.byref(a2), None) == b.CSA_OK
+    assert (a1.workspace_bytes, a2.workspace_bytes) == (8192 * 512 * 4, 8192 * 128 * 4)
+    assert L.csa_compress_pair(ctypes.byref(_compress_args(b)),
+                               ctypes.byref(_compress_args(b, ratio=3)), None) == b.CSA_ERR_UNSUPPORTED
+    assert L.csa_compress_pair(ctypes.byref(bad), ctypes.byref(_compress_args(b)),
+                               None) == b.CSA_ERR_INVALID_ARG
+    a = _compress_args(b, n_rows=1, workspace=ctypes.addressof(dummy), workspace_bytes=256)
+    a2 = _compress_args(b, n_rows=1, workspace=ctypes.addressof(dummy), workspace_bytes=256)
+    assert L.csa_compress_pair(ctypes.byref(a), ctypes.byref(a2), None) == b.CSA_ERR_INVALID_ARG
+    assert L.csa_compress_pair(None, ctypes.byref(a2), None) == b.CSA_ERR_INVALID_ARG
 
     ia = b.IndexArgs()
     ia.struct_size = ctypes.sizeof(ia)

@@ -55,6 +55,9 @@ def _rope_q(t, row, key="q_idx"):
     ("chunked_prefill", dict(ctx=[1000], chunk=[1000], seed=31)),       # ragged: 250 groups
     ("chunked_prefill", dict(ctx=[1030, 70], chunk=[1030, 70], ratio=2, seed=32, pad_rows=3)),
     ("chunked_prefill", dict(ctx=[300], chunk=[300], ratio=1, seed=33)),
+    # at most 256 rows: both compressors in one fused launch
+    ("chunked_prefill", dict(ctx=[203], chunk=[203], seed=34)),
+    ("chunked_prefill", dict(ctx=[130, 61], chunk=[130, 61], ratio=1, seed=35, pad_rows=2)),
     ("serving_decode", {}),
     ("chunked_prefill", {}),                                            # full 8192-token chunk
 ])
@@ -357,6 +360,33 @@ def test_attention_decode_full_size(name):
 def test_attention_prefill_full_size_sampled():
     spec = spec_for("chunked_prefill", cmp_init="random")
     _attn_case(spec, 10, True, rows=[0, 1, 127, 128, 2047, 4000, 8191])
+
+
+@pytest.mark.parametrize("name,over", [
+    ("serving_decode", {}),
+    ("chunked_prefill", dict(ctx=[203], chunk=[203], seed=36)),
+    ("chunked_prefill", dict(ctx=[600], chunk=[600], seed=37)),   # long path: four launches
+])
+def test_compress_pair_equals_two_calls(name, over):
+    """csa_compress_pair writes exactly what csa_compress(first) followed by
+    csa_compress(second) writes."""
+    spec = spec_for(name, **over)
+    _, t = _load(spec)
+    step = CsaStep(t, spec.ratio, spec.topk, prefill=spec.mode == "prefill")
+    main, keys = step._compress_kw()
+    names = ("cmp_pool", "idx_pool", "idx_scale")
+    before = {k: t[k].clone() for k in names}
+    step.compress()
+    torch.cuda.synchronize()
+    pair = {k: t[k].clone() for k in names}
+    for k in names:
+        t[k].copy_(before[k])
+    csa.csa_compress(**main)
+    csa.csa_compress(**keys)
+    torch.cuda.synchronize()
+    assert _status(step) == 0
+    for k, v in pair.items():
+        assert torch.equal(v, t[k]), k
 
 
 # ------------------------------------------------------------------ whole step
