@@ -180,9 +180,10 @@ __device__ __forceinline__ void softmax_tile(uint32_t tmem, int qd, int h0, bool
                    pack2(x[8 * q + 4], x[8 * q + 5]), pack2(x[8 * q + 6], x[8 * q + 7]));
 }
 
-// Rotate q's last 64 channels (chunk 7 of the swizzled q tile) at position p
-// in place, FP32 rounded to BF16; `tid` in [0, nthreads).
-__device__ __forceinline__ void rope_q_tile(uint8_t *Qs, const csa_attn_args &a, int p, int tid,
+// Rotate the last 64 channels of the 64 q rows in Qs (128-byte swizzled
+// K-major chunks of 64 channels; chunk 7 holds the RoPE half) by the row
+// position's 32 cosines `cs` and sines `sn` (global or shared memory).
+__device__ __forceinline__ void rope_q_rows(uint8_t *Qs, const float *cs, const float *sn, int tid,
                                             int nthreads) {
   for (int e = tid; e < kHeads * 8; e += nthreads) {
     const int h = e >> 3, jj = e & 7;
@@ -192,13 +193,18 @@ __device__ __forceinline__ void rope_q_tile(uint8_t *Qs, const csa_attn_args &a,
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int pair = jj * 4 + q;
-      const float cs = a.rope_cos[(long long)p * kRopeHalf + pair];
-      const float sn = a.rope_sin[(long long)p * kRopeHalf + pair];
+      const float c = cs[pair], s = sn[pair];
       const float x0 = __uint_as_float(w[q] << 16), x1 = __uint_as_float(w[q] & 0xFFFF0000u);
-      w[q] = pack2(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+      w[q] = pack2(x0 * c - x1 * s, x0 * s + x1 * c);
     }
     *slot = make_uint4(w[0], w[1], w[2], w[3]);
   }
+}
+
+__device__ __forceinline__ void rope_q_tile(uint8_t *Qs, const csa_attn_args &a, int p, int tid,
+                                            int nthreads) {
+  rope_q_rows(Qs, a.rope_cos + (long long)p * kRopeHalf, a.rope_sin + (long long)p * kRopeHalf,
+              tid, nthreads);
 }
 
 // The tile's two contractions, issued by one warp (one elected lane).

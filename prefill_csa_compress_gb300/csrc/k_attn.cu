@@ -13,11 +13,16 @@
 // it gathers its first tile with cp.async (q and the gather overlap), runs the
 // tile's two contractions on tcgen05 (see attn_common.cuh) and a softmax whose
 // running maximum only moves past a 2^8 growth.  The partial softmaxes merge
-// through distributed shared memory: every CTA parks its O^T (FP32) and its
-// per-head maximum and denominator in its own shared memory, and after a
-// cluster barrier CTA r normalises the r-th slice of the output by reading
-// the matching slices of all S partials -- no partial ever reaches HBM and no
-// second kernel runs.
+// through distributed shared memory: every CTA sends its per-head maximum and
+// denominator to all CTAs, and its O^T / l as BF16 straight from registers
+// into the shared memory of the CTA that owns those output channels (32
+// lanes store 512 contiguous bytes); the owners' tile buffers receive, so the
+// sends wait at a split cluster barrier until every CTA's last P.V is done
+// (the partial is read out of TMEM and packed meanwhile).  After a second
+// barrier each owner weighs the S contributions of its channels and writes
+// them out.  No partial reaches HBM and no second kernel runs.  Barrier
+// initialisation and the tensor-memory allocation run before the kernel
+// waits for its predecessor in the stream.
 #include <cstring>
 
 #include "attn_common.cuh"
@@ -32,7 +37,7 @@ constexpr int AD_BAR = 1;  // named barrier over all 256 threads (the softmax's)
 constexpr int AD_MAX_CLUSTER = 16;
 
 struct AdMisc {
-  uint64_t q_full, mma_bar, done_bar, recv_bar;
+  uint64_t q_full, mma_bar, done_bar;
   uint32_t tmem_base;
   int pad;
   SoftState st;
@@ -40,9 +45,8 @@ struct AdMisc {
   alignas(16) float m_all[AD_MAX_CLUSTER][kHeads];  // every CTA's reference per head (log2)
   alignas(16) float l_all[AD_MAX_CLUSTER][kHeads];  // every CTA's denominator per head
   alignas(16) float red_l[4][kHeads];
-  alignas(16) float w_all[AD_MAX_CLUSTER][kHeads];  // scale of each CTA's partial
-  alignas(16) float inv_L[kHeads];
-  alignas(16) float inv_l[kHeads];  // 1 / this CTA's denominator per head
+  alignas(16) float f_self[kHeads];       // this CTA's share of each head's output
+  alignas(16) float rope[2 * kRopeHalf];  // cos, sin at the row's position
 };
 constexpr int AD_SMEM = OFF_MISC + (int)sizeof(AdMisc) + 1024;
 static_assert(AD_SMEM <= 227 * 1024, "shared memory");
@@ -60,6 +64,14 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -83,15 +95,17 @@ __device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
 }
 
 
-// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to the
-// shared memory of CTA `rank`, completing on that CTA's mbarrier.
-__device__ __forceinline__ void bulk_to_peer(const void *src, uint32_t dst_local, uint32_t bytes,
-                                             uint64_t *bar_local, uint32_t rank) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(peer_addr_u32(dst_local, rank)),
-      "r"(tc::smem_u32(src)), "r"(bytes), "r"(peer_addr(bar_local, rank))
-      : "memory");
+__device__ __forceinline__ void st_peer_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// The output channels d in [chan_lo(r), chan_lo(r + 1)) are merged by CTA r:
+// whole 16-channel groups, so that every output row piece starts on a 32-byte
+// sector and RoPE pairs stay together.
+__device__ __forceinline__ int chan_lo(uint32_t r, uint32_t S) {
+  return 16 * (int)((kHeadDim / 16 * r) / S);
 }
 
 // Pool row of candidate j of row t (its list: top-k entries, then the
@@ -130,32 +144,15 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   uint8_t *Qs = sm + OFF_Q;
   uint8_t *KVs = sm + OFF_KV;
   uint8_t *Ps = sm + OFF_P;
-  // once the tiles are done: this CTA's normalised partial O[h][d] / l[h] (BF16)
-  uint16_t *Os = reinterpret_cast<uint16_t *>(KVs);
   AdMisc *M = reinterpret_cast<AdMisc *>(sm + OFF_MISC);
-  tc::griddep_wait();
-  tc::griddep_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t = blockIdx.y;
   const uint32_t s = cluster_rank(), S = gridDim.x;
-  const int b = a.row_req[t];
-  if (b < 0) return;  // every CTA of the cluster serves the same row
-  if (b >= a.n_req) {
-    if (tid == 0 && s == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
-    return;
-  }
-  const int p = a.row_pos[t];
-  const int V = min(visible_count(p, a.ratio, a.n_cmp[b]), a.cmp_max_blocks * kBlock);
-  const int kvl = a.kv_len[b];
-  const int n_tiles = (a.topk + a.window + CT - 1) / CT;
-  const int g_begin = (int)s * tiles_per_split;
-  const int g_end = min(n_tiles, g_begin + tiles_per_split);
 
+  // ---- set-up that reads no global memory, overlapping the previous kernel
   if (tid == 0) {
     tc::mbar_init(&M->q_full, 1);
     tc::mbar_init(&M->mma_bar, 1);
     tc::mbar_init(&M->done_bar, 1);
-    tc::mbar_init(&M->recv_bar, 1);
     tc::mbar_fence_init();
   }
   if (tid < kHeads) M->st.m[tid] = -INFINITY;
@@ -167,6 +164,26 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = M->tmem_base;
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
+
+  const int t = blockIdx.y;
+  const int b = a.row_req[t];
+  if (b < 0 || b >= a.n_req) {  // the same for every CTA of the cluster
+    if (b >= 0 && tid == 0 && s == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
+    cluster_wait();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+    return;
+  }
+  const int p = a.row_pos[t];
+  const int V = min(visible_count(p, a.ratio, a.n_cmp[b]), a.cmp_max_blocks * kBlock);
+  const int kvl = a.kv_len[b];
+  const int n_tiles = (a.topk + a.window + CT - 1) / CT;
+  const int g_begin = (int)s * tiles_per_split;
+  const int g_end = min(n_tiles, g_begin + tiles_per_split);
   const uint32_t kv = tc::smem_u32(KVs), qq = tc::smem_u32(Qs), pp = tc::smem_u32(Ps);
 
   // q of the row by TMA, in flight while the first tile is gathered
@@ -181,8 +198,10 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     rot = false;
     if (tid == 0 && s == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
   }
-
-  // the sink logit of head tid, read now rather than at the merge
+  // the row's RoPE entries and the sink logit of head tid, read up front
+  if (rot && tid < 2 * kRopeHalf)
+    M->rope[tid] = tid < kRopeHalf ? a.rope_cos[(long long)p * kRopeHalf + tid]
+                                   : a.rope_sin[(long long)p * kRopeHalf + tid - kRopeHalf];
   const float sink2 = tid < kHeads && a.sink ? a.sink[tid] * kLog2e : -INFINITY;
   const int qd = warp & 3, h0 = (warp >> 2) * 32, c = qd * 32 + lane;
   const int sub = lane >> 3, piece = lane & 7;  // gather: rows 32 i + 4 warp + sub, 16-byte piece
@@ -218,7 +237,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
         ok = false;
         flag(a.status_dev, CSA_DEV_TIMEOUT);
       }
-      if (rot) rope_q_tile(Qs, a, p, tid, AD_THREADS);
+      if (rot) rope_q_rows(Qs, M->rope, M->rope + kRopeHalf, tid, AD_THREADS);
       q_ready = true;
     }
     tc::cp_async_wait_all();
@@ -257,22 +276,27 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   }
   if (has_tiles && !q_ready) tc::mbar_wait(&M->q_full, 0, 50000000ull);  // no tile had candidates
   if (!ok && warp == 0) {
-    // nothing of ours may still run on TMEM when it is released
+    // nothing of ours may still run on TMEM when it is read or released
     tc::mma_commit_elect(&M->done_bar);
     tc::mbar_wait(&M->done_bar, 0, 100000000ull);
   }
 
-  // ---- this CTA's partial: its per-head reference and denominator go to
-  // every CTA of the cluster (remote stores, ordered by the cluster barrier);
-  // O^T / l stays here as BF16 O[h][d] (normalised, so BF16 keeps it to
-  // 2^-9 relative whatever the magnitudes)
+  // ---- this CTA's partial to the owners of its output channels, with its
+  // per-head reference and denominator to every CTA.  The partial travels as
+  // BF16 O^T / l (normalised by this CTA's own denominator, so BF16 keeps it
+  // to 2^-9 relative whatever the magnitudes); at owner r, 16-byte element
+  // (sender, hb, d - chan_lo(r)) holds heads 8 hb .. 8 hb + 7 of channel d,
+  // so the 32 lanes of a warp (32 consecutive channels) store 512
+  // contiguous bytes.  The owners receive in their tile buffer, which is
+  // free once they have arrived at the first cluster barrier below (after
+  // their last P.V); the partial is read out of TMEM and packed meanwhile.
   M->red_l[qd][h0 + lane] = lacc;
   __syncthreads();
   if (tid < kHeads) {
     const float l = (M->red_l[0][tid] + M->red_l[1][tid]) + (M->red_l[2][tid] + M->red_l[3][tid]);
-    M->inv_l[tid] = !first && l > 0.f ? 1.f / l : 0.f;
+    M->f_self[tid] = !first && l > 0.f ? 1.f / l : 0.f;
   }
-  cluster_wait();
+  cluster_wait();  // every CTA of the cluster is running
   for (int e = tid; e < kHeads * (int)S; e += AD_THREADS) {
     const int h = e % kHeads;
     const uint32_t q = e / kHeads;
@@ -282,109 +306,123 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     st_peer_f32(peer_addr(&M->m_all[s][h], q), m);
     st_peer_f32(peer_addr(&M->l_all[s][h], q), l);
   }
+  tc::tc_fence_before();
+  cluster_arrive();  // this CTA's tile buffer may now receive
   __syncthreads();
-  // output slices: CTA r normalises units [slice_lo(r), slice_lo(r + 1)) of
-  // 8 channels; peers send it their part of that slice into its (now free) q
-  // buffer, one region per sender (regions of senders above r move down one,
-  // so S - 1 regions of kUnits / S + 1 units fit in the 64 KB)
-  constexpr int kUnits = kHeads * kHeadDim / 8;
-  auto slice_lo = [&](uint32_t r) { return (int)((long long)kUnits * r / S); };
-  const int u0 = slice_lo(s), u1 = slice_lo(s + 1);
-  const uint32_t region = (uint32_t)(kUnits / S + 1) * 16;  // bytes per sender
-  if (tid == 0) tc::mbar_arrive_expect_tx(&M->recv_bar, (uint32_t)(u1 - u0) * 16 * (S - 1));
-  if (first) {
-    // no candidates here: a zero partial, so that peers may read it unmasked
-    for (int e = tid; e < kHeads * kHeadDim / 8; e += AD_THREADS)
-      reinterpret_cast<uint4 *>(Os)[e] = make_uint4(0u, 0u, 0u, 0u);
-  } else {
+  const int rows_max = 16 * (int)((kHeadDim / 16 + S - 1) / S);  // channels per owner, at most
+  uint4 pk[4][4];  // [m4][group of 8 heads]
+  {
+    float f[32];
+    load32(M->f_self + h0, f);
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
-    float il[32];
-    load32(M->inv_l + h0, il);
-#pragma unroll 1
+    tc::tc_fence_after();
+#pragma unroll
     for (int m4 = 0; m4 < 4; ++m4) {
       float v[32];
-      tc::tmem_ld32(tmem + lane_off + O_COL + m4 * 64 + h0, v);
-      const int d = m4 * 128 + qd * 32 + lane;
+      if (first) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        Os[(h0 + j) * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j] * il[j]));
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      } else {
+        tc::tmem_ld32(tmem + lane_off + O_COL + m4 * 64 + h0, v);
+      }
+#pragma unroll
+      for (int cgrp = 0; cgrp < 4; ++cgrp) {
+        pk[m4][cgrp].x = pack2(v[8 * cgrp + 0] * f[8 * cgrp + 0], v[8 * cgrp + 1] * f[8 * cgrp + 1]);
+        pk[m4][cgrp].y = pack2(v[8 * cgrp + 2] * f[8 * cgrp + 2], v[8 * cgrp + 3] * f[8 * cgrp + 3]);
+        pk[m4][cgrp].z = pack2(v[8 * cgrp + 4] * f[8 * cgrp + 4], v[8 * cgrp + 5] * f[8 * cgrp + 5]);
+        pk[m4][cgrp].w = pack2(v[8 * cgrp + 6] * f[8 * cgrp + 6], v[8 * cgrp + 7] * f[8 * cgrp + 7]);
+      }
     }
   }
-  tc::fence_async_shared();  // the parked partial is read by the bulk copies
-  tc::tc_fence_before();
-  cluster_sync();
-  if (tid == 0)
-    for (uint32_t r = 0; r < S; ++r) {
-      if (r == s) continue;
-      const int lo = slice_lo(r), hi = slice_lo(r + 1);
-      const uint32_t slot = s < r ? s : s - 1;
-      bulk_to_peer(Os + (size_t)lo * 8, tc::smem_u32(Qs) + slot * region, (uint32_t)(hi - lo) * 16,
-                   &M->recv_bar, r);
+  cluster_wait_acquire();  // every CTA's tile buffer is free; statistics have landed
+  {
+    const uint32_t recv = tc::smem_u32(KVs);
+#pragma unroll
+    for (int m4 = 0; m4 < 4; ++m4) {
+      const int d = m4 * 128 + qd * 32 + lane;
+      uint32_t r = (uint32_t)(((d >> 4) * (int)S) / (kHeadDim / 16));
+      if (r + 1 < S && chan_lo(r + 1, S) <= d) ++r;
+      const int dl = d - chan_lo(r, S);
+      const uint32_t base = peer_addr_u32(recv, r);
+#pragma unroll
+      for (int cgrp = 0; cgrp < 4; ++cgrp) {
+        const int hb = (h0 >> 3) + cgrp;
+        st_peer_v4(base + (uint32_t)((((int)s * 8 + hb) * rows_max + dl) * 16), pk[m4][cgrp]);
+      }
     }
+  }
+  cluster_sync();  // the partials have landed; nothing remote follows
 
-  // ---- merge weights: one thread per head, from the statistics every CTA sent
+  // ---- merge weights: each head's maximum and denominator over the S CTAs;
+  // m_all[q][h] becomes the weight of CTA q's partial
   if (tid < kHeads) {
     const int h = tid;
-    const float s2 = sink2;
-    float mx = s2;
+    float mx = sink2;
     for (uint32_t q = 0; q < S; ++q) mx = fmaxf(mx, M->m_all[q][h]);
     float L = 0.f;
     if (mx != -INFINITY) {
-      L = exp2f(s2 - mx);
+      L = exp2f(sink2 - mx);
       for (uint32_t q = 0; q < S; ++q) {
         const float mq = M->m_all[q][h];
-        const float w = mq == -INFINITY ? 0.f : exp2f(mq - mx);
-        M->w_all[q][h] = w * M->l_all[q][h];  // the partial was parked divided by l
-        L += w * M->l_all[q][h];
+        L += mq == -INFINITY ? 0.f : exp2f(mq - mx) * M->l_all[q][h];
       }
-    } else {
-      for (uint32_t q = 0; q < S; ++q) M->w_all[q][h] = 0.f;
     }
-    M->inv_L[h] = L > 0.f ? 1.f / L : 0.f;
+    const float inv_L = L > 0.f ? 1.f / L : 0.f;
+    for (uint32_t q = 0; q < S; ++q) {
+      const float mq = M->m_all[q][h];
+      M->m_all[q][h] = mq == -INFINITY ? 0.f : exp2f(mq - mx) * M->l_all[q][h] * inv_L;
+    }
     if (s == 0 && a.lse)
       a.lse[(long long)t * kHeads + h] = L > 0.f ? (mx + log2f(L)) * kLn2 : -INFINITY;
   }
   __syncthreads();
 
-  // ---- this CTA's slice of the output, 8 channels per step: its own part
-  // from the parked partial, the peers' parts from the receive regions
-  if (S > 1 && !tc::mbar_wait(&M->recv_bar, 0)) flag(a.status_dev, CSA_DEV_TIMEOUT);
-  const bool inv = a.inv_rope_out && a.rope_cos != nullptr && p >= 0 && p < a.rope_cap;
-  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + (long long)t * kHeads * kHeadDim;
-  for (int u = u0 + tid; u < u1; u += AD_THREADS) {
-    const int h = u / (kHeadDim / 8), d = (u % (kHeadDim / 8)) * 8;
-    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (uint32_t q = 0; q < S; ++q) {
-      const uint32_t slot = q < s ? q : q - 1;
-      const uint4 v = q == s ? reinterpret_cast<const uint4 *>(Os)[u]
-                             : *reinterpret_cast<const uint4 *>(Qs + slot * region + (u - u0) * 16);
-      const float w = M->w_all[q][h];
-      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+  // ---- this CTA's channels: warp w sums heads 8 w .. 8 w + 7 over the S
+  // partials, 32 consecutive channels per step (a RoPE pair sits in an
+  // even/odd lane pair), and stores them (64 contiguous bytes per head)
+  {
+    const int d0 = chan_lo(s, S), dn = chan_lo(s + 1, S) - d0;
+    const bool inv = a.inv_rope_out && rot;
+    const int hb = warp;
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + (long long)t * kHeads * kHeadDim;
+    for (int dl0 = 0; dl0 < dn; dl0 += 32) {  // the same trip count in every lane
+      const int dl = dl0 + lane;
+      const bool live = dl < dn;  // dn is a multiple of 16: RoPE pairs live together
+      float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (uint32_t q = 0; q < S && live; ++q) {
+        const float4 w0 = *reinterpret_cast<const float4 *>(&M->m_all[q][hb * 8]);
+        const float4 w1 = *reinterpret_cast<const float4 *>(&M->m_all[q][hb * 8 + 4]);
+        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        const uint4 v =
+            *reinterpret_cast<const uint4 *>(KVs + (((int)q * 8 + hb) * rows_max + dl) * 16);
+        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        o[2 * i] = fmaf(w, __uint_as_float(wd[i] << 16), o[2 * i]);
-        o[2 * i + 1] = fmaf(w, __uint_as_float(wd[i] & 0xFFFF0000u), o[2 * i + 1]);
+        for (int i = 0; i < 4; ++i) {
+          o[2 * i] = fmaf(wv[2 * i], __uint_as_float(wd[i] << 16), o[2 * i]);
+          o[2 * i + 1] = fmaf(wv[2 * i + 1], __uint_as_float(wd[i] & 0xFFFF0000u), o[2 * i + 1]);
+        }
+      }
+      const int d = d0 + dl;
+      if (inv) {
+        // inverse rotation of the RoPE channel pairs (partner: the neighbouring lane)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float other = __shfl_xor_sync(0xffffffffu, o[i], 1);
+          if (d >= kHeadDim - kRopeDim) {
+            const int pair = (d - (kHeadDim - kRopeDim)) >> 1;
+            const float cs = M->rope[pair], sn = M->rope[kRopeHalf + pair];
+            o[i] = (d & 1) == 0 ? o[i] * cs + other * sn : -other * sn + o[i] * cs;
+          }
+        }
+      }
+      if (live) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) out[(hb * 8 + i) * kHeadDim + d] = __float2bfloat16_rn(o[i]);
       }
     }
-    const float il = M->inv_L[h];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] *= il;
-    if (inv && d >= kHeadDim - kRopeDim) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int pair = (d + 2 * i - (kHeadDim - kRopeDim)) >> 1;
-        const float cs = a.rope_cos[(long long)p * kRopeHalf + pair];
-        const float sn = a.rope_sin[(long long)p * kRopeHalf + pair];
-        const float x0 = o[2 * i], x1 = o[2 * i + 1];
-        o[2 * i] = x0 * cs + x1 * sn;
-        o[2 * i + 1] = -x0 * sn + x1 * cs;
-      }
-    }
-    *reinterpret_cast<uint4 *>(out + h * kHeadDim + d) =
-        make_uint4(pack2(o[0], o[1]), pack2(o[2], o[3]), pack2(o[4], o[5]), pack2(o[6], o[7]));
   }
-  // this CTA's outgoing copies have landed once every peer is through its wait
-  cluster_sync();
+  tc::tc_fence_before();
+  __syncthreads();
   tc::tc_fence_after();
   if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
