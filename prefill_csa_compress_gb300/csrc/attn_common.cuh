@@ -109,19 +109,21 @@ struct SoftState {
 };
 
 // Softmax of one tile by the 256 threads of named barrier `bar` (thread =
-// candidate c = qd*32 + lane, heads h0..h0+31).  Reads S^T from TMEM, moves
-// the running reference of heads whose logits grew past 2^8 (rescaling O^T in
-// TMEM unless this is the row's first tile, and this warp's partial
-// denominators `lacc`), and writes P^T as BF16.  On return x holds the FP32
-// probabilities of this thread's candidate; the caller makes P visible to the
-// MMA (fence, barrier) and adds the column sums of x to lacc.
-__device__ __forceinline__ void softmax_tile(uint32_t tmem, int qd, int h0, bool valid, float sl2,
-                                             bool first, SoftState *st, uint8_t *Ps, int bar,
-                                             float &lacc, float (&x)[32]) {
+// candidate c = qd*32 + lane, heads h0..h0+31), from this thread's raw
+// logits x (S^T row c).  Moves the running reference of heads whose logits
+// grew past 2^8 (rescaling the n_mt O^T tiles at TMEM column o_col unless this
+// is the row's first tile, and this warp's partial denominators `lacc`), and
+// writes P^T as BF16.  `ready()` runs (in every thread) before O^T or P is
+// touched.  On return x holds the FP32 probabilities of this thread's
+// candidate; the caller makes P visible to the MMA (fence, barrier) and adds
+// the column sums of x to lacc.
+template <typename Ready>
+__device__ __forceinline__ void softmax_vals(uint32_t tmem, uint32_t o_col, int n_mt, int qd, int h0,
+                                             bool valid, float sl2, bool first, SoftState *st,
+                                             uint8_t *Ps, int bar, float &lacc, float (&x)[32],
+                                             Ready &&ready) {
   const int lane = threadIdx.x & 31, c = qd * 32 + lane;
   const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
-  tc::tc_fence_after();
-  tc::tmem_ld32(tmem + lane_off + S_COL + h0, x);
 #pragma unroll
   for (int j = 0; j < 32; ++j) x[j] = valid ? x[j] * sl2 : -INFINITY;
   float mref[32];
@@ -151,6 +153,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tmem, int qd, int h0, bool
     lacc *= corr;  // every warp's partial denominator of head h moves with it
     tc::bar_sync(bar, 256);
     load32(st->m + h0, mref);
+    ready();
     if (!first) {
       float cr[32];
       load32(st->corr + h0, cr);
@@ -158,10 +161,11 @@ __device__ __forceinline__ void softmax_tile(uint32_t tmem, int qd, int h0, bool
 #pragma unroll
       for (int j = 0; j < 32; ++j) any |= cr[j] != 1.f;
       if (__any_sync(0xffffffffu, any)) {
+        tc::tc_fence_after();
 #pragma unroll 1
-        for (int m4 = 0; m4 < 4; ++m4) {
+        for (int m4 = 0; m4 < n_mt; ++m4) {
           float v[32];
-          const uint32_t addr = tmem + lane_off + O_COL + m4 * 64 + h0;
+          const uint32_t addr = tmem + lane_off + o_col + m4 * 64 + h0;
           tc::tmem_ld32(addr, v);
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] *= cr[j];
@@ -169,6 +173,8 @@ __device__ __forceinline__ void softmax_tile(uint32_t tmem, int qd, int h0, bool
         }
       }
     }
+  } else {
+    ready();
   }
   // P = 2^(x - m) as BF16 into the MN-major P^T rows
 #pragma unroll
@@ -180,14 +186,24 @@ __device__ __forceinline__ void softmax_tile(uint32_t tmem, int qd, int h0, bool
                    pack2(x[8 * q + 4], x[8 * q + 5]), pack2(x[8 * q + 6], x[8 * q + 7]));
 }
 
-// Rotate the last 64 channels of the 64 q rows in Qs (128-byte swizzled
-// K-major chunks of 64 channels; chunk 7 holds the RoPE half) by the row
-// position's 32 cosines `cs` and sines `sn` (global or shared memory).
-__device__ __forceinline__ void rope_q_rows(uint8_t *Qs, const float *cs, const float *sn, int tid,
-                                            int nthreads) {
+// The same, reading S^T from TMEM columns [0, 64) (O^T: four tiles at O_COL).
+__device__ __forceinline__ void softmax_tile(uint32_t tmem, int qd, int h0, bool valid, float sl2,
+                                             bool first, SoftState *st, uint8_t *Ps, int bar,
+                                             float &lacc, float (&x)[32]) {
+  const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+  tc::tc_fence_after();
+  tc::tmem_ld32(tmem + lane_off + S_COL + h0, x);
+  softmax_vals(tmem, O_COL, 4, qd, h0, valid, sl2, first, st, Ps, bar, lacc, x, [] {});
+}
+
+// Rotate the RoPE chunk of the 64 q rows (the 128-byte swizzled K-major
+// chunk holding channels 448..511, 128 bytes per head) by the row position's
+// 32 cosines `cs` and sines `sn` (global or shared memory).
+__device__ __forceinline__ void rope_q_rows(uint8_t *chunk, const float *cs, const float *sn,
+                                            int tid, int nthreads) {
   for (int e = tid; e < kHeads * 8; e += nthreads) {
     const int h = e >> 3, jj = e & 7;
-    uint4 *slot = reinterpret_cast<uint4 *>(Qs + 7 * 8192 + h * 128 + ((jj ^ (h & 7)) << 4));
+    uint4 *slot = reinterpret_cast<uint4 *>(chunk + h * 128 + ((jj ^ (h & 7)) << 4));
     const uint4 x4 = *slot;
     uint32_t w[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
@@ -201,12 +217,49 @@ __device__ __forceinline__ void rope_q_rows(uint8_t *Qs, const float *cs, const 
   }
 }
 
-__device__ __forceinline__ void rope_q_tile(uint8_t *Qs, const csa_attn_args &a, int p, int tid,
-                                            int nthreads) {
-  rope_q_rows(Qs, a.rope_cos + (long long)p * kRopeHalf, a.rope_sin + (long long)p * kRopeHalf,
-              tid, nthreads);
+// ---------------------------------------------------------------- clusters
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
 }
 
+// Cluster barrier, whole or split (arrive early, wait where it matters).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+
+// Address of shared-memory address `la` (this CTA) in the shared memory of CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr_u32(uint32_t la, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(la), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank) {
+  return peer_addr_u32(tc::smem_u32(p), rank);
+}
+__device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_peer_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
 // The tile's two contractions, issued by one warp (one elected lane).
 __device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t kv, uint32_t qq, int kc) {
   constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, kHeads);

@@ -51,56 +51,6 @@ struct AdMisc {
 constexpr int AD_SMEM = OFF_MISC + (int)sizeof(AdMisc) + 1024;
 static_assert(AD_SMEM <= 227 * 1024, "shared memory");
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Split cluster barrier: arrive early, wait where it matters.
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_wait_acquire() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
-                   "memory");
-}
-
-// Address of shared-memory address `la` (this CTA) in the shared memory of CTA `rank`.
-__device__ __forceinline__ uint32_t peer_addr_u32(uint32_t la, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(la), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank) {
-  return peer_addr_u32(tc::smem_u32(p), rank);
-}
-
-__device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-
-__device__ __forceinline__ void st_peer_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
 // The output channels d in [chan_lo(r), chan_lo(r + 1)) are merged by CTA r:
 // whole 16-channel groups, so that every output row piece starts on a 32-byte
 // sector and RoPE pairs stay together.
@@ -237,7 +187,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
         ok = false;
         flag(a.status_dev, CSA_DEV_TIMEOUT);
       }
-      if (rot) rope_q_rows(Qs, M->rope, M->rope + kRopeHalf, tid, AD_THREADS);
+      if (rot) rope_q_rows(Qs + 7 * 8192, M->rope, M->rope + kRopeHalf, tid, AD_THREADS);
       q_ready = true;
     }
     tc::cp_async_wait_all();

@@ -358,7 +358,8 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
         if (stid == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
       }
       if (rot) {
-        rope_q_tile(Qs, a, R.p, stid, AP_SOFT);
+        rope_q_rows(Qs + 7 * 8192, a.rope_cos + (long long)R.p * kRopeHalf,
+                    a.rope_sin + (long long)R.p * kRopeHalf, stid, AP_SOFT);
         tc::fence_async_shared();
       }
       tc::bar_sync(AP_BAR, AP_SOFT);

@@ -53,6 +53,7 @@ struct IdxTc {
   static constexpr int NS = ATMEM ? 8 : 3;        // staging ring depth
   static constexpr int NA = 2;                    // converted A tiles
   static constexpr int NT = ATMEM ? 3 : 2;        // TMEM accumulator slots
+  static constexpr int NSC = 8;                   // scale ring: > NA + NT tiles in flight
   static constexpr int A_COL = 0;                 // TMEM A tiles (64 columns each)
   static constexpr int ACC_COL = ATMEM ? NA * 64 : 0;
   static constexpr int B_CHUNK = N * 128;         // bytes of one 64-wide K chunk of B
@@ -64,11 +65,13 @@ struct IdxTc {
   static constexpr int OFF_ST = OFF_A + (ATMEM ? 0 : NA * A_BUF);
   static constexpr int OFF_STSC = OFF_ST + NS * PAGE;
   static constexpr int OFF_SC = OFF_STSC + NS * kBlock * 4;
-  static constexpr int OFF_W = OFF_SC + 4 * kBlock * 4;
+  static constexpr int OFF_W = OFF_SC + NSC * kBlock * 4;
   static constexpr int OFF_ROPE = OFF_W + G * kHeads * 4;   // per row: 32 cos, 32 sin
   static constexpr int OFF_MISC = OFF_ROPE + G * 64 * 4;
   static constexpr int SMEM = OFF_MISC + 512 + 1024;        // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(NA + NT < NSC, "the scale ring must outlast the tiles in flight");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 struct IdxMisc {
@@ -77,10 +80,10 @@ struct IdxMisc {
   uint64_t a_full[3];    // converters -> MMA
   uint64_t a_free[3];    // MMA commit -> converters (A tile may be overwritten)
   uint64_t acc_full[4];  // MMA commit -> epilogue
-  uint64_t acc_empty[4]; // epilogue -> converters (slot and its scales free)
+  uint64_t acc_empty[4]; // epilogue -> MMA (accumulator may be overwritten)
   uint32_t tmem_base;
   int st_ok[8];
-  int a_ok[4];
+  int t_ok[8];           // per scale slot: the page was valid
   volatile int abort;
   int row_t[4];
   int row_V[4];
@@ -356,10 +359,9 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
         const int ct = tid - W_CONV0 * 32;
         for (int k = 0; k < nt; ++k) {
           const uint32_t itk = it + k;
-          const int s = itk % C::NS, j = itk % C::NA, q4 = itk % C::NT;
+          const int s = itk % C::NS, j = itk % C::NA, sc = itk % C::NSC;
           if (!tc::mbar_wait(&M->st_full[s], (itk / C::NS) & 1) ||
-              !tc::mbar_wait(&M->a_free[j], ((itk / C::NA) & 1) ^ 1) ||
-              !tc::mbar_wait(&M->acc_empty[q4], ((itk / C::NT) & 1) ^ 1)) {
+              !tc::mbar_wait(&M->a_free[j], ((itk / C::NA) & 1) ^ 1)) {
             set_abort(M, a.status_dev);
             break;
           }
@@ -389,9 +391,9 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
               tc::tmem_st32u(tmem + ((uint32_t)(wq * 32) << 16) + C::A_COL + j * 64 + half * 32,
                              packed);
               tc::tmem_wait_st();
-              if (half == 0) Sc[q4 * kBlock + r] = StSc[s * kBlock + r];
+              if (half == 0) Sc[sc * kBlock + r] = StSc[s * kBlock + r];
             }
-            if (ct == 0) M->a_ok[q4] = ok;
+            if (ct == 0) M->t_ok[sc] = ok;
             tc::tc_fence_before();
           } else {
           if (ok) {
@@ -411,9 +413,9 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
               *reinterpret_cast<uint4 *>(dst + kc * C::A_CHUNK + r * 128 + ((jj ^ (r & 7)) << 4)) =
                   i8x8_to_f16x8(raw[q]);
             }
-            if (ct < kBlock) Sc[q4 * kBlock + ct] = StSc[s * kBlock + ct];
+            if (ct < kBlock) Sc[sc * kBlock + ct] = StSc[s * kBlock + ct];
           }
-          if (ct == 0) M->a_ok[q4] = ok;
+          if (ct == 0) M->t_ok[sc] = ok;
           tc::fence_async_shared();
           }
           tc::mbar_arrive(&M->a_full[j]);
@@ -432,13 +434,14 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
             bd[kc * 4 + s16] = tc::desc_sw128(b_base + kc * C::B_CHUNK + s16 * 32);
         for (int k = 0; k < nt; ++k) {
           const uint32_t itk = it + k;
-          const int j = itk % C::NA;
-          if (!tc::mbar_wait(&M->a_full[j], (itk / C::NA) & 1)) {
+          const int j = itk % C::NA, q4 = itk % C::NT;
+          if (!tc::mbar_wait(&M->a_full[j], (itk / C::NA) & 1) ||
+              !tc::mbar_wait(&M->acc_empty[q4], ((itk / C::NT) & 1) ^ 1)) {
             set_abort(M, a.status_dev);
             break;
           }
           tc::tc_fence_after();
-          const uint32_t d = tmem + C::ACC_COL + (itk % C::NT) * C::N;
+          const uint32_t d = tmem + C::ACC_COL + q4 * C::N;
           if constexpr (C::ATMEM) {
             const uint32_t a_t = tmem + C::A_COL + j * 64;
 #pragma unroll
@@ -463,7 +466,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
             }
           }
           tc::mma_commit_elect(&M->a_free[j]);
-          tc::mma_commit_elect(&M->acc_full[itk % C::NT]);
+          tc::mma_commit_elect(&M->acc_full[q4]);
           __syncwarp();
         }
       } else if (warp < W_CONV0) {
@@ -473,14 +476,14 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
         const int i0 = warp >> 2;
         for (int k = 0; k < nt; ++k) {
           const uint32_t itk = it + k;
-          const int q4 = itk % C::NT;
+          const int q4 = itk % C::NT, sc = itk % C::NSC;
           if (!tc::mbar_wait(&M->acc_full[q4], (itk / C::NT) & 1)) {
             set_abort(M, a.status_dev);
             break;
           }
           tc::tc_fence_after();
-          const int ok = M->a_ok[q4];
-          const float scale = Sc[q4 * kBlock + r];
+          const int ok = M->t_ok[sc];
+          const float scale = Sc[sc * kBlock + r];
           const int c = (tb + k) * kBlock + r;
 #pragma unroll
           for (int i = i0; i < G; i += 2) {
