@@ -34,6 +34,19 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # kernel reports null.  Values are from `ncu --metrics dram__bytes_read.sum,
 # dram__bytes_write.sum` captures of these same bench workloads.
 NCU_TRAFFIC = {
+    ("serving_decode", "compress_fused"): {"bytes": 613675, "src": "396e39098712"},
+    ("serving_decode", "index_score"): {"bytes": 1536165, "src": "4a6ecdbb1973"},
+    ("serving_decode", "index_topk"): {"bytes": 122142, "src": "3177992dcba3"},
+    ("serving_decode", "attn_decode"): {"bytes": 4612742, "src": "8a85a42340d5"},
+    ("million_decode", "compress_fused"): {"bytes": 41947, "src": "396e39098712"},
+    ("million_decode", "index_score"): {"bytes": 142124483, "src": "4a6ecdbb1973"},
+    ("million_decode", "index_topk"): {"bytes": 8640439, "src": "3177992dcba3"},
+    ("million_decode", "attn_decode"): {"bytes": 17841061, "src": "8a85a42340d5"},
+    ("chunked_prefill", "compress_gate"): {"bytes": 5534313, "src": "396e39098712"},
+    ("chunked_prefill", "compress_pool"): {"bytes": 16081495, "src": "396e39098712"},
+    ("chunked_prefill", "index_score"): {"bytes": 149992914, "src": "4a6ecdbb1973"},
+    ("chunked_prefill", "index_topk"): {"bytes": 34516370, "src": "3177992dcba3"},
+    ("chunked_prefill", "attn_prefill"): {"bytes": 1059085687, "src": "d956f63fbd32"},
 }
 
 
