@@ -9,6 +9,7 @@ from .csa_oracle import (  # noqa: F401
     as_f64,
     bf16_round,
     compress,
+    compress_stateful,
     index_scores,
     page_rows,
     quantize_int8,

@@ -11,7 +11,8 @@ straight from the pages:
 * "DeepSeek V4.1 Flash" (pypto-lib), sections "Serving-owned full RoPE
   tables" (FP32 half-width tables, adjacent-pair rotation, negative position =
   identity), "Compressor state ownership" (pooling softmax, BF16 rounding
-  before RMSNorm, Top-K acceptance rules, per-row tolerances).
+  before RMSNorm, the recurrent state ring of kv rows and gate scores across
+  calls, Top-K acceptance rules, per-row tolerances).
 * "Hyper-Parallel ... DeepSeek V4 CP" (gitcode issue #2), sections
   "二阶段 CP 总体算法" (shared-KV sparse attention with sinks, softmax_scale,
   ori_win_left = 127), "7. Window KV Halo" (window includes self),
@@ -182,22 +183,94 @@ def compress(x, kv, w_gate, ape, ratio, positions, row_req, gamma=None, rms_eps=
                for j, s in enumerate(rows)):
             continue
         logits = x[rows] @ w_gate + ape[:r]  # [r, D]
-        mx = logits.max(axis=0, keepdims=True)
-        e = np.exp(logits - mx)
-        w = e / e.sum(axis=0, keepdims=True)
-        y = (w * kv[rows]).sum(axis=0)
-        y = bf16_round(y)
-        if gamma is not None:
-            g_ = as_f64(gamma)
-            y = bf16_round(y / np.sqrt(np.mean(y * y) + rms_eps) * g_)
-        g = p // r
-        if rotate:
-            y = rope_rotate(y, g * r, rope_cos, rope_sin, rope_dim)
-        if out == "bf16":
-            results.append((b, g, bf16_round(y)))
-        else:
-            codes, scale = quantize_int8(y)
-            results.append((b, g, codes, scale))
+        results.append(_publish_group(b, p // r, r, logits, kv[rows], gamma, rms_eps, rotate,
+                                      rope_cos, rope_sin, rope_dim, out))
+    return results
+
+
+def _publish_group(b, g, r, logits, kvs, gamma, rms_eps, rotate, rope_cos, rope_sin, rope_dim,
+                   out):
+    """Pool one group from its r gate scores and kv rows ([r, D] each) and
+    publish it: the per-channel softmax over the r tokens, BF16 rounding,
+    optional RMSNorm, optional rotation at the group start, BF16 or INT8."""
+    mx = logits.max(axis=0, keepdims=True)
+    e = np.exp(logits - mx)
+    w = e / e.sum(axis=0, keepdims=True)
+    y = (w * kvs).sum(axis=0)
+    y = bf16_round(y)
+    if gamma is not None:
+        g_ = as_f64(gamma)
+        y = bf16_round(y / np.sqrt(np.mean(y * y) + rms_eps) * g_)
+    if rotate:
+        y = rope_rotate(y, g * r, rope_cos, rope_sin, rope_dim)
+    if out == "bf16":
+        return (b, g, bf16_round(y))
+    codes, scale = quantize_int8(y)
+    return (b, g, codes, scale)
+
+
+def compress_stateful(x, kv, w_gate, ape, ratio, positions, row_req, state, state_table,
+                      gamma=None, rms_eps=1e-6, rotate=False, rope_cos=None, rope_sin=None,
+                      rope_dim=64, out="bf16"):
+    """One chunk of the compressor with its recurrent state ring ("DeepSeek
+    V4.1 Flash", "Compressor state ownership").
+
+    ``state`` (float64 [n_blocks, cap, 2 D], updated in place) is the ring:
+    slot p % cap of request b's block ``state_table[b]`` holds the kv row of
+    position p followed by its gate score x_p @ w_gate + ape[p % r].  A token
+    that closes a group (p % r == r - 1) pools its r tokens as compress()
+    does, taking each predecessor from the chunk when it is a preceding row of
+    the same request and otherwise (a position before the chunk start) from
+    the ring.  Every read happens before any write; then the last
+    min(chunk length, cap) tokens of each request's chunk write their slots.
+    ``state_table[b] < 0`` disables request b (nothing published or written);
+    negative positions neither publish nor write.  Returns the published
+    groups as compress() does.
+    """
+    x, kv, w_gate, ape = as_f64(x), as_f64(kv), as_f64(w_gate), as_f64(ape)
+    positions = as_f64(positions).astype(np.int64)
+    row_req = as_f64(row_req).astype(np.int64)
+    table = as_f64(state_table).astype(np.int64)
+    r, D, cap = int(ratio), kv.shape[1], state.shape[1]
+    T = len(positions)
+
+    def live(t):
+        b, p = int(row_req[t]), int(positions[t])
+        return b >= 0 and p >= 0 and int(table[b]) >= 0
+
+    score = {t: x[t] @ w_gate + ape[int(positions[t]) % r] for t in range(T) if live(t)}
+    results = []
+    for t in range(T):
+        if not live(t):
+            continue
+        b, p = int(row_req[t]), int(positions[t])
+        if p % r != r - 1:
+            continue
+        blk = int(table[b])
+        logits, kvs = [], []
+        for j in range(r - 1, -1, -1):  # positions p - j, oldest first
+            s_ = t - j
+            if s_ >= 0 and int(row_req[s_]) == b and int(positions[s_]) == p - j:
+                logits.append(score[s_])
+                kvs.append(kv[s_])
+            else:
+                slot = state[blk, (p - j) % cap]
+                kvs.append(slot[:D].copy())
+                logits.append(slot[D:].copy())
+        results.append(_publish_group(b, p // r, r, np.stack(logits), np.stack(kvs), gamma,
+                                      rms_eps, rotate, rope_cos, rope_sin, rope_dim, out))
+    # writes: the last min(chunk length, cap) rows of each request's chunk
+    last_row = {}
+    for t in range(T):
+        if live(t):
+            last_row[int(row_req[t])] = t
+    for t in range(T):
+        if not live(t):
+            continue
+        b, p = int(row_req[t]), int(positions[t])
+        if t > last_row[b] - cap:
+            state[int(table[b]), p % cap, :D] = kv[t]
+            state[int(table[b]), p % cap, D:] = score[t]
     return results
 
 

@@ -257,6 +257,110 @@ def test_compress_rotate_uses_group_start_and_int8_path():
         assert np.max(np.abs(codes * s - want)) <= s / 2 + 1e-9
 
 
+def _stateful_run(x, kv, w, ape, r, reqs, splits, cap=4, **kw):
+    """Feed requests' token streams chunk by chunk (``splits``: per call, the
+    number of tokens of each request), carrying one ring per request."""
+    D = kv.shape[1]
+    n_req = len(reqs)
+    state = np.full((n_req + 2, cap, 2 * D), np.nan)  # blocks 1.. hold the requests
+    table = np.arange(1, n_req + 1)
+    done = [0] * n_req
+    out = []
+    for call in splits:
+        rows, pos, req = [], [], []
+        for b, n in enumerate(call):
+            for i in range(n):
+                rows.append(reqs[b][done[b] + i])
+                pos.append(done[b] + i)
+                req.append(b)
+            done[b] += n
+        if not rows:
+            continue
+        idx = np.array(rows)
+        out += O.compress_stateful(x[idx], kv[idx], w, ape, r, np.array(pos), np.array(req),
+                                   state, table, **kw)
+    return out, state, table
+
+
+@pytest.mark.parametrize("r,splits", [
+    (2, [[1, 1]] * 9),                         # one token per call (decode)
+    (2, [[3, 2], [1, 4], [5, 1], [2, 2]]),     # odd chunk starts: a pair closes across calls
+    (4, [[1, 1]] * 11),
+    (4, [[2, 3], [7, 1], [1, 6], [3, 2]]),     # chunks longer than the ring
+    (4, [[6, 0], [0, 5], [5, 6]]),             # idle requests in some calls
+])
+def test_stateful_compress_equals_one_shot(r, splits):
+    """Chunked calls with the state ring publish exactly the groups the
+    one-shot compressor publishes over each request's whole stream."""
+    rng = np.random.default_rng(40 + r)
+    lens = [sum(c[b] for c in splits) for b in range(2)]
+    n = sum(lens)
+    x, kv = _chunk(rng, n, D=64, Dx=32)
+    w = _bf16(rng.standard_normal((32, 64)) / 6)
+    ape = rng.standard_normal((r, 64))
+    reqs = [list(range(0, lens[0])), list(range(lens[0], n))]
+    got, _, _ = _stateful_run(x, kv, w, ape, r, reqs, splits)
+    want = []
+    for b in range(2):
+        idx = np.array(reqs[b])
+        for _, g, y in O.compress(x[idx], kv[idx], w, ape, r, np.arange(len(idx)),
+                                  np.zeros(len(idx), int)):
+            want.append((b, g, y))
+    assert sorted((b, g) for b, g, _ in got) == sorted((b, g) for b, g, _ in want)
+    ref = {(b, g): y for b, g, y in want}
+    for b, g, y in got:
+        assert np.array_equal(y, ref[(b, g)]), (b, g)
+
+
+def test_stateful_compress_int8_rotated_equals_one_shot():
+    rng = np.random.default_rng(47)
+    x, kv = _chunk(rng, 13, D=128, Dx=64)
+    w = _bf16(rng.standard_normal((64, 128)) / 8)
+    ape = rng.standard_normal((4, 128))
+    kw = dict(rotate=True, rope_cos=COS, rope_sin=SIN, out="int8")
+    got, _, _ = _stateful_run(x, kv, w, ape, 4, [list(range(13))], [[3], [1], [6], [3]], **kw)
+    want = O.compress(x, kv, w, ape, 4, np.arange(13), np.zeros(13, int), **kw)
+    assert [(g, c.tolist(), sc) for _, g, c, sc in got] == [(g, c.tolist(), sc) for _, g, c, sc in want]
+
+
+def test_state_ring_holds_the_last_tokens():
+    """After a call, slot p % cap of the request's block holds the kv row and
+    the gate score of the last min(chunk length, cap) positions; older slots
+    keep what they had."""
+    rng = np.random.default_rng(48)
+    x, kv = _chunk(rng, 12, D=16, Dx=8)
+    w = _bf16(rng.standard_normal((8, 16)))
+    ape = rng.standard_normal((2, 16))
+    cap = 4
+    state = np.full((3, cap, 32), -7.0)
+    table = np.array([2])
+    # call 1: positions 0..1 (two slots written); call 2: positions 2..8 (last four written)
+    O.compress_stateful(x[:2], kv[:2], w, ape, 2, np.arange(2), np.zeros(2, int), state, table)
+    assert np.all(state[2, 2:] == -7.0) and np.all(state[:2] == -7.0)
+    O.compress_stateful(x[2:9], kv[2:9], w, ape, 2, np.arange(2, 9), np.zeros(7, int), state,
+                        table)
+    xf, kvf, wf = O.as_f64(x), O.as_f64(kv), O.as_f64(w)
+    for p in range(5, 9):
+        slot = state[2, p % cap]
+        assert np.array_equal(slot[:16], kvf[p])
+        assert np.allclose(slot[16:], xf[p] @ wf + ape[p % 2], rtol=1e-12, atol=1e-12)
+
+
+def test_stateful_disabled_requests_and_negative_positions():
+    rng = np.random.default_rng(49)
+    x, kv = _chunk(rng, 6, D=16, Dx=8)
+    w = _bf16(rng.standard_normal((8, 16)))
+    ape = rng.standard_normal((2, 16))
+    state = np.zeros((2, 4, 32))
+    # request 0 disabled (-1), request 1 with a negative position row
+    req = np.array([0, 0, 1, 1, 1, 1])
+    pos = np.array([0, 1, -1, 1, 2, 3])
+    out = O.compress_stateful(x, kv, w, ape, 2, pos, req, state, np.array([-1, 1]))
+    assert [(b, g) for b, g, _ in out] == [(1, 0), (1, 1)]  # (1, 0) takes position 0 from the ring
+    assert np.all(state[0] == 0.0)
+    assert np.all(state[1, 0] == 0.0)  # the negative-position row wrote nothing
+
+
 def test_compress_rmsnorm_unit_gamma():
     rng = np.random.default_rng(13)
     x, kv = _chunk(rng, 4)
