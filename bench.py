@@ -126,12 +126,23 @@ def algorithmic_work(wl):
     # ending at a position p with p % r == r - 1
     r = s.ratio
     rr, rp = [int(x) for x in wl.row_req], [int(x) for x in wl.row_pos]
-    groups = sum(1 for i in range(r - 1, T)
-                 if rr[i] >= 0 and rp[i] % r == r - 1 and
-                 all(rr[i - j] == rr[i] and rp[i - j] == rp[i] - j for j in range(1, r)))
+    def in_chunk(i, j):  # row i - j is the same request at position p_i - j
+        return i - j >= 0 and rr[i - j] == rr[i] and rp[i - j] == rp[i] - j
+    closing = [i for i in range(T) if rr[i] >= 0 and rp[i] >= 0 and rp[i] % r == r - 1]
+    if s.state:
+        # with state rings every closing row publishes; predecessors before the
+        # chunk come from the ring and the last 4 rows of each request write it
+        groups = len(closing)
+        ring_reads = sum(1 for i in closing for j in range(1, r) if not in_chunk(i, j))
+        ring_writes = sum(1 for i in range(T) if rr[i] >= 0 and rp[i] >= 0 and
+                          not (i + 4 < T and rr[i + 4] == rr[i]))
+    else:
+        groups = sum(1 for i in closing if all(in_chunk(i, j) for j in range(1, r)))
+        ring_reads = ring_writes = 0
     dims = ((D, D * 2), (Di, Di + 4))          # (d, output bytes per group)
     w_bytes = sum(d * d * 2 + r * d * 4 for d, _ in dims)    # W_gate and ape
     out_bytes = sum(groups * ob for _, ob in dims)
+    ring_bytes = sum((ring_reads + ring_writes) * 2 * d * 4 for d, _ in dims)
     gate_flops = 2 * T * (D * D + Di * Di)
     return {
         "index_score": {"bytes": idx_bytes, "flops": idx_flops},
@@ -141,8 +152,8 @@ def algorithmic_work(wl):
         # long chunks: x and W_gate in, FP32 logits out; then logits and kv in, rows out
         "compress_gate": {"bytes": w_bytes + sum(T * d * (2 + 4) for d, _ in dims),
                           "flops": gate_flops},
-        "compress_pool": {"bytes": sum(T * d * (4 + 2) for d, _ in dims) + out_bytes,
-                          "flops": 0},
+        "compress_pool": {"bytes": sum(T * d * (4 + 2) for d, _ in dims) + out_bytes +
+                          ring_bytes, "flops": 0},
         # short chunks: W_gate, ape and the r rows of x and kv of every group in, rows out
         "compress_fused": {"bytes": w_bytes + sum(groups * r * d * 2 * 2 for d, _ in dims) +
                            out_bytes, "flops": 2 * groups * r * (D * D + Di * Di)},

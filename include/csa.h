@@ -85,8 +85,9 @@ typedef enum { CSA_MODE_AUTO = 0, CSA_MODE_DECODE = 1, CSA_MODE_PREFILL = 2 } cs
  * (INT8 idx_kv quantised on write: amax floored at 1e-4 scaled to 127, FP32
  * per-row scale).
  *
- * Group g of request b is positions g*r .. g*r+r-1.  It is written iff rows
- * t-r+1 .. t of this chunk are request b at exactly those positions.  Per
+ * Group g of request b is positions g*r .. g*r+r-1.  Without a state ring it
+ * is written iff rows t-r+1 .. t of this chunk are request b at exactly those
+ * positions.  Per
  * channel d:  logit[j,d] = (x_j . w_gate[:,d]) + ape[j,d];  w = softmax_j;
  * y[d] = sum_j w[j,d] kv_j[d];  y = bf16(y);  optionally
  * y = bf16(gamma * y / sqrt(mean(y^2) + rms_eps));  optionally rotate at g*r;
@@ -99,6 +100,22 @@ typedef enum { CSA_MODE_AUTO = 0, CSA_MODE_DECODE = 1, CSA_MODE_PREFILL = 2 } cs
  * idx_pool i8 [n_blocks, 128, d]; idx_scale_pool f32 [n_blocks, 128].
  * Supported: ratio in {1, 2, 4}; d in {128, 512}; dx a multiple of 64 <= 1024.
  * Workspace: n_rows * d * 4 bytes (gate logits), rounded up.
+ *
+ * Recurrent state ring ("DeepSeek V4.1 Flash", "Compressor state ownership"),
+ * optional (state_cache == NULL: none).  state_cache f32
+ * [n_state_blocks, state_capacity, 2 * d] is in/out: slot p % state_capacity
+ * of block state_block_table[b] holds the kv row of position p (as FP32)
+ * followed by its gate score x_p . w_gate + ape[p % ratio].  A row closing a
+ * group takes each predecessor from this chunk when it is a preceding row of
+ * the same request, else (a position before the chunk start) from the ring.
+ * All ring reads complete before any ring write; then the last
+ * min(chunk length, state_capacity) rows of each request's chunk (its rows
+ * must be consecutive) write their slots.  state_block_table i32 [n_req]:
+ * -1 disables the request (nothing published or written); a block >=
+ * n_state_blocks sets CSA_DEV_BAD_BLOCK and skips the request.  Rows with a
+ * negative position neither publish nor write.  Requires state_capacity >=
+ * ratio.  A caller built against a header without these four fields passes a
+ * smaller struct_size and gets no ring.
  * ---------------------------------------------------------------------- */
 typedef struct {
   uint32_t struct_size;
@@ -129,6 +146,10 @@ typedef struct {
   uint32_t *status_dev;
   void *workspace;
   size_t workspace_bytes;
+  float *state_cache;                /* see "Recurrent state ring" above, or NULL */
+  const int32_t *state_block_table;  /* [n_req] */
+  int32_t n_state_blocks;
+  int32_t state_capacity;
 } csa_compress_args;
 
 CSA_API csa_status_t csa_compress(csa_compress_args *args, csa_stream_t stream);

@@ -20,14 +20,28 @@ def clone_pools(t):
 
 def compress_step(t, spec, pools=None):
     """Run both compressors over the chunk and publish into (cloned) pools.
+    With state rings (``spec.state``) the compressors read and update copies
+    of them, returned in pools["state_main"] / pools["state_idx"] (float64).
 
     Returns (pools, main_results, idx_results)."""
     pools = clone_pools(t) if pools is None else pools
-    main = O.compress(t["kv_raw"], t["kv_raw"], t["w_gate"], t["ape"], spec.ratio,
-                      t["row_pos"], t["row_req"], out="bf16")
-    idx = O.compress(t["idx_raw"], t["idx_raw"], t["w_gate_i"], t["ape_i"], spec.ratio,
-                     t["row_pos"], t["row_req"], rotate=True, rope_cos=t["rope_cos"],
-                     rope_sin=t["rope_sin"], rope_dim=spec.rope_dim, out="int8")
+    idx_kw = dict(rotate=True, rope_cos=t["rope_cos"], rope_sin=t["rope_sin"],
+                  rope_dim=spec.rope_dim, out="int8")
+    if spec.state:
+        pools["state_main"] = O.as_f64(t["state_main"]).copy()
+        pools["state_idx"] = O.as_f64(t["state_idx"]).copy()
+        table = t["state_table"].numpy()
+        main = O.compress_stateful(t["kv_raw"], t["kv_raw"], t["w_gate"], t["ape"], spec.ratio,
+                                   t["row_pos"], t["row_req"], pools["state_main"], table,
+                                   out="bf16")
+        idx = O.compress_stateful(t["idx_raw"], t["idx_raw"], t["w_gate_i"], t["ape_i"],
+                                  spec.ratio, t["row_pos"], t["row_req"], pools["state_idx"],
+                                  table, **idx_kw)
+    else:
+        main = O.compress(t["kv_raw"], t["kv_raw"], t["w_gate"], t["ape"], spec.ratio,
+                          t["row_pos"], t["row_req"], out="bf16")
+        idx = O.compress(t["idx_raw"], t["idx_raw"], t["w_gate_i"], t["ape_i"], spec.ratio,
+                         t["row_pos"], t["row_req"], **idx_kw)
     table = t["cmp_table"].numpy()
     for b, g, vals in main:
         pg = int(table[b, g // O.BLOCK])

@@ -44,7 +44,9 @@ class CompressArgs(ctypes.Structure):
         ("block_table", c_void_p), ("n_req", c_int32), ("max_blocks", c_int32),
         ("n_blocks", c_int32), ("cmp_pool", c_void_p), ("idx_pool", c_void_p),
         ("idx_scale_pool", c_void_p), ("status_dev", c_void_p), ("workspace", c_void_p),
-        ("workspace_bytes", c_size_t),
+        ("workspace_bytes", c_size_t), ("state_cache", c_void_p),
+        ("state_block_table", c_void_p), ("n_state_blocks", c_int32),
+        ("state_capacity", c_int32),
     ]
 
 
@@ -231,7 +233,8 @@ def _fill_common_rope(args, rope_cos, rope_sin):
 
 def _compress_struct(*, x, kv, w_gate, ape, ratio, positions, row_req, block_table, out="bf16",
                      cmp_pool=None, idx_pool=None, idx_scale_pool=None, gamma=None, rms_eps=1e-6,
-                     rotate=False, rope_cos=None, rope_sin=None, status=None):
+                     rotate=False, rope_cos=None, rope_sin=None, status=None, state_cache=None,
+                     state_block_table=None):
     a = CompressArgs()
     a.struct_size = ctypes.sizeof(CompressArgs)
     a.n_rows = int(x.shape[0])
@@ -259,6 +262,10 @@ def _compress_struct(*, x, kv, w_gate, ape, ratio, positions, row_req, block_tab
         a.idx_scale_pool = _p(idx_scale_pool, torch.float32, "idx_scale_pool")
         a.n_blocks = int(idx_pool.shape[0])
     a.status_dev = _p(status, torch.int32, "status")
+    if state_cache is not None:
+        a.state_cache = _p(state_cache, torch.float32, "state_cache")
+        a.state_block_table = _p(state_block_table, torch.int32, "state_block_table")
+        a.n_state_blocks, a.state_capacity = int(state_cache.shape[0]), int(state_cache.shape[1])
     return a
 
 
@@ -267,7 +274,8 @@ def csa_compress(*, workspace=None, stream=None, prepare=False, **kw):
     (``include/csa.h``: csa_compress).  Keywords: x, kv, w_gate, ape, ratio,
     positions, row_req, block_table, out ("bf16" or "int8"), cmp_pool or
     idx_pool + idx_scale_pool, gamma, rms_eps, rotate, rope_cos, rope_sin,
-    status."""
+    status, and for the recurrent state ring state_cache (FP32 [blocks,
+    capacity, 2 d]) with state_block_table (INT32 [n_req])."""
     a = _compress_struct(**kw)
     return _run("csa_compress", a, workspace, stream, kw["x"].device, prepare)
 

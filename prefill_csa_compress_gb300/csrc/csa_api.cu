@@ -1,6 +1,8 @@
 // extern "C" entry points: host-side argument checks, workspace layout and
 // kernel dispatch.  No entry point synchronises or allocates device memory.
 #include <atomic>
+#include <cstddef>
+#include <cstring>
 #include <mutex>
 #include <vector>
 
@@ -138,7 +140,7 @@ CSA_API uint64_t csa_launch_count(void) { return g_launches.load(); }
 // reports its workspace size (already stored in a->workspace_bytes).
 static csa_status_t check_compress(csa_compress_args *a, bool *size_query) {
   *size_query = false;
-  if (!a || a->struct_size < sizeof(csa_compress_args)) return CSA_ERR_INVALID_ARG;
+  if (!a || a->struct_size < offsetof(csa_compress_args, state_cache)) return CSA_ERR_INVALID_ARG;
   if (a->n_rows < 0 || a->n_req < 0) return CSA_ERR_INVALID_ARG;
   if (a->ratio != 1 && a->ratio != 2 && a->ratio != 4) return CSA_ERR_UNSUPPORTED;
   if (a->d != 128 && a->d != 512) return CSA_ERR_UNSUPPORTED;
@@ -161,26 +163,48 @@ static csa_status_t check_compress(csa_compress_args *a, bool *size_query) {
     return CSA_ERR_INVALID_ARG;
   if (a->rotate && (!a->rope_cos || !a->rope_sin || a->rope_cap <= 0)) return CSA_ERR_INVALID_ARG;
   if (!aligned16(a->x) || !aligned16(a->kv) || !aligned16(a->w_gate)) return CSA_ERR_INVALID_ARG;
+  if (a->state_cache &&
+      (!a->state_block_table || a->n_state_blocks <= 0 || a->state_capacity < a->ratio ||
+       a->state_capacity > 64))
+    return CSA_ERR_INVALID_ARG;
   return CSA_OK;
 }
 
+// The arguments as this library's struct: a caller built against the header
+// without the state-ring fields (a smaller struct_size) gets no ring.
+static csa_compress_args full_args(const csa_compress_args *a) {
+  csa_compress_args f;
+  memset(&f, 0, sizeof(f));
+  memcpy(&f, a, a->struct_size < sizeof(f) ? a->struct_size : sizeof(f));
+  f.struct_size = sizeof(f);
+  return f;
+}
+
 CSA_API csa_status_t csa_compress(csa_compress_args *a, csa_stream_t stream) {
+  if (!a || a->struct_size < offsetof(csa_compress_args, state_cache)) return CSA_ERR_INVALID_ARG;
+  csa_compress_args f = full_args(a);
   bool query = false;
-  const csa_status_t st = check_compress(a, &query);
-  if (st != CSA_OK || query || a->n_rows == 0) return st;
+  const csa_status_t st = check_compress(&f, &query);
+  if (query) a->workspace_bytes = f.workspace_bytes;
+  if (st != CSA_OK || query || f.n_rows == 0) return st;
   return from_cuda(
-      launch_compress(*a, static_cast<float *>(a->workspace), static_cast<cudaStream_t>(stream)));
+      launch_compress(f, static_cast<float *>(f.workspace), static_cast<cudaStream_t>(stream)));
 }
 
 CSA_API csa_status_t csa_compress_pair(csa_compress_args *first, csa_compress_args *second,
                                        csa_stream_t stream) {
+  for (const csa_compress_args *x : {first, second})
+    if (!x || x->struct_size < offsetof(csa_compress_args, state_cache)) return CSA_ERR_INVALID_ARG;
+  csa_compress_args f1 = full_args(first), f2 = full_args(second);
   bool q1 = false, q2 = false;
-  csa_status_t st = check_compress(first, &q1);
+  csa_status_t st = check_compress(&f1, &q1);
+  if (q1) first->workspace_bytes = f1.workspace_bytes;
   if (st != CSA_OK) return st;
-  st = check_compress(second, &q2);
+  st = check_compress(&f2, &q2);
+  if (q2) second->workspace_bytes = f2.workspace_bytes;
   if (st != CSA_OK || q1 || q2) return st;
-  return from_cuda(launch_compress_pair(*first, static_cast<float *>(first->workspace), *second,
-                                        static_cast<float *>(second->workspace),
+  return from_cuda(launch_compress_pair(f1, static_cast<float *>(f1.workspace), f2,
+                                        static_cast<float *>(f2.workspace),
                                         static_cast<cudaStream_t>(stream)));
 }
 

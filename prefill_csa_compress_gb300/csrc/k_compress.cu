@@ -197,6 +197,9 @@ __device__ __forceinline__ float block_max(float v, float *red) {
   return s;
 }
 
+// One CTA per group-closing row (d threads, one channel each).  With a state
+// ring, predecessors before the chunk start come from the ring: their kv row
+// and their gate score (ape included) as the ring stores them.
 __global__ void compress_pool_kernel(csa_compress_args a, const float *__restrict__ logits) {
   tc::griddep_wait();
   tc::griddep_launch_dependents();
@@ -205,12 +208,30 @@ __global__ void compress_pool_kernel(csa_compress_args a, const float *__restric
   const int t = blockIdx.x;
   const int r = a.ratio, D = a.d;
   const int b = a.row_req[t], p = a.positions[t];
-  if (b < 0 || p < 0 || (p % r) != r - 1 || t < r - 1) return;
-  for (int j = 1; j < r; ++j)
-    if (a.row_req[t - j] != b || a.positions[t - j] != p - j) return;
+  if (b < 0 || p < 0 || (p % r) != r - 1) return;
   if (b >= a.n_req) {
     if (threadIdx.x == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
     return;
+  }
+  const float *ring = nullptr;  // this request's ring block
+  if (a.state_cache) {
+    const int blk = a.state_block_table[b];
+    if (blk < 0) return;  // the request's compressor is disabled
+    if (blk >= a.n_state_blocks) {
+      if (threadIdx.x == 0) flag(a.status_dev, CSA_DEV_BAD_BLOCK);
+      return;
+    }
+    ring = a.state_cache + (long long)blk * a.state_capacity * 2 * D;
+  }
+  // token j of the group (position p - r + 1 + j): row t - r + 1 + j of this
+  // chunk, or (a position before the chunk start) the ring
+  uint32_t in_chunk = 0;
+  for (int j = 0; j < r; ++j) {
+    const int s = t - r + 1 + j;
+    if (s >= 0 && a.row_req[s] == b && a.positions[s] == p - r + 1 + j)
+      in_chunk |= 1u << j;
+    else if (!ring)
+      return;  // the group is not complete in this chunk
   }
   const int g = p / r;
   const int page = g / kBlock;
@@ -226,17 +247,24 @@ __global__ void compress_pool_kernel(csa_compress_args a, const float *__restric
   const uint16_t *kv = static_cast<const uint16_t *>(a.kv);
 
   // pooling softmax over the r tokens of the group, per channel
-  float lg[4];
+  float lg[4], kvv[4];
   float mx = -INFINITY;
   for (int j = 0; j < r; ++j) {
-    lg[j] = logits[(long long)(t0 + j) * D + d] + a.ape[j * D + d];
+    if (in_chunk & (1u << j)) {
+      lg[j] = logits[(long long)(t0 + j) * D + d] + a.ape[j * D + d];
+      kvv[j] = bf16_bits_to_float(kv[(long long)(t0 + j) * D + d]);
+    } else {
+      const float *slot = ring + (long long)((p - r + 1 + j) % a.state_capacity) * 2 * D;
+      kvv[j] = slot[d];
+      lg[j] = slot[D + d];
+    }
     mx = fmaxf(mx, lg[j]);
   }
   float s = 0.f, y = 0.f;
   for (int j = 0; j < r; ++j) {
     float e = expf(lg[j] - mx);
     s += e;
-    y = fmaf(e, bf16_bits_to_float(kv[(long long)(t0 + j) * D + d]), y);
+    y = fmaf(e, kvv[j], y);
   }
   y = round_bf16(y / s);
 
@@ -274,6 +302,64 @@ __global__ void compress_pool_kernel(csa_compress_args a, const float *__restric
     q = fminf(fmaxf(q, -127.f), 127.f);
     a.idx_pool[dst_row * D + d] = static_cast<int8_t>(q);
     if (d == 0) a.idx_scale_pool[dst_row] = scale;
+  }
+}
+
+// Ring writes of the state: row t among the last state_capacity rows of its
+// request's chunk stores its kv row (FP32) and its gate score (ape included)
+// in slot p % state_capacity.  Runs after the pooling kernel, so every ring
+// read of the call precedes every write.  One CTA per row, d threads.
+__global__ void compress_state_kernel(csa_compress_args a, const float *__restrict__ logits) {
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
+  const int t = blockIdx.x, d = threadIdx.x;
+  const int b = a.row_req[t], p = a.positions[t];
+  if (b < 0 || b >= a.n_req || p < 0) return;
+  const int blk = a.state_block_table[b];
+  if (blk < 0 || blk >= a.n_state_blocks) return;  // flagged by the pooling kernel
+  const int cap = a.state_capacity, D = a.d;
+  if (t + cap < a.n_rows && a.row_req[t + cap] == b) return;  // not among the last cap rows
+  float *slot = a.state_cache + ((long long)blk * cap + p % cap) * 2 * D;
+  slot[d] = bf16_bits_to_float(static_cast<const uint16_t *>(a.kv)[(long long)t * D + d]);
+  slot[D + d] = logits[(long long)t * D + d] + a.ape[(p % a.ratio) * D + d];
+}
+
+// Gate logits of a short chunk, row by row (the tensor-core GEMM's 128-row
+// tiles would be mostly empty): one CTA per (16-column slice, row) stages its
+// W_gate slice and the row's x, sums the K range split over its threads and
+// writes logits[t, c] = x_t . w_gate[:, c] (FP32, ape not added).
+constexpr int GR_THREADS = 256, GR_COLS = 16;
+__global__ void __launch_bounds__(GR_THREADS) gate_rows_kernel(csa_compress_args a, float *logits) {
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
+  extern __shared__ __align__(16) uint8_t gr_smem[];
+  constexpr int PARTS = GR_THREADS / GR_COLS;
+  const int dx = a.dx, D = a.d, tid = threadIdx.x;
+  const int c0 = blockIdx.x * GR_COLS, t = blockIdx.y;
+  const int b = a.row_req[t], p = a.positions[t];
+  if (b < 0 || b >= a.n_req || p < 0) return;  // no group or ring write reads this row
+  uint16_t *Ws = reinterpret_cast<uint16_t *>(gr_smem);   // [dx][GR_COLS]
+  uint16_t *Xs = Ws + (size_t)dx * GR_COLS;               // [dx]
+  float *part = reinterpret_cast<float *>(Xs + dx);       // [PARTS][GR_COLS]
+  const uint16_t *wg = static_cast<const uint16_t *>(a.w_gate);
+  const uint16_t *xg = static_cast<const uint16_t *>(a.x) + (long long)t * dx;
+  for (int e = tid; e < dx * (GR_COLS / 8); e += GR_THREADS) {
+    const int k = e / (GR_COLS / 8), q = e % (GR_COLS / 8);
+    tc::cp_async16(Ws + k * GR_COLS + q * 8, wg + (long long)k * D + c0 + q * 8);
+  }
+  for (int e = tid; e < dx / 8; e += GR_THREADS) tc::cp_async16(Xs + e * 8, xg + e * 8);
+  tc::cp_async_wait_all();
+  __syncthreads();
+  const int c = tid % GR_COLS, pr = tid / GR_COLS;
+  float acc = 0.f;
+  for (int k = pr * (dx / PARTS); k < (pr + 1) * (dx / PARTS); ++k)
+    acc = fmaf(bf16_bits_to_float(Xs[k]), bf16_bits_to_float(Ws[k * GR_COLS + c]), acc);
+  part[pr * GR_COLS + c] = acc;
+  __syncthreads();
+  if (tid < GR_COLS) {
+    float l = 0.f;
+    for (int q = 0; q < PARTS; ++q) l += part[q * GR_COLS + tid];
+    logits[(long long)t * D + c0 + tid] = l;
   }
 }
 
@@ -471,7 +557,7 @@ size_t fused_smem(const csa_compress_args &a) {
 
 // the short-chunk column tile for this call, or 0 when it takes the long path
 int fused_cols(const csa_compress_args &a) {
-  if (a.n_rows > 256) return 0;
+  if (a.n_rows > 256 || a.state_cache) return 0;
   if (a.d == 128 && (size_t)a.dx * 128 * 2 <= FC_MAX_W_BYTES) return 128;
   if (a.d == 512 && a.out_mode == CSA_OUT_BF16 && !a.gamma && (size_t)a.dx * 16 * 2 <= FC_MAX_W_BYTES)
     return 16;
@@ -533,14 +619,29 @@ cudaError_t launch_compress(const csa_compress_args &a, float *logits, cudaStrea
   if (cols == 16) return launch_fused<16>(a, s);
   if (a.dx % GG_K != 0 || a.d % GG_N != 0 || (reinterpret_cast<uintptr_t>(logits) & 15u) != 0)
     return cudaErrorInvalidValue;
+  cudaError_t e;
   launch_begin(CSA_K_COMPRESS_GATE, s);
-  cudaError_t e = launch_gate_gemm_tc(a, logits, s);
+  if (a.n_rows <= 256) {
+    // a short chunk with a state ring: gate logits row by row
+    const size_t smem = (size_t)a.dx * GR_COLS * 2 + (size_t)a.dx * 2 +
+                        (GR_THREADS / GR_COLS) * GR_COLS * 4;
+    e = launch_kernel(gate_rows_kernel, dim3(a.d / GR_COLS, a.n_rows), dim3(GR_THREADS), smem, s,
+                      0, false, a, logits);
+  } else {
+    e = launch_gate_gemm_tc(a, logits, s);
+  }
   launch_end(CSA_K_COMPRESS_GATE, s);
   if (e != cudaSuccess) return e;
   launch_begin(CSA_K_COMPRESS_POOL, s);
   e = launch_kernel(compress_pool_kernel, dim3(a.n_rows), dim3(a.d), 0, s, 0, false, a,
                     static_cast<const float *>(logits));
   launch_end(CSA_K_COMPRESS_POOL, s);
+  if (e == cudaSuccess && a.state_cache) {
+    launch_begin(CSA_K_COMPRESS_POOL, s);
+    e = launch_kernel(compress_state_kernel, dim3(a.n_rows), dim3(a.d), 0, s, 0, false, a,
+                      static_cast<const float *>(logits));
+    launch_end(CSA_K_COMPRESS_POOL, s);
+  }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -24,7 +24,9 @@ class CsaStep:
     ``t`` maps names to device tensors: row_req, row_pos, kv_len, n_cmp,
     kv_pool, kv_table, cmp_pool, idx_pool, idx_scale, cmp_table, q, q_idx,
     idx_w, sink, kv_raw, idx_raw, w_gate, ape, w_gate_i, ape_i, rope_cos,
-    rope_sin.  ``ratio``, ``topk`` and ``prefill`` describe the step.
+    rope_sin, and optionally the compressors' state rings state_main,
+    state_idx with state_table.  ``ratio``, ``topk`` and ``prefill``
+    describe the step.
     """
 
     def __init__(self, t: dict, ratio: int, topk: int, prefill: bool = False,
@@ -59,6 +61,9 @@ class CsaStep:
                     block_table=t["cmp_table"], out="int8", idx_pool=t["idx_pool"],
                     idx_scale_pool=t["idx_scale"], rotate=True, rope_cos=t["rope_cos"],
                     rope_sin=t["rope_sin"], status=self.status)
+        if "state_table" in t:  # the compressors' recurrent state rings
+            main.update(state_cache=t["state_main"], state_block_table=t["state_table"])
+            keys.update(state_cache=t["state_idx"], state_block_table=t["state_table"])
         return main, keys
 
     def compress(self, stream=None):

@@ -109,6 +109,18 @@ def test_workspace_queries_and_validation(L):
     a2 = _compress_args(b, n_rows=1, workspace=ctypes.addressof(dummy), workspace_bytes=256)
     assert L.csa_compress_pair(ctypes.byref(a), ctypes.byref(a2), None) == b.CSA_ERR_INVALID_ARG
     assert L.csa_compress_pair(None, ctypes.byref(a2), None) == b.CSA_ERR_INVALID_ARG
+    # a caller built without the state-ring fields (smaller struct_size) is accepted
+    old = _compress_args(b)
+    old.struct_size = b.CompressArgs.state_cache.offset
+    assert L.csa_compress(ctypes.byref(old), None) == b.CSA_OK
+    assert old.workspace_bytes == 8192 * 512 * 4
+    old.struct_size = b.CompressArgs.state_cache.offset - 8
+    assert L.csa_compress(ctypes.byref(old), None) == b.CSA_ERR_INVALID_ARG
+    # a state ring needs its table and at least `ratio` slots
+    st = ctypes.create_string_buffer(4096)
+    ring = _compress_args(b, n_rows=1, workspace=ctypes.addressof(dummy), workspace_bytes=256,
+                          state_cache=ctypes.addressof(st), n_state_blocks=1, state_capacity=4)
+    assert L.csa_compress(ctypes.byref(ring), None) == b.CSA_ERR_INVALID_ARG  # no tensors, no table
 
     ia = b.IndexArgs()
     ia.struct_size = ctypes.sizeof(ia)

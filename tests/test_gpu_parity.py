@@ -59,6 +59,7 @@ def _rope_q(t, row, key="q_idx"):
     ("chunked_prefill", dict(ctx=[203], chunk=[203], seed=34)),
     ("chunked_prefill", dict(ctx=[130, 61], chunk=[130, 61], ratio=1, seed=35, pad_rows=2)),
     ("serving_decode", {}),
+    ("stateful_decode", {}),                                            # state rings
     ("chunked_prefill", {}),                                            # full 8192-token chunk
 ])
 def test_compress_parity(name, over):
@@ -85,6 +86,15 @@ def test_compress_parity(name, over):
     check_bf16(np.stack(g_rows), np.stack(r_rows), "cmp_kv")
     # INT8 codes may differ (by one) only at rounding boundaries: rare
     assert n_diff <= INT8_FLIP_RATE * len(idx) * spec.idx_dim + 2, n_diff
+    if spec.state:
+        # the rings: kv rows exactly, gate scores to FP32 accuracy
+        for name in ("state_main", "state_idx"):
+            got_s = t[name].cpu().double().numpy()
+            ref_s = pools[name]
+            d = got_s.shape[2] // 2
+            assert np.array_equal(got_s[..., :d], ref_s[..., :d]), name
+            err = np.abs(got_s[..., d:] - ref_s[..., d:])
+            assert np.all(err <= 1e-4 * np.maximum(1.0, np.abs(ref_s[..., d:]))), (name, err.max())
     # entries not written by this step are untouched
     written = {(b, g) for b, g, _ in main}
     ref_pool = wl.cmp_pool
@@ -362,6 +372,82 @@ def test_attention_prefill_full_size_sampled():
     _attn_case(spec, 10, True, rows=[0, 1, 127, 128, 2047, 4000, 8191])
 
 
+@pytest.mark.parametrize("ratio,d,out,splits", [
+    (2, 512, "bf16", [[1, 1]] * 6 + [[3, 2], [1, 4], [5, 1]]),   # decode steps, then chunks
+    (4, 512, "bf16", [[1, 1]] * 7 + [[2, 3], [7, 1], [1, 6]]),   # chunks longer than the ring
+    (4, 128, "int8", [[3, 0], [2, 5], [0, 2], [6, 6]]),          # idle requests; rotated INT8
+])
+def test_compress_state_ring(ratio, d, out, splits):
+    """csa_compress with the recurrent state ring over a chunked stream of two
+    requests: the published groups equal the oracle's one-shot compression of
+    each request's whole stream, and the ring equals the oracle's ring."""
+    rng = np.random.default_rng(ratio * 100 + d)
+    dx, cap = 256, 4
+    lens = [sum(c[b] for c in splits) for b in range(2)]
+    n = sum(lens)
+    x = torch.from_numpy(rng.standard_normal((n, dx)).astype(np.float32)).bfloat16()
+    kv = torch.from_numpy(rng.standard_normal((n, d)).astype(np.float32)).bfloat16()
+    w = torch.from_numpy((rng.standard_normal((dx, d)) / np.sqrt(dx)).astype(np.float32)).bfloat16()
+    ape = torch.from_numpy(rng.standard_normal((ratio, d)).astype(np.float32))
+    from workloads import rope_tables
+    cos, sin = rope_tables(4096)
+    table = torch.tensor([[3, 1], [0, 2]], dtype=torch.int32)  # 2 requests x 2 pages
+    cmp_pool = torch.zeros((4, BLOCK, d), dtype=torch.bfloat16, device=DEV)
+    idx_pool = torch.zeros((4, BLOCK, d), dtype=torch.int8, device=DEV)
+    idx_scale = torch.zeros((4, BLOCK), dtype=torch.float32, device=DEV)
+    state = torch.full((3, cap, 2 * d), 12345.0, dtype=torch.float32, device=DEV)
+    state_table = torch.tensor([2, 0], dtype=torch.int32)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ref_state = np.full((3, cap, 2 * d), 12345.0)
+    reqs = [np.arange(0, lens[0]), np.arange(lens[0], n)]
+    done = [0, 0]
+    for call in splits:
+        rows, pos, req = [], [], []
+        for b, m in enumerate(call):
+            rows += list(reqs[b][done[b]:done[b] + m])
+            pos += list(range(done[b], done[b] + m))
+            req += [b] * m
+            done[b] += m
+        idx = np.array(rows)
+        kw = dict(rotate=out == "int8", rope_cos=cos, rope_sin=sin, out=out)
+        O.compress_stateful(x[idx], kv[idx], w, ape, ratio, np.array(pos), np.array(req),
+                            ref_state, state_table.numpy(), **kw)
+        csa.csa_compress(x=x[idx].to(DEV), kv=kv[idx].to(DEV), w_gate=w.to(DEV), ape=ape.to(DEV),
+                         ratio=ratio, positions=torch.tensor(pos, dtype=torch.int32, device=DEV),
+                         row_req=torch.tensor(req, dtype=torch.int32, device=DEV),
+                         block_table=table.to(DEV), out=out, cmp_pool=cmp_pool, idx_pool=idx_pool,
+                         idx_scale_pool=idx_scale, rotate=out == "int8", rope_cos=cos.to(DEV),
+                         rope_sin=sin.to(DEV), status=status, state_cache=state,
+                         state_block_table=state_table.to(DEV))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got_rows, ref_rows, n_diff, n_groups = [], [], 0, 0
+    for b in range(2):
+        i = reqs[b]
+        ref = O.compress(x[i], kv[i], w, ape, ratio, np.arange(len(i)), np.zeros(len(i), int),
+                         rotate=out == "int8", rope_cos=cos, rope_sin=sin, out=out)
+        for item in ref:
+            g = item[1]
+            pg, row = int(table[b, g // BLOCK]), g % BLOCK
+            n_groups += 1
+            if out == "bf16":
+                got_rows.append(cmp_pool[pg, row].cpu().double().numpy())
+                ref_rows.append(item[2])
+            else:
+                n_diff += check_int8(idx_pool[pg, row].cpu().numpy(), idx_scale[pg, row].item(),
+                                     item[2], np.float32(item[3]))
+    assert n_groups == sum(l // ratio for l in lens)
+    if out == "bf16":
+        check_bf16(np.stack(got_rows), np.stack(ref_rows), "compressed rows")
+    else:
+        assert n_diff <= INT8_FLIP_RATE * n_groups * d + 2, n_diff
+    # the ring: kv rows exactly (BF16 -> FP32), gate scores to FP32 accuracy
+    got_state = state.cpu().double().numpy()
+    assert np.array_equal(got_state[..., :d], ref_state[..., :d])
+    err = np.abs(got_state[..., d:] - ref_state[..., d:])
+    assert np.all(err <= 1e-4 * np.maximum(1.0, np.abs(ref_state[..., d:]))), err.max()
+
+
 @pytest.mark.parametrize("name,over", [
     ("serving_decode", {}),
     ("chunked_prefill", dict(ctx=[203], chunk=[203], seed=36)),
@@ -392,7 +478,7 @@ def test_compress_pair_equals_two_calls(name, over):
 # ------------------------------------------------------------------ whole step
 
 
-@pytest.mark.parametrize("name", ["tiny_decode", "serving_decode"])
+@pytest.mark.parametrize("name", ["tiny_decode", "serving_decode", "stateful_decode"])
 def test_decode_step_chain(name):
     """compress -> index -> attention on the GPU, against the oracle's own chain."""
     spec = spec_for(name)

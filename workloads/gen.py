@@ -41,6 +41,7 @@ class WorkloadSpec:
     kv_pages: str = "all"  # "all" or "window" (only pages the window reads; others -1)
     cmp_init: str = "random"  # "random" or "zeros" (filled by the compressor)
     pad_rows: int = 0  # trailing padding rows (row_req = -1)
+    state: bool = False  # compressors keep a recurrent state ring (capacity 4)
     extra: dict = field(default_factory=dict)
 
     @property
@@ -68,6 +69,12 @@ CONFIGS = {
     # compressor fills cmp_kv and idx_kv in the same step.
     "chunked_prefill": WorkloadSpec("chunked_prefill", [8192], [8192], ratio=4, topk=512, seed=3,
                                     mode="prefill", cmp_init="zeros"),
+    # serving_decode's requests at ratio 4 with the compressors' recurrent state
+    # rings: each request's group closes on this step's second row and takes
+    # its first two tokens from the ring.
+    "stateful_decode": WorkloadSpec("stateful_decode", [8192, 6000, 4096, 2048], [2, 2, 2, 2],
+                                    ratio=4, topk=512, seed=5, kv_pool_pages=256,
+                                    cmp_pool_pages=256, state=True),
     # 4 requests x 2 rows at 1,048,576 positions, ratio 4, top-k 2048.
     "million_decode": WorkloadSpec("million_decode", [1048576] * 4, [2] * 4, ratio=4, topk=2048,
                                    seed=4, kv_pages="window"),
@@ -223,6 +230,16 @@ def make_workload(spec: WorkloadSpec) -> Workload:
         rope_cos=rope_cos,
         rope_sin=rope_sin,
     )
+    if spec.state:
+        # one ring block per request (plus a spare) in a shuffled order; the
+        # slots hold earlier tokens' kv rows (BF16 values) and gate scores
+        cap = 4
+        t["state_table"] = torch.from_numpy(rng.permutation(B + 1)[:B].astype(np.int32))
+        for name, d in (("state_main", Dm), ("state_idx", Di)):
+            kv_part = _normal_bf16(rng, (B + 1, cap, d)).float()
+            score_part = torch.from_numpy(
+                (rng.standard_normal((B + 1, cap, d)) * 1.4).astype(np.float32))
+            t[name] = torch.cat([kv_part, score_part], dim=2).contiguous()
     return Workload(spec=spec, t=t)
 
 
