@@ -170,6 +170,25 @@ def test_compress_equal_logits_give_the_mean():
         assert np.all(np.abs(y - mean) <= 2.0 ** -8 * np.abs(mean) * (1 + 1e-12))
 
 
+def test_compress_ratio128_groups():
+    """HCA's ratio 128 ("Hyper-Parallel ... DeepSeek V4 CP", "ratio=128":
+    non-overlapping compression): equal logits pool each 128-token group to
+    its mean, only complete groups publish, and a one-hot APE row picks that
+    token of every group."""
+    rng = np.random.default_rng(6)
+    x, kv = _chunk(rng, 300, D=32, Dx=16)
+    w = torch.zeros((16, 32), dtype=torch.bfloat16)
+    res = O.compress(x, kv, w, np.zeros((128, 32)), 128, np.arange(300), np.zeros(300, int))
+    assert [g for _, g, _ in res] == [0, 1]  # tokens 256..299 do not close a group
+    for _, g, y in res:
+        mean = kv[128 * g:128 * g + 128].double().numpy().mean(axis=0)
+        assert np.all(np.abs(y - mean) <= 2.0 ** -8 * np.abs(mean) * (1 + 1e-12) + 1e-12)
+    ape = np.zeros((128, 32))
+    ape[77] = 80.0  # token 77 of each group dominates every channel's softmax
+    for _, g, y in O.compress(x, kv, w, ape, 128, np.arange(300), np.zeros(300, int)):
+        assert np.array_equal(y, kv[128 * g + 77].double().numpy())
+
+
 def test_compress_one_hot_ape_selects_a_row():
     rng = np.random.default_rng(6)
     x, kv = _chunk(rng, 4)
