@@ -139,11 +139,12 @@ def algorithmic_work(wl):
     else:
         groups = sum(1 for i in closing if all(in_chunk(i, j) for j in range(1, r)))
         ring_reads = ring_writes = 0
-    dims = ((D, D * 2), (Di, Di + 4))          # (d, output bytes per group)
+    # (d, output bytes per group); HCA (dense) runs only the main compressor
+    dims = ((D, D * 2),) if s.dense else ((D, D * 2), (Di, Di + 4))
     w_bytes = sum(d * d * 2 + r * d * 4 for d, _ in dims)    # W_gate and ape
     out_bytes = sum(groups * ob for _, ob in dims)
     ring_bytes = sum((ring_reads + ring_writes) * 2 * d * 4 for d, _ in dims)
-    gate_flops = 2 * T * (D * D + Di * Di)
+    gate_flops = sum(2 * T * d * d for d, _ in dims)
     return {
         "index_score": {"bytes": idx_bytes, "flops": idx_flops},
         "index_topk": {"bytes": topk_bytes, "flops": 0},
@@ -156,7 +157,7 @@ def algorithmic_work(wl):
                           ring_bytes, "flops": 0},
         # short chunks: W_gate, ape and the r rows of x and kv of every group in, rows out
         "compress_fused": {"bytes": w_bytes + sum(groups * r * d * 2 * 2 for d, _ in dims) +
-                           out_bytes, "flops": 2 * groups * r * (D * D + Di * Di)},
+                           out_bytes, "flops": sum(2 * groups * r * d * d for d, _ in dims)},
         "_rows": len(rows),
     }
 
@@ -352,7 +353,7 @@ def run_gpu(args, wl, rank, world, local_rank):
     s = wl.spec
     t = wl.to(dev)
     prefill = s.mode == "prefill"
-    step = CsaStep(t, s.ratio, s.topk, prefill=prefill).prepare()
+    step = CsaStep(t, s.ratio, s.topk, prefill=prefill, dense=s.dense).prepare()
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     work = algorithmic_work(wl)

@@ -98,7 +98,9 @@ typedef enum { CSA_MODE_AUTO = 0, CSA_MODE_DECODE = 1, CSA_MODE_PREFILL = 2 } cs
  * ape f32 [ratio, d]; gamma bf16 [d] or NULL; positions, row_req i32 [n_rows];
  * block_table i32 [n_req, max_blocks]; cmp_pool bf16 [n_blocks, 128, d];
  * idx_pool i8 [n_blocks, 128, d]; idx_scale_pool f32 [n_blocks, 128].
- * Supported: ratio in {1, 2, 4}; d in {128, 512}; dx a multiple of 64 <= 1024.
+ * Supported: ratio in {1, 2, 4, 128} (128: HCA's non-overlapping groups,
+ * "Hyper-Parallel ... DeepSeek V4 CP", "ratio=128"); d in {128, 512}; dx a
+ * multiple of 64 <= 1024.
  * Workspace: n_rows * d * 4 bytes (gate logits), rounded up.
  *
  * Recurrent state ring ("DeepSeek V4.1 Flash", "Compressor state ownership"),
@@ -114,7 +116,7 @@ typedef enum { CSA_MODE_AUTO = 0, CSA_MODE_DECODE = 1, CSA_MODE_PREFILL = 2 } cs
  * -1 disables the request (nothing published or written); a block >=
  * n_state_blocks sets CSA_DEV_BAD_BLOCK and skips the request.  Rows with a
  * negative position neither publish nor write.  Requires state_capacity >=
- * ratio.  A caller built against a header without these four fields passes a
+ * ratio (at most 256).  A caller built against a header without these four fields passes a
  * smaller struct_size and gets no ring.
  * ---------------------------------------------------------------------- */
 typedef struct {
@@ -274,6 +276,11 @@ CSA_API csa_status_t csa_index_topk_noalloc(csa_index_args *args, csa_stream_t s
  *
  * For row t (request b, position p), candidates are cmp entry c for every
  * c = topk_idx[t, i] >= 0 and raw row p' for p' in [max(0, p-window+1), p].
+ * topk_idx == NULL selects dense compressed visibility (HCA: "Hyper-Parallel
+ * ... DeepSeek V4 CP", "ratio=128" and "10.3 Causal mask"): every visible
+ * entry c < V = min(n_cmp[b], (p+1)/ratio) is a candidate; topk is then the
+ * capacity, and V > topk raises CSA_DEV_BAD_INDEX and keeps entries
+ * 0 .. topk-1.
  * Each candidate row k_i is both key and value.  Per head h, with q_h =
  * q[t,h,:] rotated at p:
  *   l_i = softmax_scale * q_h . k_i

@@ -29,19 +29,22 @@ def compress_step(t, spec, pools=None):
                   rope_dim=spec.rope_dim, out="int8")
     if spec.state:
         pools["state_main"] = O.as_f64(t["state_main"]).copy()
-        pools["state_idx"] = O.as_f64(t["state_idx"]).copy()
         table = t["state_table"].numpy()
         main = O.compress_stateful(t["kv_raw"], t["kv_raw"], t["w_gate"], t["ape"], spec.ratio,
                                    t["row_pos"], t["row_req"], pools["state_main"], table,
                                    out="bf16")
-        idx = O.compress_stateful(t["idx_raw"], t["idx_raw"], t["w_gate_i"], t["ape_i"],
-                                  spec.ratio, t["row_pos"], t["row_req"], pools["state_idx"],
-                                  table, **idx_kw)
+        idx = []
+        if not spec.dense:  # HCA has no indexer, hence no index-key compressor
+            pools["state_idx"] = O.as_f64(t["state_idx"]).copy()
+            idx = O.compress_stateful(t["idx_raw"], t["idx_raw"], t["w_gate_i"], t["ape_i"],
+                                      spec.ratio, t["row_pos"], t["row_req"], pools["state_idx"],
+                                      table, **idx_kw)
     else:
         main = O.compress(t["kv_raw"], t["kv_raw"], t["w_gate"], t["ape"], spec.ratio,
                           t["row_pos"], t["row_req"], out="bf16")
-        idx = O.compress(t["idx_raw"], t["idx_raw"], t["w_gate_i"], t["ape_i"], spec.ratio,
-                         t["row_pos"], t["row_req"], **idx_kw)
+        idx = [] if spec.dense else O.compress(t["idx_raw"], t["idx_raw"], t["w_gate_i"],
+                                                 t["ape_i"], spec.ratio, t["row_pos"],
+                                                 t["row_req"], **idx_kw)
     table = t["cmp_table"].numpy()
     for b, g, vals in main:
         pg = int(table[b, g // O.BLOCK])
@@ -73,13 +76,28 @@ def attention_row(t, spec, pools, row, topk_row, inv_rope_out=False, use_sink=Tr
                               inv_rope_out=inv_rope_out)
 
 
+def dense_selection(t, spec, row):
+    """HCA's candidates: every visible compressed entry, up to the capacity."""
+    b = int(t["row_req"][row])
+    v = O.visible_count(int(t["row_pos"][row]), spec.ratio, int(t["n_cmp"][b]))
+    sel = np.full(spec.topk, -1, dtype=np.int64)
+    sel[:min(v, spec.topk)] = np.arange(min(v, spec.topk))
+    return sel
+
+
 def full_step(t, spec, rows=None):
-    """Oracle's own chain: compress -> scores -> top-k -> attention for ``rows``."""
+    """Oracle's own chain: compress -> scores -> top-k -> attention for ``rows``
+    (HCA: compress -> attention over every visible compressed entry)."""
     pools, _, _ = compress_step(t, spec)
     rows = range(spec.n_rows) if rows is None else rows
     res = {}
     for row in rows:
         if int(t["row_req"][row]) < 0:
+            continue
+        if spec.dense:
+            sel = dense_selection(t, spec, row)
+            out, lse = attention_row(t, spec, pools, row, sel)
+            res[row] = dict(scores=None, topk=sel, out=out, lse=lse)
             continue
         s = index_row(t, spec, pools, row)
         sel = O.topk_select(s, spec.topk)

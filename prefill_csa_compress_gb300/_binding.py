@@ -371,14 +371,16 @@ def csa_index_topk_noalloc(*, q_idx, weights, row_req, row_pos, n_cmp, ratio, id
 def _attn(fn_name, *, q, row_req, row_pos, topk_idx, kv_pool, kv_block_table, kv_len, cmp_pool,
           cmp_block_table, n_cmp, ratio, out, lse=None, sink=None, softmax_scale=None,
           window=128, rope_cos=None, rope_sin=None, inv_rope_out=False, status=None,
-          workspace=None, stream=None, prepare=False):
+          workspace=None, stream=None, prepare=False, dense_cap=0):
+    """``topk_idx=None`` with ``dense_cap > 0``: every visible compressed entry
+    (up to dense_cap) is a candidate (dense visibility, HCA)."""
     a = AttnArgs()
     a.struct_size = ctypes.sizeof(AttnArgs)
     a.n_rows = int(q.shape[0])
     a.n_heads = int(q.shape[1])
     a.head_dim = int(q.shape[2])
     a.ratio = int(ratio)
-    a.topk = int(topk_idx.shape[1]) if topk_idx is not None else 0
+    a.topk = int(topk_idx.shape[1]) if topk_idx is not None else int(dense_cap)
     a.window = int(window)
     a.inv_rope_out = 1 if inv_rope_out else 0
     a.softmax_scale = float(softmax_scale if softmax_scale is not None else q.shape[2] ** -0.5)

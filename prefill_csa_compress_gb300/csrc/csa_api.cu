@@ -89,7 +89,6 @@ csa_status_t check_attn_args(const csa_attn_args *a) {
   if (!a->q || !a->row_req || !a->row_pos || !a->kv_pool || !a->kv_block_table || !a->kv_len ||
       !a->cmp_pool || !a->cmp_block_table || !a->n_cmp || !a->out)
     return CSA_ERR_INVALID_ARG;
-  if (a->topk > 0 && !a->topk_idx) return CSA_ERR_INVALID_ARG;
   if ((a->rope_cos == nullptr) != (a->rope_sin == nullptr)) return CSA_ERR_INVALID_ARG;
   if (a->rope_cos && a->rope_cap <= 0) return CSA_ERR_INVALID_ARG;
   if (a->kv_max_blocks <= 0 || a->cmp_max_blocks <= 0 || a->kv_n_blocks <= 0 ||
@@ -142,7 +141,8 @@ static csa_status_t check_compress(csa_compress_args *a, bool *size_query) {
   *size_query = false;
   if (!a || a->struct_size < offsetof(csa_compress_args, state_cache)) return CSA_ERR_INVALID_ARG;
   if (a->n_rows < 0 || a->n_req < 0) return CSA_ERR_INVALID_ARG;
-  if (a->ratio != 1 && a->ratio != 2 && a->ratio != 4) return CSA_ERR_UNSUPPORTED;
+  if (a->ratio != 1 && a->ratio != 2 && a->ratio != 4 && a->ratio != 128)
+    return CSA_ERR_UNSUPPORTED;
   if (a->d != 128 && a->d != 512) return CSA_ERR_UNSUPPORTED;
   if (a->dx <= 0 || a->dx % 64 != 0 || a->dx > 1024) return CSA_ERR_UNSUPPORTED;
   if (a->out_mode != CSA_OUT_BF16 && a->out_mode != CSA_OUT_INT8) return CSA_ERR_INVALID_ARG;
@@ -165,7 +165,7 @@ static csa_status_t check_compress(csa_compress_args *a, bool *size_query) {
   if (!aligned16(a->x) || !aligned16(a->kv) || !aligned16(a->w_gate)) return CSA_ERR_INVALID_ARG;
   if (a->state_cache &&
       (!a->state_block_table || a->n_state_blocks <= 0 || a->state_capacity < a->ratio ||
-       a->state_capacity > 64))
+       a->state_capacity > 256))
     return CSA_ERR_INVALID_ARG;
   return CSA_OK;
 }

@@ -63,7 +63,9 @@ __device__ __forceinline__ int chan_lo(uint32_t r, uint32_t S) {
 __device__ __forceinline__ const uint16_t *candidate_row(const csa_attn_args &a, int t, int b,
                                                          int p, int V, int kvl, int j) {
   if (j < a.topk) {
-    const int c = a.topk_idx[(long long)t * a.topk + j];
+    // dense visibility (no selection): compressed entry j itself
+    const int c = a.topk_idx ? a.topk_idx[(long long)t * a.topk + j] : (j < V ? j : -1);
+    if (!a.topk_idx && j == 0 && V > a.topk) flag(a.status_dev, CSA_DEV_BAD_INDEX);
     if (c < 0) return nullptr;
     if (c >= V) {
       flag(a.status_dev, CSA_DEV_BAD_INDEX);

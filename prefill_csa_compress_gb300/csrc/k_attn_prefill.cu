@@ -152,7 +152,9 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
       const int p = a.row_pos[t];
       const int V = min(visible_count(p, a.ratio, a.n_cmp[b]), a.cmp_max_blocks * kBlock);
       const int kvl = a.kv_len[b];
-      const int32_t *sel = a.topk_idx + (long long)t * a.topk;
+      // the row's selection, or (no selection: dense visibility) entries 0 .. V-1
+      const int32_t *sel = a.topk_idx ? a.topk_idx + (long long)t * a.topk : nullptr;
+      if (!sel && V > a.topk && lane == 0) flag(a.status_dev, CSA_DEV_BAD_INDEX);
       // the row's compressed-page table, read once (tables of up to 64 pages)
       const bool cache_tbl = a.cmp_max_blocks <= 64;
       __syncwarp();
@@ -166,7 +168,7 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int j = j0 + 32 * u + lane;
-          c[u] = j < a.topk ? sel[j] : -1;
+          c[u] = j < a.topk ? (sel ? sel[j] : (j < V ? j : -1)) : -1;
         }
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int j = g0 + 32 * u + lane;
-          c[u] = j < a.topk ? sel[j] : -1;
+          c[u] = j < a.topk ? (sel ? sel[j] : (j < V ? j : -1)) : -1;
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {

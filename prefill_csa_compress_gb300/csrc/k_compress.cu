@@ -17,6 +17,8 @@
 namespace csa {
 namespace {
 
+constexpr int kMaxRatio = 128;  // HCA
+
 // ---------------------------------------------------------------------------
 // Long chunks on the tensor cores: logits[t, d] = sum_k x[t, k] w_gate[k, d].
 // One CTA per 128-row x 128-column tile of logits.  x tiles (K-major) and
@@ -225,14 +227,18 @@ __global__ void compress_pool_kernel(csa_compress_args a, const float *__restric
   }
   // token j of the group (position p - r + 1 + j): row t - r + 1 + j of this
   // chunk, or (a position before the chunk start) the ring
-  uint32_t in_chunk = 0;
-  for (int j = 0; j < r; ++j) {
+  __shared__ uint8_t in_chunk[kMaxRatio];
+  __shared__ int s_complete;
+  if (threadIdx.x == 0) s_complete = 1;
+  __syncthreads();
+  for (int j = threadIdx.x; j < r; j += blockDim.x) {
     const int s = t - r + 1 + j;
-    if (s >= 0 && a.row_req[s] == b && a.positions[s] == p - r + 1 + j)
-      in_chunk |= 1u << j;
-    else if (!ring)
-      return;  // the group is not complete in this chunk
+    const bool here = s >= 0 && a.row_req[s] == b && a.positions[s] == p - r + 1 + j;
+    in_chunk[j] = here;
+    if (!here && !ring) s_complete = 0;
   }
+  __syncthreads();
+  if (!s_complete) return;  // the group is not complete in this chunk (uniform)
   const int g = p / r;
   const int page = g / kBlock;
   int phys = -1;
@@ -245,26 +251,44 @@ __global__ void compress_pool_kernel(csa_compress_args a, const float *__restric
   const int d = threadIdx.x;
   const int t0 = t - r + 1;
   const uint16_t *kv = static_cast<const uint16_t *>(a.kv);
-
-  // pooling softmax over the r tokens of the group, per channel
-  float lg[4], kvv[4];
-  float mx = -INFINITY;
-  for (int j = 0; j < r; ++j) {
-    if (in_chunk & (1u << j)) {
-      lg[j] = logits[(long long)(t0 + j) * D + d] + a.ape[j * D + d];
-      kvv[j] = bf16_bits_to_float(kv[(long long)(t0 + j) * D + d]);
+  // gate score and kv value of token j for this channel
+  auto token = [&](int j, float &lg, float &v) {
+    if (in_chunk[j]) {
+      lg = logits[(long long)(t0 + j) * D + d] + a.ape[j * D + d];
+      v = bf16_bits_to_float(kv[(long long)(t0 + j) * D + d]);
     } else {
       const float *slot = ring + (long long)((p - r + 1 + j) % a.state_capacity) * 2 * D;
-      kvv[j] = slot[d];
-      lg[j] = slot[D + d];
+      v = slot[d];
+      lg = slot[D + d];
     }
-    mx = fmaxf(mx, lg[j]);
-  }
-  float s = 0.f, y = 0.f;
-  for (int j = 0; j < r; ++j) {
-    float e = expf(lg[j] - mx);
-    s += e;
-    y = fmaf(e, kvv[j], y);
+  };
+
+  // pooling softmax over the r tokens of the group, per channel, in one pass
+  // over batches of 8 tokens (their loads in flight together; the running
+  // maximum moves once per batch)
+  float mx = -INFINITY, s = 0.f, y = 0.f;
+  for (int j0 = 0; j0 < r; j0 += 8) {
+    float lg[8], v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      lg[i] = -INFINITY;
+      v[i] = 0.f;
+      if (j0 + i < r) token(j0 + i, lg[i], v[i]);
+    }
+    float mb = lg[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) mb = fmaxf(mb, lg[i]);
+    const float mn = fmaxf(mx, mb);
+    const float c = expf(mx - mn);  // 0 for the first batch
+    s *= c;
+    y *= c;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float e = expf(lg[i] - mn);  // 0 past the group's end
+      s += e;
+      y = fmaf(e, v[i], y);
+    }
+    mx = mn;
   }
   y = round_bf16(y / s);
 
@@ -557,7 +581,7 @@ size_t fused_smem(const csa_compress_args &a) {
 
 // the short-chunk column tile for this call, or 0 when it takes the long path
 int fused_cols(const csa_compress_args &a) {
-  if (a.n_rows > 256 || a.state_cache) return 0;
+  if (a.n_rows > 256 || a.state_cache || a.ratio > 4) return 0;
   if (a.d == 128 && (size_t)a.dx * 128 * 2 <= FC_MAX_W_BYTES) return 128;
   if (a.d == 512 && a.out_mode == CSA_OUT_BF16 && !a.gamma && (size_t)a.dx * 16 * 2 <= FC_MAX_W_BYTES)
     return 16;

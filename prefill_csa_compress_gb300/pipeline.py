@@ -25,17 +25,20 @@ class CsaStep:
     kv_pool, kv_table, cmp_pool, idx_pool, idx_scale, cmp_table, q, q_idx,
     idx_w, sink, kv_raw, idx_raw, w_gate, ape, w_gate_i, ape_i, rope_cos,
     rope_sin, and optionally the compressors' state rings state_main,
-    state_idx with state_table.  ``ratio``, ``topk`` and ``prefill``
-    describe the step.
+    state_idx with state_table.  ``ratio``, ``topk``, ``prefill`` and
+    ``dense`` (HCA) describe the step.
     """
 
     def __init__(self, t: dict, ratio: int, topk: int, prefill: bool = False,
-                 compress: bool = True, status: bool = True):
+                 compress: bool = True, status: bool = True, dense: bool = False):
         self.t = t
         self.ratio = int(ratio)
         self.topk = int(topk)
         self.prefill = bool(prefill)
         self.do_compress = bool(compress)
+        # HCA: no indexer (and no index-key compressor); the attention takes
+        # every visible compressed entry, ``topk`` being the capacity
+        self.dense = bool(dense)
         dev = t["q"].device
         T = t["q"].shape[0]
         self.topk_idx = torch.full((T, self.topk), -1, dtype=torch.int32, device=dev)
@@ -68,6 +71,9 @@ class CsaStep:
 
     def compress(self, stream=None):
         main, keys = self._compress_kw()
+        if self.dense:
+            self.ws["cm"] = B.csa_compress(workspace=self.ws.get("cm"), stream=stream, **main)
+            return
         self.ws["cp"] = B.csa_compress_pair(main, keys, workspaces=self.ws.get("cp", (None, None)),
                                             stream=stream)
 
@@ -82,12 +88,17 @@ class CsaStep:
             mode=B.CSA_MODE_PREFILL if self.prefill else B.CSA_MODE_DECODE, status=self.status,
             workspace=self._ws("ix"), stream=stream)
 
+    def _selection(self, topk_idx=None):
+        if topk_idx is not None:
+            return topk_idx
+        return None if self.dense else self.topk_idx
+
     def attention(self, stream=None, topk_idx=None):
         t = self.t
         fn = B.csa_sparse_attn_prefill if self.prefill else B.csa_sparse_attn_decode
         self.ws["at"] = fn(
-            q=t["q"], row_req=t["row_req"], row_pos=t["row_pos"],
-            topk_idx=self.topk_idx if topk_idx is None else topk_idx, kv_pool=t["kv_pool"],
+            q=t["q"], row_req=t["row_req"], row_pos=t["row_pos"], dense_cap=self.topk,
+            topk_idx=self._selection(topk_idx), kv_pool=t["kv_pool"],
             kv_block_table=t["kv_table"], kv_len=t["kv_len"], cmp_pool=t["cmp_pool"],
             cmp_block_table=t["cmp_table"], n_cmp=t["n_cmp"], ratio=self.ratio, out=self.out,
             lse=self.lse, sink=t["sink"], rope_cos=t["rope_cos"], rope_sin=t["rope_sin"],
@@ -99,18 +110,21 @@ class CsaStep:
         calls = []
         if self.do_compress:
             main, keys = self._compress_kw()
-            calls.append(B.csa_compress_pair(main, keys, prepare=True))
-        calls.append(B.csa_index_topk(
-            q_idx=t["q_idx"], weights=t["idx_w"], row_req=t["row_req"], row_pos=t["row_pos"],
-            n_cmp=t["n_cmp"], ratio=self.ratio, idx_pool=t["idx_pool"],
-            idx_scale_pool=t["idx_scale"], cmp_block_table=t["cmp_table"], topk=self.topk,
-            topk_idx=self.topk_idx, topk_score=self.topk_score, rope_cos=t["rope_cos"],
-            rope_sin=t["rope_sin"],
-            mode=B.CSA_MODE_PREFILL if self.prefill else B.CSA_MODE_DECODE, status=self.status,
-            prepare=True))
+            calls.append(B.csa_compress(prepare=True, **main) if self.dense else
+                         B.csa_compress_pair(main, keys, prepare=True))
+        if not self.dense:
+            calls.append(B.csa_index_topk(
+                q_idx=t["q_idx"], weights=t["idx_w"], row_req=t["row_req"], row_pos=t["row_pos"],
+                n_cmp=t["n_cmp"], ratio=self.ratio, idx_pool=t["idx_pool"],
+                idx_scale_pool=t["idx_scale"], cmp_block_table=t["cmp_table"], topk=self.topk,
+                topk_idx=self.topk_idx, topk_score=self.topk_score, rope_cos=t["rope_cos"],
+                rope_sin=t["rope_sin"],
+                mode=B.CSA_MODE_PREFILL if self.prefill else B.CSA_MODE_DECODE, status=self.status,
+                prepare=True))
         fn = B.csa_sparse_attn_prefill if self.prefill else B.csa_sparse_attn_decode
         calls.append(fn(
-            q=t["q"], row_req=t["row_req"], row_pos=t["row_pos"], topk_idx=self.topk_idx,
+            q=t["q"], row_req=t["row_req"], row_pos=t["row_pos"], topk_idx=self._selection(),
+            dense_cap=self.topk,
             kv_pool=t["kv_pool"], kv_block_table=t["kv_table"], kv_len=t["kv_len"],
             cmp_pool=t["cmp_pool"], cmp_block_table=t["cmp_table"], n_cmp=t["n_cmp"],
             ratio=self.ratio, out=self.out, lse=self.lse, sink=t["sink"],
@@ -122,7 +136,8 @@ class CsaStep:
         if self._prepared is None:
             if self.do_compress:
                 self.compress(stream)
-            self.index(stream)
+            if not self.dense:
+                self.index(stream)
             self.attention(stream)
         else:
             for c in self._prepared:

@@ -60,12 +60,14 @@ def _rope_q(t, row, key="q_idx"):
     ("chunked_prefill", dict(ctx=[130, 61], chunk=[130, 61], ratio=1, seed=35, pad_rows=2)),
     ("serving_decode", {}),
     ("stateful_decode", {}),                                            # state rings
+    ("hca_prefill", dict(ctx=[700], chunk=[700], seed=61)),             # ratio 128, ragged
+    ("hca_decode", {}),                                                 # ratio 128 + ring
     ("chunked_prefill", {}),                                            # full 8192-token chunk
 ])
 def test_compress_parity(name, over):
     spec = spec_for(name, **over)
     wl, t = _load(spec)
-    step = CsaStep(t, spec.ratio, spec.topk, prefill=spec.mode == "prefill")
+    step = CsaStep(t, spec.ratio, spec.topk, prefill=spec.mode == "prefill", dense=spec.dense)
     step.compress()
     torch.cuda.synchronize()
     assert _status(step) == 0
@@ -74,13 +76,16 @@ def test_compress_parity(name, over):
     got_cmp = t["cmp_pool"].cpu()
     got_idx = t["idx_pool"].cpu()
     got_sc = t["idx_scale"].cpu()
-    assert len(main) == len(idx) > 0 or spec.name == "serving_decode"
+    assert (len(main) == len(idx) > 0 or spec.name == "serving_decode" or
+            (spec.dense and len(main) > 0 and not idx))
     g_rows, r_rows = [], []
     n_diff = 0
-    for (b, g, vals), (_, _, codes, scale) in zip(main, idx):
+    for b, g, vals in main:
         pg, row = int(table[b, g // BLOCK]), g % BLOCK
         g_rows.append(got_cmp[pg, row].double().numpy())
         r_rows.append(vals)
+    for b, g, codes, scale in idx:
+        pg, row = int(table[b, g // BLOCK]), g % BLOCK
         n_diff += check_int8(got_idx[pg, row].numpy(), got_sc[pg, row].item(), codes,
                              np.float32(scale))
     check_bf16(np.stack(g_rows), np.stack(r_rows), "cmp_kv")
@@ -88,7 +93,7 @@ def test_compress_parity(name, over):
     assert n_diff <= INT8_FLIP_RATE * len(idx) * spec.idx_dim + 2, n_diff
     if spec.state:
         # the rings: kv rows exactly, gate scores to FP32 accuracy
-        for name in ("state_main", "state_idx"):
+        for name in ("state_main",) if spec.dense else ("state_main", "state_idx"):
             got_s = t[name].cpu().double().numpy()
             ref_s = pools[name]
             d = got_s.shape[2] // 2
@@ -476,6 +481,33 @@ def test_compress_pair_equals_two_calls(name, over):
 
 
 # ------------------------------------------------------------------ whole step
+
+
+@pytest.mark.parametrize("name,over", [
+    ("hca_decode", {}),
+    ("hca_prefill", dict(ctx=[1300], chunk=[1300], seed=62)),
+])
+def test_hca_step(name, over):
+    """HCA: ratio-128 compression, then attention over every visible
+    compressed entry plus the window, against the oracle's chain."""
+    spec = spec_for(name, **over)
+    wl, t = _load(spec)
+    step = CsaStep(t, spec.ratio, spec.topk, prefill=spec.mode == "prefill", dense=True)
+    step.run()
+    torch.cuda.synchronize()
+    assert _status(step) == 0
+    rows = [r for r in range(spec.n_rows) if int(wl.row_req[r]) >= 0]
+    if len(rows) > 40:
+        rows = rows[:8] + rows[-24:] + list(np.random.default_rng(5).choice(rows, 8, replace=False))
+    _, res = OS.full_step(wl.t, spec, rows=rows)
+    out = step.out.cpu().double().numpy()
+    lse = step.lse.cpu().numpy()
+    g = np.stack([out[r] for r in res])
+    ref = np.stack([res[r]["out"] for r in res])
+    check_bf16(g, ref, "hca out", magnitude=max(1.0, float(np.max(np.abs(ref))) / 2))
+    gl = np.stack([lse[r] for r in res])
+    rl = np.stack([res[r]["lse"] for r in res])
+    assert np.max(np.abs(gl - rl)) <= LSE_ABS * max(1.0, np.max(np.abs(rl)))
 
 
 @pytest.mark.parametrize("name", ["tiny_decode", "serving_decode", "stateful_decode"])

@@ -41,7 +41,8 @@ class WorkloadSpec:
     kv_pages: str = "all"  # "all" or "window" (only pages the window reads; others -1)
     cmp_init: str = "random"  # "random" or "zeros" (filled by the compressor)
     pad_rows: int = 0  # trailing padding rows (row_req = -1)
-    state: bool = False  # compressors keep a recurrent state ring (capacity 4)
+    state: bool = False  # compressors keep a recurrent state ring (capacity max(4, ratio))
+    dense: bool = False  # HCA: no indexer, attention over every visible compressed entry
     extra: dict = field(default_factory=dict)
 
     @property
@@ -75,6 +76,14 @@ CONFIGS = {
     "stateful_decode": WorkloadSpec("stateful_decode", [8192, 6000, 4096, 2048], [2, 2, 2, 2],
                                     ratio=4, topk=512, seed=5, kv_pool_pages=256,
                                     cmp_pool_pages=256, state=True),
+    # HCA (ratio 128, dense compressed visibility): an 8192-token prefill chunk
+    # whose compressor fills the 64 entries, and a decode step of 4 requests x
+    # 2 rows at 131,072 positions whose groups close through the state ring
+    # (capacity 128).  top-k is the dense capacity.
+    "hca_prefill": WorkloadSpec("hca_prefill", [8192], [8192], ratio=128, topk=64, seed=6,
+                                mode="prefill", cmp_init="zeros", dense=True),
+    "hca_decode": WorkloadSpec("hca_decode", [131072] * 4, [2] * 4, ratio=128, topk=1024, seed=7,
+                               kv_pages="window", dense=True, state=True),
     # 4 requests x 2 rows at 1,048,576 positions, ratio 4, top-k 2048.
     "million_decode": WorkloadSpec("million_decode", [1048576] * 4, [2] * 4, ratio=4, topk=2048,
                                    seed=4, kv_pages="window"),
@@ -233,7 +242,7 @@ def make_workload(spec: WorkloadSpec) -> Workload:
     if spec.state:
         # one ring block per request (plus a spare) in a shuffled order; the
         # slots hold earlier tokens' kv rows (BF16 values) and gate scores
-        cap = 4
+        cap = max(4, r)
         t["state_table"] = torch.from_numpy(rng.permutation(B + 1)[:B].astype(np.int32))
         for name, d in (("state_main", Dm), ("state_idx", Di)):
             kv_part = _normal_bf16(rng, (B + 1, cap, d)).float()
