@@ -14,7 +14,9 @@ from .csa_oracle import (  # noqa: F401
     page_rows,
     quantize_int8,
     rope_rotate,
+    select_blocks,
     sparse_attention,
+    topk_in_blocks,
     topk_select,
     visible_count,
     window_positions,

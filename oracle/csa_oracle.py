@@ -323,6 +323,32 @@ def topk_select(scores, k):
     return out
 
 
+def select_blocks(scores, n_blocks, block=8):
+    """Level one of the hierarchical indexer ("DeepSeek V4.1 Flash": the
+    first selection takes 2,048 blocks of eight compressed positions, which
+    later reindex layers search).  A block's score is the largest score of
+    its visible positions (a reading: the page does not say how blocks are
+    ranked); the n_blocks best blocks by (score descending, block ascending)
+    are emitted ascending with trailing -1 padding, as topk_select does."""
+    scores = np.asarray(scores, dtype=np.float64)
+    nb = (len(scores) + block - 1) // block
+    best = np.array([scores[i * block:(i + 1) * block].max() for i in range(nb)])
+    return topk_select(best, n_blocks)
+
+
+def topk_in_blocks(scores, blocks, k, block=8):
+    """Level two (reindex): the k best visible positions inside the given
+    candidate blocks (-1 entries ignored), by (score descending, position
+    ascending), emitted ascending with trailing -1 padding."""
+    scores = np.asarray(scores, dtype=np.float64)
+    V = len(scores)
+    pos = sorted({b * block + i for b in np.asarray(blocks).tolist() if b >= 0
+                  for i in range(block) if b * block + i < V})
+    pos = np.array(pos, dtype=np.int64)
+    sel = topk_select(scores[pos], k) if len(pos) else np.full(k, -1, dtype=np.int64)
+    return np.where(sel >= 0, pos[np.maximum(sel, 0)] if len(pos) else -1, -1)
+
+
 # --------------------------------------------------------------------------
 # a5 / a6: shared-KV sparse attention with sink
 # --------------------------------------------------------------------------

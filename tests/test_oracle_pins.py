@@ -487,6 +487,86 @@ def test_topk_matches_lexsort_with_ties():
         assert np.all(np.diff(got[:len(want)]) > 0)
 
 
+def test_select_blocks_hand_examples():
+    # block 4: maxima 5, 9, 8 -> the two best blocks are 1 and 2
+    s = [1, 5, 2, 3, 9, 0, 4, 4, 8]
+    assert O.select_blocks(s, 2, block=4).tolist() == [1, 2]
+    # the largest entry ranks a block, not its sum or mean: block 0 sums to 20, block 1 to 9
+    s = [5, 5, 5, 5, 9, 0, 0, 0]
+    assert O.select_blocks(s, 1, block=4).tolist() == [1]
+    # equal maxima: the lower block wins
+    s = [7, 0, 0, 0, 1, 7, 1, 1, 7, 7, 7, 7]
+    assert O.select_blocks(s, 2, block=4).tolist() == [0, 1]
+    # a ragged last block competes with its visible entries only; padding past the blocks
+    s = [0, 0, 0, 0, 0, 0, 0, 0, 3]
+    assert O.select_blocks(s, 4, block=8).tolist() == [0, 1, -1, -1]
+    assert O.select_blocks(s, 1, block=8).tolist() == [1]
+
+
+def test_topk_in_blocks_hand_examples():
+    s = [1, 5, 2, 3, 9, 0, 4, 4, 8]
+    # blocks 0 and 2 of four: positions 0..3 and 8; the 9 at position 4 is outside
+    assert O.topk_in_blocks(s, [0, 2], 3, block=4).tolist() == [1, 3, 8]
+    # -1 entries are ignored; too few eligible positions pad with -1
+    assert O.topk_in_blocks(s, [2, -1], 3, block=4).tolist() == [8, -1, -1]
+    assert O.topk_in_blocks(s, [-1, -1], 2, block=4).tolist() == [-1, -1]
+    # ties inside the candidates: the lower position wins
+    s = [4, 4, 0, 0, 4, 4, 4, 4]
+    assert O.topk_in_blocks(s, [1, 0], 3, block=4).tolist() == [0, 1, 4]
+
+
+def _dominates(s, a, b):
+    return s[a] > s[b] or (s[a] == s[b] and a < b)
+
+
+def test_topk_in_blocks_by_pairwise_dominance():
+    """Brute force: every emitted position is eligible and beats every
+    eligible position left out, and exactly min(k, eligible) are emitted."""
+    rng = np.random.default_rng(48)
+    for V, nb, k in [(37, 2, 5), (64, 3, 24), (65, 9, 30), (8, 1, 8), (100, 4, 7)]:
+        s = rng.integers(-3, 4, V).astype(np.float64)
+        n_all = (V + 7) // 8
+        blocks = rng.choice(n_all, size=min(nb, n_all), replace=False)
+        got = O.topk_in_blocks(s, blocks, k)
+        elig = [p for p in range(V) if p // 8 in set(blocks.tolist())]
+        chosen = [int(p) for p in got if p >= 0]
+        assert len(chosen) == min(k, len(elig))
+        assert chosen == sorted(chosen) and np.all(got[len(chosen):] == -1)
+        assert set(chosen) <= set(elig)
+        for a in chosen:
+            for b in elig:
+                if b not in chosen:
+                    assert _dominates(s, a, b)
+
+
+def test_select_blocks_by_pairwise_dominance():
+    rng = np.random.default_rng(49)
+    for V, nb in [(37, 2), (64, 5), (129, 16), (7, 1)]:
+        s = rng.integers(-3, 4, V).astype(np.float64)
+        n_all = (V + 7) // 8
+        m = [max(s[8 * b:8 * b + 8]) for b in range(n_all)]
+        got = [int(b) for b in O.select_blocks(s, nb) if b >= 0]
+        assert len(got) == min(nb, n_all) and got == sorted(got)
+        for a in got:
+            for b in range(n_all):
+                if b not in got:
+                    assert _dominates(m, a, b)
+
+
+@pytest.mark.parametrize("V,k,extra", [(64, 8, 0), (1000, 64, 0), (1000, 64, 5), (9, 2, 0),
+                                       (4096, 512, 0)])
+def test_two_level_selection_equals_flat_when_k_fits(V, k, extra):
+    """With as many candidate blocks as selected positions (or more), ranking
+    the same scores in two levels loses nothing: a position among the overall
+    k best lies in a block whose maximum outranks every block without one."""
+    rng = np.random.default_rng(V + k + extra)
+    s = rng.integers(-4, 5, V).astype(np.float64)  # ties across blocks
+    blocks = O.select_blocks(s, k + extra)
+    assert np.array_equal(O.topk_in_blocks(s, blocks, k), O.topk_select(s, k))
+    # with every block a candidate the second level is the flat top-k
+    assert np.array_equal(O.topk_in_blocks(s, np.arange((V + 7) // 8), k), O.topk_select(s, k))
+
+
 # ---------------------------------------------------------------- attention
 
 
