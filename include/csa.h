@@ -200,6 +200,30 @@ CSA_API csa_status_t csa_compress_pair(csa_compress_args *first, csa_compress_ar
  * i32 [n_req, max_blocks]; topk_idx i32 [n_rows, topk]; topk_score f32
  * [n_rows, topk] or NULL.  Supported: n_heads == 64, head_dim == 128,
  * 1 <= topk <= 2048, ratio >= 1.
+ *
+ * Hierarchical indexer ("DeepSeek V4.1 Flash", model structure and the
+ * hierarchical indexer: a level-one layer picks 2,048 blocks of eight
+ * compressed positions; later reindex layers compute their own index query
+ * and select their final positions only inside those blocks).  Candidate
+ * block j of a row holds positions j*cand_block .. j*cand_block+cand_block-1.
+ *  - Level one (cand_out != NULL): besides the top-k above, cand_out[t]
+ *    receives the n_cand blocks with the largest block score, where a
+ *    block's score is the largest score of its visible entries (ties: the
+ *    lower block), ascending with trailing -1 padding.
+ *  - Reindex (cand_in != NULL): row t scores only the visible positions of
+ *    its candidate blocks, the longest prefix of cand_in[t] that is
+ *    strictly ascending with every block in [0, ceil(V/cand_block)); a
+ *    later entry other than -1 raises CSA_DEV_BAD_INDEX and is ignored
+ *    (a level-one cand_out row of the same position is always valid).
+ *    topk_idx[t] gets the k best of those positions, ascending, -1 padded.
+ *    `scores` then holds the candidate scores in candidate order: entry
+ *    i < the row's eligible count is the score of position
+ *    cand_in[t][i / cand_block] * cand_block + i % cand_block; score_cols
+ *    >= n_cand * cand_block.
+ * cand_block is 8, 16 or 32; 1 <= n_cand <= 2048; at most one of cand_out
+ * and cand_in is set.  A struct_size that ends before `cand_block` (the
+ * struct without these fields) turns both off.  csa_index_topk_noalloc
+ * returns CSA_ERR_UNSUPPORTED for either mode.
  * ---------------------------------------------------------------------- */
 typedef struct {
   uint32_t struct_size;
@@ -231,6 +255,10 @@ typedef struct {
   uint32_t *status_dev;
   void *workspace;
   size_t workspace_bytes;
+  int32_t cand_block;       /* positions per candidate block (8, 16 or 32) */
+  int32_t n_cand;           /* candidate blocks per row */
+  int32_t *cand_out;        /* i32 [n_rows, n_cand] or NULL: level-one selection */
+  const int32_t *cand_in;   /* i32 [n_rows, n_cand] or NULL: reindex candidates */
 } csa_index_args;
 
 CSA_API csa_status_t csa_index_topk(csa_index_args *args, csa_stream_t stream);

@@ -85,12 +85,27 @@ def dense_selection(t, spec, row):
     return sel
 
 
+def reindex_tensors(t):
+    """The reindex layer of a hierarchical workload: the level-one layer's
+    caches with the reindex layer's own q, q_idx, idx_w and sink."""
+    r = dict(t)
+    for k in ("q", "q_idx", "idx_w", "sink"):
+        r[k] = t[k + "2"]
+    return r
+
+
 def full_step(t, spec, rows=None):
     """Oracle's own chain: compress -> scores -> top-k -> attention for ``rows``
-    (HCA: compress -> attention over every visible compressed entry)."""
+    (HCA: compress -> attention over every visible compressed entry).  With
+    the hierarchical indexer (``spec.n_cand``) the level-one layer also
+    selects candidate blocks ("DeepSeek V4.1 Flash", hierarchical indexer)
+    and a reindex layer follows: its own scores, top-k inside the candidate
+    blocks, attention (entries ``cand``, ``scores2``, ``topk2``, ``out2``,
+    ``lse2``)."""
     pools, _, _ = compress_step(t, spec)
     rows = range(spec.n_rows) if rows is None else rows
     res = {}
+    t2 = reindex_tensors(t) if spec.n_cand else None
     for row in rows:
         if int(t["row_req"][row]) < 0:
             continue
@@ -103,4 +118,10 @@ def full_step(t, spec, rows=None):
         sel = O.topk_select(s, spec.topk)
         out, lse = attention_row(t, spec, pools, row, sel)
         res[row] = dict(scores=s, topk=sel, out=out, lse=lse)
+        if spec.n_cand:
+            cand = O.select_blocks(s, spec.n_cand, spec.cand_block)
+            s2 = index_row(t2, spec, pools, row)
+            sel2 = O.topk_in_blocks(s2, cand, spec.topk, spec.cand_block)
+            out2, lse2 = attention_row(t2, spec, pools, row, sel2)
+            res[row].update(cand=cand, scores2=s2, topk2=sel2, out2=out2, lse2=lse2)
     return pools, res

@@ -61,6 +61,8 @@ class IndexArgs(ctypes.Structure):
         ("rope_sin", c_void_p), ("rope_cap", c_int32), ("topk_idx", c_void_p),
         ("topk_score", c_void_p), ("scores", c_void_p), ("score_cols", c_int32),
         ("status_dev", c_void_p), ("workspace", c_void_p), ("workspace_bytes", c_size_t),
+        ("cand_block", c_int32), ("n_cand", c_int32), ("cand_out", c_void_p),
+        ("cand_in", c_void_p),
     ]
 
 
@@ -307,8 +309,13 @@ def csa_compress_pair(first: dict, second: dict, *, workspaces=(None, None), str
 def csa_index_topk(*, q_idx, weights, row_req, row_pos, n_cmp, ratio, idx_pool, idx_scale_pool,
                    cmp_block_table, topk, topk_idx, topk_score=None, scores=None, relu=True,
                    rope_cos=None, rope_sin=None, mode=CSA_MODE_AUTO, status=None,
-                   workspace=None, stream=None, prepare=False):
-    """Indexer scores and deterministic top-k (``include/csa.h``: csa_index_topk)."""
+                   cand_out=None, cand_in=None, cand_block=8, workspace=None, stream=None,
+                   prepare=False):
+    """Indexer scores and deterministic top-k (``include/csa.h``: csa_index_topk).
+
+    ``cand_out`` (i32 [n_rows, n_cand]) also selects the level-one candidate
+    blocks; ``cand_in`` restricts scoring and selection to given candidate
+    blocks (reindex)."""
     a = IndexArgs()
     a.struct_size = ctypes.sizeof(IndexArgs)
     a.n_rows = int(q_idx.shape[0])
@@ -334,6 +341,12 @@ def csa_index_topk(*, q_idx, weights, row_req, row_pos, n_cmp, ratio, idx_pool, 
     a.scores = _p(scores, torch.float32, "scores")
     a.score_cols = int(scores.shape[1]) if scores is not None else 0
     a.status_dev = _p(status, torch.int32, "status")
+    cand = cand_out if cand_out is not None else cand_in
+    if cand is not None:
+        a.cand_block = int(cand_block)
+        a.n_cand = int(cand.shape[1])
+        a.cand_out = _p(cand_out, torch.int32, "cand_out")
+        a.cand_in = _p(cand_in, torch.int32, "cand_in")
     return _run("csa_index_topk", a, workspace, stream, q_idx.device, prepare)
 
 

@@ -61,6 +61,20 @@ void launch_end(int kernel_id, cudaStream_t s) {
   }
 }
 
+// The arguments as this library's struct: a caller built against the header
+// without the hierarchical-indexer fields gets neither mode.
+csa_index_args full_index_args(const csa_index_args *a) {
+  csa_index_args f;
+  memset(&f, 0, sizeof(f));
+  memcpy(&f, a, a->struct_size < sizeof(f) ? a->struct_size : sizeof(f));
+  f.struct_size = sizeof(f);
+  return f;
+}
+
+bool index_struct_ok(const csa_index_args *a) {
+  return a && a->struct_size >= offsetof(csa_index_args, cand_block);
+}
+
 }  // namespace csa
 
 using namespace csa;
@@ -210,23 +224,70 @@ CSA_API csa_status_t csa_compress_pair(csa_compress_args *first, csa_compress_ar
 
 // ---------------------------------------------------------------- index + top-k
 
-CSA_API csa_status_t csa_index_topk(csa_index_args *a, csa_stream_t stream) {
-  if (!a || a->struct_size < sizeof(csa_index_args)) return CSA_ERR_INVALID_ARG;
+namespace {
+
+int log2_exact(int x) {
+  int s = 0;
+  while ((1 << s) < x) ++s;
+  return (1 << s) == x ? s : -1;
+}
+
+// Workspace of csa_index_topk: [scores][top-k control][level one: block
+// maxima][level one: block top-k control][reindex: per-row entry counts].
+struct IndexLayout {
+  int row_cap;   // entries of one score row
+  int blk_cols;  // level one: blocks of one row
+  size_t scores, topk, blk, topk2, v_row, total;
+};
+
+IndexLayout index_layout(const csa_index_args &a, bool own_scores) {
+  IndexLayout L{};
+  const int n_cap = a.max_blocks * kBlock;
+  const bool lvl1 = a.cand_out != nullptr, reidx = a.cand_in != nullptr;
+  L.row_cap = reidx ? a.n_cand * a.cand_block : n_cap;
+  L.blk_cols = lvl1 ? n_cap / a.cand_block : 0;
+  size_t off = 0;
+  L.scores = off;
+  off += own_scores ? 0 : align_up((size_t)a.n_rows * L.row_cap * sizeof(float), kAlign);
+  L.topk = off;
+  off += align_up(topk_ws_bytes(a.n_rows, L.row_cap), kAlign);
+  L.blk = off;
+  if (lvl1) off += align_up((size_t)a.n_rows * L.blk_cols * sizeof(float), kAlign);
+  L.topk2 = off;
+  if (lvl1) off += align_up(topk_ws_bytes(a.n_rows, L.blk_cols), kAlign);
+  L.v_row = off;
+  if (reidx) off += align_up((size_t)a.n_rows * sizeof(int32_t), kAlign);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+CSA_API csa_status_t csa_index_topk(csa_index_args *user, csa_stream_t stream) {
+  if (!index_struct_ok(user)) return CSA_ERR_INVALID_ARG;
+  const csa_index_args A = full_index_args(user);
+  const csa_index_args *a = &A;
   if (a->n_rows < 0 || a->n_req < 0) return CSA_ERR_INVALID_ARG;
   if (a->n_heads != kHeads || a->head_dim != kIdxDim) return CSA_ERR_UNSUPPORTED;
   if (a->topk < 1 || a->topk > CSA_MAX_TOPK || a->ratio < 1) return CSA_ERR_INVALID_ARG;
   if (a->max_blocks <= 0) return CSA_ERR_INVALID_ARG;
-  const int n_cap = a->max_blocks * kBlock;
+  const bool lvl1 = a->cand_out != nullptr, reidx = a->cand_in != nullptr;
+  int cb_shift = 3;
+  if (lvl1 || reidx) {
+    if (lvl1 && reidx) return CSA_ERR_INVALID_ARG;
+    if (a->cand_block != 8 && a->cand_block != 16 && a->cand_block != 32)
+      return CSA_ERR_UNSUPPORTED;
+    if (a->n_cand < 1 || a->n_cand > CSA_MAX_TOPK) return CSA_ERR_INVALID_ARG;
+    cb_shift = log2_exact(a->cand_block);
+  }
   const bool own_scores = a->scores != nullptr;
-  if (own_scores && a->score_cols < n_cap) return CSA_ERR_INVALID_ARG;
-  const size_t score_bytes =
-      own_scores ? 0 : align_up((size_t)a->n_rows * n_cap * sizeof(float), kAlign);
-  const size_t need = score_bytes + topk_ws_bytes(a->n_rows, n_cap);
+  const IndexLayout L = index_layout(*a, own_scores);
+  if (own_scores && a->score_cols < L.row_cap) return CSA_ERR_INVALID_ARG;
   if (!a->workspace) {
-    a->workspace_bytes = need;
+    user->workspace_bytes = L.total;
     return CSA_OK;
   }
-  if (a->workspace_bytes < need) return CSA_ERR_INVALID_ARG;
+  if (a->workspace_bytes < L.total) return CSA_ERR_INVALID_ARG;
   if (a->n_rows == 0) return CSA_OK;
   if (!a->q_idx || !a->weights || !a->row_req || !a->row_pos || !a->n_cmp || !a->idx_pool ||
       !a->idx_scale_pool || !a->cmp_block_table || !a->topk_idx)
@@ -237,13 +298,43 @@ CSA_API csa_status_t csa_index_topk(csa_index_args *a, csa_stream_t stream) {
   if (!aligned16(a->idx_pool) || !aligned16(a->q_idx) || !aligned16(a->idx_scale_pool))
     return CSA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float *scores = own_scores ? a->scores : static_cast<float *>(a->workspace);
-  const int cols = own_scores ? a->score_cols : n_cap;
-  void *topk_ws = static_cast<uint8_t *>(a->workspace) + score_bytes;
+  uint8_t *ws = static_cast<uint8_t *>(a->workspace);
+  float *scores = own_scores ? a->scores : reinterpret_cast<float *>(ws + L.scores);
+  const int cols = own_scores ? a->score_cols : L.row_cap;
+  void *topk_ws = ws + L.topk;
+  ScoreSel ss;
+  TopkSel ts;
+  ts.n_cap = L.row_cap;
+  if (reidx) {
+    ss.cand_in = a->cand_in;
+    ss.n_cand = a->n_cand;
+    ss.cb_shift = cb_shift;
+    ss.v_row = reinterpret_cast<int32_t *>(ws + L.v_row);
+    ts.v_row = ss.v_row;
+    ts.cand = a->cand_in;
+    ts.cand_stride = a->n_cand;
+    ts.cb_shift = cb_shift;
+  }
+  if (lvl1) {
+    ss.cb_shift = cb_shift;
+    ss.blk = reinterpret_cast<float *>(ws + L.blk);
+    ss.blk_cols = L.blk_cols;
+    ss.zero2 = topk_counters(ws + L.topk2, a->n_rows, L.blk_cols);
+  }
   cudaError_t e =
-      launch_index_scores(*a, scores, cols, topk_counters(topk_ws, a->n_rows, n_cap), s);
+      launch_index_scores(*a, scores, cols, topk_counters(topk_ws, a->n_rows, L.row_cap), s, ss);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
-  return from_cuda(launch_index_topk(*a, scores, cols, topk_ws, s));
+  e = launch_index_topk(*a, scores, cols, topk_ws, s, ts);
+  if (e != cudaSuccess || !lvl1) return from_cuda(e);
+  // level one: the best n_cand blocks by block maximum
+  csa_index_args B = *a;
+  B.topk = a->n_cand;
+  B.topk_idx = a->cand_out;
+  B.topk_score = nullptr;
+  TopkSel tb;
+  tb.v_div = a->cand_block;
+  tb.n_cap = L.blk_cols;
+  return from_cuda(launch_index_topk(B, ss.blk, L.blk_cols, ws + L.topk2, s, tb));
 }
 
 // ---------------------------------------------------------------- attention

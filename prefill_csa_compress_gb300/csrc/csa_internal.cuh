@@ -72,12 +72,37 @@ cudaError_t launch_compress_pair(const csa_compress_args &a, float *logits_a,
 // Words per row of the long-row top-k control block (barrier counter and
 // three digit histograms).
 constexpr int kTopkCtlWords = 32 + 2048 + 2048 + 1024;
+// Hierarchical-indexer options of the scoring kernel (all off by default).
+struct ScoreSel {
+  const int32_t *cand_in = nullptr;  // reindex: candidate blocks [n_rows, n_cand]
+  int n_cand = 0;
+  int cb_shift = 3;                  // log2(positions per candidate block)
+  int32_t *v_row = nullptr;          // reindex: each row's eligible entry count (written)
+  float *blk = nullptr;              // level one: block maxima [n_rows, blk_cols] (written)
+  int blk_cols = 0;
+  uint32_t *zero2 = nullptr;         // a second control block range to clear (n_rows rows)
+};
+// Options of one top-k launch (all off by default: the indexer's own selection).
+struct TopkSel {
+  int v_div = 1;                     // a row holds ceil(V / v_div) entries (block scores)
+  const int32_t *v_row = nullptr;    // a row holds v_row[t] entries (reindex)
+  const int32_t *cand = nullptr;     // emitted entry i is position cand[t][i >> cb_shift] ...
+  int cand_stride = 0;               // ... << cb_shift | (i & (2^cb_shift - 1))
+  int cb_shift = 3;
+  int n_cap = 0;                     // longest row (0: max_blocks * 128)
+};
 // `zero_ctr` (n_rows x kTopkCtlWords words, may be null) is cleared by the
 // scoring kernel for the top-k kernel that follows it on the stream.
 cudaError_t launch_index_scores(const csa_index_args &a, float *scores, int score_cols,
-                                uint32_t *zero_ctr, cudaStream_t s);
+                                uint32_t *zero_ctr, cudaStream_t s,
+                                const ScoreSel &sel = ScoreSel());
 cudaError_t launch_index_topk(const csa_index_args &a, const float *scores, int score_cols,
-                              void *topk_ws, cudaStream_t s);
+                              void *topk_ws, cudaStream_t s, const TopkSel &sel = TopkSel());
+// The caller's csa_index_args as this library's struct (fields past the
+// caller's struct_size zeroed); index_struct_ok checks that struct_size
+// covers every field before the hierarchical-indexer ones.
+csa_index_args full_index_args(const csa_index_args *a);
+bool index_struct_ok(const csa_index_args *a);
 bool topk_is_long(int n_cap);
 size_t topk_ws_bytes(int n_rows, int n_cap);
 uint32_t *topk_counters(void *ws, int n_rows, int n_cap);

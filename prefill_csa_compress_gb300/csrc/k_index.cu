@@ -173,7 +173,7 @@ template <int NT, int KPT, bool MULTI>
 __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
                                                         const float *__restrict__ scores, int cols,
                                                         int row0, int S, int slice, uint32_t *ctl,
-                                                        uint32_t *rec) {
+                                                        uint32_t *rec, TopkSel sel) {
   constexpr int NW = NT / 32;
   extern __shared__ __align__(16) uint32_t tk_smem[];
   uint32_t *priv = tk_smem;               // [NW][TK_B1]
@@ -187,15 +187,26 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
   const int b = a.row_req[t];
   if (b < 0 || b >= a.n_req) return;  // uniform over the row's CTAs
   const int n_cap = a.max_blocks * kBlock;
-  const int V = min(visible_count(a.row_pos[t], a.ratio, a.n_cmp[b]), n_cap);
+  int V = min(visible_count(a.row_pos[t], a.ratio, a.n_cmp[b]), n_cap);
+  if (sel.v_row)
+    V = sel.v_row[t];
+  else if (sel.v_div > 1)
+    V = (V + sel.v_div - 1) / sel.v_div;
+  V = max(0, min(V, sel.n_cap));
   const int k = a.topk;
   int32_t *out = a.topk_idx + (long long)t * k;
   float *out_s = a.topk_score ? a.topk_score + (long long)t * k : nullptr;
   const float *sc = scores + (long long)t * cols;
+  // entry i of the row -> the position it stands for
+  const int32_t *cand = sel.cand ? sel.cand + (long long)t * sel.cand_stride : nullptr;
+  const int cb_mask = (1 << sel.cb_shift) - 1;
+  auto position = [&](int i) {
+    return cand ? (cand[i >> sel.cb_shift] << sel.cb_shift) | (i & cb_mask) : i;
+  };
   if (V <= k) {
     if (s == 0)
       for (int i = tid; i < k; i += NT) {
-        out[i] = i < V ? i : -1;
+        out[i] = i < V ? position(i) : -1;
         if (out_s) out_s[i] = i < V ? sc[i] : -INFINITY;
       }
     return;
@@ -356,7 +367,7 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
   }
   __syncthreads();
   for (int i = tid; i < n_take; i += NT) {
-    out[offset + i] = st_idx[i];
+    out[offset + i] = position(st_idx[i]);
     if (out_s) out_s[offset + i] = key_score(st_key[i]);
   }
 }
@@ -391,7 +402,8 @@ cudaError_t allow_smem(K kern, int bytes, bool *done) {
 }
 
 template <int NT>
-cudaError_t launch_short(const csa_index_args &a, const float *scores, int cols, cudaStream_t s) {
+cudaError_t launch_short(const csa_index_args &a, const float *scores, int cols, cudaStream_t s,
+                         const TopkSel &sel) {
   static bool done[64] = {};
   const auto kern = topk_radix_kernel<NT, TK_SHORT_KPT, false>;
   constexpr int smem = topk_smem_bytes<NT>();
@@ -401,7 +413,7 @@ cudaError_t launch_short(const csa_index_args &a, const float *scores, int cols,
   for (int row0 = 0; row0 < a.n_rows && e == cudaSuccess; row0 += kMaxGridY)
     e = launch_kernel(kern, dim3(1, std::min(kMaxGridY, a.n_rows - row0)), dim3(NT),
                       (size_t)smem, s, 0, false, a, scores, cols, row0, 1, NT * TK_SHORT_KPT,
-                      static_cast<uint32_t *>(nullptr), static_cast<uint32_t *>(nullptr));
+                      static_cast<uint32_t *>(nullptr), static_cast<uint32_t *>(nullptr), sel);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -447,15 +459,18 @@ uint32_t *topk_counters(void *ws, int n_rows, int n_cap) {
 }
 
 cudaError_t launch_index_topk(const csa_index_args &a, const float *scores, int score_cols,
-                              void *topk_ws, cudaStream_t s) {
+                              void *topk_ws, cudaStream_t s, const TopkSel &sel_in) {
   if (a.n_rows <= 0) return cudaSuccess;
-  const int n_cap = a.max_blocks * kBlock;
+  TopkSel sel = sel_in;
+  if (sel.n_cap <= 0) sel.n_cap = a.max_blocks * kBlock;
+  const int n_cap = sel.n_cap;
   if (!topk_is_long(n_cap)) {
     // the smallest CTA whose threads hold a whole row, 16 entries each
     launch_begin(CSA_K_INDEX_TOPK, s);
-    const cudaError_t e = n_cap <= 128 * TK_SHORT_KPT   ? launch_short<128>(a, scores, score_cols, s)
-                          : n_cap <= 256 * TK_SHORT_KPT ? launch_short<256>(a, scores, score_cols, s)
-                                                        : launch_short<512>(a, scores, score_cols, s);
+    const cudaError_t e =
+        n_cap <= 128 * TK_SHORT_KPT   ? launch_short<128>(a, scores, score_cols, s, sel)
+        : n_cap <= 256 * TK_SHORT_KPT ? launch_short<256>(a, scores, score_cols, s, sel)
+                                      : launch_short<512>(a, scores, score_cols, s, sel);
     launch_end(CSA_K_INDEX_TOPK, s);
     return e;
   }
@@ -485,7 +500,7 @@ cudaError_t launch_index_topk(const csa_index_args &a, const float *scores, int 
   for (int row0 = 0; row0 < a.n_rows && e == cudaSuccess; row0 += rows_per_launch) {
     const int nr = std::min(rows_per_launch, a.n_rows - row0);
     e = launch_kernel(kern, dim3(S, nr), dim3(TK_LONG_THREADS), (size_t)smem, s, 0, true, aa, sp,
-                      cols, row0, S, slice, ctl, rec);
+                      cols, row0, S, slice, ctl, rec, sel);
   }
   launch_end(CSA_K_INDEX_TOPK, s);
   return e != cudaSuccess ? e : cudaGetLastError();

@@ -89,6 +89,7 @@ struct IdxMisc {
   int row_V[4];
   int row_on[4];
   int row_p[4];
+  int cand_min;
 };
 
 __device__ __forceinline__ void set_abort(IdxMisc *m, uint32_t *status) {
@@ -121,11 +122,35 @@ __device__ __forceinline__ void named_barrier(int id, int n_threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n_threads) : "memory");
 }
 
+// Reindex ("DeepSeek V4.1 Flash", hierarchical indexer): the number of
+// leading entries of a candidate list c[0..n) that are strictly ascending
+// blocks in [0, nb).  Entries after that prefix other than -1 raise
+// CSA_DEV_BAD_INDEX.  Called by every thread of the CTA.
+__device__ int candidate_prefix(const int32_t *c, int n, int nb, int *s_min, uint32_t *status) {
+  if (threadIdx.x == 0) *s_min = n;
+  __syncthreads();
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const int x = c[j];
+    if (x < 0 || x >= nb || (j > 0 && x <= c[j - 1])) {
+      atomicMin(s_min, j);
+      break;
+    }
+  }
+  __syncthreads();
+  const int nv = *s_min;
+  for (int j = nv + threadIdx.x; j < n; j += blockDim.x)
+    if (c[j] != -1) {
+      flag(status, CSA_DEV_BAD_INDEX);
+      break;
+    }
+  return nv;
+}
+
 template <int G>
 __global__ void __launch_bounds__(IT_THREADS, 1)
     index_score_tc_kernel(csa_index_args a, float *__restrict__ scores, int cols, int n_groups,
                           int chunk_tiles, int units_per_group, uint32_t *zero_ctr,
-                          const __grid_constant__ CUtensorMap keys_map) {
+                          const __grid_constant__ CUtensorMap keys_map, ScoreSel sel) {
   using C = IdxTc<G>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -142,12 +167,18 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   tc::griddep_launch_dependents();
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  if (zero_ctr) {
-    const long long n_words = (long long)a.n_rows * kTopkCtlWords;
+  const long long n_words = (long long)a.n_rows * kTopkCtlWords;
+  for (int z = 0; z < 2; ++z) {
+    uint32_t *ctr = z == 0 ? zero_ctr : sel.zero2;
+    if (!ctr) continue;
     for (long long i = (long long)blockIdx.x * IT_THREADS + tid; i < n_words;
          i += (long long)gridDim.x * IT_THREADS)
-      zero_ctr[i] = 0u;
+      ctr[i] = 0u;
   }
+  // reindex: each row is a pass of its own over its candidate blocks, 128
+  // candidate entries (128 >> cb_shift blocks) per tile
+  const bool reidx = sel.cand_in != nullptr;
+  const int cb = 1 << sel.cb_shift;
   const bool rope = a.rope_cos != nullptr;
   const int n_kchunks = rope ? 3 : 2;
   const int n_cap = a.max_blocks * kBlock;
@@ -193,24 +224,42 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
     for (int pi = 0; pi < G; ++pi) {
       const int b = rb[pi];
       bool first = b >= 0;
-      for (int j = 0; j < pi; ++j) first = first && rb[j] != b;
+      if (!reidx)
+        for (int j = 0; j < pi; ++j) first = first && rb[j] != b;
       if (!first) continue;
 
       // ---------------- pass start (all roles have finished the previous pass)
       __syncthreads();
       if (M->abort) break;
       int vmax = 0;
+      unsigned on_mask = 0;  // rows of this pass
 #pragma unroll
       for (int i = 0; i < G; ++i) {
         const int t = g * G + i;
         int V = 0;
-        const bool on = rb[i] == b;
+        const bool on = reidx ? i == pi : rb[i] == b;
         if (on) V = min(visible_count(a.row_pos[t], a.ratio, a.n_cmp[b]), n_cap);
+        on_mask |= on ? 1u << i : 0u;
         vmax = max(vmax, V);
         if (tid == 0) {
           M->row_t[i] = t;
           M->row_V[i] = V;
           M->row_on[i] = on;
+        }
+      }
+      const int32_t *cand = nullptr;
+      if (reidx) {
+        // the row's eligible entries: its valid candidate blocks, all fully
+        // visible but the last, which may be cut by V
+        const int t = g * G + pi, V = vmax;
+        cand = sel.cand_in + (long long)t * sel.n_cand;
+        const int nv = candidate_prefix(cand, sel.n_cand, (V + cb - 1) >> sel.cb_shift,
+                                        &M->cand_min, a.status_dev);
+        const int Vc = nv == 0 ? 0 : (nv - 1) * cb + min(cb, V - (cand[nv - 1] << sel.cb_shift));
+        vmax = Vc;
+        if (tid == 0) {
+          M->row_V[pi] = Vc;
+          if (chunk == 0 && sel.v_row) sel.v_row[t] = Vc;
         }
       }
       const int tiles_total = (vmax + kBlock - 1) / kBlock;
@@ -225,7 +274,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
         for (int e = bt; e < 16 * C::N; e += IT_BUILD) {
           const int n = e / 16, part = (e / 8) % 2, jj = e % 8;
           const int i = n / kHeads, h = n % kHeads;
-          if (rb[i] == b)
+          if ((on_mask >> i) & 1u)
             tc::cp_async16(Bs + part * C::B_CHUNK + n * 128 + ((jj ^ (n & 7)) << 4),
                            static_cast<const uint16_t *>(a.q_idx) +
                                ((long long)(g * G + i) * kHeads + h) * kIdxDim + part * 64 +
@@ -235,7 +284,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
         for (int e = bt; e < G * (kHeads + 64); e += IT_BUILD) {
           const int i = e / (kHeads + 64), f = e % (kHeads + 64);
           const int t = g * G + i;
-          if (rb[i] != b) continue;
+          if (!((on_mask >> i) & 1u)) continue;
           const int p = a.row_pos[t];
           if (f < kHeads) {
             Ws[i * kHeads + f] = a.weights[(long long)t * kHeads + f];
@@ -256,7 +305,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
           const bool live = e < 16 * C::N;
           const int n = live ? e / 16 : 0, part = (e / 8) % 2, jj = e % 8;
           const int i = n / kHeads;
-          const bool on = live && rb[i] == b;
+          const bool on = live && ((on_mask >> i) & 1u);
           uint8_t *d = Bs + part * C::B_CHUNK + n * 128 + ((jj ^ (n & 7)) << 4);
           float x[8];
           float mx = 0.f;
@@ -334,11 +383,52 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
               break;
             }
             const int tile = tb + k;
+            if (reidx) {
+              // the tile's candidate blocks, each a run of cb rows of one page;
+              // st_ok holds one bit per 8 rows that arrive
+              const int nbt = kBlock >> sel.cb_shift, j0 = tile * nbt;
+              int phys_j[kBlock / 8], row_j[kBlock / 8];
+              unsigned mask = 0;
+              int n_ok = 0;
+              for (int jj = 0; jj < nbt; ++jj) {
+                phys_j[jj] = -1;
+                if ((j0 + jj) * cb >= vmax) continue;
+                const int pos0 = cand[j0 + jj] << sel.cb_shift;
+                const int page = pos0 / kBlock;
+                const int ph = a.cmp_block_table[(long long)b * a.max_blocks + page];
+                if (ph < 0 || ph >= a.n_blocks) {
+                  flag(a.status_dev, CSA_DEV_BAD_BLOCK);
+                  continue;
+                }
+                phys_j[jj] = ph;
+                row_j[jj] = pos0 % kBlock;
+                mask |= ((1u << (cb / 8)) - 1u) << (jj * cb / 8);
+                ++n_ok;
+              }
+              M->st_ok[s] = (int)mask;
+              if (n_ok) {
+                tc::mbar_arrive_expect_tx(&M->st_full[s], n_ok * cb * (kIdxDim + 4));
+                for (int jj = 0; jj < nbt; ++jj) {
+                  if (phys_j[jj] < 0) continue;
+                  const long long grow = (long long)phys_j[jj] * kBlock + row_j[jj];
+                  uint8_t *dst = St + s * C::PAGE + jj * cb * kIdxDim;
+                  if constexpr (C::ATMEM)
+                    tc::tma_load_2d(dst, &keys_map, 0, (int)grow, &M->st_full[s]);
+                  else
+                    tc::bulk_g2s(dst, a.idx_pool + grow * kIdxDim, cb * kIdxDim, &M->st_full[s]);
+                  tc::bulk_g2s(StSc + s * kBlock + jj * cb, a.idx_scale_pool + grow, cb * 4,
+                               &M->st_full[s]);
+                }
+              } else {
+                tc::mbar_arrive(&M->st_full[s]);
+              }
+              continue;
+            }
             const int phys = tile < a.max_blocks
                                  ? a.cmp_block_table[(long long)b * a.max_blocks + tile]
                                  : -1;
             const bool ok = phys >= 0 && phys < a.n_blocks;
-            M->st_ok[s] = ok;
+            M->st_ok[s] = ok ? 0xFFFF : 0;
             if (ok) {
               tc::mbar_arrive_expect_tx(&M->st_full[s], C::PAGE + kBlock * 4);
               if constexpr (C::ATMEM)  // 128-byte swizzled rows: conflict-free row reads
@@ -482,7 +572,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
             break;
           }
           tc::tc_fence_after();
-          const int ok = M->t_ok[sc];
+          const bool ok = (M->t_ok[sc] >> (r >> 3)) & 1;
           const float scale = Sc[sc * kBlock + r];
           const int c = (tb + k) * kBlock + r;
 #pragma unroll
@@ -504,8 +594,17 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
               acc1 = tc::ffma2(make_float2(w.z, w.w), make_float2(x[2], x[3]), acc1);
             }
             const float sum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
-            if (c < M->row_V[i])
-              scores[(long long)M->row_t[i] * cols + c] = ok ? scale * sum : -INFINITY;
+            const bool vis = c < M->row_V[i];
+            const float val = ok ? scale * sum : -INFINITY;
+            if (vis) scores[(long long)M->row_t[i] * cols + c] = val;
+            if (sel.blk) {
+              // level one: the maximum over each block's visible entries (a
+              // block is cb consecutive lanes)
+              float m = vis ? val : -INFINITY;
+              for (int o = 1; o < cb; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+              if (vis && (lane & (cb - 1)) == 0)
+                sel.blk[(long long)M->row_t[i] * sel.blk_cols + (c >> sel.cb_shift)] = m;
+            }
           }
           tc::tc_fence_before();
           tc::mbar_arrive(&M->acc_empty[q4]);
@@ -543,8 +642,8 @@ int sm_count() {
 }
 
 // Tensor map of the INT8 key pool as a 2D [pages * 128 rows, 128 bytes] array,
-// one page per box, 128-byte swizzle.
-bool encode_keys_map(const csa_index_args &a, CUtensorMap *map) {
+// `box_rows` rows (a page, or one candidate block) per box, 128-byte swizzle.
+bool encode_keys_map(const csa_index_args &a, int box_rows, CUtensorMap *map) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     cudaDriverEntryPointQueryResult q;
@@ -557,7 +656,7 @@ bool encode_keys_map(const csa_index_args &a, CUtensorMap *map) {
   }
   const cuuint64_t dims[2] = {(cuuint64_t)kIdxDim, (cuuint64_t)a.n_blocks * kBlock};
   const cuuint64_t strides[1] = {(cuuint64_t)kIdxDim};
-  const cuuint32_t box[2] = {(cuuint32_t)kIdxDim, (cuuint32_t)kBlock};
+  const cuuint32_t box[2] = {(cuuint32_t)kIdxDim, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(a.idx_pool), dims,
                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -567,11 +666,13 @@ bool encode_keys_map(const csa_index_args &a, CUtensorMap *map) {
 
 template <int G>
 cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, uint32_t *zero_ctr,
-                      cudaStream_t s) {
+                      cudaStream_t s, const ScoreSel &sel) {
   using C = IdxTc<G>;
+  const bool reidx = sel.cand_in != nullptr;
   CUtensorMap keys_map;
   memset(&keys_map, 0, sizeof(keys_map));
-  if (C::ATMEM && !encode_keys_map(a, &keys_map)) return cudaErrorInvalidValue;
+  if (C::ATMEM && !encode_keys_map(a, reidx ? 1 << sel.cb_shift : kBlock, &keys_map))
+    return cudaErrorInvalidValue;
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -583,7 +684,9 @@ cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, uint32_t
   }
   const int sms = sm_count();
   const int n_groups = (a.n_rows + G - 1) / G;
-  const int max_tiles = a.max_blocks;
+  // tiles of one row: its pages, or (reindex) its candidate entries / 128
+  const int max_tiles =
+      reidx ? ((sel.n_cand << sel.cb_shift) + kBlock - 1) / kBlock : a.max_blocks;
   int upg = (sms + n_groups - 1) / n_groups;
   upg = max(1, min(upg, max_tiles));
   const int chunk = (max_tiles + upg - 1) / upg;
@@ -593,7 +696,7 @@ cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, uint32_t
   launch_begin(CSA_K_INDEX_SCORE, s);
   const cudaError_t e = launch_kernel(index_score_tc_kernel<G>, dim3(grid), dim3(IT_THREADS),
                                       (size_t)C::SMEM, s, 0, false, a, scores, cols, n_groups,
-                                      chunk, upg, zero_ctr, keys_map);
+                                      chunk, upg, zero_ctr, keys_map, sel);
   launch_end(CSA_K_INDEX_SCORE, s);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -601,11 +704,11 @@ cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, uint32_t
 }  // namespace
 
 cudaError_t launch_index_scores(const csa_index_args &a, float *scores, int score_cols,
-                                uint32_t *zero_ctr, cudaStream_t s) {
+                                uint32_t *zero_ctr, cudaStream_t s, const ScoreSel &sel) {
   if (a.n_rows <= 0) return cudaSuccess;
   const bool wide = a.mode == CSA_MODE_PREFILL || (a.mode == CSA_MODE_AUTO && a.n_rows > 64);
-  return wide ? launch_tc<4>(a, scores, score_cols, zero_ctr, s)
-              : launch_tc<2>(a, scores, score_cols, zero_ctr, s);
+  return wide ? launch_tc<4>(a, scores, score_cols, zero_ctr, s, sel)
+              : launch_tc<2>(a, scores, score_cols, zero_ctr, s, sel);
 }
 
 }  // namespace csa

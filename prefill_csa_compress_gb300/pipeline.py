@@ -9,6 +9,13 @@ short chunks), and every call of the step is issued on one stream, where each
 kernel is launched as a programmatic dependent of the one before it.
 ``capture`` records a whole step as a CUDA graph so that a repeated step
 costs one launch on the host.
+
+The hierarchical indexer ("DeepSeek V4.1 Flash": a level-one layer selects
+candidate blocks of compressed positions; later reindex layers compute their
+own index query but select only inside those blocks) is a ``CsaStep`` with
+``n_cand`` (level one: it also fills ``cand``) followed by a ``CsaStep`` with
+``cand_in`` (reindex: no compressors, the first layer's caches); ``StepChain``
+issues such layers back to back as one step.
 """
 
 from __future__ import annotations
@@ -26,11 +33,15 @@ class CsaStep:
     idx_w, sink, kv_raw, idx_raw, w_gate, ape, w_gate_i, ape_i, rope_cos,
     rope_sin, and optionally the compressors' state rings state_main,
     state_idx with state_table.  ``ratio``, ``topk``, ``prefill`` and
-    ``dense`` (HCA) describe the step.
+    ``dense`` (HCA) describe the step; ``n_cand`` > 0 makes the indexer also
+    select that many candidate blocks of ``cand_block`` positions into
+    ``cand`` (level one), and ``cand_in`` restricts it to given candidate
+    blocks (reindex).
     """
 
     def __init__(self, t: dict, ratio: int, topk: int, prefill: bool = False,
-                 compress: bool = True, status: bool = True, dense: bool = False):
+                 compress: bool = True, status: bool = True, dense: bool = False,
+                 n_cand: int = 0, cand_block: int = 8, cand_in=None, status_buf=None):
         self.t = t
         self.ratio = int(ratio)
         self.topk = int(topk)
@@ -45,7 +56,12 @@ class CsaStep:
         self.topk_score = torch.empty((T, self.topk), dtype=torch.float32, device=dev)
         self.out = torch.zeros_like(t["q"])
         self.lse = torch.zeros(t["q"].shape[:2], dtype=torch.float32, device=dev)
-        self.status = torch.zeros(1, dtype=torch.int32, device=dev) if status else None
+        self.status = status_buf if status_buf is not None else (
+            torch.zeros(1, dtype=torch.int32, device=dev) if status else None)
+        self.cand_block = int(cand_block)
+        self.cand = (torch.full((T, int(n_cand)), -1, dtype=torch.int32, device=dev)
+                     if n_cand else None)
+        self.cand_in = cand_in
         self.ws = {}
         self._prepared = None
         self._graph = None
@@ -77,16 +93,20 @@ class CsaStep:
         self.ws["cp"] = B.csa_compress_pair(main, keys, workspaces=self.ws.get("cp", (None, None)),
                                             stream=stream)
 
-    def index(self, stream=None, scores=None):
+    def _index_kw(self):
         t = self.t
-        self.ws["ix"] = B.csa_index_topk(
+        return dict(
             q_idx=t["q_idx"], weights=t["idx_w"], row_req=t["row_req"], row_pos=t["row_pos"],
             n_cmp=t["n_cmp"], ratio=self.ratio, idx_pool=t["idx_pool"],
             idx_scale_pool=t["idx_scale"], cmp_block_table=t["cmp_table"], topk=self.topk,
-            topk_idx=self.topk_idx, topk_score=self.topk_score, scores=scores,
-            rope_cos=t["rope_cos"], rope_sin=t["rope_sin"],
+            topk_idx=self.topk_idx, topk_score=self.topk_score, rope_cos=t["rope_cos"],
+            rope_sin=t["rope_sin"],
             mode=B.CSA_MODE_PREFILL if self.prefill else B.CSA_MODE_DECODE, status=self.status,
-            workspace=self._ws("ix"), stream=stream)
+            cand_out=self.cand, cand_in=self.cand_in, cand_block=self.cand_block)
+
+    def index(self, stream=None, scores=None):
+        self.ws["ix"] = B.csa_index_topk(scores=scores, workspace=self._ws("ix"), stream=stream,
+                                         **self._index_kw())
 
     def _selection(self, topk_idx=None):
         if topk_idx is not None:
@@ -113,14 +133,7 @@ class CsaStep:
             calls.append(B.csa_compress(prepare=True, **main) if self.dense else
                          B.csa_compress_pair(main, keys, prepare=True))
         if not self.dense:
-            calls.append(B.csa_index_topk(
-                q_idx=t["q_idx"], weights=t["idx_w"], row_req=t["row_req"], row_pos=t["row_pos"],
-                n_cmp=t["n_cmp"], ratio=self.ratio, idx_pool=t["idx_pool"],
-                idx_scale_pool=t["idx_scale"], cmp_block_table=t["cmp_table"], topk=self.topk,
-                topk_idx=self.topk_idx, topk_score=self.topk_score, rope_cos=t["rope_cos"],
-                rope_sin=t["rope_sin"],
-                mode=B.CSA_MODE_PREFILL if self.prefill else B.CSA_MODE_DECODE, status=self.status,
-                prepare=True))
+            calls.append(B.csa_index_topk(prepare=True, **self._index_kw()))
         fn = B.csa_sparse_attn_prefill if self.prefill else B.csa_sparse_attn_decode
         calls.append(fn(
             q=t["q"], row_req=t["row_req"], row_pos=t["row_pos"], topk_idx=self._selection(),
@@ -149,6 +162,52 @@ class CsaStep:
         then launches the whole step at once.  Call after a warm-up ``run``."""
         if self._prepared is None:
             self.prepare()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            self.run()
+        self._graph = g
+        return self
+
+    def replay(self):
+        self._graph.replay()
+
+    def drop_graph(self):
+        self._graph = None
+
+
+class StepChain:
+    """Layers issued back to back on one stream as one step (e.g. a level-one
+    layer and the reindex layer that consumes its candidate blocks)."""
+
+    def __init__(self, steps):
+        self.steps = list(steps)
+        self._graph = None
+
+    @property
+    def status(self):
+        return self.steps[0].status
+
+    @property
+    def out(self):
+        return self.steps[-1].out
+
+    @property
+    def lse(self):
+        return self.steps[-1].lse
+
+    def prepare(self):
+        for s in self.steps:
+            s.prepare()
+        return self
+
+    def run(self, stream=None):
+        for s in self.steps:
+            s.run(stream)
+
+    def capture(self):
+        for s in self.steps:
+            if s._prepared is None:
+                s.prepare()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, capture_error_mode="thread_local"):
             self.run()

@@ -137,6 +137,31 @@ def test_workspace_queries_and_validation(L):
     ia.topk, ia.n_heads = 512, 32
     assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_ERR_UNSUPPORTED
 
+    # hierarchical indexer: level one adds the block maxima; reindex rows hold
+    # n_cand * cand_block candidate entries plus one count per row
+    ia.n_heads, ia.max_blocks = 64, 16
+    buf = ctypes.create_string_buffer(64)
+    ia.cand_block, ia.n_cand, ia.cand_out = 8, 64, ctypes.addressof(buf)
+    assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_OK
+    assert ia.workspace_bytes == 8 * 2048 * 4 + 8 * 256 * 4
+    ia.cand_out, ia.cand_in = None, ctypes.addressof(buf)
+    assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_OK
+    assert ia.workspace_bytes == 8 * 512 * 4 + 256
+    ia.cand_block = 12
+    assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_ERR_UNSUPPORTED
+    ia.cand_block, ia.n_cand = 8, 4096
+    assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_ERR_INVALID_ARG
+    ia.n_cand, ia.cand_out = 64, ctypes.addressof(buf)  # both modes at once
+    assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_ERR_INVALID_ARG
+    ia.cand_in = None
+    assert L.csa_index_topk_noalloc(ctypes.byref(ia), None) == b.CSA_ERR_UNSUPPORTED
+    # a caller built without the hierarchical fields gets neither mode
+    ia.struct_size = b.IndexArgs.cand_block.offset
+    assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_OK
+    assert ia.workspace_bytes == 8 * 2048 * 4
+    ia.struct_size = b.IndexArgs.cand_block.offset - 8
+    assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_ERR_INVALID_ARG
+
     aa = b.AttnArgs()
     aa.struct_size = ctypes.sizeof(aa)
     aa.n_rows, aa.n_heads, aa.head_dim, aa.ratio, aa.topk, aa.window = 8, 64, 512, 4, 2048, 128

@@ -27,6 +27,7 @@ from .gen import (  # noqa: F401
     WorkloadSpec,
     make_workload,
     random_selection,
+    reindex_view,
     rope_tables,
     spec_for,
 )

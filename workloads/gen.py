@@ -43,6 +43,11 @@ class WorkloadSpec:
     pad_rows: int = 0  # trailing padding rows (row_req = -1)
     state: bool = False  # compressors keep a recurrent state ring (capacity max(4, ratio))
     dense: bool = False  # HCA: no indexer, attention over every visible compressed entry
+    # hierarchical indexer: a level-one layer selects n_cand blocks of
+    # cand_block compressed positions and a reindex layer (its own q, q_idx,
+    # idx_w and sink: q2, q_idx2, idx_w2, sink2) selects inside them; 0 = off
+    n_cand: int = 0
+    cand_block: int = 8
     extra: dict = field(default_factory=dict)
 
     @property
@@ -87,6 +92,11 @@ CONFIGS = {
     # 4 requests x 2 rows at 1,048,576 positions, ratio 4, top-k 2048.
     "million_decode": WorkloadSpec("million_decode", [1048576] * 4, [2] * 4, ratio=4, topk=2048,
                                    seed=4, kv_pages="window"),
+    # the hierarchical indexer at 1,048,576 positions: a level-one layer (ratio
+    # 4, top-k 512) also picks 2,048 blocks of 8 compressed positions; a
+    # reindex layer selects its 512 inside them.  4 requests x 2 rows.
+    "hier_decode": WorkloadSpec("hier_decode", [1048576] * 4, [2] * 4, ratio=4, topk=512,
+                                seed=8, kv_pages="window", n_cand=2048, cand_block=8),
 }
 
 
@@ -249,7 +259,23 @@ def make_workload(spec: WorkloadSpec) -> Workload:
             score_part = torch.from_numpy(
                 (rng.standard_normal((B + 1, cap, d)) * 1.4).astype(np.float32))
             t[name] = torch.cat([kv_part, score_part], dim=2).contiguous()
+    if spec.n_cand:
+        # the reindex layer's own activations and sink
+        t["q2"] = _normal_bf16(rng, (T, spec.heads, Dm))
+        t["q_idx2"] = _normal_bf16(rng, (T, spec.idx_heads, Di))
+        t["idx_w2"] = torch.from_numpy(
+            (rng.standard_normal((T, spec.idx_heads)) / 8.0).astype(np.float32))
+        t["sink2"] = torch.from_numpy(rng.standard_normal(spec.heads).astype(np.float32))
     return Workload(spec=spec, t=t)
+
+
+def reindex_view(t: dict) -> dict:
+    """The tensors of the reindex layer: the level-one layer's caches and
+    tables with the reindex layer's own q, q_idx, idx_w and sink."""
+    r = dict(t)
+    for k in ("q", "q_idx", "idx_w", "sink"):
+        r[k] = t[k + "2"]
+    return r
 
 
 def random_selection(limits, k, seed):
