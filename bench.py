@@ -4,7 +4,9 @@ One step = one pass of the whole path over one batch: the main compressor,
 the index-key compressor, the indexer top-k and the sparse attention (decode
 or prefill).  Default workload: serving decode (4 requests x 2 rows, contexts
 8192/6000/4097/2048, ratio 2, top-k 512).  Other workloads: --workload
-tiny_decode | ratio1_decode | chunked_prefill | million_decode.
+tiny_decode | ratio1_decode | chunked_prefill | million_decode |
+stateful_decode | hca_decode | hca_prefill | hier_decode (a level-one layer
+and a reindex layer of the hierarchical indexer as one step).
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 the host cores instead (a bounded sample of the same workload).
@@ -121,6 +123,22 @@ def algorithmic_work(wl):
                       len(rows) * H * D * 2 * 2 + sum(sel) * 4)
     attn_flops = sum(4 * H * D * (k + w) for k, w in zip(sel, win))
     topk_bytes = sum(vis) * 4 + len(rows) * s.topk * 8
+    if s.n_cand:
+        # hierarchical indexer: the level-one layer also writes each row's block
+        # maxima and selects n_cand blocks; the reindex layer reads each row's
+        # candidate keys (Vc entries), selects among them and attends again
+        cb = s.cand_block
+        nblk = [(v + cb - 1) // cb for v in vis]
+        vc = [min(v, s.n_cand * cb) for v in vis]
+        sel2 = [min(s.topk, v) for v in vc]
+        idx_bytes += (sum(nblk) * 4 + sum(v * (Di + 4) for v in vc) +
+                      len(rows) * (Hi * (Di * 2 + 4) + s.n_cand * 4))
+        idx_flops += sum(2 * Hi * Di * v for v in vc)
+        topk_bytes += (sum(nblk) * 4 + len(rows) * s.n_cand * 4 +
+                       sum(vc) * 4 + len(rows) * s.topk * 8)
+        attn_bytes += (sum(sel2) * D * 2 + len(req_vis) * (W + 1) * D * 2 +
+                       len(rows) * H * D * 2 * 2 + sum(sel2) * 4)
+        attn_flops += sum(4 * H * D * (k + w) for k, w in zip(sel2, win))
     # compressors (main: x, kv [T, D] BF16 -> BF16 rows; index keys: [T, Di] ->
     # INT8 rows + FP32 scale); a group is r consecutive rows of one request
     # ending at a position p with p % r == r - 1
@@ -278,12 +296,17 @@ def oracle_sample(wl, budget_s=10.0, max_rows=None):
     t_comp = time.perf_counter() - t0
     done = 0
     t1 = time.perf_counter()
+    from oracle import select_blocks, topk_in_blocks, topk_select
+
+    t2 = OS.reindex_tensors(wl.t) if s.n_cand else None
     for row in rows:
         sc = OS.index_row(wl.t, s, pools, row)
-        from oracle import topk_select
-
         sel = topk_select(sc, s.topk)
         OS.attention_row(wl.t, s, pools, row, sel)
+        if s.n_cand:  # level-one blocks, then the reindex layer
+            cand = select_blocks(sc, s.n_cand, s.cand_block)
+            sc2 = OS.index_row(t2, s, pools, row)
+            OS.attention_row(t2, s, pools, row, topk_in_blocks(sc2, cand, s.topk, s.cand_block))
         done += 1
         if time.perf_counter() - t1 > budget_s:
             break
@@ -313,11 +336,14 @@ def run_reference(args, wl):
 
 def _config(wl, args):
     s = wl.spec
-    return {"workload": s.name, "requests": s.n_req, "rows": s.n_rows, "contexts": s.ctx,
-            "ratio": s.ratio, "topk": s.topk, "heads": s.heads, "head_dim": s.head_dim,
-            "idx_heads": s.idx_heads, "idx_dim": s.idx_dim, "window": s.window,
-            "l2": "flushed before every timed step (256 MiB write)",
-            "parallelism": f"replicas x{args.gpus}"}
+    c = {"workload": s.name, "requests": s.n_req, "rows": s.n_rows, "contexts": s.ctx,
+         "ratio": s.ratio, "topk": s.topk, "heads": s.heads, "head_dim": s.head_dim,
+         "idx_heads": s.idx_heads, "idx_dim": s.idx_dim, "window": s.window,
+         "l2": "flushed before every timed step (256 MiB write)",
+         "parallelism": f"replicas x{args.gpus}"}
+    if s.n_cand:
+        c.update(layers=["level-one", "reindex"], n_cand=s.n_cand, cand_block=s.cand_block)
+    return c
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -353,7 +379,19 @@ def run_gpu(args, wl, rank, world, local_rank):
     s = wl.spec
     t = wl.to(dev)
     prefill = s.mode == "prefill"
-    step = CsaStep(t, s.ratio, s.topk, prefill=prefill, dense=s.dense).prepare()
+    if s.n_cand:
+        # hierarchical indexer: a level-one layer, then a reindex layer over
+        # the same caches with its own activations
+        from prefill_csa_compress_gb300.pipeline import StepChain
+        from workloads import reindex_view
+
+        s1 = CsaStep(t, s.ratio, s.topk, prefill=prefill, n_cand=s.n_cand,
+                     cand_block=s.cand_block)
+        s2 = CsaStep(reindex_view(t), s.ratio, s.topk, prefill=prefill, compress=False,
+                     cand_in=s1.cand, cand_block=s.cand_block, status_buf=s1.status)
+        step = StepChain([s1, s2]).prepare()
+    else:
+        step = CsaStep(t, s.ratio, s.topk, prefill=prefill, dense=s.dense).prepare()
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     work = algorithmic_work(wl)
@@ -434,6 +472,8 @@ def run_gpu(args, wl, rank, world, local_rank):
     # ---- end to end through the public API with host buffers
     per_step_inputs = ["q", "q_idx", "idx_w", "kv_raw", "idx_raw", "row_req", "row_pos",
                        "kv_len", "n_cmp"]
+    if s.n_cand:
+        per_step_inputs += ["q2", "q_idx2", "idx_w2"]
     host_in = {k: wl.t[k].pin_memory() for k in per_step_inputs}
     host_out = step.out.cpu().pin_memory()
     host_lse = step.lse.cpu().pin_memory()

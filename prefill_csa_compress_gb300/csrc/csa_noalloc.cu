@@ -47,9 +47,9 @@ extern "C" CSA_API csa_status_t csa_index_topk_noalloc(csa_index_args *user,
   if (a->topk < 1 || a->topk > CSA_MAX_TOPK || a->ratio < 1 || a->max_blocks <= 0)
     return CSA_ERR_INVALID_ARG;
   const long long n_cap = (long long)a->max_blocks * kBlock;
-  // only the single-CTA top-k (rows of at most 8192 entries) runs without
-  // further scratch; the scores must fit the static array
-  if (topk_is_long((int)n_cap)) return CSA_ERR_UNSUPPORTED;
+  // only the single-CTA top-k runs without further scratch (rows of at most
+  // 8192 entries here); the scores must fit the static array
+  if (n_cap > 8192 || topk_is_long((int)n_cap)) return CSA_ERR_UNSUPPORTED;
   const bool own_scores = a->scores != nullptr;
   if (own_scores && a->score_cols < n_cap) return CSA_ERR_INVALID_ARG;
   if (!own_scores && (long long)a->n_rows * n_cap > (long long)kMaxScores)

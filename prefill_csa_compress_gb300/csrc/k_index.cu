@@ -8,7 +8,7 @@
 // Scores become order-preserving 32-bit keys, held in registers (each thread
 // owns a contiguous run of positions).  A three-digit radix select (11, 11
 // and 10 key bits) finds the k-th largest key T and how many keys equal to T
-// are taken; equal keys are taken in ascending position.  Rows up to 8192
+// are taken; equal keys are taken in ascending position.  Rows up to 16384
 // entries are selected by one CTA.  Longer rows are split into S slices, the
 // CTAs of a cooperative launch: each slice adds its digit histogram into the
 // row's histogram in global memory and the slices meet at a bounded barrier
@@ -62,7 +62,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *
 
 // ---------------------------------------------------------------- radix select
 
-constexpr int TK_SHORT_KPT = 16;  // one CTA per row: rows up to 512 x 16 entries
+constexpr int TK_SHORT_KPT = 16;  // one CTA per row: 16 entries per thread ...
+constexpr int TK_SHORT_KPT2 = 32; // ... or 32 (512 threads: rows up to 16384 entries)
 constexpr int TK_LONG_THREADS = 512;
 constexpr int TK_LONG_KPT = 32;   // entries per thread of a long-row slice
 constexpr int TK_B1 = 2048, TK_B2 = 2048, TK_B3 = 1024;  // 11 + 11 + 10 key bits
@@ -386,7 +387,7 @@ int device_sms() {
   return cached[dev];
 }
 
-constexpr int TK_SHORT_MAX = 512 * TK_SHORT_KPT;
+constexpr int TK_SHORT_MAX = 512 * TK_SHORT_KPT2;
 constexpr int TK_SLICE_MAX = TK_LONG_THREADS * TK_LONG_KPT;
 
 // Opt a kernel into more than 48 KB of dynamic shared memory, once per device.
@@ -401,18 +402,18 @@ cudaError_t allow_smem(K kern, int bytes, bool *done) {
   return e;
 }
 
-template <int NT>
+template <int NT, int KPT>
 cudaError_t launch_short(const csa_index_args &a, const float *scores, int cols, cudaStream_t s,
                          const TopkSel &sel) {
   static bool done[64] = {};
-  const auto kern = topk_radix_kernel<NT, TK_SHORT_KPT, false>;
+  const auto kern = topk_radix_kernel<NT, KPT, false>;
   constexpr int smem = topk_smem_bytes<NT>();
   cudaError_t e = allow_smem(kern, smem, done);
   if (e != cudaSuccess) return e;
   constexpr int kMaxGridY = 65535;
   for (int row0 = 0; row0 < a.n_rows && e == cudaSuccess; row0 += kMaxGridY)
     e = launch_kernel(kern, dim3(1, std::min(kMaxGridY, a.n_rows - row0)), dim3(NT),
-                      (size_t)smem, s, 0, false, a, scores, cols, row0, 1, NT * TK_SHORT_KPT,
+                      (size_t)smem, s, 0, false, a, scores, cols, row0, 1, NT * KPT,
                       static_cast<uint32_t *>(nullptr), static_cast<uint32_t *>(nullptr), sel);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -465,12 +466,13 @@ cudaError_t launch_index_topk(const csa_index_args &a, const float *scores, int 
   if (sel.n_cap <= 0) sel.n_cap = a.max_blocks * kBlock;
   const int n_cap = sel.n_cap;
   if (!topk_is_long(n_cap)) {
-    // the smallest CTA whose threads hold a whole row, 16 entries each
+    // the smallest CTA whose threads hold a whole row, 16 (or 32) entries each
     launch_begin(CSA_K_INDEX_TOPK, s);
     const cudaError_t e =
-        n_cap <= 128 * TK_SHORT_KPT   ? launch_short<128>(a, scores, score_cols, s, sel)
-        : n_cap <= 256 * TK_SHORT_KPT ? launch_short<256>(a, scores, score_cols, s, sel)
-                                      : launch_short<512>(a, scores, score_cols, s, sel);
+        n_cap <= 128 * TK_SHORT_KPT   ? launch_short<128, TK_SHORT_KPT>(a, scores, score_cols, s, sel)
+        : n_cap <= 256 * TK_SHORT_KPT ? launch_short<256, TK_SHORT_KPT>(a, scores, score_cols, s, sel)
+        : n_cap <= 512 * TK_SHORT_KPT ? launch_short<512, TK_SHORT_KPT>(a, scores, score_cols, s, sel)
+                                      : launch_short<512, TK_SHORT_KPT2>(a, scores, score_cols, s, sel);
     launch_end(CSA_K_INDEX_TOPK, s);
     return e;
   }

@@ -67,7 +67,9 @@ struct IdxTc {
   static constexpr int OFF_SC = OFF_STSC + NS * kBlock * 4;
   static constexpr int OFF_W = OFF_SC + NSC * kBlock * 4;
   static constexpr int OFF_ROPE = OFF_W + G * kHeads * 4;   // per row: 32 cos, 32 sin
-  static constexpr int OFF_MISC = OFF_ROPE + G * 64 * 4;
+  static constexpr int OFF_GQ = OFF_ROPE + G * 64 * 4;      // reindex: looked-up blocks
+  static constexpr int GQ_TILES = 16;                        // tiles per look-up batch
+  static constexpr int OFF_MISC = OFF_GQ + GQ_TILES * (kBlock / 8) * 4;
   static constexpr int SMEM = OFF_MISC + 512 + 1024;        // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(NA + NT < NSC, "the scale ring must outlast the tiles in flight");
@@ -129,20 +131,40 @@ __device__ __forceinline__ void named_barrier(int id, int n_threads) {
 __device__ int candidate_prefix(const int32_t *c, int n, int nb, int *s_min, uint32_t *status) {
   if (threadIdx.x == 0) *s_min = n;
   __syncthreads();
-  for (int j = threadIdx.x; j < n; j += blockDim.x) {
-    const int x = c[j];
-    if (x < 0 || x >= nb || (j > 0 && x <= c[j - 1])) {
-      atomicMin(s_min, j);
-      break;
+  // every entry and its predecessor are loaded before any is tested (one
+  // round trip for lists of up to PER * blockDim.x entries)
+  constexpr int PER = 4;
+  for (int j0 = 0; j0 < n; j0 += PER * (int)blockDim.x) {
+    int x[PER], xp[PER];
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+      const int j = j0 + threadIdx.x + r * blockDim.x;
+      x[r] = j < n ? c[j] : 0;
+      xp[r] = j > 0 && j < n ? c[j - 1] : -1;
+    }
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+      const int j = j0 + threadIdx.x + r * blockDim.x;
+      if (j < n && (x[r] < 0 || x[r] >= nb || x[r] <= xp[r])) {
+        atomicMin(s_min, j);
+        break;
+      }
     }
   }
   __syncthreads();
   const int nv = *s_min;
-  for (int j = nv + threadIdx.x; j < n; j += blockDim.x)
-    if (c[j] != -1) {
-      flag(status, CSA_DEV_BAD_INDEX);
-      break;
+  bool bad = false;
+  for (int j0 = nv; j0 < n; j0 += PER * (int)blockDim.x) {
+    int x[PER];
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+      const int j = j0 + threadIdx.x + r * blockDim.x;
+      x[r] = j < n ? c[j] : -1;
     }
+#pragma unroll
+    for (int r = 0; r < PER; ++r) bad = bad || x[r] != -1;
+  }
+  if (bad) flag(status, CSA_DEV_BAD_INDEX);
   return nv;
 }
 
@@ -175,10 +197,11 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
          i += (long long)gridDim.x * IT_THREADS)
       ctr[i] = 0u;
   }
-  // reindex: each row is a pass of its own over its candidate blocks, 128
-  // candidate entries (128 >> cb_shift blocks) per tile
+  // reindex: a group is one row (rows do not share candidates), its tiles
+  // hold 128 candidate entries (128 >> cb_shift blocks) each
   const bool reidx = sel.cand_in != nullptr;
   const int cb = 1 << sel.cb_shift;
+  const int RPG = reidx ? 1 : G;  // rows per group
   const bool rope = a.rope_cos != nullptr;
   const int n_kchunks = rope ? 3 : 2;
   const int n_cap = a.max_blocks * kBlock;
@@ -214,8 +237,8 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
     int rb[G];
 #pragma unroll
     for (int i = 0; i < G; ++i) {
-      const int t = g * G + i;
-      rb[i] = t < a.n_rows ? a.row_req[t] : -1;
+      const int t = g * RPG + i;
+      rb[i] = i < RPG && t < a.n_rows ? a.row_req[t] : -1;
       if (rb[i] >= a.n_req) {
         if (chunk == 0 && tid == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
         rb[i] = -1;
@@ -235,7 +258,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
       unsigned on_mask = 0;  // rows of this pass
 #pragma unroll
       for (int i = 0; i < G; ++i) {
-        const int t = g * G + i;
+        const int t = g * RPG + i;
         int V = 0;
         const bool on = reidx ? i == pi : rb[i] == b;
         if (on) V = min(visible_count(a.row_pos[t], a.ratio, a.n_cmp[b]), n_cap);
@@ -251,7 +274,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
       if (reidx) {
         // the row's eligible entries: its valid candidate blocks, all fully
         // visible but the last, which may be cut by V
-        const int t = g * G + pi, V = vmax;
+        const int t = g * RPG + pi, V = vmax;
         cand = sel.cand_in + (long long)t * sel.n_cand;
         const int nv = candidate_prefix(cand, sel.n_cand, (V + cb - 1) >> sel.cb_shift,
                                         &M->cand_min, a.status_dev);
@@ -277,13 +300,13 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
           if ((on_mask >> i) & 1u)
             tc::cp_async16(Bs + part * C::B_CHUNK + n * 128 + ((jj ^ (n & 7)) << 4),
                            static_cast<const uint16_t *>(a.q_idx) +
-                               ((long long)(g * G + i) * kHeads + h) * kIdxDim + part * 64 +
+                               ((long long)(g * RPG + i) * kHeads + h) * kIdxDim + part * 64 +
                                jj * 8);
         }
         // head weights, row positions and the rows' RoPE table entries
         for (int e = bt; e < G * (kHeads + 64); e += IT_BUILD) {
           const int i = e / (kHeads + 64), f = e % (kHeads + 64);
-          const int t = g * G + i;
+          const int t = g * RPG + i;
           if (!((on_mask >> i) & 1u)) continue;
           const int p = a.row_pos[t];
           if (f < kHeads) {
@@ -372,7 +395,79 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
         named_barrier(1, IT_BUILD);
       }
 
-      if (warp == W_PROD) {
+      if (warp == W_PROD && reidx) {
+        // ---------------- producer (reindex): lane jj looks up and copies
+        // candidate block jj of each tile (cb rows of one page and their
+        // scales); st_ok holds one bit per 8 rows that arrive
+        const int nbt = kBlock >> sel.cb_shift;
+        int *gq = reinterpret_cast<int *>(sm + C::OFF_GQ);
+        for (int k = 0; k < nt; ++k) {
+          if (k % C::GQ_TILES == 0) {
+            // look up the blocks of the next GQ_TILES tiles at once: first every
+            // candidate entry, then every block-table entry (two round trips)
+            const int n_q = min(C::GQ_TILES, nt - k) * nbt;
+            constexpr int QPL = C::GQ_TILES * (kBlock / 8) / 32;  // per lane
+            int cv[QPL];
+#pragma unroll
+            for (int r = 0; r < QPL; ++r) {
+              const int q = lane + 32 * r, j = (tb + k) * nbt + q;
+              cv[r] = q < n_q && j * cb < vmax ? cand[j] : -1;
+            }
+            int ph[QPL];
+#pragma unroll
+            for (int r = 0; r < QPL; ++r)
+              ph[r] = cv[r] >= 0 ? a.cmp_block_table[(long long)b * a.max_blocks +
+                                                     ((cv[r] << sel.cb_shift) / kBlock)]
+                                 : -1;
+#pragma unroll
+            for (int r = 0; r < QPL; ++r) {
+              const int q = lane + 32 * r;
+              if (q >= n_q) continue;
+              int g_row = -1;
+              if (cv[r] >= 0) {
+                if (ph[r] >= 0 && ph[r] < a.n_blocks)
+                  g_row = ph[r] * kBlock + ((cv[r] << sel.cb_shift) % kBlock);
+                else
+                  flag(a.status_dev, CSA_DEV_BAD_BLOCK);
+              }
+              gq[q] = g_row;
+            }
+            __syncwarp();
+          }
+          const uint32_t itk = it + k;
+          const int s = itk % C::NS;
+          int go = 0;
+          if (lane == 0) {
+            go = !M->abort;
+            if (go && !tc::mbar_wait(&M->st_empty[s], ((itk / C::NS) & 1) ^ 1)) {
+              set_abort(M, a.status_dev);
+              go = 0;
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, go, 0)) break;
+          const long long grow = lane < nbt ? gq[(k % C::GQ_TILES) * nbt + lane] : -1;
+          const unsigned mask = __reduce_or_sync(
+              0xffffffffu, grow >= 0 ? ((1u << (cb / 8)) - 1u) << (lane * cb / 8) : 0u);
+          const int n_ok = __popc(__ballot_sync(0xffffffffu, grow >= 0));
+          if (lane == 0) {
+            M->st_ok[s] = (int)mask;
+            if (n_ok)
+              tc::mbar_arrive_expect_tx(&M->st_full[s], n_ok * cb * (kIdxDim + 4));
+            else
+              tc::mbar_arrive(&M->st_full[s]);
+          }
+          __syncwarp();
+          if (grow >= 0) {
+            uint8_t *dst = St + s * C::PAGE + lane * cb * kIdxDim;
+            if constexpr (C::ATMEM)
+              tc::tma_load_2d(dst, &keys_map, 0, (int)grow, &M->st_full[s]);
+            else
+              tc::bulk_g2s(dst, a.idx_pool + grow * kIdxDim, cb * kIdxDim, &M->st_full[s]);
+            tc::bulk_g2s(StSc + s * kBlock + lane * cb, a.idx_scale_pool + grow, cb * 4,
+                         &M->st_full[s]);
+          }
+        }
+      } else if (warp == W_PROD) {
         // ---------------- producer: one page (and its scales) per tile
         if (lane == 0) {
           for (int k = 0; k < nt && !M->abort; ++k) {
@@ -383,47 +478,6 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
               break;
             }
             const int tile = tb + k;
-            if (reidx) {
-              // the tile's candidate blocks, each a run of cb rows of one page;
-              // st_ok holds one bit per 8 rows that arrive
-              const int nbt = kBlock >> sel.cb_shift, j0 = tile * nbt;
-              int phys_j[kBlock / 8], row_j[kBlock / 8];
-              unsigned mask = 0;
-              int n_ok = 0;
-              for (int jj = 0; jj < nbt; ++jj) {
-                phys_j[jj] = -1;
-                if ((j0 + jj) * cb >= vmax) continue;
-                const int pos0 = cand[j0 + jj] << sel.cb_shift;
-                const int page = pos0 / kBlock;
-                const int ph = a.cmp_block_table[(long long)b * a.max_blocks + page];
-                if (ph < 0 || ph >= a.n_blocks) {
-                  flag(a.status_dev, CSA_DEV_BAD_BLOCK);
-                  continue;
-                }
-                phys_j[jj] = ph;
-                row_j[jj] = pos0 % kBlock;
-                mask |= ((1u << (cb / 8)) - 1u) << (jj * cb / 8);
-                ++n_ok;
-              }
-              M->st_ok[s] = (int)mask;
-              if (n_ok) {
-                tc::mbar_arrive_expect_tx(&M->st_full[s], n_ok * cb * (kIdxDim + 4));
-                for (int jj = 0; jj < nbt; ++jj) {
-                  if (phys_j[jj] < 0) continue;
-                  const long long grow = (long long)phys_j[jj] * kBlock + row_j[jj];
-                  uint8_t *dst = St + s * C::PAGE + jj * cb * kIdxDim;
-                  if constexpr (C::ATMEM)
-                    tc::tma_load_2d(dst, &keys_map, 0, (int)grow, &M->st_full[s]);
-                  else
-                    tc::bulk_g2s(dst, a.idx_pool + grow * kIdxDim, cb * kIdxDim, &M->st_full[s]);
-                  tc::bulk_g2s(StSc + s * kBlock + jj * cb, a.idx_scale_pool + grow, cb * 4,
-                               &M->st_full[s]);
-                }
-              } else {
-                tc::mbar_arrive(&M->st_full[s]);
-              }
-              continue;
-            }
             const int phys = tile < a.max_blocks
                                  ? a.cmp_block_table[(long long)b * a.max_blocks + tile]
                                  : -1;
@@ -683,7 +737,7 @@ cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, uint32_t
     attr[dev] = true;
   }
   const int sms = sm_count();
-  const int n_groups = (a.n_rows + G - 1) / G;
+  const int n_groups = reidx ? a.n_rows : (a.n_rows + G - 1) / G;
   // tiles of one row: its pages, or (reindex) its candidate entries / 128
   const int max_tiles =
       reidx ? ((sel.n_cand << sel.cb_shift) + kBlock - 1) / kBlock : a.max_blocks;
