@@ -21,6 +21,11 @@ straight from the pages:
 * "DeepSeek V4-Flash, MTP point", sections "What is quantized" (INT8 per-row
   amax floored at 1e-4, scaled to 127, FP32 per-row scale) and "Attention
   paths" (main compressor rotate=False, index-key compressor rotate=True).
+* "DeepSeek V4.1 Flash", the production cache ABI (window KV MXFP8 E4M3 with
+  E8M0 group-of-32 scales, compressed KV packed E2M1 with E4M3 group-of-16
+  scales, index keys packed E2M1 with E8M0 group-of-32 scales; quantised on
+  publication, dequantised on reads).  The rounding rules of the two FP4
+  publications are readings (the pages give only the formats).
 
 Readings taken where the pages are silent (each also listed in the design doc):
 ReLU per index head; the index-key scale applied after the head sum; the
@@ -67,6 +72,153 @@ def quantize_int8(y):
     scale = max(amax, 1e-4) / 127.0
     codes = np.clip(np.rint(y / scale), -127, 127).astype(np.int8)
     return codes, scale
+
+
+# --------------------------------------------------------------------------
+# Low-bit cache formats ("DeepSeek V4.1 Flash", production cache ABI: window
+# KV MXFP8 E4M3 with E8M0 group-of-32 scales; compressed KV packed MXFP4 E2M1
+# with E4M3 group-of-16 scales; index keys packed E2M1 with E8M0 group-of-32
+# scales; quantised on cache publication, dequantised on cache reads)
+# --------------------------------------------------------------------------
+
+
+def e2m1_decode(codes):
+    """Value of 4-bit E2M1 codes (sign, 2 exponent bits with bias 1, 1
+    mantissa bit; exponent 0 is subnormal): float64, same shape."""
+    c = np.asarray(codes, dtype=np.int64)
+    e, m = (c >> 1) & 3, c & 1
+    mag = np.where(e == 0, 0.5 * m, np.ldexp(1.0 + 0.5 * m, e - 1))
+    return np.where(c & 8, -mag, mag)
+
+
+def e4m3_decode(b):
+    """Value of E4M3 bytes (sign, 4 exponent bits with bias 7, 3 mantissa
+    bits; exponent 0 is subnormal; no infinities, S.1111.111 is NaN)."""
+    b = np.asarray(b, dtype=np.int64)
+    e, m = (b >> 3) & 15, b & 7
+    mag = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, e - 7))
+    mag = np.where((b & 0x7F) == 0x7F, np.nan, mag)
+    return np.where(b & 0x80, -mag, mag)
+
+
+def e8m0_decode(b):
+    """Value of E8M0 scale bytes: 2^(b - 127); 255 is NaN."""
+    b = np.asarray(b, dtype=np.int64)
+    return np.where(b == 255, np.nan, np.ldexp(1.0, b - 127))
+
+
+def round_e2m1(x):
+    """E2M1 code of the representable value nearest to each x (ties: the
+    code with mantissa bit 0), magnitudes above 6 saturating to 6; the sign
+    bit is set for x < 0 (also when the magnitude rounds to 0)."""
+    x = np.asarray(x, dtype=np.float64)
+    grid = e2m1_decode(np.arange(8))                      # the 8 magnitudes
+    mag = _nearest_even(np.minimum(np.abs(x), 6.0), grid)
+    return (mag | np.where(x < 0, 8, 0)).astype(np.uint8)
+
+
+def _nearest_even(x, grid):
+    """Index of the grid value nearest to each x; of two equally near ones
+    (always neighbours) the even index."""
+    d = np.abs(x[..., None] - grid)
+    near = d == d.min(axis=-1, keepdims=True)
+    return np.argmax(near * (2 - (np.arange(len(grid)) & 1)), axis=-1)
+
+
+def round_e4m3(x):
+    """E4M3 byte of the representable value nearest to each x >= 0 (ties:
+    the even byte, i.e. mantissa ending in 0), saturating at 448."""
+    x = np.asarray(x, dtype=np.float64)
+    assert np.all(x >= 0)
+    grid = e4m3_decode(np.arange(127))                    # 0 .. 448, ascending
+    return _nearest_even(np.minimum(x, 448.0), grid).astype(np.uint8)
+
+
+def pack_nibbles(codes):
+    """Two E2M1 codes per byte: element 2i in the low nibble, 2i+1 in the high."""
+    c = np.asarray(codes, dtype=np.uint8).reshape(-1, 2)
+    return (c[:, 0] | (c[:, 1] << 4)).astype(np.uint8)
+
+
+def unpack_nibbles(packed):
+    p = np.asarray(packed, dtype=np.uint8).reshape(-1)
+    return np.stack([p & 15, p >> 4], axis=-1).reshape(-1)
+
+
+def _e8m0_exponent(amax):
+    """Smallest e with 6 * 2^e >= amax, clamped to [-127, 127] (amax = 0:
+    -127): with amax = M * 2^K, M in [1, 2), e = K - 2 + (M > 1.5)."""
+    if amax == 0.0:
+        return -127
+    m, k = np.frexp(amax)  # amax = m * 2^k, m in [0.5, 1)
+    e = (k - 1) - 2 + (1 if 2.0 * m > 1.5 else 0)
+    return int(min(127, max(-127, e)))
+
+
+def quantize_fp4_e8m0(y, group=32):
+    """Index-key publication as packed E2M1 with one E8M0 scale per 32 dims.
+    Reading (the pages give the format, not the rounding rule): a group's
+    scale is the smallest power of two 2^e with 6 * 2^e >= its amax, so no
+    element clips; codes are the nearest E2M1 of y / 2^e, the quotient taken
+    in FP32 as the device takes it.  Returns (packed uint8 [n/2], scale
+    bytes uint8 [n/group])."""
+    y = np.asarray(y, dtype=np.float64).astype(np.float32)
+    codes, sbytes = [], []
+    for grp in y.reshape(-1, group):
+        e = _e8m0_exponent(float(np.max(np.abs(grp))))
+        q = grp / np.float32(np.ldexp(1.0, e))           # FP32 quotient
+        codes.append(round_e2m1(q))
+        sbytes.append(e + 127)
+    return pack_nibbles(np.concatenate(codes)), np.array(sbytes, dtype=np.uint8)
+
+
+def quantize_fp4_e4m3(y, group=16):
+    """Compressed-KV publication as packed E2M1 with one E4M3 scale per 16
+    channels.  Reading: the scale is the E4M3 value nearest to amax / 6 (so
+    the largest element lands near the top code), codes the nearest E2M1 of
+    y / scale (saturating at 6); both quotients taken in FP32 as the device
+    takes them; a scale that rounds to 0 gives zero codes."""
+    y = np.asarray(y, dtype=np.float64).astype(np.float32)
+    codes, sbytes = [], []
+    for grp in y.reshape(-1, group):
+        amax = np.float32(np.max(np.abs(grp)))
+        sb = int(round_e4m3(float(amax / np.float32(6.0))))
+        s = np.float32(e4m3_decode(sb))
+        codes.append(round_e2m1(grp / s) if s > 0 else np.zeros(group, np.uint8))
+        sbytes.append(sb)
+    return pack_nibbles(np.concatenate(codes)), np.array(sbytes, dtype=np.uint8)
+
+
+def dequant_fp4(packed, sbytes, group, scale_fmt):
+    """Values of one packed E2M1 row with its scale bytes (``scale_fmt``
+    "e8m0" or "e4m3")."""
+    v = e2m1_decode(unpack_nibbles(packed))
+    dec = e8m0_decode if scale_fmt == "e8m0" else e4m3_decode
+    return v * np.repeat(dec(np.asarray(sbytes)), group)
+
+
+def dequant_mxfp8(codes, sbytes, group=32):
+    """Values of one MXFP8 row: E4M3 bytes times their group's E8M0 scale."""
+    return e4m3_decode(codes) * np.repeat(e8m0_decode(np.asarray(sbytes)), group)
+
+
+class LowBitPool:
+    """A paged cache pool held in a low-bit format: ``codes`` uint8 [pages,
+    128, bytes per row] and ``scales`` uint8 [pages, 128, groups per row];
+    ``fmt`` is "fp4_e4m3" (packed E2M1, E4M3 per 16: compressed KV),
+    "fp4_e8m0" (packed E2M1, E8M0 per 32: index keys) or "mxfp8" (E4M3, E8M0
+    per 32: window KV)."""
+
+    def __init__(self, codes, scales, fmt):
+        assert fmt in ("fp4_e4m3", "fp4_e8m0", "mxfp8")
+        self.codes, self.scales, self.fmt = codes, scales, fmt
+
+    def dequant_row(self, codes, sbytes):
+        if self.fmt == "mxfp8":
+            return dequant_mxfp8(codes, sbytes)
+        if self.fmt == "fp4_e4m3":
+            return dequant_fp4(codes, sbytes, 16, "e4m3")
+        return dequant_fp4(codes, sbytes, 32, "e8m0")
 
 
 # --------------------------------------------------------------------------
@@ -128,6 +280,22 @@ def as_f64(a):
     return np.asarray(a, dtype=np.float64)
 
 
+def cache_rows(pool, table_row, logical):
+    """``page_rows`` of a cache pool in any format: a ``LowBitPool`` is
+    dequantised row by row (cache reads dequantise), anything else is read
+    as it is."""
+    if not isinstance(pool, LowBitPool):
+        return page_rows(pool, table_row, logical)
+    logical = list(logical)
+    codes = page_rows(pool.codes, table_row, logical).astype(np.int64)
+    scales = page_rows(pool.scales, table_row, logical).astype(np.int64)
+    D = codes.shape[1] * (1 if pool.fmt == "mxfp8" else 2)
+    out = np.zeros((len(logical), D))
+    for i in range(len(logical)):
+        out[i] = pool.dequant_row(codes[i], scales[i])
+    return out
+
+
 def page_rows(pool, table_row, logical):
     """Rows ``logical`` (iterable of request-local positions) of a paged pool
     [pages, 128, ...] through one request's block table row, as float64."""
@@ -163,11 +331,15 @@ def compress(x, kv, w_gate, ape, ratio, positions, row_req, gamma=None, rms_eps=
     RMS-normalised with ``gamma`` (rounded to BF16 again), optionally rotated
     at the group start position g*r ("compression-group start positions";
     rotate=True for the index-key compressor, "DeepSeek V4-Flash, MTP point",
-    "Attention paths"), and published as BF16 (``out="bf16"``) or as INT8
-    codes with an FP32 per-row scale (``out="int8"``).
+    "Attention paths"), and published as BF16 (``out="bf16"``), as INT8
+    codes with an FP32 per-row scale (``out="int8"``), or in a low-bit cache
+    format (``out="fp4_e4m3"``: packed E2M1 with E4M3 scales per 16;
+    ``out="fp4_e8m0"``: packed E2M1 with E8M0 scales per 32; "DeepSeek V4.1
+    Flash", production cache ABI, quantised on publication).
 
-    Returns a list of (request, g, values) for bf16 or (request, g, codes,
-    scale) for int8, in row order.
+    Returns a list of (request, g, values) for bf16, (request, g, codes,
+    scale) for int8, or (request, g, packed codes, scale bytes) for the
+    low-bit formats, in row order.
     """
     x, kv, w_gate, ape = as_f64(x), as_f64(kv), as_f64(w_gate), as_f64(ape)
     positions = as_f64(positions).astype(np.int64)
@@ -205,6 +377,10 @@ def _publish_group(b, g, r, logits, kvs, gamma, rms_eps, rotate, rope_cos, rope_
         y = rope_rotate(y, g * r, rope_cos, rope_sin, rope_dim)
     if out == "bf16":
         return (b, g, bf16_round(y))
+    if out == "fp4_e4m3":
+        return (b, g) + quantize_fp4_e4m3(y)
+    if out == "fp4_e8m0":
+        return (b, g) + quantize_fp4_e8m0(y)
     codes, scale = quantize_int8(y)
     return (b, g, codes, scale)
 
@@ -290,14 +466,18 @@ def index_scores(q_idx_row, w_row, p, n_cmp_b, ratio, idx_pool, idx_scale_pool, 
     ("Hyper-Parallel ... DeepSeek V4 CP", "10. ratio=4 Global Top-k"; INT8
     keys with an FP32 per-row scale: "DeepSeek V4-Flash, MTP point", "What is
     quantized").  Since scale_c > 0, ReLU(scale * x) = scale * ReLU(x), so the
-    scale is applied after the head sum.  Returns float64 [visible].
+    scale is applied after the head sum.  With ``idx_pool`` a ``LowBitPool``
+    (packed E2M1 keys with E8M0 group scales, "DeepSeek V4.1 Flash",
+    production cache ABI) k_c is the dequantised key and scale_c = 1
+    (``idx_scale_pool`` unused).  Returns float64 [visible].
     """
     nv = visible_count(p, ratio, n_cmp_b)
     q = as_f64(q_idx_row)  # [H, Di]
     if rope_cos is not None:
         q = rope_rotate(q, p, rope_cos, rope_sin, rope_dim)
-    keys = page_rows(idx_pool, table_row, range(nv))  # [nv, Di]
-    scales = page_rows(idx_scale_pool, table_row, range(nv))
+    keys = cache_rows(idx_pool, table_row, range(nv))  # [nv, Di]
+    scales = (np.ones(nv) if isinstance(idx_pool, LowBitPool) else
+              page_rows(idx_scale_pool, table_row, range(nv)))
     dots = keys @ q.T  # [nv, H]
     if relu:
         dots = np.maximum(dots, 0.0)
@@ -368,6 +548,7 @@ def sparse_attention(q_row, p, topk_row, kv_pool, kv_table_row, cmp_pool, cmp_ta
         o_h  = sum_i e^{l_i} k_i / (sum_i e^{l_i} + e^{sink_h})
         lse_h = log(sum_i e^{l_i} + e^{sink_h})
     A sink of None means -inf (plain softmax).  Two passes: max, then sums.
+    Either pool may be a ``LowBitPool`` (rows dequantised as they are read).
     Returns (out [H, D] float64, lse [H] float64).
     """
     q = as_f64(q_row)
@@ -377,10 +558,10 @@ def sparse_attention(q_row, p, topk_row, kv_pool, kv_table_row, cmp_pool, cmp_ta
     sel = [int(c) for c in np.asarray(topk_row).ravel() if int(c) >= 0]
     parts = []
     if sel:
-        parts.append(page_rows(cmp_pool, cmp_table_row, sel))
+        parts.append(cache_rows(cmp_pool, cmp_table_row, sel))
     win = window_positions(p, window)
     if win:
-        parts.append(page_rows(kv_pool, kv_table_row, win))
+        parts.append(cache_rows(kv_pool, kv_table_row, win))
     K = np.concatenate(parts, axis=0) if parts else np.zeros((0, D))
     logits = scale * (q @ K.T)  # [H, n]
     snk = np.full(H, -np.inf) if sink is None else as_f64(sink)

@@ -662,3 +662,191 @@ def test_attention_rotates_query_at_row_position_and_inverse_output():
     out_inv, _ = O.sparse_attention(q, p, sel, kv_pool, kv_table, cmp_pool, cmp_table, sink,
                                     scale, rope_cos=COS, rope_sin=SIN, inv_rope_out=True)
     assert np.allclose(_cplx_rotate(out_inv, p), want, atol=1e-9)
+
+
+# ---------------------------------------------------------------- low-bit cache formats
+
+
+def test_e2m1_values_match_the_format_table():
+    # the E2M1 value table of the OCP microscaling format: magnitudes of codes 0..7
+    want = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert O.e2m1_decode(np.arange(8)).tolist() == want
+    assert O.e2m1_decode(np.arange(8, 16)).tolist() == [-v for v in want]
+
+
+def test_e4m3_and_e8m0_decoders_match_torch():
+    b = torch.arange(256, dtype=torch.uint8)
+    want = b.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.e4m3_decode(np.arange(256))
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    assert np.array_equal(got[~np.isnan(got)], want[~np.isnan(want)])
+    if hasattr(torch, "float8_e8m0fnu"):
+        want = b.view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+        got = O.e8m0_decode(np.arange(256))
+        assert np.array_equal(np.isnan(got), np.isnan(want))
+        assert np.array_equal(got[~np.isnan(got)], want[~np.isnan(want)])
+    assert O.e8m0_decode([127, 0, 254]).tolist() == [1.0, 2.0 ** -127, 2.0 ** 127]
+
+
+def test_round_e4m3_matches_torch_cast():
+    rng = np.random.default_rng(50)
+    grid = O.e4m3_decode(np.arange(127))
+    mids = (grid[1:] + grid[:-1]) / 2  # every tie
+    x = np.concatenate([grid, mids, rng.uniform(0, 448, 2000), rng.uniform(0, 2 ** -5, 500)])
+    x = x.astype(np.float32)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.round_e4m3(x.astype(np.float64)), want)
+    assert O.round_e4m3([1e6]).tolist() == [0x7E]  # saturates at 448
+
+
+def test_round_e2m1_ties_and_saturation():
+    x = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.26, 0.74, 5.5, 7.0, 100.0]
+    # ties go to the code with mantissa bit 0: 0.25 -> 0, 0.75 -> 1.0, 1.25 -> 1.0,
+    # 1.75 -> 2.0, 2.5 -> 2.0, 3.5 -> 4.0, 5.0 -> 4.0
+    assert O.round_e2m1(x).tolist() == [0, 2, 2, 4, 4, 6, 6, 1, 1, 7, 7, 7]
+    assert O.round_e2m1([-0.3, -0.1, -6.0, 0.0]).tolist() == [9, 8, 15, 0]
+
+
+def test_round_e2m1_is_nearest_by_brute_force():
+    rng = np.random.default_rng(51)
+    x = rng.uniform(-7, 7, 5000)
+    got = O.e2m1_decode(O.round_e2m1(x))
+    grid = np.array([-6, -4, -3, -2, -1.5, -1, -0.5, 0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    best = np.min(np.abs(np.clip(x, -6, 6)[:, None] - grid), axis=1)
+    assert np.allclose(np.abs(np.clip(x, -6, 6) - got), best)
+
+
+def test_nibble_packing_order():
+    assert O.pack_nibbles([1, 2, 15, 0]).tolist() == [0x21, 0x0F]
+    assert O.unpack_nibbles([0x21, 0x0F]).tolist() == [1, 2, 15, 0]
+
+
+def test_fp4_e8m0_quantiser_scale_rule_and_error_bound():
+    rng = np.random.default_rng(52)
+    for _ in range(200):
+        y = rng.standard_normal(128) * np.exp(rng.uniform(-8, 8))
+        packed, sb = O.quantize_fp4_e8m0(y)
+        back = O.dequant_fp4(packed, sb, 32, "e8m0")
+        for gi in range(4):
+            grp = y[32 * gi:32 * gi + 32]
+            amax = np.max(np.abs(grp))
+            e = int(sb[gi]) - 127
+            # the smallest power of two that keeps every element inside the E2M1 range
+            assert 6 * 2.0 ** e >= amax > 6 * 2.0 ** (e - 1)
+            # no clipping; the error is at most half a step of the E2M1 grid (steps
+            # 0.5 below 2, 1 below 4, 2 above) times the scale
+            err = np.abs(back[32 * gi:32 * gi + 32] - grp)
+            step = np.where(np.abs(grp) / 2.0 ** e < 2, 0.5, np.where(np.abs(grp) / 2.0 ** e < 4,
+                                                                       1.0, 2.0))
+            assert np.all(err <= step / 2 * 2.0 ** e * (1 + 1e-6))
+    # exactly representable groups come back exactly; zero groups get scale byte 0
+    y = np.concatenate([np.array([0.5, -3, 6, 1.5] * 8) * 4.0, np.zeros(32),
+                        np.array([1.0] * 32), np.array([-6.0] + [0.0] * 31) * 2 ** -20])
+    packed, sb = O.quantize_fp4_e8m0(y)
+    assert sb.tolist() == [129, 0, 125, 107]  # amax 1: 6 * 2^-2 >= 1 > 6 * 2^-3
+    assert np.array_equal(O.dequant_fp4(packed, sb, 32, "e8m0"), y)
+
+
+def test_fp4_e4m3_quantiser_hand_example_and_bound():
+    # amax 15 -> scale E4M3(15 / 6 = 2.5) = 2.5 exactly; 15 / 2.5 = 6 -> code 7,
+    # 7 / 2.5 = 2.8 -> 3.0 (code 5), -1 / 2.5 = -0.4 -> -0.5 (code 9)
+    y = np.zeros(16)
+    y[:3] = [15.0, 7.0, -1.0]
+    packed, sb = O.quantize_fp4_e4m3(y)
+    assert sb.tolist() == [0x42]  # 0.1000.010 = 1.25 * 2^1
+    assert O.unpack_nibbles(packed)[:4].tolist() == [7, 5, 9, 0]
+    rng = np.random.default_rng(53)
+    for _ in range(200):
+        y = rng.standard_normal(512) * np.exp(rng.uniform(-4, 4))
+        packed, sb = O.quantize_fp4_e4m3(y)
+        back = O.dequant_fp4(packed, sb, 16, "e4m3")
+        s = np.repeat(O.e4m3_decode(sb), 16)
+        # the scale is the E4M3 rounding of amax/6 (torch's cast as the reference)
+        amax6 = (np.abs(y.reshape(32, 16)).max(axis=1).astype(np.float32) / np.float32(6))
+        assert np.array_equal(sb, torch.from_numpy(amax6).to(torch.float8_e4m3fn)
+                              .view(torch.uint8).numpy())
+        # error: half a grid step times the scale, or the clipping at 6 * scale
+        q = np.abs(y) / s
+        step = np.where(q < 2, 0.5, np.where(q < 4, 1.0, 2.0))
+        bound = np.maximum(step / 2 * s, np.abs(y) - 6 * s) * (1 + 1e-6)
+        assert np.all(np.abs(back - y) <= bound)
+
+
+def test_mxfp8_dequant_hand_example():
+    # 0x38 = 1.0, 0xB8 = -1.0, 0x7E = 448, 0x01 = 2^-9; scales 2^1 and 2^-3
+    codes = np.array([0x38, 0xB8, 0x7E, 0x01] + [0] * 28 + [0x38] + [0] * 31)
+    got = O.dequant_mxfp8(codes, [128, 124])
+    assert got[:4].tolist() == [2.0, -2.0, 896.0, 2.0 ** -8]
+    assert got[32] == 2.0 ** -3
+
+
+def test_compress_fp4_publication_quantises_the_bf16_row():
+    rng = np.random.default_rng(54)
+    x, kv = _chunk(rng, 8, D=128, Dx=64)
+    w = _bf16(rng.standard_normal((64, 128)) / 8)
+    ape = rng.standard_normal((4, 128))
+    pos, req = np.arange(8), np.zeros(8, int)
+    plain = O.compress(x, kv, w, ape, 4, pos, req)
+    for fmt, fn in (("fp4_e4m3", O.quantize_fp4_e4m3), ("fp4_e8m0", O.quantize_fp4_e8m0)):
+        got = O.compress(x, kv, w, ape, 4, pos, req, out=fmt)
+        assert [(b, g) for b, g, *_ in got] == [(b, g) for b, g, _ in plain]
+        for (_, _, codes, sb), (_, _, y) in zip(got, plain):
+            c2, s2 = fn(y)
+            assert np.array_equal(codes, c2) and np.array_equal(sb, s2)
+
+
+def _lowbit_pool(rng, pages, fmt, D):
+    nbytes = D if fmt == "mxfp8" else D // 2
+    groups = D // (16 if fmt == "fp4_e4m3" else 32)
+    codes = rng.integers(0, 256, size=(pages, BLOCK, nbytes), dtype=np.uint8)
+    if fmt == "mxfp8":  # no NaN codes
+        codes[(codes & 0x7F) == 0x7F] = 0
+    if fmt == "fp4_e4m3":
+        scales = rng.integers(0x20, 0x50, size=(pages, BLOCK, groups), dtype=np.uint8)
+    else:
+        scales = rng.integers(120, 132, size=(pages, BLOCK, groups), dtype=np.uint8)
+    return O.LowBitPool(codes, scales, fmt)
+
+
+def _dequant_pool(pool):
+    P, R = pool.codes.shape[:2]
+    D = pool.codes.shape[2] * (1 if pool.fmt == "mxfp8" else 2)
+    out = np.zeros((P, R, D))
+    for i in range(P):
+        for j in range(R):
+            out[i, j] = pool.dequant_row(pool.codes[i, j], pool.scales[i, j])
+    return out
+
+
+def test_lowbit_pools_read_as_their_dequantised_values():
+    """Index scores and attention over low-bit pools equal the same calls over
+    float pools holding the dequantised values (cache reads dequantise), and
+    dequantised FP4 / MXFP8 values are exactly BF16-representable."""
+    rng = np.random.default_rng(55)
+    idx = _lowbit_pool(rng, 3, "fp4_e8m0", 128)
+    cmp = _lowbit_pool(rng, 3, "fp4_e4m3", 512)
+    kvp = _lowbit_pool(rng, 3, "mxfp8", 512)
+    idx_f, cmp_f, kv_f = _dequant_pool(idx), _dequant_pool(cmp), _dequant_pool(kvp)
+    for f in (idx_f, cmp_f, kv_f):
+        assert np.array_equal(O.bf16_round(f), f)
+    table = np.array([2, 0, 1])
+    q_idx = rng.standard_normal((64, 128))
+    w = rng.standard_normal(64)
+    s1 = O.index_scores(q_idx, w, 700, 300, 2, idx, None, table, rope_cos=COS, rope_sin=SIN)
+    s2 = O.index_scores(q_idx, w, 700, 300, 2, idx_f, np.ones((3, BLOCK)), table, rope_cos=COS,
+                        rope_sin=SIN)
+    assert np.array_equal(s1, s2)
+    # brute force on a few entries: the plain weighted ReLU sum over dequantised keys
+    qr = O.rope_rotate(q_idx, 700, COS, SIN)
+    for c in (0, 131, 299):
+        k = O.dequant_fp4(idx.codes[table[c // BLOCK], c % BLOCK],
+                          idx.scales[table[c // BLOCK], c % BLOCK], 32, "e8m0")
+        want = sum(w[h] * max(0.0, float(qr[h] @ k)) for h in range(64))
+        assert np.isclose(s1[c], want, rtol=1e-12, atol=1e-12)
+    q = _bf16(rng.standard_normal((4, 512)))
+    sel = np.array([3, 17, 200, -1])
+    a1 = O.sparse_attention(q, 300, sel, kvp, table, cmp, table, np.zeros(4), 0.05,
+                            rope_cos=COS, rope_sin=SIN)
+    a2 = O.sparse_attention(q, 300, sel, kv_f, table, cmp_f, table, np.zeros(4), 0.05,
+                            rope_cos=COS, rope_sin=SIN)
+    assert np.array_equal(a1[0], a2[0]) and np.array_equal(a1[1], a2[1])
