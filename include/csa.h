@@ -70,7 +70,38 @@ typedef enum {
 #define CSA_WINDOW 128   /* raw window, self included */
 #define CSA_MAX_TOPK 2048
 
-typedef enum { CSA_OUT_BF16 = 0, CSA_OUT_INT8 = 1 } csa_out_mode_t;
+/* Publication formats of csa_compress (csa_out_mode_t) and cache formats
+ * read by csa_index_topk and the attention calls (csa_cache_fmt_t).  The
+ * low-bit formats are the production cache ABI of "DeepSeek V4.1 Flash":
+ *  - FP4_E4M3: packed E2M1 (two channels per byte, channel 2i in the low
+ *    nibble), one E4M3 scale byte per 16 channels (compressed KV).  A row of
+ *    512 channels is 256 code bytes plus 32 scale bytes.
+ *  - FP4_E8M0: packed E2M1, one E8M0 scale byte (2^(byte-127)) per 32
+ *    channels (index keys: 64 code bytes plus 4 scale bytes per 128-dim key).
+ *  - MXFP8: one E4M3 byte per channel, one E8M0 scale byte per 32 channels
+ *    (window KV: 512 code bytes plus 16 scale bytes per row).
+ * A value is its code times its group's scale.  Publication (readings; the
+ * pages give the formats only): FP4_E8M0 takes for each group the smallest
+ * 2^e with 6 * 2^e >= amax (amax = 0: e = -127), FP4_E4M3 the E4M3 value
+ * nearest to amax / 6 (saturating at 448); codes are the nearest E2M1 of
+ * value / scale (ties to the even code, saturating at 6, the sign bit set for
+ * negative values), quotients taken in FP32; a zero E4M3 scale gives zero
+ * codes.  Code pools are uint8 [n_blocks, 128, code bytes per row] and scale
+ * pools uint8 [n_blocks, 128, groups per row], both through the block table
+ * of the pool they replace. */
+typedef enum {
+  CSA_OUT_BF16 = 0,
+  CSA_OUT_INT8 = 1,
+  CSA_OUT_FP4_E4M3 = 2, /* codes into cmp_pool, scales into scale_pool */
+  CSA_OUT_FP4_E8M0 = 3  /* codes into cmp_pool, scales into scale_pool */
+} csa_out_mode_t;
+typedef enum {
+  CSA_FMT_BF16 = 0,     /* attention pools: bf16 rows */
+  CSA_FMT_INT8 = 1,     /* index keys: int8 codes, f32 scale per row */
+  CSA_FMT_FP4_E4M3 = 2, /* compressed KV */
+  CSA_FMT_FP4_E8M0 = 3, /* index keys */
+  CSA_FMT_MXFP8 = 4     /* window KV */
+} csa_cache_fmt_t;
 typedef enum { CSA_MODE_AUTO = 0, CSA_MODE_DECODE = 1, CSA_MODE_PREFILL = 2 } csa_mode_t;
 
 /* ------------------------------------------------------------------------
@@ -118,6 +149,12 @@ typedef enum { CSA_MODE_AUTO = 0, CSA_MODE_DECODE = 1, CSA_MODE_PREFILL = 2 } cs
  * negative position neither publish nor write.  Requires state_capacity >=
  * ratio (at most 256).  A caller built against a header without these four fields passes a
  * smaller struct_size and gets no ring.
+ *
+ * Low-bit publication (out_mode CSA_OUT_FP4_E4M3 or CSA_OUT_FP4_E8M0, see
+ * csa_cache_fmt_t): the row as it would be published in BF16 (rotated when
+ * `rotate`, in FP32) is quantised per group; codes go to cmp_pool as uint8
+ * [n_blocks, 128, d / 2] and scale bytes to scale_pool.  Needs a struct_size
+ * that covers scale_pool.
  * ---------------------------------------------------------------------- */
 typedef struct {
   uint32_t struct_size;
@@ -152,6 +189,7 @@ typedef struct {
   const int32_t *state_block_table;  /* [n_req] */
   int32_t n_state_blocks;
   int32_t state_capacity;
+  uint8_t *scale_pool; /* FP4 out modes: scale bytes [n_blocks, 128, d / group] */
 } csa_compress_args;
 
 CSA_API csa_status_t csa_compress(csa_compress_args *args, csa_stream_t stream);
@@ -224,6 +262,11 @@ CSA_API csa_status_t csa_compress_pair(csa_compress_args *first, csa_compress_ar
  * and cand_in is set.  A struct_size that ends before `cand_block` (the
  * struct without these fields) turns both off.  csa_index_topk_noalloc
  * returns CSA_ERR_UNSUPPORTED for either mode.
+ *
+ * Key format: key_fmt CSA_FMT_FP4_E8M0 reads idx_pool as packed E2M1 codes
+ * uint8 [n_blocks, 128, 64] with key_scale_pool, k_c is the dequantised key
+ * and scale_c = 1 (idx_scale_pool unused).  CSA_FMT_INT8 (or 0, or a
+ * struct_size that ends before key_fmt) is the INT8 + FP32 layout above.
  * ---------------------------------------------------------------------- */
 typedef struct {
   uint32_t struct_size;
@@ -259,6 +302,8 @@ typedef struct {
   int32_t n_cand;           /* candidate blocks per row */
   int32_t *cand_out;        /* i32 [n_rows, n_cand] or NULL: level-one selection */
   const int32_t *cand_in;   /* i32 [n_rows, n_cand] or NULL: reindex candidates */
+  int32_t key_fmt;          /* csa_cache_fmt_t: CSA_FMT_INT8 (0 reads as INT8) or FP4_E8M0 */
+  const uint8_t *key_scale_pool; /* FP4_E8M0: scale bytes [n_blocks, 128, 4] */
 } csa_index_args;
 
 CSA_API csa_status_t csa_index_topk(csa_index_args *args, csa_stream_t stream);
@@ -332,6 +377,13 @@ CSA_API csa_status_t csa_index_topk_noalloc(csa_index_args *args, csa_stream_t s
  * workspace (the size query returns 0; a workspace passed in is unused, but
  * a non-null pointer is what makes the call launch).  Both compute
  * the same function.
+ *
+ * Low-bit caches (see csa_cache_fmt_t): kv_fmt CSA_FMT_MXFP8 reads kv_pool
+ * as uint8 [*, 128, 512] with kv_scale_pool; cmp_fmt CSA_FMT_FP4_E4M3 reads
+ * cmp_pool as uint8 [*, 128, 256] with cmp_scale_pool.  Each candidate row is
+ * dequantised (exactly: every such value is a BF16 value) as it is gathered.
+ * A struct_size that ends before kv_fmt reads both pools as BF16.  The
+ * prefill call supports only BF16 pools (CSA_ERR_UNSUPPORTED otherwise).
  * ---------------------------------------------------------------------- */
 typedef struct {
   uint32_t struct_size;
@@ -367,6 +419,10 @@ typedef struct {
   uint32_t *status_dev;
   void *workspace;
   size_t workspace_bytes;
+  int32_t kv_fmt;  /* csa_cache_fmt_t: CSA_FMT_BF16 (0) or CSA_FMT_MXFP8 */
+  int32_t cmp_fmt; /* csa_cache_fmt_t: CSA_FMT_BF16 (0) or CSA_FMT_FP4_E4M3 */
+  const uint8_t *kv_scale_pool;  /* MXFP8: scale bytes [kv_n_blocks, 128, 16] */
+  const uint8_t *cmp_scale_pool; /* FP4_E4M3: scale bytes [cmp_n_blocks, 128, 32] */
 } csa_attn_args;
 
 CSA_API csa_status_t csa_sparse_attn_decode(csa_attn_args *args, csa_stream_t stream);

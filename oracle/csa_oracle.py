@@ -220,6 +220,21 @@ class LowBitPool:
             return dequant_fp4(codes, sbytes, 16, "e4m3")
         return dequant_fp4(codes, sbytes, 32, "e8m0")
 
+    def dequant_rows(self, codes, sbytes):
+        """``dequant_row`` of every row of codes [n, bytes] / sbytes [n, groups]."""
+        codes = np.asarray(codes, dtype=np.int64)
+        sbytes = np.asarray(sbytes, dtype=np.int64)
+        if self.fmt == "mxfp8":
+            vals, scl, group = e4m3_decode(codes), e8m0_decode(sbytes), 32
+        else:
+            nib = np.stack([codes & 15, codes >> 4], axis=-1).reshape(len(codes), -1)
+            vals = e2m1_decode(nib)
+            if self.fmt == "fp4_e4m3":
+                scl, group = e4m3_decode(sbytes), 16
+            else:
+                scl, group = e8m0_decode(sbytes), 32
+        return vals * np.repeat(scl, group, axis=1)
+
 
 # --------------------------------------------------------------------------
 # RoPE (DeepSeek V4.1 Flash, "Serving-owned full RoPE tables")
@@ -289,11 +304,7 @@ def cache_rows(pool, table_row, logical):
     logical = list(logical)
     codes = page_rows(pool.codes, table_row, logical).astype(np.int64)
     scales = page_rows(pool.scales, table_row, logical).astype(np.int64)
-    D = codes.shape[1] * (1 if pool.fmt == "mxfp8" else 2)
-    out = np.zeros((len(logical), D))
-    for i in range(len(logical)):
-        out[i] = pool.dequant_row(codes[i], scales[i])
-    return out
+    return pool.dequant_rows(codes, scales)
 
 
 def page_rows(pool, table_row, logical):

@@ -15,7 +15,27 @@ from . import csa_oracle as O
 
 
 def clone_pools(t):
-    return {k: t[k].clone() for k in ("cmp_pool", "idx_pool", "idx_scale")}
+    keys = ("cmp_pool", "idx_pool", "idx_scale", "cmp_scale", "idx_kscale")
+    return {k: t[k].clone() for k in keys if k in t}
+
+
+def _lowbit(t):
+    return "cmp_scale" in t
+
+
+def _idx_pool(t, pools):
+    """The index-key pool as the oracle reads it (FP4 keys: a LowBitPool)."""
+    if _lowbit(t):
+        return O.LowBitPool(pools["idx_pool"], pools["idx_kscale"], "fp4_e8m0")
+    return pools["idx_pool"]
+
+
+def _kv_pools(t, pools):
+    """(window pool, compressed pool) as the oracle reads them."""
+    if _lowbit(t):
+        return (O.LowBitPool(t["kv_pool"], t["kv_scale"], "mxfp8"),
+                O.LowBitPool(pools["cmp_pool"], pools["cmp_scale"], "fp4_e4m3"))
+    return t["kv_pool"], pools["cmp_pool"]
 
 
 def compress_step(t, spec, pools=None):
@@ -25,14 +45,16 @@ def compress_step(t, spec, pools=None):
 
     Returns (pools, main_results, idx_results)."""
     pools = clone_pools(t) if pools is None else pools
+    lowbit = _lowbit(t)
     idx_kw = dict(rotate=True, rope_cos=t["rope_cos"], rope_sin=t["rope_sin"],
-                  rope_dim=spec.rope_dim, out="int8")
+                  rope_dim=spec.rope_dim, out="fp4_e8m0" if lowbit else "int8")
+    main_out = "fp4_e4m3" if lowbit else "bf16"
     if spec.state:
         pools["state_main"] = O.as_f64(t["state_main"]).copy()
         table = t["state_table"].numpy()
         main = O.compress_stateful(t["kv_raw"], t["kv_raw"], t["w_gate"], t["ape"], spec.ratio,
                                    t["row_pos"], t["row_req"], pools["state_main"], table,
-                                   out="bf16")
+                                   out=main_out)
         idx = []
         if not spec.dense:  # HCA has no indexer, hence no index-key compressor
             pools["state_idx"] = O.as_f64(t["state_idx"]).copy()
@@ -41,11 +63,21 @@ def compress_step(t, spec, pools=None):
                                       table, **idx_kw)
     else:
         main = O.compress(t["kv_raw"], t["kv_raw"], t["w_gate"], t["ape"], spec.ratio,
-                          t["row_pos"], t["row_req"], out="bf16")
+                          t["row_pos"], t["row_req"], out=main_out)
         idx = [] if spec.dense else O.compress(t["idx_raw"], t["idx_raw"], t["w_gate_i"],
                                                  t["ape_i"], spec.ratio, t["row_pos"],
                                                  t["row_req"], **idx_kw)
     table = t["cmp_table"].numpy()
+    if lowbit:  # packed codes and scale bytes
+        for b, g, codes, sb in main:
+            pg = int(table[b, g // O.BLOCK])
+            pools["cmp_pool"][pg, g % O.BLOCK] = torch.from_numpy(codes)
+            pools["cmp_scale"][pg, g % O.BLOCK] = torch.from_numpy(sb)
+        for b, g, codes, sb in idx:
+            pg = int(table[b, g // O.BLOCK])
+            pools["idx_pool"][pg, g % O.BLOCK] = torch.from_numpy(codes)
+            pools["idx_kscale"][pg, g % O.BLOCK] = torch.from_numpy(sb)
+        return pools, main, idx
     for b, g, vals in main:
         pg = int(table[b, g // O.BLOCK])
         pools["cmp_pool"][pg, g % O.BLOCK] = torch.from_numpy(vals).to(torch.bfloat16)
@@ -60,7 +92,7 @@ def index_row(t, spec, pools, row, relu=True):
     b = int(t["row_req"][row])
     p = int(t["row_pos"][row])
     return O.index_scores(t["q_idx"][row], t["idx_w"][row], p, int(t["n_cmp"][b]), spec.ratio,
-                          pools["idx_pool"], pools["idx_scale"], t["cmp_table"][b].numpy(),
+                          _idx_pool(t, pools), pools.get("idx_scale"), t["cmp_table"][b].numpy(),
                           relu=relu, rope_cos=t["rope_cos"], rope_sin=t["rope_sin"],
                           rope_dim=spec.rope_dim)
 
@@ -68,8 +100,9 @@ def index_row(t, spec, pools, row, relu=True):
 def attention_row(t, spec, pools, row, topk_row, inv_rope_out=False, use_sink=True):
     b = int(t["row_req"][row])
     p = int(t["row_pos"][row])
-    return O.sparse_attention(t["q"][row], p, topk_row, t["kv_pool"], t["kv_table"][b].numpy(),
-                              pools["cmp_pool"], t["cmp_table"][b].numpy(),
+    kv_pool, cmp_pool = _kv_pools(t, pools)
+    return O.sparse_attention(t["q"][row], p, topk_row, kv_pool, t["kv_table"][b].numpy(),
+                              cmp_pool, t["cmp_table"][b].numpy(),
                               t["sink"] if use_sink else None, 1.0 / np.sqrt(spec.head_dim),
                               window=spec.window, rope_cos=t["rope_cos"],
                               rope_sin=t["rope_sin"], rope_dim=spec.rope_dim,

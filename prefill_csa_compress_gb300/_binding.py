@@ -21,6 +21,7 @@ CSA_OK, CSA_ERR_INVALID_ARG, CSA_ERR_UNSUPPORTED, CSA_ERR_CUDA, CSA_ERR_TIMEOUT 
 CSA_DEV_BAD_BLOCK, CSA_DEV_BAD_POS, CSA_DEV_BAD_INDEX, CSA_DEV_POS_GE_CAP, CSA_DEV_TIMEOUT = (
     0x1, 0x2, 0x4, 0x8, 0x10)
 CSA_OUT_BF16, CSA_OUT_INT8 = 0, 1
+CSA_FMT_BF16, CSA_FMT_INT8, CSA_FMT_FP4_E4M3, CSA_FMT_FP4_E8M0, CSA_FMT_MXFP8 = 0, 1, 2, 3, 4
 CSA_MODE_AUTO, CSA_MODE_DECODE, CSA_MODE_PREFILL = 0, 1, 2
 KERNEL_IDS = {
     "compress_gate": 0, "compress_pool": 1, "compress_fused": 2, "index_score": 3,
@@ -46,7 +47,7 @@ class CompressArgs(ctypes.Structure):
         ("idx_scale_pool", c_void_p), ("status_dev", c_void_p), ("workspace", c_void_p),
         ("workspace_bytes", c_size_t), ("state_cache", c_void_p),
         ("state_block_table", c_void_p), ("n_state_blocks", c_int32),
-        ("state_capacity", c_int32),
+        ("state_capacity", c_int32), ("scale_pool", c_void_p),
     ]
 
 
@@ -62,7 +63,7 @@ class IndexArgs(ctypes.Structure):
         ("topk_score", c_void_p), ("scores", c_void_p), ("score_cols", c_int32),
         ("status_dev", c_void_p), ("workspace", c_void_p), ("workspace_bytes", c_size_t),
         ("cand_block", c_int32), ("n_cand", c_int32), ("cand_out", c_void_p),
-        ("cand_in", c_void_p),
+        ("cand_in", c_void_p), ("key_fmt", c_int32), ("key_scale_pool", c_void_p),
     ]
 
 
@@ -78,6 +79,8 @@ class AttnArgs(ctypes.Structure):
         ("n_cmp", c_void_p), ("n_req", c_int32), ("sink", c_void_p), ("rope_cos", c_void_p),
         ("rope_sin", c_void_p), ("rope_cap", c_int32), ("out", c_void_p), ("lse", c_void_p),
         ("status_dev", c_void_p), ("workspace", c_void_p), ("workspace_bytes", c_size_t),
+        ("kv_fmt", c_int32), ("cmp_fmt", c_int32), ("kv_scale_pool", c_void_p),
+        ("cmp_scale_pool", c_void_p),
     ]
 
 
@@ -168,6 +171,14 @@ def prof_disable() -> None:
 # ---------------------------------------------------------------- marshalling helpers
 
 
+def _shape(t, want, name):
+    """Checks a tensor's shape (None matches any size)."""
+    if t is None or t.dim() != len(want) or any(w is not None and int(g) != w
+                                                   for g, w in zip(t.shape, want)):
+        raise ValueError(f"{name} must have shape {want}, got "
+                         f"{None if t is None else tuple(t.shape)}")
+
+
 def _p(t, dtype=None, name="tensor"):
     if t is None:
         return None
@@ -233,17 +244,20 @@ def _fill_common_rope(args, rope_cos, rope_sin):
 # ---------------------------------------------------------------- the four calls
 
 
+_OUT_MODES = {"bf16": 0, "int8": 1, "fp4_e4m3": 2, "fp4_e8m0": 3}
+
+
 def _compress_struct(*, x, kv, w_gate, ape, ratio, positions, row_req, block_table, out="bf16",
-                     cmp_pool=None, idx_pool=None, idx_scale_pool=None, gamma=None, rms_eps=1e-6,
-                     rotate=False, rope_cos=None, rope_sin=None, status=None, state_cache=None,
-                     state_block_table=None):
+                     cmp_pool=None, idx_pool=None, idx_scale_pool=None, scale_pool=None,
+                     gamma=None, rms_eps=1e-6, rotate=False, rope_cos=None, rope_sin=None,
+                     status=None, state_cache=None, state_block_table=None):
     a = CompressArgs()
     a.struct_size = ctypes.sizeof(CompressArgs)
     a.n_rows = int(x.shape[0])
     a.ratio = int(ratio)
     a.dx = int(x.shape[1])
     a.d = int(kv.shape[1])
-    a.out_mode = CSA_OUT_BF16 if out == "bf16" else CSA_OUT_INT8
+    a.out_mode = _OUT_MODES[out]
     a.rotate = 1 if rotate else 0
     a.x = _p(x, torch.bfloat16, "x")
     a.kv = _p(kv, torch.bfloat16, "kv")
@@ -258,6 +272,13 @@ def _compress_struct(*, x, kv, w_gate, ape, ratio, positions, row_req, block_tab
     a.n_req, a.max_blocks = int(block_table.shape[0]), int(block_table.shape[1])
     if a.out_mode == CSA_OUT_BF16:
         a.cmp_pool = _p(cmp_pool, torch.bfloat16, "cmp_pool")
+        a.n_blocks = int(cmp_pool.shape[0])
+    elif out.startswith("fp4"):  # packed codes into cmp_pool, scale bytes into scale_pool
+        group = 16 if out == "fp4_e4m3" else 32
+        _shape(cmp_pool, (None, 128, a.d // 2), "cmp_pool")
+        _shape(scale_pool, (cmp_pool.shape[0], 128, a.d // group), "scale_pool")
+        a.cmp_pool = _p(cmp_pool, torch.uint8, "cmp_pool")
+        a.scale_pool = _p(scale_pool, torch.uint8, "scale_pool")
         a.n_blocks = int(cmp_pool.shape[0])
     else:
         a.idx_pool = _p(idx_pool, torch.int8, "idx_pool")
@@ -274,7 +295,8 @@ def _compress_struct(*, x, kv, w_gate, ape, ratio, positions, row_req, block_tab
 def csa_compress(*, workspace=None, stream=None, prepare=False, **kw):
     """Gated compression of the chunk's complete groups into a paged pool
     (``include/csa.h``: csa_compress).  Keywords: x, kv, w_gate, ape, ratio,
-    positions, row_req, block_table, out ("bf16" or "int8"), cmp_pool or
+    positions, row_req, block_table, out ("bf16", "int8", "fp4_e4m3" or
+    "fp4_e8m0"), cmp_pool (bf16; uint8 codes for fp4 with scale_pool) or
     idx_pool + idx_scale_pool, gamma, rms_eps, rotate, rope_cos, rope_sin,
     status, and for the recurrent state ring state_cache (FP32 [blocks,
     capacity, 2 d]) with state_block_table (INT32 [n_req])."""
@@ -309,13 +331,15 @@ def csa_compress_pair(first: dict, second: dict, *, workspaces=(None, None), str
 def csa_index_topk(*, q_idx, weights, row_req, row_pos, n_cmp, ratio, idx_pool, idx_scale_pool,
                    cmp_block_table, topk, topk_idx, topk_score=None, scores=None, relu=True,
                    rope_cos=None, rope_sin=None, mode=CSA_MODE_AUTO, status=None,
-                   cand_out=None, cand_in=None, cand_block=8, workspace=None, stream=None,
-                   prepare=False):
+                   cand_out=None, cand_in=None, cand_block=8, key_scale_pool=None,
+                   workspace=None, stream=None, prepare=False):
     """Indexer scores and deterministic top-k (``include/csa.h``: csa_index_topk).
 
     ``cand_out`` (i32 [n_rows, n_cand]) also selects the level-one candidate
     blocks; ``cand_in`` restricts scoring and selection to given candidate
-    blocks (reindex)."""
+    blocks (reindex).  With ``key_scale_pool`` (uint8 [blocks, 128, 4]) the
+    keys are FP4 (``idx_pool`` uint8 [blocks, 128, 64]: packed E2M1 with E8M0
+    scales per 32 dims) and ``idx_scale_pool`` is unused."""
     a = IndexArgs()
     a.struct_size = ctypes.sizeof(IndexArgs)
     a.n_rows = int(q_idx.shape[0])
@@ -330,8 +354,16 @@ def csa_index_topk(*, q_idx, weights, row_req, row_pos, n_cmp, ratio, idx_pool, 
     a.row_req = _p(row_req, torch.int32, "row_req")
     a.row_pos = _p(row_pos, torch.int32, "row_pos")
     a.n_cmp = _p(n_cmp, torch.int32, "n_cmp")
-    a.idx_pool = _p(idx_pool, torch.int8, "idx_pool")
-    a.idx_scale_pool = _p(idx_scale_pool, torch.float32, "idx_scale_pool")
+    if key_scale_pool is not None:
+        _shape(idx_pool, (None, 128, 64), "idx_pool")
+        _shape(key_scale_pool, (idx_pool.shape[0], 128, 4), "key_scale_pool")
+        a.key_fmt = CSA_FMT_FP4_E8M0
+        a.idx_pool = _p(idx_pool, torch.uint8, "idx_pool")
+        a.key_scale_pool = _p(key_scale_pool, torch.uint8, "key_scale_pool")
+    else:
+        a.key_fmt = CSA_FMT_INT8
+        a.idx_pool = _p(idx_pool, torch.int8, "idx_pool")
+        a.idx_scale_pool = _p(idx_scale_pool, torch.float32, "idx_scale_pool")
     a.cmp_block_table = _p(cmp_block_table, torch.int32, "cmp_block_table")
     a.n_req, a.max_blocks = int(cmp_block_table.shape[0]), int(cmp_block_table.shape[1])
     a.n_blocks = int(idx_pool.shape[0])
@@ -384,9 +416,14 @@ def csa_index_topk_noalloc(*, q_idx, weights, row_req, row_pos, n_cmp, ratio, id
 def _attn(fn_name, *, q, row_req, row_pos, topk_idx, kv_pool, kv_block_table, kv_len, cmp_pool,
           cmp_block_table, n_cmp, ratio, out, lse=None, sink=None, softmax_scale=None,
           window=128, rope_cos=None, rope_sin=None, inv_rope_out=False, status=None,
-          workspace=None, stream=None, prepare=False, dense_cap=0):
+          workspace=None, stream=None, prepare=False, dense_cap=0, kv_scale_pool=None,
+          cmp_scale_pool=None):
     """``topk_idx=None`` with ``dense_cap > 0``: every visible compressed entry
-    (up to dense_cap) is a candidate (dense visibility, HCA)."""
+    (up to dense_cap) is a candidate (dense visibility, HCA).  With
+    ``kv_scale_pool`` the window pool is MXFP8 (uint8 [blocks, 128, 512] codes,
+    uint8 [blocks, 128, 16] scales); with ``cmp_scale_pool`` the compressed
+    pool is FP4 (uint8 [blocks, 128, 256] codes, [blocks, 128, 32] E4M3
+    scales)."""
     a = AttnArgs()
     a.struct_size = ctypes.sizeof(AttnArgs)
     a.n_rows = int(q.shape[0])
@@ -401,12 +438,23 @@ def _attn(fn_name, *, q, row_req, row_pos, topk_idx, kv_pool, kv_block_table, kv
     a.row_req = _p(row_req, torch.int32, "row_req")
     a.row_pos = _p(row_pos, torch.int32, "row_pos")
     a.topk_idx = _p(topk_idx, torch.int32, "topk_idx")
-    a.kv_pool = _p(kv_pool, torch.bfloat16, "kv_pool")
+    kv_lb, cmp_lb = kv_scale_pool is not None, cmp_scale_pool is not None
+    if kv_lb:
+        _shape(kv_pool, (None, 128, 512), "kv_pool")
+        _shape(kv_scale_pool, (kv_pool.shape[0], 128, 16), "kv_scale_pool")
+    if cmp_lb:
+        _shape(cmp_pool, (None, 128, 256), "cmp_pool")
+        _shape(cmp_scale_pool, (cmp_pool.shape[0], 128, 32), "cmp_scale_pool")
+    a.kv_fmt = CSA_FMT_MXFP8 if kv_lb else CSA_FMT_BF16
+    a.cmp_fmt = CSA_FMT_FP4_E4M3 if cmp_lb else CSA_FMT_BF16
+    a.kv_scale_pool = _p(kv_scale_pool, torch.uint8, "kv_scale_pool")
+    a.cmp_scale_pool = _p(cmp_scale_pool, torch.uint8, "cmp_scale_pool")
+    a.kv_pool = _p(kv_pool, torch.uint8 if kv_lb else torch.bfloat16, "kv_pool")
     a.kv_block_table = _p(kv_block_table, torch.int32, "kv_block_table")
     a.kv_max_blocks = int(kv_block_table.shape[1])
     a.kv_n_blocks = int(kv_pool.shape[0])
     a.kv_len = _p(kv_len, torch.int32, "kv_len")
-    a.cmp_pool = _p(cmp_pool, torch.bfloat16, "cmp_pool")
+    a.cmp_pool = _p(cmp_pool, torch.uint8 if cmp_lb else torch.bfloat16, "cmp_pool")
     a.cmp_block_table = _p(cmp_block_table, torch.int32, "cmp_block_table")
     a.cmp_max_blocks = int(cmp_block_table.shape[1])
     a.cmp_n_blocks = int(cmp_pool.shape[0])

@@ -71,6 +71,22 @@ csa_index_args full_index_args(const csa_index_args *a) {
   return f;
 }
 
+bool index_pointers_ok(const csa_index_args *a) {
+  const bool fp4 = a->key_fmt == CSA_FMT_FP4_E8M0;
+  if (!a->q_idx || !a->weights || !a->row_req || !a->row_pos || !a->n_cmp || !a->idx_pool ||
+      !a->cmp_block_table || !a->topk_idx)
+    return false;
+  if (fp4 ? !a->key_scale_pool : !a->idx_scale_pool) return false;
+  if (a->n_req <= 0 || a->n_blocks <= 0) return false;
+  if ((a->rope_cos == nullptr) != (a->rope_sin == nullptr)) return false;
+  if (a->rope_cos && a->rope_cap <= 0) return false;
+  const void *scales = fp4 ? static_cast<const void *>(a->key_scale_pool)
+                           : static_cast<const void *>(a->idx_scale_pool);
+  const uintptr_t m = reinterpret_cast<uintptr_t>(a->idx_pool) |
+                      reinterpret_cast<uintptr_t>(a->q_idx) | reinterpret_cast<uintptr_t>(scales);
+  return (m & 15u) == 0;
+}
+
 bool index_struct_ok(const csa_index_args *a) {
   return a && a->struct_size >= offsetof(csa_index_args, cand_block);
 }
@@ -89,7 +105,7 @@ csa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_E
 
 // shape checks (enough to size the workspace)
 csa_status_t check_attn_shape(const csa_attn_args *a) {
-  if (!a || a->struct_size < sizeof(csa_attn_args)) return CSA_ERR_INVALID_ARG;
+  if (!a) return CSA_ERR_INVALID_ARG;
   if (a->n_rows < 0 || a->n_req < 0 || a->topk < 0 || a->topk > CSA_MAX_TOPK)
     return CSA_ERR_INVALID_ARG;
   if (a->n_heads != kHeads || a->head_dim != kHeadDim || a->window != kWindow)
@@ -110,14 +126,31 @@ csa_status_t check_attn_args(const csa_attn_args *a) {
     return CSA_ERR_INVALID_ARG;
   if (!aligned16(a->q) || !aligned16(a->kv_pool) || !aligned16(a->cmp_pool) || !aligned16(a->out))
     return CSA_ERR_INVALID_ARG;
+  if (a->kv_fmt == CSA_FMT_MXFP8 && !a->kv_scale_pool) return CSA_ERR_INVALID_ARG;
+  if (a->cmp_fmt == CSA_FMT_FP4_E4M3 &&
+      (!a->cmp_scale_pool || (reinterpret_cast<uintptr_t>(a->cmp_scale_pool) & 1u)))
+    return CSA_ERR_INVALID_ARG;
   return CSA_OK;
 }
 
-csa_status_t run_attn(csa_attn_args *a, cudaStream_t s, bool decode) {
+csa_status_t run_attn(csa_attn_args *user, cudaStream_t s, bool decode) {
+  // the arguments as this library's struct: a caller built against the header
+  // without the cache-format fields reads both pools as BF16
+  if (!user || user->struct_size < offsetof(csa_attn_args, kv_fmt)) return CSA_ERR_INVALID_ARG;
+  csa_attn_args A;
+  memset(&A, 0, sizeof(A));
+  memcpy(&A, user, user->struct_size < sizeof(A) ? user->struct_size : sizeof(A));
+  A.struct_size = sizeof(A);
+  csa_attn_args *a = &A;
   csa_status_t st = check_attn_shape(a);
   if (st != CSA_OK) return st;
+  if ((a->kv_fmt != CSA_FMT_BF16 && a->kv_fmt != CSA_FMT_MXFP8) ||
+      (a->cmp_fmt != CSA_FMT_BF16 && a->cmp_fmt != CSA_FMT_FP4_E4M3))
+    return CSA_ERR_UNSUPPORTED;
+  if (!decode && (a->kv_fmt != CSA_FMT_BF16 || a->cmp_fmt != CSA_FMT_BF16))
+    return CSA_ERR_UNSUPPORTED;
   if (!a->workspace) {  // neither path needs scratch memory
-    a->workspace_bytes = 0;
+    user->workspace_bytes = 0;
     return CSA_OK;
   }
   if (a->n_rows == 0) return CSA_OK;
@@ -159,7 +192,7 @@ static csa_status_t check_compress(csa_compress_args *a, bool *size_query) {
     return CSA_ERR_UNSUPPORTED;
   if (a->d != 128 && a->d != 512) return CSA_ERR_UNSUPPORTED;
   if (a->dx <= 0 || a->dx % 64 != 0 || a->dx > 1024) return CSA_ERR_UNSUPPORTED;
-  if (a->out_mode != CSA_OUT_BF16 && a->out_mode != CSA_OUT_INT8) return CSA_ERR_INVALID_ARG;
+  if (a->out_mode < CSA_OUT_BF16 || a->out_mode > CSA_OUT_FP4_E8M0) return CSA_ERR_INVALID_ARG;
   const size_t need = align_up((size_t)a->n_rows * a->d * sizeof(float), kAlign);
   if (!a->workspace) {
     a->workspace_bytes = need;
@@ -174,6 +207,9 @@ static csa_status_t check_compress(csa_compress_args *a, bool *size_query) {
   if (a->n_req <= 0 || a->max_blocks <= 0 || a->n_blocks <= 0) return CSA_ERR_INVALID_ARG;
   if (a->out_mode == CSA_OUT_BF16 && !a->cmp_pool) return CSA_ERR_INVALID_ARG;
   if (a->out_mode == CSA_OUT_INT8 && (!a->idx_pool || !a->idx_scale_pool))
+    return CSA_ERR_INVALID_ARG;
+  if ((a->out_mode == CSA_OUT_FP4_E4M3 || a->out_mode == CSA_OUT_FP4_E8M0) &&
+      (!a->cmp_pool || !a->scale_pool))
     return CSA_ERR_INVALID_ARG;
   if (a->rotate && (!a->rope_cos || !a->rope_sin || a->rope_cap <= 0)) return CSA_ERR_INVALID_ARG;
   if (!aligned16(a->x) || !aligned16(a->kv) || !aligned16(a->w_gate)) return CSA_ERR_INVALID_ARG;
@@ -271,6 +307,8 @@ CSA_API csa_status_t csa_index_topk(csa_index_args *user, csa_stream_t stream) {
   if (a->n_heads != kHeads || a->head_dim != kIdxDim) return CSA_ERR_UNSUPPORTED;
   if (a->topk < 1 || a->topk > CSA_MAX_TOPK || a->ratio < 1) return CSA_ERR_INVALID_ARG;
   if (a->max_blocks <= 0) return CSA_ERR_INVALID_ARG;
+  if (a->key_fmt != 0 && a->key_fmt != CSA_FMT_INT8 && a->key_fmt != CSA_FMT_FP4_E8M0)
+    return CSA_ERR_UNSUPPORTED;
   const bool lvl1 = a->cand_out != nullptr, reidx = a->cand_in != nullptr;
   int cb_shift = 3;
   if (lvl1 || reidx) {
@@ -289,14 +327,7 @@ CSA_API csa_status_t csa_index_topk(csa_index_args *user, csa_stream_t stream) {
   }
   if (a->workspace_bytes < L.total) return CSA_ERR_INVALID_ARG;
   if (a->n_rows == 0) return CSA_OK;
-  if (!a->q_idx || !a->weights || !a->row_req || !a->row_pos || !a->n_cmp || !a->idx_pool ||
-      !a->idx_scale_pool || !a->cmp_block_table || !a->topk_idx)
-    return CSA_ERR_INVALID_ARG;
-  if (a->n_req <= 0 || a->n_blocks <= 0) return CSA_ERR_INVALID_ARG;
-  if ((a->rope_cos == nullptr) != (a->rope_sin == nullptr)) return CSA_ERR_INVALID_ARG;
-  if (a->rope_cos && a->rope_cap <= 0) return CSA_ERR_INVALID_ARG;
-  if (!aligned16(a->idx_pool) || !aligned16(a->q_idx) || !aligned16(a->idx_scale_pool))
-    return CSA_ERR_INVALID_ARG;
+  if (!index_pointers_ok(a)) return CSA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t *ws = static_cast<uint8_t *>(a->workspace);
   float *scores = own_scores ? a->scores : reinterpret_cast<float *>(ws + L.scores);

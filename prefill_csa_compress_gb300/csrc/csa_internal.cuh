@@ -103,6 +103,8 @@ cudaError_t launch_index_topk(const csa_index_args &a, const float *scores, int 
 // covers every field before the hierarchical-indexer ones.
 csa_index_args full_index_args(const csa_index_args *a);
 bool index_struct_ok(const csa_index_args *a);
+// Pointer, count and alignment checks of a launching index call.
+bool index_pointers_ok(const csa_index_args *a);
 bool topk_is_long(int n_cap);
 size_t topk_ws_bytes(int n_rows, int n_cap);
 uint32_t *topk_counters(void *ws, int n_rows, int n_cap);

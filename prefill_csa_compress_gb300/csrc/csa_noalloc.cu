@@ -55,16 +55,9 @@ extern "C" CSA_API csa_status_t csa_index_topk_noalloc(csa_index_args *user,
   if (!own_scores && (long long)a->n_rows * n_cap > (long long)kMaxScores)
     return CSA_ERR_UNSUPPORTED;
   if (a->n_rows == 0) return CSA_OK;
-  if (!a->q_idx || !a->weights || !a->row_req || !a->row_pos || !a->n_cmp || !a->idx_pool ||
-      !a->idx_scale_pool || !a->cmp_block_table || !a->topk_idx)
-    return CSA_ERR_INVALID_ARG;
-  if (a->n_req <= 0 || a->n_blocks <= 0) return CSA_ERR_INVALID_ARG;
-  if ((a->rope_cos == nullptr) != (a->rope_sin == nullptr)) return CSA_ERR_INVALID_ARG;
-  if (a->rope_cos && a->rope_cap <= 0) return CSA_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(a->idx_pool) & 15u) ||
-      (reinterpret_cast<uintptr_t>(a->q_idx) & 15u) ||
-      (reinterpret_cast<uintptr_t>(a->idx_scale_pool) & 15u))
-    return CSA_ERR_INVALID_ARG;
+  if (a->key_fmt != 0 && a->key_fmt != CSA_FMT_INT8 && a->key_fmt != CSA_FMT_FP4_E8M0)
+    return CSA_ERR_UNSUPPORTED;
+  if (!index_pointers_ok(a)) return CSA_ERR_INVALID_ARG;
   float *scores = a->scores;
   int cols = a->score_cols;
   if (!own_scores) {

@@ -26,6 +26,7 @@
 #include <cstring>
 
 #include "attn_common.cuh"
+#include "lowbit.cuh"
 
 namespace csa {
 namespace {
@@ -41,7 +42,7 @@ struct AdMisc {
   uint32_t tmem_base;
   int pad;
   SoftState st;
-  const uint16_t *src[CT];  // pool row of each candidate of the tile, or null
+  const uint8_t *src[CT];   // pool row of each candidate of the tile, or null
   alignas(16) float m_all[AD_MAX_CLUSTER][kHeads];  // every CTA's reference per head (log2)
   alignas(16) float l_all[AD_MAX_CLUSTER][kHeads];  // every CTA's denominator per head
   alignas(16) float red_l[4][kHeads];
@@ -58,10 +59,18 @@ __device__ __forceinline__ int chan_lo(uint32_t r, uint32_t S) {
   return 16 * (int)((kHeadDim / 16 * r) / S);
 }
 
+// Bytes of one pool row in the pool's format.
+__device__ __forceinline__ int cmp_row_bytes(const csa_attn_args &a) {
+  return a.cmp_fmt == CSA_FMT_FP4_E4M3 ? kHeadDim / 2 : kHeadDim * 2;
+}
+__device__ __forceinline__ int kv_row_bytes(const csa_attn_args &a) {
+  return a.kv_fmt == CSA_FMT_MXFP8 ? kHeadDim : kHeadDim * 2;
+}
+
 // Pool row of candidate j of row t (its list: top-k entries, then the
 // window), or null when absent; data errors raise their flag.
-__device__ __forceinline__ const uint16_t *candidate_row(const csa_attn_args &a, int t, int b,
-                                                         int p, int V, int kvl, int j) {
+__device__ __forceinline__ const uint8_t *candidate_row(const csa_attn_args &a, int t, int b,
+                                                        int p, int V, int kvl, int j) {
   if (j < a.topk) {
     // dense visibility (no selection): compressed entry j itself
     const int c = a.topk_idx ? a.topk_idx[(long long)t * a.topk + j] : (j < V ? j : -1);
@@ -73,7 +82,7 @@ __device__ __forceinline__ const uint16_t *candidate_row(const csa_attn_args &a,
     }
     const long long row =
         page_row(a.cmp_block_table, a.cmp_max_blocks, a.cmp_n_blocks, b, c, a.status_dev);
-    return row < 0 ? nullptr : static_cast<const uint16_t *>(a.cmp_pool) + row * kHeadDim;
+    return row < 0 ? nullptr : static_cast<const uint8_t *>(a.cmp_pool) + row * cmp_row_bytes(a);
   }
   if (j >= a.topk + a.window) return nullptr;
   const int pp = p - a.window + 1 + (j - a.topk);
@@ -84,7 +93,75 @@ __device__ __forceinline__ const uint16_t *candidate_row(const csa_attn_args &a,
   }
   const long long row =
       page_row(a.kv_block_table, a.kv_max_blocks, a.kv_n_blocks, b, pp, a.status_dev);
-  return row < 0 ? nullptr : static_cast<const uint16_t *>(a.kv_pool) + row * kHeadDim;
+  return row < 0 ? nullptr : static_cast<const uint8_t *>(a.kv_pool) + row * kv_row_bytes(a);
+}
+
+// Gather of tile g when a pool holds a low-bit format ("DeepSeek V4.1 Flash",
+// production cache ABI: FP4 compressed KV with E4M3 scales per 16 channels,
+// MXFP8 window KV): unit = (candidate row, 32-channel slab), 16 consecutive
+// threads per row.  Every low-bit unit's codes and scales are loaded before
+// any is converted; each slab becomes 64 bytes of BF16 (exact) in the
+// 128-byte-swizzled tile.  BF16 rows and absent rows go through cp.async
+// (zero fill) as in the plain gather.
+constexpr int LB_UNITS = CT * (kHeadDim / 32) / AD_THREADS;  // 8 per thread
+
+__device__ __forceinline__ void gather_lowbit(const csa_attn_args &a, const AdMisc *M,
+                                              uint8_t *KVs, int g, int tid) {
+  uint4 c0[LB_UNITS], c1[LB_UNITS];
+  uint32_t sc[LB_UNITS];
+  int kind[LB_UNITS];  // 0: cp.async (BF16 or absent), 2: FP4 + E4M3, 3: MXFP8
+#pragma unroll
+  for (int i = 0; i < LB_UNITS; ++i) {
+    const int u = i * AD_THREADS + tid, r = u >> 4, slab = u & 15;
+    const uint8_t *row = M->src[r];
+    const bool is_cmp = g * CT + r < a.topk;
+    const int fmt = is_cmp ? a.cmp_fmt : a.kv_fmt;
+    kind[i] = !row ? 0 : (fmt == CSA_FMT_FP4_E4M3 ? 2 : (fmt == CSA_FMT_MXFP8 ? 3 : 0));
+    c0[i] = c1[i] = make_uint4(0u, 0u, 0u, 0u);
+    sc[i] = 0u;
+    if (kind[i] == 2) {
+      const long long ri = (row - static_cast<const uint8_t *>(a.cmp_pool)) / (kHeadDim / 2);
+      c0[i] = *reinterpret_cast<const uint4 *>(row + slab * 16);
+      sc[i] = *reinterpret_cast<const uint16_t *>(a.cmp_scale_pool + ri * (kHeadDim / 16) + slab * 2);
+    } else if (kind[i] == 3) {
+      const long long ri = (row - static_cast<const uint8_t *>(a.kv_pool)) / kHeadDim;
+      c0[i] = *reinterpret_cast<const uint4 *>(row + slab * 32);
+      c1[i] = *reinterpret_cast<const uint4 *>(row + slab * 32 + 16);
+      sc[i] = a.kv_scale_pool[ri * (kHeadDim / 32) + slab];
+    } else {
+      // BF16 row (or absent: zero fill): the slab's four 16-byte pieces
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int piece = (slab & 1) * 4 + q;
+        uint8_t *dst = KVs + (slab >> 1) * 16384 + r * 128 + ((piece ^ (r & 7)) << 4);
+        tc::cp_async16_zfill(dst, row ? row + slab * 64 + q * 16 : static_cast<const uint8_t *>(a.kv_pool),
+                             row != nullptr);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < LB_UNITS; ++i) {
+    if (kind[i] == 0) continue;
+    const int u = i * AD_THREADS + tid, r = u >> 4, slab = u & 15;
+    uint8_t *base = KVs + (slab >> 1) * 16384 + r * 128;
+    const float e8 = lowbit::pow2f((int)sc[i] - 127);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int piece = (slab & 1) * 4 + q;
+      uint4 v;
+      if (kind[i] == 2) {
+        const uint32_t w = q == 0 ? c0[i].x : q == 1 ? c0[i].y : q == 2 ? c0[i].z : c0[i].w;
+        v = lowbit::e2m1x8_e4m3_to_bf16x8(w, (sc[i] >> (8 * (q >> 1))) & 0xFFu);
+      } else {
+        const uint2 w = q == 0 ? make_uint2(c0[i].x, c0[i].y)
+                        : q == 1 ? make_uint2(c0[i].z, c0[i].w)
+                        : q == 2 ? make_uint2(c1[i].x, c1[i].y)
+                                 : make_uint2(c1[i].z, c1[i].w);
+        v = lowbit::e4m3x8_e8m0_to_bf16x8(w, e8);
+      }
+      *reinterpret_cast<uint4 *>(base + ((piece ^ (r & 7)) << 4)) = v;
+    }
+  }
 }
 
 __global__ void __launch_bounds__(AD_THREADS, 1)
@@ -158,6 +235,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   const int qd = warp & 3, h0 = (warp >> 2) * 32, c = qd * 32 + lane;
   const int sub = lane >> 3, piece = lane & 7;  // gather: rows 32 i + 4 warp + sub, 16-byte piece
   const float sl2 = a.softmax_scale * kLog2e;
+  const bool lowbit = a.kv_fmt == CSA_FMT_MXFP8 || a.cmp_fmt == CSA_FMT_FP4_E4M3;
   float lacc = 0.f;  // this warp's partial denominator of head h0 + lane
   bool first = true, ok = true, q_ready = false;
   uint32_t phase = 0;
@@ -168,8 +246,10 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     if (__syncthreads_count(tid < CT && M->src[tid] != nullptr) == 0) continue;
     const bool valid = M->src[c] != nullptr;
     // ---- gather the tile into the swizzled layout (the previous P.V is done)
-    {
-      const uint16_t *src[4];
+    if (lowbit) {
+      gather_lowbit(a, M, KVs, g, tid);
+    } else {
+      const uint8_t *src[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) src[i] = M->src[32 * i + 4 * warp + sub];
       for (int kc = 0; kc < 8; ++kc) {
@@ -177,8 +257,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = 32 * i + 4 * warp + sub;
-          const uint16_t *gsrc = src[i] ? src[i] + kc * 64 + piece * 8
-                                        : static_cast<const uint16_t *>(a.kv_pool);
+          const uint8_t *gsrc = src[i] ? src[i] + kc * 128 + piece * 16
+                                       : static_cast<const uint8_t *>(a.kv_pool);
           tc::cp_async16_zfill(dst + r * 128 + ((piece ^ (r & 7)) << 4), gsrc, src[i] != nullptr);
         }
       }

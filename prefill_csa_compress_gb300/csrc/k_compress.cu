@@ -12,6 +12,7 @@
 #include <cstring>
 
 #include "csa_internal.cuh"
+#include "lowbit.cuh"
 #include "tc.cuh"
 
 namespace csa {
@@ -177,6 +178,35 @@ cudaError_t launch_gate_gemm_tc(const csa_compress_args &a, float *logits, cudaS
 // takes the group's logits, softmax over its r rows per channel, the pooled
 // value and the BF16 / RMSNorm / RoPE / INT8 epilogue.
 // ---------------------------------------------------------------------------
+// Low-bit publication ("DeepSeek V4.1 Flash", production cache ABI; the
+// rounding rules are the ones include/csa.h states) of channel d (value y)
+// of pool row dst_row.  Called by every lane of a warp whose lanes hold
+// consecutive channels, groups of G lanes aligned to G; `live` marks lanes
+// that hold a channel.  G == 32: E8M0 scales; G == 16: E4M3 scales.
+template <int G>
+__device__ __forceinline__ void publish_fp4(const csa_compress_args &a, long long dst_row, int d,
+                                            float y, bool live) {
+  float v = live ? fabsf(y) : 0.f;
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  float scale;
+  uint32_t sbyte;
+  if constexpr (G == 32) {
+    const int e = lowbit::e8m0_exponent(v);
+    scale = lowbit::pow2f(e);
+    sbyte = (uint32_t)(e + 127);
+  } else {
+    sbyte = lowbit::e4m3_scale_byte(v);
+    scale = lowbit::e4m3_value(sbyte);
+  }
+  const uint32_t code = scale > 0.f ? lowbit::e2m1_code(__fdiv_rn(y, scale)) : 0u;
+  const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+  const int D = a.d;
+  if (live && (d & 1) == 0)
+    static_cast<uint8_t *>(a.cmp_pool)[dst_row * (D / 2) + d / 2] = (uint8_t)(code | (hi << 4));
+  if (live && d % G == 0) a.scale_pool[dst_row * (D / G) + d / G] = (uint8_t)sbyte;
+}
+
 __device__ __forceinline__ float block_sum(float v, float *red) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -319,6 +349,10 @@ __global__ void compress_pool_kernel(csa_compress_args a, const float *__restric
   if (a.out_mode == CSA_OUT_BF16) {
     __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.cmp_pool);
     dst[dst_row * D + d] = __float2bfloat16_rn(y);
+  } else if (a.out_mode == CSA_OUT_FP4_E4M3) {
+    publish_fp4<16>(a, dst_row, d, y, true);
+  } else if (a.out_mode == CSA_OUT_FP4_E8M0) {
+    publish_fp4<32>(a, dst_row, d, y, true);
   } else {
     float amax = block_max(fabsf(y), red);
     float scale = fmaxf(amax, 1e-4f) / 127.0f;
@@ -530,6 +564,10 @@ __device__ __forceinline__ void fused_group(const csa_compress_args &a, const in
   const long long dst_row = (long long)phys * kBlock + (g % kBlock);
   if (a.out_mode == CSA_OUT_BF16) {
     if (c < COLS) static_cast<__nv_bfloat16 *>(a.cmp_pool)[dst_row * D + d] = __float2bfloat16_rn(y);
+  } else if (a.out_mode == CSA_OUT_FP4_E4M3) {
+    publish_fp4<16>(a, dst_row, d, y, c < COLS);
+  } else if (a.out_mode == CSA_OUT_FP4_E8M0) {
+    publish_fp4<32>(a, dst_row, d, y, c < COLS);
   } else {
     float v = c < COLS ? fabsf(y) : 0.f;
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -583,7 +621,9 @@ size_t fused_smem(const csa_compress_args &a) {
 int fused_cols(const csa_compress_args &a) {
   if (a.n_rows > 256 || a.state_cache || a.ratio > 4) return 0;
   if (a.d == 128 && (size_t)a.dx * 128 * 2 <= FC_MAX_W_BYTES) return 128;
-  if (a.d == 512 && a.out_mode == CSA_OUT_BF16 && !a.gamma && (size_t)a.dx * 16 * 2 <= FC_MAX_W_BYTES)
+  // the 16-column tiles of d = 512 publish BF16 or E4M3-scaled groups of 16
+  if (a.d == 512 && (a.out_mode == CSA_OUT_BF16 || a.out_mode == CSA_OUT_FP4_E4M3) && !a.gamma &&
+      (size_t)a.dx * 16 * 2 <= FC_MAX_W_BYTES)
     return 16;
   return 0;
 }

@@ -29,6 +29,7 @@
 #include <cudaTypedefs.h>
 
 #include "csa_internal.cuh"
+#include "lowbit.cuh"
 #include "tc.cuh"
 
 namespace csa {
@@ -202,6 +203,9 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   const bool reidx = sel.cand_in != nullptr;
   const int cb = 1 << sel.cb_shift;
   const int RPG = reidx ? 1 : G;  // rows per group
+  // FP4 index keys ("DeepSeek V4.1 Flash", production cache ABI): packed E2M1
+  // with one E8M0 scale per 32 dims, copied linearly and decoded to FP16
+  const bool fp4 = a.key_fmt == CSA_FMT_FP4_E8M0;
   const bool rope = a.rope_cos != nullptr;
   const int n_kchunks = rope ? 3 : 2;
   const int n_cap = a.max_blocks * kBlock;
@@ -452,12 +456,18 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
           if (lane == 0) {
             M->st_ok[s] = (int)mask;
             if (n_ok)
-              tc::mbar_arrive_expect_tx(&M->st_full[s], n_ok * cb * (kIdxDim + 4));
+              tc::mbar_arrive_expect_tx(&M->st_full[s], n_ok * cb * ((fp4 ? 64 : kIdxDim) + 4));
             else
               tc::mbar_arrive(&M->st_full[s]);
           }
           __syncwarp();
-          if (grow >= 0) {
+          if (grow >= 0 && fp4) {
+            // FP4 keys: cb rows of 64 code bytes, cb words of scale bytes
+            tc::bulk_g2s(St + s * C::PAGE + lane * cb * 64, a.idx_pool + grow * 64, cb * 64,
+                         &M->st_full[s]);
+            tc::bulk_g2s(StSc + s * kBlock + lane * cb, a.key_scale_pool + grow * 4, cb * 4,
+                         &M->st_full[s]);
+          } else if (grow >= 0) {
             uint8_t *dst = St + s * C::PAGE + lane * cb * kIdxDim;
             if constexpr (C::ATMEM)
               tc::tma_load_2d(dst, &keys_map, 0, (int)grow, &M->st_full[s]);
@@ -483,7 +493,14 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
                                  : -1;
             const bool ok = phys >= 0 && phys < a.n_blocks;
             M->st_ok[s] = ok ? 0xFFFF : 0;
-            if (ok) {
+            if (ok && fp4) {
+              // FP4 keys: 8 KB of codes and 512 bytes of scales per page
+              tc::mbar_arrive_expect_tx(&M->st_full[s], kBlock * 64 + kBlock * 4);
+              tc::bulk_g2s(St + s * C::PAGE, a.idx_pool + (long long)phys * kBlock * 64, kBlock * 64,
+                           &M->st_full[s]);
+              tc::bulk_g2s(StSc + s * kBlock, a.key_scale_pool + (long long)phys * kBlock * 4,
+                           kBlock * 4, &M->st_full[s]);
+            } else if (ok) {
               tc::mbar_arrive_expect_tx(&M->st_full[s], C::PAGE + kBlock * 4);
               if constexpr (C::ATMEM)  // 128-byte swizzled rows: conflict-free row reads
                 tc::tma_load_2d(St + s * C::PAGE, &keys_map, 0, phys * kBlock, &M->st_full[s]);
@@ -514,7 +531,34 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
             // thread = one key row (TMEM lane) x one half of its 128 dims
             const int wq = (warp - W_CONV0) & 3, half = (warp - W_CONV0) >> 2;
             const int r = wq * 32 + lane;
-            if (ok) {
+            if (ok && fp4) {
+              // FP4 keys (64 code bytes and 4 E8M0 bytes per row): this half's
+              // 32 code bytes, each group scaled by 2^(E_g - R) into FP16
+              const uint8_t *src = St + s * C::PAGE + r * 64 + half * 32;
+              const uint32_t sb4 =
+                  reinterpret_cast<const uint32_t *>(StSc)[s * kBlock + r];
+              const int R = lowbit::e8m0_row_shift(sb4);
+              uint32_t packed[32];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(src + c * 8);
+                const __half2 sc2 = lowbit::e8m0_group_h2(sb4, half * 2 + (c >> 1), R);
+                const uint4 lo = lowbit::e2m1x8_to_f16x8(w.x, sc2);
+                const uint4 hi = lowbit::e2m1x8_to_f16x8(w.y, sc2);
+                packed[8 * c + 0] = lo.x;
+                packed[8 * c + 1] = lo.y;
+                packed[8 * c + 2] = lo.z;
+                packed[8 * c + 3] = lo.w;
+                packed[8 * c + 4] = hi.x;
+                packed[8 * c + 5] = hi.y;
+                packed[8 * c + 6] = hi.z;
+                packed[8 * c + 7] = hi.w;
+              }
+              tc::tmem_st32u(tmem + ((uint32_t)(wq * 32) << 16) + C::A_COL + j * 64 + half * 32,
+                             packed);
+              tc::tmem_wait_st();
+              if (half == 0) Sc[sc * kBlock + r] = lowbit::pow2f(R);
+            } else if (ok) {
               const uint8_t *src = St + s * C::PAGE + r * 128;
               uint32_t packed[32];
 #pragma unroll
@@ -540,7 +584,30 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
             if (ct == 0) M->t_ok[sc] = ok;
             tc::tc_fence_before();
           } else {
-          if (ok) {
+          if (ok && fp4) {
+            // FP4 keys: unit = (row, 8 dims): one code word and the row's
+            // four E8M0 bytes
+            const uint8_t *src = St + s * C::PAGE;
+            const uint32_t *sbw = reinterpret_cast<const uint32_t *>(StSc) + s * kBlock;
+            uint8_t *dst = As + j * C::A_BUF;
+            uint32_t raw[8], sb4[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int unit = q * IT_CONV + ct;
+              raw[q] = *reinterpret_cast<const uint32_t *>(src + (unit >> 4) * 64 + (unit & 15) * 4);
+              sb4[q] = sbw[unit >> 4];
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int unit = q * IT_CONV + ct;
+              const int r = unit >> 4, jc = unit & 15;
+              const int kc = jc >> 3, jj = jc & 7;
+              const int R = lowbit::e8m0_row_shift(sb4[q]);
+              *reinterpret_cast<uint4 *>(dst + kc * C::A_CHUNK + r * 128 + ((jj ^ (r & 7)) << 4)) =
+                  lowbit::e2m1x8_to_f16x8(raw[q], lowbit::e8m0_group_h2(sb4[q], jc >> 2, R));
+            }
+            if (ct < kBlock) Sc[sc * kBlock + ct] = lowbit::pow2f(lowbit::e8m0_row_shift(sbw[ct]));
+          } else if (ok) {
             const uint8_t *src = St + s * C::PAGE;
             uint8_t *dst = As + j * C::A_BUF;
             uint2 raw[8];
@@ -725,7 +792,8 @@ cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, uint32_t
   const bool reidx = sel.cand_in != nullptr;
   CUtensorMap keys_map;
   memset(&keys_map, 0, sizeof(keys_map));
-  if (C::ATMEM && !encode_keys_map(a, reidx ? 1 << sel.cb_shift : kBlock, &keys_map))
+  if (C::ATMEM && a.key_fmt != CSA_FMT_FP4_E8M0 &&
+      !encode_keys_map(a, reidx ? 1 << sel.cb_shift : kBlock, &keys_map))
     return cudaErrorInvalidValue;
   static bool attr[64] = {};
   int dev = 0;

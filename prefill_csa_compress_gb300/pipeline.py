@@ -32,7 +32,9 @@ class CsaStep:
     kv_pool, kv_table, cmp_pool, idx_pool, idx_scale, cmp_table, q, q_idx,
     idx_w, sink, kv_raw, idx_raw, w_gate, ape, w_gate_i, ape_i, rope_cos,
     rope_sin, and optionally the compressors' state rings state_main,
-    state_idx with state_table.  ``ratio``, ``topk``, ``prefill`` and
+    state_idx with state_table, and the low-bit caches' scale pools kv_scale,
+    cmp_scale and idx_kscale (kv_pool MXFP8, cmp_pool FP4 with E4M3 scales,
+    idx_pool FP4 with E8M0 scales, all uint8).  ``ratio``, ``topk``, ``prefill`` and
     ``dense`` (HCA) describe the step; ``n_cand`` > 0 makes the indexer also
     select that many candidate blocks of ``cand_block`` positions into
     ``cand`` (level one), and ``cand_in`` restricts it to given candidate
@@ -62,6 +64,7 @@ class CsaStep:
         self.cand = (torch.full((T, int(n_cand)), -1, dtype=torch.int32, device=dev)
                      if n_cand else None)
         self.cand_in = cand_in
+        self.lowbit = "cmp_scale" in t
         self.ws = {}
         self._prepared = None
         self._graph = None
@@ -83,6 +86,10 @@ class CsaStep:
         if "state_table" in t:  # the compressors' recurrent state rings
             main.update(state_cache=t["state_main"], state_block_table=t["state_table"])
             keys.update(state_cache=t["state_idx"], state_block_table=t["state_table"])
+        if self.lowbit:  # publication in the low-bit cache formats
+            main.update(out="fp4_e4m3", scale_pool=t["cmp_scale"])
+            keys.update(out="fp4_e8m0", cmp_pool=t["idx_pool"], scale_pool=t["idx_kscale"],
+                        idx_pool=None, idx_scale_pool=None)
         return main, keys
 
     def compress(self, stream=None):
@@ -102,7 +109,12 @@ class CsaStep:
             topk_idx=self.topk_idx, topk_score=self.topk_score, rope_cos=t["rope_cos"],
             rope_sin=t["rope_sin"],
             mode=B.CSA_MODE_PREFILL if self.prefill else B.CSA_MODE_DECODE, status=self.status,
-            cand_out=self.cand, cand_in=self.cand_in, cand_block=self.cand_block)
+            cand_out=self.cand, cand_in=self.cand_in, cand_block=self.cand_block,
+            key_scale_pool=t.get("idx_kscale"))
+
+    def _attn_kw(self):
+        t = self.t
+        return dict(kv_scale_pool=t.get("kv_scale"), cmp_scale_pool=t.get("cmp_scale"))
 
     def index(self, stream=None, scores=None):
         self.ws["ix"] = B.csa_index_topk(scores=scores, workspace=self._ws("ix"), stream=stream,
@@ -122,7 +134,7 @@ class CsaStep:
             kv_block_table=t["kv_table"], kv_len=t["kv_len"], cmp_pool=t["cmp_pool"],
             cmp_block_table=t["cmp_table"], n_cmp=t["n_cmp"], ratio=self.ratio, out=self.out,
             lse=self.lse, sink=t["sink"], rope_cos=t["rope_cos"], rope_sin=t["rope_sin"],
-            status=self.status, workspace=self._ws("at"), stream=stream)
+            status=self.status, workspace=self._ws("at"), stream=stream, **self._attn_kw())
 
     def prepare(self):
         """Marshal the step's calls once (buffers must stay in place)."""
@@ -141,7 +153,8 @@ class CsaStep:
             kv_pool=t["kv_pool"], kv_block_table=t["kv_table"], kv_len=t["kv_len"],
             cmp_pool=t["cmp_pool"], cmp_block_table=t["cmp_table"], n_cmp=t["n_cmp"],
             ratio=self.ratio, out=self.out, lse=self.lse, sink=t["sink"],
-            rope_cos=t["rope_cos"], rope_sin=t["rope_sin"], status=self.status, prepare=True))
+            rope_cos=t["rope_cos"], rope_sin=t["rope_sin"], status=self.status, prepare=True,
+            **self._attn_kw()))
         self._prepared = calls
         return self
 

@@ -111,3 +111,25 @@ def check_int8(codes, scale, ref_codes, ref_scale):
     diff = np.abs(codes - ref_codes)
     assert diff.max() <= 1, "code off by more than one"
     return int((diff > 0).sum())
+
+
+def check_fp4(codes, sbytes, ref_codes, ref_sbytes, group, scale_fmt):
+    """A packed E2M1 row and its scale bytes from the GPU against the
+    oracle's.  Scale bytes may differ by one (an amax at a rounding boundary
+    of the scale); in groups whose scales agree, a code may differ only to a
+    neighbouring magnitude of the same sign (a quotient at a tie of the E2M1
+    grid).  Returns (differing scale groups, differing codes)."""
+    import oracle as O
+
+    sb = np.asarray(sbytes, np.int64)
+    rsb = np.asarray(ref_sbytes, np.int64)
+    assert np.all(np.abs(sb - rsb) <= 1), "scale bytes differ by more than one"
+    same = np.repeat(sb == rsb, group)
+    c = O.unpack_nibbles(codes).astype(np.int64)[same]
+    rc = O.unpack_nibbles(ref_codes).astype(np.int64)[same]
+    diff = c != rc
+    mag, rmag = c & 7, rc & 7
+    ok = (np.abs(mag - rmag) <= 1) & (((c ^ rc) & 8 == 0) | (mag == 0) | (rmag == 0))
+    assert np.all(ok[diff]), "a code differs by more than one grid step"
+    return int((sb != rsb).sum()), int(diff.sum())
+

@@ -850,3 +850,13 @@ def test_lowbit_pools_read_as_their_dequantised_values():
     a2 = O.sparse_attention(q, 300, sel, kv_f, table, cmp_f, table, np.zeros(4), 0.05,
                             rope_cos=COS, rope_sin=SIN)
     assert np.array_equal(a1[0], a2[0]) and np.array_equal(a1[1], a2[1])
+
+
+def test_lowbit_row_decoders_agree():
+    """The vectorised pool reader equals the one-row definitions."""
+    rng = np.random.default_rng(56)
+    for fmt, D in (("fp4_e4m3", 512), ("fp4_e8m0", 128), ("mxfp8", 512)):
+        pool = _lowbit_pool(rng, 1, fmt, D)
+        rows = pool.dequant_rows(pool.codes[0], pool.scales[0])
+        for j in (0, 5, 127):
+            assert np.array_equal(rows[j], pool.dequant_row(pool.codes[0, j], pool.scales[0, j]))

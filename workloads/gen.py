@@ -48,6 +48,11 @@ class WorkloadSpec:
     # idx_w and sink: q2, q_idx2, idx_w2, sink2) selects inside them; 0 = off
     n_cand: int = 0
     cand_block: int = 8
+    # low-bit caches (the production cache ABI of DeepSeek V4.1 Flash): window
+    # KV MXFP8 (kv_pool uint8 codes + kv_scale), compressed KV FP4 with E4M3
+    # scales (cmp_pool uint8 + cmp_scale), index keys FP4 with E8M0 scales
+    # (idx_pool uint8 + idx_kscale)
+    lowbit: bool = False
     extra: dict = field(default_factory=dict)
 
     @property
@@ -97,6 +102,14 @@ CONFIGS = {
     # reindex layer selects its 512 inside them.  4 requests x 2 rows.
     "hier_decode": WorkloadSpec("hier_decode", [1048576] * 4, [2] * 4, ratio=4, topk=512,
                                 seed=8, kv_pages="window", n_cand=2048, cand_block=8),
+    # serving_decode's requests with the low-bit caches (ratio 2, as the pages'
+    # FP4 compressed pools): MXFP8 window, FP4 compressed KV and index keys
+    "lowbit_decode": WorkloadSpec("lowbit_decode", [8192, 6000, 4097, 2048], [2, 2, 2, 2],
+                                  ratio=2, topk=512, seed=9, kv_pool_pages=256,
+                                  cmp_pool_pages=256, lowbit=True),
+    # million_decode with the low-bit caches
+    "lowbit_million": WorkloadSpec("lowbit_million", [1048576] * 4, [2] * 4, ratio=4, topk=2048,
+                                   seed=10, kv_pages="window", lowbit=True),
 }
 
 
@@ -192,13 +205,18 @@ def make_workload(spec: WorkloadSpec) -> Workload:
         cmp_table[b, j] = cmp_perm[i]
 
     # ---- pools
-    kv_pool = _normal_bf16(rng, (P_kv, BLOCK, Dm))
-    if spec.cmp_init == "random":
+    if spec.lowbit:
+        lb = _lowbit_pools(rng, spec, P_kv, P_c)
+        kv_pool, cmp_pool, idx_pool = lb["kv_pool"], lb["cmp_pool"], lb["idx_pool"]
+        idx_scale = torch.zeros((P_c, BLOCK), dtype=torch.float32)  # unused by FP4 keys
+    elif spec.cmp_init == "random":
+        kv_pool = _normal_bf16(rng, (P_kv, BLOCK, Dm))
         cmp_pool = _normal_bf16(rng, (P_c, BLOCK, Dm))
         idx_pool = torch.from_numpy(rng.integers(-127, 128, size=(P_c, BLOCK, Di), dtype=np.int8))
         idx_scale = torch.from_numpy(
             rng.uniform(1e-3, 1e-2, size=(P_c, BLOCK)).astype(np.float32))
     else:
+        kv_pool = _normal_bf16(rng, (P_kv, BLOCK, Dm))
         cmp_pool = torch.zeros((P_c, BLOCK, Dm), dtype=torch.bfloat16)
         idx_pool = torch.zeros((P_c, BLOCK, Di), dtype=torch.int8)
         idx_scale = torch.zeros((P_c, BLOCK), dtype=torch.float32)
@@ -214,7 +232,7 @@ def make_workload(spec: WorkloadSpec) -> Workload:
     kv_raw = torch.empty((T, Dm), dtype=torch.bfloat16)
     for t in range(T):
         b, p = row_req[t], row_pos[t]
-        if b >= 0:
+        if b >= 0 and not spec.lowbit:
             kv_raw[t] = kv_pool[int(kv_table[b, p // BLOCK]), p % BLOCK]
         else:
             kv_raw[t] = _normal_bf16(rng, (Dm,))
@@ -259,6 +277,8 @@ def make_workload(spec: WorkloadSpec) -> Workload:
             score_part = torch.from_numpy(
                 (rng.standard_normal((B + 1, cap, d)) * 1.4).astype(np.float32))
             t[name] = torch.cat([kv_part, score_part], dim=2).contiguous()
+    if spec.lowbit:
+        t.update(kv_scale=lb["kv_scale"], cmp_scale=lb["cmp_scale"], idx_kscale=lb["idx_kscale"])
     if spec.n_cand:
         # the reindex layer's own activations and sink
         t["q2"] = _normal_bf16(rng, (T, spec.heads, Dm))
@@ -267,6 +287,38 @@ def make_workload(spec: WorkloadSpec) -> Workload:
             (rng.standard_normal((T, spec.idx_heads)) / 8.0).astype(np.float32))
         t["sink2"] = torch.from_numpy(rng.standard_normal(spec.heads).astype(np.float32))
     return Workload(spec=spec, t=t)
+
+
+def _lowbit_pools(rng, spec, P_kv, P_c):
+    """Random low-bit pools: codes are random bit patterns (no quantisation
+    happens here).  Window MXFP8 codes: random sign, E4M3 exponent field 4..8
+    and mantissa (magnitudes 1/8 .. 3.75), E8M0 scales 2^-1 or 2^0; FP4
+    compressed KV: uniform nibbles, E4M3 scales with exponent field 4..7
+    (1/8 .. 1.875); FP4 index keys: uniform nibbles, E8M0 scales 2^-3 .. 2^0.
+    With ``cmp_init="zeros"`` the compressed pools start as zero bytes (the
+    step's compressors fill them)."""
+    Dm, Di = spec.head_dim, spec.idx_dim
+    shp = (P_kv, BLOCK, Dm)
+    kv = (rng.integers(0, 2, shp, dtype=np.uint8) << 7) | (rng.integers(4, 9, shp, dtype=np.uint8) << 3) \
+        | rng.integers(0, 8, shp, dtype=np.uint8)
+    out = dict(kv_pool=torch.from_numpy(kv.astype(np.uint8)),
+               kv_scale=torch.from_numpy(rng.integers(126, 128, (P_kv, BLOCK, Dm // 32),
+                                                      dtype=np.uint8)))
+    if spec.cmp_init == "random":
+        g = (P_c, BLOCK, Dm // 16)
+        out["cmp_pool"] = torch.from_numpy(rng.integers(0, 256, (P_c, BLOCK, Dm // 2), dtype=np.uint8))
+        out["cmp_scale"] = torch.from_numpy(
+            ((rng.integers(4, 8, g, dtype=np.uint8) << 3) | rng.integers(0, 8, g, dtype=np.uint8))
+            .astype(np.uint8))
+        out["idx_pool"] = torch.from_numpy(rng.integers(0, 256, (P_c, BLOCK, Di // 2), dtype=np.uint8))
+        out["idx_kscale"] = torch.from_numpy(rng.integers(124, 128, (P_c, BLOCK, Di // 32),
+                                                          dtype=np.uint8))
+    else:
+        out["cmp_pool"] = torch.zeros((P_c, BLOCK, Dm // 2), dtype=torch.uint8)
+        out["cmp_scale"] = torch.zeros((P_c, BLOCK, Dm // 16), dtype=torch.uint8)
+        out["idx_pool"] = torch.zeros((P_c, BLOCK, Di // 2), dtype=torch.uint8)
+        out["idx_kscale"] = torch.zeros((P_c, BLOCK, Di // 32), dtype=torch.uint8)
+    return out
 
 
 def reindex_view(t: dict) -> dict:
