@@ -102,8 +102,33 @@ __device__ __forceinline__ const uint8_t *candidate_row(const csa_attn_args &a, 
 // threads per row.  Every low-bit unit's codes and scales are loaded before
 // any is converted; each slab becomes 64 bytes of BF16 (exact) in the
 // 128-byte-swizzled tile.  BF16 rows and absent rows go through cp.async
-// (zero fill) as in the plain gather.
+// (zero fill) as in the plain gather.  The conversion loops stay rolled: a
+// decode CTA runs this code once or twice, cold, so its size costs more
+// than its instruction count.
 constexpr int LB_UNITS = CT * (kHeadDim / 32) / AD_THREADS;  // 8 per thread
+
+// One slab's four 16-byte pieces: FP4 (kind 2: codes in c0, two E4M3 scale
+// bytes in sc) or MXFP8 (kind 3: codes in c0, c1, one E8M0 byte in sc).
+__device__ __forceinline__ void convert_slab(int kind, uint4 c0, uint4 c1, uint32_t sc, int r,
+                                             int slab, uint8_t *KVs) {
+  uint8_t *base = KVs + (slab >> 1) * 16384 + r * 128;
+  const float e8 = lowbit::pow2f((int)(sc & 0xFFu) - 127);
+#pragma unroll 1
+  for (int q = 0; q < 4; ++q) {
+    const uint4 c = q < 2 ? c0 : c1;
+    const bool lo = (q & 1) == 0;
+    uint4 v;
+    if (kind == 2) {
+      const uint4 cc = c0;
+      const uint32_t w = q == 0 ? cc.x : q == 1 ? cc.y : q == 2 ? cc.z : cc.w;
+      v = lowbit::e2m1x8_e4m3_to_bf16x8(w, (sc >> (8 * (q >> 1))) & 0xFFu);
+    } else {
+      v = lowbit::e4m3x8_e8m0_to_bf16x8(lo ? make_uint2(c.x, c.y) : make_uint2(c.z, c.w), e8);
+    }
+    const int piece = (slab & 1) * 4 + q;
+    *reinterpret_cast<uint4 *>(base + ((piece ^ (r & 7)) << 4)) = v;
+  }
+}
 
 __device__ __forceinline__ void gather_lowbit(const csa_attn_args &a, const AdMisc *M,
                                               uint8_t *KVs, int g, int tid) {
@@ -114,8 +139,7 @@ __device__ __forceinline__ void gather_lowbit(const csa_attn_args &a, const AdMi
   for (int i = 0; i < LB_UNITS; ++i) {
     const int u = i * AD_THREADS + tid, r = u >> 4, slab = u & 15;
     const uint8_t *row = M->src[r];
-    const bool is_cmp = g * CT + r < a.topk;
-    const int fmt = is_cmp ? a.cmp_fmt : a.kv_fmt;
+    const int fmt = g * CT + r < a.topk ? a.cmp_fmt : a.kv_fmt;
     kind[i] = !row ? 0 : (fmt == CSA_FMT_FP4_E4M3 ? 2 : (fmt == CSA_FMT_MXFP8 ? 3 : 0));
     c0[i] = c1[i] = make_uint4(0u, 0u, 0u, 0u);
     sc[i] = 0u;
@@ -128,9 +152,17 @@ __device__ __forceinline__ void gather_lowbit(const csa_attn_args &a, const AdMi
       c0[i] = *reinterpret_cast<const uint4 *>(row + slab * 32);
       c1[i] = *reinterpret_cast<const uint4 *>(row + slab * 32 + 16);
       sc[i] = a.kv_scale_pool[ri * (kHeadDim / 32) + slab];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < LB_UNITS; ++i) {
+    const int u = i * AD_THREADS + tid, r = u >> 4, slab = u & 15;
+    if (kind[i] != 0) {
+      convert_slab(kind[i], c0[i], c1[i], sc[i], r, slab, KVs);
     } else {
       // BF16 row (or absent: zero fill): the slab's four 16-byte pieces
-#pragma unroll
+      const uint8_t *row = M->src[r];
+#pragma unroll 1
       for (int q = 0; q < 4; ++q) {
         const int piece = (slab & 1) * 4 + q;
         uint8_t *dst = KVs + (slab >> 1) * 16384 + r * 128 + ((piece ^ (r & 7)) << 4);
@@ -139,31 +171,11 @@ __device__ __forceinline__ void gather_lowbit(const csa_attn_args &a, const AdMi
       }
     }
   }
-#pragma unroll
-  for (int i = 0; i < LB_UNITS; ++i) {
-    if (kind[i] == 0) continue;
-    const int u = i * AD_THREADS + tid, r = u >> 4, slab = u & 15;
-    uint8_t *base = KVs + (slab >> 1) * 16384 + r * 128;
-    const float e8 = lowbit::pow2f((int)sc[i] - 127);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int piece = (slab & 1) * 4 + q;
-      uint4 v;
-      if (kind[i] == 2) {
-        const uint32_t w = q == 0 ? c0[i].x : q == 1 ? c0[i].y : q == 2 ? c0[i].z : c0[i].w;
-        v = lowbit::e2m1x8_e4m3_to_bf16x8(w, (sc[i] >> (8 * (q >> 1))) & 0xFFu);
-      } else {
-        const uint2 w = q == 0 ? make_uint2(c0[i].x, c0[i].y)
-                        : q == 1 ? make_uint2(c0[i].z, c0[i].w)
-                        : q == 2 ? make_uint2(c1[i].x, c1[i].y)
-                                 : make_uint2(c1[i].z, c1[i].w);
-        v = lowbit::e4m3x8_e8m0_to_bf16x8(w, e8);
-      }
-      *reinterpret_cast<uint4 *>(base + ((piece ^ (r & 7)) << 4)) = v;
-    }
-  }
 }
 
+// LOWBIT: a pool holds a low-bit format (its gather is a separate
+// instantiation, so that the BF16 kernel carries none of its code).
+template <bool LOWBIT>
 __global__ void __launch_bounds__(AD_THREADS, 1)
     attn_decode_kernel(csa_attn_args a, int tiles_per_split,
                        const __grid_constant__ CUtensorMap qmap) {
@@ -235,7 +247,6 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   const int qd = warp & 3, h0 = (warp >> 2) * 32, c = qd * 32 + lane;
   const int sub = lane >> 3, piece = lane & 7;  // gather: rows 32 i + 4 warp + sub, 16-byte piece
   const float sl2 = a.softmax_scale * kLog2e;
-  const bool lowbit = a.kv_fmt == CSA_FMT_MXFP8 || a.cmp_fmt == CSA_FMT_FP4_E4M3;
   float lacc = 0.f;  // this warp's partial denominator of head h0 + lane
   bool first = true, ok = true, q_ready = false;
   uint32_t phase = 0;
@@ -246,7 +257,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     if (__syncthreads_count(tid < CT && M->src[tid] != nullptr) == 0) continue;
     const bool valid = M->src[c] != nullptr;
     // ---- gather the tile into the swizzled layout (the previous P.V is done)
-    if (lowbit) {
+    if constexpr (LOWBIT) {
       gather_lowbit(a, M, KVs, g, tid);
     } else {
       const uint8_t *src[4];
@@ -480,9 +491,12 @@ int max_cluster() {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
-                             1) == cudaSuccess &&
-        cudaOccupancyMaxActiveClusters(&n, attn_decode_kernel, &cfg) == cudaSuccess && n > 0)
+    if (cudaFuncSetAttribute(attn_decode_kernel<false>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+        cudaFuncSetAttribute(attn_decode_kernel<true>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+        cudaOccupancyMaxActiveClusters(&n, attn_decode_kernel<false>, &cfg) == cudaSuccess &&
+        n > 0)
       best = 16;
     cudaGetLastError();  // a refused query leaves no error behind
     cached[dev] = best;
@@ -497,8 +511,11 @@ cudaError_t prepare_kernel() {
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (done[dev]) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(
-      attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AD_SMEM);
+  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, AD_SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AD_SMEM);
   if (e == cudaSuccess) done[dev] = true;
   return e;
 }
@@ -524,8 +541,10 @@ cudaError_t launch_attn_decode(const csa_attn_args &a, cudaStream_t s) {
   int n_splits, tps;
   attn_decode_geometry(a, &n_splits, &tps);
   launch_begin(CSA_K_ATTN_DECODE, s);
-  e = launch_kernel(attn_decode_kernel, dim3(n_splits, a.n_rows), dim3(AD_THREADS),
-                    (size_t)AD_SMEM, s, n_splits, false, a, tps, qmap);
+  const bool lowbit = a.kv_fmt == CSA_FMT_MXFP8 || a.cmp_fmt == CSA_FMT_FP4_E4M3;
+  e = launch_kernel(lowbit ? attn_decode_kernel<true> : attn_decode_kernel<false>,
+                    dim3(n_splits, a.n_rows), dim3(AD_THREADS), (size_t)AD_SMEM, s, n_splits, false,
+                    a, tps, qmap);
   launch_end(CSA_K_ATTN_DECODE, s);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

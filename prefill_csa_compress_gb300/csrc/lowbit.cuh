@@ -52,6 +52,23 @@ __device__ __forceinline__ float e4m3_value(uint32_t byte) {
   return __half2float(__half(h));
 }
 
+// Two E2M1 codes (one byte, channel 2i in the low nibble) as an FP16 pair
+// (channel 2i in the low half): the sm_100-family conversion instruction.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(uint32_t byte) {
+  uint32_t d;
+  const uint16_t v = (uint16_t)(byte & 0xFFu);
+  asm("{\n .reg .b8 b;\n cvt.u8.u16 b, %1;\n cvt.rn.f16x2.e2m1x2 %0, b;\n}" : "=r"(d) : "h"(v));
+  return d;
+}
+// Two E4M3 codes (the low byte first) as an FP16 pair (low half first).
+__device__ __forceinline__ uint32_t cvt_e4m3x2(uint32_t two) {
+  uint32_t d;
+  const uint16_t v = (uint16_t)(two & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(v));
+  return d;
+}
+__device__ __forceinline__ __half2 as_h2(uint32_t u) { return *reinterpret_cast<const __half2 *>(&u); }
+
 // 2^e as a float for e in [-127, 127] (2^-127 is an FP32 subnormal).
 __device__ __forceinline__ float pow2f(int e) { return ldexpf(1.f, e); }
 
@@ -73,9 +90,7 @@ __device__ __forceinline__ uint4 e2m1x8_to_f16x8(uint32_t w, __half2 scale2) {
   uint32_t out[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const __half2_raw r =
-        __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((w >> (8 * i)) & 0xFFu), __NV_E2M1);
-    const __half2 h = __hmul2(*reinterpret_cast<const __half2 *>(&r), scale2);
+    const __half2 h = __hmul2(as_h2(cvt_e2m1x2(w >> (8 * i))), scale2);
     out[i] = *reinterpret_cast<const uint32_t *>(&h);
   }
   return make_uint4(out[0], out[1], out[2], out[3]);
@@ -97,14 +112,11 @@ __device__ __forceinline__ __half2 e8m0_group_h2(uint32_t sb4, int g, int R) {
 // BF16 values.  The product of an E2M1 and an E4M3 value has at most six
 // significant bits and lies in [2^-10, 2688]: exact in FP16 and in BF16.
 __device__ __forceinline__ uint4 e2m1x8_e4m3_to_bf16x8(uint32_t w, uint32_t sbyte) {
-  const __half_raw sr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)sbyte, __NV_E4M3);
-  const __half2 s2 = __half2half2(__half(sr));
+  const __half2 s2 = __half2half2(__low2half(as_h2(cvt_e4m3x2(sbyte))));
   uint32_t out[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const __half2_raw r =
-        __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((w >> (8 * i)) & 0xFFu), __NV_E2M1);
-    const float2 f = __half22float2(__hmul2(*reinterpret_cast<const __half2 *>(&r), s2));
+    const float2 f = __half22float2(__hmul2(as_h2(cvt_e2m1x2(w >> (8 * i))), s2));
     const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
     out[i] = *reinterpret_cast<const uint32_t *>(&b);
   }
@@ -118,9 +130,7 @@ __device__ __forceinline__ uint4 e4m3x8_e8m0_to_bf16x8(uint2 w, float scale) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t word = i < 2 ? w.x : w.y;
-    const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(
-        (__nv_fp8x2_storage_t)((word >> (16 * (i & 1))) & 0xFFFFu), __NV_E4M3);
-    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&r));
+    const float2 f = __half22float2(as_h2(cvt_e4m3x2(word >> (16 * (i & 1)))));
     const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
     out[i] = *reinterpret_cast<const uint32_t *>(&b);
   }
