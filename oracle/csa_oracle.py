@@ -227,7 +227,8 @@ class LowBitPool:
         if self.fmt == "mxfp8":
             vals, scl, group = e4m3_decode(codes), e8m0_decode(sbytes), 32
         else:
-            nib = np.stack([codes & 15, codes >> 4], axis=-1).reshape(len(codes), -1)
+            nib = np.stack([codes & 15, codes >> 4], axis=-1).reshape(len(codes),
+                                                                      2 * codes.shape[1])
             vals = e2m1_decode(nib)
             if self.fmt == "fp4_e4m3":
                 scl, group = e4m3_decode(sbytes), 16

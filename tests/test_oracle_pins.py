@@ -860,3 +860,5 @@ def test_lowbit_row_decoders_agree():
         rows = pool.dequant_rows(pool.codes[0], pool.scales[0])
         for j in (0, 5, 127):
             assert np.array_equal(rows[j], pool.dequant_row(pool.codes[0, j], pool.scales[0, j]))
+        # no rows (a query that sees no compressed entry)
+        assert pool.dequant_rows(pool.codes[0, :0], pool.scales[0, :0]).shape == (0, D)
