@@ -6,7 +6,8 @@ or prefill).  Default workload: serving decode (4 requests x 2 rows, contexts
 8192/6000/4097/2048, ratio 2, top-k 512).  Other workloads: --workload
 tiny_decode | ratio1_decode | chunked_prefill | million_decode |
 stateful_decode | hca_decode | hca_prefill | hier_decode (a level-one layer
-and a reindex layer of the hierarchical indexer as one step).
+and a reindex layer of the hierarchical indexer as one step) | lowbit_decode |
+lowbit_million (the low-bit cache formats).
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 the host cores instead (a bounded sample of the same workload).
@@ -112,14 +113,19 @@ def algorithmic_work(wl):
     H, D, Hi, Di, W = s.heads, s.head_dim, s.idx_heads, s.idx_dim, s.window
     sel = [min(s.topk, v) for v in vis]
     win = [min(W, p + 1) for _, p in rows]
-    idx_bytes = sum(v * (Di + 4) for v in req_vis.values()) + len(rows) * Hi * (Di * 2 + 4)
+    # bytes of one cached row: index key, compressed KV row, window KV row
+    # (low-bit caches: FP4 codes + scale bytes, MXFP8 codes + scale bytes)
+    key_b = Di // 2 + Di // 32 if s.lowbit else Di + 4
+    cmp_b = D // 2 + D // 16 if s.lowbit else D * 2
+    win_b = D + D // 32 if s.lowbit else D * 2
+    idx_bytes = sum(v * key_b for v in req_vis.values()) + len(rows) * Hi * (Di * 2 + 4)
     idx_flops = sum(2 * Hi * Di * v for v in vis)
     if s.mode == "prefill":
         # window rows are shared by neighbouring query rows: count each once
-        attn_bytes = (len(rows) * H * D * 2 * 2 + sum(n_cmp) * D * 2 +
-                      sum(int(x) for x in wl.kv_len) * D * 2)
+        attn_bytes = (len(rows) * H * D * 2 * 2 + sum(n_cmp) * cmp_b +
+                      sum(int(x) for x in wl.kv_len) * win_b)
     else:
-        attn_bytes = (sum(sel) * D * 2 + len(req_vis) * (W + 1) * D * 2 +
+        attn_bytes = (sum(sel) * cmp_b + len(req_vis) * (W + 1) * win_b +
                       len(rows) * H * D * 2 * 2 + sum(sel) * 4)
     attn_flops = sum(4 * H * D * (k + w) for k, w in zip(sel, win))
     topk_bytes = sum(vis) * 4 + len(rows) * s.topk * 8
@@ -131,12 +137,12 @@ def algorithmic_work(wl):
         nblk = [(v + cb - 1) // cb for v in vis]
         vc = [min(v, s.n_cand * cb) for v in vis]
         sel2 = [min(s.topk, v) for v in vc]
-        idx_bytes += (sum(nblk) * 4 + sum(v * (Di + 4) for v in vc) +
+        idx_bytes += (sum(nblk) * 4 + sum(v * key_b for v in vc) +
                       len(rows) * (Hi * (Di * 2 + 4) + s.n_cand * 4))
         idx_flops += sum(2 * Hi * Di * v for v in vc)
         topk_bytes += (sum(nblk) * 4 + len(rows) * s.n_cand * 4 +
                        sum(vc) * 4 + len(rows) * s.topk * 8)
-        attn_bytes += (sum(sel2) * D * 2 + len(req_vis) * (W + 1) * D * 2 +
+        attn_bytes += (sum(sel2) * cmp_b + len(req_vis) * (W + 1) * win_b +
                        len(rows) * H * D * 2 * 2 + sum(sel2) * 4)
         attn_flops += sum(4 * H * D * (k + w) for k, w in zip(sel2, win))
     # compressors (main: x, kv [T, D] BF16 -> BF16 rows; index keys: [T, Di] ->
@@ -158,7 +164,7 @@ def algorithmic_work(wl):
         groups = sum(1 for i in closing if all(in_chunk(i, j) for j in range(1, r)))
         ring_reads = ring_writes = 0
     # (d, output bytes per group); HCA (dense) runs only the main compressor
-    dims = ((D, D * 2),) if s.dense else ((D, D * 2), (Di, Di + 4))
+    dims = ((D, cmp_b),) if s.dense else ((D, cmp_b), (Di, key_b))
     w_bytes = sum(d * d * 2 + r * d * 4 for d, _ in dims)    # W_gate and ape
     out_bytes = sum(groups * ob for _, ob in dims)
     ring_bytes = sum((ring_reads + ring_writes) * 2 * d * 4 for d, _ in dims)
@@ -176,6 +182,9 @@ def algorithmic_work(wl):
         # short chunks: W_gate, ape and the r rows of x and kv of every group in, rows out
         "compress_fused": {"bytes": w_bytes + sum(groups * r * d * 2 * 2 for d, _ in dims) +
                            out_bytes, "flops": sum(2 * groups * r * d * d for d, _ in dims)},
+        # low-bit prefill: every mapped page of both pools read once, written as BF16
+        "dequant": {"bytes": (sum(n_cmp) * (cmp_b + D * 2) +
+                              sum(int(x) for x in wl.kv_len) * (win_b + D * 2)), "flops": 0},
         "_rows": len(rows),
     }
 
@@ -343,6 +352,10 @@ def _config(wl, args):
          "parallelism": f"replicas x{args.gpus}"}
     if s.n_cand:
         c.update(layers=["level-one", "reindex"], n_cand=s.n_cand, cand_block=s.cand_block)
+    if s.lowbit:
+        c.update(caches={"window": "MXFP8 (E4M3, E8M0 per 32)",
+                         "compressed": "FP4 (E2M1, E4M3 per 16)",
+                         "index_keys": "FP4 (E2M1, E8M0 per 32)"})
     return c
 
 
@@ -360,7 +373,7 @@ def _src_sha(name):
 KERNEL_SRC = {"index_score": "k_index_tc.cu", "index_topk": "k_index.cu",
               "attn_decode": "k_attn.cu", "attn_prefill": "k_attn_prefill.cu",
               "compress_gate": "k_compress.cu", "compress_pool": "k_compress.cu",
-              "compress_fused": "k_compress.cu"}
+              "compress_fused": "k_compress.cu", "dequant": "k_dequant.cu"}
 
 
 def run_gpu(args, wl, rank, world, local_rank):
@@ -406,6 +419,8 @@ def run_gpu(args, wl, rank, world, local_rank):
     torch.cuda.synchronize()
     kernels = ["index_score", "index_topk", "attn_prefill" if prefill else "attn_decode",
                "compress_gate", "compress_pool", "compress_fused"]
+    if s.lowbit and prefill:
+        kernels.append("dequant")
     # per-kernel durations: the step captured with that kernel's event pairs,
     # its calls issued one after another on one stream (no kernel shares the
     # GPU with the timed one), replayed three times with L2 flushed before each

@@ -373,17 +373,22 @@ CSA_API csa_status_t csa_index_topk_noalloc(csa_index_args *args, csa_stream_t s
  * head_dim == 512, window == 128, topk <= 2048.
  * The decode call splits each row's candidates over the CTAs of a thread-
  * block cluster and merges the partial softmaxes in distributed shared
- * memory; the prefill call is tiled for many rows.  Neither needs a
- * workspace (the size query returns 0; a workspace passed in is unused, but
- * a non-null pointer is what makes the call launch).  Both compute
- * the same function.
+ * memory; the prefill call is tiled for many rows.  With BF16 pools neither
+ * needs a workspace (the size query returns 0; a workspace passed in is
+ * unused, but a non-null pointer is what makes the call launch); the
+ * prefill call with a low-bit pool needs the arena below.  Both compute the
+ * same function.
  *
  * Low-bit caches (see csa_cache_fmt_t): kv_fmt CSA_FMT_MXFP8 reads kv_pool
  * as uint8 [*, 128, 512] with kv_scale_pool; cmp_fmt CSA_FMT_FP4_E4M3 reads
  * cmp_pool as uint8 [*, 128, 256] with cmp_scale_pool.  Each candidate row is
- * dequantised (exactly: every such value is a BF16 value) as it is gathered.
- * A struct_size that ends before kv_fmt reads both pools as BF16.  The
- * prefill call supports only BF16 pools (CSA_ERR_UNSUPPORTED otherwise).
+ * dequantised (exactly: every such value is a BF16 value).  The decode call
+ * dequantises each candidate row as it gathers it.  The prefill call first
+ * dequantises every mapped page of the requests' block tables into a BF16
+ * arena in its workspace (per low-bit pool: n_req * max_blocks pages of
+ * 128 KB plus an INT32 table, as the size query reports; a table entry
+ * outside the pool is left unmapped in the arena), then reads the arena.
+ * A struct_size that ends before kv_fmt reads both pools as BF16.
  * ---------------------------------------------------------------------- */
 typedef struct {
   uint32_t struct_size;
@@ -448,7 +453,8 @@ typedef enum {
   CSA_K_INDEX_TOPK = 4,
   CSA_K_ATTN_DECODE = 5,
   CSA_K_ATTN_PREFILL = 6,
-  CSA_K_COUNT = 7
+  CSA_K_DEQUANT = 7,        /* low-bit pools into the prefill call's BF16 arena */
+  CSA_K_COUNT = 8
 } csa_kernel_id_t;
 
 /* Time every launch of kernel `kernel_id` (up to `max_launches` launches)

@@ -25,7 +25,7 @@ CSA_FMT_BF16, CSA_FMT_INT8, CSA_FMT_FP4_E4M3, CSA_FMT_FP4_E8M0, CSA_FMT_MXFP8 = 
 CSA_MODE_AUTO, CSA_MODE_DECODE, CSA_MODE_PREFILL = 0, 1, 2
 KERNEL_IDS = {
     "compress_gate": 0, "compress_pool": 1, "compress_fused": 2, "index_score": 3,
-    "index_topk": 4, "attn_decode": 5, "attn_prefill": 6,
+    "index_topk": 4, "attn_decode": 5, "attn_prefill": 6, "dequant": 7,
 }
 
 

@@ -147,18 +147,22 @@ csa_status_t run_attn(csa_attn_args *user, cudaStream_t s, bool decode) {
   if ((a->kv_fmt != CSA_FMT_BF16 && a->kv_fmt != CSA_FMT_MXFP8) ||
       (a->cmp_fmt != CSA_FMT_BF16 && a->cmp_fmt != CSA_FMT_FP4_E4M3))
     return CSA_ERR_UNSUPPORTED;
-  if (!decode && (a->kv_fmt != CSA_FMT_BF16 || a->cmp_fmt != CSA_FMT_BF16))
-    return CSA_ERR_UNSUPPORTED;
-  if (!a->workspace) {  // neither path needs scratch memory
-    user->workspace_bytes = 0;
+  // the prefill call's low-bit pools go through a BF16 arena in the workspace
+  const size_t need = decode ? 0 : attn_arena_bytes(*a);
+  if (!a->workspace) {
+    user->workspace_bytes = need;
     return CSA_OK;
   }
+  if (a->workspace_bytes < need) return CSA_ERR_INVALID_ARG;
   if (a->n_rows == 0) return CSA_OK;
   st = check_attn_args(a);
   if (st != CSA_OK) return st;
   if (decode) return from_cuda(launch_attn_decode(*a, s));
   if (!attn_prefill_supported(*a)) return CSA_ERR_UNSUPPORTED;
-  return from_cuda(launch_attn_prefill(*a, s));
+  if (need == 0) return from_cuda(launch_attn_prefill(*a, s));
+  csa_attn_args bf;
+  const cudaError_t e = launch_dequant_arena(*a, a->workspace, &bf, s);
+  return from_cuda(e != cudaSuccess ? e : launch_attn_prefill(bf, s));
 }
 
 }  // namespace

@@ -108,6 +108,12 @@ bool index_pointers_ok(const csa_index_args *a);
 bool topk_is_long(int n_cap);
 size_t topk_ws_bytes(int n_rows, int n_cap);
 uint32_t *topk_counters(void *ws, int n_rows, int n_cap);
+// Low-bit pools of a prefill call dequantised into a BF16 arena in the
+// workspace (k_dequant.cu): its size, and the launch that fills it and
+// points `bf` (a copy of `a`) at it.
+size_t attn_arena_bytes(const csa_attn_args &a);
+cudaError_t launch_dequant_arena(const csa_attn_args &a, void *ws, csa_attn_args *bf,
+                                 cudaStream_t s);
 // The persistent prefill kernel (k_attn_prefill.cu).
 bool attn_prefill_supported(const csa_attn_args &a);
 cudaError_t launch_attn_prefill(const csa_attn_args &a, cudaStream_t s);

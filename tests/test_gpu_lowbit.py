@@ -224,32 +224,66 @@ def test_lowbit_attention(name, over, combo):
     assert np.max(np.abs(np.stack(gl) - np.stack(rl))) <= LSE_ABS * max(1.0, np.max(np.abs(rl)))
 
 
-def test_lowbit_prefill_attention_is_unsupported():
-    spec = spec_for("lowbit_decode")
+@pytest.mark.parametrize("over", [
+    dict(ctx=[700], chunk=[300], ratio=4, topk=48, seed=94, kv_pool_pages=None,
+         cmp_pool_pages=None),
+    dict(ctx=[2500, 900], chunk=[130, 70], ratio=2, topk=200, seed=95),
+])
+def test_lowbit_prefill_attention(over):
+    """The prefill call dequantises the low-bit pools into its BF16 arena:
+    bit-identical to the BF16 path on dequantised copies, and the oracle's."""
+    spec = spec_for("lowbit_decode", **over)
     wl, t = _load(spec)
-    with pytest.raises(csa.CsaError):
+    limits = [O.visible_count(int(wl.row_pos[i]), spec.ratio, int(wl.n_cmp[int(wl.row_req[i])]))
+              if int(wl.row_req[i]) >= 0 else 0 for i in range(spec.n_rows)]
+    sel = random_selection(limits, spec.topk, 19).to(DEV)
+    kv_bf = _dequant_pool_bf16(t["kv_pool"], t["kv_scale"], "mxfp8")
+    cmp_bf = _dequant_pool_bf16(t["cmp_pool"], t["cmp_scale"], "fp4_e4m3")
+    outs = []
+    for lowbit in (True, False):
+        out = torch.zeros_like(t["q"])
+        lse = torch.zeros(t["q"].shape[:2], dtype=torch.float32, device=DEV)
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
         csa.csa_sparse_attn_prefill(
-            q=t["q"], row_req=t["row_req"], row_pos=t["row_pos"], topk_idx=None, dense_cap=64,
-            kv_pool=t["kv_pool"], kv_block_table=t["kv_table"], kv_len=t["kv_len"],
-            cmp_pool=t["cmp_pool"], cmp_block_table=t["cmp_table"], n_cmp=t["n_cmp"],
-            ratio=spec.ratio, out=torch.zeros_like(t["q"]), kv_scale_pool=t["kv_scale"],
-            cmp_scale_pool=t["cmp_scale"])
+            q=t["q"], row_req=t["row_req"], row_pos=t["row_pos"], topk_idx=sel,
+            kv_pool=t["kv_pool"] if lowbit else kv_bf, kv_block_table=t["kv_table"],
+            kv_len=t["kv_len"], cmp_pool=t["cmp_pool"] if lowbit else cmp_bf,
+            cmp_block_table=t["cmp_table"], n_cmp=t["n_cmp"], ratio=spec.ratio, out=out,
+            lse=lse, sink=t["sink"], rope_cos=t["rope_cos"], rope_sin=t["rope_sin"],
+            status=status, kv_scale_pool=t["kv_scale"] if lowbit else None,
+            cmp_scale_pool=t["cmp_scale"] if lowbit else None)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        outs.append((out.cpu(), lse.cpu()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    out = outs[0][0].double().numpy()
+    pools = {"cmp_pool": wl.cmp_pool, "cmp_scale": wl.cmp_scale, "idx_pool": wl.idx_pool,
+             "idx_kscale": wl.idx_kscale}
+    rows = [r for r in range(spec.n_rows) if int(wl.row_req[r]) >= 0][::17]
+    g = np.stack([out[r] for r in rows])
+    ref = np.stack([OS.attention_row(wl.t, spec, pools, r, sel[r].cpu().numpy())[0]
+                    for r in rows])
+    check_bf16(g, ref, "prefill out", magnitude=max(1.0, float(np.max(np.abs(ref))) / 2))
 
 
 # ------------------------------------------------------------------ the step
 
 
-@pytest.mark.parametrize("name", ["lowbit_decode", "lowbit_million"])
-def test_lowbit_step_chain(name):
+@pytest.mark.parametrize("name,over", [
+    ("lowbit_decode", {}),
+    ("lowbit_million", {}),
+    ("lowbit_prefill", dict(ctx=[1500], chunk=[1500], seed=96)),   # FP4 publication of 375 groups
+])
+def test_lowbit_step_chain(name, over):
     """compress (FP4 publication) -> FP4 indexer -> low-bit attention, against
     the oracle's chain on the same inputs."""
-    spec = spec_for(name)
+    spec = spec_for(name, **over)
     wl, t = _load(spec)
-    step = CsaStep(t, spec.ratio, spec.topk)
+    step = CsaStep(t, spec.ratio, spec.topk, prefill=spec.mode == "prefill")
     step.run()
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0
-    rows = [0, 3, 7] if spec.n_rows >= 8 else list(range(spec.n_rows))
+    rows = [0, 3, 7] if spec.n_rows <= 8 else [0, 5, 700, spec.n_rows - 1]
     pools, res = OS.full_step(wl.t, spec, rows=rows)
     # the published entries: FP4 codes like the oracle's (rare tie flips)
     gc, gs = t["cmp_pool"].cpu().numpy(), t["cmp_scale"].cpu().numpy()
@@ -263,6 +297,9 @@ def test_lowbit_step_chain(name):
     same = 0
     for row, rr in res.items():
         s_ref = rr["scores"]
+        if len(s_ref) == 0:  # no compressed entry visible yet
+            assert np.all(sel[row] == -1)
+            continue
         tol = np.maximum(1e-3 * np.abs(s_ref), 1e-3 * np.max(np.abs(s_ref)))
         check_topk(sel[row], s_ref, tol, spec.topk)
         if np.array_equal(sel[row], rr["topk"]):

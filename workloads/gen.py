@@ -107,6 +107,10 @@ CONFIGS = {
     "lowbit_decode": WorkloadSpec("lowbit_decode", [8192, 6000, 4097, 2048], [2, 2, 2, 2],
                                   ratio=2, topk=512, seed=9, kv_pool_pages=256,
                                   cmp_pool_pages=256, lowbit=True),
+    # chunked_prefill with the low-bit caches: the compressors publish FP4
+    # entries, the indexer reads FP4 keys, the attention its BF16 arena
+    "lowbit_prefill": WorkloadSpec("lowbit_prefill", [8192], [8192], ratio=4, topk=512, seed=11,
+                                   mode="prefill", cmp_init="zeros", lowbit=True),
     # million_decode with the low-bit caches
     "lowbit_million": WorkloadSpec("lowbit_million", [1048576] * 4, [2] * 4, ratio=4, topk=2048,
                                    seed=10, kv_pages="window", lowbit=True),
