@@ -37,19 +37,27 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # kernel reports null.  Values are from `ncu --metrics dram__bytes_read.sum,
 # dram__bytes_write.sum` captures of these same bench workloads.
 NCU_TRAFFIC = {
-    ("serving_decode", "compress_fused"): {"bytes": 613675, "src": "396e39098712"},
-    ("serving_decode", "index_score"): {"bytes": 1536165, "src": "4a6ecdbb1973"},
-    ("serving_decode", "index_topk"): {"bytes": 122142, "src": "3177992dcba3"},
-    ("serving_decode", "attn_decode"): {"bytes": 4612742, "src": "8a85a42340d5"},
-    ("million_decode", "compress_fused"): {"bytes": 41947, "src": "396e39098712"},
-    ("million_decode", "index_score"): {"bytes": 142124483, "src": "4a6ecdbb1973"},
-    ("million_decode", "index_topk"): {"bytes": 8640439, "src": "3177992dcba3"},
-    ("million_decode", "attn_decode"): {"bytes": 17841061, "src": "8a85a42340d5"},
-    ("chunked_prefill", "compress_gate"): {"bytes": 5534313, "src": "396e39098712"},
-    ("chunked_prefill", "compress_pool"): {"bytes": 16081495, "src": "396e39098712"},
-    ("chunked_prefill", "index_score"): {"bytes": 149992914, "src": "4a6ecdbb1973"},
-    ("chunked_prefill", "index_topk"): {"bytes": 34516370, "src": "3177992dcba3"},
-    ("chunked_prefill", "attn_prefill"): {"bytes": 1059085687, "src": "d956f63fbd32"},
+    ("serving_decode", "attn_decode"): {"bytes": 4614164, "src": "77022dbcfaf0"},
+    ("serving_decode", "index_topk"): {"bytes": 125243, "src": "b1465b204230"},
+    ("serving_decode", "index_score"): {"bytes": 1549154, "src": "df1f5115c7ee"},
+    ("serving_decode", "compress_fused"): {"bytes": 621361, "src": "0587b44655af"},
+    ("million_decode", "index_score"): {"bytes": 143056404, "src": "df1f5115c7ee"},
+    ("million_decode", "attn_decode"): {"bytes": 17839764, "src": "77022dbcfaf0"},
+    ("million_decode", "index_topk"): {"bytes": 8638887, "src": "b1465b204230"},
+    ("million_decode", "compress_fused"): {"bytes": 50225, "src": "0587b44655af"},
+    ("hier_decode", "index_score"): {"bytes": 80700180, "src": "df1f5115c7ee"},
+    ("hier_decode", "index_topk"): {"bytes": 3530171, "src": "b1465b204230"},
+    ("hier_decode", "attn_decode"): {"bytes": 5363865, "src": "77022dbcfaf0"},
+    ("hier_decode", "compress_fused"): {"bytes": 50097, "src": "0587b44655af"},
+    ("lowbit_decode", "attn_decode"): {"bytes": 2074821, "src": "77022dbcfaf0"},
+    ("lowbit_decode", "index_topk"): {"bytes": 124938, "src": "b1465b204230"},
+    ("lowbit_decode", "index_score"): {"bytes": 893922, "src": "df1f5115c7ee"},
+    ("lowbit_decode", "compress_fused"): {"bytes": 621460, "src": "0587b44655af"},
+    ("chunked_prefill", "attn_prefill"): {"bytes": 1058866763, "src": "96ab4a6b48bb"},
+    ("chunked_prefill", "index_score"): {"bytes": 149843403, "src": "df1f5115c7ee"},
+    ("chunked_prefill", "index_topk"): {"bytes": 34518731, "src": "b1465b204230"},
+    ("chunked_prefill", "compress_pool"): {"bytes": 16089925, "src": "0587b44655af"},
+    ("chunked_prefill", "compress_gate"): {"bytes": 5533824, "src": "0587b44655af"},
 }
 
 
