@@ -416,19 +416,26 @@ def run_gpu(args, wl, rank, world, local_rank):
     s = wl.spec
     t = wl.to(dev)
     prefill = s.mode == "prefill"
-    if s.n_cand:
-        # hierarchical indexer: a level-one layer, then a reindex layer over
-        # the same caches with its own activations
-        from prefill_csa_compress_gb300.pipeline import StepChain
-        from workloads import reindex_view
 
-        s1 = CsaStep(t, s.ratio, s.topk, prefill=prefill, n_cand=s.n_cand,
-                     cand_block=s.cand_block)
-        s2 = CsaStep(reindex_view(t), s.ratio, s.topk, prefill=prefill, compress=False,
-                     cand_in=s1.cand, cand_block=s.cand_block, status_buf=s1.status)
-        step = StepChain([s1, s2]).prepare()
-    else:
-        step = CsaStep(t, s.ratio, s.topk, prefill=prefill, dense=s.dense).prepare()
+    def make_step(t, io=None):
+        if s.n_cand:
+            # hierarchical indexer: a level-one layer, then a reindex layer over
+            # the same caches with its own activations
+            from prefill_csa_compress_gb300.pipeline import StepChain
+            from workloads import reindex_view
+
+            s1 = CsaStep(t, s.ratio, s.topk, prefill=prefill, n_cand=s.n_cand,
+                         cand_block=s.cand_block)
+            s2 = CsaStep(reindex_view(t), s.ratio, s.topk, prefill=prefill, compress=False,
+                         cand_in=s1.cand, cand_block=s.cand_block, status_buf=s1.status)
+            st = StepChain([s1, s2])
+        else:
+            st = CsaStep(t, s.ratio, s.topk, prefill=prefill, dense=s.dense)
+        if io is not None:
+            io.bind_outputs(st)
+        return st.prepare()
+
+    step = make_step(t)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     work = algorithmic_work(wl)
@@ -508,16 +515,22 @@ def run_gpu(args, wl, rank, world, local_rank):
     value = whole_job_rate(units, world, args.steps, total_ms)
     status = int(step.status.item())
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: the step's
+    # per-step inputs packed into one pinned host block and one device block
+    # (one host-to-device copy per step), out and lse likewise (one copy back)
+    from prefill_csa_compress_gb300.pipeline import StepIO
+
     per_step_inputs = ["q", "q_idx", "idx_w", "kv_raw", "idx_raw", "row_req", "row_pos",
                        "kv_len", "n_cmp"]
     if s.n_cand:
         per_step_inputs += ["q2", "q_idx2", "idx_w2"]
-    host_in = {k: wl.t[k].pin_memory() for k in per_step_inputs}
-    host_out = step.out.cpu().pin_memory()
-    host_lse = step.lse.cpu().pin_memory()
-    bi = sum(v.numel() * v.element_size() for v in host_in.values())
-    bo = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+    t_e = dict(t)
+    io = StepIO(t_e, per_step_inputs)
+    step_e = make_step(t_e, io)
+    step_e.run()
+    torch.cuda.synchronize()
+    step_e.capture()
+    bi, bo = io.in_bytes, io.out_bytes
     ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     if dist:
@@ -526,15 +539,14 @@ def run_gpu(args, wl, rank, world, local_rank):
     for i in range(args.steps):
         flush_l2()
         ee[i][0].record(stream)
-        for k, v in host_in.items():
-            t[k].copy_(v, non_blocking=True)
-        step.replay()
-        host_out.copy_(step.out, non_blocking=True)
-        host_lse.copy_(step.lse, non_blocking=True)
+        io.h2d()
+        step_e.replay()
+        io.d2h()
         ee[i][1].record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ee), dist, dev)
     e2e_value = whole_job_rate(units, world, args.steps, e2e_ms)
+    step_e.drop_graph()
     step.drop_graph()
     csa.prof_disable()  # the graph recorded these events: released after its last replay
 

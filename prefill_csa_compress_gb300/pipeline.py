@@ -232,3 +232,69 @@ class StepChain:
 
     def drop_graph(self):
         self._graph = None
+
+
+class StepIO:
+    """A step's per-step inputs packed into one contiguous device block (the
+    tensors of ``t`` named in ``names`` become views into it) and its outputs
+    into another, each with a pinned host mirror of the same layout: the
+    inputs of a step arrive in one host-to-device copy and its outputs leave
+    in one device-to-host copy, instead of one copy (and its fixed cost) per
+    tensor.  Build it, and bind the outputs, before the step is prepared or
+    captured: the step marshals the views' addresses."""
+
+    ALIGN = 256
+
+    def __init__(self, t: dict, names):
+        self.names = list(names)
+        self.offsets, off = {}, 0
+        for k in self.names:
+            self.offsets[k] = off
+            off += self._span(t[k])
+        dev = t[self.names[0]].device
+        self.dev_in = torch.empty(max(off, 1), dtype=torch.uint8, device=dev)
+        self.host_in = torch.empty(max(off, 1), dtype=torch.uint8, pin_memory=True)
+        self.in_bytes = 0
+        for k in self.names:
+            src = t[k]
+            nb = src.numel() * src.element_size()
+            o = self.offsets[k]
+            view = self.dev_in[o:o + nb].view(src.dtype).view(src.shape)
+            view.copy_(src)
+            self.host_in[o:o + nb].copy_(src.contiguous().view(-1).view(torch.uint8).cpu())
+            t[k] = view
+            self.in_bytes += nb
+        self.dev_out = self.host_out = None
+        self.out_bytes = 0
+
+    def _span(self, x):
+        nb = x.numel() * x.element_size()
+        return (nb + self.ALIGN - 1) // self.ALIGN * self.ALIGN
+
+    def host_input(self, name, like):
+        """The pinned host view (dtype and shape of ``like``) where the caller
+        writes input ``name`` of the next step."""
+        o = self.offsets[name]
+        nb = like.numel() * like.element_size()
+        return self.host_in[o:o + nb].view(like.dtype).view(like.shape)
+
+    def bind_outputs(self, step):
+        """Give ``step`` (a CsaStep, or a StepChain's last layer) out and lse
+        tensors that live in one device block with a pinned host mirror."""
+        last = step.steps[-1] if isinstance(step, StepChain) else step
+        out, lse = last.out, last.lse
+        so, sl = self._span(out), self._span(lse)
+        self.dev_out = torch.empty(so + sl, dtype=torch.uint8, device=out.device)
+        self.host_out = torch.empty(so + sl, dtype=torch.uint8, pin_memory=True)
+        nb_o = out.numel() * out.element_size()
+        nb_l = lse.numel() * lse.element_size()
+        last.out = self.dev_out[:nb_o].view(out.dtype).view(out.shape)
+        last.lse = self.dev_out[so:so + nb_l].view(lse.dtype).view(lse.shape)
+        self.out_bytes = nb_o + nb_l
+        return self
+
+    def h2d(self):
+        self.dev_in.copy_(self.host_in, non_blocking=True)
+
+    def d2h(self):
+        self.host_out.copy_(self.dev_out, non_blocking=True)

@@ -543,3 +543,43 @@ def test_decode_step_chain(name):
             same += 1
             check_bf16(out[row], rr["out"], f"row {row} out")
     assert same >= len(res) // 2
+
+
+def test_step_io_staging_matches_plain_step():
+    """StepIO packs the per-step inputs and the outputs into single blocks: a
+    step fed through one host-to-device copy gives the plain step's results,
+    and new inputs written into the host block take effect."""
+    from prefill_csa_compress_gb300.pipeline import StepIO
+
+    spec = spec_for("serving_decode", seed=57)
+    wl = make_workload(spec)
+    names = ["q", "q_idx", "idx_w", "kv_raw", "idx_raw", "row_req", "row_pos", "kv_len", "n_cmp"]
+    t1 = wl.to(DEV)
+    plain = CsaStep(t1, spec.ratio, spec.topk)
+    plain.run()
+    t2 = wl.to(DEV)
+    io = StepIO(t2, names)
+    staged = CsaStep(t2, spec.ratio, spec.topk)
+    io.bind_outputs(staged)
+    staged.prepare().capture()
+    io.h2d()
+    staged.replay()
+    io.d2h()
+    torch.cuda.synchronize()
+    n = io.out_bytes
+    host = io.host_out[:n]
+    out_b = plain.out.numel() * 2
+    assert torch.equal(host[:out_b].view(torch.bfloat16).view(plain.out.shape), plain.out.cpu())
+    assert torch.equal(staged.topk_idx, plain.topk_idx)
+    # a new query written into the host block changes the next step's result
+    q_new = io.host_input("q", wl.q)
+    q_new.copy_(-wl.q)
+    io.h2d()
+    staged.replay()
+    torch.cuda.synchronize()
+    t3 = wl.to(DEV)
+    t3["q"] = (-wl.q).to(DEV)
+    ref = CsaStep(t3, spec.ratio, spec.topk)
+    ref.run()
+    torch.cuda.synchronize()
+    assert torch.equal(staged.out, ref.out)
