@@ -41,7 +41,10 @@ def _load(spec):
 
 
 def _pools(wl):
-    return {"cmp_pool": wl.cmp_pool, "idx_pool": wl.idx_pool, "idx_scale": wl.idx_scale}
+    p = {"cmp_pool": wl.cmp_pool, "idx_pool": wl.idx_pool, "idx_scale": wl.idx_scale}
+    if "idx_kscale" in wl.t:
+        p.update(idx_kscale=wl.idx_kscale, cmp_scale=wl.cmp_scale)
+    return p
 
 
 def _floor(t, row, pools, positions):
@@ -49,8 +52,13 @@ def _floor(t, row, pools, positions):
     b = int(t["row_req"][row])
     p = int(t["row_pos"][row])
     table = t["cmp_table"][b].numpy()
-    keys = O.page_rows(pools["idx_pool"], table, positions)
-    scl = O.page_rows(pools["idx_scale"], table, positions)
+    if "idx_kscale" in pools:  # FP4 keys: dequantised, unit scale
+        keys = O.cache_rows(O.LowBitPool(pools["idx_pool"], pools["idx_kscale"], "fp4_e8m0"),
+                            table, positions)
+        scl = np.ones(len(keys))
+    else:
+        keys = O.page_rows(pools["idx_pool"], table, positions)
+        scl = O.page_rows(pools["idx_scale"], table, positions)
     q_rot = O.rope_rotate(t["q_idx"][row], p, t["rope_cos"], t["rope_sin"])
     return score_tolerance(q_rot, O.as_f64(t["idx_w"][row]), keys, scl)
 
@@ -144,6 +152,8 @@ HIER_SMALL = [
     # 32-position blocks, padding rows, every block a candidate for short rows
     dict(ctx=[5000, 100], chunk=[2, 1], n_cand=64, cand_block=32, topk=128, seed=73,
          pad_rows=2),
+    # FP4 index keys (low-bit caches): the gathered copies of 64-byte key rows
+    dict(ctx=[40000, 9000], chunk=[2, 2], n_cand=200, topk=256, seed=78, lowbit=True),
 ]
 
 

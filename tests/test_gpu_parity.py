@@ -486,6 +486,7 @@ def test_compress_pair_equals_two_calls(name, over):
 @pytest.mark.parametrize("name,over", [
     ("hca_decode", {}),
     ("hca_prefill", dict(ctx=[1300], chunk=[1300], seed=62)),
+    ("hca_decode", dict(lowbit=True, seed=63)),      # FP4 compressed KV, MXFP8 window
 ])
 def test_hca_step(name, over):
     """HCA: ratio-128 compression, then attention over every visible
