@@ -517,7 +517,8 @@ def run_gpu(args, wl, rank, world, local_rank):
 
     # ---- end to end through the public API with host buffers: the step's
     # per-step inputs packed into one pinned host block and one device block
-    # (one host-to-device copy per step), out and lse likewise (one copy back)
+    # (one host-to-device copy per step), out and lse likewise (one copy
+    # back), around the step's graph
     from prefill_csa_compress_gb300.pipeline import StepIO
 
     per_step_inputs = ["q", "q_idx", "idx_w", "kv_raw", "idx_raw", "row_req", "row_pos",

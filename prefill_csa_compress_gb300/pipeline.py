@@ -65,6 +65,9 @@ class CsaStep:
                      if n_cand else None)
         self.cand_in = cand_in
         self.lowbit = "cmp_scale" in t
+        # called with the stream right before the attention call (StepIO uses
+        # it to wait for the query rows that arrive while the indexer runs)
+        self.before_attention = None
         self.ws = {}
         self._prepared = None
         self._graph = None
@@ -164,9 +167,13 @@ class CsaStep:
                 self.compress(stream)
             if not self.dense:
                 self.index(stream)
+            if self.before_attention:
+                self.before_attention(stream)
             self.attention(stream)
         else:
-            for c in self._prepared:
+            for i, c in enumerate(self._prepared):
+                if i == len(self._prepared) - 1 and self.before_attention:
+                    self.before_attention(stream)
                 c(stream)
         B.prof_join(stream)
 
@@ -245,12 +252,21 @@ class StepIO:
 
     ALIGN = 256
 
-    def __init__(self, t: dict, names):
-        self.names = list(names)
+    def __init__(self, t: dict, names, late=()):
+        # inputs only the attention reads (the query rows) go last: they can
+        # travel on a side stream while the compressors and the indexer run
+        late = [k for k in names if k in set(late)]
+        self.names = [k for k in names if k not in set(late)] + late
         self.offsets, off = {}, 0
         for k in self.names:
+            if k == (late[0] if late else None):
+                self.split = off
             self.offsets[k] = off
             off += self._span(t[k])
+        if not late:
+            self.split = off
+        self._side = None
+        self._late_ev = None
         dev = t[self.names[0]].device
         self.dev_in = torch.empty(max(off, 1), dtype=torch.uint8, device=dev)
         self.host_in = torch.empty(max(off, 1), dtype=torch.uint8, pin_memory=True)
@@ -295,6 +311,40 @@ class StepIO:
 
     def h2d(self):
         self.dev_in.copy_(self.host_in, non_blocking=True)
+
+    def _h2d_split(self):
+        """The inputs before the split on the current stream; the late ones
+        on a side stream, joined by the step right before its attention."""
+        main = torch.cuda.current_stream()
+        self.dev_in[:self.split].copy_(self.host_in[:self.split], non_blocking=True)
+        if self.split >= self.dev_in.numel():
+            return
+        if self._side is None:
+            self._side = torch.cuda.Stream(device=self.dev_in.device)
+            self._late_ev = torch.cuda.Event()
+        self._side.wait_stream(main)
+        with torch.cuda.stream(self._side):
+            self.dev_in[self.split:].copy_(self.host_in[self.split:], non_blocking=True)
+            self._late_ev.record(self._side)
+
+    def capture(self, step):
+        """A CUDA graph of one whole step with its copies: inputs in (the late
+        ones overlapping the compressors and the indexer), the step, outputs
+        out.  Call after a warm-up ``step.run()``; returns the graph."""
+        first = step.steps[0] if isinstance(step, StepChain) else step
+        for s_ in (step.steps if isinstance(step, StepChain) else [step]):
+            if s_._prepared is None:
+                s_.prepare()
+        first.before_attention = (lambda stream: torch.cuda.current_stream().wait_event(
+            self._late_ev)) if self.split < self.dev_in.numel() else None
+        self._h2d_split()  # creates the side stream and event outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            self._h2d_split()
+            step.run()
+            self.d2h()
+        return g
 
     def d2h(self):
         self.host_out.copy_(self.dev_out, non_blocking=True)

@@ -584,3 +584,36 @@ def test_step_io_staging_matches_plain_step():
     ref.run()
     torch.cuda.synchronize()
     assert torch.equal(staged.out, ref.out)
+
+
+def test_step_io_graph_with_late_query_copy():
+    """The whole step with its copies as one graph, the query rows copied on
+    a side stream that the attention waits for: the plain step's results."""
+    from prefill_csa_compress_gb300.pipeline import StepIO
+
+    spec = spec_for("serving_decode", seed=58)
+    wl = make_workload(spec)
+    names = ["q", "q_idx", "idx_w", "kv_raw", "idx_raw", "row_req", "row_pos", "kv_len", "n_cmp"]
+    t1 = wl.to(DEV)
+    plain = CsaStep(t1, spec.ratio, spec.topk)
+    plain.run()
+    t2 = wl.to(DEV)
+    io = StepIO(t2, names, late=("q",))
+    staged = CsaStep(t2, spec.ratio, spec.topk)
+    io.bind_outputs(staged)
+    staged.run()
+    torch.cuda.synchronize()
+    g = io.capture(staged)
+    io.host_input("q", wl.q).copy_(2 * wl.q)  # the next step's query
+    g.replay()
+    torch.cuda.synchronize()
+    t3 = wl.to(DEV)
+    t3["q"] = (2 * wl.q).to(DEV)
+    ref = CsaStep(t3, spec.ratio, spec.topk)
+    ref.run()
+    torch.cuda.synchronize()
+    out_b = ref.out.numel() * 2
+    got = io.host_out[:out_b].view(torch.bfloat16).view(ref.out.shape)
+    assert torch.equal(got, ref.out.cpu())
+    assert torch.equal(staged.topk_idx, plain.topk_idx)
+
