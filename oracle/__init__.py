@@ -23,6 +23,7 @@ from .csa_oracle import (  # noqa: F401
     quantize_fp4_e4m3,
     quantize_fp4_e8m0,
     quantize_int8,
+    quantize_mxfp8,
     round_e2m1,
     round_e4m3,
     rope_rotate,

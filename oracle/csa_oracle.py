@@ -189,6 +189,39 @@ def quantize_fp4_e4m3(y, group=16):
     return pack_nibbles(np.concatenate(codes)), np.array(sbytes, dtype=np.uint8)
 
 
+def _e8m0_exponent_for(amax, top):
+    """Smallest e with top * 2^e >= amax, clamped to [-127, 127] (amax = 0:
+    -127), for a top code of the form 1.f * 2^t."""
+    if amax == 0.0:
+        return -127
+    e = int(np.ceil(np.log2(amax / top)))
+    # exact correction of the logarithm's rounding near powers of two
+    while top * np.ldexp(1.0, e - 1) >= amax:
+        e -= 1
+    while top * np.ldexp(1.0, e) < amax:
+        e += 1
+    return int(min(127, max(-127, e)))
+
+
+def quantize_mxfp8(y, group=32):
+    """Index-key publication in the FP8 index plane.  Reading (the pages name
+    an FP8 index plane but give no layout; this takes the MXFP8 layout they
+    give for the window KV): E4M3 codes with one E8M0 scale per 32 dims; a
+    group's scale is the smallest power of two 2^e with 448 * 2^e >= its
+    amax (no element clips), codes the nearest E4M3 of y / 2^e (ties to the
+    even code), the quotient taken in FP32.  Returns (codes uint8 [n], scale
+    bytes uint8 [n/group])."""
+    y = np.asarray(y, dtype=np.float64).astype(np.float32)
+    codes, sbytes = [], []
+    for grp in y.reshape(-1, group):
+        e = _e8m0_exponent_for(float(np.max(np.abs(grp))), 448.0)
+        q = (grp / np.float32(np.ldexp(1.0, e))).astype(np.float64)
+        mag = round_e4m3(np.abs(q))
+        codes.append((mag | np.where(q < 0, 0x80, 0)).astype(np.uint8))
+        sbytes.append(e + 127)
+    return np.concatenate(codes), np.array(sbytes, dtype=np.uint8)
+
+
 def dequant_fp4(packed, sbytes, group, scale_fmt):
     """Values of one packed E2M1 row with its scale bytes (``scale_fmt``
     "e8m0" or "e4m3")."""
@@ -346,8 +379,9 @@ def compress(x, kv, w_gate, ape, ratio, positions, row_req, gamma=None, rms_eps=
     "Attention paths"), and published as BF16 (``out="bf16"``), as INT8
     codes with an FP32 per-row scale (``out="int8"``), or in a low-bit cache
     format (``out="fp4_e4m3"``: packed E2M1 with E4M3 scales per 16;
-    ``out="fp4_e8m0"``: packed E2M1 with E8M0 scales per 32; "DeepSeek V4.1
-    Flash", production cache ABI, quantised on publication).
+    ``out="fp4_e8m0"``: packed E2M1 with E8M0 scales per 32; ``out="mxfp8"``:
+    E4M3 with E8M0 scales per 32; "DeepSeek V4.1 Flash", production cache ABI
+    and the FP8 index plane, quantised on publication).
 
     Returns a list of (request, g, values) for bf16, (request, g, codes,
     scale) for int8, or (request, g, packed codes, scale bytes) for the
@@ -393,6 +427,8 @@ def _publish_group(b, g, r, logits, kvs, gamma, rms_eps, rotate, rope_cos, rope_
         return (b, g) + quantize_fp4_e4m3(y)
     if out == "fp4_e8m0":
         return (b, g) + quantize_fp4_e8m0(y)
+    if out == "mxfp8":
+        return (b, g) + quantize_mxfp8(y)
     codes, scale = quantize_int8(y)
     return (b, g, codes, scale)
 

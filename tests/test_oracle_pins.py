@@ -862,3 +862,31 @@ def test_lowbit_row_decoders_agree():
             assert np.array_equal(rows[j], pool.dequant_row(pool.codes[0, j], pool.scales[0, j]))
         # no rows (a query that sees no compressed entry)
         assert pool.dequant_rows(pool.codes[0, :0], pool.scales[0, :0]).shape == (0, D)
+
+
+def test_mxfp8_quantiser_scale_rule_and_torch_codes():
+    """FP8 index plane (MXFP8 reading): the scale is the smallest power of two
+    keeping every element within 448, the codes torch's E4M3 cast of the FP32
+    quotient, and E4M3-representable groups come back exactly."""
+    rng = np.random.default_rng(57)
+    for _ in range(100):
+        y = rng.standard_normal(128) * np.exp(rng.uniform(-10, 10))
+        codes, sb = O.quantize_mxfp8(y)
+        for gi in range(4):
+            grp = y[32 * gi:32 * gi + 32]
+            amax = np.max(np.abs(grp))
+            e = int(sb[gi]) - 127
+            assert 448 * 2.0 ** e >= amax > 448 * 2.0 ** (e - 1)
+            q = torch.from_numpy(grp.astype(np.float32) / np.float32(2.0 ** e))
+            want = q.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            assert np.array_equal(codes[32 * gi:32 * gi + 32], want)
+        back = O.dequant_mxfp8(codes, sb)
+        # relative error of E4M3 rounding: at most 2^-4 of the value, or half
+        # the subnormal step 2^-10 times the scale
+        scl = np.repeat(2.0 ** (sb.astype(np.int64) - 127), 32)
+        assert np.all(np.abs(back - y) <= np.maximum(np.abs(y) * 2.0 ** -4, 2.0 ** -10 * scl))
+    y = np.array([1.0, -448.0 / 256, 0.5, 3.0] * 8 + [0.0] * 32)
+    codes, sb = O.quantize_mxfp8(y)
+    assert sb.tolist() == [120, 0]  # amax 3: 448 * 2^-7 = 3.5 >= 3 > 448 * 2^-8
+    assert np.array_equal(O.dequant_mxfp8(codes, sb)[:32], y[:32])
+    assert not codes[32:].any()
