@@ -79,28 +79,32 @@ typedef enum {
  *  - FP4_E8M0: packed E2M1, one E8M0 scale byte (2^(byte-127)) per 32
  *    channels (index keys: 64 code bytes plus 4 scale bytes per 128-dim key).
  *  - MXFP8: one E4M3 byte per channel, one E8M0 scale byte per 32 channels
- *    (window KV: 512 code bytes plus 16 scale bytes per row).
+ *    (window KV: 512 code bytes plus 16 scale bytes per row; the FP8 index
+ *    plane, read as the same layout: 128 code bytes plus 4 scale bytes per
+ *    key).
  * A value is its code times its group's scale.  Publication (readings; the
  * pages give the formats only): FP4_E8M0 takes for each group the smallest
  * 2^e with 6 * 2^e >= amax (amax = 0: e = -127), FP4_E4M3 the E4M3 value
  * nearest to amax / 6 (saturating at 448); codes are the nearest E2M1 of
  * value / scale (ties to the even code, saturating at 6, the sign bit set for
  * negative values), quotients taken in FP32; a zero E4M3 scale gives zero
- * codes.  Code pools are uint8 [n_blocks, 128, code bytes per row] and scale
+ * codes.  MXFP8 takes the smallest 2^e with 448 * 2^e >= amax and codes the
+ * nearest E4M3 of value / 2^e (ties to the even code).  Code pools are uint8 [n_blocks, 128, code bytes per row] and scale
  * pools uint8 [n_blocks, 128, groups per row], both through the block table
  * of the pool they replace. */
 typedef enum {
   CSA_OUT_BF16 = 0,
   CSA_OUT_INT8 = 1,
   CSA_OUT_FP4_E4M3 = 2, /* codes into cmp_pool, scales into scale_pool */
-  CSA_OUT_FP4_E8M0 = 3  /* codes into cmp_pool, scales into scale_pool */
+  CSA_OUT_FP4_E8M0 = 3, /* codes into cmp_pool, scales into scale_pool */
+  CSA_OUT_MXFP8 = 4     /* codes (one byte a channel) into cmp_pool, scales into scale_pool */
 } csa_out_mode_t;
 typedef enum {
   CSA_FMT_BF16 = 0,     /* attention pools: bf16 rows */
   CSA_FMT_INT8 = 1,     /* index keys: int8 codes, f32 scale per row */
   CSA_FMT_FP4_E4M3 = 2, /* compressed KV */
   CSA_FMT_FP4_E8M0 = 3, /* index keys */
-  CSA_FMT_MXFP8 = 4     /* window KV */
+  CSA_FMT_MXFP8 = 4     /* window KV; index keys (the FP8 index plane) */
 } csa_cache_fmt_t;
 typedef enum { CSA_MODE_AUTO = 0, CSA_MODE_DECODE = 1, CSA_MODE_PREFILL = 2 } csa_mode_t;
 
@@ -150,11 +154,12 @@ typedef enum { CSA_MODE_AUTO = 0, CSA_MODE_DECODE = 1, CSA_MODE_PREFILL = 2 } cs
  * ratio (at most 256).  A caller built against a header without these four fields passes a
  * smaller struct_size and gets no ring.
  *
- * Low-bit publication (out_mode CSA_OUT_FP4_E4M3 or CSA_OUT_FP4_E8M0, see
- * csa_cache_fmt_t): the row as it would be published in BF16 (rotated when
- * `rotate`, in FP32) is quantised per group; codes go to cmp_pool as uint8
- * [n_blocks, 128, d / 2] and scale bytes to scale_pool.  Needs a struct_size
- * that covers scale_pool.
+ * Low-bit publication (out_mode CSA_OUT_FP4_E4M3, CSA_OUT_FP4_E8M0 or
+ * CSA_OUT_MXFP8, see csa_cache_fmt_t): the row as it would be published in
+ * BF16 (rotated when `rotate`, in FP32) is quantised per group; codes go to
+ * cmp_pool as uint8 [n_blocks, 128, d / 2] (FP4) or [n_blocks, 128, d]
+ * (MXFP8) and scale bytes to scale_pool.  Needs a struct_size that covers
+ * scale_pool.
  * ---------------------------------------------------------------------- */
 typedef struct {
   uint32_t struct_size;
@@ -264,8 +269,10 @@ CSA_API csa_status_t csa_compress_pair(csa_compress_args *first, csa_compress_ar
  * returns CSA_ERR_UNSUPPORTED for either mode.
  *
  * Key format: key_fmt CSA_FMT_FP4_E8M0 reads idx_pool as packed E2M1 codes
- * uint8 [n_blocks, 128, 64] with key_scale_pool, k_c is the dequantised key
- * and scale_c = 1 (idx_scale_pool unused).  CSA_FMT_INT8 (or 0, or a
+ * uint8 [n_blocks, 128, 64] with key_scale_pool, CSA_FMT_MXFP8 as E4M3
+ * codes uint8 [n_blocks, 128, 128] with key_scale_pool (E8M0 bytes
+ * [n_blocks, 128, 4] either way); k_c is the dequantised key and scale_c = 1
+ * (idx_scale_pool unused).  CSA_FMT_INT8 (or 0, or a
  * struct_size that ends before key_fmt) is the INT8 + FP32 layout above.
  * ---------------------------------------------------------------------- */
 typedef struct {
@@ -302,8 +309,8 @@ typedef struct {
   int32_t n_cand;           /* candidate blocks per row */
   int32_t *cand_out;        /* i32 [n_rows, n_cand] or NULL: level-one selection */
   const int32_t *cand_in;   /* i32 [n_rows, n_cand] or NULL: reindex candidates */
-  int32_t key_fmt;          /* csa_cache_fmt_t: CSA_FMT_INT8 (0 reads as INT8) or FP4_E8M0 */
-  const uint8_t *key_scale_pool; /* FP4_E8M0: scale bytes [n_blocks, 128, 4] */
+  int32_t key_fmt;          /* csa_cache_fmt_t: CSA_FMT_INT8 (0 reads as INT8), FP4_E8M0 or MXFP8 */
+  const uint8_t *key_scale_pool; /* FP4_E8M0, MXFP8: scale bytes [n_blocks, 128, 4] */
 } csa_index_args;
 
 CSA_API csa_status_t csa_index_topk(csa_index_args *args, csa_stream_t stream);

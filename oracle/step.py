@@ -23,10 +23,15 @@ def _lowbit(t):
     return "cmp_scale" in t
 
 
+def _key_fmt(t):
+    """Low-bit index keys: "fp4_e8m0" (64 bytes a key) or "mxfp8" (128)."""
+    return "mxfp8" if t["idx_pool"].shape[-1] == t["q_idx"].shape[-1] else "fp4_e8m0"
+
+
 def _idx_pool(t, pools):
-    """The index-key pool as the oracle reads it (FP4 keys: a LowBitPool)."""
+    """The index-key pool as the oracle reads it (low-bit keys: a LowBitPool)."""
     if _lowbit(t):
-        return O.LowBitPool(pools["idx_pool"], pools["idx_kscale"], "fp4_e8m0")
+        return O.LowBitPool(pools["idx_pool"], pools["idx_kscale"], _key_fmt(t))
     return pools["idx_pool"]
 
 
@@ -47,7 +52,7 @@ def compress_step(t, spec, pools=None):
     pools = clone_pools(t) if pools is None else pools
     lowbit = _lowbit(t)
     idx_kw = dict(rotate=True, rope_cos=t["rope_cos"], rope_sin=t["rope_sin"],
-                  rope_dim=spec.rope_dim, out="fp4_e8m0" if lowbit else "int8")
+                  rope_dim=spec.rope_dim, out=_key_fmt(t) if lowbit else "int8")
     main_out = "fp4_e4m3" if lowbit else "bf16"
     if spec.state:
         pools["state_main"] = O.as_f64(t["state_main"]).copy()

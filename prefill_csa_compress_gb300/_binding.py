@@ -244,7 +244,7 @@ def _fill_common_rope(args, rope_cos, rope_sin):
 # ---------------------------------------------------------------- the four calls
 
 
-_OUT_MODES = {"bf16": 0, "int8": 1, "fp4_e4m3": 2, "fp4_e8m0": 3}
+_OUT_MODES = {"bf16": 0, "int8": 1, "fp4_e4m3": 2, "fp4_e8m0": 3, "mxfp8": 4}
 
 
 def _compress_struct(*, x, kv, w_gate, ape, ratio, positions, row_req, block_table, out="bf16",
@@ -273,9 +273,9 @@ def _compress_struct(*, x, kv, w_gate, ape, ratio, positions, row_req, block_tab
     if a.out_mode == CSA_OUT_BF16:
         a.cmp_pool = _p(cmp_pool, torch.bfloat16, "cmp_pool")
         a.n_blocks = int(cmp_pool.shape[0])
-    elif out.startswith("fp4"):  # packed codes into cmp_pool, scale bytes into scale_pool
+    elif out in ("fp4_e4m3", "fp4_e8m0", "mxfp8"):  # codes into cmp_pool, scales into scale_pool
         group = 16 if out == "fp4_e4m3" else 32
-        _shape(cmp_pool, (None, 128, a.d // 2), "cmp_pool")
+        _shape(cmp_pool, (None, 128, a.d if out == "mxfp8" else a.d // 2), "cmp_pool")
         _shape(scale_pool, (cmp_pool.shape[0], 128, a.d // group), "scale_pool")
         a.cmp_pool = _p(cmp_pool, torch.uint8, "cmp_pool")
         a.scale_pool = _p(scale_pool, torch.uint8, "scale_pool")
@@ -332,14 +332,16 @@ def csa_index_topk(*, q_idx, weights, row_req, row_pos, n_cmp, ratio, idx_pool, 
                    cmp_block_table, topk, topk_idx, topk_score=None, scores=None, relu=True,
                    rope_cos=None, rope_sin=None, mode=CSA_MODE_AUTO, status=None,
                    cand_out=None, cand_in=None, cand_block=8, key_scale_pool=None,
-                   workspace=None, stream=None, prepare=False):
+                   key_fmt="fp4", workspace=None, stream=None, prepare=False):
     """Indexer scores and deterministic top-k (``include/csa.h``: csa_index_topk).
 
     ``cand_out`` (i32 [n_rows, n_cand]) also selects the level-one candidate
     blocks; ``cand_in`` restricts scoring and selection to given candidate
     blocks (reindex).  With ``key_scale_pool`` (uint8 [blocks, 128, 4]) the
-    keys are FP4 (``idx_pool`` uint8 [blocks, 128, 64]: packed E2M1 with E8M0
-    scales per 32 dims) and ``idx_scale_pool`` is unused."""
+    keys are low-bit, ``key_fmt`` "fp4" (``idx_pool`` uint8 [blocks, 128, 64]:
+    packed E2M1 with E8M0 scales per 32 dims) or "mxfp8" (uint8 [blocks, 128,
+    128]: E4M3 with E8M0 scales per 32 dims), and ``idx_scale_pool`` is
+    unused."""
     a = IndexArgs()
     a.struct_size = ctypes.sizeof(IndexArgs)
     a.n_rows = int(q_idx.shape[0])
@@ -355,9 +357,9 @@ def csa_index_topk(*, q_idx, weights, row_req, row_pos, n_cmp, ratio, idx_pool, 
     a.row_pos = _p(row_pos, torch.int32, "row_pos")
     a.n_cmp = _p(n_cmp, torch.int32, "n_cmp")
     if key_scale_pool is not None:
-        _shape(idx_pool, (None, 128, 64), "idx_pool")
+        _shape(idx_pool, (None, 128, 64 if key_fmt == "fp4" else 128), "idx_pool")
         _shape(key_scale_pool, (idx_pool.shape[0], 128, 4), "key_scale_pool")
-        a.key_fmt = CSA_FMT_FP4_E8M0
+        a.key_fmt = CSA_FMT_FP4_E8M0 if key_fmt == "fp4" else CSA_FMT_MXFP8
         a.idx_pool = _p(idx_pool, torch.uint8, "idx_pool")
         a.key_scale_pool = _p(key_scale_pool, torch.uint8, "key_scale_pool")
     else:

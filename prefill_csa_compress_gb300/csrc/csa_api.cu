@@ -72,7 +72,7 @@ csa_index_args full_index_args(const csa_index_args *a) {
 }
 
 bool index_pointers_ok(const csa_index_args *a) {
-  const bool fp4 = a->key_fmt == CSA_FMT_FP4_E8M0;
+  const bool fp4 = a->key_fmt == CSA_FMT_FP4_E8M0 || a->key_fmt == CSA_FMT_MXFP8;
   if (!a->q_idx || !a->weights || !a->row_req || !a->row_pos || !a->n_cmp || !a->idx_pool ||
       !a->cmp_block_table || !a->topk_idx)
     return false;
@@ -196,7 +196,7 @@ static csa_status_t check_compress(csa_compress_args *a, bool *size_query) {
     return CSA_ERR_UNSUPPORTED;
   if (a->d != 128 && a->d != 512) return CSA_ERR_UNSUPPORTED;
   if (a->dx <= 0 || a->dx % 64 != 0 || a->dx > 1024) return CSA_ERR_UNSUPPORTED;
-  if (a->out_mode < CSA_OUT_BF16 || a->out_mode > CSA_OUT_FP4_E8M0) return CSA_ERR_INVALID_ARG;
+  if (a->out_mode < CSA_OUT_BF16 || a->out_mode > CSA_OUT_MXFP8) return CSA_ERR_INVALID_ARG;
   const size_t need = align_up((size_t)a->n_rows * a->d * sizeof(float), kAlign);
   if (!a->workspace) {
     a->workspace_bytes = need;
@@ -212,7 +212,8 @@ static csa_status_t check_compress(csa_compress_args *a, bool *size_query) {
   if (a->out_mode == CSA_OUT_BF16 && !a->cmp_pool) return CSA_ERR_INVALID_ARG;
   if (a->out_mode == CSA_OUT_INT8 && (!a->idx_pool || !a->idx_scale_pool))
     return CSA_ERR_INVALID_ARG;
-  if ((a->out_mode == CSA_OUT_FP4_E4M3 || a->out_mode == CSA_OUT_FP4_E8M0) &&
+  if ((a->out_mode == CSA_OUT_FP4_E4M3 || a->out_mode == CSA_OUT_FP4_E8M0 ||
+       a->out_mode == CSA_OUT_MXFP8) &&
       (!a->cmp_pool || !a->scale_pool))
     return CSA_ERR_INVALID_ARG;
   if (a->rotate && (!a->rope_cos || !a->rope_sin || a->rope_cap <= 0)) return CSA_ERR_INVALID_ARG;
@@ -311,7 +312,8 @@ CSA_API csa_status_t csa_index_topk(csa_index_args *user, csa_stream_t stream) {
   if (a->n_heads != kHeads || a->head_dim != kIdxDim) return CSA_ERR_UNSUPPORTED;
   if (a->topk < 1 || a->topk > CSA_MAX_TOPK || a->ratio < 1) return CSA_ERR_INVALID_ARG;
   if (a->max_blocks <= 0) return CSA_ERR_INVALID_ARG;
-  if (a->key_fmt != 0 && a->key_fmt != CSA_FMT_INT8 && a->key_fmt != CSA_FMT_FP4_E8M0)
+  if (a->key_fmt != 0 && a->key_fmt != CSA_FMT_INT8 && a->key_fmt != CSA_FMT_FP4_E8M0 &&
+      a->key_fmt != CSA_FMT_MXFP8)
     return CSA_ERR_UNSUPPORTED;
   const bool lvl1 = a->cand_out != nullptr, reidx = a->cand_in != nullptr;
   int cb_shift = 3;

@@ -55,7 +55,8 @@ extern "C" CSA_API csa_status_t csa_index_topk_noalloc(csa_index_args *user,
   if (!own_scores && (long long)a->n_rows * n_cap > (long long)kMaxScores)
     return CSA_ERR_UNSUPPORTED;
   if (a->n_rows == 0) return CSA_OK;
-  if (a->key_fmt != 0 && a->key_fmt != CSA_FMT_INT8 && a->key_fmt != CSA_FMT_FP4_E8M0)
+  if (a->key_fmt != 0 && a->key_fmt != CSA_FMT_INT8 && a->key_fmt != CSA_FMT_FP4_E8M0 &&
+      a->key_fmt != CSA_FMT_MXFP8)
     return CSA_ERR_UNSUPPORTED;
   if (!index_pointers_ok(a)) return CSA_ERR_INVALID_ARG;
   float *scores = a->scores;

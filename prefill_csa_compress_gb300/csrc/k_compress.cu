@@ -207,6 +207,22 @@ __device__ __forceinline__ void publish_fp4(const csa_compress_args &a, long lon
   if (live && d % G == 0) a.scale_pool[dst_row * (D / G) + d / G] = (uint8_t)sbyte;
 }
 
+// MXFP8 publication (the FP8 index plane read as MXFP8): one E4M3 code per
+// channel, one E8M0 scale per group of 32 lanes (same calling rules as
+// publish_fp4).
+__device__ __forceinline__ void publish_mxfp8(const csa_compress_args &a, long long dst_row, int d,
+                                              float y, bool live) {
+  float v = live ? fabsf(y) : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int e = lowbit::e8m0_exponent_448(v);
+  const uint32_t code = (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(y, lowbit::pow2f(e)),
+                                                        __NV_SATFINITE, __NV_E4M3);
+  const int D = a.d;
+  if (live) static_cast<uint8_t *>(a.cmp_pool)[dst_row * D + d] = (uint8_t)code;
+  if (live && d % 32 == 0) a.scale_pool[dst_row * (D / 32) + d / 32] = (uint8_t)(e + 127);
+}
+
 __device__ __forceinline__ float block_sum(float v, float *red) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -353,6 +369,8 @@ __global__ void compress_pool_kernel(csa_compress_args a, const float *__restric
     publish_fp4<16>(a, dst_row, d, y, true);
   } else if (a.out_mode == CSA_OUT_FP4_E8M0) {
     publish_fp4<32>(a, dst_row, d, y, true);
+  } else if (a.out_mode == CSA_OUT_MXFP8) {
+    publish_mxfp8(a, dst_row, d, y, true);
   } else {
     float amax = block_max(fabsf(y), red);
     float scale = fmaxf(amax, 1e-4f) / 127.0f;
@@ -568,6 +586,8 @@ __device__ __forceinline__ void fused_group(const csa_compress_args &a, const in
     publish_fp4<16>(a, dst_row, d, y, c < COLS);
   } else if (a.out_mode == CSA_OUT_FP4_E8M0) {
     publish_fp4<32>(a, dst_row, d, y, c < COLS);
+  } else if (a.out_mode == CSA_OUT_MXFP8) {
+    publish_mxfp8(a, dst_row, d, y, c < COLS);
   } else {
     float v = c < COLS ? fabsf(y) : 0.f;
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

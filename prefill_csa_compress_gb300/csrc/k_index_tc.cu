@@ -206,6 +206,9 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   // FP4 index keys ("DeepSeek V4.1 Flash", production cache ABI): packed E2M1
   // with one E8M0 scale per 32 dims, copied linearly and decoded to FP16
   const bool fp4 = a.key_fmt == CSA_FMT_FP4_E8M0;
+  // FP8 keys (the FP8 index plane, MXFP8: E4M3 codes with one E8M0 scale per
+  // 32 dims): the INT8 page layout, decoded to FP16 like the FP4 keys
+  const bool fp8 = a.key_fmt == CSA_FMT_MXFP8;
   const bool rope = a.rope_cos != nullptr;
   const int n_kchunks = rope ? 3 : 2;
   const int n_cap = a.max_blocks * kBlock;
@@ -473,8 +476,10 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
               tc::tma_load_2d(dst, &keys_map, 0, (int)grow, &M->st_full[s]);
             else
               tc::bulk_g2s(dst, a.idx_pool + grow * kIdxDim, cb * kIdxDim, &M->st_full[s]);
-            tc::bulk_g2s(StSc + s * kBlock + lane * cb, a.idx_scale_pool + grow, cb * 4,
-                         &M->st_full[s]);
+            tc::bulk_g2s(StSc + s * kBlock + lane * cb,
+                         fp8 ? static_cast<const void *>(a.key_scale_pool + grow * 4)
+                             : static_cast<const void *>(a.idx_scale_pool + grow),
+                         cb * 4, &M->st_full[s]);
           }
         }
       } else if (warp == W_PROD) {
@@ -507,7 +512,11 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
               else
                 tc::bulk_g2s(St + s * C::PAGE, a.idx_pool + (long long)phys * C::PAGE, C::PAGE,
                              &M->st_full[s]);
-              tc::bulk_g2s(StSc + s * kBlock, a.idx_scale_pool + (long long)phys * kBlock,
+              tc::bulk_g2s(StSc + s * kBlock,
+                           fp8 ? static_cast<const void *>(a.key_scale_pool +
+                                                           (long long)phys * kBlock * 4)
+                               : static_cast<const void *>(a.idx_scale_pool +
+                                                           (long long)phys * kBlock),
                            kBlock * 4, &M->st_full[s]);
             } else {
               flag(a.status_dev, CSA_DEV_BAD_BLOCK);
@@ -545,6 +554,34 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
                 const __half2 sc2 = lowbit::e8m0_group_h2(sb4, half * 2 + (c >> 1), R);
                 const uint4 lo = lowbit::e2m1x8_to_f16x8(w.x, sc2);
                 const uint4 hi = lowbit::e2m1x8_to_f16x8(w.y, sc2);
+                packed[8 * c + 0] = lo.x;
+                packed[8 * c + 1] = lo.y;
+                packed[8 * c + 2] = lo.z;
+                packed[8 * c + 3] = lo.w;
+                packed[8 * c + 4] = hi.x;
+                packed[8 * c + 5] = hi.y;
+                packed[8 * c + 6] = hi.z;
+                packed[8 * c + 7] = hi.w;
+              }
+              tc::tmem_st32u(tmem + ((uint32_t)(wq * 32) << 16) + C::A_COL + j * 64 + half * 32,
+                             packed);
+              tc::tmem_wait_st();
+              if (half == 0) Sc[sc * kBlock + r] = lowbit::pow2f(R);
+            } else if (ok && fp8) {
+              // FP8 keys: this half's four swizzled 16-byte chunks of E4M3
+              // codes, each group scaled by 2^(E_g - R) into FP16
+              const uint8_t *src = St + s * C::PAGE + r * 128;
+              const uint32_t sb4 =
+                  reinterpret_cast<const uint32_t *>(StSc)[s * kBlock + r];
+              const int R = lowbit::e8m0_row_shift(sb4);
+              uint32_t packed[32];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const int cc = half * 4 + c;
+                const uint4 raw = *reinterpret_cast<const uint4 *>(src + ((cc ^ (r & 7)) << 4));
+                const __half2 sc2 = lowbit::e8m0_group_h2(sb4, cc >> 1, R);
+                const uint4 lo = lowbit::e4m3x8_to_f16x8(make_uint2(raw.x, raw.y), sc2);
+                const uint4 hi = lowbit::e4m3x8_to_f16x8(make_uint2(raw.z, raw.w), sc2);
                 packed[8 * c + 0] = lo.x;
                 packed[8 * c + 1] = lo.y;
                 packed[8 * c + 2] = lo.z;
@@ -605,6 +642,30 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
               const int R = lowbit::e8m0_row_shift(sb4[q]);
               *reinterpret_cast<uint4 *>(dst + kc * C::A_CHUNK + r * 128 + ((jj ^ (r & 7)) << 4)) =
                   lowbit::e2m1x8_to_f16x8(raw[q], lowbit::e8m0_group_h2(sb4[q], jc >> 2, R));
+            }
+            if (ct < kBlock) Sc[sc * kBlock + ct] = lowbit::pow2f(lowbit::e8m0_row_shift(sbw[ct]));
+          } else if (ok && fp8) {
+            // FP8 keys: unit = (row, 8 dims): two code words and the row's
+            // four E8M0 bytes
+            const uint8_t *src = St + s * C::PAGE;
+            const uint32_t *sbw = reinterpret_cast<const uint32_t *>(StSc) + s * kBlock;
+            uint8_t *dst = As + j * C::A_BUF;
+            uint2 raw[8];
+            uint32_t sb4[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int unit = q * IT_CONV + ct;
+              raw[q] = *reinterpret_cast<const uint2 *>(src + (unit >> 4) * 128 + (unit & 15) * 8);
+              sb4[q] = sbw[unit >> 4];
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int unit = q * IT_CONV + ct;
+              const int r = unit >> 4, jc = unit & 15;
+              const int kc = jc >> 3, jj = jc & 7;
+              const int R = lowbit::e8m0_row_shift(sb4[q]);
+              *reinterpret_cast<uint4 *>(dst + kc * C::A_CHUNK + r * 128 + ((jj ^ (r & 7)) << 4)) =
+                  lowbit::e4m3x8_to_f16x8(raw[q], lowbit::e8m0_group_h2(sb4[q], jc >> 2, R));
             }
             if (ct < kBlock) Sc[sc * kBlock + ct] = lowbit::pow2f(lowbit::e8m0_row_shift(sbw[ct]));
           } else if (ok) {

@@ -96,6 +96,30 @@ __device__ __forceinline__ uint4 e2m1x8_to_f16x8(uint32_t w, __half2 scale2) {
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+// Eight E4M3 codes (two words, the low byte first) as eight FP16 values
+// times `scale2` (a power of two; exact unless a product falls below 2^-24).
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 w, __half2 scale2) {
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t word = i < 2 ? w.x : w.y;
+    const __half2 h = __hmul2(as_h2(cvt_e4m3x2(word >> (16 * (i & 1)))), scale2);
+    out[i] = *reinterpret_cast<const uint32_t *>(&h);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// The E8M0 exponent of an MXFP8 group: the smallest e with 448 * 2^e >=
+// amax, in [-127, 127] (amax = 0: -127).  With amax = m * 2^k, m in
+// [0.5, 1): e = k - 9 + (2m > 1.75).
+__device__ __forceinline__ int e8m0_exponent_448(float amax) {
+  if (!(amax > 0.f)) return -127;
+  int k;
+  const float m = frexpf(amax, &k);
+  const int e = k - 9 + (2.f * m > 1.75f ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
 // Row shift of an FP4 index key: R = the largest of its four E8M0 exponents
 // (scale bytes in one word).  The key's values are dequantised to FP16 as
 // code * 2^(E_g - R), and 2^R multiplies the key's score.

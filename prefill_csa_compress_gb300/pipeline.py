@@ -65,6 +65,9 @@ class CsaStep:
                      if n_cand else None)
         self.cand_in = cand_in
         self.lowbit = "cmp_scale" in t
+        # low-bit index keys: packed E2M1 (64 bytes a key) or MXFP8 (128 bytes)
+        self.key_fmt = ("mxfp8" if self.lowbit and t["idx_pool"].shape[-1] == t["q_idx"].shape[-1]
+                        else "fp4")
         # called with the stream right before the attention call (StepIO uses
         # it to wait for the query rows that arrive while the indexer runs)
         self.before_attention = None
@@ -91,8 +94,9 @@ class CsaStep:
             keys.update(state_cache=t["state_idx"], state_block_table=t["state_table"])
         if self.lowbit:  # publication in the low-bit cache formats
             main.update(out="fp4_e4m3", scale_pool=t["cmp_scale"])
-            keys.update(out="fp4_e8m0", cmp_pool=t["idx_pool"], scale_pool=t["idx_kscale"],
-                        idx_pool=None, idx_scale_pool=None)
+            keys.update(out="mxfp8" if self.key_fmt == "mxfp8" else "fp4_e8m0",
+                        cmp_pool=t["idx_pool"], scale_pool=t["idx_kscale"], idx_pool=None,
+                        idx_scale_pool=None)
         return main, keys
 
     def compress(self, stream=None):
@@ -113,7 +117,7 @@ class CsaStep:
             rope_sin=t["rope_sin"],
             mode=B.CSA_MODE_PREFILL if self.prefill else B.CSA_MODE_DECODE, status=self.status,
             cand_out=self.cand, cand_in=self.cand_in, cand_block=self.cand_block,
-            key_scale_pool=t.get("idx_kscale"))
+            key_scale_pool=t.get("idx_kscale"), key_fmt=self.key_fmt)
 
     def _attn_kw(self):
         t = self.t

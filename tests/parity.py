@@ -133,3 +133,22 @@ def check_fp4(codes, sbytes, ref_codes, ref_sbytes, group, scale_fmt):
     assert np.all(ok[diff]), "a code differs by more than one grid step"
     return int((sb != rsb).sum()), int(diff.sum())
 
+
+def check_mxfp8(codes, sbytes, ref_codes, ref_sbytes, group=32):
+    """MXFP8 codes (E4M3, one byte a channel) and E8M0 scale bytes from the
+    GPU against the oracle's, with the same allowances as check_fp4: a scale
+    byte may differ by one, a code (where the scales agree) only to the
+    neighbouring E4M3 value of the same sign.  Returns (differing scale
+    groups, differing codes)."""
+    sb = np.asarray(sbytes, np.int64)
+    rsb = np.asarray(ref_sbytes, np.int64)
+    assert np.all(np.abs(sb - rsb) <= 1), "scale bytes differ by more than one"
+    same = np.repeat(sb == rsb, group)
+    c = np.asarray(codes, np.int64)[same]
+    rc = np.asarray(ref_codes, np.int64)[same]
+    diff = c != rc
+    mag, rmag = c & 0x7F, rc & 0x7F
+    ok = (np.abs(mag - rmag) <= 1) & (((c ^ rc) & 0x80 == 0) | (mag == 0) | (rmag == 0))
+    assert np.all(ok[diff]), "a code differs by more than one step"
+    return int((sb != rsb).sum()), int(diff.sum())
+

@@ -16,8 +16,8 @@ import torch
 
 import oracle as O
 from oracle import step as OS
-from parity import (INT8_FLIP_RATE, LSE_ABS, check_bf16, check_fp4, check_scores, check_topk,
-                    score_tolerance)
+from parity import (INT8_FLIP_RATE, LSE_ABS, check_bf16, check_fp4, check_mxfp8, check_scores,
+                    check_topk, score_tolerance)
 from workloads import BLOCK, make_workload, random_selection, spec_for
 
 pytestmark = pytest.mark.gpu
@@ -51,6 +51,8 @@ def _load(spec):
     (600, 4, 256, 128, "fp4_e8m0"),   # long chunk, rotated
     (12, 2, 256, 512, "fp4_e8m0"),    # 32-channel groups of a 512-channel row: row kernels
     (9, 1, 128, 128, "fp4_e4m3"),
+    (12, 4, 128, 128, "mxfp8"),       # FP8 index keys, fused kernel
+    (600, 4, 256, 128, "mxfp8"),      # FP8 index keys, long chunk
 ])
 def test_fp4_publication(n_rows, ratio, dx, d, out):
     rng = np.random.default_rng(n_rows * 11 + ratio + d)
@@ -64,10 +66,11 @@ def test_fp4_publication(n_rows, ratio, dx, d, out):
     ape = torch.from_numpy(rng.standard_normal((ratio, d)).astype(np.float32))
     from workloads import rope_tables
     cos, sin = rope_tables(4096)
-    rotate = out == "fp4_e8m0"
-    group = 32 if out == "fp4_e8m0" else 16
+    rotate = out in ("fp4_e8m0", "mxfp8")
+    group = 16 if out == "fp4_e4m3" else 32
     table = torch.tensor([[2, 0, 3, 1]], dtype=torch.int32)
-    codes = torch.zeros((4, BLOCK, d // 2), dtype=torch.uint8, device=DEV)
+    codes = torch.zeros((4, BLOCK, d if out == "mxfp8" else d // 2), dtype=torch.uint8,
+                        device=DEV)
     scales = torch.zeros((4, BLOCK, d // group), dtype=torch.uint8, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     csa.csa_compress(x=x.to(DEV), kv=kv.to(DEV), w_gate=w.to(DEV), ape=ape.to(DEV), ratio=ratio,
@@ -84,15 +87,18 @@ def test_fp4_publication(n_rows, ratio, dx, d, out):
     n_sc = n_code = 0
     for _, g, rc, rs in ref:
         pg, row = int(table[0, g // BLOCK]), g % BLOCK
-        a, b = check_fp4(gc[pg, row], gs[pg, row], rc, rs, group,
-                         "e8m0" if out == "fp4_e8m0" else "e4m3")
+        if out == "mxfp8":
+            a, b = check_mxfp8(gc[pg, row], gs[pg, row], rc, rs)
+        else:
+            a, b = check_fp4(gc[pg, row], gs[pg, row], rc, rs, group,
+                             "e8m0" if out == "fp4_e8m0" else "e4m3")
         n_sc += a
         n_code += b
     assert n_sc <= INT8_FLIP_RATE * len(ref) * d // group + 1, n_sc
     assert n_code <= INT8_FLIP_RATE * len(ref) * d + 2, n_code
     # rows outside the published groups stay zero
     written = {int(table[0, g // BLOCK]) * BLOCK + g % BLOCK for _, g, _, _ in ref}
-    flat = gc.reshape(-1, d // 2)
+    flat = gc.reshape(-1, gc.shape[-1])
     others = [i for i in range(flat.shape[0]) if i not in written]
     assert not flat[others].any()
 
@@ -106,7 +112,8 @@ def _check_fp4_index_rows(wl, t, spec, step, rows, sc):
     pools = {"idx_pool": wl.idx_pool, "idx_kscale": wl.idx_kscale, "cmp_pool": wl.cmp_pool,
              "cmp_scale": wl.cmp_scale}
     sel = step.topk_idx.cpu().numpy()
-    kpool = O.LowBitPool(wl.idx_pool, wl.idx_kscale, "fp4_e8m0")
+    kpool = O.LowBitPool(wl.idx_pool, wl.idx_kscale,
+                         "mxfp8" if spec.key_fmt == "mxfp8" else "fp4_e8m0")
     for row in rows:
         b = int(wl.row_req[row])
         ref = OS.index_row(wl.t, spec, pools, row)
@@ -125,6 +132,10 @@ def _check_fp4_index_rows(wl, t, spec, step, rows, sc):
     ("lowbit_decode", {}),
     ("lowbit_decode", dict(ctx=[40000, 3000], chunk=[2, 2], ratio=4, topk=700, seed=91,
                            kv_pool_pages=None, cmp_pool_pages=None)),
+    ("lowbit_decode", dict(key_fmt="mxfp8", seed=97)),            # FP8 index keys
+    ("lowbit_decode", dict(ctx=[3000], chunk=[80], ratio=4, topk=128, seed=98,
+                           kv_pool_pages=None, cmp_pool_pages=None,
+                           key_fmt="mxfp8")),                     # FP8, four-row groups
 ])
 def test_fp4_index_parity(name, over):
     spec = spec_for(name, **over)
@@ -273,6 +284,7 @@ def test_lowbit_prefill_attention(over):
     ("lowbit_decode", {}),
     ("lowbit_million", {}),
     ("lowbit_prefill", dict(ctx=[1500], chunk=[1500], seed=96)),   # FP4 publication of 375 groups
+    ("lowbit_decode", dict(key_fmt="mxfp8", seed=99)),               # FP8 index keys
 ])
 def test_lowbit_step_chain(name, over):
     """compress (FP4 publication) -> FP4 indexer -> low-bit attention, against

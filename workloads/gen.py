@@ -53,6 +53,7 @@ class WorkloadSpec:
     # scales (cmp_pool uint8 + cmp_scale), index keys FP4 with E8M0 scales
     # (idx_pool uint8 + idx_kscale)
     lowbit: bool = False
+    key_fmt: str = "fp4"  # low-bit index keys: "fp4" (E2M1 + E8M0) or "mxfp8" (E4M3 + E8M0)
     extra: dict = field(default_factory=dict)
 
     @property
@@ -298,7 +299,9 @@ def _lowbit_pools(rng, spec, P_kv, P_c):
     happens here).  Window MXFP8 codes: random sign, E4M3 exponent field 4..8
     and mantissa (magnitudes 1/8 .. 3.75), E8M0 scales 2^-1 or 2^0; FP4
     compressed KV: uniform nibbles, E4M3 scales with exponent field 4..7
-    (1/8 .. 1.875); FP4 index keys: uniform nibbles, E8M0 scales 2^-3 .. 2^0.
+    (1/8 .. 1.875); FP4 index keys: uniform nibbles, E8M0 scales 2^-3 .. 2^0;
+    FP8 index keys (key_fmt "mxfp8"): E4M3 codes drawn like the window's, the
+    same E8M0 scales.
     With ``cmp_init="zeros"`` the compressed pools start as zero bytes (the
     step's compressors fill them)."""
     Dm, Di = spec.head_dim, spec.idx_dim
@@ -314,13 +317,22 @@ def _lowbit_pools(rng, spec, P_kv, P_c):
         out["cmp_scale"] = torch.from_numpy(
             ((rng.integers(4, 8, g, dtype=np.uint8) << 3) | rng.integers(0, 8, g, dtype=np.uint8))
             .astype(np.uint8))
-        out["idx_pool"] = torch.from_numpy(rng.integers(0, 256, (P_c, BLOCK, Di // 2), dtype=np.uint8))
+        if spec.key_fmt == "mxfp8":  # E4M3 codes drawn like the window's
+            ks = (P_c, BLOCK, Di)
+            out["idx_pool"] = torch.from_numpy(
+                ((rng.integers(0, 2, ks, dtype=np.uint8) << 7) |
+                 (rng.integers(4, 9, ks, dtype=np.uint8) << 3) |
+                 rng.integers(0, 8, ks, dtype=np.uint8)).astype(np.uint8))
+        else:
+            out["idx_pool"] = torch.from_numpy(
+                rng.integers(0, 256, (P_c, BLOCK, Di // 2), dtype=np.uint8))
         out["idx_kscale"] = torch.from_numpy(rng.integers(124, 128, (P_c, BLOCK, Di // 32),
                                                           dtype=np.uint8))
     else:
         out["cmp_pool"] = torch.zeros((P_c, BLOCK, Dm // 2), dtype=torch.uint8)
         out["cmp_scale"] = torch.zeros((P_c, BLOCK, Dm // 16), dtype=torch.uint8)
-        out["idx_pool"] = torch.zeros((P_c, BLOCK, Di // 2), dtype=torch.uint8)
+        out["idx_pool"] = torch.zeros((P_c, BLOCK, Di if spec.key_fmt == "mxfp8" else Di // 2),
+                                      dtype=torch.uint8)
         out["idx_kscale"] = torch.zeros((P_c, BLOCK, Di // 32), dtype=torch.uint8)
     return out
 
