@@ -37,27 +37,31 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # kernel reports null.  Values are from `ncu --metrics dram__bytes_read.sum,
 # dram__bytes_write.sum` captures of these same bench workloads.
 NCU_TRAFFIC = {
-    ("serving_decode", "attn_decode"): {"bytes": 4614164, "src": "77022dbcfaf0"},
-    ("serving_decode", "index_topk"): {"bytes": 125243, "src": "b1465b204230"},
-    ("serving_decode", "index_score"): {"bytes": 1549154, "src": "df1f5115c7ee"},
-    ("serving_decode", "compress_fused"): {"bytes": 621361, "src": "0587b44655af"},
-    ("million_decode", "index_score"): {"bytes": 143056404, "src": "df1f5115c7ee"},
-    ("million_decode", "attn_decode"): {"bytes": 17839764, "src": "77022dbcfaf0"},
-    ("million_decode", "index_topk"): {"bytes": 8638887, "src": "b1465b204230"},
-    ("million_decode", "compress_fused"): {"bytes": 50225, "src": "0587b44655af"},
-    ("hier_decode", "index_score"): {"bytes": 80700180, "src": "df1f5115c7ee"},
-    ("hier_decode", "index_topk"): {"bytes": 3530171, "src": "b1465b204230"},
-    ("hier_decode", "attn_decode"): {"bytes": 5363865, "src": "77022dbcfaf0"},
-    ("hier_decode", "compress_fused"): {"bytes": 50097, "src": "0587b44655af"},
-    ("lowbit_decode", "attn_decode"): {"bytes": 2074821, "src": "77022dbcfaf0"},
-    ("lowbit_decode", "index_topk"): {"bytes": 124938, "src": "b1465b204230"},
-    ("lowbit_decode", "index_score"): {"bytes": 893922, "src": "df1f5115c7ee"},
-    ("lowbit_decode", "compress_fused"): {"bytes": 621460, "src": "0587b44655af"},
-    ("chunked_prefill", "attn_prefill"): {"bytes": 1058866763, "src": "96ab4a6b48bb"},
-    ("chunked_prefill", "index_score"): {"bytes": 149843403, "src": "df1f5115c7ee"},
-    ("chunked_prefill", "index_topk"): {"bytes": 34518731, "src": "b1465b204230"},
-    ("chunked_prefill", "compress_pool"): {"bytes": 16089925, "src": "0587b44655af"},
-    ("chunked_prefill", "compress_gate"): {"bytes": 5533824, "src": "0587b44655af"},
+    ("serving_decode", "attn_decode"): {"bytes": 4615377, "src": "77022dbcfaf0"},
+    ("serving_decode", "index_topk"): {"bytes": 125156, "src": "b1465b204230"},
+    ("serving_decode", "index_score"): {"bytes": 1553436, "src": "7a13a25375a1"},
+    ("serving_decode", "compress_fused"): {"bytes": 624716, "src": "7a354d1303af"},
+    ("million_decode", "index_score"): {"bytes": 143111623, "src": "7a13a25375a1"},
+    ("million_decode", "attn_decode"): {"bytes": 17843447, "src": "77022dbcfaf0"},
+    ("million_decode", "index_topk"): {"bytes": 8640664, "src": "b1465b204230"},
+    ("million_decode", "compress_fused"): {"bytes": 53570, "src": "7a354d1303af"},
+    ("hier_decode", "index_score"): {"bytes": 80713183, "src": "7a13a25375a1"},
+    ("hier_decode", "index_topk"): {"bytes": 3529646, "src": "b1465b204230"},
+    ("hier_decode", "attn_decode"): {"bytes": 5364622, "src": "77022dbcfaf0"},
+    ("hier_decode", "compress_fused"): {"bytes": 53447, "src": "7a354d1303af"},
+    ("lowbit_decode", "attn_decode"): {"bytes": 2073183, "src": "77022dbcfaf0"},
+    ("lowbit_decode", "index_topk"): {"bytes": 125175, "src": "b1465b204230"},
+    ("lowbit_decode", "index_score"): {"bytes": 897982, "src": "7a13a25375a1"},
+    ("lowbit_decode", "compress_fused"): {"bytes": 624488, "src": "7a354d1303af"},
+    ("lowbit_million", "index_score"): {"bytes": 72217012, "src": "7a13a25375a1"},
+    ("lowbit_million", "attn_decode"): {"bytes": 7185209, "src": "77022dbcfaf0"},
+    ("lowbit_million", "index_topk"): {"bytes": 8639308, "src": "b1465b204230"},
+    ("lowbit_million", "compress_fused"): {"bytes": 53817, "src": "7a354d1303af"},
+    ("chunked_prefill", "attn_prefill"): {"bytes": 1058863524, "src": "96ab4a6b48bb"},
+    ("chunked_prefill", "index_score"): {"bytes": 148996628, "src": "7a13a25375a1"},
+    ("chunked_prefill", "index_topk"): {"bytes": 34523453, "src": "b1465b204230"},
+    ("chunked_prefill", "compress_pool"): {"bytes": 16092078, "src": "7a354d1303af"},
+    ("chunked_prefill", "compress_gate"): {"bytes": 5534776, "src": "7a354d1303af"},
 }
 
 
