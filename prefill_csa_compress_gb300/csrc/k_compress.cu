@@ -11,6 +11,8 @@
 
 #include <cstring>
 
+#include <algorithm>
+
 #include "csa_internal.cuh"
 #include "lowbit.cuh"
 #include "tc.cuh"
@@ -381,6 +383,156 @@ __global__ void compress_pool_kernel(csa_compress_args a, const float *__restric
   }
 }
 
+// Long groups (HCA's ratio 128) without a row-wide statistic (no RMSNorm, no
+// INT8 amax): one CTA per (group-closing row, 64-channel slice), 8 token
+// lanes per channel.  Lane j takes tokens j, j + 8, ... of the group (their
+// ring or chunk loads all in flight), keeps an online softmax of its share,
+// and the 8 partial (max, sum, weighted sum) merge in shared memory; lanes 0
+// then round, rotate and publish their 64 channels exactly as the per-row
+// kernel does.  The per-row kernel walks the r tokens with one thread per
+// channel, 8 tokens per round trip: 16 round trips for a 128-token group.
+constexpr int WP_CH = 64, WP_LANES = 8, WP_THREADS = WP_CH * WP_LANES;
+constexpr int WP_TOK = 16;  // tokens per lane held in flight (ratio <= WP_LANES * WP_TOK)
+
+__global__ void __launch_bounds__(WP_THREADS)
+    compress_pool_wide_kernel(csa_compress_args a, const float *__restrict__ logits) {
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
+  __shared__ float pm[WP_LANES][WP_CH], ps[WP_LANES][WP_CH], py[WP_LANES][WP_CH];
+  __shared__ float ys[WP_CH];
+  __shared__ uint8_t in_chunk[kMaxRatio];
+  __shared__ int s_complete;
+  const int slice = blockIdx.y;
+  const int r = a.ratio, D = a.d;
+  const int c = threadIdx.x % WP_CH, lane = threadIdx.x / WP_CH, d = slice * WP_CH + c;
+  const uint16_t *kv = static_cast<const uint16_t *>(a.kv);
+  // rows in a grid stride (a short chunk: at most one row per CTA)
+  for (int t = blockIdx.x; t < a.n_rows; t += gridDim.x) {
+    const int b = a.row_req[t], p = a.positions[t];
+    if (b < 0 || p < 0 || (p % r) != r - 1) continue;  // uniform over the CTA
+    if (b >= a.n_req) {
+      if (threadIdx.x == 0 && slice == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
+      continue;
+    }
+    const float *ring = nullptr;
+    if (a.state_cache) {
+      const int blk = a.state_block_table[b];
+      if (blk < 0) continue;
+      if (blk >= a.n_state_blocks) {
+        if (threadIdx.x == 0 && slice == 0) flag(a.status_dev, CSA_DEV_BAD_BLOCK);
+        continue;
+      }
+      ring = a.state_cache + (long long)blk * a.state_capacity * 2 * D;
+    }
+    __syncthreads();  // the previous row's shared state is no longer read
+    if (threadIdx.x == 0) s_complete = 1;
+    __syncthreads();
+    for (int j = threadIdx.x; j < r; j += blockDim.x) {
+      const int s = t - r + 1 + j;
+      const bool here = s >= 0 && a.row_req[s] == b && a.positions[s] == p - r + 1 + j;
+      in_chunk[j] = here;
+      if (!here && !ring) s_complete = 0;
+    }
+    __syncthreads();
+    if (!s_complete) continue;
+    const int g = p / r, page = g / kBlock;
+    int phys = -1;
+    if (page < a.max_blocks) phys = a.block_table[(long long)b * a.max_blocks + page];
+    if (phys < 0 || phys >= a.n_blocks) {
+      if (threadIdx.x == 0 && slice == 0) flag(a.status_dev, CSA_DEV_BAD_BLOCK);
+      continue;
+    }
+    const long long dst_row = (long long)phys * kBlock + (g % kBlock);
+    const int t0 = t - r + 1;
+    float lg[WP_TOK], v[WP_TOK];
+#pragma unroll
+    for (int i = 0; i < WP_TOK; ++i) {
+      const int j = lane + WP_LANES * i;
+      lg[i] = -INFINITY;
+      v[i] = 0.f;
+      if (j < r) {
+        if (in_chunk[j]) {
+          lg[i] = logits[(long long)(t0 + j) * D + d] + a.ape[j * D + d];
+          v[i] = bf16_bits_to_float(kv[(long long)(t0 + j) * D + d]);
+        } else {
+          const float *slot = ring + (long long)((p - r + 1 + j) % a.state_capacity) * 2 * D;
+          v[i] = slot[d];
+          lg[i] = slot[D + d];
+        }
+      }
+    }
+    float mx = lg[0];
+#pragma unroll
+    for (int i = 1; i < WP_TOK; ++i) mx = fmaxf(mx, lg[i]);
+    float sum = 0.f, y = 0.f;
+#pragma unroll
+    for (int i = 0; i < WP_TOK; ++i) {
+      const float e = lg[i] == -INFINITY ? 0.f : expf(lg[i] - mx);
+      sum += e;
+      y = fmaf(e, v[i], y);
+    }
+    pm[lane][c] = mx;
+    ps[lane][c] = sum;
+    py[lane][c] = y;
+    __syncthreads();
+    if (lane == 0) {  // threads 0 .. 63: two full warps, channels in order
+      float m = -INFINITY;
+#pragma unroll
+      for (int l = 0; l < WP_LANES; ++l) m = fmaxf(m, pm[l][c]);
+      float S = 0.f, Y = 0.f;
+#pragma unroll
+      for (int l = 0; l < WP_LANES; ++l) {
+        const float f = pm[l][c] == -INFINITY ? 0.f : expf(pm[l][c] - m);
+        S = fmaf(ps[l][c], f, S);
+        Y = fmaf(py[l][c], f, Y);
+      }
+      y = round_bf16(Y / S);
+      if (a.rotate) {
+        const int pos = g * r;
+        ys[c] = y;
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+        if (pos >= a.rope_cap) {
+          if (c == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
+        } else if (d >= D - kRopeDim) {
+          const int i = (d - (D - kRopeDim)) >> 1;
+          const float cs = a.rope_cos[(long long)pos * kRopeHalf + i];
+          const float sn = a.rope_sin[(long long)pos * kRopeHalf + i];
+          y = (d & 1) == 0 ? ys[c] * cs - ys[c + 1] * sn : ys[c - 1] * sn + ys[c] * cs;
+        }
+      }
+      if (a.out_mode == CSA_OUT_BF16)
+        static_cast<__nv_bfloat16 *>(a.cmp_pool)[dst_row * D + d] = __float2bfloat16_rn(y);
+      else if (a.out_mode == CSA_OUT_FP4_E4M3)
+        publish_fp4<16>(a, dst_row, d, y, true);
+      else if (a.out_mode == CSA_OUT_FP4_E8M0)
+        publish_fp4<32>(a, dst_row, d, y, true);
+      else
+        publish_mxfp8(a, dst_row, d, y, true);
+    }
+  }
+}
+
+int device_sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// Short chunks only: a long chunk's grid would be mostly rows that close no
+// group (measured: the per-row kernel is faster there, its idle CTAs cheaper
+// than the wide kernel's row scan).
+bool pool_wide(const csa_compress_args &a) {
+  return a.n_rows <= 256 && a.ratio > 16 && a.ratio <= WP_LANES * WP_TOK && !a.gamma &&
+         a.out_mode != CSA_OUT_INT8 && a.d % WP_CH == 0;
+}
+
 // Ring writes of the state: row t among the last state_capacity rows of its
 // request's chunk stores its kv row (FP32) and its gate score (ape included)
 // in slot p % state_capacity.  Runs after the pooling kernel, so every ring
@@ -717,8 +869,13 @@ cudaError_t launch_compress(const csa_compress_args &a, float *logits, cudaStrea
   launch_end(CSA_K_COMPRESS_GATE, s);
   if (e != cudaSuccess) return e;
   launch_begin(CSA_K_COMPRESS_POOL, s);
-  e = launch_kernel(compress_pool_kernel, dim3(a.n_rows), dim3(a.d), 0, s, 0, false, a,
-                    static_cast<const float *>(logits));
+  if (pool_wide(a))
+    e = launch_kernel(compress_pool_wide_kernel, dim3(std::min(a.n_rows, 2 * device_sm_count()),
+                                                      a.d / WP_CH),
+                      dim3(WP_THREADS), 0, s, 0, false, a, static_cast<const float *>(logits));
+  else
+    e = launch_kernel(compress_pool_kernel, dim3(a.n_rows), dim3(a.d), 0, s, 0, false, a,
+                      static_cast<const float *>(logits));
   launch_end(CSA_K_COMPRESS_POOL, s);
   if (e == cudaSuccess && a.state_cache) {
     launch_begin(CSA_K_COMPRESS_POOL, s);
