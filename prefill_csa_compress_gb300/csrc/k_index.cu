@@ -182,6 +182,12 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
   __shared__ int warp_sums[32];
   __shared__ int s_digit, s_above, s_ok;
   __shared__ int s_gt_before, s_eq_before;
+  // the first digit's per-warp histograms are cleared while the previous
+  // kernel finishes (shared memory only)
+  {
+    uint4 *p4 = reinterpret_cast<uint4 *>(priv);
+    for (int i = threadIdx.x; i < NW * TK_B1 / 4; i += NT) p4[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
   tc::griddep_wait();
   tc::griddep_launch_dependents();
   const int t = row0 + blockIdx.y, s = blockIdx.x, tid = threadIdx.x, warp = tid >> 5;
@@ -242,12 +248,8 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
   for (int j = 0; j < 3; ++j) {  // digit j: nb bins at `shift`
     const int nb = j == 2 ? TK_B3 : TK_B1;
     const int shift = j == 0 ? 21 : (j == 1 ? 10 : 0);
-    if (j == 0) {
-      uint4 *p4 = reinterpret_cast<uint4 *>(priv);
-      for (int i = tid; i < NW * TK_B1 / 4; i += NT) p4[i] = make_uint4(0u, 0u, 0u, 0u);
-    } else {
+    if (j > 0)
       for (int i = tid; i < nb; i += NT) hist[i] = 0u;
-    }
     if (MULTI && j == 2) {
       // keys above the 22-bit prefix, for the offsets of later slices
       int c = 0;

@@ -186,10 +186,29 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   float *Ws = reinterpret_cast<float *>(sm + C::OFF_W);
   float *Rope = reinterpret_cast<float *>(sm + C::OFF_ROPE);
   IdxMisc *M = reinterpret_cast<IdxMisc *>(sm + C::OFF_MISC);
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+
+  // ---- set-up that touches no global memory, overlapping the previous kernel
+  if (tid == 0) {
+    for (int s = 0; s < C::NS; ++s) {
+      tc::mbar_init(&M->st_full[s], 1);
+      tc::mbar_init(&M->st_empty[s], IT_CONV);
+    }
+    for (int j = 0; j < C::NA; ++j) {
+      tc::mbar_init(&M->a_full[j], IT_CONV);
+      tc::mbar_init(&M->a_free[j], 1);
+    }
+    for (int j = 0; j < C::NT; ++j) {
+      tc::mbar_init(&M->acc_full[j], 1);
+      tc::mbar_init(&M->acc_empty[j], IT_EPI);
+    }
+    M->abort = 0;
+    tc::mbar_fence_init();
+  }
+  if (warp == W_MMA) tc::tmem_alloc(&M->tmem_base, C::TMEM_COLS);
   tc::griddep_wait();
   tc::griddep_launch_dependents();
 
-  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const long long n_words = (long long)a.n_rows * kTopkCtlWords;
   for (int z = 0; z < 2; ++z) {
     uint32_t *ctr = z == 0 ? zero_ctr : sel.zero2;
@@ -213,23 +232,6 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   const int n_kchunks = rope ? 3 : 2;
   const int n_cap = a.max_blocks * kBlock;
 
-  if (tid == 0) {
-    for (int s = 0; s < C::NS; ++s) {
-      tc::mbar_init(&M->st_full[s], 1);
-      tc::mbar_init(&M->st_empty[s], IT_CONV);
-    }
-    for (int j = 0; j < C::NA; ++j) {
-      tc::mbar_init(&M->a_full[j], IT_CONV);
-      tc::mbar_init(&M->a_free[j], 1);
-    }
-    for (int j = 0; j < C::NT; ++j) {
-      tc::mbar_init(&M->acc_full[j], 1);
-      tc::mbar_init(&M->acc_empty[j], IT_EPI);
-    }
-    M->abort = 0;
-    tc::mbar_fence_init();
-  }
-  if (warp == W_MMA) tc::tmem_alloc(&M->tmem_base, C::TMEM_COLS);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
