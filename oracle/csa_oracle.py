@@ -359,8 +359,14 @@ def page_rows(pool, table_row, logical):
 
 
 def compress(x, kv, w_gate, ape, ratio, positions, row_req, gamma=None, rms_eps=1e-6,
-             rotate=False, rope_cos=None, rope_sin=None, rope_dim=64, out="bf16"):
+             rotate=False, rope_cos=None, rope_sin=None, rope_dim=64, out="bf16", overlap=False):
     """Gated compression of every complete group of ``ratio`` rows.
+
+    ``overlap`` (the ratio-4 overlapping compressor, "Hyper-Parallel ...
+    DeepSeek V4 CP", "ratio=4": a group needs the ratio tokens before it, a
+    shard's first slot is invalid; reading: entry g pools the tokens of group
+    g - 1 and group g, those at positions >= 0, each token's logit taking
+    ape[position % ratio]) widens every group's window to 2 * ratio tokens.
 
     A group g of request b is the positions g*r .. g*r + r - 1; it is complete
     in this chunk when rows t-r+1 .. t all belong to b at those consecutive
@@ -394,13 +400,17 @@ def compress(x, kv, w_gate, ape, ratio, positions, row_req, gamma=None, rms_eps=
     results = []
     for t in range(len(positions)):
         b, p = int(row_req[t]), int(positions[t])
-        if b < 0 or p < 0 or p % r != r - 1 or t < r - 1:
+        if b < 0 or p < 0 or p % r != r - 1:
             continue
-        rows = [t - r + 1 + j for j in range(r)]
-        if any(int(row_req[s]) != b or int(positions[s]) != p - r + 1 + j
+        n = min(p + 1, 2 * r) if overlap else r  # the group's window of tokens
+        if t < n - 1:
+            continue
+        rows = [t - n + 1 + j for j in range(n)]
+        if any(int(row_req[s]) != b or int(positions[s]) != p - n + 1 + j
                for j, s in enumerate(rows)):
             continue
-        logits = x[rows] @ w_gate + ape[:r]  # [r, D]
+        pos = np.array([p - n + 1 + j for j in range(n)])
+        logits = x[rows] @ w_gate + ape[pos % r]  # [n, D]
         results.append(_publish_group(b, p // r, r, logits, kv[rows], gamma, rms_eps, rotate,
                                       rope_cos, rope_sin, rope_dim, out))
     return results
@@ -435,7 +445,7 @@ def _publish_group(b, g, r, logits, kvs, gamma, rms_eps, rotate, rope_cos, rope_
 
 def compress_stateful(x, kv, w_gate, ape, ratio, positions, row_req, state, state_table,
                       gamma=None, rms_eps=1e-6, rotate=False, rope_cos=None, rope_sin=None,
-                      rope_dim=64, out="bf16"):
+                      rope_dim=64, out="bf16", overlap=False):
     """One chunk of the compressor with its recurrent state ring ("DeepSeek
     V4.1 Flash", "Compressor state ownership").
 
@@ -449,12 +459,14 @@ def compress_stateful(x, kv, w_gate, ape, ratio, positions, row_req, state, stat
     min(chunk length, cap) tokens of each request's chunk write their slots.
     ``state_table[b] < 0`` disables request b (nothing published or written);
     negative positions neither publish nor write.  Returns the published
-    groups as compress() does.
+    groups as compress() does; ``overlap`` widens the windows as there (the
+    ring then needs at least 2 * ratio slots).
     """
     x, kv, w_gate, ape = as_f64(x), as_f64(kv), as_f64(w_gate), as_f64(ape)
     positions = as_f64(positions).astype(np.int64)
     row_req = as_f64(row_req).astype(np.int64)
     table = as_f64(state_table).astype(np.int64)
+    assert not overlap or state.shape[1] >= 2 * int(ratio)
     r, D, cap = int(ratio), kv.shape[1], state.shape[1]
     T = len(positions)
 
@@ -472,7 +484,8 @@ def compress_stateful(x, kv, w_gate, ape, ratio, positions, row_req, state, stat
             continue
         blk = int(table[b])
         logits, kvs = [], []
-        for j in range(r - 1, -1, -1):  # positions p - j, oldest first
+        n = min(p + 1, 2 * r) if overlap else r
+        for j in range(n - 1, -1, -1):  # positions p - j, oldest first
             s_ = t - j
             if s_ >= 0 and int(row_req[s_]) == b and int(positions[s_]) == p - j:
                 logits.append(score[s_])

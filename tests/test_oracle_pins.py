@@ -342,6 +342,93 @@ def test_stateful_compress_int8_rotated_equals_one_shot():
     assert [(g, c.tolist(), sc) for _, g, c, sc in got] == [(g, c.tolist(), sc) for _, g, c, sc in want]
 
 
+# Overlapping ratio-4 compression ("Hyper-Parallel ... DeepSeek V4 CP",
+# "ratio=4" halo: a group needs the ratio tokens before it; reading: entry g
+# pools groups g - 1 and g, each token's logit taking ape[position % ratio]).
+
+
+def test_overlap_equal_logits_give_the_two_group_mean():
+    rng = np.random.default_rng(48)
+    x, kv = _chunk(rng, 12)
+    w = torch.zeros((64, 64), dtype=torch.bfloat16)
+    res = O.compress(x, kv, w, np.zeros((4, 64)), 4, np.arange(12), np.zeros(12, int),
+                     overlap=True)
+    assert [g for _, g, _ in res] == [0, 1, 2]
+    for _, g, y in res:
+        lo = max(0, 4 * g - 4)  # entry 0 has no previous group
+        mean = kv[lo:4 * g + 4].double().numpy().mean(axis=0)
+        assert np.all(np.abs(y - mean) <= 2.0 ** -8 * np.abs(mean) * (1 + 1e-12))
+
+
+def test_overlap_one_hot_ape_picks_that_token_of_both_groups():
+    rng = np.random.default_rng(49)
+    x, kv = _chunk(rng, 12)
+    w = torch.zeros((64, 64), dtype=torch.bfloat16)
+    ape = np.zeros((4, 64))
+    ape[1] = 1e4  # positions 1, 5, 9: one in each group, equal logits
+    res = O.compress(x, kv, w, ape, 4, np.arange(12), np.zeros(12, int), overlap=True)
+    k = kv.double().numpy()
+    (_, _, y0), (_, _, y1), (_, _, y2) = res
+    assert np.array_equal(y0, k[1])
+    for y, (a, b) in ((y1, (1, 5)), (y2, (5, 9))):
+        two = _bf16(0.5 * (k[a] + k[b])).double().numpy()
+        assert np.array_equal(y, two)
+
+
+def test_overlap_odd_entries_are_the_double_ratio_groups():
+    """Entry 2k + 1 of the overlapping ratio-r compressor pools positions
+    2rk .. 2rk + 2r - 1, the k-th group of the plain ratio-2r compressor
+    whose APE repeats the ratio-r rows twice."""
+    rng = np.random.default_rng(50)
+    x, kv = _chunk(rng, 27, D=64, Dx=32)
+    w = _bf16(rng.standard_normal((32, 64)) / 6)
+    ape = rng.standard_normal((4, 64))
+    ov = O.compress(x, kv, w, ape, 4, np.arange(27), np.zeros(27, int), overlap=True)
+    assert [g for _, g, _ in ov] == list(range(6))
+    wide = O.compress(x, kv, w, np.concatenate([ape, ape]), 8, np.arange(27), np.zeros(27, int))
+    assert [g for _, g, _ in wide] == [0, 1, 2]
+    for _, k, y in wide:
+        assert np.array_equal(ov[2 * k + 1][2], y)
+
+
+def test_overlap_needs_the_whole_window_in_the_chunk():
+    """One-shot calls publish an entry only when its whole window (the
+    previous group too) is in the chunk as the same request's rows."""
+    rng = np.random.default_rng(51)
+    x, kv = _chunk(rng, 10)
+    w = torch.zeros((64, 64), dtype=torch.bfloat16)
+    got = O.compress(x, kv, w, np.zeros((2, 64)), 2, np.arange(8, 18), np.zeros(10, int),
+                     overlap=True)
+    assert [g for _, g, _ in got] == [5, 6, 7, 8]  # entry 4 lacks positions 6, 7
+
+
+@pytest.mark.parametrize("r,splits", [
+    (4, [[1, 1]] * 13),                        # decode: every window reaches back one group
+    (4, [[2, 3], [7, 1], [1, 6], [3, 2]]),     # chunk starts inside groups
+    (2, [[3, 2], [1, 4], [5, 1], [2, 2]]),
+    (4, [[6, 0], [0, 5], [5, 6]]),             # idle requests in some calls
+])
+def test_stateful_overlap_equals_one_shot(r, splits):
+    rng = np.random.default_rng(52 + r)
+    lens = [sum(c[b] for c in splits) for b in range(2)]
+    n = sum(lens)
+    x, kv = _chunk(rng, n, D=64, Dx=32)
+    w = _bf16(rng.standard_normal((32, 64)) / 6)
+    ape = rng.standard_normal((r, 64))
+    reqs = [list(range(0, lens[0])), list(range(lens[0], n))]
+    got, _, _ = _stateful_run(x, kv, w, ape, r, reqs, splits, cap=2 * r, overlap=True)
+    want = []
+    for b in range(2):
+        idx = np.array(reqs[b])
+        for _, g, y in O.compress(x[idx], kv[idx], w, ape, r, np.arange(len(idx)),
+                                  np.zeros(len(idx), int), overlap=True):
+            want.append((b, g, y))
+    assert sorted((b, g) for b, g, _ in got) == sorted((b, g) for b, g, _ in want)
+    ref = {(b, g): y for b, g, y in want}
+    for b, g, y in got:
+        assert np.array_equal(y, ref[(b, g)]), (b, g)
+
+
 def test_state_ring_holds_the_last_tokens():
     """After a call, slot p % cap of the request's block holds the kv row and
     the gate score of the last min(chunk length, cap) positions; older slots
