@@ -111,8 +111,8 @@ def _peaks():
 
 
 def algorithmic_work(wl):
-    """Per-kernel algorithmic bytes and FLOPs of one step (see the design doc,
-    "Measurement"), from the workload's shapes only."""
+    """Per-kernel algorithmic bytes and FLOPs of one step: each distinct byte
+    a kernel must read or write once, from the workload's shapes only."""
     s = wl.spec
     T = s.n_rows
     rows = [(int(wl.row_req[i]), int(wl.row_pos[i])) for i in range(T)]
@@ -165,15 +165,18 @@ def algorithmic_work(wl):
     def in_chunk(i, j):  # row i - j is the same request at position p_i - j
         return i - j >= 0 and rr[i - j] == rr[i] and rp[i - j] == rp[i] - j
     closing = [i for i in range(T) if rr[i] >= 0 and rp[i] >= 0 and rp[i] % r == r - 1]
+    # tokens a closing row pools: its group, or with overlap the previous group too
+    span = {i: min(rp[i] + 1, 2 * r) if s.overlap else r for i in closing}
     if s.state:
         # with state rings every closing row publishes; predecessors before the
-        # chunk come from the ring and the last 4 rows of each request write it
+        # chunk come from the ring and the last `cap` rows of each request write it
+        cap = max(4, r) * (2 if s.overlap else 1)
         groups = len(closing)
-        ring_reads = sum(1 for i in closing for j in range(1, r) if not in_chunk(i, j))
+        ring_reads = sum(1 for i in closing for j in range(1, span[i]) if not in_chunk(i, j))
         ring_writes = sum(1 for i in range(T) if rr[i] >= 0 and rp[i] >= 0 and
-                          not (i + 4 < T and rr[i + 4] == rr[i]))
+                          not (i + cap < T and rr[i + cap] == rr[i]))
     else:
-        groups = sum(1 for i in closing if all(in_chunk(i, j) for j in range(1, r)))
+        groups = sum(1 for i in closing if all(in_chunk(i, j) for j in range(1, span[i])))
         ring_reads = ring_writes = 0
     # (d, output bytes per group); HCA (dense) runs only the main compressor
     dims = ((D, cmp_b),) if s.dense else ((D, cmp_b), (Di, key_b))
@@ -429,12 +432,12 @@ def run_gpu(args, wl, rank, world, local_rank):
             from workloads import reindex_view
 
             s1 = CsaStep(t, s.ratio, s.topk, prefill=prefill, n_cand=s.n_cand,
-                         cand_block=s.cand_block)
+                         cand_block=s.cand_block, overlap=s.overlap)
             s2 = CsaStep(reindex_view(t), s.ratio, s.topk, prefill=prefill, compress=False,
                          cand_in=s1.cand, cand_block=s.cand_block, status_buf=s1.status)
             st = StepChain([s1, s2])
         else:
-            st = CsaStep(t, s.ratio, s.topk, prefill=prefill, dense=s.dense)
+            st = CsaStep(t, s.ratio, s.topk, prefill=prefill, dense=s.dense, overlap=s.overlap)
         if io is not None:
             io.bind_outputs(st)
         return st.prepare()

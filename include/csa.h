@@ -160,6 +160,18 @@ typedef enum { CSA_MODE_AUTO = 0, CSA_MODE_DECODE = 1, CSA_MODE_PREFILL = 2 } cs
  * cmp_pool as uint8 [n_blocks, 128, d / 2] (FP4) or [n_blocks, 128, d]
  * (MXFP8) and scale bytes to scale_pool.  Needs a struct_size that covers
  * scale_pool.
+ *
+ * Overlapping compression (overlap = 1; "Hyper-Parallel ... DeepSeek V4
+ * CP", "6.1 ratio4 CSA: compressor halo": the ratio-4 compressor overlaps,
+ * a group needing the ratio tokens before it, so the first shard's first
+ * slot is padding).
+ * Entry g pools the window of the n = min(g*r + r, 2r) tokens ending at
+ * g*r + r - 1 -- the tokens of groups g-1 and g, entry 0 only its own --
+ * with the same per-channel softmax, token q's logit being
+ * x_q . w_gate[:,d] + ape[q % ratio, d].  Without a ring the whole window
+ * must be this chunk's rows of request b at those positions; with a ring,
+ * state_capacity >= 2 * ratio.  Supported for ratio <= 64 (else
+ * CSA_ERR_UNSUPPORTED).  A struct_size that ends before `overlap` means 0.
  * ---------------------------------------------------------------------- */
 typedef struct {
   uint32_t struct_size;
@@ -195,6 +207,7 @@ typedef struct {
   int32_t n_state_blocks;
   int32_t state_capacity;
   uint8_t *scale_pool; /* FP4 out modes: scale bytes [n_blocks, 128, d / group] */
+  int32_t overlap;     /* 1: each entry pools the previous group too (see above) */
 } csa_compress_args;
 
 CSA_API csa_status_t csa_compress(csa_compress_args *args, csa_stream_t stream);

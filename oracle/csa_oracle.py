@@ -27,11 +27,14 @@ straight from the pages:
   publication, dequantised on reads).  The rounding rules of the two FP4
   publications are readings (the pages give only the formats).
 
-Readings taken where the pages are silent (each also listed in the design doc):
-ReLU per index head; the index-key scale applied after the head sum; the
-gate input x of the compressor is a separate [rows, Dx] operand (the
-workloads pass the raw KV rows); the sink is already a logit; lse includes
-the sink; RMSNorm optional; RoPE uses the last ``rope_dim`` dims.
+Readings taken where the pages are silent: ReLU per index head; the
+index-key scale applied after the head sum; the gate input x of the
+compressor is a separate [rows, Dx] operand (the workloads pass the raw KV
+rows); the sink is already a logit; lse includes the sink; RMSNorm
+optional; RoPE uses the last ``rope_dim`` dims; the overlapping ratio-4
+compressor ("Hyper-Parallel ... DeepSeek V4 CP", "6.1 ratio4 CSA:
+compressor halo") pools groups g - 1 and g into entry g, token q's logit
+taking ape[q % ratio].
 
 Parity pins live in ``tests/test_oracle_pins.py``.  Functions without an
 independent pin: none (every function below has at least one).
@@ -363,10 +366,11 @@ def compress(x, kv, w_gate, ape, ratio, positions, row_req, gamma=None, rms_eps=
     """Gated compression of every complete group of ``ratio`` rows.
 
     ``overlap`` (the ratio-4 overlapping compressor, "Hyper-Parallel ...
-    DeepSeek V4 CP", "ratio=4": a group needs the ratio tokens before it, a
-    shard's first slot is invalid; reading: entry g pools the tokens of group
-    g - 1 and group g, those at positions >= 0, each token's logit taking
-    ape[position % ratio]) widens every group's window to 2 * ratio tokens.
+    DeepSeek V4 CP", "6.1 ratio4 CSA: compressor halo": a group needs the
+    ratio tokens before it, a shard's first slot is invalid; reading: entry
+    g pools the tokens of group g - 1 and group g, those at positions >= 0,
+    each token's logit taking ape[position % ratio]) widens every group's
+    window to 2 * ratio tokens.
 
     A group g of request b is the positions g*r .. g*r + r - 1; it is complete
     in this chunk when rows t-r+1 .. t all belong to b at those consecutive

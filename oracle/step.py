@@ -51,15 +51,16 @@ def compress_step(t, spec, pools=None):
     Returns (pools, main_results, idx_results)."""
     pools = clone_pools(t) if pools is None else pools
     lowbit = _lowbit(t)
+    ov = bool(getattr(spec, "overlap", False))
     idx_kw = dict(rotate=True, rope_cos=t["rope_cos"], rope_sin=t["rope_sin"],
-                  rope_dim=spec.rope_dim, out=_key_fmt(t) if lowbit else "int8")
+                  rope_dim=spec.rope_dim, out=_key_fmt(t) if lowbit else "int8", overlap=ov)
     main_out = "fp4_e4m3" if lowbit else "bf16"
     if spec.state:
         pools["state_main"] = O.as_f64(t["state_main"]).copy()
         table = t["state_table"].numpy()
         main = O.compress_stateful(t["kv_raw"], t["kv_raw"], t["w_gate"], t["ape"], spec.ratio,
                                    t["row_pos"], t["row_req"], pools["state_main"], table,
-                                   out=main_out)
+                                   out=main_out, overlap=ov)
         idx = []
         if not spec.dense:  # HCA has no indexer, hence no index-key compressor
             pools["state_idx"] = O.as_f64(t["state_idx"]).copy()
@@ -68,7 +69,7 @@ def compress_step(t, spec, pools=None):
                                       table, **idx_kw)
     else:
         main = O.compress(t["kv_raw"], t["kv_raw"], t["w_gate"], t["ape"], spec.ratio,
-                          t["row_pos"], t["row_req"], out=main_out)
+                          t["row_pos"], t["row_req"], out=main_out, overlap=ov)
         idx = [] if spec.dense else O.compress(t["idx_raw"], t["idx_raw"], t["w_gate_i"],
                                                  t["ape_i"], spec.ratio, t["row_pos"],
                                                  t["row_req"], **idx_kw)

@@ -47,7 +47,7 @@ class CompressArgs(ctypes.Structure):
         ("idx_scale_pool", c_void_p), ("status_dev", c_void_p), ("workspace", c_void_p),
         ("workspace_bytes", c_size_t), ("state_cache", c_void_p),
         ("state_block_table", c_void_p), ("n_state_blocks", c_int32),
-        ("state_capacity", c_int32), ("scale_pool", c_void_p),
+        ("state_capacity", c_int32), ("scale_pool", c_void_p), ("overlap", c_int32),
     ]
 
 
@@ -250,7 +250,7 @@ _OUT_MODES = {"bf16": 0, "int8": 1, "fp4_e4m3": 2, "fp4_e8m0": 3, "mxfp8": 4}
 def _compress_struct(*, x, kv, w_gate, ape, ratio, positions, row_req, block_table, out="bf16",
                      cmp_pool=None, idx_pool=None, idx_scale_pool=None, scale_pool=None,
                      gamma=None, rms_eps=1e-6, rotate=False, rope_cos=None, rope_sin=None,
-                     status=None, state_cache=None, state_block_table=None):
+                     status=None, state_cache=None, state_block_table=None, overlap=False):
     a = CompressArgs()
     a.struct_size = ctypes.sizeof(CompressArgs)
     a.n_rows = int(x.shape[0])
@@ -259,6 +259,7 @@ def _compress_struct(*, x, kv, w_gate, ape, ratio, positions, row_req, block_tab
     a.d = int(kv.shape[1])
     a.out_mode = _OUT_MODES[out]
     a.rotate = 1 if rotate else 0
+    a.overlap = 1 if overlap else 0
     a.x = _p(x, torch.bfloat16, "x")
     a.kv = _p(kv, torch.bfloat16, "kv")
     a.w_gate = _p(w_gate, torch.bfloat16, "w_gate")
@@ -299,7 +300,8 @@ def csa_compress(*, workspace=None, stream=None, prepare=False, **kw):
     "fp4_e8m0"), cmp_pool (bf16; uint8 codes for fp4 with scale_pool) or
     idx_pool + idx_scale_pool, gamma, rms_eps, rotate, rope_cos, rope_sin,
     status, and for the recurrent state ring state_cache (FP32 [blocks,
-    capacity, 2 d]) with state_block_table (INT32 [n_req])."""
+    capacity, 2 d]) with state_block_table (INT32 [n_req]); ``overlap`` pools
+    each entry over the previous group's tokens too."""
     a = _compress_struct(**kw)
     return _run("csa_compress", a, workspace, stream, kw["x"].device, prepare)
 

@@ -195,6 +195,8 @@ static csa_status_t check_compress(csa_compress_args *a, bool *size_query) {
   if (a->ratio != 1 && a->ratio != 2 && a->ratio != 4 && a->ratio != 128)
     return CSA_ERR_UNSUPPORTED;
   if (a->d != 128 && a->d != 512) return CSA_ERR_UNSUPPORTED;
+  if (a->overlap != 0 && a->overlap != 1) return CSA_ERR_INVALID_ARG;
+  if (a->overlap && a->ratio > 64) return CSA_ERR_UNSUPPORTED;
   if (a->dx <= 0 || a->dx % 64 != 0 || a->dx > 1024) return CSA_ERR_UNSUPPORTED;
   if (a->out_mode < CSA_OUT_BF16 || a->out_mode > CSA_OUT_MXFP8) return CSA_ERR_INVALID_ARG;
   const size_t need = align_up((size_t)a->n_rows * a->d * sizeof(float), kAlign);
@@ -219,8 +221,8 @@ static csa_status_t check_compress(csa_compress_args *a, bool *size_query) {
   if (a->rotate && (!a->rope_cos || !a->rope_sin || a->rope_cap <= 0)) return CSA_ERR_INVALID_ARG;
   if (!aligned16(a->x) || !aligned16(a->kv) || !aligned16(a->w_gate)) return CSA_ERR_INVALID_ARG;
   if (a->state_cache &&
-      (!a->state_block_table || a->n_state_blocks <= 0 || a->state_capacity < a->ratio ||
-       a->state_capacity > 256))
+      (!a->state_block_table || a->n_state_blocks <= 0 ||
+       a->state_capacity < (a->overlap ? 2 : 1) * a->ratio || a->state_capacity > 256))
     return CSA_ERR_INVALID_ARG;
   return CSA_OK;
 }

@@ -249,7 +249,10 @@ __device__ __forceinline__ float block_max(float v, float *red) {
 
 // One CTA per group-closing row (d threads, one channel each).  With a state
 // ring, predecessors before the chunk start come from the ring: their kv row
-// and their gate score (ape included) as the ring stores them.
+// and their gate score (ape included) as the ring stores them.  The pooled
+// window is the group's r tokens, or with `overlap` the previous group's too
+// (n = min(p + 1, 2r) tokens ending at p), token q's score taking
+// ape[q % r].
 __global__ void compress_pool_kernel(csa_compress_args a, const float *__restrict__ logits) {
   tc::griddep_wait();
   tc::griddep_launch_dependents();
@@ -273,15 +276,16 @@ __global__ void compress_pool_kernel(csa_compress_args a, const float *__restric
     }
     ring = a.state_cache + (long long)blk * a.state_capacity * 2 * D;
   }
-  // token j of the group (position p - r + 1 + j): row t - r + 1 + j of this
-  // chunk, or (a position before the chunk start) the ring
+  // token j of the window (position p - n + 1 + j): row t - n + 1 + j of
+  // this chunk, or (a position before the chunk start) the ring
+  const int n = a.overlap ? min(p + 1, 2 * r) : r;
   __shared__ uint8_t in_chunk[kMaxRatio];
   __shared__ int s_complete;
   if (threadIdx.x == 0) s_complete = 1;
   __syncthreads();
-  for (int j = threadIdx.x; j < r; j += blockDim.x) {
-    const int s = t - r + 1 + j;
-    const bool here = s >= 0 && a.row_req[s] == b && a.positions[s] == p - r + 1 + j;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const int s = t - n + 1 + j;
+    const bool here = s >= 0 && a.row_req[s] == b && a.positions[s] == p - n + 1 + j;
     in_chunk[j] = here;
     if (!here && !ring) s_complete = 0;
   }
@@ -297,31 +301,31 @@ __global__ void compress_pool_kernel(csa_compress_args a, const float *__restric
   }
   const long long dst_row = (long long)phys * kBlock + (g % kBlock);
   const int d = threadIdx.x;
-  const int t0 = t - r + 1;
+  const int t0 = t - n + 1, q0 = p - n + 1;
   const uint16_t *kv = static_cast<const uint16_t *>(a.kv);
   // gate score and kv value of token j for this channel
   auto token = [&](int j, float &lg, float &v) {
     if (in_chunk[j]) {
-      lg = logits[(long long)(t0 + j) * D + d] + a.ape[j * D + d];
+      lg = logits[(long long)(t0 + j) * D + d] + a.ape[((q0 + j) % r) * D + d];
       v = bf16_bits_to_float(kv[(long long)(t0 + j) * D + d]);
     } else {
-      const float *slot = ring + (long long)((p - r + 1 + j) % a.state_capacity) * 2 * D;
+      const float *slot = ring + (long long)((q0 + j) % a.state_capacity) * 2 * D;
       v = slot[d];
       lg = slot[D + d];
     }
   };
 
-  // pooling softmax over the r tokens of the group, per channel, in one pass
-  // over batches of 8 tokens (their loads in flight together; the running
-  // maximum moves once per batch)
+  // pooling softmax over the n tokens of the window, per channel, in one
+  // pass over batches of 8 tokens (their loads in flight together; the
+  // running maximum moves once per batch)
   float mx = -INFINITY, s = 0.f, y = 0.f;
-  for (int j0 = 0; j0 < r; j0 += 8) {
+  for (int j0 = 0; j0 < n; j0 += 8) {
     float lg[8], v[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       lg[i] = -INFINITY;
       v[i] = 0.f;
-      if (j0 + i < r) token(j0 + i, lg[i], v[i]);
+      if (j0 + i < n) token(j0 + i, lg[i], v[i]);
     }
     float mb = lg[0];
 #pragma unroll
@@ -529,7 +533,7 @@ int device_sm_count() {
 // group (measured: the per-row kernel is faster there, its idle CTAs cheaper
 // than the wide kernel's row scan).
 bool pool_wide(const csa_compress_args &a) {
-  return a.n_rows <= 256 && a.ratio > 16 && a.ratio <= WP_LANES * WP_TOK && !a.gamma &&
+  return a.n_rows <= 256 && !a.overlap && a.ratio > 16 && a.ratio <= WP_LANES * WP_TOK && !a.gamma &&
          a.out_mode != CSA_OUT_INT8 && a.d % WP_CH == 0;
 }
 
@@ -791,7 +795,7 @@ size_t fused_smem(const csa_compress_args &a) {
 
 // the short-chunk column tile for this call, or 0 when it takes the long path
 int fused_cols(const csa_compress_args &a) {
-  if (a.n_rows > 256 || a.state_cache || a.ratio > 4) return 0;
+  if (a.n_rows > 256 || a.state_cache || a.ratio > 4 || a.overlap) return 0;
   if (a.d == 128 && (size_t)a.dx * 128 * 2 <= FC_MAX_W_BYTES) return 128;
   // the 16-column tiles of d = 512 publish BF16 or E4M3-scaled groups of 16
   if (a.d == 512 && (a.out_mode == CSA_OUT_BF16 || a.out_mode == CSA_OUT_FP4_E4M3) && !a.gamma &&

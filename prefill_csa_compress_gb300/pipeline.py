@@ -38,13 +38,16 @@ class CsaStep:
     ``dense`` (HCA) describe the step; ``n_cand`` > 0 makes the indexer also
     select that many candidate blocks of ``cand_block`` positions into
     ``cand`` (level one), and ``cand_in`` restricts it to given candidate
-    blocks (reindex).
+    blocks (reindex).  ``overlap`` makes both compressors pool each entry
+    over the previous group's tokens too (the overlapping ratio-4 layout).
     """
 
     def __init__(self, t: dict, ratio: int, topk: int, prefill: bool = False,
                  compress: bool = True, status: bool = True, dense: bool = False,
-                 n_cand: int = 0, cand_block: int = 8, cand_in=None, status_buf=None):
+                 n_cand: int = 0, cand_block: int = 8, cand_in=None, status_buf=None,
+                 overlap: bool = False):
         self.t = t
+        self.overlap = bool(overlap)
         self.ratio = int(ratio)
         self.topk = int(topk)
         self.prefill = bool(prefill)
@@ -89,6 +92,9 @@ class CsaStep:
                     block_table=t["cmp_table"], out="int8", idx_pool=t["idx_pool"],
                     idx_scale_pool=t["idx_scale"], rotate=True, rope_cos=t["rope_cos"],
                     rope_sin=t["rope_sin"], status=self.status)
+        if self.overlap:
+            main.update(overlap=True)
+            keys.update(overlap=True)
         if "state_table" in t:  # the compressors' recurrent state rings
             main.update(state_cache=t["state_main"], state_block_table=t["state_table"])
             keys.update(state_cache=t["state_idx"], state_block_table=t["state_table"])

@@ -116,6 +116,24 @@ def test_workspace_queries_and_validation(L):
     assert old.workspace_bytes == 8192 * 512 * 4
     old.struct_size = b.CompressArgs.state_cache.offset - 8
     assert L.csa_compress(ctypes.byref(old), None) == b.CSA_ERR_INVALID_ARG
+    # overlap: 0 or 1, ratio <= 64; a struct that ends before `overlap` means 0
+    assert L.csa_compress(ctypes.byref(_compress_args(b, overlap=1)), None) == b.CSA_OK
+    assert L.csa_compress(ctypes.byref(_compress_args(b, overlap=2)),
+                          None) == b.CSA_ERR_INVALID_ARG
+    assert L.csa_compress(ctypes.byref(_compress_args(b, overlap=1, ratio=128)),
+                          None) == b.CSA_ERR_UNSUPPORTED
+    short = _compress_args(b, overlap=1, ratio=128)
+    short.struct_size = b.CompressArgs.overlap.offset
+    assert L.csa_compress(ctypes.byref(short), None) == b.CSA_OK
+    # with overlap the ring needs 2 * ratio slots: checked before any launch
+    buf = ctypes.create_string_buffer(1 << 16)
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    ptrs = dict(x=base, kv=base, w_gate=base, ape=base, positions=base, row_req=base,
+                block_table=base, cmp_pool=base, n_req=1, max_blocks=1, n_blocks=1,
+                workspace=base, workspace_bytes=1 << 14, state_cache=base,
+                state_block_table=base, n_state_blocks=1)
+    ring = _compress_args(b, n_rows=1, overlap=1, state_capacity=4, **ptrs)
+    assert L.csa_compress(ctypes.byref(ring), None) == b.CSA_ERR_INVALID_ARG
     # a state ring needs its table and at least `ratio` slots
     st = ctypes.create_string_buffer(4096)
     ring = _compress_args(b, n_rows=1, workspace=ctypes.addressof(dummy), workspace_bytes=256,

@@ -285,13 +285,14 @@ def test_lowbit_prefill_attention(over):
     ("lowbit_million", {}),
     ("lowbit_prefill", dict(ctx=[1500], chunk=[1500], seed=96)),   # FP4 publication of 375 groups
     ("lowbit_decode", dict(key_fmt="mxfp8", seed=99)),               # FP8 index keys
+    ("lowbit_prefill", dict(ctx=[1500], chunk=[1500], seed=100, overlap=True)),
 ])
 def test_lowbit_step_chain(name, over):
     """compress (FP4 publication) -> FP4 indexer -> low-bit attention, against
     the oracle's chain on the same inputs."""
     spec = spec_for(name, **over)
     wl, t = _load(spec)
-    step = CsaStep(t, spec.ratio, spec.topk, prefill=spec.mode == "prefill")
+    step = CsaStep(t, spec.ratio, spec.topk, prefill=spec.mode == "prefill", overlap=spec.overlap)
     step.run()
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0

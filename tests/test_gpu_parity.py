@@ -63,11 +63,20 @@ def _rope_q(t, row, key="q_idx"):
     ("hca_prefill", dict(ctx=[700], chunk=[700], seed=61)),             # ratio 128, ragged
     ("hca_decode", {}),                                                 # ratio 128 + ring
     ("chunked_prefill", {}),                                            # full 8192-token chunk
+    # overlapping ratio-4 compressors: long chunk, short chunks, chunks that
+    # start inside a request (their first window is incomplete), state rings
+    ("chunked_prefill", dict(ctx=[1000], chunk=[1000], seed=36, overlap=True)),
+    ("chunked_prefill", dict(ctx=[150, 90], chunk=[150, 90], seed=37, overlap=True, pad_rows=2)),
+    ("chunked_prefill", dict(ctx=[900, 500], chunk=[601, 298], seed=38, overlap=True)),
+    ("stateful_decode", dict(overlap=True)),
+    ("stateful_decode", dict(chunk=[37, 6, 3, 1], seed=39, overlap=True)),
+    ("chunked_prefill", dict(overlap=True, seed=40)),                   # full 8192-token chunk
 ])
 def test_compress_parity(name, over):
     spec = spec_for(name, **over)
     wl, t = _load(spec)
-    step = CsaStep(t, spec.ratio, spec.topk, prefill=spec.mode == "prefill", dense=spec.dense)
+    step = CsaStep(t, spec.ratio, spec.topk, prefill=spec.mode == "prefill", dense=spec.dense,
+                   overlap=spec.overlap)
     step.compress()
     torch.cuda.synchronize()
     assert _status(step) == 0
@@ -122,7 +131,25 @@ def test_compress_parity(name, over):
 def test_compress_direct(n_rows, ratio, dx, d, out, with_gamma):
     """csa_compress called directly: x separate from kv, optional RMSNorm,
     rotation at the group start, BF16 or INT8 output."""
-    rng = np.random.default_rng(n_rows * 7 + ratio)
+    _compress_direct(n_rows, ratio, dx, d, out, with_gamma)
+
+
+@pytest.mark.parametrize("n_rows,ratio,dx,d,out,with_gamma", [
+    (12, 4, 512, 512, "bf16", False),    # short chunk: gate rows + pooling kernel
+    (600, 4, 512, 512, "bf16", False),   # long chunk: tensor-core gate GEMM
+    (600, 4, 128, 128, "int8", True),    # rotated INT8 keys with RMSNorm
+    (40, 2, 192, 512, "bf16", True),
+    (9, 1, 128, 128, "bf16", False),
+])
+def test_compress_direct_overlap(n_rows, ratio, dx, d, out, with_gamma):
+    """The overlapping compressor: each entry pools the previous group's
+    tokens too; the chunk's first entries, whose windows start before it,
+    are not published."""
+    _compress_direct(n_rows, ratio, dx, d, out, with_gamma, overlap=True)
+
+
+def _compress_direct(n_rows, ratio, dx, d, out, with_gamma, overlap=False):
+    rng = np.random.default_rng(n_rows * 7 + ratio + (5 if overlap else 0))
     pos0 = 4 * 37 + 1  # the chunk starts mid-group: its first rows form no group
     positions = np.arange(pos0, pos0 + n_rows, dtype=np.int32)
     row_req = np.zeros(n_rows, np.int32)
@@ -145,12 +172,13 @@ def test_compress_direct(n_rows, ratio, dx, d, out, with_gamma):
                      row_req=torch.from_numpy(row_req).to(DEV), block_table=table.to(DEV),
                      out=out, cmp_pool=cmp_pool, idx_pool=idx_pool, idx_scale_pool=idx_scale,
                      gamma=gamma.to(DEV) if gamma is not None else None, rotate=True,
-                     rope_cos=cos.to(DEV), rope_sin=sin.to(DEV), status=status)
+                     rope_cos=cos.to(DEV), rope_sin=sin.to(DEV), status=status, overlap=overlap)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     ref = O.compress(x, kv, w, ape, ratio, positions, row_req, gamma=gamma, rotate=True,
-                     rope_cos=cos, rope_sin=sin, out=out)
-    assert len(ref) == (pos0 + n_rows) // ratio - (pos0 + ratio - 1) // ratio
+                     rope_cos=cos, rope_sin=sin, out=out, overlap=overlap)
+    first = (pos0 + ratio - 1) // ratio + (1 if overlap else 0)  # first entry with its window here
+    assert len(ref) == (pos0 + n_rows) // ratio - first
     got_rows, ref_rows, n_diff = [], [], 0
     for item in ref:
         g = item[1]
@@ -377,17 +405,20 @@ def test_attention_prefill_full_size_sampled():
     _attn_case(spec, 10, True, rows=[0, 1, 127, 128, 2047, 4000, 8191])
 
 
-@pytest.mark.parametrize("ratio,d,out,splits", [
-    (2, 512, "bf16", [[1, 1]] * 6 + [[3, 2], [1, 4], [5, 1]]),   # decode steps, then chunks
-    (4, 512, "bf16", [[1, 1]] * 7 + [[2, 3], [7, 1], [1, 6]]),   # chunks longer than the ring
-    (4, 128, "int8", [[3, 0], [2, 5], [0, 2], [6, 6]]),          # idle requests; rotated INT8
+@pytest.mark.parametrize("ratio,d,out,splits,overlap", [
+    (2, 512, "bf16", [[1, 1]] * 6 + [[3, 2], [1, 4], [5, 1]], False),  # decode, then chunks
+    (4, 512, "bf16", [[1, 1]] * 7 + [[2, 3], [7, 1], [1, 6]], False),  # chunks longer than the ring
+    (4, 128, "int8", [[3, 0], [2, 5], [0, 2], [6, 6]], False),         # idle requests; INT8
+    # overlapping windows reach back into the previous group through the ring
+    (4, 512, "bf16", [[1, 1]] * 9 + [[2, 3], [7, 1], [1, 6], [10, 11]], True),
+    (4, 128, "int8", [[3, 0], [2, 5], [0, 2], [6, 6], [1, 1]], True),
 ])
-def test_compress_state_ring(ratio, d, out, splits):
+def test_compress_state_ring(ratio, d, out, splits, overlap):
     """csa_compress with the recurrent state ring over a chunked stream of two
     requests: the published groups equal the oracle's one-shot compression of
     each request's whole stream, and the ring equals the oracle's ring."""
-    rng = np.random.default_rng(ratio * 100 + d)
-    dx, cap = 256, 4
+    rng = np.random.default_rng(ratio * 100 + d + (7 if overlap else 0))
+    dx, cap = 256, 2 * ratio if overlap else 4
     lens = [sum(c[b] for c in splits) for b in range(2)]
     n = sum(lens)
     x = torch.from_numpy(rng.standard_normal((n, dx)).astype(np.float32)).bfloat16()
@@ -414,7 +445,7 @@ def test_compress_state_ring(ratio, d, out, splits):
             req += [b] * m
             done[b] += m
         idx = np.array(rows)
-        kw = dict(rotate=out == "int8", rope_cos=cos, rope_sin=sin, out=out)
+        kw = dict(rotate=out == "int8", rope_cos=cos, rope_sin=sin, out=out, overlap=overlap)
         O.compress_stateful(x[idx], kv[idx], w, ape, ratio, np.array(pos), np.array(req),
                             ref_state, state_table.numpy(), **kw)
         csa.csa_compress(x=x[idx].to(DEV), kv=kv[idx].to(DEV), w_gate=w.to(DEV), ape=ape.to(DEV),
@@ -423,14 +454,15 @@ def test_compress_state_ring(ratio, d, out, splits):
                          block_table=table.to(DEV), out=out, cmp_pool=cmp_pool, idx_pool=idx_pool,
                          idx_scale_pool=idx_scale, rotate=out == "int8", rope_cos=cos.to(DEV),
                          rope_sin=sin.to(DEV), status=status, state_cache=state,
-                         state_block_table=state_table.to(DEV))
+                         state_block_table=state_table.to(DEV), overlap=overlap)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     got_rows, ref_rows, n_diff, n_groups = [], [], 0, 0
     for b in range(2):
         i = reqs[b]
         ref = O.compress(x[i], kv[i], w, ape, ratio, np.arange(len(i)), np.zeros(len(i), int),
-                         rotate=out == "int8", rope_cos=cos, rope_sin=sin, out=out)
+                         rotate=out == "int8", rope_cos=cos, rope_sin=sin, out=out,
+                         overlap=overlap)
         for item in ref:
             g = item[1]
             pg, row = int(table[b, g // BLOCK]), g % BLOCK
@@ -511,12 +543,13 @@ def test_hca_step(name, over):
     assert np.max(np.abs(gl - rl)) <= LSE_ABS * max(1.0, np.max(np.abs(rl)))
 
 
-@pytest.mark.parametrize("name", ["tiny_decode", "serving_decode", "stateful_decode"])
+@pytest.mark.parametrize("name", ["tiny_decode", "serving_decode", "stateful_decode",
+                                  "overlap_decode"])
 def test_decode_step_chain(name):
     """compress -> index -> attention on the GPU, against the oracle's own chain."""
     spec = spec_for(name)
     wl, t = _load(spec)
-    step = CsaStep(t, spec.ratio, spec.topk)
+    step = CsaStep(t, spec.ratio, spec.topk, overlap=spec.overlap)
     step.run()
     torch.cuda.synchronize()
     assert _status(step) == 0

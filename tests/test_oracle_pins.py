@@ -343,7 +343,8 @@ def test_stateful_compress_int8_rotated_equals_one_shot():
 
 
 # Overlapping ratio-4 compression ("Hyper-Parallel ... DeepSeek V4 CP",
-# "ratio=4" halo: a group needs the ratio tokens before it; reading: entry g
+# "6.1 ratio4 CSA: compressor halo": a group needs the ratio tokens before
+# it; reading: entry g
 # pools groups g - 1 and g, each token's logit taking ape[position % ratio]).
 
 

@@ -41,7 +41,9 @@ class WorkloadSpec:
     kv_pages: str = "all"  # "all" or "window" (only pages the window reads; others -1)
     cmp_init: str = "random"  # "random" or "zeros" (filled by the compressor)
     pad_rows: int = 0  # trailing padding rows (row_req = -1)
-    state: bool = False  # compressors keep a recurrent state ring (capacity max(4, ratio))
+    state: bool = False  # compressors keep a recurrent state ring (capacity max(4, ratio),
+    #                      doubled with overlap)
+    overlap: bool = False  # overlapping compressors: each entry pools the previous group too
     dense: bool = False  # HCA: no indexer, attention over every visible compressed entry
     # hierarchical indexer: a level-one layer selects n_cand blocks of
     # cand_block compressed positions and a reindex layer (its own q, q_idx,
@@ -115,6 +117,14 @@ CONFIGS = {
     # million_decode with the low-bit caches
     "lowbit_million": WorkloadSpec("lowbit_million", [1048576] * 4, [2] * 4, ratio=4, topk=2048,
                                    seed=10, kv_pages="window", lowbit=True),
+    # the overlapping ratio-4 compressors (each entry pools the previous
+    # group's four tokens too): stateful_decode's requests with rings of
+    # eight slots, and chunked_prefill's 8192-token chunk
+    "overlap_decode": WorkloadSpec("overlap_decode", [8192, 6000, 4096, 2048], [2, 2, 2, 2],
+                                   ratio=4, topk=512, seed=12, kv_pool_pages=256,
+                                   cmp_pool_pages=256, state=True, overlap=True),
+    "overlap_prefill": WorkloadSpec("overlap_prefill", [8192], [8192], ratio=4, topk=512, seed=13,
+                                    mode="prefill", cmp_init="zeros", overlap=True),
 }
 
 
@@ -275,7 +285,7 @@ def make_workload(spec: WorkloadSpec) -> Workload:
     if spec.state:
         # one ring block per request (plus a spare) in a shuffled order; the
         # slots hold earlier tokens' kv rows (BF16 values) and gate scores
-        cap = max(4, r)
+        cap = max(4, r) * (2 if spec.overlap else 1)
         t["state_table"] = torch.from_numpy(rng.permutation(B + 1)[:B].astype(np.int32))
         for name, d in (("state_main", Dm), ("state_idx", Di)):
             kv_part = _normal_bf16(rng, (B + 1, cap, d)).float()
