@@ -541,10 +541,9 @@ bool pool_wide(const csa_compress_args &a) {
 // request's chunk stores its kv row (FP32) and its gate score (ape included)
 // in slot p % state_capacity.  Runs after the pooling kernel, so every ring
 // read of the call precedes every write.  One CTA per row, d threads.
-__global__ void compress_state_kernel(csa_compress_args a, const float *__restrict__ logits) {
-  tc::griddep_wait();
-  tc::griddep_launch_dependents();
-  const int t = blockIdx.x, d = threadIdx.x;
+__device__ __forceinline__ void state_row(const csa_compress_args &a,
+                                          const float *__restrict__ logits, const int t,
+                                          const int d) {
   const int b = a.row_req[t], p = a.positions[t];
   if (b < 0 || b >= a.n_req || p < 0) return;
   const int blk = a.state_block_table[b];
@@ -554,6 +553,23 @@ __global__ void compress_state_kernel(csa_compress_args a, const float *__restri
   float *slot = a.state_cache + ((long long)blk * cap + p % cap) * 2 * D;
   slot[d] = bf16_bits_to_float(static_cast<const uint16_t *>(a.kv)[(long long)t * D + d]);
   slot[D + d] = logits[(long long)t * D + d] + a.ape[(p % a.ratio) * D + d];
+}
+
+__global__ void compress_state_kernel(csa_compress_args a, const float *__restrict__ logits) {
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
+  state_row(a, logits, blockIdx.x, threadIdx.x);
+}
+
+// The ring writes of a layer's two compressors in one grid (blockIdx.y picks
+// the compressor; each reads its own logits from its workspace).
+__global__ void compress_state_pair_kernel(const __grid_constant__ csa_compress_args a,
+                                           const __grid_constant__ csa_compress_args b) {
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
+  const csa_compress_args *x = blockIdx.y == 0 ? &a : &b;
+  if ((int)blockIdx.x >= x->n_rows || (int)threadIdx.x >= x->d) return;
+  state_row(*x, static_cast<const float *>(x->workspace), blockIdx.x, threadIdx.x);
 }
 
 // Gate logits of a short chunk, row by row (the tensor-core GEMM's 128-row
@@ -607,6 +623,58 @@ __global__ void __launch_bounds__(GR_THREADS) gate_rows_kernel(csa_compress_args
 // ---------------------------------------------------------------------------
 constexpr int FC_THREADS = 256;
 constexpr int FC_MAX_W_BYTES = 128 * 1024;
+
+// RMSNorm (whole-row variant), rotation at the group start and publication
+// of one pooled row (y: this thread's channel c = threadIdx.x < COLS).
+template <int COLS>
+__device__ __forceinline__ void fused_tail(const csa_compress_args &a, float y, const int cb,
+                                           const float gam, const float cs, const float sn,
+                                           const bool rope_ok, const bool rot_here, float *ys,
+                                           float *red, const long long dst_row) {
+  const int D = a.d, tid = threadIdx.x, c = tid, d = cb * COLS + c;
+  // row-wide statistics exist only in the whole-row variant (COLS == D)
+  if (a.gamma && COLS == D) {
+    float v = c < COLS ? y * y : 0.f;
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((tid & 31) == 0) red[tid >> 5] = v;
+    __syncthreads();
+    float ss = 0.f;
+    for (int i = 0; i < FC_THREADS / 32; ++i) ss += red[i];
+    __syncthreads();
+    if (c < COLS) y = round_bf16(y * rsqrtf(ss / (float)D + a.rms_eps) * gam);
+  }
+  if (a.rotate) {
+    if (c < COLS) ys[c] = y;
+    __syncthreads();
+    if (!rope_ok) {
+      if (tid == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
+    } else if (rot_here) {
+      y = (d & 1) == 0 ? ys[c] * cs - ys[c + 1] * sn : ys[c - 1] * sn + ys[c] * cs;
+    }
+  }
+  if (a.out_mode == CSA_OUT_BF16) {
+    if (c < COLS) static_cast<__nv_bfloat16 *>(a.cmp_pool)[dst_row * D + d] = __float2bfloat16_rn(y);
+  } else if (a.out_mode == CSA_OUT_FP4_E4M3) {
+    publish_fp4<16>(a, dst_row, d, y, c < COLS);
+  } else if (a.out_mode == CSA_OUT_FP4_E8M0) {
+    publish_fp4<32>(a, dst_row, d, y, c < COLS);
+  } else if (a.out_mode == CSA_OUT_MXFP8) {
+    publish_mxfp8(a, dst_row, d, y, c < COLS);
+  } else {
+    float v = c < COLS ? fabsf(y) : 0.f;
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((tid & 31) == 0) red[tid >> 5] = v;
+    __syncthreads();
+    float amax = 0.f;
+    for (int i = 0; i < FC_THREADS / 32; ++i) amax = fmaxf(amax, red[i]);
+    const float scale = fmaxf(amax, 1e-4f) / 127.0f;
+    if (c < COLS) {
+      const float q = fminf(fmaxf(rintf(y / scale), -127.f), 127.f);
+      a.idx_pool[dst_row * D + d] = static_cast<int8_t>(q);
+    }
+    if (tid == 0) a.idx_scale_pool[dst_row] = scale;
+  }
+}
 
 template <int COLS>
 __device__ __forceinline__ void fused_group(const csa_compress_args &a, const int cb, const int t,
@@ -715,64 +783,189 @@ __device__ __forceinline__ void fused_group(const csa_compress_args &a, const in
       }
     y = round_bf16(y / s);
   }
-  // row-wide statistics exist only in the whole-row variant (COLS == D)
-  if (a.gamma && COLS == D) {
-    float v = c < COLS ? y * y : 0.f;
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if ((tid & 31) == 0) red[tid >> 5] = v;
-    __syncthreads();
-    float ss = 0.f;
-    for (int i = 0; i < FC_THREADS / 32; ++i) ss += red[i];
-    __syncthreads();
-    if (c < COLS) y = round_bf16(y * rsqrtf(ss / (float)D + a.rms_eps) * gam);
-  }
-  if (a.rotate) {
-    if (c < COLS) ys[c] = y;
-    __syncthreads();
-    if (!rope_ok) {
-      if (tid == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
-    } else if (rot_here) {
-      y = (d & 1) == 0 ? ys[c] * cs - ys[c + 1] * sn : ys[c - 1] * sn + ys[c] * cs;
-    }
-  }
-  const long long dst_row = (long long)phys * kBlock + (g % kBlock);
-  if (a.out_mode == CSA_OUT_BF16) {
-    if (c < COLS) static_cast<__nv_bfloat16 *>(a.cmp_pool)[dst_row * D + d] = __float2bfloat16_rn(y);
-  } else if (a.out_mode == CSA_OUT_FP4_E4M3) {
-    publish_fp4<16>(a, dst_row, d, y, c < COLS);
-  } else if (a.out_mode == CSA_OUT_FP4_E8M0) {
-    publish_fp4<32>(a, dst_row, d, y, c < COLS);
-  } else if (a.out_mode == CSA_OUT_MXFP8) {
-    publish_mxfp8(a, dst_row, d, y, c < COLS);
-  } else {
-    float v = c < COLS ? fabsf(y) : 0.f;
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if ((tid & 31) == 0) red[tid >> 5] = v;
-    __syncthreads();
-    float amax = 0.f;
-    for (int i = 0; i < FC_THREADS / 32; ++i) amax = fmaxf(amax, red[i]);
-    const float scale = fmaxf(amax, 1e-4f) / 127.0f;
-    if (c < COLS) {
-      const float q = fminf(fmaxf(rintf(y / scale), -127.f), 127.f);
-      a.idx_pool[dst_row * D + d] = static_cast<int8_t>(q);
-    }
-    if (tid == 0) a.idx_scale_pool[dst_row] = scale;
-  }
+  fused_tail<COLS>(a, y, cb, gam, cs, sn, rope_ok, rot_here, ys, red,
+                   (long long)phys * kBlock + (g % kBlock));
 }
 
+// The short-chunk kernel with a state ring: row t's CTA computes its own gate
+// logit when the row is among the last state_capacity rows of its request
+// (into the workspace, FP32 without ape, for the ring-write kernel that runs
+// after every read of the call), and when t closes a group it pools the
+// window's tokens: rows of this chunk from x and kv, earlier positions from
+// the ring (kv row and score with ape, as stored).  The window is the r
+// tokens of the group, or with `overlap` the n = min(p + 1, 2r) tokens
+// ending at p; n <= FR_NJ.
+constexpr int FR_NJ = 8;
+
 template <int COLS>
+__device__ __forceinline__ void fused_group_ring(const csa_compress_args &a, const int cb,
+                                                 const int t, uint8_t *fc_smem) {
+  constexpr int PARTS = FC_THREADS / COLS;
+  const int dx = a.dx, D = a.d, r = a.ratio, tid = threadIdx.x;
+  uint16_t *Ws = reinterpret_cast<uint16_t *>(fc_smem);               // [dx][COLS]
+  uint16_t *Xs = Ws + (size_t)dx * COLS;                               // [FR_NJ][dx]
+  float *part = reinterpret_cast<float *>(Xs + FR_NJ * dx);           // [PARTS][FR_NJ][COLS]
+  float *ys = part + PARTS * FR_NJ * COLS;                             // [COLS]
+  float *red = ys + COLS;                                              // [32]
+  const int c0 = cb * COLS;
+  const int b = a.row_req[t], p = a.positions[t];
+  if (b < 0 || p < 0) return;
+  const bool closing = (p % r) == r - 1;
+  if (b >= a.n_req) {
+    if (closing && tid == 0 && cb == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
+    return;
+  }
+  const int blk = a.state_block_table[b];
+  if (blk < 0) return;  // the request's compressor is disabled
+  if (blk >= a.n_state_blocks) {
+    if (closing && tid == 0 && cb == 0) flag(a.status_dev, CSA_DEV_BAD_BLOCK);
+    return;
+  }
+  const int cap = a.state_capacity;
+  const bool writer = !(t + cap < a.n_rows && a.row_req[t + cap] == b);
+  if (!closing && !writer) return;
+  const int n = closing ? (a.overlap ? min(p + 1, 2 * r) : r) : 1;
+  const int t0 = t - n + 1, q0 = p - n + 1;
+  // bit j: token j of the window (position q0 + j) is row t0 + j of this chunk
+  uint32_t here = 0;
+#pragma unroll
+  for (int j = 0; j < FR_NJ; ++j) {
+    if (j >= n) break;
+    const int sj = t0 + j;
+    if (sj >= 0 && a.row_req[sj] == b && a.positions[sj] == q0 + j) here |= 1u << j;
+  }
+  const float *ring = a.state_cache + (long long)blk * cap * 2 * D;
+  // ---- every input in flight at once
+  const uint16_t *wg = static_cast<const uint16_t *>(a.w_gate);
+  const uint16_t *xg = static_cast<const uint16_t *>(a.x);
+  for (int e = tid; e < dx * (COLS / 8); e += FC_THREADS) {
+    const int k = e / (COLS / 8), q = e % (COLS / 8);
+    tc::cp_async16(Ws + k * COLS + q * 8, wg + (long long)k * D + c0 + q * 8);
+  }
+  for (int e = tid; e < n * (dx / 8); e += FC_THREADS) {
+    const int j = e / (dx / 8), q = e % (dx / 8);
+    if ((here >> j) & 1u) tc::cp_async16(Xs + j * dx + q * 8, xg + (long long)(t0 + j) * dx + q * 8);
+  }
+  const int g = p / r, page = g / kBlock;
+  int phys = -1;
+  if (closing && page < a.max_blocks) phys = a.block_table[(long long)b * a.max_blocks + page];
+  const int c = tid, d = c0 + c;
+  const int pos = g * r;  // RoPE position: the group start
+  const bool rope_ok = pos < a.rope_cap;
+  const bool rot_here = a.rotate && rope_ok && c < COLS && d >= D - kRopeDim;
+  const uint16_t *kvg = static_cast<const uint16_t *>(a.kv);
+  // per token: its kv value and the part of its score known before the dot
+  // product (ape for a chunk row, the whole stored score for a ring slot)
+  float kvj[FR_NJ], basej[FR_NJ];
+  float cs = 1.f, sn = 0.f, gam = 1.f;
+#pragma unroll
+  for (int j = 0; j < FR_NJ; ++j) {
+    kvj[j] = 0.f;
+    basej[j] = -INFINITY;
+  }
+  if (c < COLS && closing) {
+#pragma unroll
+    for (int j = 0; j < FR_NJ; ++j) {
+      if (j >= n) break;
+      if ((here >> j) & 1u) {
+        kvj[j] = bf16_bits_to_float(kvg[(long long)(t0 + j) * D + d]);
+        basej[j] = a.ape[((q0 + j) % r) * D + d];
+      } else {
+        const float *slot = ring + (long long)((q0 + j) % cap) * 2 * D;
+        kvj[j] = slot[d];
+        basej[j] = slot[D + d];
+      }
+    }
+    if (rot_here) {
+      const int i = (d - (D - kRopeDim)) >> 1;
+      cs = a.rope_cos[(long long)pos * kRopeHalf + i];
+      sn = a.rope_sin[(long long)pos * kRopeHalf + i];
+    }
+    if (a.gamma && COLS == D) gam = bf16_bits_to_float(static_cast<const uint16_t *>(a.gamma)[d]);
+  }
+  tc::cp_async_wait_all();
+  __syncthreads();
+  bool publish = closing;
+  if (closing && (phys < 0 || phys >= a.n_blocks)) {  // the same for every thread of the CTA
+    if (tid == 0 && cb == 0) flag(a.status_dev, CSA_DEV_BAD_BLOCK);
+    publish = false;
+    if (!writer) return;
+  }
+  // ---- logits of the window's chunk rows: thread (column, part) sums its K range
+  {
+    const int cc = tid % COLS, pr = tid / COLS;
+    const int k_lo = pr * (dx / PARTS), k_hi = pr == PARTS - 1 ? dx : k_lo + dx / PARTS;
+    float acc[FR_NJ];
+#pragma unroll
+    for (int j = 0; j < FR_NJ; ++j) acc[j] = 0.f;
+    for (int k = k_lo; k < k_hi; ++k) {
+      const float w = bf16_bits_to_float(Ws[k * COLS + cc]);
+#pragma unroll
+      for (int j = 0; j < FR_NJ; ++j)
+        if ((here >> j) & 1u) acc[j] = fmaf(bf16_bits_to_float(Xs[j * dx + k]), w, acc[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < FR_NJ; ++j)
+      if ((here >> j) & 1u) part[(pr * FR_NJ + j) * COLS + cc] = acc[j];
+  }
+  __syncthreads();
+  float y = 0.f;
+  if (c < COLS) {
+    float lg[FR_NJ];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < FR_NJ; ++j) {
+      lg[j] = -INFINITY;
+      if (j >= n) continue;
+      if ((here >> j) & 1u) {
+        float l = 0.f;
+        for (int pr = 0; pr < PARTS; ++pr) l += part[(pr * FR_NJ + j) * COLS + c];
+        if (j == n - 1 && writer) static_cast<float *>(a.workspace)[(long long)t * D + d] = l;
+        lg[j] = l + basej[j];
+      } else {
+        lg[j] = basej[j];
+      }
+      mx = fmaxf(mx, lg[j]);
+    }
+    if (publish) {
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < FR_NJ; ++j) {
+        if (j >= n) continue;
+        const float e = expf(lg[j] - mx);
+        sum += e;
+        y = fmaf(e, kvj[j], y);
+      }
+      y = round_bf16(y / sum);
+    }
+  }
+  if (!publish) return;  // uniform over the CTA
+  fused_tail<COLS>(a, y, cb, gam, cs, sn, rope_ok, rot_here, ys, red,
+                   (long long)phys * kBlock + (g % kBlock));
+}
+
+template <int COLS, bool RING>
+__device__ __forceinline__ void fused_dispatch(const csa_compress_args &a, const int cb,
+                                               const int t, uint8_t *fc_smem) {
+  if constexpr (RING)
+    fused_group_ring<COLS>(a, cb, t, fc_smem);
+  else
+    fused_group<COLS>(a, cb, t, fc_smem);
+}
+
+template <int COLS, bool RING>
 __global__ void __launch_bounds__(FC_THREADS)
     compress_fused_kernel(const __grid_constant__ csa_compress_args a) {
   tc::griddep_wait();
   tc::griddep_launch_dependents();
   extern __shared__ __align__(16) uint8_t fc_smem[];
-  fused_group<COLS>(a, blockIdx.x, blockIdx.y, fc_smem);
+  fused_dispatch<COLS, RING>(a, blockIdx.x, blockIdx.y, fc_smem);
 }
 
 // Two compressors of one layer (the main KV compressor and the index-key
 // compressor read the same rows) in one grid: column tiles [0, n_a) serve the
 // first, the rest the second.
-template <int CA, int CB>
+template <int CA, int CB, bool RING>
 __global__ void __launch_bounds__(FC_THREADS)
     compress_fused_pair_kernel(const __grid_constant__ csa_compress_args a,
                                const __grid_constant__ csa_compress_args b, int n_a) {
@@ -781,21 +974,24 @@ __global__ void __launch_bounds__(FC_THREADS)
   extern __shared__ __align__(16) uint8_t fc_smem[];
   const int x = blockIdx.x, t = blockIdx.y;
   if (x < n_a) {
-    if (t < a.n_rows) fused_group<CA>(a, x, t, fc_smem);
+    if (t < a.n_rows) fused_dispatch<CA, RING>(a, x, t, fc_smem);
   } else if (t < b.n_rows) {
-    fused_group<CB>(b, x - n_a, t, fc_smem);
+    fused_dispatch<CB, RING>(b, x - n_a, t, fc_smem);
   }
 }
 
-template <int COLS>
+template <int COLS, bool RING>
 size_t fused_smem(const csa_compress_args &a) {
-  return (size_t)a.dx * COLS * 2 + 4 * (size_t)a.dx * 2 +
-         (FC_THREADS / COLS) * 4 * COLS * 4 + COLS * 4 + 32 * 4;
+  const size_t nj = RING ? FR_NJ : 4;
+  return (size_t)a.dx * COLS * 2 + nj * (size_t)a.dx * 2 +
+         (FC_THREADS / COLS) * nj * COLS * 4 + COLS * 4 + 32 * 4;
 }
 
 // the short-chunk column tile for this call, or 0 when it takes the long path
+// (with a ring: windows of at most FR_NJ tokens; without one: no overlap)
 int fused_cols(const csa_compress_args &a) {
-  if (a.n_rows > 256 || a.state_cache || a.ratio > 4 || a.overlap) return 0;
+  if (a.n_rows > 256 || a.ratio > 4) return 0;
+  if (a.state_cache ? (a.overlap ? 2 : 1) * a.ratio > FR_NJ : a.overlap) return 0;
   if (a.d == 128 && (size_t)a.dx * 128 * 2 <= FC_MAX_W_BYTES) return 128;
   // the 16-column tiles of d = 512 publish BF16 or E4M3-scaled groups of 16
   if (a.d == 512 && (a.out_mode == CSA_OUT_BF16 || a.out_mode == CSA_OUT_FP4_E4M3) && !a.gamma &&
@@ -806,7 +1002,7 @@ int fused_cols(const csa_compress_args &a) {
 
 // The dynamic shared-memory limit is raised once per kernel and device
 // (CB == 0: the single-compressor kernel of column tile CA).
-template <int CA, int CB>
+template <int CA, int CB, bool RING>
 cudaError_t allow_fused_smem() {
   static bool done[64] = {};
   int dev = 0;
@@ -814,38 +1010,50 @@ cudaError_t allow_fused_smem() {
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
   cudaError_t e;
   if constexpr (CB == 0)
-    e = cudaFuncSetAttribute(compress_fused_kernel<CA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             FC_MAX_W_BYTES + 32 * 1024);
+    e = cudaFuncSetAttribute(compress_fused_kernel<CA, RING>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, FC_MAX_W_BYTES + 32 * 1024);
   else
-    e = cudaFuncSetAttribute(compress_fused_pair_kernel<CA, CB>,
+    e = cudaFuncSetAttribute(compress_fused_pair_kernel<CA, CB, RING>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, FC_MAX_W_BYTES + 32 * 1024);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
 
-template <int COLS>
+template <int COLS, bool RING>
 cudaError_t launch_fused(const csa_compress_args &a, cudaStream_t s) {
-  cudaError_t e = allow_fused_smem<COLS, 0>();
+  cudaError_t e = allow_fused_smem<COLS, 0, RING>();
   if (e != cudaSuccess) return e;
   launch_begin(CSA_K_COMPRESS_FUSED, s);
-  e = launch_kernel(compress_fused_kernel<COLS>, dim3(a.d / COLS, a.n_rows), dim3(FC_THREADS),
-                    fused_smem<COLS>(a), s, 0, false, a);
+  e = launch_kernel(compress_fused_kernel<COLS, RING>, dim3(a.d / COLS, a.n_rows),
+                    dim3(FC_THREADS), fused_smem<COLS, RING>(a), s, 0, false, a);
   launch_end(CSA_K_COMPRESS_FUSED, s);
+  if (e == cudaSuccess && RING) {  // ring writes after every read of the call
+    launch_begin(CSA_K_COMPRESS_POOL, s);
+    e = launch_kernel(compress_state_kernel, dim3(a.n_rows), dim3(a.d), 0, s, 0, false, a,
+                      static_cast<const float *>(a.workspace));
+    launch_end(CSA_K_COMPRESS_POOL, s);
+  }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int CA, int CB>
+template <int CA, int CB, bool RING>
 cudaError_t launch_fused_pair(const csa_compress_args &a, const csa_compress_args &b,
                               cudaStream_t s) {
-  cudaError_t e = allow_fused_smem<CA, CB>();
+  cudaError_t e = allow_fused_smem<CA, CB, RING>();
   if (e != cudaSuccess) return e;
   const int n_a = a.d / CA, n_b = b.d / CB;
-  const size_t smem = fused_smem<CA>(a) > fused_smem<CB>(b) ? fused_smem<CA>(a) : fused_smem<CB>(b);
+  const size_t sa = fused_smem<CA, RING>(a), sb = fused_smem<CB, RING>(b);
+  const int rows = a.n_rows > b.n_rows ? a.n_rows : b.n_rows;
   launch_begin(CSA_K_COMPRESS_FUSED, s);
-  e = launch_kernel(compress_fused_pair_kernel<CA, CB>,
-                    dim3(n_a + n_b, a.n_rows > b.n_rows ? a.n_rows : b.n_rows), dim3(FC_THREADS),
-                    smem, s, 0, false, a, b, n_a);
+  e = launch_kernel(compress_fused_pair_kernel<CA, CB, RING>, dim3(n_a + n_b, rows),
+                    dim3(FC_THREADS), sa > sb ? sa : sb, s, 0, false, a, b, n_a);
   launch_end(CSA_K_COMPRESS_FUSED, s);
+  if (e == cudaSuccess && RING) {  // both rings' writes after every read of the call
+    launch_begin(CSA_K_COMPRESS_POOL, s);
+    e = launch_kernel(compress_state_pair_kernel, dim3(rows, 2), dim3(a.d > b.d ? a.d : b.d), 0,
+                      s, 0, false, a, b);
+    launch_end(CSA_K_COMPRESS_POOL, s);
+  }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -853,10 +1061,15 @@ cudaError_t launch_fused_pair(const csa_compress_args &a, const csa_compress_arg
 
 cudaError_t launch_compress(const csa_compress_args &a, float *logits, cudaStream_t s) {
   if (a.n_rows <= 0) return cudaSuccess;
-  // short chunks (decode): one fused kernel per call
+  // short chunks (decode): one fused kernel per call (and the ring writes)
   const int cols = fused_cols(a);
-  if (cols == 128) return launch_fused<128>(a, s);
-  if (cols == 16) return launch_fused<16>(a, s);
+  if (a.state_cache) {
+    if (cols == 128) return launch_fused<128, true>(a, s);
+    if (cols == 16) return launch_fused<16, true>(a, s);
+  } else {
+    if (cols == 128) return launch_fused<128, false>(a, s);
+    if (cols == 16) return launch_fused<16, false>(a, s);
+  }
   if (a.dx % GG_K != 0 || a.d % GG_N != 0 || (reinterpret_cast<uintptr_t>(logits) & 15u) != 0)
     return cudaErrorInvalidValue;
   cudaError_t e;
@@ -893,10 +1106,16 @@ cudaError_t launch_compress(const csa_compress_args &a, float *logits, cudaStrea
 cudaError_t launch_compress_pair(const csa_compress_args &a, float *logits_a,
                                  const csa_compress_args &b, float *logits_b, cudaStream_t s) {
   const int ca = a.n_rows > 0 ? fused_cols(a) : -1, cb = b.n_rows > 0 ? fused_cols(b) : -1;
-  if (ca == 16 && cb == 128) return launch_fused_pair<16, 128>(a, b, s);
-  if (ca == 128 && cb == 16) return launch_fused_pair<128, 16>(a, b, s);
-  if (ca == 128 && cb == 128) return launch_fused_pair<128, 128>(a, b, s);
-  if (ca == 16 && cb == 16) return launch_fused_pair<16, 16>(a, b, s);
+  if (!a.state_cache && !b.state_cache) {
+    if (ca == 16 && cb == 128) return launch_fused_pair<16, 128, false>(a, b, s);
+    if (ca == 128 && cb == 16) return launch_fused_pair<128, 16, false>(a, b, s);
+    if (ca == 128 && cb == 128) return launch_fused_pair<128, 128, false>(a, b, s);
+    if (ca == 16 && cb == 16) return launch_fused_pair<16, 16, false>(a, b, s);
+  } else if (a.state_cache && b.state_cache) {
+    // the layer's main (d = 512) and index-key (d = 128) compressors
+    if (ca == 16 && cb == 128) return launch_fused_pair<16, 128, true>(a, b, s);
+    if (ca == 128 && cb == 128) return launch_fused_pair<128, 128, true>(a, b, s);
+  }
   const cudaError_t e = launch_compress(a, logits_a, s);
   return e != cudaSuccess ? e : launch_compress(b, logits_b, s);
 }
