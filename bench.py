@@ -37,31 +37,36 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # kernel reports null.  Values are from `ncu --metrics dram__bytes_read.sum,
 # dram__bytes_write.sum` captures of these same bench workloads.
 NCU_TRAFFIC = {
-    ("serving_decode", "attn_decode"): {"bytes": 4615377, "src": "77022dbcfaf0"},
-    ("serving_decode", "index_topk"): {"bytes": 125156, "src": "b1465b204230"},
-    ("serving_decode", "index_score"): {"bytes": 1553436, "src": "7a13a25375a1"},
-    ("serving_decode", "compress_fused"): {"bytes": 624716, "src": "7a354d1303af"},
-    ("million_decode", "index_score"): {"bytes": 143111623, "src": "7a13a25375a1"},
-    ("million_decode", "attn_decode"): {"bytes": 17843447, "src": "77022dbcfaf0"},
-    ("million_decode", "index_topk"): {"bytes": 8640664, "src": "b1465b204230"},
-    ("million_decode", "compress_fused"): {"bytes": 53570, "src": "7a354d1303af"},
-    ("hier_decode", "index_score"): {"bytes": 80713183, "src": "7a13a25375a1"},
-    ("hier_decode", "index_topk"): {"bytes": 3529646, "src": "b1465b204230"},
-    ("hier_decode", "attn_decode"): {"bytes": 5364622, "src": "77022dbcfaf0"},
-    ("hier_decode", "compress_fused"): {"bytes": 53447, "src": "7a354d1303af"},
-    ("lowbit_decode", "attn_decode"): {"bytes": 2073183, "src": "77022dbcfaf0"},
-    ("lowbit_decode", "index_topk"): {"bytes": 125175, "src": "b1465b204230"},
-    ("lowbit_decode", "index_score"): {"bytes": 897982, "src": "7a13a25375a1"},
-    ("lowbit_decode", "compress_fused"): {"bytes": 624488, "src": "7a354d1303af"},
-    ("lowbit_million", "index_score"): {"bytes": 72217012, "src": "7a13a25375a1"},
-    ("lowbit_million", "attn_decode"): {"bytes": 7185209, "src": "77022dbcfaf0"},
-    ("lowbit_million", "index_topk"): {"bytes": 8639308, "src": "b1465b204230"},
-    ("lowbit_million", "compress_fused"): {"bytes": 53817, "src": "7a354d1303af"},
-    ("chunked_prefill", "attn_prefill"): {"bytes": 1058863524, "src": "96ab4a6b48bb"},
-    ("chunked_prefill", "index_score"): {"bytes": 148996628, "src": "7a13a25375a1"},
-    ("chunked_prefill", "index_topk"): {"bytes": 34523453, "src": "b1465b204230"},
-    ("chunked_prefill", "compress_pool"): {"bytes": 16092078, "src": "7a354d1303af"},
-    ("chunked_prefill", "compress_gate"): {"bytes": 5534776, "src": "7a354d1303af"},
+    ("serving_decode", "attn_decode"): {"bytes": 4613480, "src": "77022dbcfaf0"},
+    ("serving_decode", "index_topk"): {"bytes": 125108, "src": "2b8bb3a236f3"},
+    ("serving_decode", "index_score"): {"bytes": 1551720, "src": "fcdb94044445"},
+    ("serving_decode", "compress_fused"): {"bytes": 624583, "src": "ac9642133bd1"},
+    ("million_decode", "index_score"): {"bytes": 143141433, "src": "fcdb94044445"},
+    ("million_decode", "attn_decode"): {"bytes": 17840735, "src": "77022dbcfaf0"},
+    ("million_decode", "index_topk"): {"bytes": 8639099, "src": "2b8bb3a236f3"},
+    ("million_decode", "compress_fused"): {"bytes": 52859, "src": "ac9642133bd1"},
+    ("hier_decode", "index_score"): {"bytes": 80720555, "src": "fcdb94044445"},
+    ("hier_decode", "index_topk"): {"bytes": 3531305, "src": "2b8bb3a236f3"},
+    ("hier_decode", "attn_decode"): {"bytes": 5363541, "src": "77022dbcfaf0"},
+    ("hier_decode", "compress_fused"): {"bytes": 53210, "src": "ac9642133bd1"},
+    ("lowbit_decode", "attn_decode"): {"bytes": 2072282, "src": "77022dbcfaf0"},
+    ("lowbit_decode", "index_topk"): {"bytes": 124653, "src": "2b8bb3a236f3"},
+    ("lowbit_decode", "index_score"): {"bytes": 896199, "src": "fcdb94044445"},
+    ("lowbit_decode", "compress_fused"): {"bytes": 624251, "src": "ac9642133bd1"},
+    ("lowbit_million", "index_score"): {"bytes": 72206260, "src": "fcdb94044445"},
+    ("lowbit_million", "attn_decode"): {"bytes": 7184981, "src": "77022dbcfaf0"},
+    ("lowbit_million", "index_topk"): {"bytes": 8638388, "src": "2b8bb3a236f3"},
+    ("lowbit_million", "compress_fused"): {"bytes": 52897, "src": "ac9642133bd1"},
+    ("chunked_prefill", "attn_prefill"): {"bytes": 1058759936, "src": "96ab4a6b48bb"},
+    ("chunked_prefill", "index_score"): {"bytes": 149854822, "src": "fcdb94044445"},
+    ("chunked_prefill", "index_topk"): {"bytes": 34512456, "src": "2b8bb3a236f3"},
+    ("chunked_prefill", "compress_pool"): {"bytes": 16095468, "src": "ac9642133bd1"},
+    ("chunked_prefill", "compress_gate"): {"bytes": 5533819, "src": "ac9642133bd1"},
+    ("overlap_decode", "attn_decode"): {"bytes": 4260807, "src": "77022dbcfaf0"},
+    ("overlap_decode", "compress_fused"): {"bytes": 777946, "src": "ac9642133bd1"},
+    ("overlap_decode", "index_topk"): {"bytes": 84414, "src": "2b8bb3a236f3"},
+    ("overlap_decode", "index_score"): {"bytes": 875956, "src": "fcdb94044445"},
+    ("overlap_decode", "compress_pool"): {"bytes": 40676, "src": "ac9642133bd1"},
 }
 
 
