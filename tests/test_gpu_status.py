@@ -164,3 +164,42 @@ def test_empty_batches_launch_nothing():
     torch.cuda.synchronize()
     assert csa.launch_count() == n0
     assert int(step.status.item()) == 0
+
+
+def test_ring_compressor_flags_unmapped_destination_and_still_updates_the_ring():
+    """The short-chunk compressor with state rings (overlapping windows): a
+    group whose destination page is unmapped is flagged and not written,
+    while the rings still receive every row as the oracle's rings do."""
+    spec = spec_for("overlap_decode", seed=83)
+    wl = make_workload(spec)
+    t = wl.to(DEV)
+    assert int(wl.row_req[1]) == 0 and int(wl.row_pos[1]) % spec.ratio == spec.ratio - 1
+    g0 = int(wl.row_pos[1]) // spec.ratio  # the group row 1 closes
+    table = wl.cmp_table.clone()
+    table[0, g0 // BLOCK] = -1
+    t_bad = dict(t)
+    t_bad["cmp_table"] = table.to(DEV)
+    before = t["cmp_pool"].clone()
+    step = CsaStep(t_bad, spec.ratio, spec.topk, overlap=True)
+    step.compress()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) & BAD_BLOCK
+    pools, main, _ = OS.compress_step(wl.t, spec)
+    got = t["cmp_pool"].cpu()
+    ref_table = wl.cmp_table.numpy()
+    n_other = 0
+    for b, g, y in main:
+        pg, row = int(ref_table[b, g // BLOCK]), g % BLOCK
+        if b == 0 and g == g0:
+            assert torch.equal(got[pg, row], before[pg, row].cpu())
+        else:
+            check_bf16(got[pg, row].double().numpy(), y, f"entry {b}/{g}")
+            n_other += 1
+    assert n_other > 0
+    for name in ("state_main", "state_idx"):
+        got_s = t[name].cpu().double().numpy()
+        ref_s = pools[name]
+        d = got_s.shape[2] // 2
+        assert np.array_equal(got_s[..., :d], ref_s[..., :d]), name
+        err = np.abs(got_s[..., d:] - ref_s[..., d:])
+        assert np.all(err <= 1e-4 * np.maximum(1.0, np.abs(ref_s[..., d:]))), (name, err.max())
