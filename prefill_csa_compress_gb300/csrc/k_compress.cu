@@ -253,15 +253,12 @@ __device__ __forceinline__ float block_max(float v, float *red) {
 // window is the group's r tokens, or with `overlap` the previous group's too
 // (n = min(p + 1, 2r) tokens ending at p), token q's score taking
 // ape[q % r].
-__global__ void compress_pool_kernel(csa_compress_args a, const float *__restrict__ logits) {
-  tc::griddep_wait();
-  tc::griddep_launch_dependents();
+__device__ __forceinline__ void pool_row(const csa_compress_args &a,
+                                         const float *__restrict__ logits, const int t, const int b,
+                                         const int p) {
   __shared__ float ys[512];
   __shared__ float red[32];
-  const int t = blockIdx.x;
   const int r = a.ratio, D = a.d;
-  const int b = a.row_req[t], p = a.positions[t];
-  if (b < 0 || p < 0 || (p % r) != r - 1) return;
   if (b >= a.n_req) {
     if (threadIdx.x == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
     return;
@@ -384,6 +381,40 @@ __global__ void compress_pool_kernel(csa_compress_args a, const float *__restric
     q = fminf(fmaxf(q, -127.f), 127.f);
     a.idx_pool[dst_row * D + d] = static_cast<int8_t>(q);
     if (d == 0) a.idx_scale_pool[dst_row] = scale;
+  }
+}
+
+// One CTA per row (long groups: HCA's ratio 128).
+__global__ void compress_pool_kernel(csa_compress_args a, const float *__restrict__ logits) {
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
+  const int t = blockIdx.x;
+  const int b = a.row_req[t], p = a.positions[t];
+  if (b < 0 || p < 0 || (p % a.ratio) != a.ratio - 1) return;
+  pool_row(a, logits, t, b, p);
+}
+
+// Short groups: a chunk's group-closing rows are one in every r, so a CTA
+// takes rows_per_cta = r consecutive rows (their requests and positions
+// loaded at once) and pools those that close a group.
+constexpr int kPoolRows = 4;
+__global__ void compress_pool_rows_kernel(csa_compress_args a, const float *__restrict__ logits,
+                                          int rows_per_cta) {
+  tc::griddep_wait();
+  tc::griddep_launch_dependents();
+  __shared__ int rb[kPoolRows], rq[kPoolRows];
+  const int t0 = blockIdx.x * rows_per_cta;
+  const int m = min(rows_per_cta, a.n_rows - t0);
+  if ((int)threadIdx.x < m) {
+    rb[threadIdx.x] = a.row_req[t0 + threadIdx.x];
+    rq[threadIdx.x] = a.positions[t0 + threadIdx.x];
+  }
+  __syncthreads();
+  for (int i = 0; i < m; ++i) {
+    const int b = rb[i], p = rq[i];
+    if (b < 0 || p < 0 || (p % a.ratio) != a.ratio - 1) continue;  // uniform over the CTA
+    pool_row(a, logits, t0 + i, b, p);
+    __syncthreads();  // the row's shared state is no longer read
   }
 }
 
@@ -1090,6 +1121,9 @@ cudaError_t launch_compress(const csa_compress_args &a, float *logits, cudaStrea
     e = launch_kernel(compress_pool_wide_kernel, dim3(std::min(a.n_rows, 2 * device_sm_count()),
                                                       a.d / WP_CH),
                       dim3(WP_THREADS), 0, s, 0, false, a, static_cast<const float *>(logits));
+  else if (a.ratio <= kPoolRows)
+    e = launch_kernel(compress_pool_rows_kernel, dim3((a.n_rows + a.ratio - 1) / a.ratio),
+                      dim3(a.d), 0, s, 0, false, a, static_cast<const float *>(logits), a.ratio);
   else
     e = launch_kernel(compress_pool_kernel, dim3(a.n_rows), dim3(a.d), 0, s, 0, false, a,
                       static_cast<const float *>(logits));
