@@ -37,36 +37,36 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # kernel reports null.  Values are from `ncu --metrics dram__bytes_read.sum,
 # dram__bytes_write.sum` captures of these same bench workloads.
 NCU_TRAFFIC = {
-    ("serving_decode", "attn_decode"): {"bytes": 4613480, "src": "77022dbcfaf0"},
-    ("serving_decode", "index_topk"): {"bytes": 125108, "src": "2b8bb3a236f3"},
-    ("serving_decode", "index_score"): {"bytes": 1551720, "src": "fcdb94044445"},
-    ("serving_decode", "compress_fused"): {"bytes": 624583, "src": "ac9642133bd1"},
-    ("million_decode", "index_score"): {"bytes": 143141433, "src": "fcdb94044445"},
-    ("million_decode", "attn_decode"): {"bytes": 17840735, "src": "77022dbcfaf0"},
-    ("million_decode", "index_topk"): {"bytes": 8639099, "src": "2b8bb3a236f3"},
-    ("million_decode", "compress_fused"): {"bytes": 52859, "src": "ac9642133bd1"},
-    ("hier_decode", "index_score"): {"bytes": 80720555, "src": "fcdb94044445"},
-    ("hier_decode", "index_topk"): {"bytes": 3531305, "src": "2b8bb3a236f3"},
-    ("hier_decode", "attn_decode"): {"bytes": 5363541, "src": "77022dbcfaf0"},
-    ("hier_decode", "compress_fused"): {"bytes": 53210, "src": "ac9642133bd1"},
-    ("lowbit_decode", "attn_decode"): {"bytes": 2072282, "src": "77022dbcfaf0"},
-    ("lowbit_decode", "index_topk"): {"bytes": 124653, "src": "2b8bb3a236f3"},
-    ("lowbit_decode", "index_score"): {"bytes": 896199, "src": "fcdb94044445"},
-    ("lowbit_decode", "compress_fused"): {"bytes": 624251, "src": "ac9642133bd1"},
-    ("lowbit_million", "index_score"): {"bytes": 72206260, "src": "fcdb94044445"},
-    ("lowbit_million", "attn_decode"): {"bytes": 7184981, "src": "77022dbcfaf0"},
-    ("lowbit_million", "index_topk"): {"bytes": 8638388, "src": "2b8bb3a236f3"},
-    ("lowbit_million", "compress_fused"): {"bytes": 52897, "src": "ac9642133bd1"},
-    ("chunked_prefill", "attn_prefill"): {"bytes": 1058759936, "src": "96ab4a6b48bb"},
-    ("chunked_prefill", "index_score"): {"bytes": 149854822, "src": "fcdb94044445"},
-    ("chunked_prefill", "index_topk"): {"bytes": 34512456, "src": "2b8bb3a236f3"},
-    ("chunked_prefill", "compress_pool"): {"bytes": 16095468, "src": "ac9642133bd1"},
-    ("chunked_prefill", "compress_gate"): {"bytes": 5533819, "src": "ac9642133bd1"},
-    ("overlap_decode", "attn_decode"): {"bytes": 4260807, "src": "77022dbcfaf0"},
-    ("overlap_decode", "compress_fused"): {"bytes": 777946, "src": "ac9642133bd1"},
-    ("overlap_decode", "index_topk"): {"bytes": 84414, "src": "2b8bb3a236f3"},
-    ("overlap_decode", "index_score"): {"bytes": 875956, "src": "fcdb94044445"},
-    ("overlap_decode", "compress_pool"): {"bytes": 40676, "src": "ac9642133bd1"},
+    ("serving_decode", "attn_decode"): {"bytes": 4614381, "src": "77022dbcfaf0"},
+    ("serving_decode", "index_topk"): {"bytes": 124843, "src": "2b8bb3a236f3"},
+    ("serving_decode", "index_score"): {"bytes": 1553683, "src": "fcdb94044445"},
+    ("serving_decode", "compress_fused"): {"bytes": 624251, "src": "474e737aae10"},
+    ("million_decode", "index_score"): {"bytes": 143178411, "src": "fcdb94044445"},
+    ("million_decode", "attn_decode"): {"bytes": 17843371, "src": "77022dbcfaf0"},
+    ("million_decode", "index_topk"): {"bytes": 8640085, "src": "2b8bb3a236f3"},
+    ("million_decode", "compress_fused"): {"bytes": 53257, "src": "474e737aae10"},
+    ("hier_decode", "index_score"): {"bytes": 80736009, "src": "fcdb94044445"},
+    ("hier_decode", "index_topk"): {"bytes": 3531112, "src": "2b8bb3a236f3"},
+    ("hier_decode", "attn_decode"): {"bytes": 5365139, "src": "77022dbcfaf0"},
+    ("hier_decode", "compress_fused"): {"bytes": 53077, "src": "474e737aae10"},
+    ("lowbit_decode", "attn_decode"): {"bytes": 2073505, "src": "77022dbcfaf0"},
+    ("lowbit_decode", "index_topk"): {"bytes": 124966, "src": "2b8bb3a236f3"},
+    ("lowbit_decode", "index_score"): {"bytes": 898740, "src": "fcdb94044445"},
+    ("lowbit_decode", "compress_fused"): {"bytes": 624156, "src": "474e737aae10"},
+    ("lowbit_million", "index_score"): {"bytes": 72221459, "src": "fcdb94044445"},
+    ("lowbit_million", "attn_decode"): {"bytes": 7184090, "src": "77022dbcfaf0"},
+    ("lowbit_million", "index_topk"): {"bytes": 8641214, "src": "2b8bb3a236f3"},
+    ("lowbit_million", "compress_fused"): {"bytes": 52916, "src": "474e737aae10"},
+    ("chunked_prefill", "attn_prefill"): {"bytes": 1058926612, "src": "96ab4a6b48bb"},
+    ("chunked_prefill", "index_score"): {"bytes": 149808794, "src": "fcdb94044445"},
+    ("chunked_prefill", "index_topk"): {"bytes": 34506793, "src": "2b8bb3a236f3"},
+    ("chunked_prefill", "compress_pool"): {"bytes": 16097080, "src": "474e737aae10"},
+    ("chunked_prefill", "compress_gate"): {"bytes": 5534019, "src": "474e737aae10"},
+    ("overlap_decode", "attn_decode"): {"bytes": 4260608, "src": "77022dbcfaf0"},
+    ("overlap_decode", "compress_fused"): {"bytes": 778145, "src": "474e737aae10"},
+    ("overlap_decode", "index_topk"): {"bytes": 84983, "src": "2b8bb3a236f3"},
+    ("overlap_decode", "index_score"): {"bytes": 876402, "src": "fcdb94044445"},
+    ("overlap_decode", "compress_pool"): {"bytes": 40761, "src": "474e737aae10"},
 }
 
 
