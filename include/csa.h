@@ -53,7 +53,7 @@ typedef void *csa_stream_t; /* a cudaStream_t */
 typedef enum {
   CSA_OK = 0,
   CSA_ERR_INVALID_ARG = 1, /* a null pointer, a bad size or a misaligned pointer */
-  CSA_ERR_UNSUPPORTED = 2, /* a shape this build does not implement */
+  CSA_ERR_UNSUPPORTED = 2, /* a shape this library does not implement */
   CSA_ERR_CUDA = 3,        /* a CUDA launch or runtime error */
   CSA_ERR_TIMEOUT = 4      /* reserved: a bounded device wait gave up */
 } csa_status_t;
