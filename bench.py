@@ -2,12 +2,16 @@
 
 One step = one pass of the whole path over one batch: the main compressor,
 the index-key compressor, the indexer top-k and the sparse attention (decode
-or prefill).  Default workload: serving decode (4 requests x 2 rows, contexts
-8192/6000/4097/2048, ratio 2, top-k 512).  Other workloads: --workload
-tiny_decode | ratio1_decode | chunked_prefill | million_decode |
-stateful_decode | hca_decode | hca_prefill | hier_decode (a level-one layer
-and a reindex layer of the hierarchical indexer as one step) | lowbit_decode |
-lowbit_million (the low-bit cache formats).
+or prefill).  Default workload: million-position decode (4 requests x 2
+rows, contexts of 1,048,576 positions, ratio 4, top-k 2048), the largest
+single-GPU configuration.  Other workloads: --workload tiny_decode |
+serving_decode | ratio1_decode | chunked_prefill | stateful_decode |
+hca_decode | hca_prefill | hier_decode (a level-one layer and a reindex layer
+of the hierarchical indexer as one step) | lowbit_decode | lowbit_million (the
+low-bit cache formats).
+
+The step is timed as one CUDA graph per step (the headline ``value``) and,
+beside it, issued eagerly call by call (``eager``).
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 the host cores instead (a bounded sample of the same workload).
@@ -297,16 +301,35 @@ class ClockSampler:
 # ---------------------------------------------------------------- reference arm (CPU oracle)
 
 
-def _oracle_cores():
+def _oracle_threads():
+    """Threads the oracle uses: its row loop runs in one Python thread, and
+    numpy's BLAS (matrix products) runs on the BLAS thread pool.  Returns
+    (threads, description)."""
+    blas = None
     try:
         from threadpoolctl import threadpool_info
 
         n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
         if n:
-            return int(max(n))
+            blas = int(max(n))
     except Exception:  # threadpoolctl is optional
         pass
-    return os.cpu_count() or 1
+    if blas is None:
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            if os.environ.get(var, "").isdigit():
+                blas = int(os.environ[var])
+                break
+    if blas is None:
+        blas = os.cpu_count() or 1
+    desc = (f"one Python thread drives the oracle's per-row loop; numpy's BLAS calls "
+            f"use up to {blas} threads; the host has {os.cpu_count()} cores")
+    return blas, desc
+
+
+def _cpu_line(rate, unit, desc):
+    threads, how = _oracle_threads()
+    return {"value": rate, "unit": unit, "cores": threads, "nproc": os.cpu_count(),
+            "threads": how, "kind": "oracle", "sample": desc}
 
 
 def oracle_sample(wl, budget_s=10.0, max_rows=None):
@@ -365,15 +388,13 @@ def oracle_sample(wl, budget_s=10.0, max_rows=None):
 
 def run_reference(args, wl):
     rate, desc, done = oracle_sample(wl, budget_s=args.ref_budget)
-    cores = _oracle_cores()
     unit = "tokens/s" if wl.spec.mode == "prefill" else "token_rows/s"
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": _config(wl, args),
-        "cpu_baseline": {"value": rate, "unit": unit, "cores": cores, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": _cpu_line(rate, unit, desc),
         "e2e": {"value": rate, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -523,6 +544,23 @@ def run_gpu(args, wl, rank, world, local_rank):
     if dist:
         dist.barrier()
     total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), dist, dev)
+
+    # ---- the same K steps issued eagerly (the step's calls one by one from
+    # the host, each crossing the C ABI), L2 flushed before each
+    step.drop_graph()
+    csa.prof_disable()
+    ev_e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush_l2()
+        ev_e[i][0].record(stream)
+        step.run()
+        ev_e[i][1].record(stream)
+    torch.cuda.synchronize()
+    eager_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev_e), dist, dev)
     ms_per_step = total_ms / args.steps
     value = whole_job_rate(units, world, args.steps, total_ms)
     status = int(step.status.item())
@@ -560,8 +598,6 @@ def run_gpu(args, wl, rank, world, local_rank):
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ee), dist, dev)
     e2e_value = whole_job_rate(units, world, args.steps, e2e_ms)
     step_e.drop_graph()
-    step.drop_graph()
-    csa.prof_disable()  # the graph recorded these events: released after its last replay
 
     # ---- roofline of the dominant kernel
     peaks = _peaks()
@@ -593,6 +629,9 @@ def run_gpu(args, wl, rank, world, local_rank):
             "data": "synthetic", "config": _config(wl, args), "roofline": roof,
             "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": bi,
                     "d2h_bytes_per_step": bo},
+            "eager": {"value": whole_job_rate(units, world, args.steps, eager_ms), "unit": unit,
+                      "ms_per_step": eager_ms / args.steps,
+                      "how": "the step's calls issued one by one through the C ABI, no graph"},
             "gpu_launches": launches, "launches_per_step": launches_per_step,
             "clocks": clk.summary(), "wall_s": wall, "device_status": status,
             "per_kernel_ms": {k: v["ms_per_launch"] * v["launches_per_step"]
@@ -610,7 +649,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="serving_decode")
+    ap.add_argument("--workload", default="million_decode")
     ap.add_argument("--ref-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -633,8 +672,7 @@ def main(argv=None):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         rate, desc, _ = oracle_sample(wl, budget_s=args.ref_budget)
-        cpu = {"value": rate, "unit": "tokens/s" if spec.mode == "prefill" else "token_rows/s",
-               "cores": _oracle_cores(), "kind": "oracle", "sample": desc}
+        cpu = _cpu_line(rate, "tokens/s" if spec.mode == "prefill" else "token_rows/s", desc)
     res = run_gpu(args, wl, rank, world, local_rank)
     if rank == 0:
         res["cpu_baseline"] = cpu

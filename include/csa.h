@@ -55,7 +55,7 @@ typedef enum {
   CSA_ERR_INVALID_ARG = 1, /* a null pointer, a bad size or a misaligned pointer */
   CSA_ERR_UNSUPPORTED = 2, /* a shape this library does not implement */
   CSA_ERR_CUDA = 3,        /* a CUDA launch or runtime error */
-  CSA_ERR_TIMEOUT = 4      /* reserved: a bounded device wait gave up */
+  CSA_ERR_TIMEOUT = 4      /* a bounded wait gave up (device waits report CSA_DEV_TIMEOUT) */
 } csa_status_t;
 
 /* bits OR-ed into *status_dev by the kernels */
@@ -63,7 +63,7 @@ typedef enum {
 #define CSA_DEV_BAD_POS 0x2u    /* a window position >= kv_len, or a bad request id */
 #define CSA_DEV_BAD_INDEX 0x4u  /* a top-k entry outside [0, visible count) */
 #define CSA_DEV_POS_GE_CAP 0x8u /* a position >= rope_cap (rotation skipped) */
-#define CSA_DEV_TIMEOUT 0x10u   /* reserved */
+#define CSA_DEV_TIMEOUT 0x10u   /* a bounded device wait gave up; the call's outputs are invalid */
 
 #define CSA_BLOCK 128    /* rows per page */
 #define CSA_ROPE_DIM 64  /* rotated channels (the last 64) */
@@ -344,8 +344,10 @@ CSA_API csa_status_t csa_index_topk(csa_index_args *args, csa_stream_t stream);
  * entries (max_blocks * 128 <= 8192) and, unless the caller passes its own
  * `scores` buffer, n_rows * max_blocks * 128 <= CSA_NOALLOC_MAX_SCORES; larger
  * calls return CSA_ERR_UNSUPPORTED and launch nothing.
- * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  Every
+ * Every call looks up the array's device address in the current device's
+ * context (cudaGetSymbolAddress, a host-side lookup); the first call on a
+ * device may also load the library's device code there, so make that first
+ * call before any stream capture.  Every
  * call on a device shares the array, so calls that overlap on the GPU (two
  * streams, or two threads) race and must be serialised by the caller.  The
  * array keeps the previous call's scores; nothing in it has to start at zero,

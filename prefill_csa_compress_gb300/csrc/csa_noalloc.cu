@@ -1,8 +1,6 @@
 // csa_index_topk_noalloc: the indexer top-k for callers that cannot allocate
 // device memory (see include/csa.h).  Its score scratch is a file-scope device
 // array shared by every call on a device.
-#include <mutex>
-
 #include "csa_internal.cuh"
 
 namespace {
@@ -15,21 +13,14 @@ constexpr size_t kMaxScores = CSA_NOALLOC_MAX_SCORES;
 // comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) float g_noalloc_scores[kMaxScores];
 
-std::mutex g_mu;
-float *g_ptr[64] = {};
-
-// Device address of the scratch array on the current device, looked up once
-// per device (with that device current).  Returns nullptr on failure.
+// Device address of the scratch array in the current device's context.  The
+// lookup runs on every call (a host-side table lookup once the module is
+// loaded), so a context that was reset or replaced never gets a stale
+// address.  Returns nullptr on failure.
 float *scratch_for_current_device() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_ptr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scores) != cudaSuccess || !p) return nullptr;
-    g_ptr[dev] = static_cast<float *>(p);
-  }
-  return g_ptr[dev];
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scores) != cudaSuccess || !p) return nullptr;
+  return static_cast<float *>(p);
 }
 
 }  // namespace

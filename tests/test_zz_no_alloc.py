@@ -43,14 +43,22 @@ def _args(t, topk, topk_idx, topk_score, workspace=None, ws_bytes=0):
     return a
 
 
-def test_noalloc_matches_workspace_entry_point_on_two_calls():
+# Calls in a row over the shared scratch array: the later calls see fewer
+# entries per row (and a different row pitch) than the first, so leftover
+# scores past a row's visible count are there to be misread if the kernel
+# ever read them.
+_CALLS = [
+    ("serving_decode", dict(seed=61)),
+    ("tiny_decode", dict(seed=62)),
+    ("serving_decode", dict(ctx=[900, 300, 2000, 129], seed=63)),
+]
+
+
+def test_noalloc_matches_workspace_entry_point_on_calls_in_a_row():
     L = B.lib()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    results = []
-    # two different workloads in a row: the second call runs over the first
-    # call's leftover scratch contents
-    for seed in (61, 62):
-        spec = spec_for("serving_decode", seed=seed)
+    for name, over in _CALLS:
+        spec = spec_for(name, **over)
         t = make_workload(spec).to(DEV)
         k = spec.topk
         ref_idx = torch.full((spec.n_rows, k), -7, dtype=torch.int32, device=DEV)
@@ -65,13 +73,11 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         n = _args(t, k, got_idx, got_sc)
         assert L.csa_index_topk_noalloc(ctypes.byref(n), stream) == B.CSA_OK
         torch.cuda.synchronize()
-        assert torch.equal(got_idx, ref_idx)
+        assert torch.equal(got_idx, ref_idx), name
         tol = SCORE_REL * ref_sc.abs() + 1e-30
         fin = torch.isfinite(ref_sc)
         assert torch.equal(fin, torch.isfinite(got_sc))
         assert bool(((got_sc - ref_sc).abs()[fin] <= tol[fin]).all())
-        results.append(got_idx.cpu())
-    assert not torch.equal(results[0], results[1])
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
