@@ -362,7 +362,8 @@ def page_rows(pool, table_row, logical):
 
 
 def compress(x, kv, w_gate, ape, ratio, positions, row_req, gamma=None, rms_eps=1e-6,
-             rotate=False, rope_cos=None, rope_sin=None, rope_dim=64, out="bf16", overlap=False):
+             rotate=False, rope_cos=None, rope_sin=None, rope_dim=64, out="bf16", overlap=False,
+             trace=None):
     """Gated compression of every complete group of ``ratio`` rows.
 
     ``overlap`` (the ratio-4 overlapping compressor, "Hyper-Parallel ...
@@ -396,6 +397,10 @@ def compress(x, kv, w_gate, ape, ratio, positions, row_req, gamma=None, rms_eps=
     Returns a list of (request, g, values) for bf16, (request, g, codes,
     scale) for int8, or (request, g, packed codes, scale bytes) for the
     low-bit formats, in row order.
+
+    ``trace`` (a list, or None) receives one record per published group with
+    the intermediate values a comparison needs to tell a rounding tie from an
+    error (see ``_publish_group``); the arithmetic is the same either way.
     """
     x, kv, w_gate, ape = as_f64(x), as_f64(kv), as_f64(w_gate), as_f64(ape)
     positions = as_f64(positions).astype(np.int64)
@@ -415,26 +420,42 @@ def compress(x, kv, w_gate, ape, ratio, positions, row_req, gamma=None, rms_eps=
             continue
         pos = np.array([p - n + 1 + j for j in range(n)])
         logits = x[rows] @ w_gate + ape[pos % r]  # [n, D]
+        mag = None
+        if trace is not None:  # sqrt(sum_i (x_i w_id)^2 + ape_d^2) per token and channel
+            mag = np.sqrt((x[rows] ** 2) @ (w_gate ** 2) + ape[pos % r] ** 2)
         results.append(_publish_group(b, p // r, r, logits, kv[rows], gamma, rms_eps, rotate,
-                                      rope_cos, rope_sin, rope_dim, out))
+                                      rope_cos, rope_sin, rope_dim, out, trace, mag))
     return results
 
 
 def _publish_group(b, g, r, logits, kvs, gamma, rms_eps, rotate, rope_cos, rope_sin, rope_dim,
-                   out):
+                   out, trace=None, mag=None):
     """Pool one group from its r gate scores and kv rows ([r, D] each) and
     publish it: the per-channel softmax over the r tokens, BF16 rounding,
-    optional RMSNorm, optional rotation at the group start, BF16 or INT8."""
+    optional RMSNorm, optional rotation at the group start, BF16 or INT8.
+
+    With ``trace`` (a list) a record is appended: b, g, the logits and kv
+    rows, ``mag`` (per token and channel, the root sum of squares of the
+    terms of its logit),
+    ``pooled`` (the pooled value before its BF16 rounding), ``ybf16`` (after
+    it), ``normed`` (the RMSNorm output before its rounding, or None) and
+    ``y`` (the value handed to the publication format)."""
     mx = logits.max(axis=0, keepdims=True)
     e = np.exp(logits - mx)
     w = e / e.sum(axis=0, keepdims=True)
     y = (w * kvs).sum(axis=0)
+    pooled = y
     y = bf16_round(y)
+    ybf16, normed = y, None
     if gamma is not None:
         g_ = as_f64(gamma)
-        y = bf16_round(y / np.sqrt(np.mean(y * y) + rms_eps) * g_)
+        normed = y / np.sqrt(np.mean(y * y) + rms_eps) * g_
+        y = bf16_round(normed)
     if rotate:
         y = rope_rotate(y, g * r, rope_cos, rope_sin, rope_dim)
+    if trace is not None:
+        trace.append(dict(b=b, g=g, logits=logits, kvs=kvs, mag=mag, pooled=pooled, y=y,
+                          ybf16=ybf16, normed=normed, rotated=bool(rotate)))
     if out == "bf16":
         return (b, g, bf16_round(y))
     if out == "fp4_e4m3":
@@ -449,7 +470,7 @@ def _publish_group(b, g, r, logits, kvs, gamma, rms_eps, rotate, rope_cos, rope_
 
 def compress_stateful(x, kv, w_gate, ape, ratio, positions, row_req, state, state_table,
                       gamma=None, rms_eps=1e-6, rotate=False, rope_cos=None, rope_sin=None,
-                      rope_dim=64, out="bf16", overlap=False):
+                      rope_dim=64, out="bf16", overlap=False, trace=None):
     """One chunk of the compressor with its recurrent state ring ("DeepSeek
     V4.1 Flash", "Compressor state ownership").
 
@@ -464,7 +485,8 @@ def compress_stateful(x, kv, w_gate, ape, ratio, positions, row_req, state, stat
     ``state_table[b] < 0`` disables request b (nothing published or written);
     negative positions neither publish nor write.  Returns the published
     groups as compress() does; ``overlap`` widens the windows as there (the
-    ring then needs at least 2 * ratio slots).
+    ring then needs at least 2 * ratio slots); ``trace`` as in compress()
+    (a token taken from the ring has |its stored score| as its ``mag``).
     """
     x, kv, w_gate, ape = as_f64(x), as_f64(kv), as_f64(w_gate), as_f64(ape)
     positions = as_f64(positions).astype(np.int64)
@@ -487,19 +509,24 @@ def compress_stateful(x, kv, w_gate, ape, ratio, positions, row_req, state, stat
         if p % r != r - 1:
             continue
         blk = int(table[b])
-        logits, kvs = [], []
+        logits, kvs, mags = [], [], []
         n = min(p + 1, 2 * r) if overlap else r
         for j in range(n - 1, -1, -1):  # positions p - j, oldest first
             s_ = t - j
             if s_ >= 0 and int(row_req[s_]) == b and int(positions[s_]) == p - j:
                 logits.append(score[s_])
                 kvs.append(kv[s_])
+                if trace is not None:
+                    mags.append(np.sqrt((x[s_] ** 2) @ (w_gate ** 2) + ape[(p - j) % r] ** 2))
             else:
                 slot = state[blk, (p - j) % cap]
                 kvs.append(slot[:D].copy())
                 logits.append(slot[D:].copy())
+                if trace is not None:
+                    mags.append(np.abs(slot[D:]))
         results.append(_publish_group(b, p // r, r, np.stack(logits), np.stack(kvs), gamma,
-                                      rms_eps, rotate, rope_cos, rope_sin, rope_dim, out))
+                                      rms_eps, rotate, rope_cos, rope_sin, rope_dim, out, trace,
+                                      np.stack(mags) if trace is not None else None))
     # writes: the last min(chunk length, cap) rows of each request's chunk
     last_row = {}
     for t in range(T):

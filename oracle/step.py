@@ -43,12 +43,19 @@ def _kv_pools(t, pools):
     return t["kv_pool"], pools["cmp_pool"]
 
 
-def compress_step(t, spec, pools=None):
+def compress_step(t, spec, pools=None, trace=None):
     """Run both compressors over the chunk and publish into (cloned) pools.
     With state rings (``spec.state``) the compressors read and update copies
     of them, returned in pools["state_main"] / pools["state_idx"] (float64).
+    ``trace`` (a dict, or None) receives the compressors' trace records
+    (``trace["main"]``, ``trace["idx"]``, see ``compress``) and their results
+    (``trace["main_out"]``, ``trace["idx_out"]``).
 
     Returns (pools, main_results, idx_results)."""
+    tr_main = tr_idx = None
+    if trace is not None:
+        tr_main = trace.setdefault("main", [])
+        tr_idx = trace.setdefault("idx", [])
     pools = clone_pools(t) if pools is None else pools
     lowbit = _lowbit(t)
     ov = bool(getattr(spec, "overlap", False))
@@ -60,19 +67,21 @@ def compress_step(t, spec, pools=None):
         table = t["state_table"].numpy()
         main = O.compress_stateful(t["kv_raw"], t["kv_raw"], t["w_gate"], t["ape"], spec.ratio,
                                    t["row_pos"], t["row_req"], pools["state_main"], table,
-                                   out=main_out, overlap=ov)
+                                   out=main_out, overlap=ov, trace=tr_main)
         idx = []
         if not spec.dense:  # HCA has no indexer, hence no index-key compressor
             pools["state_idx"] = O.as_f64(t["state_idx"]).copy()
             idx = O.compress_stateful(t["idx_raw"], t["idx_raw"], t["w_gate_i"], t["ape_i"],
                                       spec.ratio, t["row_pos"], t["row_req"], pools["state_idx"],
-                                      table, **idx_kw)
+                                      table, trace=tr_idx, **idx_kw)
     else:
         main = O.compress(t["kv_raw"], t["kv_raw"], t["w_gate"], t["ape"], spec.ratio,
-                          t["row_pos"], t["row_req"], out=main_out, overlap=ov)
+                          t["row_pos"], t["row_req"], out=main_out, overlap=ov, trace=tr_main)
         idx = [] if spec.dense else O.compress(t["idx_raw"], t["idx_raw"], t["w_gate_i"],
                                                  t["ape_i"], spec.ratio, t["row_pos"],
-                                                 t["row_req"], **idx_kw)
+                                                 t["row_req"], trace=tr_idx, **idx_kw)
+    if trace is not None:
+        trace["main_out"], trace["idx_out"] = main, idx
     table = t["cmp_table"].numpy()
     if lowbit:  # packed codes and scale bytes
         for b, g, codes, sb in main:
@@ -133,15 +142,15 @@ def reindex_tensors(t):
     return r
 
 
-def full_step(t, spec, rows=None):
+def full_step(t, spec, rows=None, trace=None):
     """Oracle's own chain: compress -> scores -> top-k -> attention for ``rows``
     (HCA: compress -> attention over every visible compressed entry).  With
     the hierarchical indexer (``spec.n_cand``) the level-one layer also
     selects candidate blocks ("DeepSeek V4.1 Flash", hierarchical indexer)
     and a reindex layer follows: its own scores, top-k inside the candidate
     blocks, attention (entries ``cand``, ``scores2``, ``topk2``, ``out2``,
-    ``lse2``)."""
-    pools, _, _ = compress_step(t, spec)
+    ``lse2``).  ``trace`` is handed to ``compress_step``."""
+    pools, _, _ = compress_step(t, spec, trace=trace)
     rows = range(spec.n_rows) if rows is None else rows
     res = {}
     t2 = reindex_tensors(t) if spec.n_cand else None
