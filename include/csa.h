@@ -10,7 +10,8 @@
  * Conventions shared by every call
  * --------------------------------
  * - All tensors are caller-owned DEVICE pointers, dense and row-major in the
- *   shapes given below (no strides beyond those shapes).  The library keeps no
+ *   shapes given below, except the paged pools, which take explicit strides
+ *   (see "Pool strides").  The library keeps no
  *   pointer after a call returns and allocates no device memory: scratch is
  *   the caller's `workspace`.  Calling with workspace == NULL only stores the
  *   number of bytes the call needs in `workspace_bytes` and returns CSA_OK.
@@ -35,6 +36,16 @@
  * - A row with row_req[t] < 0 is padding: it is neither read nor written
  *   ("DeepSeek-V4.1 native paged runtime": a padding token's batch id is -1).
  * - Every args struct starts with `struct_size`; set it to sizeof(struct).
+ * - Pool strides.  A paged pool [pages, 128, width] may be a view into a
+ *   larger allocation (a cache holding several layers, or several fields
+ *   per row): `*_page_stride` is the byte distance between consecutive
+ *   pages and `*_row_stride` between consecutive rows of a page; a row's
+ *   own bytes are contiguous.  0 means dense (row stride = the row's bytes,
+ *   page stride = 128 row strides); a struct_size that ends before the
+ *   fields means dense.  Strides must be multiples of 16 bytes, a row
+ *   stride at least the row's bytes and a page stride at least 128 row
+ *   strides; otherwise CSA_ERR_INVALID_ARG.  The low-bit cache formats take
+ *   dense pools only (non-zero strides: CSA_ERR_UNSUPPORTED).
  */
 #ifndef CSA_H_
 #define CSA_H_
@@ -208,6 +219,9 @@ typedef struct {
   int32_t state_capacity;
   uint8_t *scale_pool; /* FP4 out modes: scale bytes [n_blocks, 128, d / group] */
   int32_t overlap;     /* 1: each entry pools the previous group too (see above) */
+  int64_t pool_page_stride;  /* cmp_pool (BF16) or idx_pool (INT8), bytes; 0: dense */
+  int64_t pool_row_stride;   /* ditto */
+  int64_t scale_page_stride; /* idx_scale_pool, bytes between pages (rows contiguous); 0: dense */
 } csa_compress_args;
 
 CSA_API csa_status_t csa_compress(csa_compress_args *args, csa_stream_t stream);
@@ -254,7 +268,8 @@ CSA_API csa_status_t csa_compress_pair(csa_compress_args *first, csa_compress_ar
  * row_req, row_pos i32 [n_rows]; n_cmp i32 [n_req]; idx_pool i8
  * [n_blocks, 128, 128]; idx_scale_pool f32 [n_blocks, 128]; cmp_block_table
  * i32 [n_req, max_blocks]; topk_idx i32 [n_rows, topk]; topk_score f32
- * [n_rows, topk] or NULL.  Supported: n_heads == 64, head_dim == 128,
+ * [n_rows, topk] or NULL.  Supported: 1 <= n_heads <= 128 (index heads;
+ * the hierarchical modes below: n_heads <= 64), head_dim == 128,
  * 1 <= topk <= 2048, ratio >= 1.
  *
  * Hierarchical indexer ("DeepSeek V4.1 Flash", model structure and the
@@ -280,6 +295,16 @@ CSA_API csa_status_t csa_compress_pair(csa_compress_args *first, csa_compress_ar
  * and cand_in is set.  A struct_size that ends before `cand_block` (the
  * struct without these fields) turns both off.  csa_index_topk_noalloc
  * returns CSA_ERR_UNSUPPORTED for either mode.
+ *
+ * Bounded waits: the top-k of rows longer than 16384 entries splits each
+ * row over the CTAs of a cooperative launch, which meet at barriers in
+ * global memory.  Each
+ * wait there gives up after wait_limit_ns (0, or a struct_size that ends
+ * before the field: 1 s; negative: at once, without waiting -- a hook for
+ * testing the timeout path); a wait that gives up ORs CSA_DEV_TIMEOUT into
+ * *status_dev and its CTA stops, so the call's outputs are invalid but the
+ * device stays usable.  The call still returns CSA_OK: it does not wait for
+ * the device.
  *
  * Key format: key_fmt CSA_FMT_FP4_E8M0 reads idx_pool as packed E2M1 codes
  * uint8 [n_blocks, 128, 64] with key_scale_pool, CSA_FMT_MXFP8 as E4M3
@@ -324,6 +349,10 @@ typedef struct {
   const int32_t *cand_in;   /* i32 [n_rows, n_cand] or NULL: reindex candidates */
   int32_t key_fmt;          /* csa_cache_fmt_t: CSA_FMT_INT8 (0 reads as INT8), FP4_E8M0 or MXFP8 */
   const uint8_t *key_scale_pool; /* FP4_E8M0, MXFP8: scale bytes [n_blocks, 128, 4] */
+  int64_t wait_limit_ns;    /* bounded device waits: 0 = 1 s, < 0 = give up at once (see above) */
+  int64_t key_page_stride;  /* idx_pool (INT8 or FP8 keys), bytes; 0: dense */
+  int64_t key_row_stride;   /* ditto */
+  int64_t scale_page_stride; /* idx_scale_pool, bytes between pages (rows contiguous); 0: dense */
 } csa_index_args;
 
 CSA_API csa_status_t csa_index_topk(csa_index_args *args, csa_stream_t stream);
@@ -391,7 +420,8 @@ CSA_API csa_status_t csa_index_topk_noalloc(csa_index_args *args, csa_stream_t s
  * [*, 128, 512]; kv_block_table i32 [n_req, kv_max_blocks]; cmp_block_table
  * i32 [n_req, cmp_max_blocks]; kv_len, n_cmp i32 [n_req]; topk_idx i32
  * [n_rows, topk]; sink f32 [n_heads] or NULL; out bf16 [n_rows, n_heads,
- * 512]; lse f32 [n_rows, n_heads] or NULL.  Supported: n_heads == 64,
+ * 512]; lse f32 [n_rows, n_heads] or NULL.  Supported: 1 <= n_heads <= 128
+ * (the kernels work in groups of 64 heads, a group of a row at a time),
  * head_dim == 512, window == 128, topk <= 2048.
  * The decode call splits each row's candidates over the CTAs of a thread-
  * block cluster and merges the partial softmaxes in distributed shared
@@ -450,6 +480,10 @@ typedef struct {
   int32_t cmp_fmt; /* csa_cache_fmt_t: CSA_FMT_BF16 (0) or CSA_FMT_FP4_E4M3 */
   const uint8_t *kv_scale_pool;  /* MXFP8: scale bytes [kv_n_blocks, 128, 16] */
   const uint8_t *cmp_scale_pool; /* FP4_E4M3: scale bytes [cmp_n_blocks, 128, 32] */
+  int64_t kv_page_stride;  /* kv_pool (BF16), bytes; 0: dense (see "Pool strides") */
+  int64_t kv_row_stride;
+  int64_t cmp_page_stride; /* cmp_pool (BF16), bytes; 0: dense */
+  int64_t cmp_row_stride;
 } csa_attn_args;
 
 CSA_API csa_status_t csa_sparse_attn_decode(csa_attn_args *args, csa_stream_t stream);

@@ -48,6 +48,8 @@ class CompressArgs(ctypes.Structure):
         ("workspace_bytes", c_size_t), ("state_cache", c_void_p),
         ("state_block_table", c_void_p), ("n_state_blocks", c_int32),
         ("state_capacity", c_int32), ("scale_pool", c_void_p), ("overlap", c_int32),
+        ("pool_page_stride", ctypes.c_int64), ("pool_row_stride", ctypes.c_int64),
+        ("scale_page_stride", ctypes.c_int64),
     ]
 
 
@@ -64,6 +66,8 @@ class IndexArgs(ctypes.Structure):
         ("status_dev", c_void_p), ("workspace", c_void_p), ("workspace_bytes", c_size_t),
         ("cand_block", c_int32), ("n_cand", c_int32), ("cand_out", c_void_p),
         ("cand_in", c_void_p), ("key_fmt", c_int32), ("key_scale_pool", c_void_p),
+        ("wait_limit_ns", ctypes.c_int64), ("key_page_stride", ctypes.c_int64),
+        ("key_row_stride", ctypes.c_int64), ("scale_page_stride", ctypes.c_int64),
     ]
 
 
@@ -80,7 +84,9 @@ class AttnArgs(ctypes.Structure):
         ("rope_sin", c_void_p), ("rope_cap", c_int32), ("out", c_void_p), ("lse", c_void_p),
         ("status_dev", c_void_p), ("workspace", c_void_p), ("workspace_bytes", c_size_t),
         ("kv_fmt", c_int32), ("cmp_fmt", c_int32), ("kv_scale_pool", c_void_p),
-        ("cmp_scale_pool", c_void_p),
+        ("cmp_scale_pool", c_void_p), ("kv_page_stride", ctypes.c_int64),
+        ("kv_row_stride", ctypes.c_int64), ("cmp_page_stride", ctypes.c_int64),
+        ("cmp_row_stride", ctypes.c_int64),
     ]
 
 
@@ -193,6 +199,32 @@ def _p(t, dtype=None, name="tensor"):
     return t.data_ptr()
 
 
+def _pool(t, dtype, name):
+    """A paged pool [pages, 128, ...] that may be a view into a larger
+    allocation: its pointer and its page and row strides in bytes (each row's
+    own elements contiguous).  A scale pool [pages, 128] must have
+    contiguous rows.  Returns (pointer, page stride, row stride)."""
+    if t is None:
+        return None, 0, 0
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() < 2 or t.shape[1] != 128:
+        raise ValueError(f"{name} must be [pages, 128, ...]")
+    inner = t[0, 0] if t.shape[0] else t
+    if t.shape[0] and t.dim() > 2 and not inner.is_contiguous():
+        raise ValueError(f"{name}: a row's elements must be contiguous")
+    es = t.element_size()
+    if t.dim() == 2:
+        if t.stride(1) != 1:
+            raise ValueError(f"{name}: a page's entries must be contiguous")
+        return t.data_ptr(), t.stride(0) * es, es
+    return t.data_ptr(), t.stride(0) * es, t.stride(1) * es
+
+
 def _stream(stream):
     s = torch.cuda.current_stream() if stream is None else stream
     return c_void_p(s.cuda_stream)
@@ -272,7 +304,8 @@ def _compress_struct(*, x, kv, w_gate, ape, ratio, positions, row_req, block_tab
     a.block_table = _p(block_table, torch.int32, "block_table")
     a.n_req, a.max_blocks = int(block_table.shape[0]), int(block_table.shape[1])
     if a.out_mode == CSA_OUT_BF16:
-        a.cmp_pool = _p(cmp_pool, torch.bfloat16, "cmp_pool")
+        a.cmp_pool, a.pool_page_stride, a.pool_row_stride = _pool(cmp_pool, torch.bfloat16,
+                                                                  "cmp_pool")
         a.n_blocks = int(cmp_pool.shape[0])
     elif out in ("fp4_e4m3", "fp4_e8m0", "mxfp8"):  # codes into cmp_pool, scales into scale_pool
         group = 16 if out == "fp4_e4m3" else 32
@@ -282,8 +315,10 @@ def _compress_struct(*, x, kv, w_gate, ape, ratio, positions, row_req, block_tab
         a.scale_pool = _p(scale_pool, torch.uint8, "scale_pool")
         a.n_blocks = int(cmp_pool.shape[0])
     else:
-        a.idx_pool = _p(idx_pool, torch.int8, "idx_pool")
-        a.idx_scale_pool = _p(idx_scale_pool, torch.float32, "idx_scale_pool")
+        a.idx_pool, a.pool_page_stride, a.pool_row_stride = _pool(idx_pool, torch.int8,
+                                                                  "idx_pool")
+        a.idx_scale_pool, a.scale_page_stride, _ = _pool(idx_scale_pool, torch.float32,
+                                                         "idx_scale_pool")
         a.n_blocks = int(idx_pool.shape[0])
     a.status_dev = _p(status, torch.int32, "status")
     if state_cache is not None:
@@ -334,7 +369,8 @@ def csa_index_topk(*, q_idx, weights, row_req, row_pos, n_cmp, ratio, idx_pool, 
                    cmp_block_table, topk, topk_idx, topk_score=None, scores=None, relu=True,
                    rope_cos=None, rope_sin=None, mode=CSA_MODE_AUTO, status=None,
                    cand_out=None, cand_in=None, cand_block=8, key_scale_pool=None,
-                   key_fmt="fp4", workspace=None, stream=None, prepare=False):
+                   key_fmt="fp4", wait_limit_ns=0, workspace=None, stream=None,
+                   prepare=False):
     """Indexer scores and deterministic top-k (``include/csa.h``: csa_index_topk).
 
     ``cand_out`` (i32 [n_rows, n_cand]) also selects the level-one candidate
@@ -343,7 +379,8 @@ def csa_index_topk(*, q_idx, weights, row_req, row_pos, n_cmp, ratio, idx_pool, 
     keys are low-bit, ``key_fmt`` "fp4" (``idx_pool`` uint8 [blocks, 128, 64]:
     packed E2M1 with E8M0 scales per 32 dims) or "mxfp8" (uint8 [blocks, 128,
     128]: E4M3 with E8M0 scales per 32 dims), and ``idx_scale_pool`` is
-    unused."""
+    unused.  ``wait_limit_ns`` bounds the cooperative top-k's barrier waits
+    (0: the library's default)."""
     a = IndexArgs()
     a.struct_size = ctypes.sizeof(IndexArgs)
     a.n_rows = int(q_idx.shape[0])
@@ -366,8 +403,9 @@ def csa_index_topk(*, q_idx, weights, row_req, row_pos, n_cmp, ratio, idx_pool, 
         a.key_scale_pool = _p(key_scale_pool, torch.uint8, "key_scale_pool")
     else:
         a.key_fmt = CSA_FMT_INT8
-        a.idx_pool = _p(idx_pool, torch.int8, "idx_pool")
-        a.idx_scale_pool = _p(idx_scale_pool, torch.float32, "idx_scale_pool")
+        a.idx_pool, a.key_page_stride, a.key_row_stride = _pool(idx_pool, torch.int8, "idx_pool")
+        a.idx_scale_pool, a.scale_page_stride, _ = _pool(idx_scale_pool, torch.float32,
+                                                         "idx_scale_pool")
     a.cmp_block_table = _p(cmp_block_table, torch.int32, "cmp_block_table")
     a.n_req, a.max_blocks = int(cmp_block_table.shape[0]), int(cmp_block_table.shape[1])
     a.n_blocks = int(idx_pool.shape[0])
@@ -377,6 +415,7 @@ def csa_index_topk(*, q_idx, weights, row_req, row_pos, n_cmp, ratio, idx_pool, 
     a.scores = _p(scores, torch.float32, "scores")
     a.score_cols = int(scores.shape[1]) if scores is not None else 0
     a.status_dev = _p(status, torch.int32, "status")
+    a.wait_limit_ns = int(wait_limit_ns)
     cand = cand_out if cand_out is not None else cand_in
     if cand is not None:
         a.cand_block = int(cand_block)
@@ -453,12 +492,19 @@ def _attn(fn_name, *, q, row_req, row_pos, topk_idx, kv_pool, kv_block_table, kv
     a.cmp_fmt = CSA_FMT_FP4_E4M3 if cmp_lb else CSA_FMT_BF16
     a.kv_scale_pool = _p(kv_scale_pool, torch.uint8, "kv_scale_pool")
     a.cmp_scale_pool = _p(cmp_scale_pool, torch.uint8, "cmp_scale_pool")
-    a.kv_pool = _p(kv_pool, torch.uint8 if kv_lb else torch.bfloat16, "kv_pool")
+    if kv_lb:
+        a.kv_pool = _p(kv_pool, torch.uint8, "kv_pool")
+    else:  # BF16 pools may be strided views
+        a.kv_pool, a.kv_page_stride, a.kv_row_stride = _pool(kv_pool, torch.bfloat16, "kv_pool")
     a.kv_block_table = _p(kv_block_table, torch.int32, "kv_block_table")
     a.kv_max_blocks = int(kv_block_table.shape[1])
     a.kv_n_blocks = int(kv_pool.shape[0])
     a.kv_len = _p(kv_len, torch.int32, "kv_len")
-    a.cmp_pool = _p(cmp_pool, torch.uint8 if cmp_lb else torch.bfloat16, "cmp_pool")
+    if cmp_lb:
+        a.cmp_pool = _p(cmp_pool, torch.uint8, "cmp_pool")
+    else:
+        a.cmp_pool, a.cmp_page_stride, a.cmp_row_stride = _pool(cmp_pool, torch.bfloat16,
+                                                                "cmp_pool")
     a.cmp_block_table = _p(cmp_block_table, torch.int32, "cmp_block_table")
     a.cmp_max_blocks = int(cmp_block_table.shape[1])
     a.cmp_n_blocks = int(cmp_pool.shape[0])

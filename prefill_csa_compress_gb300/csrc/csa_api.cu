@@ -87,6 +87,24 @@ bool index_pointers_ok(const csa_index_args *a) {
   return (m & 15u) == 0;
 }
 
+csa_status_t index_normalize_strides(csa_index_args *a) {
+  if (a->key_fmt == CSA_FMT_FP4_E8M0) {  // packed keys: dense only
+    if (a->key_page_stride || a->key_row_stride || a->scale_page_stride)
+      return CSA_ERR_UNSUPPORTED;
+    a->key_row_stride = kIdxDim / 2;
+    a->key_page_stride = kBlock * a->key_row_stride;
+    a->scale_page_stride = kBlock * 4;
+    return CSA_OK;
+  }
+  if (a->key_fmt == CSA_FMT_MXFP8 && a->scale_page_stride) return CSA_ERR_UNSUPPORTED;
+  if (!normalize_strides(&a->key_page_stride, &a->key_row_stride, kIdxDim))
+    return CSA_ERR_INVALID_ARG;
+  if (a->scale_page_stride == 0) a->scale_page_stride = kBlock * 4;
+  if (a->scale_page_stride % 16 != 0 || a->scale_page_stride < kBlock * 4)
+    return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
 bool index_struct_ok(const csa_index_args *a) {
   return a && a->struct_size >= offsetof(csa_index_args, cand_block);
 }
@@ -108,7 +126,7 @@ csa_status_t check_attn_shape(const csa_attn_args *a) {
   if (!a) return CSA_ERR_INVALID_ARG;
   if (a->n_rows < 0 || a->n_req < 0 || a->topk < 0 || a->topk > CSA_MAX_TOPK)
     return CSA_ERR_INVALID_ARG;
-  if (a->n_heads != kHeads || a->head_dim != kHeadDim || a->window != kWindow)
+  if (a->n_heads < 1 || a->n_heads > kMaxHeads || a->head_dim != kHeadDim || a->window != kWindow)
     return CSA_ERR_UNSUPPORTED;
   if (a->ratio < 1) return CSA_ERR_INVALID_ARG;
   return CSA_OK;
@@ -147,6 +165,15 @@ csa_status_t run_attn(csa_attn_args *user, cudaStream_t s, bool decode) {
   if ((a->kv_fmt != CSA_FMT_BF16 && a->kv_fmt != CSA_FMT_MXFP8) ||
       (a->cmp_fmt != CSA_FMT_BF16 && a->cmp_fmt != CSA_FMT_FP4_E4M3))
     return CSA_ERR_UNSUPPORTED;
+  // pool strides: explicit for BF16 pools, dense for the low-bit formats
+  if ((a->kv_fmt != CSA_FMT_BF16 && (a->kv_page_stride || a->kv_row_stride)) ||
+      (a->cmp_fmt != CSA_FMT_BF16 && (a->cmp_page_stride || a->cmp_row_stride)))
+    return CSA_ERR_UNSUPPORTED;
+  if (!normalize_strides(&a->kv_page_stride, &a->kv_row_stride,
+                         a->kv_fmt == CSA_FMT_BF16 ? 2 * kHeadDim : kHeadDim) ||
+      !normalize_strides(&a->cmp_page_stride, &a->cmp_row_stride,
+                         a->cmp_fmt == CSA_FMT_BF16 ? 2 * kHeadDim : kHeadDim / 2))
+    return CSA_ERR_INVALID_ARG;
   // the prefill call's low-bit pools go through a BF16 arena in the workspace
   const size_t need = decode ? 0 : attn_arena_bytes(*a);
   if (!a->workspace) {
@@ -224,6 +251,18 @@ static csa_status_t check_compress(csa_compress_args *a, bool *size_query) {
       (!a->state_block_table || a->n_state_blocks <= 0 ||
        a->state_capacity < (a->overlap ? 2 : 1) * a->ratio || a->state_capacity > 256))
     return CSA_ERR_INVALID_ARG;
+  // output pool strides: explicit for BF16 and INT8 publication, dense for
+  // the low-bit formats
+  if (a->out_mode == CSA_OUT_BF16 || a->out_mode == CSA_OUT_INT8) {
+    if (!normalize_strides(&a->pool_page_stride, &a->pool_row_stride,
+                           a->out_mode == CSA_OUT_BF16 ? 2 * a->d : a->d))
+      return CSA_ERR_INVALID_ARG;
+    if (a->scale_page_stride == 0) a->scale_page_stride = kBlock * 4;
+    if (a->scale_page_stride % 4 != 0 || a->scale_page_stride < kBlock * 4)
+      return CSA_ERR_INVALID_ARG;
+  } else if (a->pool_page_stride || a->pool_row_stride || a->scale_page_stride) {
+    return CSA_ERR_UNSUPPORTED;
+  }
   return CSA_OK;
 }
 
@@ -308,12 +347,19 @@ IndexLayout index_layout(const csa_index_args &a, bool own_scores) {
 
 CSA_API csa_status_t csa_index_topk(csa_index_args *user, csa_stream_t stream) {
   if (!index_struct_ok(user)) return CSA_ERR_INVALID_ARG;
-  const csa_index_args A = full_index_args(user);
+  csa_index_args A = full_index_args(user);
   const csa_index_args *a = &A;
   if (a->n_rows < 0 || a->n_req < 0) return CSA_ERR_INVALID_ARG;
-  if (a->n_heads != kHeads || a->head_dim != kIdxDim) return CSA_ERR_UNSUPPORTED;
+  {
+    const csa_status_t st = index_normalize_strides(&A);
+    if (st != CSA_OK) return st;
+  }
+  if (a->n_heads < 1 || a->n_heads > kMaxHeads || a->head_dim != kIdxDim)
+    return CSA_ERR_UNSUPPORTED;
   if (a->topk < 1 || a->topk > CSA_MAX_TOPK || a->ratio < 1) return CSA_ERR_INVALID_ARG;
   if (a->max_blocks <= 0) return CSA_ERR_INVALID_ARG;
+  // the hierarchical modes take one 64-head slot per row
+  if (a->n_heads > kHeads && (a->cand_out || a->cand_in)) return CSA_ERR_UNSUPPORTED;
   if (a->key_fmt != 0 && a->key_fmt != CSA_FMT_INT8 && a->key_fmt != CSA_FMT_FP4_E8M0 &&
       a->key_fmt != CSA_FMT_MXFP8)
     return CSA_ERR_UNSUPPORTED;

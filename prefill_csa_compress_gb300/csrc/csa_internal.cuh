@@ -14,7 +14,8 @@ constexpr int kRopeDim = CSA_ROPE_DIM;  // rotated channels
 constexpr int kRopeHalf = kRopeDim / 2;
 constexpr int kHeadDim = 512;           // attention head / KV width
 constexpr int kIdxDim = 128;            // index-key width
-constexpr int kHeads = 64;              // query heads and index heads
+constexpr int kHeads = 64;              // heads per MMA tile (a group of heads)
+constexpr int kMaxHeads = 128;          // query heads and index heads of a call, at most
 constexpr int kWindow = CSA_WINDOW;
 
 // ---------------------------------------------------------------- host side
@@ -25,6 +26,16 @@ void launch_begin(int kernel_id, cudaStream_t s);
 void launch_end(int kernel_id, cudaStream_t s);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// A paged pool's strides in bytes, 0 meaning dense (a row stride of
+// `row_bytes`, a page stride of 128 row strides); false when they are not
+// multiples of 16, the row stride is below the row's bytes or the page
+// stride below 128 row strides.
+inline bool normalize_strides(int64_t *page, int64_t *row, int64_t row_bytes) {
+  if (*row == 0) *row = row_bytes;
+  if (*page == 0) *page = 128 * *row;
+  return *row % 16 == 0 && *page % 16 == 0 && *row >= row_bytes && *page >= 128 * *row;
+}
 
 // Launch a kernel with programmatic dependent launch: it may be scheduled
 // while the previous kernel on the stream finishes, and waits for it in
@@ -105,6 +116,9 @@ csa_index_args full_index_args(const csa_index_args *a);
 bool index_struct_ok(const csa_index_args *a);
 // Pointer, count and alignment checks of a launching index call.
 bool index_pointers_ok(const csa_index_args *a);
+// The key pool's strides made explicit (0: dense); CSA_OK, or the status to
+// return.
+csa_status_t index_normalize_strides(csa_index_args *a);
 bool topk_is_long(int n_cap);
 size_t topk_ws_bytes(int n_rows, int n_cap);
 uint32_t *topk_counters(void *ws, int n_rows, int n_cap);
@@ -151,6 +165,12 @@ __device__ __forceinline__ long long page_row(const int32_t *table, int max_bloc
     return -1;
   }
   return (long long)phys * kBlock + (pos % kBlock);
+}
+
+// Byte offset of pool row `row` (physical page * 128 + row in the page).
+__device__ __forceinline__ long long pool_offset(long long row, long long page_stride,
+                                                 long long row_stride) {
+  return (row >> 7) * page_stride + (row & 127) * row_stride;
 }
 
 // Number of compressed entries visible to a query at position p:

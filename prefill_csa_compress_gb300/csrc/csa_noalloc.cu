@@ -30,11 +30,16 @@ using namespace csa;
 extern "C" CSA_API csa_status_t csa_index_topk_noalloc(csa_index_args *user,
                                                         csa_stream_t stream) {
   if (!index_struct_ok(user)) return CSA_ERR_INVALID_ARG;
-  const csa_index_args A = full_index_args(user);
+  csa_index_args A = full_index_args(user);
   const csa_index_args *a = &A;
   if (a->cand_out || a->cand_in) return CSA_ERR_UNSUPPORTED;
+  {
+    const csa_status_t st = index_normalize_strides(&A);
+    if (st != CSA_OK) return st;
+  }
   if (a->n_rows < 0 || a->n_req < 0) return CSA_ERR_INVALID_ARG;
-  if (a->n_heads != kHeads || a->head_dim != kIdxDim) return CSA_ERR_UNSUPPORTED;
+  if (a->n_heads < 1 || a->n_heads > kMaxHeads || a->head_dim != kIdxDim)
+    return CSA_ERR_UNSUPPORTED;
   if (a->topk < 1 || a->topk > CSA_MAX_TOPK || a->ratio < 1 || a->max_blocks <= 0)
     return CSA_ERR_INVALID_ARG;
   const long long n_cap = (long long)a->max_blocks * kBlock;

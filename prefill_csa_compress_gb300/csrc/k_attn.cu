@@ -59,14 +59,6 @@ __device__ __forceinline__ int chan_lo(uint32_t r, uint32_t S) {
   return 16 * (int)((kHeadDim / 16 * r) / S);
 }
 
-// Bytes of one pool row in the pool's format.
-__device__ __forceinline__ int cmp_row_bytes(const csa_attn_args &a) {
-  return a.cmp_fmt == CSA_FMT_FP4_E4M3 ? kHeadDim / 2 : kHeadDim * 2;
-}
-__device__ __forceinline__ int kv_row_bytes(const csa_attn_args &a) {
-  return a.kv_fmt == CSA_FMT_MXFP8 ? kHeadDim : kHeadDim * 2;
-}
-
 // Pool row of candidate j of row t (its list: top-k entries, then the
 // window), or null when absent; data errors raise their flag.
 __device__ __forceinline__ const uint8_t *candidate_row(const csa_attn_args &a, int t, int b,
@@ -82,7 +74,9 @@ __device__ __forceinline__ const uint8_t *candidate_row(const csa_attn_args &a, 
     }
     const long long row =
         page_row(a.cmp_block_table, a.cmp_max_blocks, a.cmp_n_blocks, b, c, a.status_dev);
-    return row < 0 ? nullptr : static_cast<const uint8_t *>(a.cmp_pool) + row * cmp_row_bytes(a);
+    return row < 0 ? nullptr
+                   : static_cast<const uint8_t *>(a.cmp_pool) +
+                         pool_offset(row, a.cmp_page_stride, a.cmp_row_stride);
   }
   if (j >= a.topk + a.window) return nullptr;
   const int pp = p - a.window + 1 + (j - a.topk);
@@ -93,7 +87,9 @@ __device__ __forceinline__ const uint8_t *candidate_row(const csa_attn_args &a, 
   }
   const long long row =
       page_row(a.kv_block_table, a.kv_max_blocks, a.kv_n_blocks, b, pp, a.status_dev);
-  return row < 0 ? nullptr : static_cast<const uint8_t *>(a.kv_pool) + row * kv_row_bytes(a);
+  return row < 0 ? nullptr
+                 : static_cast<const uint8_t *>(a.kv_pool) +
+                       pool_offset(row, a.kv_page_stride, a.kv_row_stride);
 }
 
 // Gather of tile g when a pool holds a low-bit format ("DeepSeek V4.1 Flash",
@@ -208,7 +204,11 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   tc::griddep_wait();
   tc::griddep_launch_dependents();
 
-  const int t = blockIdx.y;
+  // blockIdx.y = (row, group of 64 heads); heads past n_heads are computed
+  // from padding (their columns are independent of the others) and never stored
+  const int HG = (a.n_heads + kHeads - 1) / kHeads;
+  const int t = blockIdx.y / HG, h_lo = (blockIdx.y % HG) * kHeads;
+  const int nh = min(kHeads, a.n_heads - h_lo);
   const int b = a.row_req[t];
   if (b < 0 || b >= a.n_req) {  // the same for every CTA of the cluster
     if (b >= 0 && tid == 0 && s == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   if (has_tiles && tid == 0) {
     tc::mbar_arrive_expect_tx(&M->q_full, 8 * 8192);
     for (int kc = 0; kc < 8; ++kc)
-      tc::tma_load_2d(Qs + kc * 8192, &qmap, kc * 64, t * kHeads, &M->q_full);
+      tc::tma_load_2d(Qs + kc * 8192, &qmap, kc * 64, t * a.n_heads + h_lo, &M->q_full);
   }
   bool rot = a.rope_cos != nullptr && p >= 0;
   if (rot && p >= a.rope_cap) {
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   if (rot && tid < 2 * kRopeHalf)
     M->rope[tid] = tid < kRopeHalf ? a.rope_cos[(long long)p * kRopeHalf + tid]
                                    : a.rope_sin[(long long)p * kRopeHalf + tid - kRopeHalf];
-  const float sink2 = tid < kHeads && a.sink ? a.sink[tid] * kLog2e : -INFINITY;
+  const float sink2 = tid < nh && a.sink ? a.sink[h_lo + tid] * kLog2e : -INFINITY;
   const int qd = warp & 3, h0 = (warp >> 2) * 32, c = qd * 32 + lane;
   const int sub = lane >> 3, piece = lane & 7;  // gather: rows 32 i + 4 warp + sub, 16-byte piece
   const float sl2 = a.softmax_scale * kLog2e;
@@ -415,8 +415,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
       const float mq = M->m_all[q][h];
       M->m_all[q][h] = mq == -INFINITY ? 0.f : exp2f(mq - mx) * M->l_all[q][h] * inv_L;
     }
-    if (s == 0 && a.lse)
-      a.lse[(long long)t * kHeads + h] = L > 0.f ? (mx + log2f(L)) * kLn2 : -INFINITY;
+    if (s == 0 && a.lse && h < nh)
+      a.lse[(long long)t * a.n_heads + h_lo + h] = L > 0.f ? (mx + log2f(L)) * kLn2 : -INFINITY;
   }
   __syncthreads();
 
@@ -427,7 +427,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     const int d0 = chan_lo(s, S), dn = chan_lo(s + 1, S) - d0;
     const bool inv = a.inv_rope_out && rot;
     const int hb = warp;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + (long long)t * kHeads * kHeadDim;
+    __nv_bfloat16 *out =
+        static_cast<__nv_bfloat16 *>(a.out) + ((long long)t * a.n_heads + h_lo) * kHeadDim;
     for (int dl0 = 0; dl0 < dn; dl0 += 32) {  // the same trip count in every lane
       const int dl = dl0 + lane;
       const bool live = dl < dn;  // dn is a multiple of 16: RoPE pairs live together
@@ -460,7 +461,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
       }
       if (live) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) out[(hb * 8 + i) * kHeadDim + d] = __float2bfloat16_rn(o[i]);
+        for (int i = 0; i < 8; ++i)
+          if (hb * 8 + i < nh) out[(hb * 8 + i) * kHeadDim + d] = __float2bfloat16_rn(o[i]);
       }
     }
   }
@@ -534,7 +536,7 @@ cudaError_t launch_attn_decode(const csa_attn_args &a, cudaStream_t s) {
   if (a.n_rows <= 0) return cudaSuccess;
   CUtensorMap qmap;
   memset(&qmap, 0, sizeof(qmap));
-  if (!encode_rows_map(&qmap, a.q, (long long)a.n_rows * kHeads, kHeads))
+  if (!encode_rows_map(&qmap, a.q, (long long)a.n_rows * a.n_heads, kHeads))
     return cudaErrorInvalidValue;
   cudaError_t e = prepare_kernel();
   if (e != cudaSuccess) return e;
@@ -543,7 +545,8 @@ cudaError_t launch_attn_decode(const csa_attn_args &a, cudaStream_t s) {
   launch_begin(CSA_K_ATTN_DECODE, s);
   const bool lowbit = a.kv_fmt == CSA_FMT_MXFP8 || a.cmp_fmt == CSA_FMT_FP4_E4M3;
   e = launch_kernel(lowbit ? attn_decode_kernel<true> : attn_decode_kernel<false>,
-                    dim3(n_splits, a.n_rows), dim3(AD_THREADS), (size_t)AD_SMEM, s, n_splits, false,
+                    dim3(n_splits, a.n_rows * ((a.n_heads + kHeads - 1) / kHeads)), dim3(AD_THREADS),
+                    (size_t)AD_SMEM, s, n_splits, false,
                     a, tps, qmap);
   launch_end(CSA_K_ATTN_DECODE, s);
   return e != cudaSuccess ? e : cudaGetLastError();

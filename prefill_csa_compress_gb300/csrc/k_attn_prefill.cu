@@ -48,6 +48,7 @@ using namespace attn;
 
 struct ApRow {
   int t, p, b;
+  int h_lo;        // first head of the item's group of 64 heads
   uint32_t tiles;  // bit g: tile g of the row's candidate list is processed
 };
 
@@ -127,13 +128,18 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
   tc::tc_fence_after();
   const uint32_t tmem = M->tmem_base;
 
-  // the rows this CTA serves: t = blockIdx.x + i * gridDim.x with a valid request
-  auto next_row = [&](int t) {
-    for (t += gridDim.x; t < a.n_rows; t += gridDim.x) {
-      const int b = a.row_req[t];
-      if (b >= 0 && b < a.n_req) return t;
+  // The items this CTA serves: w = blockIdx.x + i * gridDim.x, item w being
+  // row w / HG with its group w % HG of 64 heads (heads past n_heads are
+  // computed from padding -- every head's column is independent -- and never
+  // stored), for rows with a valid request.
+  const int HG = (a.n_heads + kHeads - 1) / kHeads;
+  const int n_items = a.n_rows * HG;
+  auto next_row = [&](int w) {
+    for (w += gridDim.x; w < n_items; w += gridDim.x) {
+      const int b = a.row_req[w / HG];
+      if (b >= 0 && b < a.n_req) return w;
     }
-    return a.n_rows;
+    return n_items;
   };
   const int first_row = next_row((int)blockIdx.x - (int)gridDim.x);
 
@@ -141,7 +147,8 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
     // ================================================================ producer
     uint32_t row_it = 0, tile_it = 0, q_loads = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < a.n_rows; t += gridDim.x) {
+    for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+      const int t = w / HG, h_lo = (w % HG) * kHeads;
       const int b = a.row_req[t];
       if (b < 0) continue;
       if (b >= a.n_req) {
@@ -202,8 +209,11 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
           const int j = g0 + 32 * u + lane;
           long long row = -1;
           const void *pool = a.kv_pool;
+          long long ps = a.kv_page_stride, rs = a.kv_row_stride;
           if (j < a.topk) {
             pool = a.cmp_pool;
+            ps = a.cmp_page_stride;
+            rs = a.cmp_row_stride;
             if (c[u] >= 0 && c[u] < V) {
               if (cache_tbl) {
                 const int phys = M->tbl[c[u] / kBlock];
@@ -223,7 +233,9 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
                              a.status_dev);
           }
           M->src[slot][32 * u + lane] =
-              row < 0 ? nullptr : static_cast<const uint16_t *>(pool) + row * kHeadDim;
+              row < 0 ? nullptr
+                      : reinterpret_cast<const uint16_t *>(static_cast<const uint8_t *>(pool) +
+                                                           pool_offset(row, ps, rs));
         }
         tc::mbar_arrive(&M->tab_full[slot]);
         if (mm == tiles) {
@@ -234,10 +246,11 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
             R.t = t;
             R.p = p;
             R.b = b;
+            R.h_lo = h_lo;
             R.tiles = tiles;
             tc::mbar_arrive_expect_tx(&M->q_full, 8 * 8192);
             for (int kc = 0; kc < 8; ++kc)
-              tc::tma_load_2d(Qs + kc * 8192, &qmap, kc * 64, t * kHeads, &M->q_full);
+              tc::tma_load_2d(Qs + kc * 8192, &qmap, kc * 64, t * a.n_heads + h_lo, &M->q_full);
           }
           if (ok) ++q_loads;
           __syncwarp();
@@ -253,7 +266,7 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
     const uint32_t kv = tc::smem_u32(KVs), qq = tc::smem_u32(Qs), pp = tc::smem_u32(Ps);
     uint32_t row_it = 0, tile_it = 0;
     bool ok = true;
-    for (int t = first_row; t < a.n_rows && ok; t = next_row(t)) {
+    for (int t = first_row; t < n_items && ok; t = next_row(t)) {
       ok = __all_sync(0xffffffffu, ap_wait(&M->q_full, row_it & 1, abort, a.status_dev));
       if (!ok) break;
       const uint32_t tiles = M->row[row_it & 1].tiles;
@@ -370,11 +383,11 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
 
     bool valid = false;
     ApRow R_next;
-    if (first_row < a.n_rows) {
+    if (first_row < n_items) {
       valid = gather(0, [] {});
       rope_row(0, R_next);
     }
-    for (int t = first_row; t < a.n_rows && ok; t = next_row(t)) {
+    for (int t = first_row; t < n_items && ok; t = next_row(t)) {
       const ApRow R = R_next;
       bool first = true;
       float lacc = 0.f;  // this warp's partial denominator of head h0 + lane
@@ -390,7 +403,7 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
         // FP32 denominators (this warp's per-head sums of the unrounded
         // probabilities, lane l: head h0 + l) while the next tile is gathered
         auto colsum = [&] { lacc += warp_col_reduce32<false>(x); };
-        const bool more = (mm & (mm - 1)) != 0 || next_row(t) < a.n_rows;
+        const bool more = (mm & (mm - 1)) != 0 || next_row(t) < n_items;
         if (more)
           valid = gather(tile_it + 1, colsum);
         else
@@ -401,7 +414,7 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
       if (!ok) break;
       // the next row's q is rotated before this row's epilogue, so that its
       // first QK^T does not wait for the output stores
-      if (next_row(t) < a.n_rows) {
+      if (next_row(t) < n_items) {
         rope_row(row_it + 1, R_next);
         if (!ok) break;
       }
@@ -411,9 +424,10 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
       if (!ok) break;
       M->red_l[qd][h0 + lane] = lacc;
       tc::bar_sync(AP_BAR, AP_SOFT);
+      const int nh = min(kHeads, a.n_heads - R.h_lo);  // stored heads of this item
       if (qd == 0) {
         const int h = h0 + lane;
-        const float s2 = a.sink ? a.sink[h] * kLog2e : -INFINITY;
+        const float s2 = a.sink && h < nh ? a.sink[R.h_lo + h] * kLog2e : -INFINITY;
         float m = M->st.m[h];
         float l = (M->red_l[0][h] + M->red_l[1][h]) + (M->red_l[2][h] + M->red_l[3][h]);
         if (m == -INFINITY) {
@@ -422,14 +436,16 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
         }
         const float L = (m == -INFINITY) ? 0.f : l + exp2f(s2 - m);
         M->inv_s[h] = L > 0.f ? 1.f / L : 0.f;
-        if (a.lse) a.lse[(long long)R.t * kHeads + h] = L > 0.f ? (m + log2f(L)) * kLn2 : -INFINITY;
+        if (a.lse && h < nh)
+          a.lse[(long long)R.t * a.n_heads + R.h_lo + h] =
+              L > 0.f ? (m + log2f(L)) * kLn2 : -INFINITY;
       }
       tc::bar_sync(AP_BAR, AP_SOFT);
       float inv[32];
       load32(M->inv_s + h0, inv);
       const bool inv_rope = a.inv_rope_out && a.rope_cos != nullptr && R.p >= 0 && R.p < a.rope_cap;
-      __nv_bfloat16 *out =
-          static_cast<__nv_bfloat16 *>(a.out) + (long long)R.t * kHeads * kHeadDim;
+      __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) +
+                           ((long long)R.t * a.n_heads + R.h_lo) * kHeadDim;
       tc::tc_fence_after();
 #pragma unroll 1
       for (int m4 = 0; m4 < 4; ++m4) {
@@ -449,7 +465,7 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
             const float other = __shfl_xor_sync(0xffffffffu, o, 1);
             o = (d & 1) ? (-other * sn + o * cs) : (o * cs + other * sn);
           }
-          out[(h0 + j) * kHeadDim + d] = __float2bfloat16_rn(o);
+          if (h0 + j < nh) out[(h0 + j) * kHeadDim + d] = __float2bfloat16_rn(o);
         }
       }
       tc::tc_fence_before();
@@ -504,7 +520,7 @@ cudaError_t launch_attn_prefill(const csa_attn_args &a, cudaStream_t s) {
   if (a.n_rows <= 0) return cudaSuccess;
   CUtensorMap qmap;
   memset(&qmap, 0, sizeof(qmap));
-  if (!encode_rows_map(&qmap, a.q, (long long)a.n_rows * kHeads, kHeads))
+  if (!encode_rows_map(&qmap, a.q, (long long)a.n_rows * a.n_heads, kHeads))
     return cudaErrorInvalidValue;
   static bool attr[64] = {};
   int dev = 0;
@@ -519,7 +535,8 @@ cudaError_t launch_attn_prefill(const csa_attn_args &a, cudaStream_t s) {
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     sms = 148;
-  const int grid = a.n_rows < sms ? a.n_rows : sms;
+  const long long items = (long long)a.n_rows * ((a.n_heads + kHeads - 1) / kHeads);
+  const int grid = items < sms ? (int)items : sms;
   launch_begin(CSA_K_ATTN_PREFILL, s);
   const cudaError_t e = launch_kernel(attn_prefill_kernel, dim3(grid), dim3(AP_THREADS),
                                       (size_t)AP_SMEM, s, 0, false, a, qmap);

@@ -175,6 +175,21 @@ cudaError_t launch_gate_gemm_tc(const csa_compress_args &a, float *logits, cudaS
                        logits, a.n_rows, a.dx, a.d, xmap, wmap, a.status_dev);
 }
 
+// Output rows of the BF16 and INT8 publications through the pool's strides
+// (bytes; the host makes them explicit), and the row's FP32 scale slot.
+__device__ __forceinline__ __nv_bfloat16 *bf16_out_row(const csa_compress_args &a,
+                                                      long long row) {
+  return reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(a.cmp_pool) +
+                                           pool_offset(row, a.pool_page_stride, a.pool_row_stride));
+}
+__device__ __forceinline__ int8_t *int8_out_row(const csa_compress_args &a, long long row) {
+  return a.idx_pool + pool_offset(row, a.pool_page_stride, a.pool_row_stride);
+}
+__device__ __forceinline__ float *scale_out_slot(const csa_compress_args &a, long long row) {
+  return reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(a.idx_scale_pool) +
+                                   (row >> 7) * a.scale_page_stride + (row & 127) * 4);
+}
+
 // ---------------------------------------------------------------------------
 // Long chunks, pooling: one CTA per row that closes a group (thread = channel)
 // takes the group's logits, softmax over its r rows per channel, the pooled
@@ -366,8 +381,7 @@ __device__ __forceinline__ void pool_row(const csa_compress_args &a,
   }
 
   if (a.out_mode == CSA_OUT_BF16) {
-    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.cmp_pool);
-    dst[dst_row * D + d] = __float2bfloat16_rn(y);
+    bf16_out_row(a, dst_row)[d] = __float2bfloat16_rn(y);
   } else if (a.out_mode == CSA_OUT_FP4_E4M3) {
     publish_fp4<16>(a, dst_row, d, y, true);
   } else if (a.out_mode == CSA_OUT_FP4_E8M0) {
@@ -379,8 +393,8 @@ __device__ __forceinline__ void pool_row(const csa_compress_args &a,
     float scale = fmaxf(amax, 1e-4f) / 127.0f;
     float q = rintf(y / scale);
     q = fminf(fmaxf(q, -127.f), 127.f);
-    a.idx_pool[dst_row * D + d] = static_cast<int8_t>(q);
-    if (d == 0) a.idx_scale_pool[dst_row] = scale;
+    int8_out_row(a, dst_row)[d] = static_cast<int8_t>(q);
+    if (d == 0) *scale_out_slot(a, dst_row) = scale;
   }
 }
 
@@ -536,7 +550,7 @@ __global__ void __launch_bounds__(WP_THREADS)
         }
       }
       if (a.out_mode == CSA_OUT_BF16)
-        static_cast<__nv_bfloat16 *>(a.cmp_pool)[dst_row * D + d] = __float2bfloat16_rn(y);
+        bf16_out_row(a, dst_row)[d] = __float2bfloat16_rn(y);
       else if (a.out_mode == CSA_OUT_FP4_E4M3)
         publish_fp4<16>(a, dst_row, d, y, true);
       else if (a.out_mode == CSA_OUT_FP4_E8M0)
@@ -684,7 +698,7 @@ __device__ __forceinline__ void fused_tail(const csa_compress_args &a, float y, 
     }
   }
   if (a.out_mode == CSA_OUT_BF16) {
-    if (c < COLS) static_cast<__nv_bfloat16 *>(a.cmp_pool)[dst_row * D + d] = __float2bfloat16_rn(y);
+    if (c < COLS) bf16_out_row(a, dst_row)[d] = __float2bfloat16_rn(y);
   } else if (a.out_mode == CSA_OUT_FP4_E4M3) {
     publish_fp4<16>(a, dst_row, d, y, c < COLS);
   } else if (a.out_mode == CSA_OUT_FP4_E8M0) {
@@ -701,9 +715,9 @@ __device__ __forceinline__ void fused_tail(const csa_compress_args &a, float y, 
     const float scale = fmaxf(amax, 1e-4f) / 127.0f;
     if (c < COLS) {
       const float q = fminf(fmaxf(rintf(y / scale), -127.f), 127.f);
-      a.idx_pool[dst_row * D + d] = static_cast<int8_t>(q);
+      int8_out_row(a, dst_row)[d] = static_cast<int8_t>(q);
     }
-    if (tid == 0) a.idx_scale_pool[dst_row] = scale;
+    if (tid == 0) *scale_out_slot(a, dst_row) = scale;
   }
 }
 

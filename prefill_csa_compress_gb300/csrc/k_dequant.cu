@@ -96,12 +96,16 @@ cudaError_t launch_dequant_arena(const csa_attn_args &a, void *ws, csa_attn_args
     if (e != cudaSuccess) return e;
     if (cmp) {
       bf->cmp_pool = arena;
+      bf->cmp_row_stride = 2 * kHeadDim;
+      bf->cmp_page_stride = (long long)kBlock * 2 * kHeadDim;
       bf->cmp_block_table = table;
       bf->cmp_n_blocks = (int)pages;
       bf->cmp_fmt = CSA_FMT_BF16;
       bf->cmp_scale_pool = nullptr;
     } else {
       bf->kv_pool = arena;
+      bf->kv_row_stride = 2 * kHeadDim;
+      bf->kv_page_stride = (long long)kBlock * 2 * kHeadDim;
       bf->kv_block_table = table;
       bf->kv_n_blocks = (int)pages;
       bf->kv_fmt = CSA_FMT_BF16;

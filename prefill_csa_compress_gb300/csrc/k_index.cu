@@ -81,22 +81,27 @@ constexpr int topk_smem_bytes() {
 }
 
 // Barrier of the S CTAs that share a row: the counter only grows, barrier j
-// waits for j*S arrivals.  Waits at most ~1 s; returns false (and flags
-// CSA_DEV_TIMEOUT) when it gives up.
-__device__ bool row_barrier(uint32_t *ctr, uint32_t target, uint32_t *status, int *s_ok) {
+// waits for j*S arrivals.  Waits at most `limit_ns` (0: 1 s; negative: not
+// at all -- a CTA that is not the last to arrive gives up at once); returns
+// false (and flags CSA_DEV_TIMEOUT) when it gives up.
+__device__ bool row_barrier(uint32_t *ctr, uint32_t target, uint32_t *status, int *s_ok,
+                            long long limit_ns) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    atomicAdd(ctr, 1u);
-    const uint64_t t0 = tc::global_ns();
+    const uint32_t arrived = atomicAdd(ctr, 1u) + 1u;
+    const uint64_t lim = limit_ns == 0 ? 1000000000ull : (uint64_t)max(limit_ns, 0ll);
     int ok = 1;
-    while (*reinterpret_cast<volatile uint32_t *>(ctr) < target) {
-      if (tc::global_ns() - t0 > 1000000000ull) {
-        ok = 0;
-        flag(status, CSA_DEV_TIMEOUT);
-        break;
+    if (arrived < target) {
+      const uint64_t t0 = tc::global_ns();
+      while (*reinterpret_cast<volatile uint32_t *>(ctr) < target) {
+        if (limit_ns < 0 || tc::global_ns() - t0 > lim) {
+          ok = 0;
+          flag(status, CSA_DEV_TIMEOUT);
+          break;
+        }
+        __nanosleep(32);
       }
-      __nanosleep(32);
     }
     __threadfence();
     *s_ok = ok;
@@ -299,7 +304,8 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
           r[TK_REC_GT] = (uint32_t)gt22;
         }
       }
-      if (!row_barrier(row_ctl, (uint32_t)((j + 1) * S), a.status_dev, &s_ok)) return;
+      if (!row_barrier(row_ctl, (uint32_t)((j + 1) * S), a.status_dev, &s_ok, a.wait_limit_ns))
+        return;
       for (int i = tid; i < nb; i += NT) hist[i] = __ldcg(&g[i]);
       __syncthreads();
     }

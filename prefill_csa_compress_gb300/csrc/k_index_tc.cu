@@ -169,7 +169,7 @@ __device__ int candidate_prefix(const int32_t *c, int n, int nb, int *s_min, uin
   return nv;
 }
 
-template <int G>
+template <int G, int HS>
 __global__ void __launch_bounds__(IT_THREADS, 1)
     index_score_tc_kernel(csa_index_args a, float *__restrict__ scores, int cols, int n_groups,
                           int chunk_tiles, int units_per_group, uint32_t *zero_ctr,
@@ -221,7 +221,12 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
   // hold 128 candidate entries (128 >> cb_shift blocks) each
   const bool reidx = sel.cand_in != nullptr;
   const int cb = 1 << sel.cb_shift;
-  const int RPG = reidx ? 1 : G;  // rows per group
+  // The G slots of a group (64 MMA columns each) hold 64 heads of one row:
+  // with up to 64 index heads a slot is a row (heads past n_heads are zero
+  // queries with zero weights); with 65..128 heads a row takes two slots,
+  // slot i holding heads 64 (i / RR) .. of row i % RR of the group.
+  constexpr int RR = G / HS;                  // rows per group (HS: slots per row)
+  const int RPG = reidx ? 1 : RR;             // rows per group actually used
   // FP4 index keys ("DeepSeek V4.1 Flash", production cache ABI): packed E2M1
   // with one E8M0 scale per 32 dims, copied linearly and decoded to FP16
   const bool fp4 = a.key_fmt == CSA_FMT_FP4_E8M0;
@@ -246,8 +251,9 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
     int rb[G];
 #pragma unroll
     for (int i = 0; i < G; ++i) {
-      const int t = g * RPG + i;
-      rb[i] = i < RPG && t < a.n_rows ? a.row_req[t] : -1;
+      const int r = i % RR;  // the slot's row in the group
+      const int t = g * RPG + r;
+      rb[i] = r < RPG && t < a.n_rows ? a.row_req[t] : -1;
       if (rb[i] >= a.n_req) {
         if (chunk == 0 && tid == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
         rb[i] = -1;
@@ -267,7 +273,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
       unsigned on_mask = 0;  // rows of this pass
 #pragma unroll
       for (int i = 0; i < G; ++i) {
-        const int t = g * RPG + i;
+        const int t = g * RPG + i % RR;
         int V = 0;
         const bool on = reidx ? i == pi : rb[i] == b;
         if (on) V = min(visible_count(a.row_pos[t], a.ratio, a.n_cmp[b]), n_cap);
@@ -305,21 +311,22 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
         const int bt = warp < W_PROD ? tid : tid - 32;
         for (int e = bt; e < 16 * C::N; e += IT_BUILD) {
           const int n = e / 16, part = (e / 8) % 2, jj = e % 8;
-          const int i = n / kHeads, h = n % kHeads;
-          if ((on_mask >> i) & 1u)
+          const int i = n / kHeads, hq = (i / RR) * kHeads + n % kHeads;  // head of the row
+          if (((on_mask >> i) & 1u) && hq < a.n_heads)
             tc::cp_async16(Bs + part * C::B_CHUNK + n * 128 + ((jj ^ (n & 7)) << 4),
                            static_cast<const uint16_t *>(a.q_idx) +
-                               ((long long)(g * RPG + i) * kHeads + h) * kIdxDim + part * 64 +
-                               jj * 8);
+                               ((long long)(g * RPG + i % RR) * a.n_heads + hq) * kIdxDim +
+                               part * 64 + jj * 8);
         }
         // head weights, row positions and the rows' RoPE table entries
         for (int e = bt; e < G * (kHeads + 64); e += IT_BUILD) {
           const int i = e / (kHeads + 64), f = e % (kHeads + 64);
-          const int t = g * RPG + i;
+          const int t = g * RPG + i % RR;
           if (!((on_mask >> i) & 1u)) continue;
           const int p = a.row_pos[t];
           if (f < kHeads) {
-            Ws[i * kHeads + f] = a.weights[(long long)t * kHeads + f];
+            const int hq = (i / RR) * kHeads + f;
+            Ws[i * kHeads + f] = hq < a.n_heads ? a.weights[(long long)t * a.n_heads + hq] : 0.f;
           } else if (rope && p >= 0 && p < a.rope_cap) {
             const int q = f - kHeads;  // 0..31 cos, 32..63 sin
             Rope[i * 64 + q] = q < 32 ? a.rope_cos[(long long)p * kRopeHalf + q]
@@ -337,7 +344,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
           const bool live = e < 16 * C::N;
           const int n = live ? e / 16 : 0, part = (e / 8) % 2, jj = e % 8;
           const int i = n / kHeads;
-          const bool on = live && ((on_mask >> i) & 1u);
+          const bool on = live && ((on_mask >> i) & 1u) && (i / RR) * kHeads + n % kHeads < a.n_heads;
           uint8_t *d = Bs + part * C::B_CHUNK + n * 128 + ((jj ^ (n & 7)) << 4);
           float x[8];
           float mx = 0.f;
@@ -474,13 +481,13 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
                          &M->st_full[s]);
           } else if (grow >= 0) {
             uint8_t *dst = St + s * C::PAGE + lane * cb * kIdxDim;
-            if constexpr (C::ATMEM)
-              tc::tma_load_2d(dst, &keys_map, 0, (int)grow, &M->st_full[s]);
-            else
-              tc::bulk_g2s(dst, a.idx_pool + grow * kIdxDim, cb * kIdxDim, &M->st_full[s]);
+            tc::tma_load_3d(dst, &keys_map, 0, (int)(grow & (kBlock - 1)), (int)(grow / kBlock),
+                            &M->st_full[s]);
             tc::bulk_g2s(StSc + s * kBlock + lane * cb,
                          fp8 ? static_cast<const void *>(a.key_scale_pool + grow * 4)
-                             : static_cast<const void *>(a.idx_scale_pool + grow),
+                             : static_cast<const void *>(
+                                   reinterpret_cast<const uint8_t *>(a.idx_scale_pool) +
+                                   (grow / kBlock) * a.scale_page_stride + (grow & (kBlock - 1)) * 4),
                          cb * 4, &M->st_full[s]);
           }
         }
@@ -509,16 +516,15 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
                            kBlock * 4, &M->st_full[s]);
             } else if (ok) {
               tc::mbar_arrive_expect_tx(&M->st_full[s], C::PAGE + kBlock * 4);
-              if constexpr (C::ATMEM)  // 128-byte swizzled rows: conflict-free row reads
-                tc::tma_load_2d(St + s * C::PAGE, &keys_map, 0, phys * kBlock, &M->st_full[s]);
-              else
-                tc::bulk_g2s(St + s * C::PAGE, a.idx_pool + (long long)phys * C::PAGE, C::PAGE,
-                             &M->st_full[s]);
+              // one page as a box of the [pages, 128, 128 B] key map (128-byte
+              // swizzled rows for conflict-free row reads when A goes to TMEM)
+              tc::tma_load_3d(St + s * C::PAGE, &keys_map, 0, 0, phys, &M->st_full[s]);
               tc::bulk_g2s(StSc + s * kBlock,
                            fp8 ? static_cast<const void *>(a.key_scale_pool +
                                                            (long long)phys * kBlock * 4)
-                               : static_cast<const void *>(a.idx_scale_pool +
-                                                           (long long)phys * kBlock),
+                               : static_cast<const void *>(
+                                     reinterpret_cast<const uint8_t *>(a.idx_scale_pool) +
+                                     (long long)phys * a.scale_page_stride),
                            kBlock * 4, &M->st_full[s]);
             } else {
               flag(a.status_dev, CSA_DEV_BAD_BLOCK);
@@ -745,7 +751,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
         }
       } else if (warp < W_CONV0) {
         // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 and
-        // the rows i with i % 2 == w / 4
+        // the rows rr with rr % 2 == w / 4 (a row's score sums its slots)
         const int r = (warp & 3) * 32 + lane;  // key within the tile
         const int i0 = warp >> 2;
         for (int k = 0; k < nt; ++k) {
@@ -759,25 +765,31 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
           const bool ok = (M->t_ok[sc] >> (r >> 3)) & 1;
           const float scale = Sc[sc * kBlock + r];
           const int c = (tb + k) * kBlock + r;
+          for (int rr = i0; rr < RR; rr += 2) {
+            if (!M->row_on[rr]) continue;
+            float sum = 0.f;
+#pragma unroll 1
+            for (int sl = 0; sl < HS; ++sl) {
+              const int i = sl * RR + rr;
+              float v[64];
+              tc::tmem_ld64(tmem + ((uint32_t)((warp & 3) * 32) << 16) + C::ACC_COL + q4 * C::N +
+                                i * kHeads,
+                            v);
+              const float4 *w4 = reinterpret_cast<const float4 *>(Ws + i * kHeads);
+              float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int i = i0; i < G; i += 2) {
-            if (!M->row_on[i]) continue;
-            float v[64];
-            tc::tmem_ld64(tmem + ((uint32_t)((warp & 3) * 32) << 16) + C::ACC_COL + q4 * C::N +
-                              i * kHeads,
-                          v);
-            const float4 *w4 = reinterpret_cast<const float4 *>(Ws + i * kHeads);
-            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+              for (int h4 = 0; h4 < 16; ++h4) {
+                const float4 w = w4[h4];
+                float x[4];
 #pragma unroll
-            for (int h4 = 0; h4 < 16; ++h4) {
-              const float4 w = w4[h4];
-              float x[4];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) x[q] = a.relu ? fmaxf(v[4 * h4 + q], 0.f) : v[4 * h4 + q];
-              acc0 = tc::ffma2(make_float2(w.x, w.y), make_float2(x[0], x[1]), acc0);
-              acc1 = tc::ffma2(make_float2(w.z, w.w), make_float2(x[2], x[3]), acc1);
+                for (int q = 0; q < 4; ++q)
+                  x[q] = a.relu ? fmaxf(v[4 * h4 + q], 0.f) : v[4 * h4 + q];
+                acc0 = tc::ffma2(make_float2(w.x, w.y), make_float2(x[0], x[1]), acc0);
+                acc1 = tc::ffma2(make_float2(w.z, w.w), make_float2(x[2], x[3]), acc1);
+              }
+              sum += (acc0.x + acc0.y) + (acc1.x + acc1.y);
             }
-            const float sum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+            const int i = rr;
             const bool vis = c < M->row_V[i];
             const float val = ok ? scale * sum : -INFINITY;
             if (vis) scores[(long long)M->row_t[i] * cols + c] = val;
@@ -825,9 +837,11 @@ int sm_count() {
   return cached[dev];
 }
 
-// Tensor map of the INT8 key pool as a 2D [pages * 128 rows, 128 bytes] array,
-// `box_rows` rows (a page, or one candidate block) per box, 128-byte swizzle.
-bool encode_keys_map(const csa_index_args &a, int box_rows, CUtensorMap *map) {
+// Tensor map of the INT8 (or FP8) key pool as a 3D [pages, 128 rows, 128
+// bytes] array with the pool's page and row strides, `box_rows` rows (a page,
+// or one candidate block) per box; 128-byte swizzle when the converters read
+// rows of a swizzled tile (A in TMEM), none otherwise (a linear tile).
+bool encode_keys_map(const csa_index_args &a, int box_rows, bool swizzle, CUtensorMap *map) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     cudaDriverEntryPointQueryResult q;
@@ -838,37 +852,39 @@ bool encode_keys_map(const csa_index_args &a, int box_rows, CUtensorMap *map) {
       return false;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  const cuuint64_t dims[2] = {(cuuint64_t)kIdxDim, (cuuint64_t)a.n_blocks * kBlock};
-  const cuuint64_t strides[1] = {(cuuint64_t)kIdxDim};
-  const cuuint32_t box[2] = {(cuuint32_t)kIdxDim, (cuuint32_t)box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(a.idx_pool), dims,
-                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  const cuuint64_t dims[3] = {(cuuint64_t)kIdxDim, (cuuint64_t)kBlock, (cuuint64_t)a.n_blocks};
+  const cuuint64_t strides[2] = {(cuuint64_t)a.key_row_stride, (cuuint64_t)a.key_page_stride};
+  const cuuint32_t box[3] = {(cuuint32_t)kIdxDim, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<int8_t *>(a.idx_pool), dims,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int G>
+template <int G, int HS>
 cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, uint32_t *zero_ctr,
                       cudaStream_t s, const ScoreSel &sel) {
   using C = IdxTc<G>;
   const bool reidx = sel.cand_in != nullptr;
   CUtensorMap keys_map;
   memset(&keys_map, 0, sizeof(keys_map));
-  if (C::ATMEM && a.key_fmt != CSA_FMT_FP4_E8M0 &&
-      !encode_keys_map(a, reidx ? 1 << sel.cb_shift : kBlock, &keys_map))
+  if (a.key_fmt != CSA_FMT_FP4_E8M0 &&
+      !encode_keys_map(a, reidx ? 1 << sel.cb_shift : kBlock, C::ATMEM, &keys_map))
     return cudaErrorInvalidValue;
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel<G>,
+    cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel<G, HS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr[dev] = true;
   }
   const int sms = sm_count();
-  const int n_groups = reidx ? a.n_rows : (a.n_rows + G - 1) / G;
+  constexpr int RR = G / HS;
+  const int n_groups = reidx ? a.n_rows : (a.n_rows + RR - 1) / RR;
   // tiles of one row: its pages, or (reindex) its candidate entries / 128
   const int max_tiles =
       reidx ? ((sel.n_cand << sel.cb_shift) + kBlock - 1) / kBlock : a.max_blocks;
@@ -879,7 +895,7 @@ cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, uint32_t
   const long long n_units = (long long)n_groups * upg;
   const int grid = (int)(n_units < sms ? n_units : sms);
   launch_begin(CSA_K_INDEX_SCORE, s);
-  const cudaError_t e = launch_kernel(index_score_tc_kernel<G>, dim3(grid), dim3(IT_THREADS),
+  const cudaError_t e = launch_kernel(index_score_tc_kernel<G, HS>, dim3(grid), dim3(IT_THREADS),
                                       (size_t)C::SMEM, s, 0, false, a, scores, cols, n_groups,
                                       chunk, upg, zero_ctr, keys_map, sel);
   launch_end(CSA_K_INDEX_SCORE, s);
@@ -892,8 +908,11 @@ cudaError_t launch_index_scores(const csa_index_args &a, float *scores, int scor
                                 uint32_t *zero_ctr, cudaStream_t s, const ScoreSel &sel) {
   if (a.n_rows <= 0) return cudaSuccess;
   const bool wide = a.mode == CSA_MODE_PREFILL || (a.mode == CSA_MODE_AUTO && a.n_rows > 64);
-  return wide ? launch_tc<4>(a, scores, score_cols, zero_ctr, s, sel)
-              : launch_tc<2>(a, scores, score_cols, zero_ctr, s, sel);
+  if (a.n_heads > kHeads)  // two 64-head slots per row
+    return wide ? launch_tc<4, 2>(a, scores, score_cols, zero_ctr, s, sel)
+                : launch_tc<2, 2>(a, scores, score_cols, zero_ctr, s, sel);
+  return wide ? launch_tc<4, 1>(a, scores, score_cols, zero_ctr, s, sel)
+              : launch_tc<2, 1>(a, scores, score_cols, zero_ctr, s, sel);
 }
 
 }  // namespace csa

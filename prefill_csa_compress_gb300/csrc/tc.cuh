@@ -92,6 +92,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, 
       : "memory");
 }
 
+// 3D tensor-map load (TMA) of one box, completing on an mbarrier; (x, y, z)
+// are element coordinates of the box's first element.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, int y, int z,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // TMA gather of four rows r0..r3 of a 2D tensor map (whose box is one row
 // high), each one box wide starting at column x, into four consecutive box
 // rows of shared memory; completes on an mbarrier.

@@ -152,8 +152,15 @@ def test_workspace_queries_and_validation(L):
     ia.max_blocks = 2048
     ia.topk = 4096
     assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_ERR_INVALID_ARG
-    ia.topk, ia.n_heads = 512, 32
+    ia.topk = 512
+    for heads, want in ((0, b.CSA_ERR_UNSUPPORTED), (1, b.CSA_OK), (32, b.CSA_OK),
+                        (128, b.CSA_OK), (129, b.CSA_ERR_UNSUPPORTED)):
+        ia.n_heads = heads
+        assert L.csa_index_topk(ctypes.byref(ia), None) == want, heads
+    ia.head_dim = 64
+    ia.n_heads = 64
     assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_ERR_UNSUPPORTED
+    ia.head_dim = 128
 
     # hierarchical indexer: level one adds the block maxima; reindex rows hold
     # n_cand * cand_block candidate entries plus one count per row
@@ -173,6 +180,9 @@ def test_workspace_queries_and_validation(L):
     assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_ERR_INVALID_ARG
     ia.cand_in = None
     assert L.csa_index_topk_noalloc(ctypes.byref(ia), None) == b.CSA_ERR_UNSUPPORTED
+    ia.n_heads = 128  # the hierarchical modes take at most 64 index heads
+    assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_ERR_UNSUPPORTED
+    ia.n_heads = 64
     # a caller built without the hierarchical fields gets neither mode
     ia.struct_size = b.IndexArgs.cand_block.offset
     assert L.csa_index_topk(ctypes.byref(ia), None) == b.CSA_OK
@@ -191,5 +201,11 @@ def test_workspace_queries_and_validation(L):
     aa.workspace_bytes = 123
     assert L.csa_sparse_attn_prefill(ctypes.byref(aa), None) == b.CSA_OK
     assert aa.workspace_bytes == 0
+    for heads, want in ((0, b.CSA_ERR_UNSUPPORTED), (16, b.CSA_OK), (128, b.CSA_OK),
+                        (129, b.CSA_ERR_UNSUPPORTED)):
+        aa.n_heads = heads
+        assert L.csa_sparse_attn_decode(ctypes.byref(aa), None) == want, heads
+        assert L.csa_sparse_attn_prefill(ctypes.byref(aa), None) == want, heads
+    aa.n_heads = 64
     aa.window = 64
     assert L.csa_sparse_attn_decode(ctypes.byref(aa), None) == b.CSA_ERR_UNSUPPORTED

@@ -654,3 +654,62 @@ def test_step_io_graph_with_late_query_copy():
     assert torch.equal(got, ref.out.cpu())
     assert torch.equal(staged.topk_idx, plain.topk_idx)
 
+
+
+# ------------------------------------------------------------------ head counts
+
+
+@pytest.mark.parametrize("heads", [16, 96, 128])
+@pytest.mark.parametrize("prefill", [False, True])
+def test_attention_head_counts(heads, prefill):
+    """1 <= heads <= 128: the kernels work in groups of 64 heads; heads past
+    the count are padding, computed and never stored."""
+    spec = spec_for("serving_decode", heads=heads, topk=256, seed=70 + heads, pad_rows=1)
+    _attn_case(spec, 13, prefill)
+
+
+@pytest.mark.parametrize("idx_heads", [16, 96, 128])
+@pytest.mark.parametrize("prefill", [False, True])
+def test_index_head_counts(idx_heads, prefill):
+    """1 <= index heads <= 128 under both tilings: fewer than 64 are padded with
+    zero queries and weights; above 64 a row's score sums its two 64-head
+    slots."""
+    spec = spec_for("serving_decode", idx_heads=idx_heads, seed=80 + idx_heads, pad_rows=1)
+    wl, t = _load(spec)
+    step = CsaStep(t, spec.ratio, spec.topk, prefill=prefill, compress=False)
+    n_cap = t["cmp_table"].shape[1] * BLOCK
+    scores = torch.full((spec.n_rows, n_cap), float("nan"), device=DEV)
+    step.index(scores=scores)
+    _check_index_rows(wl, t, spec, step, range(spec.n_rows), scores)
+
+
+def test_full_size_step_with_128_heads():
+    """The whole decode step with 128 query heads and 128 index heads."""
+    spec = spec_for("serving_decode", heads=128, idx_heads=128, seed=91)
+    wl, t = _load(spec)
+    step = CsaStep(t, spec.ratio, spec.topk)
+    step.run()
+    torch.cuda.synchronize()
+    assert _status(step) == 0
+    pools, res = OS.full_step(wl.t, spec)
+    sel = step.topk_idx.cpu().numpy()
+    out = step.out.cpu().double().numpy()
+    g, r = [], []
+    for row, rr in res.items():
+        b = int(wl.row_req[row])
+        V = len(rr["scores"])
+        table = wl.cmp_table[b].numpy()
+        keys = O.page_rows(pools["idx_pool"], table, range(V))
+        scl = O.page_rows(pools["idx_scale"], table, range(V))
+        q_rot = _rope_q(wl.t, row)
+        w = O.as_f64(wl.idx_w[row])
+        tol = np.maximum(1e-4 * np.abs(rr["scores"]), score_tolerance(q_rot, w, keys, scl))
+        # keys published differently by the two sides move a score by at most this
+        gk = O.page_rows(t["idx_pool"].cpu(), table, range(V))
+        gs = O.page_rows(t["idx_scale"].cpu(), table, range(V))
+        dk = np.abs(gk * gs[:, None] - keys * scl[:, None])
+        tol += ((dk @ np.abs(q_rot).T) @ np.abs(w)) * 1.001
+        check_topk(sel[row], rr["scores"], tol, spec.topk)
+        g.append(out[row])
+        r.append(OS.attention_row(wl.t, spec, pools, row, sel[row])[0])
+    check_bf16(np.stack(g), np.stack(r), "out")

@@ -203,3 +203,41 @@ def test_ring_compressor_flags_unmapped_destination_and_still_updates_the_ring()
         assert np.array_equal(got_s[..., :d], ref_s[..., :d]), name
         err = np.abs(got_s[..., d:] - ref_s[..., d:])
         assert np.all(err <= 1e-4 * np.maximum(1.0, np.abs(ref_s[..., d:]))), (name, err.max())
+
+
+def test_cooperative_topk_wait_gives_up_and_the_next_call_succeeds():
+    """The bounded barrier wait of the cooperative top-k (rows longer than
+    16384 entries): with wait_limit_ns < 0 every
+    CTA that is not the last to reach a barrier gives up at once, raises
+    CSA_DEV_TIMEOUT and stops; the call returns, the context stays usable and
+    the next call (default limit) selects exactly the (score desc, index asc)
+    top-k of its scores."""
+    spec = spec_for("ratio1_decode", ctx=[40000, 30000], chunk=[2, 2], topk=512, seed=83)
+    wl = make_workload(spec)
+    t = wl.to(DEV)
+    TIMEOUT = 0x10
+    n_cap = t["cmp_table"].shape[1] * BLOCK
+
+    def call(limit):
+        idx = torch.full((spec.n_rows, spec.topk), -7, dtype=torch.int32, device=DEV)
+        sc = torch.full((spec.n_rows, n_cap), float("nan"), device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        csa.csa_index_topk(q_idx=t["q_idx"], weights=t["idx_w"], row_req=t["row_req"],
+                           row_pos=t["row_pos"], n_cmp=t["n_cmp"], ratio=spec.ratio,
+                           idx_pool=t["idx_pool"], idx_scale_pool=t["idx_scale"],
+                           cmp_block_table=t["cmp_table"], topk=spec.topk, topk_idx=idx,
+                           scores=sc, rope_cos=t["rope_cos"], rope_sin=t["rope_sin"],
+                           mode=csa.CSA_MODE_PREFILL, status=st, wait_limit_ns=limit)
+        torch.cuda.synchronize()
+        return idx.cpu().numpy(), sc.cpu().numpy(), int(st.item())
+
+    _, _, st = call(-1)
+    assert st & TIMEOUT
+    got, sc, st = call(0)
+    assert st == 0
+    for row in range(spec.n_rows):
+        b = int(wl.row_req[row])
+        V = O.visible_count(int(wl.row_pos[row]), spec.ratio, int(wl.n_cmp[b]))
+        assert V > 16384
+        mine = np.sort(np.lexsort((np.arange(V), -sc[row, :V].astype(np.float64)))[:spec.topk])
+        assert np.array_equal(got[row], mine)
