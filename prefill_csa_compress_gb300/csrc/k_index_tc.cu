@@ -517,15 +517,17 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
             } else if (ok) {
               tc::mbar_arrive_expect_tx(&M->st_full[s], C::PAGE + kBlock * 4);
               // one page as a box of the [pages, 128, 128 B] key map (128-byte
-              // swizzled rows for conflict-free row reads when A goes to TMEM)
-              tc::tma_load_3d(St + s * C::PAGE, &keys_map, 0, 0, phys, &M->st_full[s]);
-              tc::bulk_g2s(StSc + s * kBlock,
-                           fp8 ? static_cast<const void *>(a.key_scale_pool +
-                                                           (long long)phys * kBlock * 4)
-                               : static_cast<const void *>(
-                                     reinterpret_cast<const uint8_t *>(a.idx_scale_pool) +
-                                     (long long)phys * a.scale_page_stride),
-                           kBlock * 4, &M->st_full[s]);
+              // swizzled rows for conflict-free row reads when A goes to TMEM);
+              // keys and scales are read once: they leave L2 first
+              const uint64_t once = tc::l2_evict_first();
+              tc::tma_load_3d_hint(St + s * C::PAGE, &keys_map, 0, 0, phys, &M->st_full[s], once);
+              tc::bulk_g2s_hint(StSc + s * kBlock,
+                                fp8 ? static_cast<const void *>(a.key_scale_pool +
+                                                                (long long)phys * kBlock * 4)
+                                    : static_cast<const void *>(
+                                          reinterpret_cast<const uint8_t *>(a.idx_scale_pool) +
+                                          (long long)phys * a.scale_page_stride),
+                                kBlock * 4, &M->st_full[s], once);
             } else {
               flag(a.status_dev, CSA_DEV_BAD_BLOCK);
               tc::mbar_arrive(&M->st_full[s]);
@@ -754,6 +756,7 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
         // the rows rr with rr % 2 == w / 4 (a row's score sums its slots)
         const int r = (warp & 3) * 32 + lane;  // key within the tile
         const int i0 = warp >> 2;
+        const uint64_t keep = tc::l2_evict_last();
         for (int k = 0; k < nt; ++k) {
           const uint32_t itk = it + k;
           const int q4 = itk % C::NT, sc = itk % C::NSC;
@@ -792,7 +795,9 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
             const int i = rr;
             const bool vis = c < M->row_V[i];
             const float val = ok ? scale * sum : -INFINITY;
-            if (vis) scores[(long long)M->row_t[i] * cols + c] = val;
+            // scores stay in L2 for the top-k that reads them next, instead of
+            // being written back while the key stream still flows
+            if (vis) tc::st_global_hint(scores + (long long)M->row_t[i] * cols + c, val, keep);
             if (sel.blk) {
               // level one: the maximum over each block's visible entries (a
               // block is cb consecutive lanes)

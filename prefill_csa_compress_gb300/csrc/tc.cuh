@@ -103,6 +103,45 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, 
       : "memory");
 }
 
+// L2 cache policies (createpolicy): data read once, that should not displace
+// anything (evict_first), and data that should stay for a later kernel
+// (evict_last).
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_3d and bulk_g2s with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint(void *dst, const void *tmap, int x, int y, int z,
+                                                 uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)),
+      "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes,
+                                              uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// A 32-bit global store with an L2 cache policy.
+__device__ __forceinline__ void st_global_hint(float *addr, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(addr), "f"(v), "l"(policy)
+               : "memory");
+}
+
 // TMA gather of four rows r0..r3 of a 2D tensor map (whose box is one row
 // high), each one box wide starting at column x, into four consecutive box
 // rows of shared memory; completes on an mbarrier.
