@@ -19,10 +19,10 @@
 //               heads).  Right after handing tile i's P to the MMA they gather
 //               tile i+1 with 16-byte cp.async straight into the
 //               128-byte-swizzled layout (eight lanes per 128-byte row slice,
-//               so each warp request covers whole sectors), all 128 KB in
-//               flight; a 64-channel chunk is refilled as soon as tile i's P.V
-//               has finished reading it, and the MMA starts on each chunk as
-//               it lands.  The running maximum per head only moves (and O^T is
+//               so each warp request covers whole sectors): warps 2m, 2m+1
+//               refill the 128-channel pair m as soon as tile i's P.V has
+//               finished reading it and mark it landed on their own, and the
+//               MMA starts QK^T on each pair as it lands.  The running maximum per head only moves (and O^T is
 //               rescaled in TMEM) when a tile's logits exceed it by more than
 //               2^8; checking that costs one barrier reduction per tile.  FP32
 //               denominators come from a warp reduce-scatter.  At the end of a
@@ -54,7 +54,7 @@ struct ApRow {
 
 struct ApMisc {
   uint64_t q_full, q_rot, q_empty, s_full, p_full, o_full, o_empty, mma_done;
-  uint64_t kv_full[8];
+  uint64_t kv_full[4];   // one per pair of chunks, arrived by the two warps that copy it
   uint64_t kv_empty[4];  // one per pair of chunks (one 128-channel tile of P.V)
   uint64_t tab_full[2];   // the producer filled the tile's address table
   uint64_t tab_empty[2];  // the gatherers have read it
@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
     tc::mbar_init(&M->o_full, 1);
     tc::mbar_init(&M->o_empty, 1);
     tc::mbar_init(&M->mma_done, 1);
-    for (int i = 0; i < 8; ++i) tc::mbar_init(&M->kv_full[i], AP_SOFT);
+    for (int i = 0; i < 4; ++i) tc::mbar_init(&M->kv_full[i], 64);
     for (int i = 0; i < 4; ++i) tc::mbar_init(&M->kv_empty[i], 1);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&M->tab_full[i], 32);
@@ -273,13 +273,24 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
       bool first = true;
       for (uint32_t mm = tiles; mm && ok; mm &= mm - 1) {
         const bool last = (mm & (mm - 1)) == 0;
-        for (int kc = 0; kc < 8; ++kc) {
-          ok = __all_sync(0xffffffffu, ap_wait(&M->kv_full[kc], tile_it & 1, abort, a.status_dev));
-          if (ok && first && kc == 7)
+        // QK^T pair by pair as the gather lands them: wait for the next
+        // chunk pair, take every later pair that has landed as well, and
+        // issue the batch behind one tcgen05 fence (a fence per chunk drains
+        // the MMA pipe and halves its rate).
+        for (int kp = 0; kp < 4 && ok;) {
+          ok = __all_sync(0xffffffffu, ap_wait(&M->kv_full[kp], tile_it & 1, abort, a.status_dev));
+          if (!ok) break;
+          int ke = kp + 1;
+          while (ke < 4 && __all_sync(0xffffffffu, tc::mbar_test_wait(&M->kv_full[ke], tile_it & 1)))
+            ++ke;
+          if (first && ke == 4)  // the row's q, rotated (its last chunk), before chunk 7
             ok = __all_sync(0xffffffffu, ap_wait(&M->q_rot, row_it & 1, abort, a.status_dev));
           if (!ok) break;
           tc::tc_fence_after();
-          issue_qk(tmem, kv, qq, kc);
+          for (; kp < ke; ++kp) {
+            issue_qk(tmem, kv, qq, 2 * kp);
+            issue_qk(tmem, kv, qq, 2 * kp + 1);
+          }
         }
         if (!ok) break;
         tc::mma_commit_elect(&M->s_full);
@@ -314,49 +325,45 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
     const int stid = sw * 32 + lane;        // 0..255
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const float sl2 = a.softmax_scale * kLog2e;
-    // gather: this thread copies 16-byte piece `piece` of rows r = 32 * i +
-    // 4 * sw + sub (i < 4) of every chunk
+    // gather: this thread copies 16-byte piece `piece` of rows
+    // 8 j + 4 (sw & 1) + sub (j < 16) of chunk pair sw / 2
     const int sub = lane >> 3, piece = lane & 7;
     uint32_t row_it = 0, tile_it = 0;
     bool ok = true;
 
-    // Gather tile `it` (its address table in slot it & 1) into the KV buffer;
-    // returns this thread's candidate validity for that tile.  While the
-    // copies fly, `mid()` runs.
+    // Gather tile `it` (its address table in slot it & 1) into the KV buffer.
+    // Warps 2m and 2m+1 of the group copy chunk pair m (channels 128m ..
+    // 128m + 127 of all 128 candidates) as soon as tile it - 1's P.V has
+    // released it, wait for their own copies and mark the pair landed: QK^T
+    // starts on the first pairs while the later ones are still in flight.
+    // Returns this thread's candidate validity for the tile; `mid()` runs
+    // while the copies fly.
     auto gather = [&](uint32_t it, auto &&mid) -> bool {
-      const int slot = it & 1;
+      const int slot = it & 1, grp = sw >> 1;
+      const int r0 = (sw & 1) * 4 + sub;  // this thread's rows: r0 + 8 j
       bool good = ap_wait(&M->tab_full[slot], (it >> 1) & 1, abort, a.status_dev);
-      const uint16_t *src[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) src[i] = M->src[slot][32 * i + 4 * sw + sub];
       const bool my_valid = M->src[slot][c] != nullptr;
+      if (good) good = ap_wait(&M->kv_empty[grp], (it & 1) ^ 1, abort, a.status_dev);
+      if (good) {
+        uint8_t *dst = KVs + 2 * grp * 16384 + r0 * 128 + ((piece ^ r0) << 4);
+#pragma unroll 4
+        for (int j = 0; j < 16; ++j) {
+          const uint16_t *row = M->src[slot][8 * j + r0];
+          const uint16_t *g =
+              row ? row + grp * 128 + piece * 8 : static_cast<const uint16_t *>(a.kv_pool);
+          tc::cp_async16_zfill(dst + j * 1024, g, row != nullptr);
+          tc::cp_async16_zfill(dst + j * 1024 + 16384, row ? g + 64 : g, row != nullptr);
+        }
+      }
+      tc::cp_async_commit();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&M->tab_empty[slot]);
-      for (int kc = 0; kc < 8; ++kc) {
-        if ((kc & 1) == 0 && good)
-          good = ap_wait(&M->kv_empty[kc >> 1], (it & 1) ^ 1, abort, a.status_dev);
-        if (good) {
-          uint8_t *dst = KVs + kc * 16384;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = 32 * i + 4 * sw + sub;
-            const uint16_t *g = src[i] ? src[i] + kc * 64 + piece * 8
-                                       : static_cast<const uint16_t *>(a.kv_pool);
-            tc::cp_async16_zfill(dst + r * 128 + ((piece ^ (r & 7)) << 4), g, src[i] != nullptr);
-          }
-        }
-        tc::cp_async_commit();
-      }
       mid();
-      // chunk kc has landed once at most 7 - kc newer groups are pending
-#define AP_LAND(N)                                      \
-  tc::cp_async_wait<N>();                              \
-  if (good) {                                          \
-    tc::fence_async_shared();                          \
-    tc::mbar_arrive(&M->kv_full[7 - N]);               \
-  }
-      AP_LAND(7) AP_LAND(6) AP_LAND(5) AP_LAND(4) AP_LAND(3) AP_LAND(2) AP_LAND(1) AP_LAND(0)
-#undef AP_LAND
+      tc::cp_async_wait<0>();
+      if (good) {
+        tc::fence_async_shared();
+        tc::mbar_arrive(&M->kv_full[grp]);
+      }
       ok = ok && good;
       return my_valid;
     };
