@@ -101,6 +101,31 @@ __device__ __forceinline__ void load32(const float *src, float (&v)[32]) {
   }
 }
 
+// 2^t on the FMA pipe, for t <= 8 (keeps part of a tile's exponentials off
+// the special-function unit, which bounds the softmax): t = n + f with n the
+// nearest integer and f in [-1/2, 1/2]; 2^f is the degree-4 polynomial that
+// interpolates it at the five Chebyshev nodes of [-1/2, 1/2] (relative error
+// below 4e-6 in FP32 Horner form) and n is added to its exponent.  t is
+// clamped at -125, so results below 2^-125 come out as 2^-125.
+__device__ __forceinline__ float exp2_fma(float t) {
+  t = fmaxf(t, -125.f);
+  const float r = t + 12582912.f;  // 1.5 * 2^23: n in the low mantissa bits of r
+  const float f = t - (r - 12582912.f);
+  float p = 0.00966636837f;
+  p = fmaf(p, f, 0.0559219755f);
+  p = fmaf(p, f, 0.240223497f);
+  p = fmaf(p, f, 0.693121016f);
+  p = fmaf(p, f, 1.f);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(r) << 23));
+}
+
+// 2^t on the special-function unit (PTX ex2.approx.ftz).
+__device__ __forceinline__ float exp2_sfu(float t) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(t));
+  return y;
+}
+
 // Per-head softmax state of a row, in shared memory.
 struct SoftState {
   alignas(16) float m[kHeads];     // running reference per head (log2 domain)
@@ -125,13 +150,19 @@ __device__ __forceinline__ void softmax_vals(uint32_t tmem, uint32_t o_col, int 
   const int lane = threadIdx.x & 31, c = qd * 32 + lane;
   const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) x[j] = valid ? x[j] * sl2 : -INFINITY;
+  for (int j = 0; j < 32; ++j) x[j] *= sl2;
   float mref[32];
   load32(st->m + h0, mref);
   bool exceed = false;
+  if (valid) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) exceed |= x[j] > mref[j] + kRescaleLog2;
+    for (int j = 0; j < 32; ++j) exceed |= x[j] > mref[j] + kRescaleLog2;
+  }
   if (tc::bar_or(bar, 256, exceed)) {
+    if (!valid) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] = -INFINITY;
+    }
     const float mx = warp_col_reduce32<true>(x);
     const int h = h0 + lane;
     st->red[qd][h] = mx;
@@ -176,9 +207,20 @@ __device__ __forceinline__ void softmax_vals(uint32_t tmem, uint32_t o_col, int 
   } else {
     ready();
   }
-  // P = 2^(x - m) as BF16 into the MN-major P^T rows
+  // P = 2^(x - m) as BF16 into the MN-major P^T rows (a valid candidate's
+  // logits are at most m + 2^3 here, and its heads' references are finite:
+  // any finite logit exceeds a reference of -inf); one in four
+  // exponentials on the FMA pipe
+  if (valid) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) x[j] = mref[j] == -INFINITY ? 0.f : exp2f(x[j] - mref[j]);
+    for (int j = 0; j < 32; ++j) {
+      const float t = x[j] - mref[j];
+      x[j] = (j & 3) == 3 ? exp2_fma(t) : exp2_sfu(t);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = 0.f;
+  }
 #pragma unroll
   for (int q = 0; q < 4; ++q)
     *reinterpret_cast<uint4 *>(prow_chunk(Ps, c, (h0 >> 3) + q)) =
