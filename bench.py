@@ -20,6 +20,7 @@ the host cores instead (a bounded sample of the same workload).
 from __future__ import annotations
 
 import argparse
+import glob
 import hashlib
 import json
 import math
@@ -41,36 +42,19 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # kernel reports null.  Values are from `ncu --metrics dram__bytes_read.sum,
 # dram__bytes_write.sum` captures of these same bench workloads.
 NCU_TRAFFIC = {
-    ("serving_decode", "attn_decode"): {"bytes": 4614381, "src": "77022dbcfaf0"},
-    ("serving_decode", "index_topk"): {"bytes": 124843, "src": "2b8bb3a236f3"},
-    ("serving_decode", "index_score"): {"bytes": 1553683, "src": "fcdb94044445"},
-    ("serving_decode", "compress_fused"): {"bytes": 624251, "src": "474e737aae10"},
-    ("million_decode", "index_score"): {"bytes": 143178411, "src": "fcdb94044445"},
-    ("million_decode", "attn_decode"): {"bytes": 17843371, "src": "77022dbcfaf0"},
-    ("million_decode", "index_topk"): {"bytes": 8640085, "src": "2b8bb3a236f3"},
-    ("million_decode", "compress_fused"): {"bytes": 53257, "src": "474e737aae10"},
-    ("hier_decode", "index_score"): {"bytes": 80736009, "src": "fcdb94044445"},
-    ("hier_decode", "index_topk"): {"bytes": 3531112, "src": "2b8bb3a236f3"},
-    ("hier_decode", "attn_decode"): {"bytes": 5365139, "src": "77022dbcfaf0"},
-    ("hier_decode", "compress_fused"): {"bytes": 53077, "src": "474e737aae10"},
-    ("lowbit_decode", "attn_decode"): {"bytes": 2073505, "src": "77022dbcfaf0"},
-    ("lowbit_decode", "index_topk"): {"bytes": 124966, "src": "2b8bb3a236f3"},
-    ("lowbit_decode", "index_score"): {"bytes": 898740, "src": "fcdb94044445"},
-    ("lowbit_decode", "compress_fused"): {"bytes": 624156, "src": "474e737aae10"},
-    ("lowbit_million", "index_score"): {"bytes": 72221459, "src": "fcdb94044445"},
-    ("lowbit_million", "attn_decode"): {"bytes": 7184090, "src": "77022dbcfaf0"},
-    ("lowbit_million", "index_topk"): {"bytes": 8641214, "src": "2b8bb3a236f3"},
-    ("lowbit_million", "compress_fused"): {"bytes": 52916, "src": "474e737aae10"},
-    ("chunked_prefill", "attn_prefill"): {"bytes": 1058926612, "src": "96ab4a6b48bb"},
-    ("chunked_prefill", "index_score"): {"bytes": 149808794, "src": "fcdb94044445"},
-    ("chunked_prefill", "index_topk"): {"bytes": 34506793, "src": "2b8bb3a236f3"},
-    ("chunked_prefill", "compress_pool"): {"bytes": 16097080, "src": "474e737aae10"},
-    ("chunked_prefill", "compress_gate"): {"bytes": 5534019, "src": "474e737aae10"},
-    ("overlap_decode", "attn_decode"): {"bytes": 4260608, "src": "77022dbcfaf0"},
-    ("overlap_decode", "compress_fused"): {"bytes": 778145, "src": "474e737aae10"},
-    ("overlap_decode", "index_topk"): {"bytes": 84983, "src": "2b8bb3a236f3"},
-    ("overlap_decode", "index_score"): {"bytes": 876402, "src": "fcdb94044445"},
-    ("overlap_decode", "compress_pool"): {"bytes": 40761, "src": "474e737aae10"},
+    # dram__bytes_read.sum + dram__bytes_write.sum of one launch (one-kernel ncu
+    # captures, profiles/dram_traffic.md), keyed by the kernel's source hash
+    ("tiny_decode", "attn_decode"): {"bytes": 560380, "src": "249bf1d9da5c"},
+    ("tiny_decode", "index_score"): {"bytes": 166656, "src": "5126a7266c48"},
+    ("serving_decode", "attn_decode"): {"bytes": 4611840, "src": "249bf1d9da5c"},
+    ("serving_decode", "index_score"): {"bytes": 1556992, "src": "5126a7266c48"},
+    ("ratio1_decode", "index_score"): {"bytes": 70001664, "src": "5126a7266c48"},
+    ("ratio1_decode", "index_topk"): {"bytes": 4443648, "src": "1cddedc9778d"},
+    ("million_decode", "index_score"): {"bytes": 142582016, "src": "5126a7266c48"},
+    ("million_decode", "attn_decode"): {"bytes": 17850624, "src": "249bf1d9da5c"},
+    ("million_decode", "index_topk"): {"bytes": 8639232, "src": "1cddedc9778d"},
+    ("chunked_prefill", "attn_prefill"): {"bytes": 1061655040, "src": "1bf26f9923e9"},
+    ("chunked_prefill", "index_score"): {"bytes": 153969152, "src": "5126a7266c48"},
 }
 
 
@@ -420,11 +404,16 @@ def _config(wl, args):
 
 
 def _src_sha(name):
-    path = os.path.join(ROOT, "prefill_csa_compress_gb300", "csrc", name)
+    """Hash of a kernel's source file and of every shared header it may
+    include: a stored traffic figure counts only while both are unchanged."""
+    csrc = os.path.join(ROOT, "prefill_csa_compress_gb300", "csrc")
+    h = hashlib.sha1()
     try:
-        return hashlib.sha1(open(path, "rb").read()).hexdigest()[:12]
+        for path in [os.path.join(csrc, name)] + sorted(glob.glob(os.path.join(csrc, "*.cuh"))):
+            h.update(open(path, "rb").read())
     except OSError:
         return None
+    return h.hexdigest()[:12]
 
 
 KERNEL_SRC = {"index_score": "k_index_tc.cu", "index_topk": "k_index.cu",

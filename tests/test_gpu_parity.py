@@ -309,8 +309,12 @@ def test_index_topk_prefill_full_size_sampled():
 
 
 def _attn_case(spec, sel_seed, prefill, rows=None, use_sink=True, inv_rope_out=False,
-               softmax_scale=None, shrink_first=0):
-    if shrink_first:
+               softmax_scale=None, shrink_first=0, sink_values=None):
+    if sink_values is not None:
+        wl = make_workload(spec)
+        wl.t["sink"] = torch.tensor(sink_values, dtype=torch.float32)
+        t = wl.to(DEV)
+    elif shrink_first:
         # a fresh workload whose first `shrink_first` compressed entries are
         # scaled down 16x: the first candidate tile then has far smaller logits
         # than the later ones and the running maximum must move
@@ -393,8 +397,17 @@ def test_attention_large_logits_move_the_running_max(prefill):
                         seed=55), 12, prefill, softmax_scale=0.15, shrink_first=200)
 
 
-def test_attention_without_sink():
-    _attn_case(spec_for("serving_decode", topk=64, seed=53), 8, False, use_sink=False)
+@pytest.mark.parametrize("prefill", [False, True])
+def test_attention_without_sink(prefill):
+    _attn_case(spec_for("serving_decode", topk=64, seed=53), 8, prefill, use_sink=False)
+
+
+@pytest.mark.parametrize("prefill", [False, True])
+def test_attention_extreme_sinks(prefill):
+    # sinks far above the logits (the sink carries nearly all the weight), far
+    # below them, -inf (plain softmax) and ordinary values, head by head
+    vals = [40.0, -40.0, -np.inf, 0.0, 12.0, -12.0, 3.0, -3.0] * 8
+    _attn_case(spec_for("serving_decode", topk=200, seed=56), 13, prefill, sink_values=vals)
 
 
 @pytest.mark.parametrize("name", ["ratio1_decode", "million_decode"])
