@@ -423,13 +423,19 @@ CSA_API csa_status_t csa_index_topk_noalloc(csa_index_args *args, csa_stream_t s
  * 512]; lse f32 [n_rows, n_heads] or NULL.  Supported: 1 <= n_heads <= 128
  * (the kernels work in groups of 64 heads, a group of a row at a time),
  * head_dim == 512, window == 128, topk <= 2048.
- * The decode call splits each row's candidates over the CTAs of a thread-
- * block cluster and merges the partial softmaxes in distributed shared
- * memory; the prefill call is tiled for many rows.  With BF16 pools neither
- * needs a workspace (the size query returns 0; a workspace passed in is
- * unused, but a non-null pointer is what makes the call launch); the
- * prefill call with a low-bit pool needs the arena below.  Both compute the
- * same function.
+ * The decode call splits each row's candidates over up to 17 CTAs (one per
+ * 128-candidate tile while the whole grid fits one CTA per SM) and merges the
+ * partial softmaxes through its workspace: per (row, group of 64 heads) and
+ * split, 64 KB of BF16 partial output and 512 bytes of statistics, plus two
+ * 32-bit counters per (row, head group) at the end.  The counters must read
+ * zero before the workspace's first decode call; every call that completes
+ * leaves them at zero (a call that raised CSA_DEV_TIMEOUT may not: zero them
+ * again).  Counters that do not start at zero make the call's wait run out
+ * and raise CSA_DEV_TIMEOUT rather than pass early.  The workspace must be
+ * 256-byte aligned.  The prefill call is tiled for many rows; with BF16 pools
+ * it needs no workspace (the size query returns 0; a workspace passed in is
+ * unused, but a non-null pointer is what makes the call launch) and with a
+ * low-bit pool it needs the arena below.  Both compute the same function.
  *
  * Low-bit caches (see csa_cache_fmt_t): kv_fmt CSA_FMT_MXFP8 reads kv_pool
  * as uint8 [*, 128, 512] with kv_scale_pool; cmp_fmt CSA_FMT_FP4_E4M3 reads

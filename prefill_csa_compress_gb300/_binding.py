@@ -257,7 +257,8 @@ def _run(fn_name, args, workspace, stream, device, prepare=False):
         raise CsaError(fn_name, st)
     need = int(args.workspace_bytes)
     if workspace is None or workspace.numel() < need:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        # zero-filled: the decode attention's split counters must start at zero
+        workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=device)
     args.workspace = workspace.data_ptr()
     args.workspace_bytes = workspace.numel()
     call = PreparedCall(fn_name, args, workspace)

@@ -174,8 +174,9 @@ csa_status_t run_attn(csa_attn_args *user, cudaStream_t s, bool decode) {
       !normalize_strides(&a->cmp_page_stride, &a->cmp_row_stride,
                          a->cmp_fmt == CSA_FMT_BF16 ? 2 * kHeadDim : kHeadDim / 2))
     return CSA_ERR_INVALID_ARG;
-  // the prefill call's low-bit pools go through a BF16 arena in the workspace
-  const size_t need = decode ? 0 : attn_arena_bytes(*a);
+  // the decode call merges its split partials through the workspace; the
+  // prefill call's low-bit pools go through a BF16 arena in it
+  const size_t need = decode ? attn_decode_workspace(*a) : attn_arena_bytes(*a);
   if (!a->workspace) {
     user->workspace_bytes = need;
     return CSA_OK;

@@ -134,6 +134,7 @@ cudaError_t launch_attn_prefill(const csa_attn_args &a, cudaStream_t s);
 // Decode attention (k_attn.cu): a row's candidate tiles split over the CTAs
 // of one cluster, merged in distributed shared memory.
 void attn_decode_geometry(const csa_attn_args &a, int *n_splits, int *tiles_per_split);
+size_t attn_decode_workspace(const csa_attn_args &a);
 cudaError_t launch_attn_decode(const csa_attn_args &a, cudaStream_t s);
 
 // ---------------------------------------------------------------- device side

@@ -1,28 +1,26 @@
 // Decode shared-KV sparse attention with an attention sink, the candidates of
-// a row split over the CTAs of one thread-block cluster.  Candidates of a
-// query row are its selected compressed entries followed by its raw causal
-// window; each candidate row is both key and value.
+// a row split over several CTAs.  Candidates of a query row are its selected
+// compressed entries followed by its raw causal window; each candidate row is
+// both key and value.
 //
 // Source: "Hyper-Parallel ... DeepSeek V4 CP" (gitcode issue #2),
 // "二阶段 CP 总体算法" (Stage-2 sparse attention with sinks, softmax_scale,
 // ori_win_left = 127; outputs out and lse), "9.1" (candidate list = window KV
 // and selected compressed KV) and "7. Window KV Halo" (window includes self).
 //
-// GB300 mapping.  A row's 128-candidate tiles are dealt to the S CTAs of a
-// cluster (S <= 16, one CTA per SM).  Each CTA loads the row's q with TMA while
-// it gathers its first tile with cp.async (q and the gather overlap), runs the
-// tile's two contractions on tcgen05 (see attn_common.cuh) and a softmax whose
-// running maximum only moves past a 2^8 growth.  The partial softmaxes merge
-// through distributed shared memory: every CTA sends its per-head maximum and
-// denominator to all CTAs, and its O^T / l as BF16 straight from registers
-// into the shared memory of the CTA that owns those output channels (32
-// lanes store 512 contiguous bytes); the owners' tile buffers receive, so the
-// sends wait at a split cluster barrier until every CTA's last P.V is done
-// (the partial is read out of TMEM and packed meanwhile).  After a second
-// barrier each owner weighs the S contributions of its channels and writes
-// them out.  No partial reaches HBM and no second kernel runs.  Barrier
-// initialisation and the tensor-memory allocation run before the kernel
-// waits for its predecessor in the stream.
+// GB300 mapping.  A row's 128-candidate tiles are dealt to S CTAs (one tile
+// each while the grid fits one CTA per SM, S <= 17).  Each CTA loads the row's
+// q with TMA while it gathers its first tile with cp.async (q and the gather
+// overlap), runs the tile's two contractions on tcgen05 (see attn_common.cuh)
+// and a softmax whose running maximum only moves past a 2^8 growth.  The
+// partial softmaxes merge through the workspace (L2): every CTA stores its
+// O^T / l as BF16 (512 contiguous bytes per warp store) with its per-head
+// maximum and denominator, the S CTAs of the row meet at a counter (bounded
+// wait; the grid fits the GPU, so all of them are resident), and each then
+// weighs the S partials of its own slice of the output channels and writes
+// it.  Barrier initialisation and the tensor-memory allocation run before the
+// kernel waits for its predecessor in the stream.
+#include <algorithm>
 #include <cstring>
 
 #include "attn_common.cuh"
@@ -35,16 +33,16 @@ using namespace attn;
 
 constexpr int AD_THREADS = 256;
 constexpr int AD_BAR = 1;  // named barrier over all 256 threads (the softmax's)
-constexpr int AD_MAX_CLUSTER = 16;
+constexpr int AD_MAX_SPLITS = 17;  // (topk <= 2048 + window 128) / 128 tiles
 
 struct AdMisc {
   uint64_t q_full, mma_bar, done_bar;
   uint32_t tmem_base;
-  int pad;
+  int flag;
   SoftState st;
   const uint8_t *src[CT];   // pool row of each candidate of the tile, or null
-  alignas(16) float m_all[AD_MAX_CLUSTER][kHeads];  // every CTA's reference per head (log2)
-  alignas(16) float l_all[AD_MAX_CLUSTER][kHeads];  // every CTA's denominator per head
+  alignas(16) float w[AD_MAX_SPLITS][kHeads];   // references, then merge weights, per partial
+  alignas(16) float lq[AD_MAX_SPLITS][kHeads];  // denominators per partial
   alignas(16) float red_l[4][kHeads];
   alignas(16) float f_self[kHeads];       // this CTA's share of each head's output
   alignas(16) float rope[2 * kRopeHalf];  // cos, sin at the row's position
@@ -57,6 +55,66 @@ static_assert(AD_SMEM <= 227 * 1024, "shared memory");
 // sector and RoPE pairs stay together.
 __device__ __forceinline__ int chan_lo(uint32_t r, uint32_t S) {
   return 16 * (int)((kHeadDim / 16 * r) / S);
+}
+
+// Workspace of a call with `items` (row, group of 64 heads) pairs split S
+// ways: the BF16 partials (8 head groups x 512 channels of 16-byte units per
+// split), the per-head reference and denominator of each split, and two
+// counters per item (arrivals, departures), which must read zero before the
+// first call and are left at zero by every call that completes.
+struct AdWs {
+  uint4 *part;
+  float *stat;
+  uint32_t *ctr;
+};
+__host__ __device__ __forceinline__ long long ad_ws_bytes(long long items, long long S) {
+  return items * S * (8 * kHeadDim * 16 + 2 * kHeads * 4) + items * 8;
+}
+__device__ __forceinline__ AdWs ad_ws(void *ws, long long items, long long S) {
+  uint8_t *b = static_cast<uint8_t *>(ws);
+  AdWs w;
+  w.part = reinterpret_cast<uint4 *>(b);
+  w.stat = reinterpret_cast<float *>(b + items * S * (8 * kHeadDim * 16));
+  w.ctr = reinterpret_cast<uint32_t *>(b + items * S * (8 * kHeadDim * 16 + 2 * kHeads * 4));
+  return w;
+}
+
+// The S CTAs of an item meet once their partials are in the workspace:
+// thread 0 counts this CTA in (after a release fence) and waits, at most a
+// second, until the count equals S exactly (a counter that did not start at
+// zero makes the wait run out rather than pass early); false, with
+// CSA_DEV_TIMEOUT flagged, when it gives up.
+__device__ bool split_barrier(uint32_t *ctr, uint32_t S, uint32_t *status, int *s_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    int ok = 1;
+    if (atomicAdd(ctr, 1u) + 1u != S) {
+      const uint64_t t0 = tc::global_ns();
+      while (*reinterpret_cast<volatile uint32_t *>(ctr) != S) {
+        if (tc::global_ns() - t0 > 1000000000ull) {
+          ok = 0;
+          flag(status, CSA_DEV_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __threadfence();
+    *s_flag = ok;
+  }
+  __syncthreads();
+  return *s_flag != 0;
+}
+
+// Counts this CTA out; the last of the S to leave (every one has passed the
+// barrier) puts both counters back to zero for the next call.
+__device__ __forceinline__ void split_depart(uint32_t *ctr, uint32_t S) {
+  __syncthreads();
+  if (threadIdx.x == 0 && atomicAdd(ctr + 1, 1u) + 1u == S) {
+    ctr[0] = 0u;
+    ctr[1] = 0u;
+    __threadfence();
+  }
 }
 
 // Pool row of candidate j of row t (its list: top-k entries, then the
@@ -183,7 +241,7 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   uint8_t *Ps = sm + OFF_P;
   AdMisc *M = reinterpret_cast<AdMisc *>(sm + OFF_MISC);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t s = cluster_rank(), S = gridDim.x;
+  const uint32_t s = blockIdx.x, S = gridDim.x;
 
   // ---- set-up that reads no global memory, overlapping the previous kernel
   if (tid == 0) {
@@ -193,9 +251,6 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     tc::mbar_fence_init();
   }
   if (tid < kHeads) M->st.m[tid] = -INFINITY;
-  // every CTA of the cluster must have started before any of them touches a
-  // peer's shared memory: the matching wait comes before the first remote store
-  cluster_arrive_relaxed();
   if (warp == 0) tc::tmem_alloc(&M->tmem_base, TMEM_COLS);
   tc::tc_fence_before();
   __syncthreads();
@@ -210,9 +265,8 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
   const int t = blockIdx.y / HG, h_lo = (blockIdx.y % HG) * kHeads;
   const int nh = min(kHeads, a.n_heads - h_lo);
   const int b = a.row_req[t];
-  if (b < 0 || b >= a.n_req) {  // the same for every CTA of the cluster
+  if (b < 0 || b >= a.n_req) {  // the same for every CTA of the item: none waits
     if (b >= 0 && tid == 0 && s == 0) flag(a.status_dev, CSA_DEV_BAD_POS);
-    cluster_wait();
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -239,11 +293,13 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     rot = false;
     if (tid == 0 && s == 0) flag(a.status_dev, CSA_DEV_POS_GE_CAP);
   }
-  // the row's RoPE entries and the sink logit of head tid, read up front
+  // the row's RoPE entries and the sink logit of head tid % 64, read up front
+  const float sink_h = (tid & (kHeads - 1)) < nh && a.sink
+                           ? a.sink[h_lo + (tid & (kHeads - 1))] * kLog2e
+                           : -INFINITY;
   if (rot && tid < 2 * kRopeHalf)
     M->rope[tid] = tid < kRopeHalf ? a.rope_cos[(long long)p * kRopeHalf + tid]
                                    : a.rope_sin[(long long)p * kRopeHalf + tid - kRopeHalf];
-  const float sink2 = tid < nh && a.sink ? a.sink[h_lo + tid] * kLog2e : -INFINITY;
   const int qd = warp & 3, h0 = (warp >> 2) * 32, c = qd * 32 + lane;
   const int sub = lane >> 3, piece = lane & 7;  // gather: rows 32 i + 4 warp + sub, 16-byte piece
   const float sl2 = a.softmax_scale * kLog2e;
@@ -263,14 +319,15 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
       const uint8_t *src[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) src[i] = M->src[32 * i + 4 * warp + sub];
-      for (int kc = 0; kc < 8; ++kc) {
-        uint8_t *dst = KVs + kc * 16384;
+      // a candidate row's eight 128-byte pieces are requested back to back
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = 32 * i + 4 * warp + sub;
+      for (int i = 0; i < 4; ++i) {
+        const int r = 32 * i + 4 * warp + sub;
+        uint8_t *dst = KVs + r * 128 + ((piece ^ (r & 7)) << 4);
+        for (int kc = 0; kc < 8; ++kc) {
           const uint8_t *gsrc = src[i] ? src[i] + kc * 128 + piece * 16
                                        : static_cast<const uint8_t *>(a.kv_pool);
-          tc::cp_async16_zfill(dst + r * 128 + ((piece ^ (r & 7)) << 4), gsrc, src[i] != nullptr);
+          tc::cp_async16_zfill(dst + kc * 16384, gsrc, src[i] != nullptr);
         }
       }
     }
@@ -324,42 +381,29 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     tc::mbar_wait(&M->done_bar, 0, 100000000ull);
   }
 
-  // ---- this CTA's partial to the owners of its output channels, with its
-  // per-head reference and denominator to every CTA.  The partial travels as
-  // BF16 O^T / l (normalised by this CTA's own denominator, so BF16 keeps it
-  // to 2^-9 relative whatever the magnitudes); at owner r, 16-byte element
-  // (sender, hb, d - chan_lo(r)) holds heads 8 hb .. 8 hb + 7 of channel d,
-  // so the 32 lanes of a warp (32 consecutive channels) store 512
-  // contiguous bytes.  The owners receive in their tile buffer, which is
-  // free once they have arrived at the first cluster barrier below (after
-  // their last P.V); the partial is read out of TMEM and packed meanwhile.
+  // ---- this CTA's partial into the workspace: O^T / l as BF16 (normalised
+  // by this CTA's own denominator, so BF16 keeps it to 2^-9 relative whatever
+  // the magnitudes), 16-byte unit (hb, d) holding heads 8 hb .. 8 hb + 7 of
+  // channel d (the 32 lanes of a warp store 512 contiguous bytes), and its
+  // per-head reference and denominator.
+  const AdWs W = ad_ws(a.workspace, gridDim.y, S);
+  uint4 *part = W.part + ((long long)blockIdx.y * S + s) * (8 * kHeadDim);
+  float *stat = W.stat + ((long long)blockIdx.y * S + s) * (2 * kHeads);
   M->red_l[qd][h0 + lane] = lacc;
   __syncthreads();
   if (tid < kHeads) {
     const float l = (M->red_l[0][tid] + M->red_l[1][tid]) + (M->red_l[2][tid] + M->red_l[3][tid]);
     M->f_self[tid] = !first && l > 0.f ? 1.f / l : 0.f;
+    stat[tid] = first ? -INFINITY : M->st.m[tid];
+    stat[kHeads + tid] = first ? 0.f : l;
   }
-  cluster_wait();  // every CTA of the cluster is running
-  for (int e = tid; e < kHeads * (int)S; e += AD_THREADS) {
-    const int h = e % kHeads;
-    const uint32_t q = e / kHeads;
-    const float m = first ? -INFINITY : M->st.m[h];
-    const float l =
-        first ? 0.f : (M->red_l[0][h] + M->red_l[1][h]) + (M->red_l[2][h] + M->red_l[3][h]);
-    st_peer_f32(peer_addr(&M->m_all[s][h], q), m);
-    st_peer_f32(peer_addr(&M->l_all[s][h], q), l);
-  }
-  tc::tc_fence_before();
-  cluster_arrive();  // this CTA's tile buffer may now receive
   __syncthreads();
-  const int rows_max = 16 * (int)((kHeadDim / 16 + S - 1) / S);  // channels per owner, at most
-  uint4 pk[4][4];  // [m4][group of 8 heads]
   {
     float f[32];
     load32(M->f_self + h0, f);
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     tc::tc_fence_after();
-#pragma unroll
+#pragma unroll 1
     for (int m4 = 0; m4 < 4; ++m4) {
       float v[32];
       if (first) {
@@ -368,54 +412,74 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
       } else {
         tc::tmem_ld32(tmem + lane_off + O_COL + m4 * 64 + h0, v);
       }
-#pragma unroll
-      for (int cgrp = 0; cgrp < 4; ++cgrp) {
-        pk[m4][cgrp].x = pack2(v[8 * cgrp + 0] * f[8 * cgrp + 0], v[8 * cgrp + 1] * f[8 * cgrp + 1]);
-        pk[m4][cgrp].y = pack2(v[8 * cgrp + 2] * f[8 * cgrp + 2], v[8 * cgrp + 3] * f[8 * cgrp + 3]);
-        pk[m4][cgrp].z = pack2(v[8 * cgrp + 4] * f[8 * cgrp + 4], v[8 * cgrp + 5] * f[8 * cgrp + 5]);
-        pk[m4][cgrp].w = pack2(v[8 * cgrp + 6] * f[8 * cgrp + 6], v[8 * cgrp + 7] * f[8 * cgrp + 7]);
-      }
-    }
-  }
-  cluster_wait_acquire();  // every CTA's tile buffer is free; statistics have landed
-  {
-    const uint32_t recv = tc::smem_u32(KVs);
-#pragma unroll
-    for (int m4 = 0; m4 < 4; ++m4) {
       const int d = m4 * 128 + qd * 32 + lane;
-      uint32_t r = (uint32_t)(((d >> 4) * (int)S) / (kHeadDim / 16));
-      if (r + 1 < S && chan_lo(r + 1, S) <= d) ++r;
-      const int dl = d - chan_lo(r, S);
-      const uint32_t base = peer_addr_u32(recv, r);
 #pragma unroll
       for (int cgrp = 0; cgrp < 4; ++cgrp) {
         const int hb = (h0 >> 3) + cgrp;
-        st_peer_v4(base + (uint32_t)((((int)s * 8 + hb) * rows_max + dl) * 16), pk[m4][cgrp]);
+        part[hb * kHeadDim + d] =
+            make_uint4(pack2(v[8 * cgrp + 0] * f[8 * cgrp + 0], v[8 * cgrp + 1] * f[8 * cgrp + 1]),
+                       pack2(v[8 * cgrp + 2] * f[8 * cgrp + 2], v[8 * cgrp + 3] * f[8 * cgrp + 3]),
+                       pack2(v[8 * cgrp + 4] * f[8 * cgrp + 4], v[8 * cgrp + 5] * f[8 * cgrp + 5]),
+                       pack2(v[8 * cgrp + 6] * f[8 * cgrp + 6], v[8 * cgrp + 7] * f[8 * cgrp + 7]));
       }
     }
   }
-  cluster_sync();  // the partials have landed; nothing remote follows
 
-  // ---- merge weights: each head's maximum and denominator over the S CTAs;
-  // m_all[q][h] becomes the weight of CTA q's partial
-  if (tid < kHeads) {
-    const int h = tid;
-    float mx = sink2;
-    for (uint32_t q = 0; q < S; ++q) mx = fmaxf(mx, M->m_all[q][h]);
-    float L = 0.f;
-    if (mx != -INFINITY) {
-      L = exp2f(sink2 - mx);
-      for (uint32_t q = 0; q < S; ++q) {
-        const float mq = M->m_all[q][h];
-        L += mq == -INFINITY ? 0.f : exp2f(mq - mx) * M->l_all[q][h];
+  // ---- the S CTAs of the row meet: every partial is in the workspace
+  ok = split_barrier(W.ctr + 2 * blockIdx.y, S, a.status_dev, &M->flag) && ok;
+
+  // ---- merge weights: every partial's statistics into shared memory at once
+  // (independent loads), then each head's maximum and denominator over the S
+  // partials (thread = (head, quarter of the partials)); w[q][h] becomes the
+  // weight of partial q
+  {
+    constexpr int PER = (AD_MAX_SPLITS * 2 * kHeads + AD_THREADS - 1) / AD_THREADS;
+    const float *st_row = W.stat + (long long)blockIdx.y * S * (2 * kHeads);
+    const int n_st = (int)S * 2 * kHeads;
+    float v[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int e = tid + u * AD_THREADS;
+      v[u] = e < n_st && ok ? __ldcg(st_row + e) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int e = tid + u * AD_THREADS;
+      if (e < n_st) {
+        const int q = e / (2 * kHeads), k = e % (2 * kHeads);
+        if (k < kHeads)
+          M->w[q][k] = ok ? v[u] : -INFINITY;
+        else
+          M->lq[q][k - kHeads] = v[u];
       }
     }
+  }
+  __syncthreads();
+  {
+    const int h = tid & (kHeads - 1), jq = tid >> 6;
+    float mx = -INFINITY;
+    for (uint32_t q = jq; q < S; q += 4) mx = fmaxf(mx, M->w[q][h]);
+    M->red_l[jq][h] = mx;
+    __syncthreads();
+    mx = fmaxf(fmaxf(M->red_l[0][h], M->red_l[1][h]), fmaxf(M->red_l[2][h], M->red_l[3][h]));
+    const float s2 = sink_h;
+    mx = fmaxf(mx, s2);
+    float part_l = 0.f;
+    if (mx != -INFINITY)
+      for (uint32_t q = jq; q < S; q += 4) {
+        const float mq = M->w[q][h];
+        const float e = mq == -INFINITY ? 0.f : exp2_sfu(mq - mx) * M->lq[q][h];
+        M->w[q][h] = e;
+        part_l += e;
+      }
+    __syncthreads();
+    M->red_l[jq][h] = part_l;
+    __syncthreads();
+    float L = (M->red_l[0][h] + M->red_l[1][h]) + (M->red_l[2][h] + M->red_l[3][h]);
+    if (mx != -INFINITY) L += exp2_sfu(s2 - mx);
     const float inv_L = L > 0.f ? 1.f / L : 0.f;
-    for (uint32_t q = 0; q < S; ++q) {
-      const float mq = M->m_all[q][h];
-      M->m_all[q][h] = mq == -INFINITY ? 0.f : exp2f(mq - mx) * M->l_all[q][h] * inv_L;
-    }
-    if (s == 0 && a.lse && h < nh)
+    for (uint32_t q = jq; q < S; q += 4) M->w[q][h] = mx == -INFINITY ? 0.f : M->w[q][h] * inv_L;
+    if (jq == 0 && s == 0 && a.lse && h < nh)
       a.lse[(long long)t * a.n_heads + h_lo + h] = L > 0.f ? (mx + log2f(L)) * kLn2 : -INFINITY;
   }
   __syncthreads();
@@ -427,26 +491,33 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
     const int d0 = chan_lo(s, S), dn = chan_lo(s + 1, S) - d0;
     const bool inv = a.inv_rope_out && rot;
     const int hb = warp;
+    const uint4 *parts = W.part + (long long)blockIdx.y * S * (8 * kHeadDim) + hb * kHeadDim;
     __nv_bfloat16 *out =
         static_cast<__nv_bfloat16 *>(a.out) + ((long long)t * a.n_heads + h_lo) * kHeadDim;
     for (int dl0 = 0; dl0 < dn; dl0 += 32) {  // the same trip count in every lane
       const int dl = dl0 + lane;
       const bool live = dl < dn;  // dn is a multiple of 16: RoPE pairs live together
+      const int d = d0 + (live ? dl : 0);
       float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (uint32_t q = 0; q < S && live; ++q) {
-        const float4 w0 = *reinterpret_cast<const float4 *>(&M->m_all[q][hb * 8]);
-        const float4 w1 = *reinterpret_cast<const float4 *>(&M->m_all[q][hb * 8 + 4]);
+      // every partial's unit requested before any is used (one L2 round trip)
+      uint4 v[AD_MAX_SPLITS];
+#pragma unroll
+      for (int u = 0; u < AD_MAX_SPLITS; ++u)
+        v[u] = u < (int)S ? __ldcg(parts + (long long)u * (8 * kHeadDim) + d)
+                          : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < AD_MAX_SPLITS; ++u) {
+        if (u >= (int)S) break;
+        const float4 w0 = *reinterpret_cast<const float4 *>(&M->w[u][hb * 8]);
+        const float4 w1 = *reinterpret_cast<const float4 *>(&M->w[u][hb * 8 + 4]);
         const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        const uint4 v =
-            *reinterpret_cast<const uint4 *>(KVs + (((int)q * 8 + hb) * rows_max + dl) * 16);
-        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t wd[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           o[2 * i] = fmaf(wv[2 * i], __uint_as_float(wd[i] << 16), o[2 * i]);
           o[2 * i + 1] = fmaf(wv[2 * i + 1], __uint_as_float(wd[i] & 0xFFFF0000u), o[2 * i + 1]);
         }
       }
-      const int d = d0 + dl;
       if (inv) {
         // inverse rotation of the RoPE channel pairs (partner: the neighbouring lane)
 #pragma unroll
@@ -459,51 +530,18 @@ __global__ void __launch_bounds__(AD_THREADS, 1)
           }
         }
       }
-      if (live) {
+      if (live && ok) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           if (hb * 8 + i < nh) out[(hb * 8 + i) * kHeadDim + d] = __float2bfloat16_rn(o[i]);
       }
     }
   }
+  split_depart(W.ctr + 2 * blockIdx.y, S);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
-}
-
-// Largest cluster the decode kernel may use on this device (16 where the
-// device schedules it, else the portable 8).
-int max_cluster() {
-  static int cached[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return 8;
-  if (!cached[dev]) {
-    int best = 8;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(16, 1, 1);
-    cfg.blockDim = dim3(AD_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = AD_SMEM;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 16;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaFuncSetAttribute(attn_decode_kernel<false>,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-        cudaFuncSetAttribute(attn_decode_kernel<true>,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-        cudaOccupancyMaxActiveClusters(&n, attn_decode_kernel<false>, &cfg) == cudaSuccess &&
-        n > 0)
-      best = 16;
-    cudaGetLastError();  // a refused query leaves no error behind
-    cached[dev] = best;
-  }
-  return cached[dev];
 }
 
 // Opt the kernel into its shared memory, once per device.
@@ -524,12 +562,31 @@ cudaError_t prepare_kernel() {
 
 }  // namespace
 
+// Splits per (row, head group): as many CTAs as the row has tiles while the
+// whole grid fits one CTA per SM (its CTAs wait for one another, so all of a
+// row's must be resident at once); with more items than SMs, one CTA per item.
 void attn_decode_geometry(const csa_attn_args &a, int *n_splits, int *tiles_per_split) {
   const int tiles = (a.topk + a.window + CT - 1) / CT;
-  const int mc = prepare_kernel() == cudaSuccess ? max_cluster() : 8;
-  const int tps = (tiles + mc - 1) / mc;
+  const long long items = (long long)a.n_rows * ((a.n_heads + kHeads - 1) / kHeads);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();  // no device (a size query on a host without one): one split
+    sms = 1;
+  }
+  const long long fit = items > 0 ? sms / items : 1;
+  const int S = (int)std::max(1ll, std::min<long long>(tiles, fit));
+  const int tps = (tiles + S - 1) / S;
   *tiles_per_split = tps;
   *n_splits = (tiles + tps - 1) / tps;
+}
+
+size_t attn_decode_workspace(const csa_attn_args &a) {
+  if (a.n_rows <= 0) return 0;
+  int S = 1, tps = 1;
+  attn_decode_geometry(a, &S, &tps);
+  const long long items = (long long)a.n_rows * ((a.n_heads + kHeads - 1) / kHeads);
+  return (size_t)ad_ws_bytes(items, S);
 }
 
 cudaError_t launch_attn_decode(const csa_attn_args &a, cudaStream_t s) {
@@ -546,8 +603,7 @@ cudaError_t launch_attn_decode(const csa_attn_args &a, cudaStream_t s) {
   const bool lowbit = a.kv_fmt == CSA_FMT_MXFP8 || a.cmp_fmt == CSA_FMT_FP4_E4M3;
   e = launch_kernel(lowbit ? attn_decode_kernel<true> : attn_decode_kernel<false>,
                     dim3(n_splits, a.n_rows * ((a.n_heads + kHeads - 1) / kHeads)), dim3(AD_THREADS),
-                    (size_t)AD_SMEM, s, n_splits, false,
-                    a, tps, qmap);
+                    (size_t)AD_SMEM, s, 0, false, a, tps, qmap);
   launch_end(CSA_K_ATTN_DECODE, s);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -193,11 +193,17 @@ def test_workspace_queries_and_validation(L):
     aa = b.AttnArgs()
     aa.struct_size = ctypes.sizeof(aa)
     aa.n_rows, aa.n_heads, aa.head_dim, aa.ratio, aa.topk, aa.window = 8, 64, 512, 4, 2048, 128
-    # both attention calls keep their scratch on chip (the decode split merges
-    # in distributed shared memory): no workspace
+    # the decode call merges its split partials through the workspace: per
+    # (row, head group) and split 64 KB of partials and 512 bytes of statistics,
+    # plus two counters per (row, head group); the split count depends on the
+    # device's SM count (one split without a device), at most 17 here
     aa.workspace_bytes = 123
     assert L.csa_sparse_attn_decode(ctypes.byref(aa), None) == b.CSA_OK
-    assert aa.workspace_bytes == 0
+    items = 8
+    per_split = items * (8 * 512 * 16 + 2 * 64 * 4)
+    rest = aa.workspace_bytes - items * 8
+    assert rest > 0 and rest % per_split == 0 and 1 <= rest // per_split <= 17
+    # the BF16 prefill call keeps its scratch on chip: no workspace
     aa.workspace_bytes = 123
     assert L.csa_sparse_attn_prefill(ctypes.byref(aa), None) == b.CSA_OK
     assert aa.workspace_bytes == 0

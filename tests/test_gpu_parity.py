@@ -21,6 +21,7 @@ if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 import prefill_csa_compress_gb300 as csa  # noqa: E402
+import prefill_csa_compress_gb300._binding as B  # noqa: E402
 from prefill_csa_compress_gb300.pipeline import CsaStep  # noqa: E402
 
 DEV = torch.device("cuda:0")
@@ -726,3 +727,66 @@ def test_full_size_step_with_128_heads():
         g.append(out[row])
         r.append(OS.attention_row(wl.t, spec, pools, row, sel[row])[0])
     check_bf16(np.stack(g), np.stack(r), "out")
+
+
+# ------------------------------------------------------------------ decode split merge
+
+
+def _decode_attn_call(spec, t, step, sel, ws=None):
+    return csa.csa_sparse_attn_decode(
+        q=t["q"], row_req=t["row_req"], row_pos=t["row_pos"], topk_idx=sel,
+        kv_pool=t["kv_pool"], kv_block_table=t["kv_table"], kv_len=t["kv_len"],
+        cmp_pool=t["cmp_pool"], cmp_block_table=t["cmp_table"], n_cmp=t["n_cmp"],
+        ratio=spec.ratio, out=step.out, lse=step.lse, sink=t["sink"], rope_cos=t["rope_cos"],
+        rope_sin=t["rope_sin"], status=step.status, workspace=ws)
+
+
+@pytest.mark.parametrize("name", ["serving_decode", "million_decode"])
+def test_decode_merge_repeats_bit_exactly_on_one_workspace(name):
+    # the split counters put themselves back to zero: later calls on the same
+    # workspace see the same partials meet and give the same bits
+    spec = spec_for(name)
+    wl, t = _load(spec)
+    limits = [O.visible_count(int(wl.row_pos[i]), spec.ratio, int(wl.n_cmp[int(wl.row_req[i])]))
+              for i in range(spec.n_rows)]
+    sel = random_selection(limits, spec.topk, 21).to(DEV)
+    step = CsaStep(t, spec.ratio, spec.topk, compress=False)
+    ws = _decode_attn_call(spec, t, step, sel)
+    torch.cuda.synchronize()
+    assert _status(step) == 0
+    ref_out, ref_lse = step.out.clone(), step.lse.clone()
+    for _ in range(3):
+        step.out.zero_()
+        ws = _decode_attn_call(spec, t, step, sel, ws)
+        torch.cuda.synchronize()
+        assert _status(step) == 0
+        assert torch.equal(step.out, ref_out) and torch.equal(step.lse, ref_lse)
+    # the counters (the last 8 bytes per (row, head group)) read zero again
+    assert int(ws[-8 * spec.n_rows:].sum().item()) == 0
+
+
+def test_decode_merge_counters_not_zero_time_out_loudly():
+    # a workspace whose counters do not start at zero: the partials never count
+    # up to exactly S, every CTA gives up after its bounded wait, the call raises
+    # CSA_DEV_TIMEOUT and stores no output
+    spec = spec_for("serving_decode")
+    wl, t = _load(spec)
+    limits = [O.visible_count(int(wl.row_pos[i]), spec.ratio, int(wl.n_cmp[int(wl.row_req[i])]))
+              for i in range(spec.n_rows)]
+    sel = random_selection(limits, spec.topk, 22).to(DEV)
+    step = CsaStep(t, spec.ratio, spec.topk, compress=False)
+    ws = _decode_attn_call(spec, t, step, sel)
+    torch.cuda.synchronize()
+    assert _status(step) == 0
+    ws[-8 * spec.n_rows:] = 0x77
+    step.out.fill_(3.0)
+    _decode_attn_call(spec, t, step, sel, ws)
+    torch.cuda.synchronize()
+    assert _status(step) & B.CSA_DEV_TIMEOUT
+    assert bool((step.out == 3.0).all())
+    # zeroed again, the workspace works
+    ws[-8 * spec.n_rows:] = 0
+    step.status.zero_()
+    _decode_attn_call(spec, t, step, sel, ws)
+    torch.cuda.synchronize()
+    assert _status(step) == 0
