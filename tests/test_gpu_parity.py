@@ -275,17 +275,20 @@ def test_index_topk_full_size_every_row(name):
     assert torch.equal(sel_a, step.topk_idx)
 
 
-@pytest.mark.parametrize("ctx,topk", [([3000, 2500], 512), ([40000, 30000], 2048),
-                                      ([9000, 8500], 2048)])
-def test_index_topk_exact_ties(ctx, topk):
-    # three distinct key rows under one scale: each query row's scores take
-    # three values, so the cut falls inside a large group of equal scores and
-    # the smallest positions of that group must be taken (one CTA per row for
-    # the first case, rows split over many CTAs for the others)
+@pytest.mark.parametrize("ctx,topk,distinct", [([3000, 2500], 512, 3), ([40000, 30000], 2048, 3),
+                                               ([40000, 30000], 2048, 24), ([9000, 8500], 2048, 3)])
+def test_index_topk_exact_ties(ctx, topk, distinct):
+    # a few distinct key rows under one scale: each query row's scores take
+    # `distinct` values, so the cut falls inside a large group of equal scores
+    # and the smallest positions of that group must be taken (one CTA per row
+    # for 3000 and 9000 entries, rows split over many CTAs for 40000: with 3
+    # values the k-th key's first-digit bin is too crowded for the bin path,
+    # with 24 it is not, and its equal keys span every slice)
     spec = spec_for("ratio1_decode", ctx=ctx, chunk=[2, 2], topk=topk, seed=44)
     wl = make_workload(spec)
-    pick = torch.from_numpy(np.random.default_rng(7).integers(0, 3, size=wl.idx_pool.shape[:2]))
-    base = wl.idx_pool[0, :3].clone()
+    pick = torch.from_numpy(
+        np.random.default_rng(7).integers(0, distinct, size=wl.idx_pool.shape[:2]))
+    base = wl.idx_pool[0, :distinct].clone()
     wl.t["idx_pool"] = base[pick].contiguous()
     wl.t["idx_scale"] = torch.full_like(wl.idx_scale, float(wl.idx_scale[0, 0]))
     t = wl.to(DEV)
