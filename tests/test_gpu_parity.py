@@ -793,3 +793,11 @@ def test_decode_merge_counters_not_zero_time_out_loudly():
     _decode_attn_call(spec, t, step, sel, ws)
     torch.cuda.synchronize()
     assert _status(step) == 0
+
+
+@pytest.mark.parametrize("chunk", [[10, 10, 10, 10], [40, 40, 40, 40]])
+def test_decode_attention_split_geometries(chunk):
+    # 40 rows: three CTAs per row, two tiles each, merged through the
+    # workspace; 160 rows (more rows than SMs): one CTA per row, no merge wait
+    spec = spec_for("serving_decode", chunk=chunk, topk=512, seed=57)
+    _attn_case(spec, 23, False, rows=range(0, spec.n_rows, 7))
