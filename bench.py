@@ -43,18 +43,19 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # dram__bytes_write.sum` captures of these same bench workloads.
 NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch (one-kernel ncu
-    # captures, profiles/dram_traffic.md), keyed by the kernel's source hash
-    ("tiny_decode", "attn_decode"): {"bytes": 560380, "src": "249bf1d9da5c"},
-    ("tiny_decode", "index_score"): {"bytes": 166656, "src": "5126a7266c48"},
-    ("serving_decode", "attn_decode"): {"bytes": 4611840, "src": "249bf1d9da5c"},
-    ("serving_decode", "index_score"): {"bytes": 1556992, "src": "5126a7266c48"},
-    ("ratio1_decode", "index_score"): {"bytes": 70001664, "src": "5126a7266c48"},
-    ("ratio1_decode", "index_topk"): {"bytes": 4443648, "src": "1cddedc9778d"},
-    ("million_decode", "index_score"): {"bytes": 142582016, "src": "5126a7266c48"},
-    ("million_decode", "attn_decode"): {"bytes": 17850624, "src": "249bf1d9da5c"},
-    ("million_decode", "index_topk"): {"bytes": 8639232, "src": "1cddedc9778d"},
-    ("chunked_prefill", "attn_prefill"): {"bytes": 1061655040, "src": "1bf26f9923e9"},
-    ("chunked_prefill", "index_score"): {"bytes": 153969152, "src": "5126a7266c48"},
+    # captures, profiles/dram_traffic.md), keyed by the hash of the kernel's
+    # source and the shared headers
+    ("tiny_decode", "attn_decode"): {"bytes": 557310, "src": "3c516bde6e00"},
+    ("tiny_decode", "index_score"): {"bytes": 166400, "src": "6c06b8da1923"},
+    ("serving_decode", "attn_decode"): {"bytes": 4609280, "src": "3c516bde6e00"},
+    ("serving_decode", "index_score"): {"bytes": 1556992, "src": "6c06b8da1923"},
+    ("ratio1_decode", "index_score"): {"bytes": 70199808, "src": "6c06b8da1923"},
+    ("ratio1_decode", "index_topk"): {"bytes": 4443904, "src": "bc6ae714b60a"},
+    ("million_decode", "index_score"): {"bytes": 142274816, "src": "6c06b8da1923"},
+    ("million_decode", "attn_decode"): {"bytes": 17844736, "src": "3c516bde6e00"},
+    ("million_decode", "index_topk"): {"bytes": 8639488, "src": "bc6ae714b60a"},
+    ("chunked_prefill", "attn_prefill"): {"bytes": 1061633792, "src": "49504fb2111a"},
+    ("chunked_prefill", "index_score"): {"bytes": 153903616, "src": "6c06b8da1923"},
 }
 
 
