@@ -46,16 +46,16 @@ NCU_TRAFFIC = {
     # captures, profiles/dram_traffic.md), keyed by the hash of the kernel's
     # source and the shared headers
     ("tiny_decode", "attn_decode"): {"bytes": 557310, "src": "3c516bde6e00"},
-    ("tiny_decode", "index_score"): {"bytes": 166400, "src": "6c06b8da1923"},
+    ("tiny_decode", "index_score"): {"bytes": 166400, "src": "6218551176ee"},
     ("serving_decode", "attn_decode"): {"bytes": 4609280, "src": "3c516bde6e00"},
-    ("serving_decode", "index_score"): {"bytes": 1556992, "src": "6c06b8da1923"},
-    ("ratio1_decode", "index_score"): {"bytes": 70199808, "src": "6c06b8da1923"},
+    ("serving_decode", "index_score"): {"bytes": 1559040, "src": "6218551176ee"},
+    ("ratio1_decode", "index_score"): {"bytes": 70078720, "src": "6218551176ee"},
     ("ratio1_decode", "index_topk"): {"bytes": 4443904, "src": "bc6ae714b60a"},
-    ("million_decode", "index_score"): {"bytes": 142274816, "src": "6c06b8da1923"},
+    ("million_decode", "index_score"): {"bytes": 142403072, "src": "6218551176ee"},
     ("million_decode", "attn_decode"): {"bytes": 17844736, "src": "3c516bde6e00"},
     ("million_decode", "index_topk"): {"bytes": 8639488, "src": "bc6ae714b60a"},
     ("chunked_prefill", "attn_prefill"): {"bytes": 1061633792, "src": "49504fb2111a"},
-    ("chunked_prefill", "index_score"): {"bytes": 153903616, "src": "6c06b8da1923"},
+    ("chunked_prefill", "index_score"): {"bytes": 151814400, "src": "6218551176ee"},
 }
 
 

@@ -321,7 +321,8 @@ typedef struct {
   int32_t ratio;
   int32_t topk;
   int32_t relu;
-  int32_t mode; /* csa_mode_t: a tiling hint only; results do not depend on it */
+  int32_t mode; /* csa_mode_t: a tiling hint only; results do not depend on it.
+                    AUTO and DECODE: rows in pairs; PREFILL: rows in fours */
   const void *q_idx;
   const float *weights;
   const int32_t *row_req;

@@ -912,7 +912,10 @@ cudaError_t launch_tc(const csa_index_args &a, float *scores, int cols, uint32_t
 cudaError_t launch_index_scores(const csa_index_args &a, float *scores, int score_cols,
                                 uint32_t *zero_ctr, cudaStream_t s, const ScoreSel &sel) {
   if (a.n_rows <= 0) return cudaSuccess;
-  const bool wide = a.mode == CSA_MODE_PREFILL || (a.mode == CSA_MODE_AUTO && a.n_rows > 64);
+  // the two-row tiling (keys through TMEM) is the default: measured on the
+  // prefill workloads it also beats the four-row one (8,192 rows: 427 against
+  // 442 us a call), whose per-pass query build weighs more
+  const bool wide = a.mode == CSA_MODE_PREFILL;
   if (a.n_heads > kHeads)  // two 64-head slots per row
     return wide ? launch_tc<4, 2>(a, scores, score_cols, zero_ctr, s, sel)
                 : launch_tc<2, 2>(a, scores, score_cols, zero_ctr, s, sel);

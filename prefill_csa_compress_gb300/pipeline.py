@@ -75,6 +75,9 @@ class CsaStep:
         # it to wait for the query rows that arrive while the indexer runs)
         self.before_attention = None
         self.ws = {}
+        # the indexer's tiling hint (results do not depend on it): rows in pairs
+        # unless set to CSA_MODE_PREFILL (rows in fours)
+        self.index_mode = B.CSA_MODE_AUTO
         self._prepared = None
         self._graph = None
 
@@ -121,7 +124,7 @@ class CsaStep:
             idx_scale_pool=t["idx_scale"], cmp_block_table=t["cmp_table"], topk=self.topk,
             topk_idx=self.topk_idx, topk_score=self.topk_score, rope_cos=t["rope_cos"],
             rope_sin=t["rope_sin"],
-            mode=B.CSA_MODE_PREFILL if self.prefill else B.CSA_MODE_DECODE, status=self.status,
+            mode=self.index_mode, status=self.status,
             cand_out=self.cand, cand_in=self.cand_in, cand_block=self.cand_block,
             key_scale_pool=t.get("idx_kscale"), key_fmt=self.key_fmt)
 

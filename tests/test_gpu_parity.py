@@ -299,10 +299,14 @@ def test_index_topk_exact_ties(ctx, topk, distinct):
     _check_index_rows(wl, t, spec, step, range(spec.n_rows), scores)
 
 
-def test_index_topk_prefill_full_size_sampled():
+@pytest.mark.parametrize("four_rows", [False, True])
+def test_index_topk_prefill_full_size_sampled(four_rows):
+    # the default tiling (rows in pairs) and the four-row one (CSA_MODE_PREFILL)
     spec = spec_for("chunked_prefill", cmp_init="random")
     wl, t = _load(spec)
     step = CsaStep(t, spec.ratio, spec.topk, prefill=True, compress=False)
+    if four_rows:
+        step.index_mode = B.CSA_MODE_PREFILL
     n_cap = t["cmp_table"].shape[1] * BLOCK
     scores = torch.empty((spec.n_rows, n_cap), device=DEV)
     step.index(scores=scores)
