@@ -182,16 +182,22 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
                                                         uint32_t *rec, TopkSel sel) {
   constexpr int NW = NT / 32;
   extern __shared__ __align__(16) uint32_t tk_smem[];
-  uint32_t *priv = tk_smem;               // [NW][TK_B1]
-  uint32_t *hist = tk_smem + NW * TK_B1;  // [TK_B1]
+  // long rows: one first-digit histogram per warp (the first digit is the most
+  // crowded: keep warps off each other's counters) and the CTA's histogram;
+  // short rows (one CTA per row, at most 16384 entries): the CTA's histogram
+  // alone, then the staging of the winners -- a smaller CTA, so that more rows
+  // are resident at once
+  uint32_t *priv = MULTI ? tk_smem : tk_smem + TK_B1;  // [NW][TK_B1] or staging [2 k]
+  uint32_t *hist = MULTI ? tk_smem + NW * TK_B1 : tk_smem;  // [TK_B1]
   __shared__ int warp_sums[32];
   __shared__ int s_digit, s_above, s_ok;
   __shared__ int s_gt_before, s_eq_before;
-  // the first digit's per-warp histograms are cleared while the previous
-  // kernel finishes (shared memory only)
+  // the first digit's histograms are cleared while the previous kernel
+  // finishes (shared memory only)
   {
-    uint4 *p4 = reinterpret_cast<uint4 *>(priv);
-    for (int i = threadIdx.x; i < NW * TK_B1 / 4; i += NT) p4[i] = make_uint4(0u, 0u, 0u, 0u);
+    uint4 *p4 = reinterpret_cast<uint4 *>(MULTI ? priv : hist);
+    for (int i = threadIdx.x; i < (MULTI ? NW : 1) * TK_B1 / 4; i += NT)
+      p4[i] = make_uint4(0u, 0u, 0u, 0u);
   }
   tc::griddep_wait();
   tc::griddep_launch_dependents();
@@ -265,7 +271,7 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
       gt22 = tot;
     }
     __syncthreads();
-    if (j == 0) {
+    if (MULTI && j == 0) {
       uint32_t *mine = priv + warp * TK_B1;
 #pragma unroll
       for (int i = 0; i < KPT; ++i)
@@ -415,8 +421,9 @@ cudaError_t launch_short(const csa_index_args &a, const float *scores, int cols,
                          const TopkSel &sel) {
   static bool done[64] = {};
   const auto kern = topk_radix_kernel<NT, KPT, false>;
-  constexpr int smem = topk_smem_bytes<NT>();
-  cudaError_t e = allow_smem(kern, smem, done);
+  // the CTA's histogram and the staging of at most k winners (keys and indices)
+  const int smem = (TK_B1 + 2 * a.topk) * 4;
+  cudaError_t e = allow_smem(kern, (TK_B1 + 2 * 2048) * 4, done);
   if (e != cudaSuccess) return e;
   constexpr int kMaxGridY = 65535;
   for (int row0 = 0; row0 < a.n_rows && e == cudaSuccess; row0 += kMaxGridY)
