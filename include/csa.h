@@ -431,9 +431,9 @@ CSA_API csa_status_t csa_index_topk_noalloc(csa_index_args *args, csa_stream_t s
  * 32-bit counters per (row, head group) at the end.  The counters must read
  * zero before the workspace's first decode call; every call that completes
  * leaves them at zero (a call that raised CSA_DEV_TIMEOUT may not: zero them
- * again).  Counters that do not start at zero make the call's wait run out
- * and raise CSA_DEV_TIMEOUT rather than pass early.  The workspace must be
- * 256-byte aligned.  The prefill call is tiled for many rows; with BF16 pools
+ * again).  Counters that do not start at zero make the call raise
+ * CSA_DEV_TIMEOUT (a wait for exactly the number of splits runs out); its
+ * output is then undefined.  The workspace must be 256-byte aligned.  The prefill call is tiled for many rows; with BF16 pools
  * it needs no workspace (the size query returns 0; a workspace passed in is
  * unused, but a non-null pointer is what makes the call launch) and with a
  * low-bit pool it needs the arena below.  Both compute the same function.
