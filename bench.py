@@ -50,10 +50,10 @@ NCU_TRAFFIC = {
     ("serving_decode", "attn_decode"): {"bytes": 4609280, "src": "3c516bde6e00"},
     ("serving_decode", "index_score"): {"bytes": 1559040, "src": "6218551176ee"},
     ("ratio1_decode", "index_score"): {"bytes": 70078720, "src": "6218551176ee"},
-    ("ratio1_decode", "index_topk"): {"bytes": 4444672, "src": "c95c88e96f0d"},
+    ("ratio1_decode", "index_topk"): {"bytes": 4444672, "src": "b48cf42776fd"},
     ("million_decode", "index_score"): {"bytes": 142403072, "src": "6218551176ee"},
     ("million_decode", "attn_decode"): {"bytes": 17844736, "src": "3c516bde6e00"},
-    ("million_decode", "index_topk"): {"bytes": 8638208, "src": "c95c88e96f0d"},
+    ("million_decode", "index_topk"): {"bytes": 8638208, "src": "b48cf42776fd"},
     ("chunked_prefill", "attn_prefill"): {"bytes": 1061633792, "src": "49504fb2111a"},
     ("chunked_prefill", "index_score"): {"bytes": 151814400, "src": "6218551176ee"},
 }
