@@ -454,25 +454,39 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
       __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) +
                            ((long long)R.t * a.n_heads + R.h_lo) * kHeadDim;
       tc::tc_fence_after();
+      // the inverse rotation touches channels 448.. only: warps of lane
+      // quarters 2 and 3 in the last slice (every branch below is warp-uniform
+      // and sits outside the per-head loops)
+      const bool rot_warp = inv_rope && qd >= 2;
+      float cs = 1.f, sn = 0.f;
+      if (rot_warp) {
+        const int pair = (qd * 32 + lane - 64) >> 1;
+        cs = a.rope_cos[(long long)R.p * kRopeHalf + pair];
+        sn = a.rope_sin[(long long)R.p * kRopeHalf + pair];
+      }
+      const bool all_heads = h0 + 32 <= nh;
 #pragma unroll 1
       for (int m4 = 0; m4 < 4; ++m4) {
         float v[32];
         tc::tmem_ld32(tmem + lane_off + O_COL + m4 * 64 + h0, v);
         const int d = m4 * 128 + qd * 32 + lane;
-        float cs = 1.f, sn = 0.f;
-        if (inv_rope && d >= kHeadDim - kRopeDim) {
-          const int pair = (d - (kHeadDim - kRopeDim)) >> 1;
-          cs = a.rope_cos[(long long)R.p * kRopeHalf + pair];
-          sn = a.rope_sin[(long long)R.p * kRopeHalf + pair];
-        }
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float o = v[j] * inv[j];
-          if (inv_rope && m4 == 3 && qd >= 2) {  // channels 448.. of the last tile
-            const float other = __shfl_xor_sync(0xffffffffu, o, 1);
-            o = (d & 1) ? (-other * sn + o * cs) : (o * cs + other * sn);
+        for (int j = 0; j < 32; ++j) v[j] *= inv[j];
+        if (m4 == 3 && rot_warp) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
+            v[j] = (lane & 1) ? (-other * sn + v[j] * cs) : (v[j] * cs + other * sn);
           }
-          if (h0 + j < nh) out[(h0 + j) * kHeadDim + d] = __float2bfloat16_rn(o);
+        }
+        __nv_bfloat16 *o = out + h0 * kHeadDim + d;
+        if (all_heads) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j * kHeadDim] = __float2bfloat16_rn(v[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (h0 + j < nh) o[j * kHeadDim] = __float2bfloat16_rn(v[j]);
         }
       }
       tc::tc_fence_before();
