@@ -116,6 +116,11 @@ __device__ __forceinline__ uint4 i8x8_to_f16x8(uint2 raw) {
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+// Hint: bring the 128-byte line holding `p` into L2.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint32_t pack_f16(float a, float b) {
   const __half2 v = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t *>(&v);
@@ -531,6 +536,31 @@ __global__ void __launch_bounds__(IT_THREADS, 1)
             } else {
               flag(a.status_dev, CSA_DEV_BAD_BLOCK);
               tc::mbar_arrive(&M->st_full[s]);
+            }
+          }
+        }
+        // The next unit's query rows, head weights, positions and RoPE rows
+        // into L2 while this pass streams: its query build, which every role
+        // waits for, then reads L2 instead of DRAM.  (Hints only: they read
+        // nothing the kernel depends on.)
+        __syncwarp();
+        const int un = u + (int)gridDim.x;
+        if (un < n_units && !M->abort) {
+          const long long t0 = (long long)(un / units_per_group) * RPG;
+          const int nr = (int)min((long long)RPG, (long long)a.n_rows - t0);
+          if (nr > 0) {
+            const uint8_t *qb = static_cast<const uint8_t *>(a.q_idx) + t0 * a.n_heads * kIdxDim * 2;
+            const int qbytes = nr * a.n_heads * kIdxDim * 2;
+            for (int off = lane * 128; off < qbytes; off += 32 * 128) prefetch_l2(qb + off);
+            const uint8_t *wb = reinterpret_cast<const uint8_t *>(a.weights + t0 * a.n_heads);
+            for (int off = lane * 128; off < nr * a.n_heads * 4; off += 32 * 128)
+              prefetch_l2(wb + off);
+            if (lane < nr) {
+              const int p = a.row_pos[t0 + lane];
+              if (rope && p >= 0 && p < a.rope_cap) {
+                prefetch_l2(a.rope_cos + (long long)p * kRopeHalf);
+                prefetch_l2(a.rope_sin + (long long)p * kRopeHalf);
+              }
             }
           }
         }
