@@ -88,6 +88,54 @@ __device__ __forceinline__ bool ap_wait(uint64_t *bar, uint32_t parity, volatile
   }
 }
 
+// Softmax of one tile (thread = candidate c = qd*32 + lane, heads h0..h0+31)
+// that speculates that no logit moves the running reference: P is computed
+// with the current reference and the block-wide "exceeded" test rides on the
+// barrier that hands P to the MMA.  On a row's first tile, or when some
+// valid logit exceeded its reference by more than 2^8, the tile reloads its
+// logits (S^T stays in TMEM until P is handed over) and takes the reference
+// move of softmax_vals, which rewrites P.  Returns past that final barrier
+// with P stored and fenced for the MMA; x holds this thread's probabilities.
+__device__ __forceinline__ void softmax_tile_spec(uint32_t tmem, int qd, int h0, bool valid,
+                                                  float sl2, bool first, SoftState *st,
+                                                  uint8_t *Ps, int bar, float &lacc,
+                                                  float (&x)[32]) {
+  const int lane = threadIdx.x & 31, c = qd * 32 + lane;
+  const uint32_t s_addr = tmem + ((uint32_t)(qd * 32) << 16) + S_COL + h0;
+  tc::tc_fence_after();
+  tc::tmem_ld32(s_addr, x);
+  if (!first) {
+    float mref[32];
+    load32(st->m + h0, mref);
+    bool exceed = false;
+    if (valid) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float t = x[j] * sl2 - mref[j];
+        exceed |= t > kRescaleLog2;
+        x[j] = (j & 3) == 3 ? exp2_fma(t) : exp2_sfu(t);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] = 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4 *>(prow_chunk(Ps, c, (h0 >> 3) + q)) =
+          make_uint4(pack2(x[8 * q], x[8 * q + 1]), pack2(x[8 * q + 2], x[8 * q + 3]),
+                     pack2(x[8 * q + 4], x[8 * q + 5]), pack2(x[8 * q + 6], x[8 * q + 7]));
+    tc::fence_async_shared();
+    tc::tc_fence_before();
+    if (!tc::bar_or(bar, 256, exceed)) return;
+    tc::tc_fence_after();
+    tc::tmem_ld32(s_addr, x);
+  }
+  softmax_vals(tmem, O_COL, 4, qd, h0, valid, sl2, first, st, Ps, bar, lacc, x, [] {});
+  tc::fence_async_shared();
+  tc::tc_fence_before();
+  tc::bar_sync(bar, 256);
+}
+
 __global__ void __launch_bounds__(AP_THREADS, 1)
     attn_prefill_kernel(csa_attn_args a, const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ uint8_t smem_raw[];
@@ -402,10 +450,7 @@ __global__ void __launch_bounds__(AP_THREADS, 1)
         ok = tc::bar_and(AP_BAR, AP_SOFT, ok && ap_wait(&M->s_full, tile_it & 1, abort, a.status_dev));
         if (!ok) break;
         float x[32];
-        softmax_tile(tmem, qd, h0, valid, sl2, first, &M->st, Ps, AP_BAR, lacc, x);
-        tc::fence_async_shared();
-        tc::tc_fence_before();
-        tc::bar_sync(AP_BAR, AP_SOFT);
+        softmax_tile_spec(tmem, qd, h0, valid, sl2, first, &M->st, Ps, AP_BAR, lacc, x);
         if (stid == 0) tc::mbar_arrive(&M->p_full);
         // FP32 denominators (this warp's per-head sums of the unrounded
         // probabilities, lane l: head h0 + l) while the next tile is gathered
