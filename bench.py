@@ -46,16 +46,16 @@ NCU_TRAFFIC = {
     # captures, profiles/dram_traffic.md), keyed by the hash of the kernel's
     # source and the shared headers
     ("tiny_decode", "attn_decode"): {"bytes": 557310, "src": "3c516bde6e00"},
-    ("tiny_decode", "index_score"): {"bytes": 166400, "src": "6218551176ee"},
+    ("tiny_decode", "index_score"): {"bytes": 168448, "src": "5a17c226935a"},
     ("serving_decode", "attn_decode"): {"bytes": 4609280, "src": "3c516bde6e00"},
-    ("serving_decode", "index_score"): {"bytes": 1559040, "src": "6218551176ee"},
-    ("ratio1_decode", "index_score"): {"bytes": 70078720, "src": "6218551176ee"},
-    ("ratio1_decode", "index_topk"): {"bytes": 4444672, "src": "b48cf42776fd"},
-    ("million_decode", "index_score"): {"bytes": 142403072, "src": "6218551176ee"},
+    ("serving_decode", "index_score"): {"bytes": 1558784, "src": "5a17c226935a"},
+    ("ratio1_decode", "index_score"): {"bytes": 70123776, "src": "5a17c226935a"},
+    ("ratio1_decode", "index_topk"): {"bytes": 4448768, "src": "92c03cfa512b"},
+    ("million_decode", "index_score"): {"bytes": 142287616, "src": "5a17c226935a"},
     ("million_decode", "attn_decode"): {"bytes": 17844736, "src": "3c516bde6e00"},
-    ("million_decode", "index_topk"): {"bytes": 8638208, "src": "b48cf42776fd"},
-    ("chunked_prefill", "attn_prefill"): {"bytes": 1061633792, "src": "49504fb2111a"},
-    ("chunked_prefill", "index_score"): {"bytes": 151814400, "src": "6218551176ee"},
+    ("million_decode", "index_topk"): {"bytes": 8640768, "src": "92c03cfa512b"},
+    ("chunked_prefill", "attn_prefill"): {"bytes": 1061745408, "src": "6c2a1d534303"},
+    ("chunked_prefill", "index_score"): {"bytes": 151614976, "src": "5a17c226935a"},
 }
 
 
