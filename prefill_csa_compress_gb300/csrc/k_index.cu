@@ -65,19 +65,22 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *
 constexpr int TK_SHORT_KPT = 16;  // one CTA per row: 16 entries per thread ...
 constexpr int TK_SHORT_KPT2 = 32; // ... or 32 (512 threads: rows up to 16384 entries)
 constexpr int TK_LONG_THREADS = 512;
-constexpr int TK_LONG_KPT = 32;   // entries per thread of a long-row slice
+constexpr int TK_LONG_KPT = 16;   // entries per thread of a long-row slice
+constexpr int TK_PRIV = 4;        // first-digit histograms of a long-row slice, 4 warps each
+constexpr int TK_LONG_PER_SM = 2; // long-row slices per SM (the grid is resident at once)
 constexpr int TK_B1 = 2048, TK_B2 = 2048, TK_B3 = 1024;  // 11 + 11 + 10 key bits
 constexpr int TK_CTL_HDR = 32;  // barrier counter, alone in its 128-byte line
 static_assert(TK_CTL_HDR + TK_B1 + TK_B2 + TK_B3 == kTopkCtlWords, "row control block");
 constexpr int TK_REC_WORDS = 1056;  // per slice: suffix counts [0, 1024] and the count above
 constexpr int TK_REC_GT = 1025;     // the 22-bit prefix, at word 1025
 
-// Dynamic shared memory of a CTA of NT threads: one first-digit histogram per
-// warp (the first digit is the most crowded: keep warps off each other's
-// counters) and the CTA's histogram.
+// Dynamic shared memory of a long-row CTA: TK_PRIV first-digit histograms,
+// each shared by a quarter of the warps (the first digit is the most crowded:
+// spread the warps' counters), and the CTA's histogram -- 40 KB, so that two
+// slices share an SM.
 template <int NT>
 constexpr int topk_smem_bytes() {
-  return (NT / 32 + 1) * TK_B1 * 4;
+  return (TK_PRIV + 1) * TK_B1 * 4;
 }
 
 // Barrier of the S CTAs that share a row: the counter only grows, barrier j
@@ -189,15 +192,14 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
                                                         const float *__restrict__ scores, int cols,
                                                         int row0, int S, int slice, uint32_t *ctl,
                                                         uint32_t *rec, TopkSel sel) {
-  constexpr int NW = NT / 32;
   extern __shared__ __align__(16) uint32_t tk_smem[];
-  // long rows: one first-digit histogram per warp (the first digit is the most
-  // crowded: keep warps off each other's counters) and the CTA's histogram;
+  // long rows: TK_PRIV first-digit histograms (warp w counts into w % TK_PRIV;
+  // the first digit is the most crowded) and the CTA's histogram;
   // short rows (one CTA per row, at most 16384 entries): the CTA's histogram
   // alone, then the staging of the winners -- a smaller CTA, so that more rows
   // are resident at once
-  uint32_t *priv = MULTI ? tk_smem : tk_smem + TK_B1;  // [NW][TK_B1] or staging [2 k]
-  uint32_t *hist = MULTI ? tk_smem + NW * TK_B1 : tk_smem;  // [TK_B1]
+  uint32_t *priv = MULTI ? tk_smem : tk_smem + TK_B1;  // [TK_PRIV][TK_B1] or staging [2 k]
+  uint32_t *hist = MULTI ? tk_smem + TK_PRIV * TK_B1 : tk_smem;  // [TK_B1]
   __shared__ int warp_sums[32];
   __shared__ int s_digit, s_above, s_ok;
   __shared__ int s_gt_before, s_eq_before;
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
   // finishes (shared memory only)
   {
     uint4 *p4 = reinterpret_cast<uint4 *>(MULTI ? priv : hist);
-    for (int i = threadIdx.x; i < (MULTI ? NW : 1) * TK_B1 / 4; i += NT)
+    for (int i = threadIdx.x; i < (MULTI ? TK_PRIV : 1) * TK_B1 / 4; i += NT)
       p4[i] = make_uint4(0u, 0u, 0u, 0u);
   }
   tc::griddep_wait();
@@ -289,7 +291,7 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
     }
     __syncthreads();
     if (MULTI && j == 0) {
-      uint32_t *mine = priv + warp * TK_B1;
+      uint32_t *mine = priv + (warp % TK_PRIV) * TK_B1;
 #pragma unroll
       for (int i = 0; i < KPT; ++i)
         if (i < nv) atomicAdd(&mine[key[i] >> 21], 1u);
@@ -297,7 +299,7 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(csa_index_args a,
       for (int i = tid; i < TK_B1; i += NT) {
         uint32_t sum = 0;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) sum += priv[w * TK_B1 + i];
+        for (int w = 0; w < TK_PRIV; ++w) sum += priv[w * TK_B1 + i];
         hist[i] = sum;
       }
     } else {
@@ -466,11 +468,11 @@ LongLayout long_layout(int n_rows, int S) {
 
 bool topk_is_long(int n_cap) { return n_cap > TK_SHORT_MAX; }
 
-// Slices per row for the long-row path: about one CTA per SM over the rows,
-// each slice a multiple of 32 entries and at most 512 x 32 entries.
+// Slices per row for the long-row path: about TK_LONG_PER_SM CTAs per SM over
+// the rows, each slice a multiple of 32 entries and at most 512 x 16 entries.
 void topk_long_geometry(int n_rows, int n_cap, int *S, int *slice) {
   const int s_min = (n_cap + TK_SLICE_MAX - 1) / TK_SLICE_MAX;
-  int s = n_rows > 0 ? device_sms() / n_rows : 1;
+  int s = n_rows > 0 ? TK_LONG_PER_SM * device_sms() / n_rows : 1;
   if (s < s_min) s = s_min;
   int sl = (n_cap + s - 1) / s;
   sl = (sl + 31) / 32 * 32;
