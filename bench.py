@@ -50,10 +50,10 @@ NCU_TRAFFIC = {
     ("serving_decode", "attn_decode"): {"bytes": 4609280, "src": "3c516bde6e00"},
     ("serving_decode", "index_score"): {"bytes": 1558784, "src": "5a17c226935a"},
     ("ratio1_decode", "index_score"): {"bytes": 70123776, "src": "5a17c226935a"},
-    ("ratio1_decode", "index_topk"): {"bytes": 4448768, "src": "92c03cfa512b"},
+    ("ratio1_decode", "index_topk"): {"bytes": 4454144, "src": "4a72031579c9"},
     ("million_decode", "index_score"): {"bytes": 142287616, "src": "5a17c226935a"},
     ("million_decode", "attn_decode"): {"bytes": 17844736, "src": "3c516bde6e00"},
-    ("million_decode", "index_topk"): {"bytes": 8640768, "src": "92c03cfa512b"},
+    ("million_decode", "index_topk"): {"bytes": 8648704, "src": "4a72031579c9"},
     ("chunked_prefill", "attn_prefill"): {"bytes": 1061745408, "src": "6c2a1d534303"},
     ("chunked_prefill", "index_score"): {"bytes": 151614976, "src": "5a17c226935a"},
 }
